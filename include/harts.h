@@ -1,0 +1,221 @@
+/*
+ * harts.h - C ABI of the packed-tree KDA library (GB300, sm_103a).
+ *
+ * The library runs chunkwise gated-delta (KDA-style) linear attention, forward and
+ * backward, once over a prefix-compressed rollout tree instead of once per
+ * root-to-leaf trajectory, as HARTS describes it (arXiv 2608.28158; page
+ * "HARTS ... 精读", sections 4.2-4.3; page "thelatestinai ... 2608.28158", Fig. 1(c),
+ * Fig. 2 and Figure C.1 captions).
+ *
+ * Model of one layer.  Per trajectory and head, with per-channel log-decay g_t,
+ *     S_t = (I - beta_t k_t k_t^T) diag(exp g_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ * computed chunkwise with chunk length B (chunks anchored at trajectory position 0).
+ *
+ * Conventions for every call below:
+ *  - Return 0 on success, or a negative HARTS_E* code; harts_last_error() then holds
+ *    a message for the calling thread.  No C++ exception crosses the ABI.
+ *  - "device pointer" = memory on the current CUDA device, allocated and owned by the
+ *    caller.  The library never allocates device memory and never frees caller memory.
+ *  - Work is enqueued on the given stream and returns without synchronising.  Faults
+ *    found by the kernels (a bad plan, out-of-range decay) are recorded in the plan's
+ *    device error word; harts_plan_device_error() reads it (it synchronises).
+ *  - All tensors are contiguous, token-major: [rows, H, d].  Rows are compact tokens
+ *    in the plan's layout (see harts_plan_arrays.seg_offset).
+ *  - A plan is immutable once built; the forward and the backward pass reuse the same
+ *    plan (activation recomputation re-runs the same rounds, replays and handoffs,
+ *    section 4.3).  Distinct plans may be used from distinct threads.
+ */
+#ifndef HARTS_H
+#define HARTS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HARTS_OK            0
+#define HARTS_EINVAL       -1   /* malformed argument (tree, pointer, size) */
+#define HARTS_EUNSUPPORTED -2   /* chunk/head dim/dtype combination without a kernel */
+#define HARTS_EOVERFLOW    -3   /* a size or index does not fit the library's types */
+#define HARTS_ESMALLBUF    -4   /* caller buffer smaller than required */
+#define HARTS_ECUDA        -5   /* a CUDA runtime call failed */
+#define HARTS_ETIMEOUT     -6   /* a bounded device wait ran out */
+#define HARTS_EDEVICE      -7   /* a kernel recorded an error in the device error word */
+#define HARTS_ENOPLAN      -8   /* plan not uploaded to the device */
+
+typedef enum { HARTS_FP32 = 0, HARTS_BF16 = 1 } harts_dtype;
+
+/* Kernel selection.  AUTO picks the tensor-core kernels where they exist
+ * (bf16, dk = dv = 128, B = 64) and the exact fp32 CUDA-core kernels otherwise. */
+typedef enum { HARTS_KERNEL_AUTO = 0, HARTS_KERNEL_SIMT = 1, HARTS_KERNEL_TC = 2 } harts_kernel;
+
+typedef struct CUstream_st *harts_stream_t;   /* same type as cudaStream_t */
+typedef struct harts_plan harts_plan;          /* opaque, host memory, library-owned */
+
+/* ------------------------------------------------------------------------------ */
+/* Planning (host only).                                                          */
+/* ------------------------------------------------------------------------------ */
+
+/*
+ * harts_plan_calls - minimum-call plan over a segment forest (section 4.2).
+ *
+ * n_seg    number of segments (fork-free token paths), >= 1.
+ * parent   host [n_seg]: parent[i] < i, or -1 for a root (forests allowed).
+ * seg_len  host [n_seg]: tokens per segment, >= 1.
+ * chunk    chunk length B >= 1 (the kernels support 16, 32, 64).
+ * flags    0 (reserved).
+ * out      receives a new plan; free it with harts_plan_free.
+ *
+ * The plan holds: the rounds (one packed call each; their number is the minimum
+ * under the packed chunkwise-call model, T_pre/T_in recurrence with a
+ * max/second-max pass, linear time), the input sequences per round, the compact
+ * layout, each side branch's resume anchor a(p) = B*floor(p/B) and replay rows
+ * [a(p), p), and the boundary-state slots with their consumers.  Conventions that
+ * make the plan unique: the continuation is the lowest-id child of maximal T_pre;
+ * rounds are as early as possible; sequences are ordered by round, then by the id
+ * of their first segment; slots by producer sequence, then position.
+ * Errors: HARTS_EINVAL (bad parent order, zero length, chunk < 1),
+ *         HARTS_EOVERFLOW (token counts beyond int32 rows).
+ */
+int harts_plan_calls(int32_t n_seg, const int32_t *parent, const int64_t *seg_len,
+                     int32_t chunk, uint32_t flags, harts_plan **out);
+
+typedef struct {
+    int32_t n_seg, n_roots, n_leaves, chunk;
+    int32_t n_rounds;        /* packed calls per pass */
+    int32_t n_seq;           /* input sequences (= leaves) */
+    int32_t n_states;        /* materialised boundary-state slots */
+    int32_t n_cons;          /* sequences that start from a slot */
+    int64_t C;               /* compact (non-replay) tokens */
+    int64_t S;               /* expanded trajectory tokens */
+    int64_t R;               /* replay tokens, sum of (|children|-1)*(e_v mod B) */
+    int64_t n_chunks;        /* chunks over all sequences, replay rows included */
+    int32_t max_seq_chunks;  /* longest sequence in chunks */
+    int32_t n_fold_rows;     /* distinct compact rows that are replayed */
+} harts_plan_info;
+
+int harts_plan_get_info(const harts_plan *plan, harts_plan_info *out);
+
+/* Plan arrays, exported into caller-allocated host arrays sized from the info.
+ * Any pointer may be NULL to skip that array. */
+typedef struct {
+    int64_t *seg_offset;     /* [n_seg]   compact row of the segment's first token     */
+    int64_t *seg_pos;        /* [n_seg]   trajectory position s_v of that token         */
+    int32_t *seg_seq;        /* [n_seg]   sequence that executes the segment            */
+    int32_t *seg_ctop;       /* [n_seg]   direct-continuation child, -1 for a leaf      */
+    int32_t *seg_tpre;       /* [n_seg]   T_pre(v)                                      */
+    int32_t *seg_tin;        /* [n_seg]   T_in(v)                                       */
+    int32_t *round_seq_ptr;  /* [n_rounds+1] sequences of round r: [ptr[r], ptr[r+1])   */
+    int64_t *cu_seqlens;     /* [n_seq+1] own (non-replay) rows of sequence i           */
+    int32_t *seq_round;      /* [n_seq]   1-based round                                  */
+    int32_t *seq_first_seg;  /* [n_seq]                                                  */
+    int64_t *seq_anchor;     /* [n_seq]   trajectory position of local position 0       */
+    int32_t *seq_replay;     /* [n_seq]   replay rows rho < B before the own rows        */
+    int32_t *seq_src;        /* [n_seq]   initial state: slot id >= 0, or -1-r = root r  */
+    int64_t *replay_ptr;     /* [n_seq+1]                                               */
+    int64_t *replay_idx;     /* [R]       compact rows replayed, in position order       */
+    int32_t *seq_state_ptr;  /* [n_seq+1] slots produced by sequence i                   */
+    int32_t *state_seq;      /* [n_states] producer sequence                             */
+    int64_t *state_pos;      /* [n_states] local position (multiple of B) in producer    */
+    int32_t *state_cons_ptr; /* [n_states+1]                                             */
+    int32_t *state_cons;     /* [n_cons]   consumer sequences, ascending                 */
+    int32_t *root_cons_ptr;  /* [n_roots+1]                                              */
+    int32_t *root_cons;      /* [n_seq - n_cons] sequences starting from a root state    */
+} harts_plan_arrays;
+
+int harts_plan_export(const harts_plan *plan, harts_plan_arrays *dst);
+
+/* Bytes of device memory the plan needs (int32 tables plus the device error word). */
+size_t harts_plan_device_bytes(const harts_plan *plan);
+
+/* Copy the plan tables into dev_buf (device pointer, >= harts_plan_device_bytes,
+ * 256-byte aligned, caller-owned, kept alive while the plan is used) on `stream`.
+ * Records dev_buf in the plan; clears the device error word. */
+int harts_plan_upload(harts_plan *plan, void *dev_buf, size_t bytes, harts_stream_t stream);
+
+/* Synchronise `stream`, read the device error word; 0 or HARTS_EDEVICE.  The word
+ * is cleared after reading.  *code (nullable) receives the raw device code. */
+int harts_plan_device_error(harts_plan *plan, harts_stream_t stream, int32_t *code);
+
+void harts_plan_free(harts_plan *plan);
+
+/* ------------------------------------------------------------------------------ */
+/* Forward: one packed call per round (section 4.3, "KDA").                       */
+/* ------------------------------------------------------------------------------ */
+
+typedef struct {
+    int32_t H, dk, dv;
+    int32_t dtype;           /* harts_dtype of q, k, v, g, beta, o, chunk_states */
+    int32_t kernel;          /* harts_kernel */
+    float scale;             /* o = scale * S^T q */
+    const void *q;           /* device [C,H,dk] */
+    const void *k;           /* device [C,H,dk] */
+    const void *v;           /* device [C,H,dv] */
+    const void *g;           /* device [C,H,dk] natural-log per-channel decay (<= 0) */
+    const void *beta;        /* device [C,H] */
+    void *o;                 /* device [C,H,dv] output */
+    float *states;           /* device [n_states,H,dk,dv] fp32 boundary-state slots;
+                                may be NULL only if n_states == 0 */
+    float *final_state;      /* device [n_seq,H,dk,dv] fp32, nullable */
+    const float *h0;         /* device [n_roots,H,dk,dv] fp32 root initial state, nullable
+                                (NULL = zero state) */
+    void *chunk_states;      /* device [n_chunks,H,dk,dv] in `dtype`, nullable: the state
+                                at the start of every chunk, saved for the backward pass */
+} harts_kda_fwd_args;
+
+/* Bytes for chunk_states (n_chunks * H * dk * dv * sizeof(dtype)). */
+size_t harts_kda_chunk_state_bytes(const harts_plan *plan, int32_t H, int32_t dk, int32_t dv,
+                                   int32_t dtype);
+
+/*
+ * harts_kda_fwd - forward pass over all rounds, enqueued on `stream`.
+ * Round r launches one kernel over its (sequence, head) pairs.  A sequence starts
+ * from the zero state (root; or h0), or from a slot written by an earlier round,
+ * runs its replay rows and own rows chunk by chunk, writes o for its own rows only,
+ * stores requested boundary states into their slots and its final state.
+ * Errors: HARTS_EINVAL, HARTS_EUNSUPPORTED (dk, dv not in {32,64,128}, dk != dv,
+ * B not in {16,32,64}), HARTS_ENOPLAN, HARTS_ECUDA.
+ */
+int harts_kda_fwd(const harts_plan *plan, const harts_kda_fwd_args *args, harts_stream_t stream);
+
+/* ------------------------------------------------------------------------------ */
+/* Backward: rounds in reverse, gradients through the state handoffs.             */
+/* ------------------------------------------------------------------------------ */
+
+typedef struct {
+    harts_kda_fwd_args fwd;  /* the forward arguments; fwd.o is not read; fwd.states and
+                                fwd.chunk_states must hold what harts_kda_fwd wrote */
+    const void *d_o;         /* device [C,H,dv] gradient of the loss w.r.t. o */
+    const float *d_final;    /* device [n_seq,H,dk,dv] fp32, nullable (zero) */
+    void *dq, *dk, *dv, *dg; /* device [C,H,dk] / [C,H,dv] outputs in `dtype` */
+    void *dbeta;             /* device [C,H] output in `dtype` */
+    float *dh0;              /* device [n_roots,H,dk,dv] fp32, nullable */
+    void *workspace;         /* device, >= harts_kda_bwd_workspace_bytes, 256-B aligned */
+    size_t workspace_bytes;
+} harts_kda_bwd_args;
+
+size_t harts_kda_bwd_workspace_bytes(const harts_plan *plan, int32_t H, int32_t dk, int32_t dv);
+
+/*
+ * harts_kda_bwd - backward pass, enqueued on `stream`.
+ * Rounds run in reverse.  Per (sequence, head) a reverse chunk loop carries dS; at a
+ * slot the sequence produced, the gradients w.r.t. that slot from all its consumers
+ * (sequences of later rounds) are added in ascending consumer order; the gradient
+ * w.r.t. the sequence's own initial state is stored for its producer (section 4.3:
+ * the initial-state gradient flows back into the call that produced the boundary).
+ * Replay rows get no dq; their dk, dv, dg, dbeta are added into the ancestor rows
+ * in a fixed order after all rounds.  Deterministic: no floating-point atomics.
+ * Errors: as harts_kda_fwd, plus HARTS_ESMALLBUF.
+ */
+int harts_kda_bwd(const harts_plan *plan, const harts_kda_bwd_args *args, harts_stream_t stream);
+
+/* Message for the last error on the calling thread ("" if none). */
+const char *harts_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HARTS_H */

@@ -1,0 +1,161 @@
+"""Thin Python binding over the C ABI: the same calls, with torch tensors for device
+memory and streams.  Every step of the computation runs in the library's kernels;
+this module only marshals pointers and sizes."""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import _lib as L
+
+__all__ = ["Plan", "kda_fwd", "kda_bwd", "dtype_code"]
+
+
+def dtype_code(torch_dtype):
+    import torch
+    if torch_dtype == torch.float32:
+        return L.HARTS_FP32
+    if torch_dtype == torch.bfloat16:
+        return L.HARTS_BF16
+    raise ValueError(f"unsupported dtype {torch_dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Plan:
+    """harts_plan_calls + harts_plan_get_info / export / upload / free."""
+
+    def __init__(self, parent, seg_len, chunk: int):
+        parent = np.ascontiguousarray(parent, np.int32)
+        seg_len = np.ascontiguousarray(seg_len, np.int64)
+        h = ctypes.c_void_p()
+        rc = L.lib().harts_plan_calls(len(parent), parent.ctypes.data_as(L._pi32),
+                                      seg_len.ctypes.data_as(L._pi64), int(chunk), 0,
+                                      ctypes.byref(h))
+        L.check(rc, "harts_plan_calls")
+        self._h = h
+        info = L.PlanInfo()
+        L.check(L.lib().harts_plan_get_info(self._h, ctypes.byref(info)), "harts_plan_get_info")
+        self.info = {n: getattr(info, n) for n, _ in L.PlanInfo._fields_}
+        self._dev = None
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            L.lib().harts_plan_free(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    def arrays(self) -> dict:
+        """Export every plan array into numpy (harts_plan_export)."""
+        info = self.info
+        env = dict(info)
+        out, arr = {}, L.PlanArrays()
+        for name, ty, size in L.PLAN_ARRAY_FIELDS:
+            n = eval(size, {}, env)
+            a = np.zeros(max(n, 1), np.int64 if ty == "i64" else np.int32)
+            out[name] = (a, n)
+            setattr(arr, name, a.ctypes.data_as(L._pi64 if ty == "i64" else L._pi32))
+        L.check(L.lib().harts_plan_export(self._h, ctypes.byref(arr)), "harts_plan_export")
+        return {k: a[:n] for k, (a, n) in out.items()}
+
+    def device_bytes(self) -> int:
+        return int(L.lib().harts_plan_device_bytes(self._h))
+
+    def upload(self, device="cuda", stream=None):
+        """Allocate the plan's device tables through torch and upload them."""
+        import torch
+        nb = self.device_bytes()
+        buf = torch.empty(nb, dtype=torch.uint8, device=device)
+        L.check(L.lib().harts_plan_upload(self._h, _ptr(buf), nb, _stream(stream)),
+                "harts_plan_upload")
+        self._dev = buf
+        return self
+
+    def device_error(self, stream=None) -> int:
+        code = ctypes.c_int32(0)
+        rc = L.lib().harts_plan_device_error(self._h, _stream(stream), ctypes.byref(code))
+        if rc not in (0, -7):
+            L.check(rc, "harts_plan_device_error")
+        return code.value
+
+    def chunk_state_bytes(self, H, dk, dv, dtype_c):
+        return int(L.lib().harts_kda_chunk_state_bytes(self._h, H, dk, dv, dtype_c))
+
+    def bwd_workspace_bytes(self, H, dk, dv):
+        return int(L.lib().harts_kda_bwd_workspace_bytes(self._h, H, dk, dv))
+
+
+def _fwd_args(plan, q, k, v, g, beta, o, states, final_state, h0, chunk_states, scale, kernel):
+    C, H, dk = q.shape
+    dv = v.shape[2]
+    a = L.FwdArgs()
+    a.H, a.dk, a.dv = H, dk, dv
+    a.dtype = dtype_code(q.dtype)
+    a.kernel = kernel
+    a.scale = float(scale)
+    for n, t in dict(q=q, k=k, v=v, g=g, beta=beta, o=o, states=states, final_state=final_state,
+                     h0=h0, chunk_states=chunk_states).items():
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+        setattr(a, n, None if t is None else t.data_ptr())
+    return a
+
+
+def kda_fwd(plan: Plan, q, k, v, g, beta, *, o=None, states=None, final_state=None, h0=None,
+            chunk_states=None, scale=1.0, kernel=L.HARTS_KERNEL_AUTO, stream=None):
+    """harts_kda_fwd.  Allocates any missing output through torch; returns
+    (o, states, final_state, chunk_states)."""
+    import torch
+    C, H, dk = q.shape
+    dv = v.shape[2]
+    info = plan.info
+    dev = q.device
+    if o is None:
+        o = torch.empty((C, H, dv), dtype=q.dtype, device=dev)
+    if states is None and info["n_states"] > 0:
+        states = torch.empty((info["n_states"], H, dk, dv), dtype=torch.float32, device=dev)
+    a = _fwd_args(plan, q, k, v, g, beta, o, states, final_state, h0, chunk_states, scale, kernel)
+    L.check(L.lib().harts_kda_fwd(plan.handle, ctypes.byref(a), _stream(stream)), "harts_kda_fwd")
+    return o, states, final_state, chunk_states
+
+
+def kda_bwd(plan: Plan, q, k, v, g, beta, d_o, *, states, chunk_states, d_final=None,
+            h0=None, dh0=None, scale=1.0, grads=None, workspace=None,
+            kernel=L.HARTS_KERNEL_AUTO, stream=None):
+    """harts_kda_bwd.  Returns dict(dq, dk, dv, dg, dbeta[, dh0])."""
+    import torch
+    C, H, dk = q.shape
+    dv = v.shape[2]
+    dev = q.device
+    if grads is None:
+        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                     dg=torch.empty_like(g), dbeta=torch.empty_like(beta))
+    nb = plan.bwd_workspace_bytes(H, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+    a = L.BwdArgs()
+    a.fwd = _fwd_args(plan, q, k, v, g, beta, None, states, None, h0, chunk_states, scale, kernel)
+    a.d_o = d_o.data_ptr()
+    a.d_final = None if d_final is None else d_final.data_ptr()
+    for n in ("dq", "dk", "dv", "dg", "dbeta"):
+        setattr(a, n, grads[n].data_ptr())
+    a.dh0 = None if dh0 is None else dh0.data_ptr()
+    a.workspace = workspace.data_ptr()
+    a.workspace_bytes = workspace.numel()
+    L.check(L.lib().harts_kda_bwd(plan.handle, ctypes.byref(a), _stream(stream)), "harts_kda_bwd")
+    if dh0 is not None:
+        grads["dh0"] = dh0
+    return grads

@@ -1,0 +1,203 @@
+// C ABI entry points that touch the device: plan upload, forward and backward dispatch.
+#include <cstring>
+
+#include "kda_common.cuh"
+
+namespace harts {
+
+bool simt_supported(bool backward, int D, int BC);
+cudaError_t simt_fwd_round(int dtype, int BC, const FwdParams &p, const PlanDev &pd,
+                           int32_t base, int32_t n_items, cudaStream_t st);
+cudaError_t simt_bwd_round(int dtype, int BC, const BwdParams &p, const PlanDev &pd,
+                           int32_t base, int32_t n_items, cudaStream_t st);
+cudaError_t bwd_finish(int dtype, const BwdParams &p, const PlanDev &pd, cudaStream_t st);
+
+bool tc_supported(bool backward, int dtype, int D, int BC);
+cudaError_t tc_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, int32_t n_items,
+                         int32_t max_chunks, cudaStream_t st);
+cudaError_t tc_bwd_round(const BwdParams &p, const PlanDev &pd, int32_t base, int32_t n_items,
+                         int32_t max_chunks, cudaStream_t st);
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int cuda_fail(cudaError_t e, const char *what) {
+    set_error(std::string(what) + ": " + cudaGetErrorString(e));
+    return HARTS_ECUDA;
+}
+
+size_t dtype_size(int32_t dt) { return dt == HARTS_FP32 ? 4 : 2; }
+
+int check_fwd_args(const harts_plan *P, const harts_kda_fwd_args *a) {
+    if (!P || !a) { set_error("NULL plan or args"); return HARTS_EINVAL; }
+    if (!P->dev) { set_error("plan not uploaded (harts_plan_upload)"); return HARTS_ENOPLAN; }
+    if (a->dtype != HARTS_FP32 && a->dtype != HARTS_BF16) { set_error("dtype"); return HARTS_EUNSUPPORTED; }
+    if (a->H < 1 || a->dk < 1 || a->dv < 1) { set_error("H, dk, dv must be >= 1"); return HARTS_EINVAL; }
+    if (a->dk != a->dv) { set_error("dk != dv is not supported"); return HARTS_EUNSUPPORTED; }
+    if (!a->q || !a->k || !a->v || !a->g || !a->beta) { set_error("NULL input"); return HARTS_EINVAL; }
+    if (P->info.n_states > 0 && !a->states) { set_error("states required (n_states > 0)"); return HARTS_EINVAL; }
+    if (a->kernel < HARTS_KERNEL_AUTO || a->kernel > HARTS_KERNEL_TC) { set_error("kernel"); return HARTS_EINVAL; }
+    const int64_t rows = P->info.C * a->H;
+    if (rows > (int64_t(1) << 31) / 1) {
+        // row * H * D products are formed in int64 inside the kernels; only C*H must fit int32
+    }
+    return HARTS_OK;
+}
+
+// Which kernel family runs: 0 = SIMT, 1 = tensor core, -1 = none.
+int pick(const harts_kda_fwd_args *a, int BC, bool backward) {
+    const int D = a->dk;
+    const bool tc = tc_supported(backward, a->dtype, D, BC);
+    const bool simt = simt_supported(backward, D, BC);
+    if (a->kernel == HARTS_KERNEL_TC) return tc ? 1 : -1;
+    if (a->kernel == HARTS_KERNEL_SIMT) return simt ? 0 : -1;
+    if (tc) return 1;
+    return simt ? 0 : -1;
+}
+
+FwdParams make_fwd(const harts_kda_fwd_args *a) {
+    FwdParams p{};
+    p.q = a->q; p.k = a->k; p.v = a->v; p.g = a->g; p.beta = a->beta; p.o = a->o;
+    p.states = a->states; p.final_state = a->final_state; p.h0 = a->h0;
+    p.chunk_states = a->chunk_states; p.H = a->H; p.D = a->dk; p.scale = a->scale;
+    return p;
+}
+
+struct BwdWs { size_t ds_init, rep_grad, total; };
+BwdWs bwd_ws(const harts_plan *P, int32_t H, int32_t D) {
+    BwdWs w{};
+    w.ds_init = 0;
+    size_t a = align_up(sizeof(float) * size_t(P->info.n_seq) * H * D * D);
+    w.rep_grad = a;
+    size_t b = align_up(sizeof(float) * size_t(P->info.R) * H * (3 * D + 1));
+    w.total = a + b;
+    return w;
+}
+
+}  // namespace
+}  // namespace harts
+
+using namespace harts;
+
+extern "C" {
+
+int harts_plan_upload(harts_plan *P, void *dev_buf, size_t bytes, harts_stream_t stream) {
+    if (!P || !dev_buf) { set_error("NULL plan or buffer"); return HARTS_EINVAL; }
+    const size_t need = harts_plan_device_bytes(P);
+    if (bytes < need) { set_error("plan device buffer too small"); return HARTS_ESMALLBUF; }
+    if (reinterpret_cast<uintptr_t>(dev_buf) % 256) { set_error("plan buffer must be 256-B aligned"); return HARTS_EINVAL; }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(dev_buf, P->image.words.data(), need, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload");
+    // The copy reads pageable host memory; make sure it finished before the plan can change.
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload sync");
+    P->dev = dev_buf;
+    int32_t *w = static_cast<int32_t *>(dev_buf);
+    const PlanImage &I = P->image;
+    PlanDev &v = P->view;
+    v.err = w + I.off_err;
+    v.round_seq_ptr = w + I.off_round_seq_ptr; v.round_order = w + I.off_round_order;
+    v.seq_row0 = w + I.off_seq_row0; v.seq_nown = w + I.off_seq_nown; v.seq_rho = w + I.off_seq_rho;
+    v.seq_rptr = w + I.off_seq_rptr; v.seq_src = w + I.off_seq_src; v.seq_sptr = w + I.off_seq_sptr;
+    v.state_lpos = w + I.off_state_lpos; v.seq_cbase = w + I.off_seq_cbase;
+    v.state_cptr = w + I.off_state_cptr; v.state_cons = w + I.off_state_cons;
+    v.root_cptr = w + I.off_root_cptr; v.root_cons = w + I.off_root_cons;
+    v.replay_idx = w + I.off_replay_idx; v.fold_rows = w + I.off_fold_rows;
+    v.fold_ptr = w + I.off_fold_ptr; v.fold_occ = w + I.off_fold_occ;
+    v.n_rounds = P->info.n_rounds; v.n_seq = P->info.n_seq; v.n_states = P->info.n_states;
+    v.n_roots = P->info.n_roots; v.n_fold = P->info.n_fold_rows; v.chunk = P->info.chunk;
+    v.R = P->info.R; v.n_chunks = P->info.n_chunks;
+    set_error("");
+    return HARTS_OK;
+}
+
+int harts_plan_device_error(harts_plan *P, harts_stream_t stream, int32_t *code) {
+    if (!P) { set_error("NULL plan"); return HARTS_EINVAL; }
+    if (!P->dev) { set_error("plan not uploaded"); return HARTS_ENOPLAN; }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int32_t host[4] = {0, 0, 0, 0};
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "sync");
+    e = cudaMemcpy(host, P->view.err, sizeof(host), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read error word");
+    if (code) *code = host[0];
+    if (host[0] != 0) {
+        const int32_t zero[4] = {0, 0, 0, 0};
+        cudaMemcpy(P->view.err, zero, sizeof(zero), cudaMemcpyHostToDevice);
+        set_error("device error " + std::to_string(host[0]) + " (seq " + std::to_string(host[1]) +
+                  ", pos " + std::to_string(host[2]) + ")");
+        return HARTS_EDEVICE;
+    }
+    return HARTS_OK;
+}
+
+size_t harts_kda_chunk_state_bytes(const harts_plan *P, int32_t H, int32_t dk, int32_t dv,
+                                   int32_t dtype) {
+    if (!P || H < 1 || dk < 1 || dv < 1) return 0;
+    return size_t(P->info.n_chunks) * H * dk * dv * dtype_size(dtype);
+}
+
+size_t harts_kda_bwd_workspace_bytes(const harts_plan *P, int32_t H, int32_t dk, int32_t dv) {
+    if (!P || H < 1 || dk < 1 || dk != dv) return 0;
+    return bwd_ws(P, H, dk).total;
+}
+
+int harts_kda_fwd(const harts_plan *P, const harts_kda_fwd_args *a, harts_stream_t stream) {
+    int rc = check_fwd_args(P, a);
+    if (rc) return rc;
+    if (!a->o) { set_error("NULL output o"); return HARTS_EINVAL; }
+    const int BC = P->info.chunk;
+    const int fam = pick(a, BC, false);
+    if (fam < 0) { set_error("no kernel for this dk/dv/chunk/dtype"); return HARTS_EUNSUPPORTED; }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    FwdParams p = make_fwd(a);
+    for (int32_t r = 0; r < P->info.n_rounds; ++r) {
+        const int32_t base = P->round_seq_ptr[r];
+        const int32_t n = (P->round_seq_ptr[r + 1] - base) * a->H;
+        if (n == 0) continue;
+        cudaError_t e = fam == 1 ? tc_fwd_round(p, P->view, base, n, P->info.max_seq_chunks, st)
+                                 : simt_fwd_round(a->dtype, BC, p, P->view, base, n, st);
+        if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    }
+    set_error("");
+    return HARTS_OK;
+}
+
+int harts_kda_bwd(const harts_plan *P, const harts_kda_bwd_args *a, harts_stream_t stream) {
+    if (!a) { set_error("NULL args"); return HARTS_EINVAL; }
+    int rc = check_fwd_args(P, &a->fwd);
+    if (rc) return rc;
+    if (!a->d_o || !a->dq || !a->dk || !a->dv || !a->dg || !a->dbeta) { set_error("NULL gradient pointer"); return HARTS_EINVAL; }
+    if (!a->fwd.chunk_states) { set_error("chunk_states from the forward pass are required"); return HARTS_EINVAL; }
+    const int D = a->fwd.dk, H = a->fwd.H, BC = P->info.chunk;
+    const BwdWs ws = bwd_ws(P, H, D);
+    if (!a->workspace || a->workspace_bytes < ws.total) { set_error("workspace too small"); return HARTS_ESMALLBUF; }
+    if (reinterpret_cast<uintptr_t>(a->workspace) % 256) { set_error("workspace must be 256-B aligned"); return HARTS_EINVAL; }
+    const int fam = pick(&a->fwd, BC, true);
+    if (fam < 0) { set_error("no backward kernel for this dk/dv/chunk/dtype"); return HARTS_EUNSUPPORTED; }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    BwdParams p{};
+    p.f = make_fwd(&a->fwd);
+    p.d_o = a->d_o; p.d_final = a->d_final;
+    p.dq = a->dq; p.dk = a->dk; p.dv = a->dv; p.dg = a->dg; p.dbeta = a->dbeta; p.dh0 = a->dh0;
+    char *w = static_cast<char *>(a->workspace);
+    p.ds_init = reinterpret_cast<float *>(w + ws.ds_init);
+    p.rep_grad = reinterpret_cast<float *>(w + ws.rep_grad);
+    for (int32_t r = P->info.n_rounds - 1; r >= 0; --r) {
+        const int32_t base = P->round_seq_ptr[r];
+        const int32_t n = (P->round_seq_ptr[r + 1] - base) * H;
+        if (n == 0) continue;
+        cudaError_t e = fam == 1 ? tc_bwd_round(p, P->view, base, n, P->info.max_seq_chunks, st)
+                                 : simt_bwd_round(a->fwd.dtype, BC, p, P->view, base, n, st);
+        if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    }
+    cudaError_t e = bwd_finish(a->fwd.dtype, p, P->view, st);
+    if (e != cudaSuccess) return cuda_fail(e, "backward reductions");
+    set_error("");
+    return HARTS_OK;
+}
+
+}  // extern "C"

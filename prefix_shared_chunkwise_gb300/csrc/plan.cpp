@@ -1,0 +1,380 @@
+// Host planner: minimum number of sequential packed KDA calls over a segment forest.
+//
+// HARTS (page "HARTS ... 精读", section 4.2): the rollout tree is contracted into
+// fork-free segments.  A boundary state produced inside a packed chunkwise call can
+// only initialise another input sequence after that call returns, so at each fork at
+// most one child (the direct continuation) stays in the current sequence.  A side
+// branch at fork end p resumes from the chunk-boundary state at a(p) = B*floor(p/B)
+// and replays the ancestor tokens [a(p), p).  T_pre(v) / T_in(v) are the fewest
+// rounds for v's subtree when v's entry anchor state is ready before the call /
+// when v enters the call as a direct continuation; a continuation does not wait, a
+// side branch waits one round -- unless the fork lies in the chunk where the current
+// sequence starts, in which case the side branch can start in the same call from the
+// same anchor state (Fig. 2(c): "replay-started v2" in round 1).  Linear time: one
+// bottom-up pass keeping the largest and second-largest child T_pre, one top-down
+// pass assigning rounds as early as possible.
+#include <algorithm>
+#include <cstring>
+#include <new>
+
+#include "plan_internal.h"
+
+namespace harts {
+
+thread_local std::string g_last_error;
+void set_error(const std::string &msg) { g_last_error = msg; }
+
+namespace {
+
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+
+int64_t floor_to(int64_t x, int64_t B) { return (x / B) * B; }
+
+int build(harts_plan &P, int32_t n, const int32_t *parent, const int64_t *len, int32_t B) {
+    // ---- a1: validate, positions s_v, e_v --------------------------------------
+    std::vector<int64_t> s(n), e(n);
+    std::vector<int32_t> nkids(n, 0);
+    int64_t C = 0;
+    int32_t n_roots = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t p = parent[i];
+        if (p < -1 || p >= i) { set_error("parent[i] must be -1 or < i"); return HARTS_EINVAL; }
+        if (len[i] < 1) { set_error("segment length must be >= 1"); return HARTS_EINVAL; }
+        if (len[i] > kMaxRows) { set_error("segment too long"); return HARTS_EOVERFLOW; }
+        s[i] = p < 0 ? 0 : e[p];
+        e[i] = s[i] + len[i];
+        if (e[i] > (int64_t(1) << 40)) { set_error("trajectory too long"); return HARTS_EOVERFLOW; }
+        C += len[i];
+        if (C > kMaxRows) { set_error("more than 2^31-1 compact rows"); return HARTS_EOVERFLOW; }
+        if (p >= 0) nkids[p]++; else n_roots++;
+    }
+    // children in ascending id order (CSR)
+    std::vector<int32_t> kptr(n + 1, 0), kids(std::max(n - n_roots, 0));
+    for (int32_t i = 0; i < n; ++i) kptr[i + 1] = kptr[i] + nkids[i];
+    {
+        std::vector<int32_t> fill(kptr.begin(), kptr.end() - 1);
+        for (int32_t i = 0; i < n; ++i) if (parent[i] >= 0) kids[fill[parent[i]]++] = i;
+    }
+
+    // ---- a2: bottom-up T_pre / T_in ------------------------------------------------
+    std::vector<int32_t> tpre(n), tin(n), ctop(n, -1);
+    for (int32_t v = n - 1; v >= 0; --v) {
+        if (nkids[v] == 0) { tpre[v] = tin[v] = 1; continue; }
+        int32_t best = -1, m1 = 0, m2 = 0;
+        for (int32_t j = kptr[v]; j < kptr[v + 1]; ++j) {
+            int32_t c = kids[j], t = tpre[c];
+            if (t > m1) { m2 = m1; m1 = t; best = c; }   // ascending ids: first max wins
+            else if (t > m2) m2 = t;
+        }
+        ctop[v] = best;
+        tin[v] = std::max(tin[best], 1 + m2);
+        tpre[v] = (floor_to(s[v], B) == floor_to(e[v], B)) ? m1 : tin[v];
+    }
+
+    // ---- a2: top-down ASAP recovery ------------------------------------------------
+    // Sequences are first identified by their first segment.  Per segment: the first
+    // segment of its sequence.  Per first segment: round, anchor, source.
+    struct SeqTmp { int32_t round; int64_t anchor; int32_t src_kind; int32_t src_a; int64_t src_b; };
+    // src_kind 0: root (src_a = root index); 1: slot of producer first seg src_a at src_b
+    std::vector<int32_t> head(n, -1);        // first segment of v's sequence
+    std::vector<SeqTmp> tmp(n);
+    std::vector<int32_t> root_index(n, -1);
+    // temp slots discovered in segment order; per producer the last slot for dedup
+    std::vector<int32_t> last_slot(n, -1);
+    std::vector<int32_t> slot_prod;          // temp slot -> producer first seg
+    std::vector<int64_t> slot_lpos;          // temp slot -> local position
+    std::vector<int32_t> tmp_src_slot(n, -1); // first seg -> temp slot id (src_kind 1)
+    {
+        int32_t r = 0;
+        for (int32_t v = 0; v < n; ++v) if (parent[v] < 0) root_index[v] = r++;
+    }
+    for (int32_t v = 0; v < n; ++v) {
+        if (parent[v] < 0) {
+            head[v] = v;
+            tmp[v] = SeqTmp{1, 0, 0, root_index[v], 0};
+        }
+        const int32_t f = head[v];
+        const SeqTmp &sq = tmp[f];
+        for (int32_t j = kptr[v]; j < kptr[v + 1]; ++j) {
+            int32_t c = kids[j];
+            if (c == ctop[v]) { head[c] = f; continue; }
+            head[c] = c;
+            const int64_t a_e = floor_to(e[v], B);
+            if (a_e == sq.anchor) {
+                tmp[c] = sq;
+                tmp_src_slot[c] = tmp_src_slot[f];
+            } else {
+                const int64_t lpos = a_e - sq.anchor;
+                int32_t ls = last_slot[f];
+                if (ls < 0 || slot_lpos[ls] != lpos) {
+                    ls = static_cast<int32_t>(slot_prod.size());
+                    slot_prod.push_back(f);
+                    slot_lpos.push_back(lpos);
+                    last_slot[f] = ls;
+                }
+                tmp[c] = SeqTmp{sq.round + 1, a_e, 1, f, lpos};
+                tmp_src_slot[c] = ls;
+            }
+        }
+    }
+
+    // ---- a3: layout order: by round, then by first segment id (bucket pass) ----------
+    int32_t n_rounds = 0, n_seq = 0;
+    for (int32_t v = 0; v < n; ++v) if (head[v] == v) { n_seq++; n_rounds = std::max(n_rounds, tmp[v].round); }
+    std::vector<int32_t> rptr(n_rounds + 2, 0);
+    for (int32_t v = 0; v < n; ++v) if (head[v] == v) rptr[tmp[v].round + 1]++;
+    for (int32_t r = 1; r <= n_rounds + 1 && r < (int32_t)rptr.size(); ++r) rptr[r] += rptr[r - 1];
+    std::vector<int32_t> order(n_seq), seq_of_first(n, -1);
+    {
+        std::vector<int32_t> fill(rptr.begin(), rptr.end());
+        for (int32_t v = 0; v < n; ++v)
+            if (head[v] == v) { int32_t id = fill[tmp[v].round]++; order[id] = v; seq_of_first[v] = id; }
+    }
+
+    P.info.n_seg = n; P.info.n_roots = n_roots; P.info.chunk = B;
+    P.info.n_rounds = n_rounds; P.info.n_seq = n_seq;
+    int32_t n_leaves = 0;
+    for (int32_t v = 0; v < n; ++v) n_leaves += nkids[v] == 0;
+    P.info.n_leaves = n_leaves;
+    P.round_seq_ptr.assign(n_rounds + 1, 0);
+    for (int32_t r = 0; r <= n_rounds; ++r) P.round_seq_ptr[r] = rptr[r + 1 - 1 + 1 - 1 + 1 - 1];
+    // rptr[r] = number of sequences with round < r (rounds are 1-based)
+    for (int32_t r = 0; r <= n_rounds; ++r) P.round_seq_ptr[r] = rptr[r + 1];
+
+    // compact rows: sequence order, then continuation chain
+    P.seg_offset.assign(n, 0); P.seg_pos.assign(s.begin(), s.end()); P.seg_seq.assign(n, 0);
+    P.cu_seqlens.assign(n_seq + 1, 0);
+    int64_t row = 0;
+    for (int32_t i = 0; i < n_seq; ++i) {
+        P.cu_seqlens[i] = row;
+        for (int32_t v = order[i]; v >= 0; v = ctop[v]) {
+            P.seg_offset[v] = row;
+            P.seg_seq[v] = i;
+            row += len[v];
+        }
+    }
+    P.cu_seqlens[n_seq] = row;
+
+    // slots numbered by producer sequence, then position (temp slots of one producer
+    // were discovered in increasing position along its chain)
+    const int32_t n_tmp = static_cast<int32_t>(slot_prod.size());
+    std::vector<int32_t> per_seq(n_seq + 1, 0);
+    for (int32_t t = 0; t < n_tmp; ++t) per_seq[seq_of_first[slot_prod[t]] + 1]++;
+    for (int32_t i = 0; i < n_seq; ++i) per_seq[i + 1] += per_seq[i];
+    std::vector<int32_t> slot_final(n_tmp);
+    P.state_seq.assign(n_tmp, 0); P.state_pos.assign(n_tmp, 0);
+    {
+        std::vector<int32_t> fill(per_seq.begin(), per_seq.end() - 1);
+        for (int32_t t = 0; t < n_tmp; ++t) {
+            int32_t sq = seq_of_first[slot_prod[t]];
+            int32_t id = fill[sq]++;
+            slot_final[t] = id;
+            P.state_seq[id] = sq;
+            P.state_pos[id] = slot_lpos[t];
+        }
+    }
+    P.seq_state_ptr.assign(per_seq.begin(), per_seq.end());
+    P.info.n_states = n_tmp;
+
+    // per-sequence arrays, replay gather lists
+    P.seq_round.assign(n_seq, 0); P.seq_first_seg.assign(n_seq, 0); P.seq_anchor.assign(n_seq, 0);
+    P.seq_replay.assign(n_seq, 0); P.seq_src.assign(n_seq, 0); P.replay_ptr.assign(n_seq + 1, 0);
+    P.seq_nchunks.assign(n_seq, 0);
+    P.replay_idx.clear();
+    std::vector<int32_t> upath;
+    int32_t n_cons = 0, max_chunks = 0;
+    int64_t n_chunks = 0;
+    for (int32_t i = 0; i < n_seq; ++i) {
+        const int32_t f = order[i];
+        const SeqTmp &sq = tmp[f];
+        P.seq_round[i] = sq.round;
+        P.seq_first_seg[i] = f;
+        P.seq_anchor[i] = sq.anchor;
+        const int64_t rho = s[f] - sq.anchor;
+        if (rho < 0 || rho >= B) { set_error("internal: replay out of range"); return HARTS_EINVAL; }
+        P.seq_replay[i] = static_cast<int32_t>(rho);
+        if (sq.src_kind == 0) P.seq_src[i] = -1 - sq.src_a;
+        else { P.seq_src[i] = slot_final[tmp_src_slot[f]]; n_cons++; }
+        P.replay_ptr[i] = static_cast<int64_t>(P.replay_idx.size());
+        upath.clear();
+        for (int32_t w = parent[f]; w >= 0 && e[w] > sq.anchor; w = parent[w]) upath.push_back(w);
+        for (auto it = upath.rbegin(); it != upath.rend(); ++it) {
+            const int32_t w = *it;
+            for (int64_t p = std::max(s[w], sq.anchor); p < e[w]; ++p)
+                P.replay_idx.push_back(P.seg_offset[w] + (p - s[w]));
+        }
+        if (static_cast<int64_t>(P.replay_idx.size()) - P.replay_ptr[i] != rho) {
+            set_error("internal: replay gather length mismatch"); return HARTS_EINVAL;
+        }
+        const int64_t L = rho + (P.cu_seqlens[i + 1] - P.cu_seqlens[i]);
+        const int64_t nc = (L + B - 1) / B;
+        P.seq_nchunks[i] = static_cast<int32_t>(nc);
+        max_chunks = std::max<int32_t>(max_chunks, static_cast<int32_t>(nc));
+        n_chunks += nc;
+    }
+    P.replay_ptr[n_seq] = static_cast<int64_t>(P.replay_idx.size());
+    P.info.n_cons = n_cons;
+    P.info.C = C;
+    P.info.R = static_cast<int64_t>(P.replay_idx.size());
+    P.info.n_chunks = n_chunks;
+    P.info.max_seq_chunks = max_chunks;
+    if (n_chunks > kMaxRows || P.info.R > kMaxRows) { set_error("too many chunks"); return HARTS_EOVERFLOW; }
+
+    // expanded size S = sum_v len_v * leaves under v
+    {
+        std::vector<int64_t> lv(n, 0);
+        int64_t S = 0;
+        for (int32_t v = n - 1; v >= 0; --v) {
+            if (nkids[v] == 0) lv[v] += 1;
+            S += len[v] * lv[v];
+            if (parent[v] >= 0) lv[parent[v]] += lv[v];
+        }
+        P.info.S = S;
+    }
+
+    // consumers of every slot and root, ascending sequence id (counting sort)
+    P.state_cons_ptr.assign(n_tmp + 1, 0);
+    P.root_cons_ptr.assign(n_roots + 1, 0);
+    for (int32_t i = 0; i < n_seq; ++i) {
+        if (P.seq_src[i] >= 0) P.state_cons_ptr[P.seq_src[i] + 1]++;
+        else P.root_cons_ptr[-1 - P.seq_src[i] + 1]++;
+    }
+    for (int32_t j = 0; j < n_tmp; ++j) P.state_cons_ptr[j + 1] += P.state_cons_ptr[j];
+    for (int32_t j = 0; j < n_roots; ++j) P.root_cons_ptr[j + 1] += P.root_cons_ptr[j];
+    P.state_cons.assign(n_cons, 0);
+    P.root_cons.assign(n_seq - n_cons, 0);
+    {
+        std::vector<int32_t> fs(P.state_cons_ptr.begin(), P.state_cons_ptr.end() - 1);
+        std::vector<int32_t> fr(P.root_cons_ptr.begin(), P.root_cons_ptr.end() - 1);
+        for (int32_t i = 0; i < n_seq; ++i) {
+            if (P.seq_src[i] >= 0) P.state_cons[fs[P.seq_src[i]]++] = i;
+            else P.root_cons[fr[-1 - P.seq_src[i]]++] = i;
+        }
+    }
+
+    P.seg_ctop = ctop; P.seg_tpre = tpre; P.seg_tin = tin;
+    return HARTS_OK;
+}
+
+void build_image(harts_plan &P) {
+    auto &I = P.image;
+    auto &w = I.words;
+    w.clear();
+    auto put = [&](int64_t &off, const int32_t *src, size_t cnt) {
+        // 16-byte aligned tables
+        while (w.size() % 4) w.push_back(0);
+        off = static_cast<int64_t>(w.size());
+        w.insert(w.end(), src, src + cnt);
+    };
+    const int32_t n_seq = P.info.n_seq, n_st = P.info.n_states, n_rounds = P.info.n_rounds;
+    int32_t zero4[4] = {0, 0, 0, 0};
+    put(I.off_err, zero4, 4);
+    put(I.off_round_seq_ptr, P.round_seq_ptr.data(), n_rounds + 1);
+    // per round: longest sequence first (ties: lower id first)
+    std::vector<int32_t> ord(n_seq);
+    for (int32_t i = 0; i < n_seq; ++i) ord[i] = i;
+    for (int32_t r = 0; r < n_rounds; ++r)
+        std::stable_sort(ord.begin() + P.round_seq_ptr[r], ord.begin() + P.round_seq_ptr[r + 1],
+                         [&](int32_t a, int32_t b) { return P.seq_nchunks[a] > P.seq_nchunks[b]; });
+    put(I.off_round_order, ord.data(), n_seq);
+    std::vector<int32_t> t(n_seq);
+    for (int32_t i = 0; i < n_seq; ++i) t[i] = static_cast<int32_t>(P.cu_seqlens[i]);
+    put(I.off_seq_row0, t.data(), n_seq);
+    for (int32_t i = 0; i < n_seq; ++i) t[i] = static_cast<int32_t>(P.cu_seqlens[i + 1] - P.cu_seqlens[i]);
+    put(I.off_seq_nown, t.data(), n_seq);
+    put(I.off_seq_rho, P.seq_replay.data(), n_seq);
+    for (int32_t i = 0; i < n_seq; ++i) t[i] = static_cast<int32_t>(P.replay_ptr[i]);
+    put(I.off_seq_rptr, t.data(), n_seq);
+    put(I.off_seq_src, P.seq_src.data(), n_seq);
+    put(I.off_seq_sptr, P.seq_state_ptr.data(), n_seq + 1);
+    std::vector<int32_t> lp(n_st);
+    for (int32_t j = 0; j < n_st; ++j) lp[j] = static_cast<int32_t>(P.state_pos[j]);
+    put(I.off_state_lpos, lp.data(), n_st);
+    int64_t cb = 0;
+    for (int32_t i = 0; i < n_seq; ++i) { t[i] = static_cast<int32_t>(cb); cb += P.seq_nchunks[i]; }
+    put(I.off_seq_cbase, t.data(), n_seq);
+    put(I.off_state_cptr, P.state_cons_ptr.data(), n_st + 1);
+    put(I.off_state_cons, P.state_cons.data(), P.state_cons.size());
+    put(I.off_root_cptr, P.root_cons_ptr.data(), P.info.n_roots + 1);
+    put(I.off_root_cons, P.root_cons.data(), P.root_cons.size());
+    const int64_t R = P.info.R;
+    std::vector<int32_t> ri(R);
+    for (int64_t j = 0; j < R; ++j) ri[j] = static_cast<int32_t>(P.replay_idx[j]);
+    put(I.off_replay_idx, ri.data(), R);
+    // fold lists: replay occurrences grouped by compact row (stable counting sort)
+    std::vector<int32_t> occ(R);
+    for (int64_t j = 0; j < R; ++j) occ[j] = static_cast<int32_t>(j);
+    std::stable_sort(occ.begin(), occ.end(), [&](int32_t a, int32_t b) { return ri[a] < ri[b]; });
+    std::vector<int32_t> frows, fptr;
+    for (int64_t j = 0; j < R; ++j) {
+        if (j == 0 || ri[occ[j]] != ri[occ[j - 1]]) { frows.push_back(ri[occ[j]]); fptr.push_back(static_cast<int32_t>(j)); }
+    }
+    fptr.push_back(static_cast<int32_t>(R));
+    P.info.n_fold_rows = static_cast<int32_t>(frows.size());
+    put(I.off_fold_rows, frows.data(), frows.size());
+    put(I.off_fold_ptr, fptr.data(), fptr.size());
+    put(I.off_fold_occ, occ.data(), R);
+    while (w.size() % 64) w.push_back(0);
+}
+
+}  // namespace
+}  // namespace harts
+
+using harts::set_error;
+
+extern "C" {
+
+const char *harts_last_error(void) { return harts::g_last_error.c_str(); }
+
+int harts_plan_calls(int32_t n_seg, const int32_t *parent, const int64_t *seg_len, int32_t chunk,
+                     uint32_t flags, harts_plan **out) {
+    if (!out) { set_error("out is NULL"); return HARTS_EINVAL; }
+    *out = nullptr;
+    if (n_seg < 1 || !parent || !seg_len) { set_error("empty or NULL tree"); return HARTS_EINVAL; }
+    if (chunk < 1 || chunk > (1 << 20)) { set_error("chunk must be >= 1"); return HARTS_EINVAL; }
+    if (flags != 0) { set_error("unknown flags"); return HARTS_EINVAL; }
+    harts_plan *P = new (std::nothrow) harts_plan();
+    if (!P) { set_error("out of host memory"); return HARTS_EINVAL; }
+    try {
+        int rc = harts::build(*P, n_seg, parent, seg_len, chunk);
+        if (rc != HARTS_OK) { delete P; return rc; }
+        harts::build_image(*P);
+    } catch (const std::bad_alloc &) {
+        delete P; set_error("out of host memory"); return HARTS_EOVERFLOW;
+    }
+    *out = P;
+    set_error("");
+    return HARTS_OK;
+}
+
+int harts_plan_get_info(const harts_plan *plan, harts_plan_info *out) {
+    if (!plan || !out) { set_error("NULL argument"); return HARTS_EINVAL; }
+    *out = plan->info;
+    return HARTS_OK;
+}
+
+int harts_plan_export(const harts_plan *P, harts_plan_arrays *d) {
+    if (!P || !d) { set_error("NULL argument"); return HARTS_EINVAL; }
+    auto cp = [](auto *dst, const auto &v) {
+        if (dst && !v.empty()) std::memcpy(dst, v.data(), v.size() * sizeof(v[0]));
+    };
+    cp(d->seg_offset, P->seg_offset); cp(d->seg_pos, P->seg_pos); cp(d->seg_seq, P->seg_seq);
+    cp(d->seg_ctop, P->seg_ctop); cp(d->seg_tpre, P->seg_tpre); cp(d->seg_tin, P->seg_tin);
+    cp(d->round_seq_ptr, P->round_seq_ptr); cp(d->cu_seqlens, P->cu_seqlens);
+    cp(d->seq_round, P->seq_round); cp(d->seq_first_seg, P->seq_first_seg);
+    cp(d->seq_anchor, P->seq_anchor); cp(d->seq_replay, P->seq_replay); cp(d->seq_src, P->seq_src);
+    cp(d->replay_ptr, P->replay_ptr); cp(d->replay_idx, P->replay_idx);
+    cp(d->seq_state_ptr, P->seq_state_ptr); cp(d->state_seq, P->state_seq);
+    cp(d->state_pos, P->state_pos); cp(d->state_cons_ptr, P->state_cons_ptr);
+    cp(d->state_cons, P->state_cons); cp(d->root_cons_ptr, P->root_cons_ptr);
+    cp(d->root_cons, P->root_cons);
+    return HARTS_OK;
+}
+
+size_t harts_plan_device_bytes(const harts_plan *P) {
+    return P ? P->image.words.size() * sizeof(int32_t) : 0;
+}
+
+void harts_plan_free(harts_plan *P) { delete P; }
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// Internal plan representation shared by the host planner and the kernel launchers.
+#pragma once
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/harts.h"
+
+namespace harts {
+
+// Device view of an uploaded plan: pointers into one int32 image.
+struct PlanDev {
+    int32_t *err;                // [4] device error word: code, info, info, info
+    const int32_t *round_seq_ptr;  // [n_rounds+1]
+    const int32_t *round_order;    // [n_seq] per round, sequences longest first
+    const int32_t *seq_row0;       // [n_seq] first own compact row
+    const int32_t *seq_nown;       // [n_seq] own rows
+    const int32_t *seq_rho;        // [n_seq] replay rows
+    const int32_t *seq_rptr;       // [n_seq] start in replay_idx
+    const int32_t *seq_src;        // [n_seq] slot id, or -1-root
+    const int32_t *seq_sptr;       // [n_seq+1] slots produced by the sequence
+    const int32_t *state_lpos;     // [n_states] local position of the slot
+    const int32_t *seq_cbase;      // [n_seq] first chunk index of the sequence
+    const int32_t *state_cptr;     // [n_states+1]
+    const int32_t *state_cons;     // consumers of each slot, ascending
+    const int32_t *root_cptr;      // [n_roots+1]
+    const int32_t *root_cons;      // sequences starting from root r, ascending
+    const int32_t *replay_idx;     // [R]
+    const int32_t *fold_rows;      // [n_fold] distinct replayed rows, ascending
+    const int32_t *fold_ptr;       // [n_fold+1]
+    const int32_t *fold_occ;       // [R] replay occurrence ids grouped by row
+    int32_t n_rounds, n_seq, n_states, n_roots, n_fold, chunk;
+    int64_t R, n_chunks;
+};
+
+// Word offsets of each table inside the device image.
+struct PlanImage {
+    std::vector<int32_t> words;
+    int64_t off_err, off_round_seq_ptr, off_round_order, off_seq_row0, off_seq_nown,
+        off_seq_rho, off_seq_rptr, off_seq_src, off_seq_sptr, off_state_lpos, off_seq_cbase,
+        off_state_cptr, off_state_cons, off_root_cptr, off_root_cons, off_replay_idx,
+        off_fold_rows, off_fold_ptr, off_fold_occ;
+};
+
+void set_error(const std::string &msg);
+
+}  // namespace harts
+
+struct harts_plan {
+    harts_plan_info info{};
+    std::vector<int64_t> seg_offset, seg_pos;
+    std::vector<int32_t> seg_seq, seg_ctop, seg_tpre, seg_tin;
+    std::vector<int32_t> round_seq_ptr;
+    std::vector<int64_t> cu_seqlens;
+    std::vector<int32_t> seq_round, seq_first_seg, seq_replay, seq_src;
+    std::vector<int64_t> seq_anchor, replay_ptr, replay_idx;
+    std::vector<int32_t> seq_state_ptr, state_seq;
+    std::vector<int64_t> state_pos;
+    std::vector<int32_t> state_cons_ptr, state_cons, root_cons_ptr, root_cons;
+    std::vector<int32_t> seq_nchunks;
+    harts::PlanImage image;
+    void *dev = nullptr;           // uploaded image (caller-owned)
+    harts::PlanDev view{};         // valid once uploaded
+};

@@ -1,0 +1,125 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same
+seeded inputs.  Relative L2 per output tensor: <= 1e-5 for fp32 workloads, <= 1e-2
+for bf16 workloads.  Plans are compared bit-exactly elsewhere (test_plan_abi.py)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from oracle import plan_twin
+from prefix_shared_chunkwise_gb300 import _lib
+from prefix_shared_chunkwise_gb300.api import Plan, kda_bwd, kda_fwd
+from prefix_shared_chunkwise_gb300.synth import WORKLOADS, fig1_tree, make_inputs, make_tree
+from tests._parity import oracle_run, rel_l2
+
+pytestmark = pytest.mark.gpu
+TOL = {"fp32": 1e-5, "bf16": 1e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from prefix_shared_chunkwise_gb300 import build
+    build.build()
+
+
+def _run(parent, seg_len, B, H, D, dtype, seed, *, backward, kernel=_lib.HARTS_KERNEL_AUTO,
+         h0=False, d_final=False, decay=1.0, scale=1.0):
+    pl = Plan(parent, seg_len, B).upload()
+    info = pl.info
+    C = info["C"]
+    x = make_inputs(C, H, D, D, dtype, seed, device="cpu")
+    if decay != 1.0:
+        x["g"] = (x["g"].float() * decay).to(x["g"].dtype)
+    dev = {k: v.cuda() for k, v in x.items()}
+    td = dev["q"].dtype
+    h0_t = None
+    if h0:
+        gen = torch.Generator().manual_seed(seed + 77)
+        h0_t = torch.randn((info["n_roots"], H, D, D), generator=gen) * 0.3
+    dF = None
+    if d_final:
+        gen = torch.Generator().manual_seed(seed + 78)
+        dF = torch.randn((info["n_seq"], H, D, D), generator=gen)
+    cs = torch.empty(pl.chunk_state_bytes(H, D, D, 0 if dtype == "fp32" else 1) // (4 if dtype == "fp32" else 2),
+                     dtype=td, device="cuda")
+    fin = torch.empty((info["n_seq"], H, D, D), dtype=torch.float32, device="cuda")
+    o, states, fin, cs = kda_fwd(pl, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
+                                 final_state=fin, h0=None if h0_t is None else h0_t.cuda(),
+                                 chunk_states=cs, scale=scale, kernel=kernel)
+    out = dict(o=o, final=fin)
+    if backward:
+        dh0 = torch.empty_like(h0_t).cuda() if h0 else None
+        gr = kda_bwd(pl, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["W"],
+                     states=states, chunk_states=cs, d_final=None if dF is None else dF.cuda(),
+                     h0=None if h0_t is None else h0_t.cuda(), dh0=dh0, scale=scale,
+                     kernel=kernel)
+        out.update(gr)
+    torch.cuda.synchronize()
+    assert pl.device_error() == 0
+    ref = oracle_run(parent, seg_len, B, x, backward=backward,
+                     h0=None if h0_t is None else h0_t.double().numpy(),
+                     d_final_seq=None if dF is None else dF.double().numpy(), scale=scale)
+    errs = {"o": rel_l2(out["o"].float().cpu().numpy(), ref["o"]),
+            "final": rel_l2(out["final"].cpu().numpy(), ref["final_seq"])}
+    if backward:
+        for n in ("dq", "dk", "dv", "dg", "dbeta"):
+            errs[n] = rel_l2(out[n].float().cpu().numpy(), ref[n])
+        if h0:
+            errs["dh0"] = rel_l2(out["dh0"].cpu().numpy(), ref["dh0"])
+    return errs
+
+
+def _assert(errs, tol):
+    bad = {k: v for k, v in errs.items() if not (v <= tol)}
+    assert not bad, f"rel L2 above {tol}: {bad} (all: {errs})"
+
+
+def test_fig1_fp32_fwd_bwd():
+    wl = WORKLOADS["fig1_fp32"]
+    parent, seg_len = fig1_tree()
+    errs = _run(parent, seg_len, wl.chunk, wl.H, wl.dk, "fp32", 0, backward=True)
+    _assert(errs, TOL["fp32"])
+
+
+@pytest.mark.parametrize("B", [16, 32, 64])
+@pytest.mark.parametrize("seed", [1, 2])
+def test_random_forest_fp32_with_h0_and_dfinal(B, seed):
+    rng = np.random.Generator(np.random.PCG64(seed * 10 + B))
+    n = 14
+    parent = np.array([-1 if (i == 0 or rng.random() < 0.15) else int(rng.integers(0, i))
+                       for i in range(n)], np.int32)
+    seg_len = rng.integers(1, 3 * B, size=n).astype(np.int64)
+    errs = _run(parent, seg_len, B, 2, 32, "fp32", seed, backward=True, h0=True, d_final=True,
+                decay=0.1, scale=0.8)
+    _assert(errs, TOL["fp32"])
+
+
+def test_fp32_d64_fwd_bwd_mild_decay():
+    rng = np.random.Generator(np.random.PCG64(5))
+    n = 9
+    parent = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)], np.int32)
+    seg_len = rng.integers(1, 90, size=n).astype(np.int64)
+    errs = _run(parent, seg_len, 32, 2, 64, "fp32", 3, backward=True, decay=0.05)
+    _assert(errs, TOL["fp32"])
+
+
+@pytest.mark.parametrize("kernel", [_lib.HARTS_KERNEL_SIMT, _lib.HARTS_KERNEL_AUTO])
+def test_bf16_d128_forward_small_forest(kernel):
+    rng = np.random.Generator(np.random.PCG64(8))
+    n = 12
+    parent = np.array([-1 if (i == 0 or rng.random() < 0.1) else int(rng.integers(0, i))
+                       for i in range(n)], np.int32)
+    seg_len = rng.integers(1, 200, size=n).astype(np.int64)
+    errs = _run(parent, seg_len, 64, 4, 128, "bf16", 4, backward=False, kernel=kernel)
+    _assert(errs, TOL["bf16"])
+
+
+def test_bf16_d128_forward_mild_decay():
+    rng = np.random.Generator(np.random.PCG64(9))
+    n = 10
+    parent = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)], np.int32)
+    seg_len = rng.integers(1, 300, size=n).astype(np.int64)
+    errs = _run(parent, seg_len, 64, 2, 128, "bf16", 6, backward=False, decay=0.02)
+    _assert(errs, TOL["bf16"])

@@ -1,0 +1,104 @@
+"""The C++ planner behind harts_plan_calls against the planner oracle: call counts,
+rounds, layout, replay gather lists, slots and consumers must be bit-exact.  Also:
+the library loads and exports every symbol include/harts.h declares, and host-side
+argument validation rejects malformed trees."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import plan_twin
+from prefix_shared_chunkwise_gb300 import _lib
+from prefix_shared_chunkwise_gb300.api import Plan
+from prefix_shared_chunkwise_gb300.synth import WORKLOAD_ORDER, WORKLOADS, make_tree
+from tests._golden import load_calls
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from prefix_shared_chunkwise_gb300 import build
+    build.build()
+
+
+def test_library_exports_every_declared_symbol():
+    hdr = open(os.path.join(ROOT, "include", "harts.h")).read()
+    declared = set(re.findall(r"\b(harts_[a-z_0-9]+)\s*\(", hdr))
+    assert declared == set(_lib.EXPORTED)
+    L = ctypes.CDLL(_lib.SO_PATH)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+KEYS = ["seg_offset", "seg_pos", "seg_seq", "round_seq_ptr", "cu_seqlens", "seq_round",
+        "seq_first_seg", "seq_anchor", "seq_replay", "seq_src", "replay_ptr", "replay_idx",
+        "seq_state_ptr", "state_seq", "state_pos", "state_cons_ptr", "state_cons",
+        "root_cons_ptr", "root_cons"]
+
+
+def _compare(parent, seg_len, B):
+    tw = plan_twin.plan(parent, seg_len, B)
+    pl = Plan(parent, seg_len, B)
+    ar = pl.arrays()
+    info = pl.info
+    assert info["n_rounds"] == tw["n_rounds"]
+    assert info["n_seq"] == tw["n_seq"] and info["n_states"] == tw["n_states"]
+    assert info["C"] == tw["C"] and info["S"] == tw["S"] and info["R"] == tw["R"]
+    for k in KEYS:
+        np.testing.assert_array_equal(ar[k], tw[k], err_msg=k)
+    np.testing.assert_array_equal(ar["seg_tpre"], tw["Tpre"])
+    np.testing.assert_array_equal(ar["seg_tin"], tw["Tin"])
+    np.testing.assert_array_equal(ar["seg_ctop"], tw["ctop"])
+    return pl, tw
+
+
+@pytest.mark.parametrize("fixture", ["fig1_calls.txt", "fig2_calls.txt", "figC1_calls.txt"])
+def test_planner_matches_oracle_on_figures(fixture):
+    gd = load_calls(fixture)
+    _compare(gd["parent"], gd["seg_len"], gd["chunk"])
+
+
+def test_planner_matches_oracle_random_forests():
+    rng = np.random.Generator(np.random.PCG64(21))
+    for _ in range(400):
+        n = int(rng.integers(1, 60))
+        B = int(rng.choice([1, 4, 16, 64]))
+        parent = np.array([-1 if (i == 0 or rng.random() < 0.08) else int(rng.integers(0, i))
+                           for i in range(n)], np.int32)
+        seg_len = rng.integers(1, 3 * B + 2, size=n).astype(np.int64)
+        _compare(parent, seg_len, B)
+
+
+@pytest.mark.parametrize("name", WORKLOAD_ORDER)
+def test_planner_matches_oracle_on_workloads(name):
+    parent, seg_len = make_tree(name)
+    pl, tw = _compare(parent, seg_len, WORKLOADS[name].chunk)
+    assert pl.info["n_rounds"] >= 1
+
+
+def test_planner_linear_time_on_a_million_segments():
+    import time
+    rng = np.random.Generator(np.random.PCG64(1))
+    n = 1_000_000
+    parent = np.maximum(np.arange(n) - 1 - rng.integers(0, 4, size=n), -1).astype(np.int32)
+    parent[0] = -1
+    seg_len = rng.integers(1, 200, size=n).astype(np.int64)
+    t = time.time()
+    pl = Plan(parent, seg_len, 64)
+    assert time.time() - t < 10.0
+    assert pl.info["n_seq"] >= 1
+
+
+@pytest.mark.parametrize("parent,seg_len,chunk", [
+    ([0], [5], 16),            # parent not < index
+    ([-1, 1], [5, 5], 16),     # parent not < index
+    ([-1, 0], [5, 0], 16),     # zero-length segment
+    ([-1], [5], 0),            # chunk < 1
+])
+def test_planner_rejects_malformed_input(parent, seg_len, chunk):
+    with pytest.raises(_lib.HartsError) as e:
+        Plan(np.array(parent), np.array(seg_len), chunk)
+    assert e.value.rc == -1
