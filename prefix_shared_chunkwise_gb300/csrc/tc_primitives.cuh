@@ -1,0 +1,178 @@
+// sm_103a building blocks written as inline PTX: tensor memory (TMEM) allocation,
+// tcgen05.mma (bf16 operands from shared memory, fp32 accumulators in TMEM),
+// completion tracking through mbarriers (every wait bounded), and TMEM <-> register
+// moves.  Operand tiles live in shared memory in the 128-byte-swizzled K-major layout:
+// rows of 64 bf16 (128 B) per "atom column", 8-row groups 1024 B apart, the 16-byte
+// chunk j of row r stored at chunk position j ^ (r % 8).
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace harts {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- shared-memory operand layout -----------------------------------------------------
+
+// Byte offset of element (row, col) in a K-major SW128 tile of `rows` rows whose K
+// extent is split into atoms of 64 columns (each atom: rows x 128 B, 1024-B aligned).
+__device__ __forceinline__ uint32_t sw128_offset(int rows, int row, int col) {
+    const int atom = col >> 6, c = col & 63;
+    return static_cast<uint32_t>(atom * rows * 128 + row * 128 +
+                                 ((((c >> 3) ^ (row & 7)) << 4) | ((c & 7) << 1)));
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);          // start address
+    d |= static_cast<uint64_t>(1) << 16;                         // leading offset (unused)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;                 // stride offset: 8 rows
+    d |= static_cast<uint64_t>(1) << 46;                         // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                         // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4)                                   // D format: f32
+         | (1u << 7)                                   // A format: bf16
+         | (1u << 10)                                  // B format: bf16
+         | (static_cast<uint32_t>(N >> 3) << 17)
+         | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---- TMEM allocation (one full warp executes these) ------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_addr(dst_smem)), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                 :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+// ---- MMA issue (one thread) -------------------------------------------------------------
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// D[M x N] (+)= A[M x K] * B[N x K]^T with both operands K-major SW128 tiles; K is a
+// multiple of 16, atoms of 64 columns placed `a_atom_bytes` / `b_atom_bytes` apart.
+__device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_atom_bytes,
+                                         uint32_t b_saddr, uint32_t b_atom_bytes, int K,
+                                         uint32_t idesc, bool accumulate) {
+    for (int kk = 0; kk < K / 16; ++kk) {
+        const uint32_t aoff = (kk >> 2) * a_atom_bytes + (kk & 3) * 32;
+        const uint32_t boff = (kk >> 2) * b_atom_bytes + (kk & 3) * 32;
+        mma_bf16(d_tmem, desc_sw128(a_saddr + aoff), desc_sw128(b_saddr + boff), idesc,
+                 (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+// Arrive on `bar` when every tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Make this thread's ordinary shared-memory writes visible to the tensor cores.
+__device__ __forceinline__ void fence_smem_to_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- mbarriers --------------------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(phase) : "memory");
+    return ok != 0;
+}
+
+// Wait for the given phase; gives up after ~`max_cycles` SM cycles and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase,
+                                          long long max_cycles = 4000000000LL) {
+    if (mbar_try(bar, phase)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try(bar, phase)) {
+        if (clock64() - t0 > max_cycles) return false;
+    }
+    return true;
+}
+
+// ---- TMEM <-> registers (warp-collective; warp w may touch lanes 32*(w%4)..+31) ---------
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
+    uint32_t *u = reinterpret_cast<uint32_t *>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]),
+          "=r"(u[13]), "=r"(u[14]), "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]),
+          "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]),
+          "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]),
+          "=r"(u[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&r)[32]) {
+    const uint32_t *u = reinterpret_cast<const uint32_t *>(r);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        :: "r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]),
+           "r"(u[6]), "r"(u[7]), "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]),
+           "r"(u[13]), "r"(u[14]), "r"(u[15]), "r"(u[16]), "r"(u[17]), "r"(u[18]), "r"(u[19]),
+           "r"(u[20]), "r"(u[21]), "r"(u[22]), "r"(u[23]), "r"(u[24]), "r"(u[25]), "r"(u[26]),
+           "r"(u[27]), "r"(u[28]), "r"(u[29]), "r"(u[30]), "r"(u[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Pack two floats to a bf16x2 word (lower address = first).
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Store 8 consecutive K-columns (col % 8 == 0) of one row into a SW128 tile (16 B).
+__device__ __forceinline__ void st_sw128_8(uint8_t *tile, int rows, int row, int col,
+                                           const float *v) {
+    uint4 w;
+    w.x = pack_bf16(v[0], v[1]); w.y = pack_bf16(v[2], v[3]);
+    w.z = pack_bf16(v[4], v[5]); w.w = pack_bf16(v[6], v[7]);
+    *reinterpret_cast<uint4 *>(tile + sw128_offset(rows, row, col)) = w;
+}
+
+}  // namespace tc
+}  // namespace harts

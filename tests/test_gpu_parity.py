@@ -123,3 +123,34 @@ def test_bf16_d128_forward_mild_decay():
     seg_len = rng.integers(1, 300, size=n).astype(np.int64)
     errs = _run(parent, seg_len, 64, 2, 128, "bf16", 6, backward=False, decay=0.02)
     _assert(errs, TOL["bf16"])
+
+
+def test_fwd16k_workload_forward_tc():
+    """The 8-tree, 16K-token forward workload at full size, all heads, tensor-core path."""
+    wl = WORKLOADS["fwd16k_bf16"]
+    parent, seg_len = make_tree("fwd16k_bf16")
+    errs = _run(parent, seg_len, wl.chunk, wl.H, wl.dk, "bf16", 1, backward=False,
+                kernel=_lib.HARTS_KERNEL_TC)
+    _assert(errs, TOL["bf16"])
+
+
+def test_tc_forward_matches_simt_forward():
+    """Both kernel families on identical inputs: the tensor-core forward stays within
+    bf16 rounding of the exact fp32 CUDA-core forward."""
+    rng = np.random.Generator(np.random.PCG64(12))
+    n = 16
+    parent = np.array([-1 if (i == 0 or rng.random() < 0.1) else int(rng.integers(0, i))
+                       for i in range(n)], np.int32)
+    seg_len = rng.integers(1, 260, size=n).astype(np.int64)
+    pl = Plan(parent, seg_len, 64).upload()
+    x = make_inputs(pl.info["C"], 4, 128, 128, "bf16", 11, device="cuda")
+    outs = []
+    for kern in (_lib.HARTS_KERNEL_SIMT, _lib.HARTS_KERNEL_TC):
+        fin = torch.empty((pl.info["n_seq"], 4, 128, 128), device="cuda")
+        o, _, fin, _ = kda_fwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], final_state=fin,
+                               kernel=kern)
+        outs.append((o.float().cpu().numpy(), fin.cpu().numpy()))
+    torch.cuda.synchronize()
+    assert pl.device_error() == 0
+    assert rel_l2(outs[1][0], outs[0][0]) < 5e-3
+    assert rel_l2(outs[1][1], outs[0][1]) < 5e-3
