@@ -162,8 +162,9 @@ typedef struct {
     float *final_state;      /* device [n_seq,H,dk,dv] fp32, nullable */
     const float *h0;         /* device [n_roots,H,dk,dv] fp32 root initial state, nullable
                                 (NULL = zero state) */
-    void *chunk_states;      /* device [n_chunks,H,dk,dv] in `dtype`, nullable: the state
-                                at the start of every chunk, saved for the backward pass */
+    void *chunk_states;      /* device [n_chunks,H,dv,dk] in `dtype`, nullable: the state
+                                at the start of every chunk, stored transposed (S^T), saved
+                                for the backward pass; chunk index = sequence base + chunk */
 } harts_kda_fwd_args;
 
 /* Bytes for chunk_states (n_chunks * H * dk * dv * sizeof(dtype)). */

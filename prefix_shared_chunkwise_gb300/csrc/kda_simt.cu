@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(256) kda_fwd_simt(FwdParams p, PlanDev pd, int
         if (p.chunk_states) {
             T *cs = static_cast<T *>(p.chunk_states) +
                     (static_cast<int64_t>(pd.seq_cbase[seq] + ci) * H + h) * D * D;
-            for (int i = tid; i < D * D; i += nth) st_out(cs, i, S[i]);
+            for (int i = tid; i < D * D; i += nth) st_out(cs, (i % D) * D + i / D, S[i]);
         }
         load_and_prep<D, BC, T>(p, pd, seq, h, rho, L, c0, Kp, Km, Qp, V, Km, bet, el, em, ekt,
                                 static_cast<const T *>(nullptr), nullptr);
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(256) kda_bwd_simt(BwdParams p, PlanDev pd, int
         {
             const T *cs = static_cast<const T *>(f.chunk_states) +
                           (static_cast<int64_t>(pd.seq_cbase[seq] + ci) * H + h) * D * D;
-            for (int i = tid; i < D * D; i += nth) S[i] = ld_in(cs, i);
+            for (int i = tid; i < D * D; i += nth) S[i] = ld_in(cs, (i % D) * D + i / D);
         }
         load_and_prep<D, BC, T>(f, pd, seq, h, rho, L, c0, Kp, Km, Qp, V, Gam, bet, el, em, ekt,
                                 dO_in, dO);

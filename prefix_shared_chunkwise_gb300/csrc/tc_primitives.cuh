@@ -176,3 +176,22 @@ __device__ __forceinline__ void st_sw128_8(uint8_t *tile, int rows, int row, int
 
 }  // namespace tc
 }  // namespace harts
+
+namespace harts {
+namespace tc {
+
+// ---- asynchronous global -> shared copies (16 B; zero-filled when src_bytes == 0) -------
+
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 :: "r"(smem_addr(dst_smem)), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
+                 :: "r"(smem_addr(dst_smem)), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+}  // namespace tc
+}  // namespace harts
