@@ -162,12 +162,14 @@ typedef struct {
     float *final_state;      /* device [n_seq,H,dk,dv] fp32, nullable */
     const float *h0;         /* device [n_roots,H,dk,dv] fp32 root initial state, nullable
                                 (NULL = zero state) */
-    void *chunk_states;      /* device [n_chunks,H,dv,dk] in `dtype`, nullable: the state
-                                at the start of every chunk, stored transposed (S^T), saved
-                                for the backward pass; chunk index = sequence base + chunk */
+    void *chunk_states;      /* device, nullable: per (chunk, head) a record of dk*dv + B*B
+                                elements in `dtype`: the state at the chunk start stored
+                                transposed (S^T, [dv][dk]) followed by the chunk's
+                                T = (I + diag(beta) A)^-1 ([B][B]); saved for the backward
+                                pass; records ordered [chunk][head], chunks by sequence */
 } harts_kda_fwd_args;
 
-/* Bytes for chunk_states (n_chunks * H * dk * dv * sizeof(dtype)). */
+/* Bytes for chunk_states (n_chunks * H * (dk*dv + B*B) * sizeof(dtype)). */
 size_t harts_kda_chunk_state_bytes(const harts_plan *plan, int32_t H, int32_t dk, int32_t dv,
                                    int32_t dtype);
 

@@ -15,8 +15,10 @@ cudaError_t bwd_finish(int dtype, const BwdParams &p, const PlanDev &pd, cudaStr
 bool tc_supported(bool backward, int dtype, int D, int BC);
 cudaError_t tc_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, int32_t n_items,
                          int32_t max_chunks, cudaStream_t st);
-cudaError_t tc_bwd_round(const BwdParams &p, const PlanDev &pd, int32_t base, int32_t n_items,
-                         int32_t max_chunks, cudaStream_t st);
+cudaError_t tc_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t base,
+                               int32_t n_items, cudaStream_t st);
+cudaError_t tc_bwd_grad(const BwdParams &p, const PlanDev &pd, int32_t chunk_begin,
+                        int32_t n_items, cudaStream_t st);
 
 namespace {
 
@@ -65,14 +67,16 @@ FwdParams make_fwd(const harts_kda_fwd_args *a) {
     return p;
 }
 
-struct BwdWs { size_t ds_init, rep_grad, total; };
-BwdWs bwd_ws(const harts_plan *P, int32_t H, int32_t D) {
+// Backward workspace: per-sequence initial-state gradients (fp32), per-replay-occurrence
+// gradients (fp32), and the carried state gradient at every chunk end (bf16, tensor-core
+// path only).
+struct BwdWs { size_t ds_init, rep_grad, dchunk, total; };
+BwdWs bwd_ws(const harts_plan *P, int32_t H, int32_t D, bool tc) {
     BwdWs w{};
     w.ds_init = 0;
-    size_t a = align_up(sizeof(float) * size_t(P->info.n_seq) * H * D * D);
-    w.rep_grad = a;
-    size_t b = align_up(sizeof(float) * size_t(P->info.R) * H * (3 * D + 1));
-    w.total = a + b;
+    w.rep_grad = align_up(sizeof(float) * size_t(P->info.n_seq) * H * D * D);
+    w.dchunk = w.rep_grad + align_up(sizeof(float) * size_t(P->info.R) * H * (3 * D + 1));
+    w.total = w.dchunk + (tc ? align_up(size_t(2) * size_t(P->info.n_chunks) * H * D * D) : 0);
     return w;
 }
 
@@ -107,6 +111,7 @@ int harts_plan_upload(harts_plan *P, void *dev_buf, size_t bytes, harts_stream_t
     v.root_cptr = w + I.off_root_cptr; v.root_cons = w + I.off_root_cons;
     v.replay_idx = w + I.off_replay_idx; v.fold_rows = w + I.off_fold_rows;
     v.fold_ptr = w + I.off_fold_ptr; v.fold_occ = w + I.off_fold_occ;
+    v.chunk_seq = w + I.off_chunk_seq;
     v.n_rounds = P->info.n_rounds; v.n_seq = P->info.n_seq; v.n_states = P->info.n_states;
     v.n_roots = P->info.n_roots; v.n_fold = P->info.n_fold_rows; v.chunk = P->info.chunk;
     v.R = P->info.R; v.n_chunks = P->info.n_chunks;
@@ -137,12 +142,13 @@ int harts_plan_device_error(harts_plan *P, harts_stream_t stream, int32_t *code)
 size_t harts_kda_chunk_state_bytes(const harts_plan *P, int32_t H, int32_t dk, int32_t dv,
                                    int32_t dtype) {
     if (!P || H < 1 || dk < 1 || dv < 1) return 0;
-    return size_t(P->info.n_chunks) * H * dk * dv * dtype_size(dtype);
+    const size_t B = static_cast<size_t>(P->info.chunk);
+    return size_t(P->info.n_chunks) * H * (size_t(dk) * dv + B * B) * dtype_size(dtype);
 }
 
 size_t harts_kda_bwd_workspace_bytes(const harts_plan *P, int32_t H, int32_t dk, int32_t dv) {
     if (!P || H < 1 || dk < 1 || dk != dv) return 0;
-    return bwd_ws(P, H, dk).total;
+    return bwd_ws(P, H, dk, true).total;
 }
 
 int harts_kda_fwd(const harts_plan *P, const harts_kda_fwd_args *a, harts_stream_t stream) {
@@ -173,11 +179,11 @@ int harts_kda_bwd(const harts_plan *P, const harts_kda_bwd_args *a, harts_stream
     if (!a->d_o || !a->dq || !a->dk || !a->dv || !a->dg || !a->dbeta) { set_error("NULL gradient pointer"); return HARTS_EINVAL; }
     if (!a->fwd.chunk_states) { set_error("chunk_states from the forward pass are required"); return HARTS_EINVAL; }
     const int D = a->fwd.dk, H = a->fwd.H, BC = P->info.chunk;
-    const BwdWs ws = bwd_ws(P, H, D);
-    if (!a->workspace || a->workspace_bytes < ws.total) { set_error("workspace too small"); return HARTS_ESMALLBUF; }
-    if (reinterpret_cast<uintptr_t>(a->workspace) % 256) { set_error("workspace must be 256-B aligned"); return HARTS_EINVAL; }
     const int fam = pick(&a->fwd, BC, true);
     if (fam < 0) { set_error("no backward kernel for this dk/dv/chunk/dtype"); return HARTS_EUNSUPPORTED; }
+    const BwdWs ws = bwd_ws(P, H, D, fam == 1);
+    if (!a->workspace || a->workspace_bytes < ws.total) { set_error("workspace too small"); return HARTS_ESMALLBUF; }
+    if (reinterpret_cast<uintptr_t>(a->workspace) % 256) { set_error("workspace must be 256-B aligned"); return HARTS_EINVAL; }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     BwdParams p{};
     p.f = make_fwd(&a->fwd);
@@ -186,13 +192,21 @@ int harts_kda_bwd(const harts_plan *P, const harts_kda_bwd_args *a, harts_stream
     char *w = static_cast<char *>(a->workspace);
     p.ds_init = reinterpret_cast<float *>(w + ws.ds_init);
     p.rep_grad = reinterpret_cast<float *>(w + ws.rep_grad);
+    p.dchunk = fam == 1 ? static_cast<void *>(w + ws.dchunk) : nullptr;
     for (int32_t r = P->info.n_rounds - 1; r >= 0; --r) {
         const int32_t base = P->round_seq_ptr[r];
         const int32_t n = (P->round_seq_ptr[r + 1] - base) * H;
         if (n == 0) continue;
-        cudaError_t e = fam == 1 ? tc_bwd_round(p, P->view, base, n, P->info.max_seq_chunks, st)
+        cudaError_t e = fam == 1 ? tc_bwd_state_round(p, P->view, base, n, st)
                                  : simt_bwd_round(a->fwd.dtype, BC, p, P->view, base, n, st);
         if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    }
+    if (fam == 1) {
+        // every chunk's gradients at once: they only depend on saved per-chunk states
+        const int64_t items = P->info.n_chunks * H;
+        if (items > 0x7fffffff) { set_error("too many (chunk, head) items"); return HARTS_EOVERFLOW; }
+        cudaError_t e = tc_bwd_grad(p, P->view, 0, static_cast<int32_t>(items), st);
+        if (e != cudaSuccess) return cuda_fail(e, "backward gradient launch");
     }
     cudaError_t e = bwd_finish(a->fwd.dtype, p, P->view, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward reductions");

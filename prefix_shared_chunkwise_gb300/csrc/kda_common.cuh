@@ -37,6 +37,7 @@ struct BwdParams {
     float *dh0;
     float *ds_init;          // [n_seq, H, D, D] gradient w.r.t. each sequence's initial state
     float *rep_grad;         // [R, H, 3*D+1]: dk, dv, dg, dbeta of every replay occurrence
+    void *dchunk;            // [n_chunks, H, D, D] bf16: dL/dS^T at every chunk end (tensor-core path)
 };
 
 __device__ __forceinline__ float ld_in(const float *p, int64_t i) { return p[i]; }

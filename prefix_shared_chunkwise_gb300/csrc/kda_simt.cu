@@ -143,15 +143,20 @@ __global__ void __launch_bounds__(256) kda_fwd_simt(FwdParams p, PlanDev pd, int
     for (int32_t ci = 0; ci < nch; ++ci) {
         const int32_t c0 = ci * BC;
         __syncthreads();
-        if (p.chunk_states) {
-            T *cs = static_cast<T *>(p.chunk_states) +
-                    (static_cast<int64_t>(pd.seq_cbase[seq] + ci) * H + h) * D * D;
-            for (int i = tid; i < D * D; i += nth) st_out(cs, (i % D) * D + i / D, S[i]);
-        }
+        T *rec = p.chunk_states ? static_cast<T *>(p.chunk_states) +
+                     (static_cast<int64_t>(pd.seq_cbase[seq] + ci) * H + h) * (D * D + BC * BC)
+                                : nullptr;
+        if (rec)
+            for (int i = tid; i < D * D; i += nth) st_out(rec, (i % D) * D + i / D, S[i]);
         load_and_prep<D, BC, T>(p, pd, seq, h, rho, L, c0, Kp, Km, Qp, V, Km, bet, el, em, ekt,
                                 static_cast<const T *>(nullptr), nullptr);
         // load_and_prep used Km as the Gamma scratch; it is overwritten by Km itself.
         build_T<D, BC>(Kp, Km, bet, A);
+        if (rec)
+            for (int i = tid; i < BC * BC; i += nth) {
+                const int t = i / BC, s = i % BC;
+                st_out(rec + D * D, i, s < t ? A[s * BC + t] : (s == t ? 1.f : 0.f));
+            }
         // Y = V - Kd S  (in place)
         for (int i = tid; i < BC * D; i += nth) {
             const int t = i / D, j = i % D;
@@ -267,7 +272,7 @@ __global__ void __launch_bounds__(256) kda_bwd_simt(BwdParams p, PlanDev pd, int
         }
         {
             const T *cs = static_cast<const T *>(f.chunk_states) +
-                          (static_cast<int64_t>(pd.seq_cbase[seq] + ci) * H + h) * D * D;
+                          (static_cast<int64_t>(pd.seq_cbase[seq] + ci) * H + h) * (D * D + BC * BC);
             for (int i = tid; i < D * D; i += nth) S[i] = ld_in(cs, (i % D) * D + i / D);
         }
         load_and_prep<D, BC, T>(f, pd, seq, h, rho, L, c0, Kp, Km, Qp, V, Gam, bet, el, em, ekt,

@@ -22,6 +22,8 @@ namespace harts {
 namespace {
 
 constexpr int D = 128, BC = 64, NT = 256;
+// Saved per (chunk, head): S^T [dv][dk] then T [t][s], bf16.
+constexpr int64_t kRecBytes = (D * D + BC * BC) * 2;
 
 // Shared-memory layout (bytes from a 1024-aligned base).  Regions are reused once the
 // MMA that reads them has completed.
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
     // Copy the bf16 S^T tile (SW128) to a saved chunk state, [dv][dk] row-major, 16 B per thread.
     auto save_chunk_state = [&](int32_t chunk_index) {
         if (!cst) return;
-        uint8_t *dst = cst + (static_cast<int64_t>(chunk_index) * H + h) * D * D * 2;
+        uint8_t *dst = cst + (static_cast<int64_t>(chunk_index) * H + h) * kRecBytes;
         for (int e = tid; e < 128 * 16; e += NT) {
             const int r = e >> 4, piece = e & 15;
             *reinterpret_cast<uint4 *>(dst + r * 256 + piece * 16) =
@@ -316,6 +318,16 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
             for (int j = 0; j < 16; ++j) r[j] = (s0 + j <= t) ? Tfp[fidx(t, s0 + j)] : 0.f;
             tc::st_sw128_8(sm + Tm, 64, t, s0, r);
             tc::st_sw128_8(sm + Tm, 64, t, s0 + 8, r + 8);
+            if (cst) {
+                uint8_t *dst = cst + (static_cast<int64_t>(cbase + ci) * H + h) * kRecBytes + D * D * 2;
+                uint4 w0, w1;
+                w0.x = tc::pack_bf16(r[0], r[1]); w0.y = tc::pack_bf16(r[2], r[3]);
+                w0.z = tc::pack_bf16(r[4], r[5]); w0.w = tc::pack_bf16(r[6], r[7]);
+                w1.x = tc::pack_bf16(r[8], r[9]); w1.y = tc::pack_bf16(r[10], r[11]);
+                w1.z = tc::pack_bf16(r[12], r[13]); w1.w = tc::pack_bf16(r[14], r[15]);
+                *reinterpret_cast<uint4 *>(dst + t * 128 + s0 * 2) = w0;
+                *reinterpret_cast<uint4 *>(dst + t * 128 + s0 * 2 + 16) = w1;
+            }
         }
         sync_for_mma();
         if (tid == 0) {
@@ -411,10 +423,731 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
     if (warp == 0) tc::tmem_dealloc(tm, 512);
 }
 
+// ======================================================================================
+// Backward, tensor-core path.  Two kernels:
+//  kda_bwd_state_tc : per (sequence, head), chunks in reverse; carries dS (as dS^T in
+//                     TMEM) and saves the carry at every chunk end.  Per chunk:
+//                       dU^T = dO^T P + (dS'^T e^{Gamma_L-m}) Km^T     (= (P^T dO + Kt dS')^T)
+//                       Z^T  = dU^T T                                   (Z = T^T dU)
+//                       dS^T <- dS'^T diag(e^{Gamma_L}) + dO^T Qd - (beta Z)^T Kd
+//  kda_bwd_grad_tc  : per (chunk, head), all chunks independent; recomputes the chunk
+//                     from its saved S and dS' and forms every input gradient.
+// T comes from the forward pass's saved chunk record.
+// ======================================================================================
+
+// 16-byte piece p of row t of a [64 rows][128 cols] SW128 tile.
+__device__ __forceinline__ uint32_t piece64(int t, int p) {
+    return static_cast<uint32_t>((p >> 3) * 8192 + t * 128 + (((p & 7) ^ (t & 7)) << 4));
+}
+// 16-byte piece p of row r of a [128 rows][128 cols] SW128 tile.
+__device__ __forceinline__ uint32_t piece128(int r, int p) {
+    return static_cast<uint32_t>((p >> 3) * 16384 + r * 128 + (((p & 7) ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ float sw_val(const uint8_t *tile, int rows, int r, int c) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + tc::sw128_offset(rows, r, c)));
+}
+
+// Stage one chunk's rows of a token-major [C,H,128] bf16 tensor into a SW128 [64][128]
+// tile (rows past the sequence end and, if own_only, replay rows read as zero).
+__device__ void stage_rows(uint8_t *tile, const void *src_, const PlanDev &pd, int32_t seq,
+                           int32_t h, int H, int32_t rho, int32_t L, int32_t c0, bool own_only) {
+    const uint8_t *src = static_cast<const uint8_t *>(src_);
+    for (int e = threadIdx.x; e < 64 * 16; e += NT) {
+        const int t = e >> 4, p = e & 15;
+        int64_t row = local_row(pd, seq, rho, L, c0 + t);
+        if (own_only && c0 + t < rho) row = -1;
+        const uint8_t *s = row >= 0 ? src + ((row * H + h) * D * 2 + p * 16) : src;
+        tc::cp_async16(tile + piece64(t, p), s, row >= 0 ? 16u : 0u);
+    }
+}
+
+__device__ void stage_beta(uint8_t *words, int *par, const void *beta, const PlanDev &pd,
+                           int32_t seq, int32_t h, int H, int32_t rho, int32_t L, int32_t c0) {
+    for (int t = threadIdx.x; t < 64; t += NT) {
+        const int64_t row = local_row(pd, seq, rho, L, c0 + t);
+        const int64_t idx = row >= 0 ? row * H + h : 0;
+        const uint8_t *s = static_cast<const uint8_t *>(beta) + (idx & ~int64_t(1)) * 2;
+        tc::cp_async4(words + t * 4, s, row >= 0 ? 4u : 0u);
+        par[t] = static_cast<int>(idx & 1);
+    }
+}
+
+__device__ __forceinline__ float beta_of(const uint8_t *words, const int *par, int t) {
+    const uint32_t w = reinterpret_cast<const uint32_t *>(words)[t];
+    const uint16_t hb = par[t] ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w & 0xFFFF);
+    return __bfloat162float(__ushort_as_bfloat16(hb));
+}
+
+// Cumulative decay pass 1 for thread (c, half): partial sums and the reference row.
+__device__ __forceinline__ void gamma_pass1(const uint8_t *G, int c, int half, int mid, float *vt0,
+                                            float *vt1, float *vm) {
+    float s = 0.f, mref = 0.f;
+#pragma unroll 8
+    for (int t = half * 32; t < half * 32 + 32; ++t) {
+        s += sw_val(G, 64, t, c);
+        if (t == mid) mref = s;
+    }
+    if (half == 0) { vt0[c] = s; vm[c] = mref; } else vt1[c] = s;
+}
+
+namespace bws_sm {
+constexpr uint32_t RawQ = 0, RawK = 16384, RawG = 32768, dOm = 49152;
+constexpr uint32_t Qpm = 65536, Km = 81920, Kdm = 98304, Qdm = 114688;
+constexpr uint32_t Pm = 131072, Tm = 139264, dSTs = 147456, dUTs = 180224;
+constexpr uint32_t SBeta = 196608, SBpar = SBeta + 256, Vec = SBpar + 256;
+constexpr uint32_t vBeta = Vec, vEl = vBeta + 256, vEkt = vEl + 512, vM = vEkt + 512,
+                   vT0 = vM + 512, vT1 = vT0 + 512, vEnd = vT1 + 512;
+constexpr uint32_t bytes = vEnd + 1024;
+}  // namespace bws_sm
+
+__global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev pd, int32_t round_base) {
+    using namespace bws_sm;
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
+    __shared__ uint64_t bars[4];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_fail;
+    float *vbeta = reinterpret_cast<float *>(sm + vBeta), *vel = reinterpret_cast<float *>(sm + vEl),
+          *vekt = reinterpret_cast<float *>(sm + vEkt), *vm = reinterpret_cast<float *>(sm + vM),
+          *vt0 = reinterpret_cast<float *>(sm + vT0), *vt1 = reinterpret_cast<float *>(sm + vT1);
+    int *spar = reinterpret_cast<int *>(sm + SBpar);
+    const FwdParams &f = p.f;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, ch = warp >> 2;
+    const int H = f.H;
+    const int32_t h = blockIdx.x % H;
+    const int32_t seq = pd.round_order[round_base + blockIdx.x / H];
+    const int32_t rho = pd.seq_rho[seq], L = rho + pd.seq_nown[seq];
+    const int32_t nch = (L + BC - 1) / BC;
+    const int32_t src = pd.seq_src[seq], cbase = pd.seq_cbase[seq];
+    const uint8_t *rec0 = static_cast<const uint8_t *>(f.chunk_states);
+    uint8_t *dch = static_cast<uint8_t *>(p.dchunk);
+
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) tc::mbar_init(&bars[i], 1);
+        s_fail = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = s_tmem;
+    const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+    const uint32_t tST = tm, tP = tm + 128, tUT = tm + 192, tZT = tm + 256;
+    const int jv = lg * 32 + lane;
+
+    // carry <- d_final (S layout [dk][dv] in memory; TMEM holds dS^T)
+    for (int hf = 0; hf < 2; ++hf) {
+        float r[32];
+        const int cb = ch * 64 + hf * 32;
+        const float *df = p.d_final ? p.d_final + (static_cast<int64_t>(seq) * H + h) * D * D : nullptr;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = df ? df[(cb + j) * D + jv] : 0.f;
+        tc::tmem_st32(tST + lane_off + cb, r);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    const int32_t sp_begin = pd.seq_sptr[seq];
+    int32_t sp = pd.seq_sptr[seq + 1] - 1;
+    const int c = tid & 127, half = tid >> 7;
+    for (int32_t ci = nch - 1; ci >= 0; --ci) {
+        const uint32_t ph = (nch - 1 - ci) & 1;
+        const int32_t c0 = ci * BC, pend = c0 + BC, g = cbase + ci;
+        const int nv = min(BC, L - c0);
+        const int mid = (nv - 1) / 2;
+        // ---- stage inputs and the forward's T ------------------------------------------
+        stage_rows(sm + RawQ, f.q, pd, seq, h, H, rho, L, c0, false);
+        stage_rows(sm + RawK, f.k, pd, seq, h, H, rho, L, c0, false);
+        stage_rows(sm + RawG, f.g, pd, seq, h, H, rho, L, c0, false);
+        stage_rows(sm + dOm, p.d_o, pd, seq, h, H, rho, L, c0, true);
+        stage_beta(sm + SBeta, spar, f.beta, pd, seq, h, H, rho, L, c0);
+        {
+            const uint8_t *rt = rec0 + (static_cast<int64_t>(g) * H + h) * kRecBytes + D * D * 2;
+            for (int e = tid; e < 64 * 8; e += NT) {
+                const int t = e >> 3, pc = e & 7;
+                tc::cp_async16(sm + Tm + t * 128 + ((pc ^ (t & 7)) << 4), rt + t * 128 + pc * 16, 16u);
+            }
+        }
+        tc::cp_async_commit();
+        // ---- consumers of the boundary state at this chunk's end add their gradients ----
+        if (sp >= sp_begin && pd.state_lpos[sp] == pend) {
+            const int32_t cb_ = pd.state_cptr[sp], ce_ = pd.state_cptr[sp + 1];
+            for (int hf = 0; hf < 2; ++hf) {
+                float r[32];
+                const int cb = ch * 64 + hf * 32;
+                tc::tmem_ld32(tST + lane_off + cb, r);
+                for (int32_t cc = cb_; cc < ce_; ++cc) {
+                    const float *di = p.ds_init + (static_cast<int64_t>(pd.state_cons[cc]) * H + h) * D * D;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] += di[(cb + j) * D + jv];
+                }
+                tc::tmem_st32(tST + lane_off + cb, r);
+            }
+            --sp;
+        }
+        // ---- save the carry dS' (bf16 dS^T) for the gradient kernel ----------------------
+        for (int hf = 0; hf < 2; ++hf) {
+            float r[32];
+            const int cb = ch * 64 + hf * 32;
+            tc::tmem_ld32(tST + lane_off + cb, r);
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + dSTs, 128, jv, cb + j, r + j);
+        }
+        tc::cp_async_wait_all();
+        __syncthreads();
+        {
+            uint8_t *dst = dch + (static_cast<int64_t>(g) * H + h) * D * D * 2;
+            for (int e = tid; e < 128 * 16; e += NT) {
+                const int r = e >> 4, pc = e & 15;
+                *reinterpret_cast<uint4 *>(dst + r * 256 + pc * 16) =
+                    *reinterpret_cast<const uint4 *>(sm + dSTs + piece128(r, pc));
+            }
+        }
+        // ---- prep ------------------------------------------------------------------------
+        gamma_pass1(sm + RawG, c, half, mid, vt0, vt1, vm);
+        if (tid < 64) vbeta[tid] = beta_of(sm + SBeta, spar, tid);
+        __syncthreads();
+        {
+            const float m = vm[c], gl = vt0[c] + vt1[c];
+            float gam = half ? vt0[c] : 0.f;
+            if (-m > kMaxExpArg || m - gl > kMaxExpArg) dev_error(pd, kDevErrDecayRange, seq, c0);
+            const float em = __expf(m);
+            if (half == 0) { vel[c] = __expf(gl); vekt[c] = __expf(gl - m); }
+            for (int t = half * 32; t < half * 32 + 32; ++t) {
+                const float kk = sw_val(sm + RawK, 64, t, c), qq = sw_val(sm + RawQ, 64, t, c) * f.scale;
+                gam += sw_val(sm + RawG, 64, t, c);
+                const float e1 = __expf(gam - m), e2 = __expf(m - gam);
+                st_bf16(sm + Qpm, 64, t, c, qq * e1);
+                st_bf16(sm + Km, 64, t, c, kk * e2);
+                st_bf16(sm + Kdm, 64, t, c, kk * e1 * em);
+                st_bf16(sm + Qdm, 64, t, c, qq * e1 * em);
+            }
+        }
+        sync_for_mma();
+        if (tid == 0) {
+            tc::mma_tile(tP, tc::smem_addr(sm + Qpm), 8192, tc::smem_addr(sm + Km), 8192, 128,
+                         tc::idesc_bf16(64, 64), false);
+            tc::mma_commit(&bars[0]);
+        }
+        // carry: bf16 copy scaled by e^{Gamma_L - m} per key channel; TMEM scaled by e^{Gamma_L}
+        for (int hf = 0; hf < 2; ++hf) {
+            float r[32];
+            const int cb = ch * 64 + hf * 32;
+            tc::tmem_ld32(tST + lane_off + cb, r);
+            float w[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) { w[j] = r[j] * vekt[cb + j]; r[j] *= vel[cb + j]; }
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + dSTs, 128, jv, cb + j, w + j);
+            tc::tmem_st32(tST + lane_off + cb, r);
+        }
+        if (!wait_all(&bars[0], ph, &s_fail)) break;
+        // ---- P (M = 64 layout: warp lg holds rows 16 lg .. 16 lg + 15 in lanes 0-15) ------
+        {
+            float r[32];
+            tc::tmem_ld32(tP + lane_off + ch * 32, r);
+            if (lane < 16) {
+                const int t = lg * 16 + lane;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = (ch * 32 + j <= t) ? r[j] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + Pm, 64, t, ch * 32 + j, r + j);
+            }
+        }
+        sync_for_mma();
+        if (tid == 0) {
+            tc::mma_op(tUT, tc::Opnd{tc::smem_addr(sm + dOm), 8192, true},
+                       tc::Opnd{tc::smem_addr(sm + Pm), 8192, true}, 128, 64, 64, false);
+            tc::mma_op(tUT, tc::Opnd{tc::smem_addr(sm + dSTs), 16384, false},
+                       tc::Opnd{tc::smem_addr(sm + Km), 8192, false}, 128, 64, 128, true);
+            tc::mma_commit(&bars[1]);
+        }
+        if (!wait_all(&bars[1], ph, &s_fail)) break;
+        {
+            float r[32];
+            tc::tmem_ld32(tUT + lane_off + ch * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + dUTs, 128, jv, ch * 32 + j, r + j);
+        }
+        sync_for_mma();
+        if (tid == 0) {
+            tc::mma_op(tZT, tc::Opnd{tc::smem_addr(sm + dUTs), 16384, false},
+                       tc::Opnd{tc::smem_addr(sm + Tm), 8192, true}, 128, 64, 64, false);
+            tc::mma_commit(&bars[2]);
+        }
+        if (!wait_all(&bars[2], ph, &s_fail)) break;
+        {
+            float r[32];
+            tc::tmem_ld32(tZT + lane_off + ch * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] *= -vbeta[ch * 32 + j];
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + dUTs, 128, jv, ch * 32 + j, r + j);
+        }
+        sync_for_mma();
+        if (tid == 0) {
+            tc::mma_op(tST, tc::Opnd{tc::smem_addr(sm + dOm), 8192, true},
+                       tc::Opnd{tc::smem_addr(sm + Qdm), 8192, true}, 128, 128, 64, true);
+            tc::mma_op(tST, tc::Opnd{tc::smem_addr(sm + dUTs), 16384, false},
+                       tc::Opnd{tc::smem_addr(sm + Kdm), 8192, true}, 128, 128, 64, true);
+            tc::mma_commit(&bars[3]);
+        }
+        if (!wait_all(&bars[3], ph, &s_fail)) break;
+    }
+    tc::cp_async_wait_all();
+    if (!s_fail && (src >= 0 || p.dh0)) {
+        float *dst = p.ds_init + (static_cast<int64_t>(seq) * H + h) * D * D;
+        for (int hf = 0; hf < 2; ++hf) {
+            float r[32];
+            const int cb = ch * 64 + hf * 32;
+            tc::tmem_ld32(tST + lane_off + cb, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dst[(cb + j) * D + jv] = r[j];
+        }
+    }
+    if (s_fail) {
+        dev_error(pd, kDevErrTimeout, seq, h);
+        for (int i = 0; i < 4; ++i) tc::mbar_wait(&bars[i], 0, 100000000LL);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tm, 512);
+}
+
+namespace bwg_sm {
+constexpr uint32_t SemT = 0, dSekT = 32768, dOm = 65536, KQp = 81920, Km = 114688, Tm = 131072;
+constexpr uint32_t RV = 139264, RQ = 155648, RK = 172032, RG = 188416, PmS = 204800, TBm = 212992;
+constexpr uint32_t SBeta = 221184, SBpar = SBeta + 256, Vec = SBpar + 256;
+// fp32 vectors
+constexpr uint32_t vBeta = Vec, vM = vBeta + 256, vEm = vM + 512, vEkt = vEm + 512, vEl = vEkt + 512,
+                   vT0 = vEl + 512, vT1 = vT0 + 512, vDel = vT1 + 512, vDgl = vDel + 1024,
+                   vTot = vDgl + 1024, rZY = vTot + 512, rMA = rZY + 1024, vEnd = rMA + 512;
+constexpr uint32_t bytes = vEnd + 1024;
+}  // namespace bwg_sm
+
+// Warp-reduce 32 per-lane values (one per column t) and write the warp sums.
+__device__ __forceinline__ void warp_col_sums(float (&x)[32], float *out) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        float v = x[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        x[j] = v;
+    }
+    if ((threadIdx.x & 31) == 0)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) out[j] = x[j];
+}
+
+__global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd, int32_t chunk_begin) {
+    using namespace bwg_sm;
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
+    __shared__ uint64_t bars[6];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_fail;
+    float *vbeta = reinterpret_cast<float *>(sm + vBeta), *vm = reinterpret_cast<float *>(sm + vM),
+          *vem = reinterpret_cast<float *>(sm + vEm), *vekt = reinterpret_cast<float *>(sm + vEkt),
+          *vel = reinterpret_cast<float *>(sm + vEl), *vt0 = reinterpret_cast<float *>(sm + vT0),
+          *vt1 = reinterpret_cast<float *>(sm + vT1), *vdel = reinterpret_cast<float *>(sm + vDel),
+          *vdgl = reinterpret_cast<float *>(sm + vDgl), *vtot = reinterpret_cast<float *>(sm + vTot),
+          *rzy = reinterpret_cast<float *>(sm + rZY), *rma = reinterpret_cast<float *>(sm + rMA);
+    int *spar = reinterpret_cast<int *>(sm + SBpar);
+    const FwdParams &f = p.f;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, ch = warp >> 2;
+    const int H = f.H;
+    const int32_t h = blockIdx.x % H;
+    const int32_t g = chunk_begin + blockIdx.x / H;
+    const int32_t seq = pd.chunk_seq[g];
+    const int32_t ci = g - pd.seq_cbase[seq];
+    const int32_t rho = pd.seq_rho[seq], L = rho + pd.seq_nown[seq];
+    const int32_t c0 = ci * BC;
+    const int nv = min(BC, L - c0), mid = (nv - 1) / 2;
+    const int32_t row0 = pd.seq_row0[seq], rptr = pd.seq_rptr[seq];
+    const uint8_t *rec = static_cast<const uint8_t *>(f.chunk_states) + (static_cast<int64_t>(g) * H + h) * kRecBytes;
+    const uint8_t *dcs = static_cast<const uint8_t *>(p.dchunk) + (static_cast<int64_t>(g) * H + h) * D * D * 2;
+    __nv_bfloat16 *gdq = static_cast<__nv_bfloat16 *>(p.dq), *gdk = static_cast<__nv_bfloat16 *>(p.dk),
+                  *gdv = static_cast<__nv_bfloat16 *>(p.dv), *gdg = static_cast<__nv_bfloat16 *>(p.dg),
+                  *gdb = static_cast<__nv_bfloat16 *>(p.dbeta);
+    const int W = 3 * D + 1;
+
+    // ---- stage everything the chunk needs ------------------------------------------------
+    for (int e = tid; e < 128 * 16; e += NT) {
+        const int r = e >> 4, pc = e & 15;
+        tc::cp_async16(sm + SemT + piece128(r, pc), rec + r * 256 + pc * 16, 16u);
+        tc::cp_async16(sm + dSekT + piece128(r, pc), dcs + r * 256 + pc * 16, 16u);
+    }
+    for (int e = tid; e < 64 * 8; e += NT) {
+        const int t = e >> 3, pc = e & 7;
+        tc::cp_async16(sm + Tm + t * 128 + ((pc ^ (t & 7)) << 4), rec + D * D * 2 + t * 128 + pc * 16, 16u);
+    }
+    stage_rows(sm + RQ, f.q, pd, seq, h, H, rho, L, c0, false);
+    stage_rows(sm + RK, f.k, pd, seq, h, H, rho, L, c0, false);
+    stage_rows(sm + RV, f.v, pd, seq, h, H, rho, L, c0, false);
+    stage_rows(sm + RG, f.g, pd, seq, h, H, rho, L, c0, false);
+    stage_rows(sm + dOm, p.d_o, pd, seq, h, H, rho, L, c0, true);
+    stage_beta(sm + SBeta, spar, f.beta, pd, seq, h, H, rho, L, c0);
+    tc::cp_async_commit();
+    if (tid == 0) {
+        for (int i = 0; i < 6; ++i) tc::mbar_init(&bars[i], 1);
+        s_fail = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
+    tc::cp_async_wait_all();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = s_tmem;
+    const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+    const uint32_t tAP = tm, tGam = tm + 64, tXm = tm + 128, tXq = tm + 192, tP1 = tm + 256,
+                   tP2 = tm + 320, tS1 = tm + 384, tS2 = tm + 448;
+    const int jv = lg * 32 + lane;
+    const int c = tid & 127, half = tid >> 7;
+
+    // ---- d(e^{Gamma_L}) part from the state: d_el = sum_dv S . dS' (before scaling) ------
+    {
+        float acc = 0.f;
+        for (int r = half * 64; r < half * 64 + 64; ++r)
+            acc += sw_val(sm + SemT, 128, r, c) * sw_val(sm + dSekT, 128, r, c);
+        vdel[half * 128 + c] = acc;
+    }
+    // ---- prep: Gamma (kept in TMEM, lane = key channel), Kp, Qp, Km --------------------
+    gamma_pass1(sm + RG, c, half, mid, vt0, vt1, vm);
+    if (tid < 64) vbeta[tid] = beta_of(sm + SBeta, spar, tid);
+    __syncthreads();
+    {
+        const float m = vm[c], gl = vt0[c] + vt1[c];
+        float gam = half ? vt0[c] : 0.f;
+        if (-m > kMaxExpArg || m - gl > kMaxExpArg) dev_error(pd, kDevErrDecayRange, seq, c0);
+        if (half == 0) { vem[c] = __expf(m); vekt[c] = __expf(gl - m); vel[c] = __expf(gl); }
+        float gv[32];
+#pragma unroll 4
+        for (int u = 0; u < 32; ++u) {
+            const int t = half * 32 + u;
+            const float kk = sw_val(sm + RK, 64, t, c), qq = sw_val(sm + RQ, 64, t, c) * f.scale;
+            gam += sw_val(sm + RG, 64, t, c);
+            gv[u] = gam;
+            const float e1 = __expf(gam - m), e2 = __expf(m - gam);
+            st_bf16(sm + KQp, 128, t, c, kk * e1);
+            st_bf16(sm + KQp, 128, 64 + t, c, qq * e1);
+            st_bf16(sm + Km, 64, t, c, kk * e2);
+        }
+        tc::tmem_st32(tGam + lane_off + half * 32, gv);   // thread (c, half) sits in lane c
+    }
+    __syncthreads();
+    // S^T columns * e^{m}, dS'^T columns * e^{Gamma_L - m}, T columns * beta
+    for (int e = tid; e < 128 * 16; e += NT) {
+        const int r = e >> 4, pc = e & 15;
+        for (int which = 0; which < 2; ++which) {
+            uint8_t *a = sm + (which ? dSekT : SemT) + piece128(r, pc);
+            const float *sc = which ? vekt : vem;
+            uint4 w = *reinterpret_cast<uint4 *>(a);
+            __nv_bfloat162 *b2 = reinterpret_cast<__nv_bfloat162 *>(&w);
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 fv = __bfloat1622float2(b2[i]);
+                v[2 * i] = fv.x * sc[pc * 8 + 2 * i];
+                v[2 * i + 1] = fv.y * sc[pc * 8 + 2 * i + 1];
+            }
+            w.x = tc::pack_bf16(v[0], v[1]); w.y = tc::pack_bf16(v[2], v[3]);
+            w.z = tc::pack_bf16(v[4], v[5]); w.w = tc::pack_bf16(v[6], v[7]);
+            *reinterpret_cast<uint4 *>(a) = w;
+        }
+    }
+    for (int e = tid; e < 64 * 8; e += NT) {
+        const int t = e >> 3, pc = e & 7;
+        const uint32_t off = t * 128 + ((pc ^ (t & 7)) << 4);
+        uint4 w = *reinterpret_cast<const uint4 *>(sm + Tm + off);
+        __nv_bfloat162 *b2 = reinterpret_cast<__nv_bfloat162 *>(&w);
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 fv = __bfloat1622float2(b2[i]);
+            v[2 * i] = fv.x * vbeta[pc * 8 + 2 * i];
+            v[2 * i + 1] = fv.y * vbeta[pc * 8 + 2 * i + 1];
+        }
+        w.x = tc::pack_bf16(v[0], v[1]); w.y = tc::pack_bf16(v[2], v[3]);
+        w.z = tc::pack_bf16(v[4], v[5]); w.w = tc::pack_bf16(v[6], v[7]);
+        *reinterpret_cast<uint4 *>(sm + TBm + off) = w;
+    }
+    sync_for_mma();
+    if (tid == 0) {
+        tc::mma_tile(tAP, tc::smem_addr(sm + KQp), 16384, tc::smem_addr(sm + Km), 8192, 128,
+                     tc::idesc_bf16(128, 64), false);
+        // X^T = (S^T e^m) Kp^T = S^T Kd^T
+        tc::mma_tile(tS1, tc::smem_addr(sm + SemT), 16384, tc::smem_addr(sm + KQp), 16384, 128,
+                     tc::idesc_bf16(128, 64), false);
+        tc::mma_commit(&bars[0]);
+    }
+    if (!wait_all(&bars[0], 0, &s_fail)) goto done;
+    {
+        float r[32];
+        // P (lanes 64-127) -> Pm, incl lower
+        tc::tmem_ld32(tAP + lane_off + ch * 32, r);
+        if (lg >= 2) {
+            const int t = jv - 64;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = (ch * 32 + j <= t) ? r[j] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + PmS, 64, t, ch * 32 + j, r + j);
+        }
+        // Y^T = V^T - X^T -> YT [dv][t] (in RQ)
+        tc::tmem_ld32(tS1 + lane_off + ch * 32, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = sw_val(sm + RV, 64, ch * 32 + j, jv) - r[j];
+        __syncthreads();   // raw q (RQ) no longer read by anyone
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RQ, 128, jv, ch * 32 + j, r + j);
+    }
+    sync_for_mma();
+    if (tid == 0) {
+        // U^T = Y^T (T diag(beta))^T
+        tc::mma_op(tS1, tc::Opnd{tc::smem_addr(sm + RQ), 16384, false},
+                   tc::Opnd{tc::smem_addr(sm + TBm), 8192, false}, 128, 64, 64, false);
+        // dU^T = dO^T P + (dS'^T e^{Gamma_L-m}) Km^T
+        tc::mma_op(tS2, tc::Opnd{tc::smem_addr(sm + dOm), 8192, true},
+                   tc::Opnd{tc::smem_addr(sm + PmS), 8192, true}, 128, 64, 64, false);
+        tc::mma_op(tS2, tc::Opnd{tc::smem_addr(sm + dSekT), 16384, false},
+                   tc::Opnd{tc::smem_addr(sm + Km), 8192, false}, 128, 64, 128, true);
+        tc::mma_commit(&bars[1]);
+    }
+    if (!wait_all(&bars[1], 0, &s_fail)) goto done;
+    {
+        float r[32];
+        tc::tmem_ld32(tS1 + lane_off + ch * 32, r);
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RV, 128, jv, ch * 32 + j, r + j);   // UTs
+        tc::tmem_ld32(tS2 + lane_off + ch * 32, r);
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RK, 128, jv, ch * 32 + j, r + j);   // dUTs
+    }
+    sync_for_mma();
+    if (tid == 0) {
+        // Z^T = dU^T T
+        tc::mma_op(tS1, tc::Opnd{tc::smem_addr(sm + RK), 16384, false},
+                   tc::Opnd{tc::smem_addr(sm + Tm), 8192, true}, 128, 64, 64, false);
+        // dP = dO U^T (rows 64-127 of the A operand are padding)
+        tc::mma_op(tS2, tc::Opnd{tc::smem_addr(sm + dOm), 8192, false},
+                   tc::Opnd{tc::smem_addr(sm + RV), 16384, true}, 128, 64, 128, false);
+        // Xm <- dK~ e^{Gamma_L-m} = U (dS' e^{Gamma_L-m})^T, transposed: [dk][s]
+        tc::mma_op(tXm, tc::Opnd{tc::smem_addr(sm + dSekT), 16384, true},
+                   tc::Opnd{tc::smem_addr(sm + RV), 16384, true}, 128, 64, 128, false);
+        // dT' = dU Y^T (padding rows)
+        tc::mma_op(tP1, tc::Opnd{tc::smem_addr(sm + RK), 16384, true},
+                   tc::Opnd{tc::smem_addr(sm + RQ), 16384, true}, 128, 64, 128, false);
+        tc::mma_commit(&bars[2]);
+    }
+    if (!wait_all(&bars[2], 0, &s_fail)) goto done;
+    {
+        float r[32], y[32];
+        // Z^T: dv output, unscaled Z^T tile (RG), sum_dv Z Y per row
+        tc::tmem_ld32(tS1 + lane_off + ch * 32, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] = r[j] * sw_val(sm + RQ, 128, jv, ch * 32 + j);
+        for (int j = 0; j < 32; ++j) {
+            const int32_t lr = c0 + ch * 32 + j;
+            if (lr >= L) break;
+            const float x = vbeta[ch * 32 + j] * r[j];
+            if (lr >= rho) {
+                const int64_t row = static_cast<int64_t>(row0) + (lr - rho);
+                gdv[(row * H + h) * D + jv] = __float2bfloat16_rn(x);
+            } else {
+                p.rep_grad[(static_cast<int64_t>(rptr + lr) * H + h) * W + D + jv] = x;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RG, 128, jv, ch * 32 + j, r + j);
+        warp_col_sums(y, rzy + lg * 64 + ch * 32);
+        // dP -> PmS (incl lower)
+        tc::tmem_ld32(tS2 + lane_off + ch * 32, r);
+        if (lg < 2) {
+            const int t = jv;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = (ch * 32 + j <= t) ? r[j] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + PmS, 64, t, ch * 32 + j, r + j);
+        }
+        // dT = dT' diag(beta), strict lower -> RK (dTm)
+        tc::tmem_ld32(tP1 + lane_off + ch * 32, r);
+        if (lg < 2) {
+            const int t = jv;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = (ch * 32 + j < t) ? r[j] * vbeta[ch * 32 + j] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RK, 64, t, ch * 32 + j, r + j);
+        }
+        // sum_s (dK~ e^{Gamma_L-m})[dk][s] Km[s][dk] for dGamma_L
+        tc::tmem_ld32(tXm + lane_off + ch * 32, r);
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc += r[j] * sw_val(sm + Km, 64, ch * 32 + j, jv);
+        vdgl[ch * 128 + jv] = acc;
+    }
+    sync_for_mma();
+    if (tid == 0) {
+        // W = dT T^T (padding rows)
+        tc::mma_op(tS1, tc::Opnd{tc::smem_addr(sm + RK), 8192, false},
+                   tc::Opnd{tc::smem_addr(sm + Tm), 8192, false}, 128, 64, 64, false);
+        tc::mma_commit(&bars[3]);
+    }
+    if (!wait_all(&bars[3], 0, &s_fail)) goto done;
+    {
+        float r[32];
+        tc::tmem_ld32(tS1 + lane_off + ch * 32, r);
+        if (lg < 2) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RQ, 64, jv, ch * 32 + j, r + j);  // Wm
+        }
+    }
+    sync_for_mma();
+    if (tid == 0) {
+        // T^T W (padding rows); dM = -T^T W
+        tc::mma_op(tS2, tc::Opnd{tc::smem_addr(sm + Tm), 8192, true},
+                   tc::Opnd{tc::smem_addr(sm + RQ), 8192, true}, 128, 64, 64, false);
+        tc::mma_commit(&bars[4]);
+    }
+    if (!wait_all(&bars[4], 0, &s_fail)) goto done;
+    {
+        float r[32], a[32];
+        tc::tmem_ld32(tS2 + lane_off + ch * 32, r);
+        tc::tmem_ld32(tAP + lane_off + ch * 32, a);
+        if (lg < 2) {
+            const int t = jv;
+            const float bt = vbeta[t];
+            float dba = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const bool low = ch * 32 + j < t;
+                const float dm = low ? -r[j] : 0.f;
+                dba += dm * a[j];
+                r[j] = bt * dm;
+            }
+            rma[ch * 64 + t] = dba;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + TBm, 64, t, ch * 32 + j, r + j);  // dAm
+        }
+    }
+    sync_for_mma();
+    if (tid == 0) {
+        // Xq^T = (S e^m) dO^T + Km^T dP^T
+        tc::mma_op(tXq, tc::Opnd{tc::smem_addr(sm + SemT), 16384, true},
+                   tc::Opnd{tc::smem_addr(sm + dOm), 8192, false}, 128, 64, 128, false);
+        tc::mma_op(tXq, tc::Opnd{tc::smem_addr(sm + Km), 8192, true},
+                   tc::Opnd{tc::smem_addr(sm + PmS), 8192, false}, 128, 64, 64, true);
+        // P1^T = Km^T dA^T
+        tc::mma_op(tP1, tc::Opnd{tc::smem_addr(sm + Km), 8192, true},
+                   tc::Opnd{tc::smem_addr(sm + TBm), 8192, false}, 128, 64, 64, false);
+        // P2^T = (S e^m) Z^T
+        tc::mma_op(tP2, tc::Opnd{tc::smem_addr(sm + SemT), 16384, true},
+                   tc::Opnd{tc::smem_addr(sm + RG), 16384, true}, 128, 64, 128, false);
+        // Xm^T += Kp^T dA + Qp^T dP
+        tc::mma_op(tXm, tc::Opnd{tc::smem_addr(sm + KQp), 16384, true},
+                   tc::Opnd{tc::smem_addr(sm + TBm), 8192, true}, 128, 64, 64, true);
+        tc::mma_op(tXm, tc::Opnd{tc::smem_addr(sm + KQp) + 8192, 16384, true},
+                   tc::Opnd{tc::smem_addr(sm + PmS), 8192, true}, 128, 64, 64, true);
+        tc::mma_commit(&bars[5]);
+    }
+    if (!wait_all(&bars[5], 0, &s_fail)) goto done;
+    {
+        // thread: key channel dk = jv, rows t = 32 ch .. 32 ch + 31
+        const int dk = jv;
+        const float m = vm[dk];
+        for (int hc = 0; hc < 2; ++hc) {
+            const int tb = ch * 32 + hc * 16;
+            float xq[16], p1[16], p2[16], xm[16], gm[16];
+            tc::tmem_ld16(tXq + lane_off + tb, xq);
+            tc::tmem_ld16(tP1 + lane_off + tb, p1);
+            tc::tmem_ld16(tP2 + lane_off + tb, p2);
+            tc::tmem_ld16(tXm + lane_off + tb, xm);
+            tc::tmem_ld16(tGam + lane_off + tb, gm);
+            float dgm[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int t = tb + u;
+                const float ep = __expf(gm[u] - m), en = __expf(m - gm[u]);
+                // dGamma pairs row and column terms of A and P (and Kt with Gamma_L); they
+                // cancel in the suffix sums only if both use the operands the MMAs used,
+                // so take Kp, Qp, Km as the rounded tile values.
+                const float kp = sw_val(sm + KQp, 128, t, dk), qp = sw_val(sm + KQp, 128, 64 + t, dk),
+                            km = sw_val(sm + Km, 64, t, dk);
+                const float bt = vbeta[t];
+                const float xp = p1[u] - bt * p2[u];
+                const float dqv = xq[u] * ep * f.scale;
+                const float dkv = xp * ep + xm[u] * en;
+                dgm[u] = xq[u] * qp + xp * kp - xm[u] * km;
+                const int32_t lr = c0 + t;
+                if (lr < L) {
+                    if (lr >= rho) {
+                        const int64_t o = ((static_cast<int64_t>(row0) + (lr - rho)) * H + h) * D + dk;
+                        gdq[o] = __float2bfloat16_rn(dqv);
+                        gdk[o] = __float2bfloat16_rn(dkv);
+                    } else {
+                        p.rep_grad[(static_cast<int64_t>(rptr + lr) * H + h) * W + dk] = dkv;
+                    }
+                }
+            }
+            // keep dGamma in registers of this pass through TMEM (reuse the Gamma columns)
+            {
+                uint32_t *uu = reinterpret_cast<uint32_t *>(dgm);
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                    "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                    :: "r"(tGam + lane_off + tb), "r"(uu[0]), "r"(uu[1]), "r"(uu[2]), "r"(uu[3]),
+                       "r"(uu[4]), "r"(uu[5]), "r"(uu[6]), "r"(uu[7]), "r"(uu[8]), "r"(uu[9]),
+                       "r"(uu[10]), "r"(uu[11]), "r"(uu[12]), "r"(uu[13]), "r"(uu[14]), "r"(uu[15])
+                    : "memory");
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+        }
+        // reverse cumulative sum of dGamma over t, plus dGamma_L
+        float dg[32];
+        tc::tmem_ld32(tGam + lane_off + ch * 32, dg);
+        float run = 0.f;
+#pragma unroll
+        for (int j = 31; j >= 0; --j) { run += dg[j]; dg[j] = run; }
+        if (ch == 1) vtot[dk] = run;
+        __syncthreads();
+        const float dgl = vdgl[dk] + vdgl[128 + dk] + (vdel[dk] + vdel[128 + dk]) * vel[dk];
+        const float off = (ch == 0 ? vtot[dk] : 0.f) + dgl;
+        for (int j = 0; j < 32; ++j) {
+            const int32_t lr = c0 + ch * 32 + j;
+            if (lr >= L) break;
+            const float x = dg[j] + off;
+            if (lr >= rho) {
+                gdg[((static_cast<int64_t>(row0) + (lr - rho)) * H + h) * D + dk] = __float2bfloat16_rn(x);
+            } else {
+                p.rep_grad[(static_cast<int64_t>(rptr + lr) * H + h) * W + 2 * D + dk] = x;
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < 64) {
+        const int t = tid;
+        const int32_t lr = c0 + t;
+        // dbeta = sum_dv Z (V - Kd S) + sum_s dM A   (the first sum holds both the beta V
+        // and the beta Kd paths of W = T diag(beta) [Kd | V])
+        const float db = rzy[t] + rzy[64 + t] + rzy[128 + t] + rzy[192 + t] + rma[t] + rma[64 + t];
+        if (lr < L) {
+            if (lr >= rho) gdb[(static_cast<int64_t>(row0) + (lr - rho)) * H + h] = __float2bfloat16_rn(db);
+            else p.rep_grad[(static_cast<int64_t>(rptr + lr) * H + h) * W + 3 * D] = db;
+        }
+    }
+done:
+    tc::cp_async_wait_all();
+    if (s_fail) {
+        dev_error(pd, kDevErrTimeout, seq, h);
+        for (int i = 0; i < 6; ++i) tc::mbar_wait(&bars[i], 0, 100000000LL);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tm, 512);
+}
+
 }  // namespace
 
-bool tc_supported(bool backward, int dtype, int Dd, int BCc) {
-    if (backward) return false;
+bool tc_supported(bool, int dtype, int Dd, int BCc) {
     return dtype == HARTS_BF16 && Dd == D && BCc == BC;
 }
 
@@ -427,8 +1160,22 @@ cudaError_t tc_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, in
     return cudaGetLastError();
 }
 
-cudaError_t tc_bwd_round(const BwdParams &, const PlanDev &, int32_t, int32_t, int32_t, cudaStream_t) {
-    return cudaErrorNotSupported;
+cudaError_t tc_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t base,
+                               int32_t n_items, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(kda_bwd_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bws_sm::bytes));
+    if (e != cudaSuccess) return e;
+    kda_bwd_state_tc<<<n_items, NT, bws_sm::bytes, st>>>(p, pd, base);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_bwd_grad(const BwdParams &p, const PlanDev &pd, int32_t chunk_begin,
+                        int32_t n_items, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(kda_bwd_grad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bwg_sm::bytes));
+    if (e != cudaSuccess) return e;
+    kda_bwd_grad_tc<<<n_items, NT, bwg_sm::bytes, st>>>(p, pd, chunk_begin);
+    return cudaGetLastError();
 }
 
 }  // namespace harts

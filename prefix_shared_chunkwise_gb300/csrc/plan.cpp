@@ -137,7 +137,6 @@ int build(harts_plan &P, int32_t n, const int32_t *parent, const int64_t *len, i
     for (int32_t v = 0; v < n; ++v) n_leaves += nkids[v] == 0;
     P.info.n_leaves = n_leaves;
     P.round_seq_ptr.assign(n_rounds + 1, 0);
-    for (int32_t r = 0; r <= n_rounds; ++r) P.round_seq_ptr[r] = rptr[r + 1 - 1 + 1 - 1 + 1 - 1];
     // rptr[r] = number of sequences with round < r (rounds are 1-based)
     for (int32_t r = 0; r <= n_rounds; ++r) P.round_seq_ptr[r] = rptr[r + 1];
 
@@ -314,6 +313,11 @@ void build_image(harts_plan &P) {
     put(I.off_fold_rows, frows.data(), frows.size());
     put(I.off_fold_ptr, fptr.data(), fptr.size());
     put(I.off_fold_occ, occ.data(), R);
+    std::vector<int32_t> cseq;
+    cseq.reserve(static_cast<size_t>(P.info.n_chunks));
+    for (int32_t i = 0; i < n_seq; ++i)
+        for (int32_t c = 0; c < P.seq_nchunks[i]; ++c) cseq.push_back(i);
+    put(I.off_chunk_seq, cseq.data(), cseq.size());
     while (w.size() % 64) w.push_back(0);
 }
 

@@ -29,6 +29,7 @@ struct PlanDev {
     const int32_t *fold_rows;      // [n_fold] distinct replayed rows, ascending
     const int32_t *fold_ptr;       // [n_fold+1]
     const int32_t *fold_occ;       // [R] replay occurrence ids grouped by row
+    const int32_t *chunk_seq;      // [n_chunks] sequence of every chunk
     int32_t n_rounds, n_seq, n_states, n_roots, n_fold, chunk;
     int64_t R, n_chunks;
 };
@@ -39,7 +40,7 @@ struct PlanImage {
     int64_t off_err, off_round_seq_ptr, off_round_order, off_seq_row0, off_seq_nown,
         off_seq_rho, off_seq_rptr, off_seq_src, off_seq_sptr, off_state_lpos, off_seq_cbase,
         off_state_cptr, off_state_cons, off_root_cptr, off_root_cons, off_replay_idx,
-        off_fold_rows, off_fold_ptr, off_fold_occ;
+        off_fold_rows, off_fold_ptr, off_fold_occ, off_chunk_seq;
 };
 
 void set_error(const std::string &msg);

@@ -36,13 +36,44 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.  a_mn / b_mn
+// select the MN-major (transposed) reading of the operand.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn = false,
+                                                  bool b_mn = false) {
     return (1u << 4)                                   // D format: f32
          | (1u << 7)                                   // A format: bf16
          | (1u << 10)                                  // B format: bf16
+         | (a_mn ? (1u << 15) : 0u)
+         | (b_mn ? (1u << 16) : 0u)
          | (static_cast<uint32_t>(N >> 3) << 17)
          | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Descriptor for reading a SW128 tile stored as [K rows][MN columns] (a K-major tile
+// of another product, read transposed): 64-column atoms `atom_bytes` apart, 8-row
+// groups 1024 B apart.
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t atom_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+    d |= static_cast<uint64_t>((atom_bytes >> 4) & 0x3FFF) << 16;   // next 64 MN columns
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;                    // next 8 K rows
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Operand of a tile product: base address, atom stride, and whether it is read MN-major
+// (stored [K][MN]) or K-major (stored [MN][K]).
+struct Opnd {
+    uint32_t saddr, atom_bytes;
+    bool mn;
+};
+
+__device__ __forceinline__ uint64_t opnd_desc(const Opnd &o, int kk) {
+    // K-major: 16 K-columns = 32 B inside an atom, atoms every 4 steps.
+    // MN-major: 16 K-rows = 2048 B.
+    return o.mn ? desc_sw128_mn(o.saddr + kk * 2048, o.atom_bytes)
+                : desc_sw128(o.saddr + (kk >> 2) * o.atom_bytes + (kk & 3) * 32);
 }
 
 // ---- TMEM allocation (one full warp executes these) ------------------------------------
@@ -80,6 +111,14 @@ __device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_saddr, uint
         mma_bf16(d_tmem, desc_sw128(a_saddr + aoff), desc_sw128(b_saddr + boff), idesc,
                  (accumulate || kk > 0) ? 1u : 0u);
     }
+}
+
+// D[M x N] (+)= op(A) * op(B)^T for any mix of K-major / MN-major operands.
+__device__ __forceinline__ void mma_op(uint32_t d_tmem, const Opnd &a, const Opnd &b, int M, int N,
+                                       int K, bool accumulate) {
+    const uint32_t id = idesc_bf16(M, N, a.mn, b.mn);
+    for (int kk = 0; kk < K / 16; ++kk)
+        mma_bf16(d_tmem, opnd_desc(a, kk), opnd_desc(b, kk), id, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // Arrive on `bar` when every tcgen05 operation issued so far by this thread completes.
@@ -140,6 +179,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
           "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]),
           "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]),
           "=r"(u[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
+    uint32_t *u = reinterpret_cast<uint32_t *>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]),
+          "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

@@ -154,3 +154,26 @@ def test_tc_forward_matches_simt_forward():
     assert pl.device_error() == 0
     assert rel_l2(outs[1][0], outs[0][0]) < 5e-3
     assert rel_l2(outs[1][1], outs[0][1]) < 5e-3
+
+
+@pytest.mark.parametrize("decay", [1.0, 0.03])
+def test_bf16_d128_fwd_bwd_small_forest_tc(decay):
+    """Tensor-core forward + backward (state-carry and per-chunk gradient kernels)."""
+    rng = np.random.Generator(np.random.PCG64(31))
+    n = 14
+    parent = np.array([-1 if (i == 0 or rng.random() < 0.1) else int(rng.integers(0, i))
+                       for i in range(n)], np.int32)
+    seg_len = rng.integers(1, 220, size=n).astype(np.int64)
+    errs = _run(parent, seg_len, 64, 2, 128, "bf16", 21, backward=True, kernel=_lib.HARTS_KERNEL_TC,
+                d_final=True, decay=decay)
+    _assert(errs, TOL["bf16"])
+
+
+def test_bf16_d128_fwd_bwd_with_h0_tc():
+    rng = np.random.Generator(np.random.PCG64(32))
+    n = 9
+    parent = np.array([-1, 0, 0, 1, -1, 4, 4, 5, 2], np.int32)
+    seg_len = rng.integers(20, 200, size=n).astype(np.int64)
+    errs = _run(parent, seg_len, 64, 2, 128, "bf16", 22, backward=True, kernel=_lib.HARTS_KERNEL_TC,
+                h0=True, decay=0.05, scale=0.7)
+    _assert(errs, TOL["bf16"])
