@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Packed-tree KDA forward + backward throughput on one GB300 (or N, weak scaling).
+
+A step is one pass of the whole hot path over one synthetic rollout forest: the
+forward (one packed call per round), the backward state pass (rounds in reverse,
+gradients through the state handoffs) and the per-chunk gradient pass with the
+replay-row fold.  The metric is compact tokens per second, C / step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own forest (weak scaling, no collective on the data
+path); the timed region is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "wide256k_bf16"
+METRIC = "packed-tree KDA fwd+bwd compact tokens/s"
+UNIT = "compact tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--expanded", action="store_true",
+                    help="also time the same kernels on the trajectory-expanded input")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---- algorithmic cost model (per step) ---------------------------------------------------
+
+def cost_model(info, H, D, B):
+    """Algorithmic bytes and flops of the path (bf16 tensors, fp32 states).
+
+    Per compact or replay token-head: fwd reads q, k, v, g (2 B each per channel) and
+    beta (2 B), writes o for own rows; bwd reads the same plus dO for own rows and writes
+    dq, dk, dv, dg, dbeta; a replay row's dk, dv, dg, dbeta are read-modified-written.
+    Handoffs: 4 dk dv H bytes per slot write/read and per consumer gradient write/read.
+    Flops: 2B(3dk + 2dv) + 6 dk dv per token-head forward, backward twice that."""
+    C, R, Nst, Ncons = info["C"], info["R"], info["n_states"], info["n_cons"]
+    tok_in = 4 * 2 * D + 2
+    fwd_b = (C + R) * H * tok_in + C * H * 2 * D + 4 * D * D * H * (Nst + Ncons)
+    bwd_b = ((C + R) * H * tok_in + C * H * 2 * D + C * H * tok_in
+             + R * H * 2 * (3 * 2 * D + 2) + 4 * D * D * H * (Nst + 2 * Ncons))
+    f_tok = 2 * B * (3 * D + 2 * D) + 6 * D * D
+    fwd_f = (C + R) * H * f_tok
+    bwd_f = 2 * fwd_f
+    return dict(fwd_bytes=fwd_b, bwd_bytes=bwd_b, fwd_flops=fwd_f, bwd_flops=bwd_f)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def traffic_from_profiles(kernel):
+    """DRAM bytes per launch for `kernel` from the committed ncu summary, if present."""
+    p = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 2 and parts[0] == kernel:
+            try:
+                return float(parts[1])
+            except ValueError:
+                return None
+    return None
+
+
+# ---- clocks ------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        import torch
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        uuid = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            pass
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if uuid:
+            cmd[1:1] = ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), hw=f[5], hwt=f[6], swt=f[7], pc=f[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sms = sorted(r["sm"] for r in rows)
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pc", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return dict(sm_mhz=sms[len(sms) // 2], sm_max_mhz=max(r["smax"] for r in rows),
+                    reasons=sorted(reasons), samples=len(rows))
+
+
+# ---- oracle baseline on host cores -------------------------------------------------------
+
+def pick_sample_tree(parent, seg_len, target_S):
+    """Split the forest into trees; return the segment ids of the tree whose expanded
+    size is closest to target_S."""
+    import numpy as np
+    n = len(parent)
+    root = np.zeros(n, np.int64)
+    for i in range(n):
+        root[i] = i if parent[i] < 0 else root[parent[i]]
+    from prefix_shared_chunkwise_gb300.synth import tree_stats
+    best, best_d = None, None
+    for r in np.unique(root):
+        ids = np.nonzero(root == r)[0]
+        remap = {int(v): j for j, v in enumerate(ids)}
+        sub_parent = np.array([-1 if parent[v] < 0 else remap[int(parent[v])] for v in ids], np.int32)
+        st = tree_stats(sub_parent, seg_len[ids])
+        d = abs(st["S"] - target_S)
+        if best is None or d < best_d:
+            best, best_d = (ids, sub_parent, st), d
+    return best
+
+
+def oracle_sample(parent, seg_len, seg_offset, inputs, H_sample, B, target_S):
+    """Run the fp64 oracle forward + backward over one tree of the forest (heads
+    [0, H_sample)); returns (compact tokens of the tree, heads, seconds, threads, stats)."""
+    import numpy as np
+    import oracle
+    ids, sub_parent, st = pick_sample_tree(parent, seg_len, target_S)
+    rows = np.concatenate([np.arange(seg_offset[v], seg_offset[v] + seg_len[v]) for v in ids])
+    sub_off = np.zeros(len(ids), np.int64)
+    acc = 0
+    for j, v in enumerate(ids):
+        sub_off[j] = acc
+        acc += int(seg_len[v])
+    import torch
+    idx = torch.as_tensor(rows, device=inputs["q"].device)
+    host = {k: inputs[k].index_select(0, idx)[:, :H_sample].float().cpu().double().numpy()
+            for k in ("q", "k", "v", "g", "beta", "W")}
+    threads = len(os.sched_getaffinity(0))
+    t0 = time.time()
+    oracle.kda_forest(sub_parent, seg_len[ids], sub_off, host["q"], host["k"], host["v"],
+                      host["g"], host["beta"], chunk=B, W=host["W"], n_threads=threads)
+    dt = time.time() - t0
+    return st["C"], H_sample, dt, min(threads, H_sample), st
+
+
+# ---- our arm -----------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from prefix_shared_chunkwise_gb300 import _lib, build
+    from prefix_shared_chunkwise_gb300.api import Plan, kda_bwd, kda_fwd
+    from prefix_shared_chunkwise_gb300.synth import WORKLOAD_ORDER, WORKLOADS, make_inputs, make_tree
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        build.build()
+    if ws > 1:
+        dist.barrier()
+    wl = WORKLOADS[args.workload]
+    H, D, B = wl.H, wl.dk, wl.chunk
+    seed = WORKLOAD_ORDER.index(args.workload) + 1000 * rank
+    parent, seg_len = make_tree(args.workload, seed=seed)
+    pl = Plan(parent, seg_len, B).upload()
+    info = pl.info
+    C = info["C"]
+    x = make_inputs(C, H, D, D, wl.dtype, seed=3 + rank, device="cuda")
+    dev = torch.device("cuda", local)
+    dtc = 1 if wl.dtype == "bf16" else 0
+    esz = 2 if wl.dtype == "bf16" else 4
+    o = torch.empty((C, H, D), dtype=x["q"].dtype, device=dev)
+    states = torch.empty((max(info["n_states"], 1), H, D, D), dtype=torch.float32, device=dev)
+    cs = torch.empty(pl.chunk_state_bytes(H, D, D, dtc) // esz, dtype=x["q"].dtype, device=dev)
+    grads = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]),
+                 dg=torch.empty_like(x["g"]), dbeta=torch.empty_like(x["beta"]))
+    wsb = torch.empty(max(pl.bwd_workspace_bytes(H, D, D), 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd(inp):
+        kda_fwd(pl, inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], o=o, states=states,
+                chunk_states=cs)
+
+    def bwd(inp, phase):
+        kda_bwd(pl, inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["W"], states=states,
+                chunk_states=cs, grads=grads, workspace=wsb, phase=phase)
+
+    for _ in range(max(args.warmup, 3)):
+        fwd(x); bwd(x, "state"); bwd(x, "grad")
+    torch.cuda.synchronize()
+    if pl.device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        fwd(x)
+        ev[i][1].record(stream)
+        bwd(x, "state")
+        ev[i][2].record(stream)
+        bwd(x, "grad")
+        ev[i][3].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    ph = np.array([[ev[i][0].elapsed_time(ev[i][1]), ev[i][1].elapsed_time(ev[i][2]),
+                    ev[i][2].elapsed_time(ev[i][3])] for i in range(K)]).mean(0)
+    if pl.device_error() != 0:
+        raise RuntimeError("device error during the timed steps")
+    ms = total_ms / K
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = C * ws / (ms / 1e3)
+
+    # ---- end to end through the public API with host buffers --------------------------
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in x.items()}
+        for k in host_in:
+            host_in[k].copy_(x[k])
+        dev_in = {k: torch.empty_like(v) for k, v in x.items()}
+        outs = dict(o=o, **grads)
+        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for k in host_in:
+                dev_in[k].copy_(host_in[k], non_blocking=True)
+            fwd(dev_in); bwd(dev_in, "state"); bwd(dev_in, "grad")
+            for k in host_out:
+                host_out[k].copy_(outs[k], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        K2 = max(2, min(K, 5))
+        if ws > 1:
+            dist.barrier()
+        a0 = torch.cuda.Event(enable_timing=True); a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(K2):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ems = a0.elapsed_time(a1) / K2
+        if ws > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = dict(value=C * ws / (ems / 1e3), unit=UNIT, h2d_bytes_per_step=int(h2d),
+                   d2h_bytes_per_step=int(d2h), ms_per_step=round(ems, 3))
+        del host_in, host_out, dev_in
+
+    # ---- roofline ----------------------------------------------------------------------
+    cm = cost_model(info, H, D, B)
+    hbm, tf_burst, tf_sus, src = peaks()
+    phase_ms = dict(fwd=float(ph[0]), bwd_state=float(ph[1]), bwd_grad=float(ph[2]))
+    # bytes / flops attributed to each phase: the state pass reads its inputs and the
+    # handoff gradients; the gradient pass does the rest of the backward
+    phase_bytes = dict(fwd=cm["fwd_bytes"],
+                       bwd_state=(info["C"] + info["R"]) * H * (3 * 2 * D + 2) + info["C"] * H * 2 * D
+                       + 4 * D * D * H * 2 * info["n_cons"],
+                       bwd_grad=cm["bwd_bytes"])
+    phase_bytes["bwd_grad"] -= phase_bytes["bwd_state"]
+    dom = max(phase_ms, key=phase_ms.get)
+    kernel_name = {"fwd": "kda_fwd_tc", "bwd_state": "kda_bwd_state_tc", "bwd_grad": "kda_bwd_grad_tc"}[dom]
+    achieved = phase_bytes[dom] / (phase_ms[dom] / 1e3) / 1e9
+    traffic = traffic_from_profiles(kernel_name)
+    step_bytes = cm["fwd_bytes"] + cm["bwd_bytes"]
+    step_flops = cm["fwd_flops"] + cm["bwd_flops"]
+    t_star = max(step_bytes / (hbm * 1e9), step_flops / (tf_sus * 1e12))
+    roofline = dict(bound="hbm", kernel=kernel_name, achieved=round(achieved, 1), peak=hbm,
+                    unit="GB/s", frac=round(achieved / hbm, 4), traffic=traffic,
+                    peak_source=f"{src} hbm_gbs",
+                    step=dict(algorithmic_bytes=int(step_bytes), algorithmic_flops=int(step_flops),
+                              t_star_ms=round(t_star * 1e3, 3), frac=round(t_star * 1e3 / ms, 4)))
+
+    expanded = None
+    if args.expanded:
+        expanded = run_expanded(parent, seg_len, pl, x, wl, ms)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        c_s, h_s, dt, thr, st = oracle_sample(parent, seg_len, pl.arrays()["seg_offset"], x, H, B,
+                                              target_S=12000)
+        cpu = dict(value=round(c_s / dt, 2), unit=UNIT, cores=thr, kind="oracle",
+                   sample=f"one tree of the forest ({c_s} compact / {st['S']} expanded tokens, "
+                          f"all {h_s} heads), fp64 token recurrence fwd+bwd, {dt:.1f} s")
+
+    if rank == 0:
+        line = dict(metric=METRIC, value=round(value, 1), unit=UNIT, n_gpus=ws, steps=K,
+                    warmup=max(args.warmup, 3), ms_per_step=round(ms, 3), higher_is_better=True,
+                    scaling="weak", vs_baseline=None, dtype=wl.dtype, data="synthetic",
+                    config=dict(workload=args.workload, trees=wl.n_trees, C=C, S=info["S"],
+                                R=info["R"], calls=info["n_rounds"], sequences=info["n_seq"],
+                                states=info["n_states"], H=H, dk=D, dv=D, chunk=B,
+                                parallelism=f"dp{ws} (one forest per GPU)",
+                                l2="inputs larger than L2 (each input tensor 2.1 GB)"),
+                    phases_ms={k: round(v, 3) for k, v in phase_ms.items()},
+                    gpu_launches=K * (2 * info["n_rounds"] + 1 + (1 if info["n_fold_rows"] else 0)),
+                    roofline=roofline, cpu_baseline=cpu, e2e=e2e, clocks=clk)
+        if expanded:
+            line["expanded"] = expanded
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def run_expanded(parent, seg_len, pl_tree, x, wl, tree_ms):
+    """Same kernels on the trajectory-expanded input: every root-to-leaf trajectory is
+    its own root sequence (S rows, one round)."""
+    import numpy as np
+    import torch
+    from prefix_shared_chunkwise_gb300.api import Plan, kda_bwd, kda_fwd
+    from prefix_shared_chunkwise_gb300.synth import expand_rows
+    rows, ptr, _ = expand_rows(parent, seg_len, pl_tree.arrays()["seg_offset"])
+    n_traj = len(ptr) - 1
+    e_parent = -np.ones(n_traj, np.int32)
+    e_len = np.diff(ptr).astype(np.int64)
+    pl = Plan(e_parent, e_len, wl.chunk).upload()
+    H, D = wl.H, wl.dk
+    idx = torch.as_tensor(rows, device=x["q"].device)
+    xe = {k: v.index_select(0, idx) for k, v in x.items()}
+    dev = x["q"].device
+    o = torch.empty_like(xe["v"])
+    cs = torch.empty(pl.chunk_state_bytes(H, D, D, 1) // 2, dtype=torch.bfloat16, device=dev)
+    grads = dict(dq=torch.empty_like(xe["q"]), dk=torch.empty_like(xe["k"]), dv=torch.empty_like(xe["v"]),
+                 dg=torch.empty_like(xe["g"]), dbeta=torch.empty_like(xe["beta"]))
+    wsb = torch.empty(max(pl.bwd_workspace_bytes(H, D, D), 256), dtype=torch.uint8, device=dev)
+
+    def step():
+        kda_fwd(pl, xe["q"], xe["k"], xe["v"], xe["g"], xe["beta"], o=o, chunk_states=cs)
+        kda_bwd(pl, xe["q"], xe["k"], xe["v"], xe["g"], xe["beta"], xe["W"], states=None,
+                chunk_states=cs, grads=grads, workspace=wsb)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ems = e0.elapsed_time(e1) / 3
+    return dict(rows=int(pl.info["C"]), trajectories=n_traj, ms_per_step=round(ems, 3),
+                speedup_tree_vs_expanded=round(ems / tree_ms, 3))
+
+
+# ---- reference arm: the oracle on host cores ---------------------------------------------
+
+def run_reference(args):
+    import numpy as np
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from prefix_shared_chunkwise_gb300.synth import WORKLOAD_ORDER, WORKLOADS, make_inputs, make_tree
+    wl = WORKLOADS[args.workload]
+    H, D, B = wl.H, wl.dk, wl.chunk
+    seed = WORKLOAD_ORDER.index(args.workload)
+    parent, seg_len = make_tree(args.workload, seed=seed)
+    ids, sub_parent, st = pick_sample_tree(parent, seg_len, target_S=6000)
+    # seeded inputs of the workload's distributions for the sampled tree only
+    h_s = min(H, 8)
+    sub = make_inputs(st["C"], h_s, D, D, wl.dtype, seed=3, device="cpu")
+    host = {k: v.float().double().numpy() for k, v in sub.items()}
+    sub_off = np.cumsum([0] + [int(seg_len[v]) for v in ids[:-1]]).astype(np.int64)
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+
+    def step():
+        oracle.kda_forest(sub_parent, seg_len[ids], sub_off, host["q"], host["k"], host["v"],
+                          host["g"], host["beta"], chunk=B, W=host["W"], n_threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.time()
+    for _ in range(args.steps):
+        step()
+    dt = (time.time() - t0) / args.steps
+    # the sample covers st["C"] compact tokens on h_s of H heads
+    value = st["C"] * (h_s / H) / dt
+    sample = (f"one tree ({st['C']} compact / {st['S']} expanded tokens), {h_s} of {H} heads, "
+              f"fp64 token recurrence fwd+bwd per step")
+    line = dict(metric=METRIC, value=round(value, 2), unit=UNIT, n_gpus=ws, steps=args.steps,
+                warmup=args.warmup, ms_per_step=round(dt * 1e3, 1), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
+                config=dict(workload=args.workload, trees=wl.n_trees, H=H, dk=D, dv=D, chunk=B),
+                cpu_baseline=dict(value=round(value, 2), unit=UNIT, kind="oracle",
+                                  cores=min(threads, h_s), sample=sample),
+                e2e=dict(value=round(value, 2), unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

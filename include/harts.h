@@ -215,6 +215,21 @@ size_t harts_kda_bwd_workspace_bytes(const harts_plan *plan, int32_t H, int32_t 
  */
 int harts_kda_bwd(const harts_plan *plan, const harts_kda_bwd_args *args, harts_stream_t stream);
 
+/*
+ * The backward pass in its two phases; harts_kda_bwd is harts_kda_bwd_state followed by
+ * harts_kda_bwd_grad with the same arguments (same workspace, same stream order).
+ *  - state: rounds in reverse, one launch per round; carries dL/dS through every
+ *    sequence and its handoffs; stores each sequence's initial-state gradient and (on
+ *    the tensor-core path) the carried gradient at every chunk end in the workspace.
+ *    On the exact fp32 path this phase also forms all input gradients.
+ *  - grad:  on the tensor-core path one launch over every (chunk, head), forming dq, dk,
+ *    dv, dg, dbeta from the saved chunk states; then the deterministic fold of replay-row
+ *    gradients into ancestor rows and dh0.
+ * Errors: as harts_kda_bwd.
+ */
+int harts_kda_bwd_state(const harts_plan *plan, const harts_kda_bwd_args *args, harts_stream_t stream);
+int harts_kda_bwd_grad(const harts_plan *plan, const harts_kda_bwd_args *args, harts_stream_t stream);
+
 /* Message for the last error on the calling thread ("" if none). */
 const char *harts_last_error(void);
 

@@ -21,7 +21,7 @@ EXPORTED = [
     "harts_plan_calls", "harts_plan_get_info", "harts_plan_export", "harts_plan_device_bytes",
     "harts_plan_upload", "harts_plan_device_error", "harts_plan_free",
     "harts_kda_chunk_state_bytes", "harts_kda_fwd", "harts_kda_bwd_workspace_bytes",
-    "harts_kda_bwd", "harts_last_error",
+    "harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad", "harts_last_error",
 ]
 
 _i32, _i64, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
@@ -92,7 +92,9 @@ def lib():
         L.harts_kda_fwd.argtypes = [_vp, ctypes.POINTER(FwdArgs), _vp]
         L.harts_kda_bwd_workspace_bytes.argtypes = [_vp, _i32, _i32, _i32]
         L.harts_kda_bwd_workspace_bytes.restype = ctypes.c_size_t
-        L.harts_kda_bwd.argtypes = [_vp, ctypes.POINTER(BwdArgs), _vp]
+        for fn in ("harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad"):
+            getattr(L, fn).argtypes = [_vp, ctypes.POINTER(BwdArgs), _vp]
+            getattr(L, fn).restype = ctypes.c_int
         L.harts_last_error.argtypes = []
         L.harts_last_error.restype = ctypes.c_char_p
         for fn in ("harts_plan_calls", "harts_plan_get_info", "harts_plan_export",

@@ -134,8 +134,9 @@ def kda_fwd(plan: Plan, q, k, v, g, beta, *, o=None, states=None, final_state=No
 
 def kda_bwd(plan: Plan, q, k, v, g, beta, d_o, *, states, chunk_states, d_final=None,
             h0=None, dh0=None, scale=1.0, grads=None, workspace=None,
-            kernel=L.HARTS_KERNEL_AUTO, stream=None):
-    """harts_kda_bwd.  Returns dict(dq, dk, dv, dg, dbeta[, dh0])."""
+            kernel=L.HARTS_KERNEL_AUTO, stream=None, phase="all"):
+    """harts_kda_bwd (phase "all"), harts_kda_bwd_state ("state") or harts_kda_bwd_grad
+    ("grad").  Returns dict(dq, dk, dv, dg, dbeta[, dh0])."""
     import torch
     C, H, dk = q.shape
     dv = v.shape[2]
@@ -155,7 +156,8 @@ def kda_bwd(plan: Plan, q, k, v, g, beta, d_o, *, states, chunk_states, d_final=
     a.dh0 = None if dh0 is None else dh0.data_ptr()
     a.workspace = workspace.data_ptr()
     a.workspace_bytes = workspace.numel()
-    L.check(L.lib().harts_kda_bwd(plan.handle, ctypes.byref(a), _stream(stream)), "harts_kda_bwd")
+    fn = {"all": "harts_kda_bwd", "state": "harts_kda_bwd_state", "grad": "harts_kda_bwd_grad"}[phase]
+    L.check(getattr(L.lib(), fn)(plan.handle, ctypes.byref(a), _stream(stream)), fn)
     if dh0 is not None:
         grads["dh0"] = dh0
     return grads

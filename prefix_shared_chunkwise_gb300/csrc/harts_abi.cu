@@ -172,7 +172,8 @@ int harts_kda_fwd(const harts_plan *P, const harts_kda_fwd_args *a, harts_stream
     return HARTS_OK;
 }
 
-int harts_kda_bwd(const harts_plan *P, const harts_kda_bwd_args *a, harts_stream_t stream) {
+static int kda_bwd_phases(const harts_plan *P, const harts_kda_bwd_args *a, harts_stream_t stream,
+                          bool do_state, bool do_grad) {
     if (!a) { set_error("NULL args"); return HARTS_EINVAL; }
     int rc = check_fwd_args(P, &a->fwd);
     if (rc) return rc;
@@ -193,25 +194,41 @@ int harts_kda_bwd(const harts_plan *P, const harts_kda_bwd_args *a, harts_stream
     p.ds_init = reinterpret_cast<float *>(w + ws.ds_init);
     p.rep_grad = reinterpret_cast<float *>(w + ws.rep_grad);
     p.dchunk = fam == 1 ? static_cast<void *>(w + ws.dchunk) : nullptr;
-    for (int32_t r = P->info.n_rounds - 1; r >= 0; --r) {
-        const int32_t base = P->round_seq_ptr[r];
-        const int32_t n = (P->round_seq_ptr[r + 1] - base) * H;
-        if (n == 0) continue;
-        cudaError_t e = fam == 1 ? tc_bwd_state_round(p, P->view, base, n, st)
-                                 : simt_bwd_round(a->fwd.dtype, BC, p, P->view, base, n, st);
-        if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    if (do_state) {
+        for (int32_t r = P->info.n_rounds - 1; r >= 0; --r) {
+            const int32_t base = P->round_seq_ptr[r];
+            const int32_t n = (P->round_seq_ptr[r + 1] - base) * H;
+            if (n == 0) continue;
+            cudaError_t e = fam == 1 ? tc_bwd_state_round(p, P->view, base, n, st)
+                                     : simt_bwd_round(a->fwd.dtype, BC, p, P->view, base, n, st);
+            if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+        }
     }
-    if (fam == 1) {
-        // every chunk's gradients at once: they only depend on saved per-chunk states
-        const int64_t items = P->info.n_chunks * H;
-        if (items > 0x7fffffff) { set_error("too many (chunk, head) items"); return HARTS_EOVERFLOW; }
-        cudaError_t e = tc_bwd_grad(p, P->view, 0, static_cast<int32_t>(items), st);
-        if (e != cudaSuccess) return cuda_fail(e, "backward gradient launch");
+    if (do_grad) {
+        if (fam == 1) {
+            // every chunk's gradients at once: they only depend on saved per-chunk states
+            const int64_t items = P->info.n_chunks * H;
+            if (items > 0x7fffffff) { set_error("too many (chunk, head) items"); return HARTS_EOVERFLOW; }
+            cudaError_t e = tc_bwd_grad(p, P->view, 0, static_cast<int32_t>(items), st);
+            if (e != cudaSuccess) return cuda_fail(e, "backward gradient launch");
+        }
+        cudaError_t e = bwd_finish(a->fwd.dtype, p, P->view, st);
+        if (e != cudaSuccess) return cuda_fail(e, "backward reductions");
     }
-    cudaError_t e = bwd_finish(a->fwd.dtype, p, P->view, st);
-    if (e != cudaSuccess) return cuda_fail(e, "backward reductions");
     set_error("");
     return HARTS_OK;
+}
+
+int harts_kda_bwd(const harts_plan *P, const harts_kda_bwd_args *a, harts_stream_t stream) {
+    return kda_bwd_phases(P, a, stream, true, true);
+}
+
+int harts_kda_bwd_state(const harts_plan *P, const harts_kda_bwd_args *a, harts_stream_t stream) {
+    return kda_bwd_phases(P, a, stream, true, false);
+}
+
+int harts_kda_bwd_grad(const harts_plan *P, const harts_kda_bwd_args *a, harts_stream_t stream) {
+    return kda_bwd_phases(P, a, stream, false, true);
 }
 
 }  // extern "C"
