@@ -230,6 +230,30 @@ int harts_kda_bwd(const harts_plan *plan, const harts_kda_bwd_args *args, harts_
 int harts_kda_bwd_state(const harts_plan *plan, const harts_kda_bwd_args *args, harts_stream_t stream);
 int harts_kda_bwd_grad(const harts_plan *plan, const harts_kda_bwd_args *args, harts_stream_t stream);
 
+/*
+ * harts_kda_bwd_static - harts_kda_bwd without any caller-provided device memory.
+ * (This entry point has no counterpart in the paper; it is a deployment convenience.)
+ *
+ * For callers that cannot give the library device memory of its own: plugins inside a
+ * host framework that owns the device pool and offers no allocation hook, or step loops
+ * that must not allocate.  The caller still passes every input and output; the scratch
+ * (initial-state gradients, replay-row gradients, saved chunk-end state gradients) lives
+ * in a file-scope device array of harts_kda_bwd_static_max_bytes() = 32 MiB that every
+ * GPU loading the library holds until the process exits.
+ *  - args->workspace and args->workspace_bytes are ignored.
+ *  - The first call on a device (with that device current) looks up the array's device
+ *    address; make that first call before any stream capture.  It allocates nothing and
+ *    calls no allocating routine.
+ *  - Every call on a device shares the one array and leaves its last contents there.
+ *    Nothing in it needs to start at zero: each call writes every scratch entry before
+ *    reading it.  Calls whose work overlaps on the GPU (two streams, or two host
+ *    threads) race on the array; serialise them.
+ * Errors: as harts_kda_bwd, plus HARTS_ESMALLBUF when the plan, heads and head size need
+ * more scratch than the array holds (harts_kda_bwd_workspace_bytes tells the need).
+ */
+int harts_kda_bwd_static(const harts_plan *plan, const harts_kda_bwd_args *args, harts_stream_t stream);
+size_t harts_kda_bwd_static_max_bytes(void);
+
 /* Message for the last error on the calling thread ("" if none). */
 const char *harts_last_error(void);
 

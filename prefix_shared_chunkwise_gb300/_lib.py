@@ -21,7 +21,8 @@ EXPORTED = [
     "harts_plan_calls", "harts_plan_get_info", "harts_plan_export", "harts_plan_device_bytes",
     "harts_plan_upload", "harts_plan_device_error", "harts_plan_free",
     "harts_kda_chunk_state_bytes", "harts_kda_fwd", "harts_kda_bwd_workspace_bytes",
-    "harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad", "harts_last_error",
+    "harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad", "harts_kda_bwd_static",
+    "harts_kda_bwd_static_max_bytes", "harts_last_error",
 ]
 
 _i32, _i64, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
@@ -92,7 +93,9 @@ def lib():
         L.harts_kda_fwd.argtypes = [_vp, ctypes.POINTER(FwdArgs), _vp]
         L.harts_kda_bwd_workspace_bytes.argtypes = [_vp, _i32, _i32, _i32]
         L.harts_kda_bwd_workspace_bytes.restype = ctypes.c_size_t
-        for fn in ("harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad"):
+        L.harts_kda_bwd_static_max_bytes.argtypes = []
+        L.harts_kda_bwd_static_max_bytes.restype = ctypes.c_size_t
+        for fn in ("harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad", "harts_kda_bwd_static"):
             getattr(L, fn).argtypes = [_vp, ctypes.POINTER(BwdArgs), _vp]
             getattr(L, fn).restype = ctypes.c_int
         L.harts_last_error.argtypes = []

@@ -135,8 +135,9 @@ def kda_fwd(plan: Plan, q, k, v, g, beta, *, o=None, states=None, final_state=No
 def kda_bwd(plan: Plan, q, k, v, g, beta, d_o, *, states, chunk_states, d_final=None,
             h0=None, dh0=None, scale=1.0, grads=None, workspace=None,
             kernel=L.HARTS_KERNEL_AUTO, stream=None, phase="all"):
-    """harts_kda_bwd (phase "all"), harts_kda_bwd_state ("state") or harts_kda_bwd_grad
-    ("grad").  Returns dict(dq, dk, dv, dg, dbeta[, dh0])."""
+    """harts_kda_bwd (phase "all"), harts_kda_bwd_state ("state"), harts_kda_bwd_grad
+    ("grad"), or harts_kda_bwd_static ("static": no workspace, the library's own scratch).
+    Returns dict(dq, dk, dv, dg, dbeta[, dh0])."""
     import torch
     C, H, dk = q.shape
     dv = v.shape[2]
@@ -145,7 +146,7 @@ def kda_bwd(plan: Plan, q, k, v, g, beta, d_o, *, states, chunk_states, d_final=
         grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                      dg=torch.empty_like(g), dbeta=torch.empty_like(beta))
     nb = plan.bwd_workspace_bytes(H, dk, dv)
-    if workspace is None:
+    if workspace is None and phase != "static":
         workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
     a = L.BwdArgs()
     a.fwd = _fwd_args(plan, q, k, v, g, beta, None, states, None, h0, chunk_states, scale, kernel)
@@ -154,9 +155,10 @@ def kda_bwd(plan: Plan, q, k, v, g, beta, d_o, *, states, chunk_states, d_final=
     for n in ("dq", "dk", "dv", "dg", "dbeta"):
         setattr(a, n, grads[n].data_ptr())
     a.dh0 = None if dh0 is None else dh0.data_ptr()
-    a.workspace = workspace.data_ptr()
-    a.workspace_bytes = workspace.numel()
-    fn = {"all": "harts_kda_bwd", "state": "harts_kda_bwd_state", "grad": "harts_kda_bwd_grad"}[phase]
+    a.workspace = None if workspace is None else workspace.data_ptr()
+    a.workspace_bytes = 0 if workspace is None else workspace.numel()
+    fn = {"all": "harts_kda_bwd", "state": "harts_kda_bwd_state", "grad": "harts_kda_bwd_grad",
+          "static": "harts_kda_bwd_static"}[phase]
     L.check(getattr(L.lib(), fn)(plan.handle, ctypes.byref(a), _stream(stream)), fn)
     if dh0 is not None:
         grads["dh0"] = dh0

@@ -1,5 +1,6 @@
 // C ABI entry points that touch the device: plan upload, forward and backward dispatch.
 #include <cstring>
+#include <mutex>
 
 #include "kda_common.cuh"
 
@@ -229,6 +230,61 @@ int harts_kda_bwd_state(const harts_plan *P, const harts_kda_bwd_args *a, harts_
 
 int harts_kda_bwd_grad(const harts_plan *P, const harts_kda_bwd_args *a, harts_stream_t stream) {
     return kda_bwd_phases(P, a, stream, false, true);
+}
+
+}  // extern "C"
+
+// ---- backward without caller-provided device memory ------------------------------------
+// Some callers cannot hand this library any device memory of its own: a plugin running
+// inside a host framework that owns the whole device pool through its own allocator and
+// gives third-party code no allocation hook, or a step loop that must not pay for (or
+// synchronise on) an allocation.  For them the backward pass can run on scratch that the
+// library carries as a file-scope device array, sized once at load time.
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;   // 32 MiB per device
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+std::mutex g_static_mu;
+constexpr int kMaxDevices = 64;
+void *g_static_addr[kMaxDevices] = {};   // device address of the array, per device id
+}  // namespace
+
+extern "C" {
+
+size_t harts_kda_bwd_static_max_bytes(void) { return kStaticScratchBytes; }
+
+int harts_kda_bwd_static(const harts_plan *P, const harts_kda_bwd_args *args, harts_stream_t stream) {
+    if (!args) { set_error("NULL args"); return HARTS_EINVAL; }
+    int rc = check_fwd_args(P, &args->fwd);
+    if (rc) return rc;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) { set_error("device id out of range"); return HARTS_EINVAL; }
+    void *scratch = nullptr;
+    {
+        // First call on this device: look up the array's device address (the host-side
+        // symbol is only a stand-in).  Done with the device current; no allocation.
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (!g_static_addr[dev]) {
+            void *ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+            g_static_addr[dev] = ptr;
+        }
+        scratch = g_static_addr[dev];
+    }
+    const int fam = pick(&args->fwd, P->info.chunk, true);
+    if (fam < 0) { set_error("no backward kernel for this dk/dv/chunk/dtype"); return HARTS_EUNSUPPORTED; }
+    const size_t need = bwd_ws(P, args->fwd.H, args->fwd.dk, fam == 1).total;
+    if (need > kStaticScratchBytes) {
+        set_error("backward needs " + std::to_string(need) + " bytes of scratch; the static scratch holds " +
+                  std::to_string(kStaticScratchBytes) + " (use harts_kda_bwd with a workspace)");
+        return HARTS_ESMALLBUF;
+    }
+    harts_kda_bwd_args a = *args;
+    a.workspace = scratch;
+    a.workspace_bytes = kStaticScratchBytes;
+    return kda_bwd_phases(P, &a, stream, true, true);
 }
 
 }  // extern "C"
