@@ -50,6 +50,28 @@ def dist_env():
     return ws, rank, local
 
 
+def forest_for_rank(workload, rank):
+    """Each rank runs its own seeded forest of the workload (weak scaling: the per-GPU
+    work stays fixed as ranks are added; no data crosses ranks)."""
+    from prefix_shared_chunkwise_gb300.synth import WORKLOAD_ORDER, make_tree
+    seed = WORKLOAD_ORDER.index(workload) + 1000 * rank
+    parent, seg_len = make_tree(workload, seed=seed)
+    return parent, seg_len, seed
+
+
+def reduce_across_ranks(C_local, ms_local, device):
+    """Whole-job compact tokens (sum over ranks) and the slowest rank's step time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return int(C_local), float(ms_local)
+    c = torch.tensor([float(C_local)], dtype=torch.float64, device=device)
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    dist.all_reduce(c, op=dist.ReduceOp.SUM)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return int(round(c.item())), float(t.item())
+
+
 # ---- algorithmic cost model (per step) ---------------------------------------------------
 
 def cost_model(info, H, D, B):
@@ -204,7 +226,7 @@ def run_ours(args):
 
     from prefix_shared_chunkwise_gb300 import _lib, build
     from prefix_shared_chunkwise_gb300.api import Plan, kda_bwd, kda_fwd
-    from prefix_shared_chunkwise_gb300.synth import WORKLOAD_ORDER, WORKLOADS, make_inputs, make_tree
+    from prefix_shared_chunkwise_gb300.synth import WORKLOADS, make_inputs
 
     ws, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -216,8 +238,7 @@ def run_ours(args):
         dist.barrier()
     wl = WORKLOADS[args.workload]
     H, D, B = wl.H, wl.dk, wl.chunk
-    seed = WORKLOAD_ORDER.index(args.workload) + 1000 * rank
-    parent, seg_len = make_tree(args.workload, seed=seed)
+    parent, seg_len, seed = forest_for_rank(args.workload, rank)
     pl = Plan(parent, seg_len, B).upload()
     info = pl.info
     C = info["C"]
@@ -274,12 +295,8 @@ def run_ours(args):
                     ev[i][2].elapsed_time(ev[i][3])] for i in range(K)]).mean(0)
     if pl.device_error() != 0:
         raise RuntimeError("device error during the timed steps")
-    ms = total_ms / K
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = C * ws / (ms / 1e3)
+    C_all, ms = reduce_across_ranks(C, total_ms / K, dev)
+    value = C_all / (ms / 1e3)
 
     # ---- end to end through the public API with host buffers --------------------------
     e2e = None
@@ -311,12 +328,8 @@ def run_ours(args):
             e2e_step()
         a1.record(stream)
         torch.cuda.synchronize()
-        ems = a0.elapsed_time(a1) / K2
-        if ws > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = dict(value=C * ws / (ems / 1e3), unit=UNIT, h2d_bytes_per_step=int(h2d),
+        _, ems = reduce_across_ranks(C, a0.elapsed_time(a1) / K2, dev)
+        e2e = dict(value=round(C_all / (ems / 1e3), 1), unit=UNIT, h2d_bytes_per_step=int(h2d),
                    d2h_bytes_per_step=int(d2h), ms_per_step=round(ems, 3))
         del host_in, host_out, dev_in
 
@@ -364,7 +377,7 @@ def run_ours(args):
                                 R=info["R"], calls=info["n_rounds"], sequences=info["n_seq"],
                                 states=info["n_states"], H=H, dk=D, dv=D, chunk=B,
                                 parallelism=f"dp{ws} (one forest per GPU)",
-                                l2="inputs larger than L2 (each input tensor 2.1 GB)"),
+                                l2=f"inputs larger than L2 (each input tensor {C * H * D * 2 / 1e9:.2f} GB)"),
                     phases_ms={k: round(v, 3) for k, v in phase_ms.items()},
                     gpu_launches=K * (2 * info["n_rounds"] + 1 + (1 if info["n_fold_rows"] else 0)),
                     roofline=roofline, cpu_baseline=cpu, e2e=e2e, clocks=clk)
