@@ -472,6 +472,35 @@ __device__ void stage_beta(uint8_t *words, int *par, const void *beta, const Pla
     }
 }
 
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+
+// Stage rows through a per-chunk table of compact rows (-1: past the sequence end);
+// rows t < zero_below read as zero.
+__device__ void stage_tab(uint8_t *tile, const void *src_, const int *tab, int32_t h, int H,
+                          int zero_below) {
+    const uint8_t *src = static_cast<const uint8_t *>(src_);
+    for (int e = threadIdx.x; e < 64 * 16; e += NT) {
+        const int t = e >> 4, pc = e & 15;
+        const int row = t < zero_below ? -1 : tab[t];
+        const uint8_t *sp = row >= 0 ? src + ((static_cast<int64_t>(row) * H + h) * D * 2 + pc * 16) : src;
+        tc::cp_async16(tile + piece64(t, pc), sp, row >= 0 ? 16u : 0u);
+    }
+}
+
+__device__ void stage_beta_tab(uint8_t *words, int *par, const void *beta, const int *tab,
+                               int32_t h, int H) {
+    for (int t = threadIdx.x; t < 64; t += NT) {
+        const int row = tab[t];
+        const int64_t idx = row >= 0 ? static_cast<int64_t>(row) * H + h : 0;
+        const uint8_t *sp = static_cast<const uint8_t *>(beta) + (idx & ~int64_t(1)) * 2;
+        tc::cp_async4(words + t * 4, sp, row >= 0 ? 4u : 0u);
+        par[t] = static_cast<int>(idx & 1);
+    }
+}
+
 __device__ __forceinline__ float beta_of(const uint8_t *words, const int *par, int t) {
     const uint32_t w = reinterpret_cast<const uint32_t *>(words)[t];
     const uint16_t hb = par[t] ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w & 0xFFFF);
@@ -721,24 +750,10 @@ constexpr uint32_t RV = 139264, RQ = 155648, RK = 172032, RG = 188416, PmS = 204
 constexpr uint32_t SBeta = 221184, SBpar = SBeta + 256, Vec = SBpar + 256;
 // fp32 vectors
 constexpr uint32_t vBeta = Vec, vM = vBeta + 256, vEm = vM + 512, vEkt = vEm + 512, vEl = vEkt + 512,
-                   vT0 = vEl + 512, vT1 = vT0 + 512, vDel = vT1 + 512, vDgl = vDel + 1024,
-                   vTot = vDgl + 1024, rZY = vTot + 512, rMA = rZY + 1024, vEnd = rMA + 512;
+                   vT0 = vEl + 512, vT1 = vT0 + 512, vDel = vT1 + 512, vDgl = vDel + 2048,
+                   vTot = vDgl + 1024, rZY = vTot + 512, rMA = rZY + 256, vEnd = rMA + 512;
 constexpr uint32_t bytes = vEnd + 1024;
 }  // namespace bwg_sm
-
-// Warp-reduce 32 per-lane values (one per column t) and write the warp sums.
-__device__ __forceinline__ void warp_col_sums(float (&x)[32], float *out) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        float v = x[j];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        x[j] = v;
-    }
-    if ((threadIdx.x & 31) == 0)
-#pragma unroll
-        for (int j = 0; j < 32; ++j) out[j] = x[j];
-}
 
 __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd, int32_t chunk_begin) {
     using namespace bwg_sm;
@@ -747,6 +762,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
     __shared__ uint64_t bars[6];
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
+    __shared__ int s_rows[64];
     float *vbeta = reinterpret_cast<float *>(sm + vBeta), *vm = reinterpret_cast<float *>(sm + vM),
           *vem = reinterpret_cast<float *>(sm + vEm), *vekt = reinterpret_cast<float *>(sm + vEkt),
           *vel = reinterpret_cast<float *>(sm + vEl), *vt0 = reinterpret_cast<float *>(sm + vT0),
@@ -767,12 +783,23 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
     const int32_t row0 = pd.seq_row0[seq], rptr = pd.seq_rptr[seq];
     const uint8_t *rec = static_cast<const uint8_t *>(f.chunk_states) + (static_cast<int64_t>(g) * H + h) * kRecBytes;
     const uint8_t *dcs = static_cast<const uint8_t *>(p.dchunk) + (static_cast<int64_t>(g) * H + h) * D * D * 2;
-    __nv_bfloat16 *gdq = static_cast<__nv_bfloat16 *>(p.dq), *gdk = static_cast<__nv_bfloat16 *>(p.dk),
-                  *gdv = static_cast<__nv_bfloat16 *>(p.dv), *gdg = static_cast<__nv_bfloat16 *>(p.dg),
-                  *gdb = static_cast<__nv_bfloat16 *>(p.dbeta);
     const int W = 3 * D + 1;
+    // local rows [t_own, t_end) of this chunk are own rows of the sequence
+    const int t_own = max(0, rho - c0), t_end = nv;
 
-    // ---- stage everything the chunk needs ------------------------------------------------
+    if (tid < 64) s_rows[tid] = static_cast<int>(local_row(pd, seq, rho, L, c0 + tid));
+    if (tid == 0) {
+        for (int i = 0; i < 6; ++i) tc::mbar_init(&bars[i], 1);
+        s_fail = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
+    __syncthreads();
+    // ---- staging in three groups, waited for in the order they are used -------------------
+    stage_tab(sm + RQ, f.q, s_rows, h, H, 0);
+    stage_tab(sm + RK, f.k, s_rows, h, H, 0);
+    stage_tab(sm + RG, f.g, s_rows, h, H, 0);
+    stage_beta_tab(sm + SBeta, spar, f.beta, s_rows, h, H);
+    tc::cp_async_commit();
     for (int e = tid; e < 128 * 16; e += NT) {
         const int r = e >> 4, pc = e & 15;
         tc::cp_async16(sm + SemT + piece128(r, pc), rec + r * 256 + pc * 16, 16u);
@@ -782,20 +809,10 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         const int t = e >> 3, pc = e & 7;
         tc::cp_async16(sm + Tm + t * 128 + ((pc ^ (t & 7)) << 4), rec + D * D * 2 + t * 128 + pc * 16, 16u);
     }
-    stage_rows(sm + RQ, f.q, pd, seq, h, H, rho, L, c0, false);
-    stage_rows(sm + RK, f.k, pd, seq, h, H, rho, L, c0, false);
-    stage_rows(sm + RV, f.v, pd, seq, h, H, rho, L, c0, false);
-    stage_rows(sm + RG, f.g, pd, seq, h, H, rho, L, c0, false);
-    stage_rows(sm + dOm, p.d_o, pd, seq, h, H, rho, L, c0, true);
-    stage_beta(sm + SBeta, spar, f.beta, pd, seq, h, H, rho, L, c0);
     tc::cp_async_commit();
-    if (tid == 0) {
-        for (int i = 0; i < 6; ++i) tc::mbar_init(&bars[i], 1);
-        s_fail = 0;
-    }
-    if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
-    tc::cp_async_wait_all();
-    __syncthreads();
+    stage_tab(sm + RV, f.v, s_rows, h, H, 0);
+    stage_tab(sm + dOm, p.d_o, s_rows, h, H, t_own);
+    tc::cp_async_commit();
     tc::fence_after_sync();
     const uint32_t tm = s_tmem;
     const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
@@ -804,14 +821,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
     const int jv = lg * 32 + lane;
     const int c = tid & 127, half = tid >> 7;
 
-    // ---- d(e^{Gamma_L}) part from the state: d_el = sum_dv S . dS' (before scaling) ------
-    {
-        float acc = 0.f;
-        for (int r = half * 64; r < half * 64 + 64; ++r)
-            acc += sw_val(sm + SemT, 128, r, c) * sw_val(sm + dSekT, 128, r, c);
-        vdel[half * 128 + c] = acc;
-    }
     // ---- prep: Gamma (kept in TMEM, lane = key channel), Kp, Qp, Km --------------------
+    cp_async_wait_group<2>();
+    __syncthreads();
     gamma_pass1(sm + RG, c, half, mid, vt0, vt1, vm);
     if (tid < 64) vbeta[tid] = beta_of(sm + SBeta, spar, tid);
     __syncthreads();
@@ -821,7 +833,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         if (-m > kMaxExpArg || m - gl > kMaxExpArg) dev_error(pd, kDevErrDecayRange, seq, c0);
         if (half == 0) { vem[c] = __expf(m); vekt[c] = __expf(gl - m); vel[c] = __expf(gl); }
         float gv[32];
-#pragma unroll 4
+#pragma unroll
         for (int u = 0; u < 32; ++u) {
             const int t = half * 32 + u;
             const float kk = sw_val(sm + RK, 64, t, c), qq = sw_val(sm + RQ, 64, t, c) * f.scale;
@@ -833,6 +845,23 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
             st_bf16(sm + Km, 64, t, c, kk * e2);
         }
         tc::tmem_st32(tGam + lane_off + half * 32, gv);   // thread (c, half) sits in lane c
+    }
+    // ---- d_el = sum_dv S . dS' per key channel (before scaling), two channels per thread --
+    cp_async_wait_group<1>();
+    __syncthreads();
+    {
+        const int pr = tid & 63, qr = tid >> 6;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+        for (int r = qr * 32; r < qr * 32 + 32; ++r) {
+            const uint32_t off = tc::sw128_offset(128, r, 2 * pr);
+            const float2 sv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm + SemT + off));
+            const float2 dv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm + dSekT + off));
+            a0 += sv.x * dv.x;
+            a1 += sv.y * dv.y;
+        }
+        vdel[qr * 128 + 2 * pr] = a0;
+        vdel[qr * 128 + 2 * pr + 1] = a1;
     }
     __syncthreads();
     // S^T columns * e^{m}, dS'^T columns * e^{Gamma_L - m}, T columns * beta
@@ -871,6 +900,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         w.z = tc::pack_bf16(v[4], v[5]); w.w = tc::pack_bf16(v[6], v[7]);
         *reinterpret_cast<uint4 *>(sm + TBm + off) = w;
     }
+    cp_async_wait_group<0>();
     sync_for_mma();
     if (tid == 0) {
         tc::mma_tile(tAP, tc::smem_addr(sm + KQp), 16384, tc::smem_addr(sm + Km), 8192, 128,
@@ -892,11 +922,10 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
 #pragma unroll
             for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + PmS, 64, t, ch * 32 + j, r + j);
         }
-        // Y^T = V^T - X^T -> YT [dv][t] (in RQ)
+        // Y^T = V^T - X^T -> YT [dv][t] (in RQ; raw q was last read in the prep)
         tc::tmem_ld32(tS1 + lane_off + ch * 32, r);
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = sw_val(sm + RV, 64, ch * 32 + j, jv) - r[j];
-        __syncthreads();   // raw q (RQ) no longer read by anyone
 #pragma unroll
         for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RQ, 128, jv, ch * 32 + j, r + j);
     }
@@ -940,25 +969,21 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
     }
     if (!wait_all(&bars[2], 0, &s_fail)) goto done;
     {
-        float r[32], y[32];
-        // Z^T: dv output, unscaled Z^T tile (RG), sum_dv Z Y per row
+        float r[32];
+        // Z^T: dv = beta Z staged [t][dv] in RV (U^T is consumed); replay rows go to the
+        // replay-gradient buffer; unscaled Z^T tile in RG
         tc::tmem_ld32(tS1 + lane_off + ch * 32, r);
+        __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + RV);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) y[j] = r[j] * sw_val(sm + RQ, 128, jv, ch * 32 + j);
         for (int j = 0; j < 32; ++j) {
-            const int32_t lr = c0 + ch * 32 + j;
-            if (lr >= L) break;
-            const float x = vbeta[ch * 32 + j] * r[j];
-            if (lr >= rho) {
-                const int64_t row = static_cast<int64_t>(row0) + (lr - rho);
-                gdv[(row * H + h) * D + jv] = __float2bfloat16_rn(x);
-            } else {
-                p.rep_grad[(static_cast<int64_t>(rptr + lr) * H + h) * W + D + jv] = x;
-            }
+            const int t = ch * 32 + j;
+            const float x = vbeta[t] * r[j];
+            dvs[t * D + jv] = __float2bfloat16_rn(x);
+            if (t < t_own && t < t_end)
+                p.rep_grad[(static_cast<int64_t>(rptr + c0 + t) * H + h) * W + D + jv] = x;
         }
 #pragma unroll
         for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RG, 128, jv, ch * 32 + j, r + j);
-        warp_col_sums(y, rzy + lg * 64 + ch * 32);
         // dP -> PmS (incl lower)
         tc::tmem_ld32(tS2 + lane_off + ch * 32, r);
         if (lg < 2) {
@@ -989,7 +1014,18 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         // W = dT T^T (padding rows)
         tc::mma_op(tS1, tc::Opnd{tc::smem_addr(sm + RK), 8192, false},
                    tc::Opnd{tc::smem_addr(sm + Tm), 8192, false}, 128, 64, 64, false);
+        // diag(Z Y^T) = sum_dv Z (V - Kd S) per row, for dbeta (padding rows)
+        tc::mma_op(tS2, tc::Opnd{tc::smem_addr(sm + RG), 16384, true},
+                   tc::Opnd{tc::smem_addr(sm + RQ), 16384, true}, 128, 64, 128, false);
         tc::mma_commit(&bars[3]);
+    }
+    // own rows of dv, coalesced, while the MMAs run
+    for (int e = tid; e < 64 * 16; e += NT) {
+        const int t = e >> 4, pc = e & 15;
+        if (t < t_own || t >= t_end) continue;
+        const int64_t row = static_cast<int64_t>(row0) + (c0 + t - rho);
+        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dv) + (row * H + h) * D + pc * 8) =
+            *reinterpret_cast<const uint4 *>(sm + RV + t * 256 + pc * 16);
     }
     if (!wait_all(&bars[3], 0, &s_fail)) goto done;
     {
@@ -998,6 +1034,13 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         if (lg < 2) {
 #pragma unroll
             for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RQ, 64, jv, ch * 32 + j, r + j);  // Wm
+        }
+        tc::tmem_ld32(tS2 + lane_off + ch * 32, r);
+        if (lg < 2 && (jv >> 5) == ch) {
+            float d = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) d = (j == (jv & 31)) ? r[j] : d;
+            rzy[jv] = d;
         }
     }
     sync_for_mma();
@@ -1050,7 +1093,11 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
     }
     if (!wait_all(&bars[5], 0, &s_fail)) goto done;
     {
-        // thread: key channel dk = jv, rows t = 32 ch .. 32 ch + 31
+        // thread: key channel dk = jv, rows t = 32 ch .. 32 ch + 31.  dq, dk, dg are staged
+        // [t][dk] (dq, dk over S^T, dg over dS'^T: both consumed) for coalesced stores.
+        __nv_bfloat16 *dqs = reinterpret_cast<__nv_bfloat16 *>(sm + SemT);
+        __nv_bfloat16 *dks = reinterpret_cast<__nv_bfloat16 *>(sm + SemT + 16384);
+        __nv_bfloat16 *dgs = reinterpret_cast<__nv_bfloat16 *>(sm + dSekT);
         const int dk = jv;
         const float m = vm[dk];
         for (int hc = 0; hc < 2; ++hc) {
@@ -1076,18 +1123,12 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
                 const float dqv = xq[u] * ep * f.scale;
                 const float dkv = xp * ep + xm[u] * en;
                 dgm[u] = xq[u] * qp + xp * kp - xm[u] * km;
-                const int32_t lr = c0 + t;
-                if (lr < L) {
-                    if (lr >= rho) {
-                        const int64_t o = ((static_cast<int64_t>(row0) + (lr - rho)) * H + h) * D + dk;
-                        gdq[o] = __float2bfloat16_rn(dqv);
-                        gdk[o] = __float2bfloat16_rn(dkv);
-                    } else {
-                        p.rep_grad[(static_cast<int64_t>(rptr + lr) * H + h) * W + dk] = dkv;
-                    }
-                }
+                dqs[t * D + dk] = __float2bfloat16_rn(dqv);
+                dks[t * D + dk] = __float2bfloat16_rn(dkv);
+                if (t < t_own && t < t_end)
+                    p.rep_grad[(static_cast<int64_t>(rptr + c0 + t) * H + h) * W + dk] = dkv;
             }
-            // keep dGamma in registers of this pass through TMEM (reuse the Gamma columns)
+            // keep dGamma through TMEM (reuse the Gamma columns)
             {
                 uint32_t *uu = reinterpret_cast<uint32_t *>(dgm);
                 asm volatile(
@@ -1108,29 +1149,39 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         for (int j = 31; j >= 0; --j) { run += dg[j]; dg[j] = run; }
         if (ch == 1) vtot[dk] = run;
         __syncthreads();
-        const float dgl = vdgl[dk] + vdgl[128 + dk] + (vdel[dk] + vdel[128 + dk]) * vel[dk];
+        const float dgl = vdgl[dk] + vdgl[128 + dk] +
+                          (vdel[dk] + vdel[128 + dk] + vdel[256 + dk] + vdel[384 + dk]) * vel[dk];
         const float off = (ch == 0 ? vtot[dk] : 0.f) + dgl;
+#pragma unroll
         for (int j = 0; j < 32; ++j) {
-            const int32_t lr = c0 + ch * 32 + j;
-            if (lr >= L) break;
+            const int t = ch * 32 + j;
             const float x = dg[j] + off;
-            if (lr >= rho) {
-                gdg[((static_cast<int64_t>(row0) + (lr - rho)) * H + h) * D + dk] = __float2bfloat16_rn(x);
-            } else {
-                p.rep_grad[(static_cast<int64_t>(rptr + lr) * H + h) * W + 2 * D + dk] = x;
-            }
+            dgs[t * D + dk] = __float2bfloat16_rn(x);
+            if (t < t_own && t < t_end)
+                p.rep_grad[(static_cast<int64_t>(rptr + c0 + t) * H + h) * W + 2 * D + dk] = x;
         }
     }
     __syncthreads();
+    for (int e = tid; e < 3 * 64 * 16; e += NT) {
+        const int which = e >> 10, t = (e >> 4) & 63, pc = e & 15;
+        if (t < t_own || t >= t_end) continue;
+        const int64_t row = static_cast<int64_t>(row0) + (c0 + t - rho);
+        void *dst = which == 0 ? p.dq : (which == 1 ? p.dk : p.dg);
+        const uint8_t *srcp = which == 2 ? sm + dSekT : sm + SemT + which * 16384;
+        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(dst) + (row * H + h) * D + pc * 8) =
+            *reinterpret_cast<const uint4 *>(srcp + t * 256 + pc * 16);
+    }
     if (tid < 64) {
         const int t = tid;
-        const int32_t lr = c0 + t;
         // dbeta = sum_dv Z (V - Kd S) + sum_s dM A   (the first sum holds both the beta V
         // and the beta Kd paths of W = T diag(beta) [Kd | V])
-        const float db = rzy[t] + rzy[64 + t] + rzy[128 + t] + rzy[192 + t] + rma[t] + rma[64 + t];
-        if (lr < L) {
-            if (lr >= rho) gdb[(static_cast<int64_t>(row0) + (lr - rho)) * H + h] = __float2bfloat16_rn(db);
-            else p.rep_grad[(static_cast<int64_t>(rptr + lr) * H + h) * W + 3 * D] = db;
+        const float db = rzy[t] + rma[t] + rma[64 + t];
+        if (t < t_end) {
+            if (t >= t_own)
+                static_cast<__nv_bfloat16 *>(p.dbeta)[(static_cast<int64_t>(row0) + (c0 + t - rho)) * H + h] =
+                    __float2bfloat16_rn(db);
+            else
+                p.rep_grad[(static_cast<int64_t>(rptr + c0 + t) * H + h) * W + 3 * D] = db;
         }
     }
 done:
