@@ -523,7 +523,8 @@ namespace bws_sm {
 constexpr uint32_t RawQ = 0, RawK = 16384, RawG = 32768, dOm = 49152;
 constexpr uint32_t Qpm = 65536, Km = 81920, Kdm = 98304, Qdm = 114688;
 constexpr uint32_t Pm = 131072, Tm = 139264, dSTs = 147456, dUTs = 180224;
-constexpr uint32_t SBeta = 196608, SBpar = SBeta + 256, Vec = SBpar + 256;
+constexpr uint32_t dOm2 = 196608, Tm2 = 212992;          // second buffers (prefetch)
+constexpr uint32_t SBeta = 221184, SBpar = SBeta + 256, Vec = SBpar + 256;
 constexpr uint32_t vBeta = Vec, vEl = vBeta + 256, vEkt = vEl + 512, vM = vEkt + 512,
                    vT0 = vM + 512, vT1 = vT0 + 512, vEnd = vT1 + 512;
 constexpr uint32_t bytes = vEnd + 1024;
@@ -536,6 +537,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
     __shared__ uint64_t bars[4];
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
+    __shared__ int s_rows[64];
     float *vbeta = reinterpret_cast<float *>(sm + vBeta), *vel = reinterpret_cast<float *>(sm + vEl),
           *vekt = reinterpret_cast<float *>(sm + vEkt), *vm = reinterpret_cast<float *>(sm + vM),
           *vt0 = reinterpret_cast<float *>(sm + vT0), *vt1 = reinterpret_cast<float *>(sm + vT1);
@@ -579,25 +581,31 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
     const int32_t sp_begin = pd.seq_sptr[seq];
     int32_t sp = pd.seq_sptr[seq + 1] - 1;
     const int c = tid & 127, half = tid >> 7;
+    // Stage chunk cj's raw q, k, g, beta and (into buffer `b`) dO and the forward's T.
+    auto stage_chunk = [&](int32_t cj, int b) {
+        const int32_t cc0 = cj * BC;
+        if (tid < 64) s_rows[tid] = static_cast<int>(local_row(pd, seq, rho, L, cc0 + tid));
+        __syncthreads();
+        stage_tab(sm + RawQ, f.q, s_rows, h, H, 0);
+        stage_tab(sm + RawK, f.k, s_rows, h, H, 0);
+        stage_tab(sm + RawG, f.g, s_rows, h, H, 0);
+        stage_tab(sm + (b ? dOm2 : dOm), p.d_o, s_rows, h, H, max(0, rho - cc0));
+        stage_beta_tab(sm + SBeta, spar, f.beta, s_rows, h, H);
+        const uint8_t *rt = rec0 + (static_cast<int64_t>(cbase + cj) * H + h) * kRecBytes + D * D * 2;
+        for (int e = tid; e < 64 * 8; e += NT) {
+            const int t = e >> 3, pc = e & 7;
+            tc::cp_async16(sm + (b ? Tm2 : Tm) + t * 128 + ((pc ^ (t & 7)) << 4), rt + t * 128 + pc * 16, 16u);
+        }
+        tc::cp_async_commit();
+    };
+    stage_chunk(nch - 1, 0);
     for (int32_t ci = nch - 1; ci >= 0; --ci) {
         const uint32_t ph = (nch - 1 - ci) & 1;
         const int32_t c0 = ci * BC, pend = c0 + BC, g = cbase + ci;
         const int nv = min(BC, L - c0);
         const int mid = (nv - 1) / 2;
-        // ---- stage inputs and the forward's T ------------------------------------------
-        stage_rows(sm + RawQ, f.q, pd, seq, h, H, rho, L, c0, false);
-        stage_rows(sm + RawK, f.k, pd, seq, h, H, rho, L, c0, false);
-        stage_rows(sm + RawG, f.g, pd, seq, h, H, rho, L, c0, false);
-        stage_rows(sm + dOm, p.d_o, pd, seq, h, H, rho, L, c0, true);
-        stage_beta(sm + SBeta, spar, f.beta, pd, seq, h, H, rho, L, c0);
-        {
-            const uint8_t *rt = rec0 + (static_cast<int64_t>(g) * H + h) * kRecBytes + D * D * 2;
-            for (int e = tid; e < 64 * 8; e += NT) {
-                const int t = e >> 3, pc = e & 7;
-                tc::cp_async16(sm + Tm + t * 128 + ((pc ^ (t & 7)) << 4), rt + t * 128 + pc * 16, 16u);
-            }
-        }
-        tc::cp_async_commit();
+        const int buf = (nch - 1 - ci) & 1;
+        const uint32_t dOc = buf ? dOm2 : dOm, Tc = buf ? Tm2 : Tm;
         // ---- consumers of the boundary state at this chunk's end add their gradients ----
         if (sp >= sp_begin && pd.state_lpos[sp] == pend) {
             const int32_t cb_ = pd.state_cptr[sp], ce_ = pd.state_cptr[sp + 1];
@@ -653,6 +661,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
             }
         }
         sync_for_mma();
+        // raw q, k, g, beta are consumed: prefetch the previous chunk while this one runs
+        if (ci > 0) stage_chunk(ci - 1, buf ^ 1);
         if (tid == 0) {
             tc::mma_tile(tP, tc::smem_addr(sm + Qpm), 8192, tc::smem_addr(sm + Km), 8192, 128,
                          tc::idesc_bf16(64, 64), false);
@@ -685,7 +695,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
         }
         sync_for_mma();
         if (tid == 0) {
-            tc::mma_op(tUT, tc::Opnd{tc::smem_addr(sm + dOm), 8192, true},
+            tc::mma_op(tUT, tc::Opnd{tc::smem_addr(sm + dOc), 8192, true},
                        tc::Opnd{tc::smem_addr(sm + Pm), 8192, true}, 128, 64, 64, false);
             tc::mma_op(tUT, tc::Opnd{tc::smem_addr(sm + dSTs), 16384, false},
                        tc::Opnd{tc::smem_addr(sm + Km), 8192, false}, 128, 64, 128, true);
@@ -701,7 +711,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
         sync_for_mma();
         if (tid == 0) {
             tc::mma_op(tZT, tc::Opnd{tc::smem_addr(sm + dUTs), 16384, false},
-                       tc::Opnd{tc::smem_addr(sm + Tm), 8192, true}, 128, 64, 64, false);
+                       tc::Opnd{tc::smem_addr(sm + Tc), 8192, true}, 128, 64, 64, false);
             tc::mma_commit(&bars[2]);
         }
         if (!wait_all(&bars[2], ph, &s_fail)) break;
@@ -715,7 +725,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
         }
         sync_for_mma();
         if (tid == 0) {
-            tc::mma_op(tST, tc::Opnd{tc::smem_addr(sm + dOm), 8192, true},
+            tc::mma_op(tST, tc::Opnd{tc::smem_addr(sm + dOc), 8192, true},
                        tc::Opnd{tc::smem_addr(sm + Qdm), 8192, true}, 128, 128, 64, true);
             tc::mma_op(tST, tc::Opnd{tc::smem_addr(sm + dUTs), 16384, false},
                        tc::Opnd{tc::smem_addr(sm + Kdm), 8192, true}, 128, 128, 64, true);
