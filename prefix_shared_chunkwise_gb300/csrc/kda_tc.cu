@@ -447,31 +447,6 @@ __device__ __forceinline__ float sw_val(const uint8_t *tile, int rows, int r, in
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + tc::sw128_offset(rows, r, c)));
 }
 
-// Stage one chunk's rows of a token-major [C,H,128] bf16 tensor into a SW128 [64][128]
-// tile (rows past the sequence end and, if own_only, replay rows read as zero).
-__device__ void stage_rows(uint8_t *tile, const void *src_, const PlanDev &pd, int32_t seq,
-                           int32_t h, int H, int32_t rho, int32_t L, int32_t c0, bool own_only) {
-    const uint8_t *src = static_cast<const uint8_t *>(src_);
-    for (int e = threadIdx.x; e < 64 * 16; e += NT) {
-        const int t = e >> 4, p = e & 15;
-        int64_t row = local_row(pd, seq, rho, L, c0 + t);
-        if (own_only && c0 + t < rho) row = -1;
-        const uint8_t *s = row >= 0 ? src + ((row * H + h) * D * 2 + p * 16) : src;
-        tc::cp_async16(tile + piece64(t, p), s, row >= 0 ? 16u : 0u);
-    }
-}
-
-__device__ void stage_beta(uint8_t *words, int *par, const void *beta, const PlanDev &pd,
-                           int32_t seq, int32_t h, int H, int32_t rho, int32_t L, int32_t c0) {
-    for (int t = threadIdx.x; t < 64; t += NT) {
-        const int64_t row = local_row(pd, seq, rho, L, c0 + t);
-        const int64_t idx = row >= 0 ? row * H + h : 0;
-        const uint8_t *s = static_cast<const uint8_t *>(beta) + (idx & ~int64_t(1)) * 2;
-        tc::cp_async4(words + t * 4, s, row >= 0 ? 4u : 0u);
-        par[t] = static_cast<int>(idx & 1);
-    }
-}
-
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() {
     asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
