@@ -48,7 +48,7 @@ constexpr uint32_t SBeta = Stage + 65536;   // [64] 32-bit words holding the bf1
 constexpr uint32_t SBpar = SBeta + 256;     // [64] int: which half of the word
 constexpr uint32_t Vec = SBpar + 256;       // fp32 vectors
 constexpr uint32_t vBeta = Vec, vEl = vBeta + 64 * 4, vT0 = vEl + 128 * 4, vT1 = vT0 + 128 * 4,
-                   vM = vT1 + 128 * 4, vEnd = vM + 128 * 4;
+                   vM = vT1 + 128 * 4, vPart = vM + 128 * 4, vEnd = vPart + 4 * 128 * 4;
 constexpr uint32_t bytes = vEnd + 1024;     // + alignment slack
 }  // namespace fwd_sm
 
@@ -124,22 +124,24 @@ __device__ __forceinline__ void sync_for_mma() {
 }
 
 // Issue asynchronous copies of one chunk's raw q, k, v, g rows (256 B each) and beta
-// into the staging buffer; rows past the sequence end are zero-filled.
+// into the staging buffer; rows past the sequence end are zero-filled.  `tab` receives
+// the chunk's compact rows (-1 past the end); all threads call this.
 __device__ void prefetch_chunk(const FwdParams &p, const PlanDev &pd, int32_t seq, int32_t h,
-                               int32_t rho, int32_t L, int32_t c0, uint8_t *sm) {
+                               int32_t rho, int32_t L, int32_t c0, uint8_t *sm, int *tab) {
     using namespace fwd_sm;
     const int H = p.H;
-    const uint8_t *base[4] = {static_cast<const uint8_t *>(p.q), static_cast<const uint8_t *>(p.k),
-                              static_cast<const uint8_t *>(p.v), static_cast<const uint8_t *>(p.g)};
+    if (threadIdx.x < 64) tab[threadIdx.x] = static_cast<int>(local_row(pd, seq, rho, L, c0 + threadIdx.x));
+    __syncthreads();
     for (int e = threadIdx.x; e < 64 * 16 * 4; e += NT) {
         const int ten = e >> 10, t = (e >> 4) & 63, piece = e & 15;
-        const int64_t row = local_row(pd, seq, rho, L, c0 + t);
-        const uint8_t *src = row >= 0 ? base[ten] + ((row * H + h) * D * 2 + piece * 16) : base[ten];
+        const uint8_t *base = static_cast<const uint8_t *>(ten == 0 ? p.q : ten == 1 ? p.k : ten == 2 ? p.v : p.g);
+        const int row = tab[t];
+        const uint8_t *src = row >= 0 ? base + ((static_cast<int64_t>(row) * H + h) * D * 2 + piece * 16) : base;
         tc::cp_async16(sm + Stage + ten * 16384 + t * 256 + piece * 16, src, row >= 0 ? 16u : 0u);
     }
     for (int t = threadIdx.x; t < 64; t += NT) {
-        const int64_t row = local_row(pd, seq, rho, L, c0 + t);
-        const int64_t idx = row >= 0 ? row * H + h : 0;
+        const int row = tab[t];
+        const int64_t idx = row >= 0 ? static_cast<int64_t>(row) * H + h : 0;
         const uint8_t *src = static_cast<const uint8_t *>(p.beta) + (idx & ~int64_t(1)) * 2;
         tc::cp_async4(sm + SBeta + t * 4, src, row >= 0 ? 4u : 0u);
         reinterpret_cast<int *>(sm + SBpar)[t] = static_cast<int>(idx & 1);
@@ -147,8 +149,13 @@ __device__ void prefetch_chunk(const FwdParams &p, const PlanDev &pd, int32_t se
     tc::cp_async_commit();
 }
 
-__device__ __forceinline__ float stage_val(const uint8_t *sm, uint32_t off, int t, int c) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + off + t * 256 + c * 2));
+__device__ __forceinline__ float2 stage2(const uint8_t *sm, uint32_t off, int t, int c) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm + off + t * 256 + c * 2));
+}
+
+// Two adjacent columns (col even) of one row of a SW128 tile, packed into one 4-byte store.
+__device__ __forceinline__ void st_bf16x2(uint8_t *tile, int rows, int row, int col, float a, float b) {
+    *reinterpret_cast<uint32_t *>(tile + tc::sw128_offset(rows, row, col)) = tc::pack_bf16(a, b);
 }
 
 __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int32_t round_base) {
@@ -158,9 +165,9 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
     __shared__ uint64_t bars[4];
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
+    __shared__ int s_rows[64];
     float *vbeta = reinterpret_cast<float *>(sm + vBeta), *vel = reinterpret_cast<float *>(sm + vEl),
-          *vt0 = reinterpret_cast<float *>(sm + vT0), *vt1 = reinterpret_cast<float *>(sm + vT1),
-          *vm = reinterpret_cast<float *>(sm + vM);
+          *vm = reinterpret_cast<float *>(sm + vM), *vpart = reinterpret_cast<float *>(sm + vPart);
     float *Mfp = reinterpret_cast<float *>(sm + Mf), *Tfp = reinterpret_cast<float *>(sm + Tf);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, ch = warp >> 2;
@@ -174,13 +181,12 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
     uint8_t *cst = static_cast<uint8_t *>(p.chunk_states);
 
-    prefetch_chunk(p, pd, seq, h, rho, L, 0, sm);
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) tc::mbar_init(&bars[i], 1);
         s_fail = 0;
     }
     if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
-    __syncthreads();
+    prefetch_chunk(p, pd, seq, h, rho, L, 0, sm, s_rows);
     tc::fence_after_sync();
     const uint32_t tm = s_tmem;
     const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
@@ -218,7 +224,6 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
 
     int32_t sp = pd.seq_sptr[seq];
     const int32_t sp_end = pd.seq_sptr[seq + 1];
-    const int c = tid & 127, half = tid >> 7;
     for (int32_t ci = 0; ci < nch; ++ci) {
         const uint32_t ph = ci & 1;
         const int32_t c0 = ci * BC;
@@ -227,14 +232,19 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
         tc::cp_async_wait_all();
         __syncthreads();
         // ---- prep: cumulative decay, scaled operands (from the staged raw tiles) ----------
+        // thread: key channels c2, c2 + 1; rows 16 qr .. 16 qr + 15
         {
-            float s = 0.f, mref = 0.f;
-#pragma unroll 8
-            for (int t = half * 32; t < half * 32 + 32; ++t) {
-                s += stage_val(sm, SG, t, c);
-                if (t == mid) mref = s;
+            const int cp = tid & 63, qr = tid >> 6, c2 = 2 * cp, qmid = mid >> 4;
+            float s0 = 0.f, s1 = 0.f, ml0 = 0.f, ml1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int t = qr * 16 + u;
+                const float2 gg = stage2(sm, SG, t, c2);
+                s0 += gg.x; s1 += gg.y;
+                if (t == mid) { ml0 = s0; ml1 = s1; }
             }
-            if (half == 0) { vt0[c] = s; vm[c] = mref; } else vt1[c] = s;
+            vpart[qr * 128 + c2] = s0; vpart[qr * 128 + c2 + 1] = s1;
+            if (qr == qmid) { vm[c2] = ml0; vm[c2 + 1] = ml1; }
             if (tid < 64) {
                 const uint32_t w = reinterpret_cast<const uint32_t *>(sm + SBeta)[tid];
                 const int par = reinterpret_cast<const int *>(sm + SBpar)[tid];
@@ -242,36 +252,56 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
                 vbeta[tid] = __bfloat162float(__ushort_as_bfloat16(hb));
             }
             __syncthreads();
-            const float m = vm[c], gl = vt0[c] + vt1[c];
-            float gam = half ? vt0[c] : 0.f;
-            if (-m > kMaxExpArg || m - gl > kMaxExpArg) dev_error(pd, kDevErrDecayRange, seq, c0);
-            const float em = __expf(m), ekt = __expf(gl - m);
-            if (half == 0) vel[c] = __expf(gl);
-            for (int t0 = half * 32; t0 < half * 32 + 32; t0 += 8) {
-                float bkd[8], bv[8], kt[8];
+            float gam0 = 0.f, gam1 = 0.f, m0 = vm[c2], m1 = vm[c2 + 1], gl0 = 0.f, gl1 = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float p0 = vpart[q * 128 + c2], p1 = vpart[q * 128 + c2 + 1];
+                if (q < qr) { gam0 += p0; gam1 += p1; }
+                if (q < qmid) { m0 += p0; m1 += p1; }
+                gl0 += p0; gl1 += p1;
+            }
+            if (-m0 > kMaxExpArg || m0 - gl0 > kMaxExpArg || -m1 > kMaxExpArg || m1 - gl1 > kMaxExpArg)
+                dev_error(pd, kDevErrDecayRange, seq, c0);
+            const float em0 = __expf(m0), ekt0 = __expf(gl0 - m0), em1 = __expf(m1), ekt1 = __expf(gl1 - m1);
+            if (qr == 0) { vel[c2] = __expf(gl0); vel[c2 + 1] = __expf(gl1); }
+            const bool lo = lane < 16;    // half-warps store even / odd rows of the transposed tiles
+#pragma unroll
+            for (int grp = 0; grp < 2; ++grp) {
+                const int t0 = qr * 16 + grp * 8;
+                float bkd0[8], bkd1[8], bv0[8], bv1[8], kt0[8], kt1[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int t = t0 + u;
-                    const float kk = stage_val(sm, SK, t, c), qq = stage_val(sm, SQ, t, c) * p.scale,
-                                vv = stage_val(sm, SV, t, c), bb = vbeta[t];
-                    gam += stage_val(sm, SG, t, c);
-                    const float e1 = __expf(gam - m), e2 = __expf(m - gam);
-                    st_bf16(sm + KQp, 128, t, c, kk * e1);
-                    st_bf16(sm + KQp, 128, 64 + t, c, qq * e1);
-                    st_bf16(sm + Km, 64, t, c, kk * e2);
-                    st_bf16(sm + Qd, 64, t, c, qq * e1 * em);
-                    bkd[u] = bb * kk * e1 * em;
-                    bv[u] = bb * vv;
-                    kt[u] = kk * e2 * ekt;
+                    const float2 kk = stage2(sm, SK, t, c2), qv = stage2(sm, SQ, t, c2),
+                                 vv = stage2(sm, SV, t, c2), gg = stage2(sm, SG, t, c2);
+                    const float bb = vbeta[t], q0 = qv.x * p.scale, q1 = qv.y * p.scale;
+                    gam0 += gg.x; gam1 += gg.y;
+                    const float e10 = __expf(gam0 - m0), e20 = __expf(m0 - gam0);
+                    const float e11 = __expf(gam1 - m1), e21 = __expf(m1 - gam1);
+                    st_bf16x2(sm + KQp, 128, t, c2, kk.x * e10, kk.y * e11);
+                    st_bf16x2(sm + KQp, 128, 64 + t, c2, q0 * e10, q1 * e11);
+                    st_bf16x2(sm + Km, 64, t, c2, kk.x * e20, kk.y * e21);
+                    st_bf16x2(sm + Qd, 64, t, c2, q0 * e10 * em0, q1 * e11 * em1);
+                    bkd0[u] = bb * kk.x * e10 * em0; bkd1[u] = bb * kk.y * e11 * em1;
+                    bv0[u] = bb * vv.x; bv1[u] = bb * vv.y;
+                    kt0[u] = kk.x * e20 * ekt0; kt1[u] = kk.y * e21 * ekt1;
                 }
-                tc::st_sw128_8(sm + BKdT, 128, c, t0, bkd);
-                tc::st_sw128_8(sm + BVT, 128, c, t0, bv);
-                tc::st_sw128_8(sm + KtT, 128, c, t0, kt);
+                float a[8], b[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) { a[u] = lo ? bkd0[u] : bkd1[u]; b[u] = lo ? bkd1[u] : bkd0[u]; }
+                tc::st_sw128_8(sm + BKdT, 128, c2 + (lo ? 0 : 1), t0, a);
+                tc::st_sw128_8(sm + BKdT, 128, c2 + (lo ? 1 : 0), t0, b);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) { a[u] = lo ? bv0[u] : bv1[u]; b[u] = lo ? bv1[u] : bv0[u]; }
+                tc::st_sw128_8(sm + BVT, 128, c2 + (lo ? 0 : 1), t0, a);
+                tc::st_sw128_8(sm + BVT, 128, c2 + (lo ? 1 : 0), t0, b);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) { a[u] = lo ? kt0[u] : kt1[u]; b[u] = lo ? kt1[u] : kt0[u]; }
+                tc::st_sw128_8(sm + KtT, 128, c2 + (lo ? 0 : 1), t0, a);
+                tc::st_sw128_8(sm + KtT, 128, c2 + (lo ? 1 : 0), t0, b);
             }
         }
         sync_for_mma();
-        // the staging buffer is free: fetch the next chunk while this one computes
-        if (ci + 1 < nch) prefetch_chunk(p, pd, seq, h, rho, L, c0 + BC, sm);
         if (tid == 0) {
             tc::mma_tile(tAP, tc::smem_addr(sm + KQp), 128 * 128, tc::smem_addr(sm + Km), 64 * 128,
                          128, tc::idesc_bf16(128, 64), false);
@@ -279,6 +309,8 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
                          128, tc::idesc_bf16(128, 64), false);
             tc::mma_commit(&bars[0]);
         }
+        // the staging buffer is free: fetch the next chunk while this one computes
+        if (ci + 1 < nch) prefetch_chunk(p, pd, seq, h, rho, L, c0 + BC, sm, s_rows);
         // ---- scale the TMEM state by e^{Gamma_L} per key channel (used by MMA7) -----------
         for (int hf = 0; hf < 2; ++hf) {
             float r[32];
