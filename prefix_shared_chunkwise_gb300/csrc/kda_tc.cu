@@ -72,36 +72,64 @@ __device__ void invert_unit_lower(float *Mf, float *Tf) {
         float col[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-            float acc = 0.f;
+            const float *mrow = Mf + (16 * b + t) * 64;
+            const int x = (16 * b + t) & 31;
+            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int j = 0; j < t; ++j) acc += Mf[fidx(16 * b + t, 16 * b + j)] * col[j];
-            col[t] = t < s ? 0.f : (t == s ? 1.f : -acc);
+            for (int j = 0; j < t; j += 2) {
+                a0 += mrow[(16 * b + j) ^ x] * col[j];
+                if (j + 1 < t) a1 += mrow[(16 * b + j + 1) ^ x] * col[j + 1];
+            }
+            col[t] = t < s ? 0.f : (t == s ? 1.f : -(a0 + a1));
         }
 #pragma unroll
         for (int t = 0; t < 16; ++t) Tf[fidx(16 * b + t, 16 * b + s)] = col[t];
     }
     __syncthreads();
+    // off-diagonal blocks: each thread forms four adjacent columns of one row
 #pragma unroll 1
     for (int d = 1; d < 4; ++d) {
-        const int nblk = 4 - d;
-        for (int e = threadIdx.x; e < nblk * 256; e += NT) {
-            const int j = e >> 8, i = j + d, t = (e >> 4) & 15, s = e & 15;
-            float acc = 0.f;
+        const int nstrip = (4 - d) * 64;
+        if (tid < nstrip) {
+            const int j = tid >> 6, i = j + d, t = (tid >> 2) & 15, s0 = (tid & 3) * 4;
+            const int rowM = 16 * i + t, xm = rowM & 31;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
             for (int kb = j; kb < i; ++kb) {
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    acc += Mf[fidx(16 * i + t, 16 * kb + u)] * Tf[fidx(16 * kb + u, 16 * j + s)];
+                for (int u = 0; u < 16; ++u) {
+                    const float mv = Mf[rowM * 64 + ((16 * kb + u) ^ xm)];
+                    const int rT = 16 * kb + u, xt = rT & 31;
+                    const float *tr = Tf + rT * 64;
+                    a0 += mv * tr[(16 * j + s0) ^ xt];
+                    a1 += mv * tr[(16 * j + s0 + 1) ^ xt];
+                    a2 += mv * tr[(16 * j + s0 + 2) ^ xt];
+                    a3 += mv * tr[(16 * j + s0 + 3) ^ xt];
+                }
             }
-            Mf[fidx(16 * j + s, 16 * i + t)] = acc;
+            // X_ij kept transposed in the unused upper triangle of Mf
+            Mf[fidx(16 * j + s0, rowM)] = a0;
+            Mf[fidx(16 * j + s0 + 1, rowM)] = a1;
+            Mf[fidx(16 * j + s0 + 2, rowM)] = a2;
+            Mf[fidx(16 * j + s0 + 3, rowM)] = a3;
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < nblk * 256; e += NT) {
-            const int j = e >> 8, i = j + d, t = (e >> 4) & 15, s = e & 15;
-            float acc = 0.f;
+        if (tid < nstrip) {
+            const int j = tid >> 6, i = j + d, t = (tid >> 2) & 15, s0 = (tid & 3) * 4;
+            const int rowT = 16 * i + t, xt = rowT & 31;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-                acc += Tf[fidx(16 * i + t, 16 * i + u)] * Mf[fidx(16 * j + s, 16 * i + u)];
-            Tf[fidx(16 * i + t, 16 * j + s)] = -acc;
+            for (int u = 0; u < 16; ++u) {
+                const float tv = Tf[rowT * 64 + ((16 * i + u) ^ xt)];
+                const int col = 16 * i + u;
+                a0 += tv * Mf[fidx(16 * j + s0, col)];
+                a1 += tv * Mf[fidx(16 * j + s0 + 1, col)];
+                a2 += tv * Mf[fidx(16 * j + s0 + 2, col)];
+                a3 += tv * Mf[fidx(16 * j + s0 + 3, col)];
+            }
+            Tf[fidx(rowT, 16 * j + s0)] = -a0;
+            Tf[fidx(rowT, 16 * j + s0 + 1)] = -a1;
+            Tf[fidx(rowT, 16 * j + s0 + 2)] = -a2;
+            Tf[fidx(rowT, 16 * j + s0 + 3)] = -a3;
         }
         __syncthreads();
     }
