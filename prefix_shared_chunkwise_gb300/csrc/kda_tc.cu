@@ -542,6 +542,44 @@ __device__ __forceinline__ float beta_of(const uint8_t *words, const int *par, i
     return __bfloat162float(__ushort_as_bfloat16(hb));
 }
 
+__device__ __forceinline__ float2 sw_val2(const uint8_t *tile, int rows, int r, int c) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(tile + tc::sw128_offset(rows, r, c)));
+}
+
+// Two-channel cumulative decay over row quarters, thread (cp, qr): channels 2cp, 2cp+1,
+// rows 16 qr .. 16 qr + 15.  Pass 1 publishes quarter sums and the local prefix at the
+// reference row; after a barrier, gamma2_setup gives the starting offsets, the reference
+// value m and Gamma_L of both channels.
+struct Gam2 { float gam0, gam1, m0, m1, gl0, gl1; };
+
+__device__ __forceinline__ void gamma2_pass1(const uint8_t *G, int cp, int qr, int mid, float *vpart,
+                                             float *vm) {
+    const int c2 = 2 * cp;
+    float s0 = 0.f, s1 = 0.f, ml0 = 0.f, ml1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const int t = qr * 16 + u;
+        const float2 gg = sw_val2(G, 64, t, c2);
+        s0 += gg.x; s1 += gg.y;
+        if (t == mid) { ml0 = s0; ml1 = s1; }
+    }
+    vpart[qr * 128 + c2] = s0; vpart[qr * 128 + c2 + 1] = s1;
+    if (qr == (mid >> 4)) { vm[c2] = ml0; vm[c2 + 1] = ml1; }
+}
+
+__device__ __forceinline__ Gam2 gamma2_setup(int cp, int qr, int mid, const float *vpart, const float *vm) {
+    const int c2 = 2 * cp, qmid = mid >> 4;
+    Gam2 r{0.f, 0.f, vm[c2], vm[c2 + 1], 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float p0 = vpart[q * 128 + c2], p1 = vpart[q * 128 + c2 + 1];
+        if (q < qr) { r.gam0 += p0; r.gam1 += p1; }
+        if (q < qmid) { r.m0 += p0; r.m1 += p1; }
+        r.gl0 += p0; r.gl1 += p1;
+    }
+    return r;
+}
+
 // Cumulative decay pass 1 for thread (c, half): partial sums and the reference row.
 __device__ __forceinline__ void gamma_pass1(const uint8_t *G, int c, int half, int mid, float *vt0,
                                             float *vt1, float *vm) {
@@ -561,7 +599,7 @@ constexpr uint32_t Pm = 131072, Tm = 139264, dSTs = 147456, dUTs = 180224;
 constexpr uint32_t dOm2 = 196608, Tm2 = 212992;          // second buffers (prefetch)
 constexpr uint32_t SBeta = 221184, SBpar = SBeta + 256, Vec = SBpar + 256;
 constexpr uint32_t vBeta = Vec, vEl = vBeta + 256, vEkt = vEl + 512, vM = vEkt + 512,
-                   vT0 = vM + 512, vT1 = vT0 + 512, vEnd = vT1 + 512;
+                   vPart = vM + 512, vEnd = vPart + 2048;
 constexpr uint32_t bytes = vEnd + 1024;
 }  // namespace bws_sm
 
@@ -575,7 +613,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
     __shared__ int s_rows[64];
     float *vbeta = reinterpret_cast<float *>(sm + vBeta), *vel = reinterpret_cast<float *>(sm + vEl),
           *vekt = reinterpret_cast<float *>(sm + vEkt), *vm = reinterpret_cast<float *>(sm + vM),
-          *vt0 = reinterpret_cast<float *>(sm + vT0), *vt1 = reinterpret_cast<float *>(sm + vT1);
+          *vpart = reinterpret_cast<float *>(sm + vPart);
     int *spar = reinterpret_cast<int *>(sm + SBpar);
     const FwdParams &f = p.f;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, ch = warp >> 2;
@@ -615,7 +653,6 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
 
     const int32_t sp_begin = pd.seq_sptr[seq];
     int32_t sp = pd.seq_sptr[seq + 1] - 1;
-    const int c = tid & 127, half = tid >> 7;
     // Stage chunk cj's raw q, k, g, beta and (into buffer `b`) dO and the forward's T.
     auto stage_chunk = [&](int32_t cj, int b) {
         const int32_t cc0 = cj * BC;
@@ -675,24 +712,34 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
                     *reinterpret_cast<const uint4 *>(sm + dSTs + piece128(r, pc));
             }
         }
-        // ---- prep ------------------------------------------------------------------------
-        gamma_pass1(sm + RawG, c, half, mid, vt0, vt1, vm);
-        if (tid < 64) vbeta[tid] = beta_of(sm + SBeta, spar, tid);
-        __syncthreads();
+        // ---- prep: two key channels per thread over a quarter of the rows ---------------
         {
-            const float m = vm[c], gl = vt0[c] + vt1[c];
-            float gam = half ? vt0[c] : 0.f;
-            if (-m > kMaxExpArg || m - gl > kMaxExpArg) dev_error(pd, kDevErrDecayRange, seq, c0);
-            const float em = __expf(m);
-            if (half == 0) { vel[c] = __expf(gl); vekt[c] = __expf(gl - m); }
-            for (int t = half * 32; t < half * 32 + 32; ++t) {
-                const float kk = sw_val(sm + RawK, 64, t, c), qq = sw_val(sm + RawQ, 64, t, c) * f.scale;
-                gam += sw_val(sm + RawG, 64, t, c);
-                const float e1 = __expf(gam - m), e2 = __expf(m - gam);
-                st_bf16(sm + Qpm, 64, t, c, qq * e1);
-                st_bf16(sm + Km, 64, t, c, kk * e2);
-                st_bf16(sm + Kdm, 64, t, c, kk * e1 * em);
-                st_bf16(sm + Qdm, 64, t, c, qq * e1 * em);
+            const int cp = tid & 63, qr = tid >> 6, c2 = 2 * cp;
+            gamma2_pass1(sm + RawG, cp, qr, mid, vpart, vm);
+            if (tid < 64) vbeta[tid] = beta_of(sm + SBeta, spar, tid);
+            __syncthreads();
+            Gam2 gs = gamma2_setup(cp, qr, mid, vpart, vm);
+            if (-gs.m0 > kMaxExpArg || gs.m0 - gs.gl0 > kMaxExpArg || -gs.m1 > kMaxExpArg ||
+                gs.m1 - gs.gl1 > kMaxExpArg)
+                dev_error(pd, kDevErrDecayRange, seq, c0);
+            const float em0 = __expf(gs.m0), em1 = __expf(gs.m1);
+            if (qr == 0) {
+                vel[c2] = __expf(gs.gl0); vel[c2 + 1] = __expf(gs.gl1);
+                vekt[c2] = __expf(gs.gl0 - gs.m0); vekt[c2 + 1] = __expf(gs.gl1 - gs.m1);
+            }
+#pragma unroll 4
+            for (int u = 0; u < 16; ++u) {
+                const int t = qr * 16 + u;
+                const float2 kk = sw_val2(sm + RawK, 64, t, c2), qv = sw_val2(sm + RawQ, 64, t, c2),
+                             gg = sw_val2(sm + RawG, 64, t, c2);
+                const float q0 = qv.x * f.scale, q1 = qv.y * f.scale;
+                gs.gam0 += gg.x; gs.gam1 += gg.y;
+                const float e10 = __expf(gs.gam0 - gs.m0), e20 = __expf(gs.m0 - gs.gam0);
+                const float e11 = __expf(gs.gam1 - gs.m1), e21 = __expf(gs.m1 - gs.gam1);
+                st_bf16x2(sm + Qpm, 64, t, c2, q0 * e10, q1 * e11);
+                st_bf16x2(sm + Km, 64, t, c2, kk.x * e20, kk.y * e21);
+                st_bf16x2(sm + Kdm, 64, t, c2, kk.x * e10 * em0, kk.y * e11 * em1);
+                st_bf16x2(sm + Qdm, 64, t, c2, q0 * e10 * em0, q1 * e11 * em1);
             }
         }
         sync_for_mma();
