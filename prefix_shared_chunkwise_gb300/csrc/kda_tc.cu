@@ -15,6 +15,11 @@
 // substitution in fp32 on the CUDA cores.  Bounded replay (page "HARTS ... 精读",
 // section 4.2): the first chunk of a side branch starts with its replay rows, which
 // update the state but write no output.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "tc_primitives.cuh"
 
@@ -836,6 +841,40 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
     if (warp == 0) tc::tmem_dealloc(tm, 512);
 }
 
+// Tensor maps of the gradient kernel.  Row tensors (q, k, g, v, dO, in that order) are
+// 3-D {D, H, C}, one map per box height 8 << j rows (j = 0..3) of 64 channels; the
+// chunk records are 2-D: S^T as 256-byte rows (box 128 x 64), T as 128-byte rows (box
+// 64 x 64), dS'^T as 256-byte rows (box 128 x 64).  All use the 128-byte swizzle of the
+// MMA operand tiles.
+struct GradMaps {
+    CUtensorMap rows[5][4];
+    CUtensorMap rec_s, rec_t, dch;
+};
+
+// Box b (largest first, heights 8 << j rows) of the cover of the 8-row groups [glo, ghi):
+// its first group and its height index j.  At most four boxes.
+__device__ __forceinline__ void cover_box(int glo, int ghi, int b, int &gi, int &j) {
+    gi = glo;
+    j = 0;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        j = 3;
+        while ((1 << j) > ghi - gi) --j;
+        if (x == b) break;
+        gi += 1 << j;
+    }
+}
+
+__device__ __forceinline__ int cover_count(int glo, int ghi) {
+    int n = 0;
+    for (int gi = glo; gi < ghi; ++n) {
+        int j = 3;
+        while ((1 << j) > ghi - gi) --j;
+        gi += 1 << j;
+    }
+    return n;
+}
+
 namespace bwg_sm {
 constexpr uint32_t SemT = 0, dSekT = 32768, dOm = 65536, KQp = 81920, Km = 114688, Tm = 131072;
 constexpr uint32_t RV = 139264, RQ = 155648, RK = 172032, RG = 188416, PmS = 204800, TBm = 212992;
@@ -847,14 +886,108 @@ constexpr uint32_t vBeta = Vec, vM = vBeta + 256, vEm = vM + 512, vEkt = vEm + 5
 constexpr uint32_t bytes = vEnd + 1024;
 }  // namespace bwg_sm
 
-__global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd, int32_t chunk_begin) {
+// A work item of the gradient kernel is one (chunk, head); a block takes items in steps
+// of the grid size.
+struct GradItem {
+    int32_t h, g, seq, rho, L, c0, nv, row0, rptr;
+};
+
+__device__ __forceinline__ GradItem grad_item(const PlanDev &pd, int32_t chunk_begin, int H, int32_t item) {
+    GradItem it;
+    it.h = item % H;
+    it.g = chunk_begin + item / H;
+    it.seq = pd.chunk_seq[it.g];
+    it.rho = pd.seq_rho[it.seq];
+    it.L = it.rho + pd.seq_nown[it.seq];
+    it.c0 = (it.g - pd.seq_cbase[it.seq]) * BC;
+    it.nv = min(BC, it.L - it.c0);
+    it.row0 = pd.seq_row0[it.seq];
+    it.rptr = pd.seq_rptr[it.seq];
+    return it;
+}
+
+// Staging of the gradient kernel's inputs in three groups, waited for in the order they
+// are used: A = q, k, g, beta (the prep); C = v, dO and the forward's T; B = S^T and
+// dS'^T.  Row tiles: every 8-row group made only of own rows of the sequence comes by TMA
+// (the lanes of warp 0 issue one box each, counted on the group's barrier); the other rows
+// (replayed rows, a group cut by the sequence's start or end, zero rows) by cp.async
+// through the row table `tab`.
+__device__ __forceinline__ void grad_stage_ac(const GradMaps *maps, const void *q, const void *k, const void *g,
+                                              const void *v, const void *d_o, const void *beta, GradItem it,
+                                              const int *tab, int H, uint8_t *sm, uint64_t *tbar) {
+    using namespace bwg_sm;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int glo = (max(0, it.rho - it.c0) + 7) >> 3, ghi = max(glo, it.nv >> 3);
+    const int t_zero = max(0, it.rho - it.c0);        // dO rows below this are zero
+    if (warp == 0) {
+        const int nb = cover_count(glo, ghi);
+        const int z0 = it.row0 + it.c0 - it.rho;       // compact row of local row 0
+        if (lane == 0) {
+            tc::mbar_expect_tx(&tbar[0], static_cast<uint32_t>(3 * (ghi - glo) * 2048));
+            tc::mbar_expect_tx(&tbar[1], static_cast<uint32_t>(2 * (ghi - glo) * 2048 + 8192));
+        }
+        __syncwarp();
+        // jobs: tensor x (q, k, g, v, dO) x box x half; one per lane
+        for (int jb = lane; jb < 5 * nb * 2; jb += 32) {
+            const int x = jb / (nb * 2), r = jb - x * nb * 2, a = r & 1;
+            int gi, j;
+            cover_box(glo, ghi, r >> 1, gi, j);
+            const uint32_t tile = x == 0 ? RQ : x == 1 ? RK : x == 2 ? RG : x == 3 ? RV : dOm;
+            tc::tma_load_3d(sm + tile + a * 8192 + gi * 1024, &maps->rows[x][j], 64 * a, it.h, z0 + 8 * gi,
+                            &tbar[x < 3 ? 0 : 1]);
+        }
+        if (lane == 31) {
+            const int64_t rid = static_cast<int64_t>(it.g) * H + it.h;
+            tc::tma_load_2d(sm + Tm, &maps->rec_t, 0, static_cast<int>(rid * 320 + 256), &tbar[1]);
+        }
+    }
+    // rows outside the TMA groups, A then C
+    for (int x = 0; x < 5; ++x) {
+        if (x == 3) {
+            stage_beta_tab(sm + SBeta, reinterpret_cast<int *>(sm + SBpar), beta, tab, it.h, H);
+            tc::cp_async_commit();
+        }
+        const uint8_t *src = static_cast<const uint8_t *>(x == 0 ? q : x == 1 ? k : x == 2 ? g : x == 3 ? v : d_o);
+        uint8_t *tile = sm + (x == 0 ? RQ : x == 1 ? RK : x == 2 ? RG : x == 3 ? RV : dOm);
+        const int zero_below = x == 4 ? t_zero : 0;
+        for (int e = tid; e < 64 * 16; e += NT) {
+            const int t = e >> 4, pc = e & 15;
+            if ((t >> 3) >= glo && (t >> 3) < ghi) continue;
+            const int row = t < zero_below ? -1 : tab[t];
+            const uint8_t *sp = row >= 0 ? src + ((static_cast<int64_t>(row) * H + it.h) * D * 2 + pc * 16) : src;
+            tc::cp_async16(tile + piece64(t, pc), sp, row >= 0 ? 16u : 0u);
+        }
+    }
+    tc::cp_async_commit();
+}
+
+__device__ __forceinline__ void grad_stage_b(const GradMaps *maps, GradItem it, int H, uint8_t *sm, uint64_t *bar) {
+    using namespace bwg_sm;
+    const int lane = threadIdx.x & 31;
+    if ((threadIdx.x >> 5) != 0) return;
+    const int64_t rid = static_cast<int64_t>(it.g) * H + it.h;
+    if (lane == 0) tc::mbar_expect_tx(bar, 4 * 16384);
+    __syncwarp();
+    if (lane < 4) {
+        const int a = lane & 1;
+        if (lane < 2)
+            tc::tma_load_2d(sm + SemT + a * 16384, &maps->rec_s, 64 * a, static_cast<int>(rid * 160), bar);
+        else
+            tc::tma_load_2d(sm + dSekT + a * 16384, &maps->dch, 64 * a, static_cast<int>(rid * 128), bar);
+    }
+}
+
+__global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd, int32_t chunk_begin,
+                                                         int32_t n_items,
+                                                         const __grid_constant__ GradMaps maps) {
     using namespace bwg_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
     __shared__ uint64_t bars[6];
+    __shared__ uint64_t tbar[3];      // staging groups A, C, B (see below)
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
-    __shared__ int s_rows[64];
+    __shared__ int s_rows[2][64];
     float *vbeta = reinterpret_cast<float *>(sm + vBeta), *vm = reinterpret_cast<float *>(sm + vM),
           *vem = reinterpret_cast<float *>(sm + vEm), *vekt = reinterpret_cast<float *>(sm + vEkt),
           *vel = reinterpret_cast<float *>(sm + vEl), *vt0 = reinterpret_cast<float *>(sm + vT0),
@@ -865,57 +998,59 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
     const FwdParams &f = p.f;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, ch = warp >> 2;
     const int H = f.H;
-    const int32_t h = blockIdx.x % H;
-    const int32_t g = chunk_begin + blockIdx.x / H;
-    const int32_t seq = pd.chunk_seq[g];
-    const int32_t ci = g - pd.seq_cbase[seq];
-    const int32_t rho = pd.seq_rho[seq], L = rho + pd.seq_nown[seq];
-    const int32_t c0 = ci * BC;
-    const int nv = min(BC, L - c0), mid = (nv - 1) / 2;
-    const int32_t row0 = pd.seq_row0[seq], rptr = pd.seq_rptr[seq];
-    const uint8_t *rec = static_cast<const uint8_t *>(f.chunk_states) + (static_cast<int64_t>(g) * H + h) * kRecBytes;
-    const uint8_t *dcs = static_cast<const uint8_t *>(p.dchunk) + (static_cast<int64_t>(g) * H + h) * D * D * 2;
     const int W = 3 * D + 1;
-    // local rows [t_own, t_end) of this chunk are own rows of the sequence
-    const int t_own = max(0, rho - c0), t_end = nv;
+    const int jv = lg * 32 + lane;
+    const int c = tid & 127, half = tid >> 7;
+    const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
 
-    if (tid < 64) s_rows[tid] = static_cast<int>(local_row(pd, seq, rho, L, c0 + tid));
+    auto decode = [&](int32_t item) { return grad_item(pd, chunk_begin, H, item); };
+    auto rows_of = [&](const GradItem &it, int *tab) {
+        if (tid < 64) tab[tid] = static_cast<int>(local_row(pd, it.seq, it.rho, it.L, it.c0 + tid));
+    };
+    auto stage_ac = [&](const GradItem &it, const int *tab) {
+        grad_stage_ac(&maps, f.q, f.k, f.g, f.v, p.d_o, f.beta, it, tab, H, sm, tbar);
+    };
+    auto stage_b = [&](const GradItem &it) { grad_stage_b(&maps, it, H, sm, &tbar[2]); };
+
     if (tid == 0) {
         for (int i = 0; i < 6; ++i) tc::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 3; ++i) tc::mbar_init(&tbar[i], 1);
+        tc::fence_mbar_init();
         s_fail = 0;
     }
     if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
+    int32_t item = blockIdx.x;
+    GradItem nx{};
+    if (item < n_items) {
+        nx = decode(item);
+        rows_of(nx, s_rows[0]);
+    }
     __syncthreads();
-    // ---- staging in three groups, waited for in the order they are used -------------------
-    stage_tab(sm + RQ, f.q, s_rows, h, H, 0);
-    stage_tab(sm + RK, f.k, s_rows, h, H, 0);
-    stage_tab(sm + RG, f.g, s_rows, h, H, 0);
-    stage_beta_tab(sm + SBeta, spar, f.beta, s_rows, h, H);
-    tc::cp_async_commit();
-    for (int e = tid; e < 128 * 16; e += NT) {
-        const int r = e >> 4, pc = e & 15;
-        tc::cp_async16(sm + SemT + piece128(r, pc), rec + r * 256 + pc * 16, 16u);
-        tc::cp_async16(sm + dSekT + piece128(r, pc), dcs + r * 256 + pc * 16, 16u);
-    }
-    for (int e = tid; e < 64 * 8; e += NT) {
-        const int t = e >> 3, pc = e & 7;
-        tc::cp_async16(sm + Tm + t * 128 + ((pc ^ (t & 7)) << 4), rec + D * D * 2 + t * 128 + pc * 16, 16u);
-    }
-    tc::cp_async_commit();
-    stage_tab(sm + RV, f.v, s_rows, h, H, 0);
-    stage_tab(sm + dOm, p.d_o, s_rows, h, H, t_own);
-    tc::cp_async_commit();
     tc::fence_after_sync();
     const uint32_t tm = s_tmem;
-    const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
     const uint32_t tAP = tm, tGam = tm + 64, tXm = tm + 128, tXq = tm + 192, tP1 = tm + 256,
                    tP2 = tm + 320, tS1 = tm + 384, tS2 = tm + 448;
-    const int jv = lg * 32 + lane;
-    const int c = tid & 127, half = tid >> 7;
+    if (item < n_items) {
+        stage_ac(nx, s_rows[0]);
+        stage_b(nx);
+    }
+    uint32_t ph = 0;
+    int32_t cur_seq = 0, cur_h = 0, n_done = 0, n_armed = item < n_items ? 1 : 0;
+    for (; item < n_items; item += gridDim.x, ++n_done) {
+    ph = n_done & 1;
+    const GradItem I = nx;
+    const int32_t h = I.h, seq = I.seq, rho = I.rho, c0 = I.c0, row0 = I.row0, rptr = I.rptr;
+    cur_seq = seq; cur_h = h;
+    const int mid = (I.nv - 1) / 2;
+    // local rows [t_own, t_end) of this chunk are own rows of the sequence
+    const int t_own = max(0, rho - c0), t_end = I.nv;
+    const int32_t nxt = item + gridDim.x;
+    int *nrows = s_rows[(n_done + 1) & 1];
 
     // ---- prep: Gamma (kept in TMEM, lane = key channel), Kp, Qp, Km --------------------
-    cp_async_wait_group<2>();
-    __syncthreads();
+    cp_async_wait_group<1>();
+    tc::fence_before_sync();
+    if (!wait_all(&tbar[0], ph, &s_fail)) goto done;
     gamma_pass1(sm + RG, c, half, mid, vt0, vt1, vm);
     if (tid < 64) vbeta[tid] = beta_of(sm + SBeta, spar, tid);
     __syncthreads();
@@ -939,8 +1074,10 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         tc::tmem_st32(tGam + lane_off + half * 32, gv);   // thread (c, half) sits in lane c
     }
     // ---- d_el = sum_dv S . dS' per key channel (before scaling), two channels per thread --
-    cp_async_wait_group<1>();
+    cp_async_wait_group<0>();
+    if (!tc::mbar_wait(&tbar[1], ph) || !tc::mbar_wait(&tbar[2], ph)) atomicOr(&s_fail, 1);
     __syncthreads();
+    if (s_fail) goto done;
     {
         const int pr = tid & 63, qr = tid >> 6;
         float a0 = 0.f, a1 = 0.f;
@@ -992,7 +1129,6 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         w.z = tc::pack_bf16(v[4], v[5]); w.w = tc::pack_bf16(v[6], v[7]);
         *reinterpret_cast<uint4 *>(sm + TBm + off) = w;
     }
-    cp_async_wait_group<0>();
     sync_for_mma();
     if (tid == 0) {
         tc::mma_tile(tAP, tc::smem_addr(sm + KQp), 16384, tc::smem_addr(sm + Km), 8192, 128,
@@ -1002,7 +1138,11 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
                      tc::idesc_bf16(128, 64), false);
         tc::mma_commit(&bars[0]);
     }
-    if (!wait_all(&bars[0], 0, &s_fail)) goto done;
+    if (nxt < n_items) {           // the plan-table loads overlap the MMAs
+        nx = decode(nxt);
+        rows_of(nx, nrows);
+    }
+    if (!wait_all(&bars[0], ph, &s_fail)) goto done;
     {
         float r[32];
         // P (lanes 64-127) -> Pm, incl lower
@@ -1033,7 +1173,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
                    tc::Opnd{tc::smem_addr(sm + Km), 8192, false}, 128, 64, 128, true);
         tc::mma_commit(&bars[1]);
     }
-    if (!wait_all(&bars[1], 0, &s_fail)) goto done;
+    if (!wait_all(&bars[1], ph, &s_fail)) goto done;
     {
         float r[32];
         tc::tmem_ld32(tS1 + lane_off + ch * 32, r);
@@ -1059,7 +1199,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
                    tc::Opnd{tc::smem_addr(sm + RQ), 16384, true}, 128, 64, 128, false);
         tc::mma_commit(&bars[2]);
     }
-    if (!wait_all(&bars[2], 0, &s_fail)) goto done;
+    if (!wait_all(&bars[2], ph, &s_fail)) goto done;
     {
         float r[32];
         // Z^T: dv = beta Z staged [t][dv] in RV (U^T is consumed); replay rows go to the
@@ -1119,7 +1259,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dv) + (row * H + h) * D + pc * 8) =
             *reinterpret_cast<const uint4 *>(sm + RV + t * 256 + pc * 16);
     }
-    if (!wait_all(&bars[3], 0, &s_fail)) goto done;
+    if (!wait_all(&bars[3], ph, &s_fail)) goto done;
     {
         float r[32];
         tc::tmem_ld32(tS1 + lane_off + ch * 32, r);
@@ -1142,7 +1282,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
                    tc::Opnd{tc::smem_addr(sm + RQ), 8192, true}, 128, 64, 64, false);
         tc::mma_commit(&bars[4]);
     }
-    if (!wait_all(&bars[4], 0, &s_fail)) goto done;
+    if (!wait_all(&bars[4], ph, &s_fail)) goto done;
     {
         float r[32], a[32];
         tc::tmem_ld32(tS2 + lane_off + ch * 32, r);
@@ -1183,7 +1323,11 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
                    tc::Opnd{tc::smem_addr(sm + PmS), 8192, true}, 128, 64, 64, true);
         tc::mma_commit(&bars[5]);
     }
-    if (!wait_all(&bars[5], 0, &s_fail)) goto done;
+    if (!wait_all(&bars[5], ph, &s_fail)) goto done;
+    if (nxt < n_items) {
+        stage_ac(nx, nrows);
+        ++n_armed;
+    }
     {
         // thread: key channel dk = jv, rows t = 32 ch .. 32 ch + 31.  dq, dk, dg are staged
         // [t][dk] (dq, dk over S^T, dg over dS'^T: both consumed) for coalesced stores.
@@ -1276,11 +1420,19 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
                 p.rep_grad[(static_cast<int64_t>(rptr + c0 + t) * H + h) * W + 3 * D] = db;
         }
     }
+    tc::fence_smem_to_async();     // SemT / dSekT were read and written by threads
+    __syncthreads();
+    if (nxt < n_items) stage_b(nx);
+    }
 done:
     tc::cp_async_wait_all();
     if (s_fail) {
-        dev_error(pd, kDevErrTimeout, seq, h);
-        for (int i = 0; i < 6; ++i) tc::mbar_wait(&bars[i], 0, 100000000LL);
+        dev_error(pd, kDevErrTimeout, cur_seq, cur_h);
+        for (int i = 0; i < 6; ++i) tc::mbar_wait(&bars[i], ph, 100000000LL);
+        // staging copies still in flight land before the block's shared memory is released
+        if (tid == 0)
+            for (int j = n_done; j < n_armed; ++j)
+                for (int k = 0; k < 3; ++k) tc::mbar_wait(&tbar[k], j & 1, 100000000LL);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -1312,12 +1464,75 @@ cudaError_t tc_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t ba
     return cudaGetLastError();
 }
 
+namespace {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+            const cuuint32_t *box) {
+    auto fn = encode_tiled();
+    if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [C rows][H heads][D] bf16, boxes of (8 << j) rows of 64 channels, j = 0..3.
+bool rows_maps(CUtensorMap *m, const void *base, int H, int64_t C) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(C)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+    for (int j = 0; j < 4; ++j) {
+        const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(8 << j)};
+        if (!encode(m + j, base, 3, dims, strides, box)) return false;
+    }
+    return true;
+}
+
+// A buffer seen as [n_rows][cols] bf16, boxes of box_rows x 64.
+bool flat_map(CUtensorMap *m, const void *base, int64_t n_rows, int cols, int box_rows) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(n_rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    return encode(m, base, 2, dims, strides, box);
+}
+
+}  // namespace
+
 cudaError_t tc_bwd_grad(const BwdParams &p, const PlanDev &pd, int32_t chunk_begin,
                         int32_t n_items, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(kda_bwd_grad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(bwg_sm::bytes));
     if (e != cudaSuccess) return e;
-    kda_bwd_grad_tc<<<n_items, NT, bwg_sm::bytes, st>>>(p, pd, chunk_begin);
+    if (n_items <= 0) return cudaSuccess;
+    const int H = p.f.H;
+    const int64_t n_rec = pd.n_chunks * H;
+    if (n_rec * (kRecBytes / 128) > INT32_MAX) return cudaErrorInvalidValue;   // TMA coordinates are int32
+    GradMaps maps;
+    if (!rows_maps(maps.rows[0], p.f.q, H, pd.C) || !rows_maps(maps.rows[1], p.f.k, H, pd.C) ||
+        !rows_maps(maps.rows[2], p.f.g, H, pd.C) || !rows_maps(maps.rows[3], p.f.v, H, pd.C) ||
+        !rows_maps(maps.rows[4], p.d_o, H, pd.C) ||
+        !flat_map(&maps.rec_s, p.f.chunk_states, n_rec * (kRecBytes / 256), 128, 128) ||
+        !flat_map(&maps.rec_t, p.f.chunk_states, n_rec * (kRecBytes / 128), 64, 64) ||
+        !flat_map(&maps.dch, p.dchunk, n_rec * D, 128, 128))
+        return cudaErrorInvalidValue;
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    // persistent: one block per SM, items in steps of the grid size
+    kda_bwd_grad_tc<<<min(n_items, nsm), NT, bwg_sm::bytes, st>>>(p, pd, chunk_begin, n_items, maps);
     return cudaGetLastError();
 }
 

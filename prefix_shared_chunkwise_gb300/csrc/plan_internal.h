@@ -31,7 +31,7 @@ struct PlanDev {
     const int32_t *fold_occ;       // [R] replay occurrence ids grouped by row
     const int32_t *chunk_seq;      // [n_chunks] sequence of every chunk
     int32_t n_rounds, n_seq, n_states, n_roots, n_fold, chunk;
-    int64_t R, n_chunks;
+    int64_t R, n_chunks, C;
 };
 
 // Word offsets of each table inside the device image.

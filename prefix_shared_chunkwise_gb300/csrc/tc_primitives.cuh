@@ -165,6 +165,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase,
     return true;
 }
 
+// Arrive on a barrier (count 1) and add `bytes` to the transactions its phase waits for.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+// Make barrier initialisation visible to the asynchronous proxy (TMA completions).
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// ---- TMA tiled loads (tensor map in kernel parameter space; completion on an mbarrier) --
+// The destination must be 1024-byte aligned for the 128-byte swizzle used here; every
+// coordinate passed by this library lies inside the tensor.
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x, int y, int z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+           "r"(smem_addr(bar))
+        : "memory");
+}
+
 // ---- TMEM <-> registers (warp-collective; warp w may touch lanes 32*(w%4)..+31) ---------
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
