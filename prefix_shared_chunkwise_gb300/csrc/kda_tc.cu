@@ -1143,23 +1143,26 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         rows_of(nx, nrows);
     }
     if (!wait_all(&bars[0], ph, &s_fail)) goto done;
-    {
-        float r[32];
+    // epilogues walk this thread's 32 columns in two rolled halves of 16 (code size)
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        const int cb = ch * 32 + hh * 16;
+        float r[16];
         // P (lanes 64-127) -> Pm, incl lower
-        tc::tmem_ld32(tAP + lane_off + ch * 32, r);
+        tc::tmem_ld16(tAP + lane_off + cb, r);
         if (lg >= 2) {
             const int t = jv - 64;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = (ch * 32 + j <= t) ? r[j] : 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + PmS, 64, t, ch * 32 + j, r + j);
+            for (int j = 0; j < 16; ++j) r[j] = (cb + j <= t) ? r[j] : 0.f;
+            tc::st_sw128_8(sm + PmS, 64, t, cb, r);
+            tc::st_sw128_8(sm + PmS, 64, t, cb + 8, r + 8);
         }
         // Y^T = V^T - X^T -> YT [dv][t] (in RQ; raw q was last read in the prep)
-        tc::tmem_ld32(tS1 + lane_off + ch * 32, r);
+        tc::tmem_ld16(tS1 + lane_off + cb, r);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = sw_val(sm + RV, 64, ch * 32 + j, jv) - r[j];
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RQ, 128, jv, ch * 32 + j, r + j);
+        for (int j = 0; j < 16; ++j) r[j] = sw_val(sm + RV, 64, cb + j, jv) - r[j];
+        tc::st_sw128_8(sm + RQ, 128, jv, cb, r);
+        tc::st_sw128_8(sm + RQ, 128, jv, cb + 8, r + 8);
     }
     sync_for_mma();
     if (tid == 0) {
@@ -1174,14 +1177,16 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         tc::mma_commit(&bars[1]);
     }
     if (!wait_all(&bars[1], ph, &s_fail)) goto done;
-    {
-        float r[32];
-        tc::tmem_ld32(tS1 + lane_off + ch * 32, r);
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RV, 128, jv, ch * 32 + j, r + j);   // UTs
-        tc::tmem_ld32(tS2 + lane_off + ch * 32, r);
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RK, 128, jv, ch * 32 + j, r + j);   // dUTs
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        const int cb = ch * 32 + hh * 16;
+        float r[16];
+        tc::tmem_ld16(tS1 + lane_off + cb, r);
+        tc::st_sw128_8(sm + RV, 128, jv, cb, r);            // UTs
+        tc::st_sw128_8(sm + RV, 128, jv, cb + 8, r + 8);
+        tc::tmem_ld16(tS2 + lane_off + cb, r);
+        tc::st_sw128_8(sm + RK, 128, jv, cb, r);            // dUTs
+        tc::st_sw128_8(sm + RK, 128, jv, cb + 8, r + 8);
     }
     sync_for_mma();
     if (tid == 0) {
@@ -1201,44 +1206,48 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
     }
     if (!wait_all(&bars[2], ph, &s_fail)) goto done;
     {
-        float r[32];
-        // Z^T: dv = beta Z staged [t][dv] in RV (U^T is consumed); replay rows go to the
-        // replay-gradient buffer; unscaled Z^T tile in RG
-        tc::tmem_ld32(tS1 + lane_off + ch * 32, r);
-        __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + RV);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int t = ch * 32 + j;
-            const float x = vbeta[t] * r[j];
-            dvs[t * D + jv] = __float2bfloat16_rn(x);
-            if (t < t_own && t < t_end)
-                p.rep_grad[(static_cast<int64_t>(rptr + c0 + t) * H + h) * W + D + jv] = x;
-        }
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RG, 128, jv, ch * 32 + j, r + j);
-        // dP -> PmS (incl lower)
-        tc::tmem_ld32(tS2 + lane_off + ch * 32, r);
-        if (lg < 2) {
-            const int t = jv;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = (ch * 32 + j <= t) ? r[j] : 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + PmS, 64, t, ch * 32 + j, r + j);
-        }
-        // dT = dT' diag(beta), strict lower -> RK (dTm)
-        tc::tmem_ld32(tP1 + lane_off + ch * 32, r);
-        if (lg < 2) {
-            const int t = jv;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = (ch * 32 + j < t) ? r[j] * vbeta[ch * 32 + j] : 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + RK, 64, t, ch * 32 + j, r + j);
-        }
-        // sum_s (dK~ e^{Gamma_L-m})[dk][s] Km[s][dk] for dGamma_L
-        tc::tmem_ld32(tXm + lane_off + ch * 32, r);
         float acc = 0.f;
+        __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + RV);
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+            const int cb = ch * 32 + hh * 16;
+            float r[16];
+            // Z^T: dv = beta Z staged [t][dv] in RV (U^T is consumed); replay rows go to the
+            // replay-gradient buffer; unscaled Z^T tile in RG
+            tc::tmem_ld16(tS1 + lane_off + cb, r);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc += r[j] * sw_val(sm + Km, 64, ch * 32 + j, jv);
+            for (int j = 0; j < 16; ++j) {
+                const int t = cb + j;
+                const float x = vbeta[t] * r[j];
+                dvs[t * D + jv] = __float2bfloat16_rn(x);
+                if (t < t_own && t < t_end)
+                    p.rep_grad[(static_cast<int64_t>(rptr + c0 + t) * H + h) * W + D + jv] = x;
+            }
+            tc::st_sw128_8(sm + RG, 128, jv, cb, r);
+            tc::st_sw128_8(sm + RG, 128, jv, cb + 8, r + 8);
+            // dP -> PmS (incl lower)
+            tc::tmem_ld16(tS2 + lane_off + cb, r);
+            if (lg < 2) {
+                const int t = jv;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) r[j] = (cb + j <= t) ? r[j] : 0.f;
+                tc::st_sw128_8(sm + PmS, 64, t, cb, r);
+                tc::st_sw128_8(sm + PmS, 64, t, cb + 8, r + 8);
+            }
+            // dT = dT' diag(beta), strict lower -> RK (dTm)
+            tc::tmem_ld16(tP1 + lane_off + cb, r);
+            if (lg < 2) {
+                const int t = jv;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) r[j] = (cb + j < t) ? r[j] * vbeta[cb + j] : 0.f;
+                tc::st_sw128_8(sm + RK, 64, t, cb, r);
+                tc::st_sw128_8(sm + RK, 64, t, cb + 8, r + 8);
+            }
+            // sum_s (dK~ e^{Gamma_L-m})[dk][s] Km[s][dk] for dGamma_L
+            tc::tmem_ld16(tXm + lane_off + cb, r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc += r[j] * sw_val(sm + Km, 64, cb + j, jv);
+        }
         vdgl[ch * 128 + jv] = acc;
     }
     sync_for_mma();
@@ -1336,6 +1345,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc(BwdParams p, PlanDev pd
         __nv_bfloat16 *dgs = reinterpret_cast<__nv_bfloat16 *>(sm + dSekT);
         const int dk = jv;
         const float m = vm[dk];
+#pragma unroll 1
         for (int hc = 0; hc < 2; ++hc) {
             const int tb = ch * 32 + hc * 16;
             float xq[16], p1[16], p2[16], xm[16], gm[16];
