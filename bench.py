@@ -38,6 +38,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--expanded", action="store_true",
                     help="also time the same kernels on the trajectory-expanded input")
+    ap.add_argument("--nodewise", action="store_true",
+                    help="also time the same kernels on the node-wise plan of the forest")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -360,6 +362,9 @@ def run_ours(args):
     expanded = None
     if args.expanded:
         expanded = run_expanded(parent, seg_len, pl, x, wl, ms)
+    nodewise = None
+    if args.nodewise:
+        nodewise = run_nodewise(parent, seg_len, pl, x, wl, ms)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -383,6 +388,8 @@ def run_ours(args):
                     roofline=roofline, cpu_baseline=cpu, e2e=e2e, clocks=clk)
         if expanded:
             line["expanded"] = expanded
+        if nodewise:
+            line["nodewise"] = nodewise
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -427,6 +434,51 @@ def run_expanded(parent, seg_len, pl_tree, x, wl, tree_ms):
     ems = e0.elapsed_time(e1) / 3
     return dict(rows=int(pl.info["C"]), trajectories=n_traj, ms_per_step=round(ems, 3),
                 speedup_tree_vs_expanded=round(ems / tree_ms, 3))
+
+
+def run_nodewise(parent, seg_len, pl_tree, x, wl, tree_ms):
+    """Same kernels on the node-wise plan of the same forest (one sequence per segment,
+    one call per tree level, handoffs at segment ends): the pages' "Node-wise LA"
+    comparison.  The inputs are moved into that plan's row layout first (untimed)."""
+    import numpy as np
+    import torch
+    from prefix_shared_chunkwise_gb300.api import Plan, kda_bwd, kda_fwd
+    pl = Plan(parent, seg_len, wl.chunk, nodewise=True).upload()
+    so_t = pl_tree.arrays()["seg_offset"]
+    so_n = pl.arrays()["seg_offset"]
+    C = int(pl.info["C"])
+    rows = np.empty(C, np.int64)
+    for v in range(len(parent)):
+        rows[so_n[v]:so_n[v] + seg_len[v]] = so_t[v] + np.arange(seg_len[v])
+    H, D = wl.H, wl.dk
+    dev = x["q"].device
+    idx = torch.as_tensor(rows, device=dev)
+    xn = {k: t.index_select(0, idx) for k, t in x.items()}
+    o = torch.empty_like(xn["v"])
+    st = torch.empty((max(pl.info["n_states"], 1), H, D, D), dtype=torch.float32, device=dev)
+    cs = torch.empty(pl.chunk_state_bytes(H, D, D, 1) // 2, dtype=torch.bfloat16, device=dev)
+    grads = dict(dq=torch.empty_like(xn["q"]), dk=torch.empty_like(xn["k"]), dv=torch.empty_like(xn["v"]),
+                 dg=torch.empty_like(xn["g"]), dbeta=torch.empty_like(xn["beta"]))
+    wsb = torch.empty(max(pl.bwd_workspace_bytes(H, D, D), 256), dtype=torch.uint8, device=dev)
+
+    def step():
+        kda_fwd(pl, xn["q"], xn["k"], xn["v"], xn["g"], xn["beta"], o=o, states=st, chunk_states=cs)
+        kda_bwd(pl, xn["q"], xn["k"], xn["v"], xn["g"], xn["beta"], xn["W"], states=st,
+                chunk_states=cs, grads=grads, workspace=wsb)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    nms = e0.elapsed_time(e1) / 5
+    return dict(calls=int(pl.info["n_rounds"]), sequences=int(pl.info["n_seq"]),
+                states=int(pl.info["n_states"]), chunks=int(pl.info["n_chunks"]),
+                ms_per_step=round(nms, 3), speedup_tree_vs_nodewise=round(nms / tree_ms, 3))
 
 
 # ---- reference arm: the oracle on host cores ---------------------------------------------

@@ -66,7 +66,12 @@ typedef struct harts_plan harts_plan;          /* opaque, host memory, library-o
  * parent   host [n_seg]: parent[i] < i, or -1 for a root (forests allowed).
  * seg_len  host [n_seg]: tokens per segment, >= 1.
  * chunk    chunk length B >= 1 (the kernels support 16, 32, 64).
- * flags    0 (reserved).
+ * flags    0: the minimum-call plan below.  HARTS_PLAN_NODEWISE: the node-wise
+ *          baseline the pages compare against (one call per tree level; section 5,
+ *          Fig. 4 "Node-wise LA"): every segment is its own sequence, starting one
+ *          round after its parent from the parent sequence's end state (a slot at
+ *          that sequence's end), with its own chunk grid and no replay.  Any other
+ *          bit: HARTS_EINVAL.
  * out      receives a new plan; free it with harts_plan_free.
  *
  * The plan holds: the rounds (one packed call each; their number is the minimum
@@ -82,6 +87,8 @@ typedef struct harts_plan harts_plan;          /* opaque, host memory, library-o
  */
 int harts_plan_calls(int32_t n_seg, const int32_t *parent, const int64_t *seg_len,
                      int32_t chunk, uint32_t flags, harts_plan **out);
+
+#define HARTS_PLAN_NODEWISE 1u   /* harts_plan_calls flag: one sequence per segment */
 
 typedef struct {
     int32_t n_seg, n_roots, n_leaves, chunk;

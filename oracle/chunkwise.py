@@ -30,7 +30,8 @@ import numpy as np
 
 def chunk_fwd_seq(q, k, v, g, beta, S0, B, scale=1.0):
     """One sequence, one head. q,k,g: [L,dk]; v: [L,dv]; beta: [L]; S0: [dk,dv].
-    Returns (o [L,dv], states at local positions B,2B,... as a dict, final state)."""
+    Returns (o [L,dv], the state at every chunk end B, 2B, ... and at L, as a dict
+    keyed by local position, final state)."""
     L, dk = k.shape
     S = np.array(S0, dtype=np.float64)
     o = np.zeros((L, v.shape[1]))
@@ -53,8 +54,7 @@ def chunk_fwd_seq(q, k, v, g, beta, S0, B, scale=1.0):
         o[c0:c1] = (Q * np.exp(Gam)) @ S + np.tril(QK) @ U
         Kt = K * np.exp(Gam[-1][None, :] - Gam)
         S = np.exp(Gam[-1])[:, None] * S + Kt.T @ U
-        if c1 < L and c1 % B == 0:
-            bstates[c1] = S.copy()
+        bstates[c1] = S.copy()
     return o, bstates, S
 
 

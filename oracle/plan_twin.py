@@ -101,13 +101,20 @@ def min_calls(parent, seg_len, B):
     return dict(calls=calls, Tpre=Tpre, Tin=Tin, ctop=ctop, s=s, e=e, children=ch)
 
 
-def plan(parent, seg_len, B):
-    """Full plan: rounds, sequences, replay gather lists, state slots, layout."""
+def plan(parent, seg_len, B, nodewise=False):
+    """Full plan: rounds, sequences, replay gather lists, state slots, layout.
+
+    nodewise=True gives the node-wise baseline of the pages' comparison (section 5,
+    Fig. 4 "Node-wise LA"): no continuation anywhere, so every segment is a sequence;
+    a child starts one round after its parent from the state at the parent's end
+    (trajectory position e_v, not rounded to the chunk grid), replaying nothing."""
     parent = [int(x) for x in parent]
     seg_len = [int(x) for x in seg_len]
     n = len(parent)
     dp = min_calls(parent, seg_len, B)
     ch, ctop, s, e = dp["children"], dp["ctop"], dp["s"], dp["e"]
+    if nodewise:
+        ctop = [-1] * n
     roots = [i for i in range(n) if parent[i] < 0]
     root_idx = {r: j for j, r in enumerate(roots)}
 
@@ -127,8 +134,8 @@ def plan(parent, seg_len, B):
             for c in ch[v]:
                 if c == ctop[v]:
                     continue
-                a_e = B * (e[v] // B)
-                if a_e == anchor:
+                a_e = e[v] if nodewise else B * (e[v] // B)
+                if not nodewise and a_e == anchor:
                     work.append((c, rnd, anchor, src))
                 else:
                     pos = a_e - anchor
@@ -136,6 +143,8 @@ def plan(parent, seg_len, B):
                         slots.append(pos)
                     work.append((c, rnd + 1, a_e, ("slot", first, pos)))
             v = ctop[v]
+            if v < 0:          # node-wise: no continuation
+                break
         seqs.append(dict(first=first, round=rnd, anchor=anchor, src=src, chain=chain,
                          slots=sorted(slots)))
     seqs.sort(key=lambda d: (d["round"], d["first"]))

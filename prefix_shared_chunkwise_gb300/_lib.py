@@ -12,6 +12,7 @@ SO_PATH = os.path.join(_HERE, "_harts.so")
 
 HARTS_FP32, HARTS_BF16 = 0, 1
 HARTS_KERNEL_AUTO, HARTS_KERNEL_SIMT, HARTS_KERNEL_TC = 0, 1, 2
+HARTS_PLAN_NODEWISE = 1                       # harts_plan_calls flag
 
 ERRORS = {0: "HARTS_OK", -1: "HARTS_EINVAL", -2: "HARTS_EUNSUPPORTED", -3: "HARTS_EOVERFLOW",
           -4: "HARTS_ESMALLBUF", -5: "HARTS_ECUDA", -6: "HARTS_ETIMEOUT", -7: "HARTS_EDEVICE",

@@ -32,14 +32,18 @@ def _stream(stream):
 
 
 class Plan:
-    """harts_plan_calls + harts_plan_get_info / export / upload / free."""
+    """harts_plan_calls + harts_plan_get_info / export / upload / free.
 
-    def __init__(self, parent, seg_len, chunk: int):
+    nodewise=True asks for the node-wise plan (HARTS_PLAN_NODEWISE): one sequence per
+    segment, one round per tree level."""
+
+    def __init__(self, parent, seg_len, chunk: int, nodewise: bool = False):
         parent = np.ascontiguousarray(parent, np.int32)
         seg_len = np.ascontiguousarray(seg_len, np.int64)
         h = ctypes.c_void_p()
+        flags = L.HARTS_PLAN_NODEWISE if nodewise else 0
         rc = L.lib().harts_plan_calls(len(parent), parent.ctypes.data_as(L._pi32),
-                                      seg_len.ctypes.data_as(L._pi64), int(chunk), 0,
+                                      seg_len.ctypes.data_as(L._pi64), int(chunk), flags,
                                       ctypes.byref(h))
         L.check(rc, "harts_plan_calls")
         self._h = h

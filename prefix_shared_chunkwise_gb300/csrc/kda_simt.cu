@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(256) kda_fwd_simt(FwdParams p, PlanDev pd, int
             S[i] = el[c] * S[i] + ekt[c] * acc;
         }
         __syncthreads();
-        const int32_t pend = c0 + BC;
+        const int32_t pend = min(c0 + BC, L);     // a slot may sit at the sequence end
         if (sp < sp_end && pd.state_lpos[sp] == pend) {
             float *dst = p.states + (static_cast<int64_t>(sp) * H + h) * D * D;
             for (int i = tid; i < D * D; i += nth) dst[i] = S[i];
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(256) kda_bwd_simt(BwdParams p, PlanDev pd, int
     const int32_t sp_begin = pd.seq_sptr[seq];
     int32_t sp = pd.seq_sptr[seq + 1] - 1;
     for (int32_t ci = nch - 1; ci >= 0; --ci) {
-        const int32_t c0 = ci * BC, pend = c0 + BC;
+        const int32_t c0 = ci * BC, pend = min(c0 + BC, L);
         __syncthreads();
         // consumers of the boundary state at the end of this chunk add their gradients
         if (sp >= sp_begin && pd.state_lpos[sp] == pend) {

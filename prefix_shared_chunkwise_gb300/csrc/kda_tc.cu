@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
 #pragma unroll
             for (int j = 0; j < 32; ++j) os[(ch * 32 + j) * D + jv] = __float2bfloat16_rn(r[j]);
         }
-        const int32_t pend = c0 + BC;
+        const int32_t pend = min(c0 + BC, L);     // a slot may sit at the sequence end
         const bool slot = sp < sp_end && pd.state_lpos[sp] == pend;
         const bool last = ci == nch - 1;
         for (int hf = 0; hf < 2; ++hf) {
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
     stage_chunk(nch - 1, 0);
     for (int32_t ci = nch - 1; ci >= 0; --ci) {
         const uint32_t ph = (nch - 1 - ci) & 1;
-        const int32_t c0 = ci * BC, pend = c0 + BC, g = cbase + ci;
+        const int32_t c0 = ci * BC, pend = min(c0 + BC, L), g = cbase + ci;
         const int nv = min(BC, L - c0);
         const int mid = (nv - 1) / 2;
         const int buf = (nch - 1 - ci) & 1;

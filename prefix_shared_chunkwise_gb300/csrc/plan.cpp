@@ -30,7 +30,7 @@ constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
 
 int64_t floor_to(int64_t x, int64_t B) { return (x / B) * B; }
 
-int build(harts_plan &P, int32_t n, const int32_t *parent, const int64_t *len, int32_t B) {
+int build(harts_plan &P, int32_t n, const int32_t *parent, const int64_t *len, int32_t B, bool nodewise) {
     // ---- a1: validate, positions s_v, e_v --------------------------------------
     std::vector<int64_t> s(n), e(n);
     std::vector<int32_t> nkids(n, 0);
@@ -71,6 +71,11 @@ int build(harts_plan &P, int32_t n, const int32_t *parent, const int64_t *len, i
         tpre[v] = (floor_to(s[v], B) == floor_to(e[v], B)) ? m1 : tin[v];
     }
 
+    // Node-wise mode: no segment continues its parent's sequence; every segment is a
+    // sequence of its own that starts, one round after its parent, from the parent
+    // sequence's end state, with its own chunk grid and nothing replayed.
+    if (nodewise) std::fill(ctop.begin(), ctop.end(), -1);
+
     // ---- a2: top-down ASAP recovery ------------------------------------------------
     // Sequences are first identified by their first segment.  Per segment: the first
     // segment of its sequence.  Per first segment: round, anchor, source.
@@ -99,8 +104,8 @@ int build(harts_plan &P, int32_t n, const int32_t *parent, const int64_t *len, i
             int32_t c = kids[j];
             if (c == ctop[v]) { head[c] = f; continue; }
             head[c] = c;
-            const int64_t a_e = floor_to(e[v], B);
-            if (a_e == sq.anchor) {
+            const int64_t a_e = nodewise ? e[v] : floor_to(e[v], B);
+            if (!nodewise && a_e == sq.anchor) {
                 tmp[c] = sq;
                 tmp_src_slot[c] = tmp_src_slot[f];
             } else {
@@ -336,11 +341,11 @@ int harts_plan_calls(int32_t n_seg, const int32_t *parent, const int64_t *seg_le
     *out = nullptr;
     if (n_seg < 1 || !parent || !seg_len) { set_error("empty or NULL tree"); return HARTS_EINVAL; }
     if (chunk < 1 || chunk > (1 << 20)) { set_error("chunk must be >= 1"); return HARTS_EINVAL; }
-    if (flags != 0) { set_error("unknown flags"); return HARTS_EINVAL; }
+    if (flags & ~HARTS_PLAN_NODEWISE) { set_error("unknown flags"); return HARTS_EINVAL; }
     harts_plan *P = new (std::nothrow) harts_plan();
     if (!P) { set_error("out of host memory"); return HARTS_EINVAL; }
     try {
-        int rc = harts::build(*P, n_seg, parent, seg_len, chunk);
+        int rc = harts::build(*P, n_seg, parent, seg_len, chunk, (flags & HARTS_PLAN_NODEWISE) != 0);
         if (rc != HARTS_OK) { delete P; return rc; }
         harts::build_image(*P);
     } catch (const std::bad_alloc &) {

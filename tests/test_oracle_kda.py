@@ -167,3 +167,43 @@ def test_tree_execution_with_replay_equals_trajectories(seed):
     for s, chain in enumerate(pl["seq_chain"]):
         assert np.abs(fin[s] - r["final"][leaves.index(chain[-1])]).max() < 1e-12
 
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_nodewise_tree_execution_equals_trajectories(seed):
+    """Node-wise plans (one sequence per segment, handoff at each segment's exact end,
+    fresh chunk grid, no replay) compute the same outputs as the token recurrence; the
+    end state of every internal sequence is the state at that segment's end, which the
+    token recurrence gives at the first leaf below it (the path is shared)."""
+    rng = np.random.default_rng(200 + seed)
+    n = int(rng.integers(2, 14))
+    parent = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)], np.int32)
+    B = int(rng.choice([4, 8]))
+    seg_len = rng.integers(1, 3 * B, size=n).astype(np.int64)
+    pl = plan_twin.plan(parent, seg_len, B, nodewise=True)
+    assert pl["n_seq"] == n and pl["R"] == 0
+    depth = np.zeros(n, np.int64)
+    for i in range(n):
+        depth[i] = 0 if parent[i] < 0 else depth[parent[i]] + 1
+    assert pl["n_rounds"] == depth.max() + 1
+    q, k, v, g, b = _rand(rng, pl["C"], 2, 4, 3, decay=0.2)
+    r = oracle.kda_forest(parent, seg_len, pl["seg_offset"], q, k, v, g, b, chunk=B)
+    o, fin = chunkwise.tree_exec(pl, q, k, v, g, b, B)
+    assert np.abs(o - r["o"]).max() < 1e-12
+    leaves = [i for i in range(n) if not np.any(parent == i)]
+    for s, chain in enumerate(pl["seq_chain"]):
+        v_end = chain[-1]
+        if v_end in leaves:
+            assert np.abs(fin[s] - r["final"][leaves.index(v_end)]).max() < 1e-12
+        else:
+            # internal segment: run its path alone through the token recurrence
+            path = []
+            w = v_end
+            while w >= 0:
+                path.append(w)
+                w = parent[w]
+            rows = np.concatenate([np.arange(pl["seg_offset"][w], pl["seg_offset"][w] + seg_len[w])
+                                   for w in reversed(path)])
+            one = oracle.kda_forest(np.array([-1], np.int32), np.array([len(rows)]), np.array([0]),
+                                    q[rows], k[rows], v[rows], g[rows], b[rows], chunk=B)
+            assert np.abs(fin[s] - one["final"][0]).max() < 1e-12

@@ -39,9 +39,9 @@ KEYS = ["seg_offset", "seg_pos", "seg_seq", "round_seq_ptr", "cu_seqlens", "seq_
         "root_cons_ptr", "root_cons"]
 
 
-def _compare(parent, seg_len, B):
-    tw = plan_twin.plan(parent, seg_len, B)
-    pl = Plan(parent, seg_len, B)
+def _compare(parent, seg_len, B, nodewise=False):
+    tw = plan_twin.plan(parent, seg_len, B, nodewise=nodewise)
+    pl = Plan(parent, seg_len, B, nodewise=nodewise)
     ar = pl.arrays()
     info = pl.info
     assert info["n_rounds"] == tw["n_rounds"]
@@ -51,7 +51,7 @@ def _compare(parent, seg_len, B):
         np.testing.assert_array_equal(ar[k], tw[k], err_msg=k)
     np.testing.assert_array_equal(ar["seg_tpre"], tw["Tpre"])
     np.testing.assert_array_equal(ar["seg_tin"], tw["Tin"])
-    np.testing.assert_array_equal(ar["seg_ctop"], tw["ctop"])
+    np.testing.assert_array_equal(ar["seg_ctop"], [-1] * len(parent) if nodewise else tw["ctop"])
     return pl, tw
 
 
@@ -70,6 +70,45 @@ def test_planner_matches_oracle_random_forests():
                            for i in range(n)], np.int32)
         seg_len = rng.integers(1, 3 * B + 2, size=n).astype(np.int64)
         _compare(parent, seg_len, B)
+
+
+def test_nodewise_planner_matches_oracle_random_forests():
+    """HARTS_PLAN_NODEWISE: one sequence per segment, rounds = tree depth + 1, no replay,
+    every handoff at the producer sequence's end; bit-exact against the twin."""
+    rng = np.random.Generator(np.random.PCG64(22))
+    for _ in range(300):
+        n = int(rng.integers(1, 60))
+        B = int(rng.choice([1, 4, 16, 64]))
+        parent = np.array([-1 if (i == 0 or rng.random() < 0.08) else int(rng.integers(0, i))
+                           for i in range(n)], np.int32)
+        seg_len = rng.integers(1, 3 * B + 2, size=n).astype(np.int64)
+        pl, tw = _compare(parent, seg_len, B, nodewise=True)
+        depth = np.zeros(n, np.int64)
+        for i in range(n):
+            depth[i] = 0 if parent[i] < 0 else depth[parent[i]] + 1
+        info = pl.info
+        assert info["n_seq"] == n and info["R"] == 0 and info["n_rounds"] == depth.max() + 1
+        ar = pl.arrays()
+        seq_len = np.diff(ar["cu_seqlens"])
+        # every slot sits at its producer sequence's end
+        np.testing.assert_array_equal(ar["state_pos"], seq_len[ar["state_seq"]])
+
+
+@pytest.mark.parametrize("name", WORKLOAD_ORDER)
+def test_nodewise_planner_matches_oracle_on_workloads(name):
+    parent, seg_len = make_tree(name)
+    pl, tw = _compare(parent, seg_len, WORKLOADS[name].chunk, nodewise=True)
+    assert pl.info["n_rounds"] >= 1
+
+
+def test_planner_rejects_unknown_flags():
+    import ctypes
+    h = ctypes.c_void_p()
+    parent = np.array([-1, 0], np.int32)
+    seg_len = np.array([3, 4], np.int64)
+    rc = _lib.lib().harts_plan_calls(2, parent.ctypes.data_as(_lib._pi32), seg_len.ctypes.data_as(_lib._pi64),
+                                     16, 2, ctypes.byref(h))
+    assert rc == -1 and not h.value
 
 
 @pytest.mark.parametrize("name", WORKLOAD_ORDER)
