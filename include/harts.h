@@ -70,8 +70,13 @@ typedef struct harts_plan harts_plan;          /* opaque, host memory, library-o
  *          baseline the pages compare against (one call per tree level; section 5,
  *          Fig. 4 "Node-wise LA"): every segment is its own sequence, starting one
  *          round after its parent from the parent sequence's end state (a slot at
- *          that sequence's end), with its own chunk grid and no replay.  Any other
- *          bit: HARTS_EINVAL.
+ *          that sequence's end), with its own chunk grid and no replay.
+ *          HARTS_PLAN_NOREPLAY: the pages' no-replay comparison (section 5.3, Fig. 5):
+ *          the continuations of the minimum-call plan, but every side branch starts
+ *          one round after its producer from the producer's exact state at the fork
+ *          position e_v (usually inside a chunk), with its own chunk grid and no
+ *          replay; forward only (harts_kda_bwd returns HARTS_EUNSUPPORTED).
+ *          Both bits, or any other bit: HARTS_EINVAL.
  * out      receives a new plan; free it with harts_plan_free.
  *
  * The plan holds: the rounds (one packed call each; their number is the minimum
@@ -89,6 +94,7 @@ int harts_plan_calls(int32_t n_seg, const int32_t *parent, const int64_t *seg_le
                      int32_t chunk, uint32_t flags, harts_plan **out);
 
 #define HARTS_PLAN_NODEWISE 1u   /* harts_plan_calls flag: one sequence per segment */
+#define HARTS_PLAN_NOREPLAY 2u   /* harts_plan_calls flag: exact-position handoffs, no replay */
 
 typedef struct {
     int32_t n_seg, n_roots, n_leaves, chunk;
@@ -102,6 +108,7 @@ typedef struct {
     int64_t n_chunks;        /* chunks over all sequences, replay rows included */
     int32_t max_seq_chunks;  /* longest sequence in chunks */
     int32_t n_fold_rows;     /* distinct compact rows that are replayed */
+    uint32_t flags;          /* the harts_plan_calls flags the plan was built with */
 } harts_plan_info;
 
 int harts_plan_get_info(const harts_plan *plan, harts_plan_info *out);

@@ -28,10 +28,13 @@ from __future__ import annotations
 import numpy as np
 
 
-def chunk_fwd_seq(q, k, v, g, beta, S0, B, scale=1.0):
+def chunk_fwd_seq(q, k, v, g, beta, S0, B, scale=1.0, positions=()):
     """One sequence, one head. q,k,g: [L,dk]; v: [L,dv]; beta: [L]; S0: [dk,dv].
-    Returns (o [L,dv], the state at every chunk end B, 2B, ... and at L, as a dict
-    keyed by local position, final state)."""
+    Returns (o [L,dv], the state at every chunk end B, 2B, ... and at L, plus at each
+    local position in `positions` that falls inside a chunk, as a dict keyed by local
+    position, final state).  Inside a chunk, the state after its first r rows is the
+    chunk update restricted to those rows: diag(e^{Gamma_r}) S + K_r~^T U_r with
+    K_r~ = K e^{Gamma_r - Gamma} over rows < r."""
     L, dk = k.shape
     S = np.array(S0, dtype=np.float64)
     o = np.zeros((L, v.shape[1]))
@@ -52,6 +55,11 @@ def chunk_fwd_seq(q, k, v, g, beta, S0, B, scale=1.0):
         Wv = T @ (b[:, None] * V)
         U = Wv - Wk @ S
         o[c0:c1] = (Q * np.exp(Gam)) @ S + np.tril(QK) @ U
+        for pos in positions:
+            if c0 < pos < c1:
+                r = pos - c0
+                Kr = K[:r] * np.exp(Gam[r - 1][None, :] - Gam[:r])
+                bstates[pos] = np.exp(Gam[r - 1])[:, None] * S + Kr.T @ U[:r]
         Kt = K * np.exp(Gam[-1][None, :] - Gam)
         S = np.exp(Gam[-1])[:, None] * S + Kt.T @ U
         bstates[c1] = S.copy()
@@ -84,7 +92,7 @@ def tree_exec(pl, q, k, v, g, beta, B, scale=1.0, h0=None):
                 else:
                     S0 = np.zeros((dk, dv))
                 oo, bst, Sf = chunk_fwd_seq(q[rows, h], k[rows, h], v[rows, h], g[rows, h],
-                                            beta[rows, h], S0, B, scale)
+                                            beta[rows, h], S0, B, scale, positions=tuple(want))
                 o[rows[rho:], h] = oo[rho:]
                 for pos, j in want.items():
                     slots[j, h] = bst[pos]

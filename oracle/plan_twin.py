@@ -101,13 +101,18 @@ def min_calls(parent, seg_len, B):
     return dict(calls=calls, Tpre=Tpre, Tin=Tin, ctop=ctop, s=s, e=e, children=ch)
 
 
-def plan(parent, seg_len, B, nodewise=False):
+def plan(parent, seg_len, B, nodewise=False, noreplay=False):
     """Full plan: rounds, sequences, replay gather lists, state slots, layout.
 
     nodewise=True gives the node-wise baseline of the pages' comparison (section 5,
     Fig. 4 "Node-wise LA"): no continuation anywhere, so every segment is a sequence;
     a child starts one round after its parent from the state at the parent's end
-    (trajectory position e_v, not rounded to the chunk grid), replaying nothing."""
+    (trajectory position e_v, not rounded to the chunk grid), replaying nothing.
+
+    noreplay=True gives the no-replay comparison of section 5.3 / Fig. 5: the same
+    continuations, but every side branch starts one round after its producer from the
+    producer's exact state at e_v (a position inside a chunk in general), with its own
+    chunk grid and nothing replayed."""
     parent = [int(x) for x in parent]
     seg_len = [int(x) for x in seg_len]
     n = len(parent)
@@ -134,8 +139,9 @@ def plan(parent, seg_len, B, nodewise=False):
             for c in ch[v]:
                 if c == ctop[v]:
                     continue
-                a_e = e[v] if nodewise else B * (e[v] // B)
-                if not nodewise and a_e == anchor:
+                exact = nodewise or noreplay
+                a_e = e[v] if exact else B * (e[v] // B)
+                if not exact and a_e == anchor:
                     work.append((c, rnd, anchor, src))
                 else:
                     pos = a_e - anchor

@@ -12,7 +12,8 @@ SO_PATH = os.path.join(_HERE, "_harts.so")
 
 HARTS_FP32, HARTS_BF16 = 0, 1
 HARTS_KERNEL_AUTO, HARTS_KERNEL_SIMT, HARTS_KERNEL_TC = 0, 1, 2
-HARTS_PLAN_NODEWISE = 1                       # harts_plan_calls flag
+HARTS_PLAN_NODEWISE = 1                       # harts_plan_calls flags
+HARTS_PLAN_NOREPLAY = 2
 
 ERRORS = {0: "HARTS_OK", -1: "HARTS_EINVAL", -2: "HARTS_EUNSUPPORTED", -3: "HARTS_EOVERFLOW",
           -4: "HARTS_ESMALLBUF", -5: "HARTS_ECUDA", -6: "HARTS_ETIMEOUT", -7: "HARTS_EDEVICE",
@@ -34,7 +35,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("n_seg", _i32), ("n_roots", _i32), ("n_leaves", _i32), ("chunk", _i32),
                 ("n_rounds", _i32), ("n_seq", _i32), ("n_states", _i32), ("n_cons", _i32),
                 ("C", _i64), ("S", _i64), ("R", _i64), ("n_chunks", _i64),
-                ("max_seq_chunks", _i32), ("n_fold_rows", _i32)]
+                ("max_seq_chunks", _i32), ("n_fold_rows", _i32), ("flags", ctypes.c_uint32)]
 
 
 PLAN_ARRAY_FIELDS = [

@@ -35,13 +35,14 @@ class Plan:
     """harts_plan_calls + harts_plan_get_info / export / upload / free.
 
     nodewise=True asks for the node-wise plan (HARTS_PLAN_NODEWISE): one sequence per
-    segment, one round per tree level."""
+    segment, one round per tree level.  noreplay=True asks for the no-replay plan
+    (HARTS_PLAN_NOREPLAY, forward only): side branches start from the exact fork state."""
 
-    def __init__(self, parent, seg_len, chunk: int, nodewise: bool = False):
+    def __init__(self, parent, seg_len, chunk: int, nodewise: bool = False, noreplay: bool = False):
         parent = np.ascontiguousarray(parent, np.int32)
         seg_len = np.ascontiguousarray(seg_len, np.int64)
         h = ctypes.c_void_p()
-        flags = L.HARTS_PLAN_NODEWISE if nodewise else 0
+        flags = (L.HARTS_PLAN_NODEWISE if nodewise else 0) | (L.HARTS_PLAN_NOREPLAY if noreplay else 0)
         rc = L.lib().harts_plan_calls(len(parent), parent.ctypes.data_as(L._pi32),
                                       seg_len.ctypes.data_as(L._pi64), int(chunk), flags,
                                       ctypes.byref(h))

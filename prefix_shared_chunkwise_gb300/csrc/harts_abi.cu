@@ -178,6 +178,10 @@ static int kda_bwd_phases(const harts_plan *P, const harts_kda_bwd_args *a, hart
     if (!a) { set_error("NULL args"); return HARTS_EINVAL; }
     int rc = check_fwd_args(P, &a->fwd);
     if (rc) return rc;
+    if (P->info.flags & HARTS_PLAN_NOREPLAY) {
+        set_error("no-replay plans are forward only");
+        return HARTS_EUNSUPPORTED;
+    }
     if (!a->d_o || !a->dq || !a->dk || !a->dv || !a->dg || !a->dbeta) { set_error("NULL gradient pointer"); return HARTS_EINVAL; }
     if (!a->fwd.chunk_states) { set_error("chunk_states from the forward pass are required"); return HARTS_EINVAL; }
     const int D = a->fwd.dk, H = a->fwd.H, BC = P->info.chunk;

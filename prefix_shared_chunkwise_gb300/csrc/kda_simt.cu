@@ -199,6 +199,31 @@ __global__ void __launch_bounds__(256) kda_fwd_simt(FwdParams p, PlanDev pd, int
             st_out(o, (row * H + h) * D + j, acc);
         }
         __syncthreads();
+        // slots inside this chunk (no-replay plans): the state after the chunk's first r
+        // rows, diag(e^{Gamma_{r-1}}) S + (K e^{Gamma_{r-1} - Gamma})_{<r}^T U_{<r}, as
+        // e^{Gamma_{r-1} - Gamma_L} (diag(e^{Gamma_L}) S + e^{Gamma_L - m} Km_{<r}^T U_{<r}),
+        // the first factor from the raw g rows r .. end of chunk
+        while (sp < sp_end && pd.state_lpos[sp] < min(c0 + BC, L)) {
+            __shared__ float s_gp[D];
+            const int r = pd.state_lpos[sp] - c0;       // 1 <= r < rows of this chunk
+            const int nv = min(BC, L - c0);
+            for (int c = tid; c < D; c += nth) {
+                float sum = 0.f;
+                for (int t = r; t < nv; ++t)
+                    sum += ld_in(static_cast<const T *>(p.g), (local_row(pd, seq, rho, L, c0 + t) * H + h) * D + c);
+                s_gp[c] = __expf(-sum);
+            }
+            __syncthreads();
+            float *dst = p.states + (static_cast<int64_t>(sp) * H + h) * D * D;
+            for (int i = tid; i < D * D; i += nth) {
+                const int c = i / D, j = i % D;
+                float acc = 0.f;
+                for (int t = 0; t < r; ++t) acc += Km[t * D + c] * V[t * D + j];
+                dst[i] = s_gp[c] * (el[c] * S[i] + ekt[c] * acc);
+            }
+            __syncthreads();
+            ++sp;
+        }
         // S <- diag(e^{Gamma_L}) S + Kt^T U
         for (int i = tid; i < D * D; i += nth) {
             const int c = i / D, j = i % D;

@@ -52,13 +52,18 @@ constexpr uint32_t SQ = Stage, SK = Stage + 16384, SV = Stage + 32768, SG = Stag
 constexpr uint32_t SBeta = Stage + 65536;   // [64] 32-bit words holding the bf16 beta
 constexpr uint32_t SBpar = SBeta + 256;     // [64] int: which half of the word
 constexpr uint32_t Vec = SBpar + 256;       // fp32 vectors
-constexpr uint32_t vBeta = Vec, vEl = vBeta + 64 * 4, vT0 = vEl + 128 * 4, vT1 = vT0 + 128 * 4,
-                   vM = vT1 + 128 * 4, vPart = vM + 128 * 4, vEnd = vPart + 4 * 128 * 4;
+constexpr uint32_t vBeta = Vec, vEl = vBeta + 64 * 4, vGp = vEl + 128 * 4, vM = vGp + 256 * 4,
+                   vPart = vM + 128 * 4, vEnd = vPart + 4 * 128 * 4;
 constexpr uint32_t bytes = vEnd + 1024;     // + alignment slack
 }  // namespace fwd_sm
 
 // fp32 64x64 scratch index with a per-row XOR so that column-wise access is conflict-free.
 __device__ __forceinline__ int fidx(int t, int s) { return t * 64 + (s ^ (t & 31)); }
+
+// Element (r, c) of a [rows][*] 128-byte-swizzled bf16 tile.
+__device__ __forceinline__ float sw_val(const uint8_t *tile, int rows, int r, int c) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + tc::sw128_offset(rows, r, c)));
+}
 
 __device__ __forceinline__ void st_bf16(uint8_t *tile, int rows, int row, int col, float x) {
     *reinterpret_cast<__nv_bfloat16 *>(tile + tc::sw128_offset(rows, row, col)) =
@@ -200,7 +205,8 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
     __shared__ int s_fail;
     __shared__ int s_rows[64];
     float *vbeta = reinterpret_cast<float *>(sm + vBeta), *vel = reinterpret_cast<float *>(sm + vEl),
-          *vm = reinterpret_cast<float *>(sm + vM), *vpart = reinterpret_cast<float *>(sm + vPart);
+          *vm = reinterpret_cast<float *>(sm + vM), *vpart = reinterpret_cast<float *>(sm + vPart),
+          *vgp = reinterpret_cast<float *>(sm + vGp);
     float *Mfp = reinterpret_cast<float *>(sm + Mf), *Tfp = reinterpret_cast<float *>(sm + Tf);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, ch = warp >> 2;
@@ -425,6 +431,40 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
             for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + UTs, 128, jv, ch * 32 + j, r + j);
         }
         sync_for_mma();
+        // ---- slots inside this chunk (no-replay plans) ------------------------------------
+        // The state after the chunk's first r rows is diag(e^{Gamma_{r-1}}) S +
+        // (K e^{Gamma_{r-1} - Gamma})_{<r}^T U_{<r}.  TMEM holds S^T diag(e^{Gamma_L}) until
+        // the update MMA below, and KtT = (K e^{Gamma_L - Gamma})^T, so its transpose is
+        // (S^T diag(e^{Gamma_L}) + U_{<r}^T Kt_{<r}) diag(e^{Gamma_{r-1} - Gamma_L}), the last
+        // factor from the raw g rows r .. nv-1 (read through the plan: the row table
+        // already holds the next chunk).  Thread (dv = jv, 64 key channels per half).
+        while (sp < sp_end && pd.state_lpos[sp] < min(c0 + BC, L)) {
+            const int r = pd.state_lpos[sp] - c0;       // 1 <= r < nv
+            if (tid < 128) {
+                float sum = 0.f;
+                for (int t = r; t < nv; ++t) {
+                    const int64_t row = local_row(pd, seq, rho, L, c0 + t);
+                    sum += __bfloat162float(static_cast<const __nv_bfloat16 *>(p.g)[(row * H + h) * D + tid]);
+                }
+                vgp[tid] = __expf(-sum);
+            }
+            __syncthreads();
+            float *dst = p.states + (static_cast<int64_t>(sp) * H + h) * D * D;
+            for (int hf = 0; hf < 2; ++hf) {
+                float rr[32];
+                const int cb = ch * 64 + hf * 32;
+                tc::tmem_ld32(tST + lane_off + cb, rr);
+                for (int t = 0; t < r; ++t) {
+                    const float u = sw_val(sm + UTs, 128, jv, t);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) rr[j] += u * sw_val(sm + KtT, 128, cb + j, t);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dst[(cb + j) * D + jv] = rr[j] * vgp[cb + j];
+            }
+            ++sp;
+            sync_for_mma();     // TMEM reads and vgp done before the next slot or the update MMA
+        }
         if (tid == 0) {
             tc::mma_tile(tOT, tc::smem_addr(sm + UTs), 128 * 128, tc::smem_addr(sm + Pm), 64 * 128,
                          64, tc::idesc_bf16(128, 64), true);
@@ -507,9 +547,6 @@ __device__ __forceinline__ uint32_t piece64(int t, int p) {
 // 16-byte piece p of row r of a [128 rows][128 cols] SW128 tile.
 __device__ __forceinline__ uint32_t piece128(int r, int p) {
     return static_cast<uint32_t>((p >> 3) * 16384 + r * 128 + (((p & 7) ^ (r & 7)) << 4));
-}
-__device__ __forceinline__ float sw_val(const uint8_t *tile, int rows, int r, int c) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + tc::sw128_offset(rows, r, c)));
 }
 
 template <int N>

@@ -30,7 +30,8 @@ constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
 
 int64_t floor_to(int64_t x, int64_t B) { return (x / B) * B; }
 
-int build(harts_plan &P, int32_t n, const int32_t *parent, const int64_t *len, int32_t B, bool nodewise) {
+int build(harts_plan &P, int32_t n, const int32_t *parent, const int64_t *len, int32_t B, uint32_t flags) {
+    const bool nodewise = (flags & HARTS_PLAN_NODEWISE) != 0, noreplay = (flags & HARTS_PLAN_NOREPLAY) != 0;
     // ---- a1: validate, positions s_v, e_v --------------------------------------
     std::vector<int64_t> s(n), e(n);
     std::vector<int32_t> nkids(n, 0);
@@ -104,8 +105,11 @@ int build(harts_plan &P, int32_t n, const int32_t *parent, const int64_t *len, i
             int32_t c = kids[j];
             if (c == ctop[v]) { head[c] = f; continue; }
             head[c] = c;
-            const int64_t a_e = nodewise ? e[v] : floor_to(e[v], B);
-            if (!nodewise && a_e == sq.anchor) {
+            // No-replay mode: side branches resume at the exact fork position from the
+            // producer's state there, so none can start in the producer's round.
+            const bool exact = nodewise || noreplay;
+            const int64_t a_e = exact ? e[v] : floor_to(e[v], B);
+            if (!exact && a_e == sq.anchor) {
                 tmp[c] = sq;
                 tmp_src_slot[c] = tmp_src_slot[f];
             } else {
@@ -257,6 +261,7 @@ int build(harts_plan &P, int32_t n, const int32_t *parent, const int64_t *len, i
     }
 
     P.seg_ctop = ctop; P.seg_tpre = tpre; P.seg_tin = tin;
+    P.info.flags = flags;
     return HARTS_OK;
 }
 
@@ -341,11 +346,14 @@ int harts_plan_calls(int32_t n_seg, const int32_t *parent, const int64_t *seg_le
     *out = nullptr;
     if (n_seg < 1 || !parent || !seg_len) { set_error("empty or NULL tree"); return HARTS_EINVAL; }
     if (chunk < 1 || chunk > (1 << 20)) { set_error("chunk must be >= 1"); return HARTS_EINVAL; }
-    if (flags & ~HARTS_PLAN_NODEWISE) { set_error("unknown flags"); return HARTS_EINVAL; }
+    if ((flags & ~(HARTS_PLAN_NODEWISE | HARTS_PLAN_NOREPLAY)) ||
+        flags == (HARTS_PLAN_NODEWISE | HARTS_PLAN_NOREPLAY)) {
+        set_error("unknown or conflicting flags"); return HARTS_EINVAL;
+    }
     harts_plan *P = new (std::nothrow) harts_plan();
     if (!P) { set_error("out of host memory"); return HARTS_EINVAL; }
     try {
-        int rc = harts::build(*P, n_seg, parent, seg_len, chunk, (flags & HARTS_PLAN_NODEWISE) != 0);
+        int rc = harts::build(*P, n_seg, parent, seg_len, chunk, flags);
         if (rc != HARTS_OK) { delete P; return rc; }
         harts::build_image(*P);
     } catch (const std::bad_alloc &) {

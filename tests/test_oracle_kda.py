@@ -207,3 +207,24 @@ def test_nodewise_tree_execution_equals_trajectories(seed):
             one = oracle.kda_forest(np.array([-1], np.int32), np.array([len(rows)]), np.array([0]),
                                     q[rows], k[rows], v[rows], g[rows], b[rows], chunk=B)
             assert np.abs(fin[s] - one["final"][0]).max() < 1e-12
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_noreplay_tree_execution_equals_trajectories(seed):
+    """No-replay plans (side branches resume at the exact fork position from the
+    producer's state there, no replay, own chunk grid) compute the same outputs and
+    final states as the token recurrence; the handoff states are taken inside chunks."""
+    rng = np.random.default_rng(300 + seed)
+    n = int(rng.integers(2, 14))
+    parent = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)], np.int32)
+    B = int(rng.choice([4, 8]))
+    seg_len = rng.integers(1, 3 * B, size=n).astype(np.int64)
+    pl = plan_twin.plan(parent, seg_len, B, noreplay=True)
+    assert pl["R"] == 0
+    q, k, v, g, b = _rand(rng, pl["C"], 2, 4, 3, decay=0.2)
+    r = oracle.kda_forest(parent, seg_len, pl["seg_offset"], q, k, v, g, b, chunk=B)
+    o, fin = chunkwise.tree_exec(pl, q, k, v, g, b, B)
+    assert np.abs(o - r["o"]).max() < 1e-12
+    leaves = [i for i in range(n) if not np.any(parent == i)]
+    for s, chain in enumerate(pl["seq_chain"]):
+        assert np.abs(fin[s] - r["final"][leaves.index(chain[-1])]).max() < 1e-12

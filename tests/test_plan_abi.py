@@ -101,14 +101,42 @@ def test_nodewise_planner_matches_oracle_on_workloads(name):
     assert pl.info["n_rounds"] >= 1
 
 
-def test_planner_rejects_unknown_flags():
+@pytest.mark.parametrize("flags", [4, _lib.HARTS_PLAN_NODEWISE | _lib.HARTS_PLAN_NOREPLAY])
+def test_planner_rejects_unknown_or_conflicting_flags(flags):
     import ctypes
     h = ctypes.c_void_p()
     parent = np.array([-1, 0], np.int32)
     seg_len = np.array([3, 4], np.int64)
     rc = _lib.lib().harts_plan_calls(2, parent.ctypes.data_as(_lib._pi32), seg_len.ctypes.data_as(_lib._pi64),
-                                     16, 2, ctypes.byref(h))
+                                     16, flags, ctypes.byref(h))
     assert rc == -1 and not h.value
+
+
+def test_noreplay_planner_matches_oracle_random_forests():
+    """HARTS_PLAN_NOREPLAY: the minimum-call continuations, side branches one round after
+    their producer at the exact fork position, no replay; bit-exact against the twin."""
+    rng = np.random.Generator(np.random.PCG64(23))
+    for _ in range(300):
+        n = int(rng.integers(1, 60))
+        B = int(rng.choice([1, 4, 16, 64]))
+        parent = np.array([-1 if (i == 0 or rng.random() < 0.08) else int(rng.integers(0, i))
+                           for i in range(n)], np.int32)
+        seg_len = rng.integers(1, 3 * B + 2, size=n).astype(np.int64)
+        tw = plan_twin.plan(parent, seg_len, B, noreplay=True)
+        pl = Plan(parent, seg_len, B, noreplay=True)
+        ar = pl.arrays()
+        info = pl.info
+        assert info["flags"] == _lib.HARTS_PLAN_NOREPLAY and info["R"] == 0
+        assert info["n_rounds"] == tw["n_rounds"] and info["n_seq"] == tw["n_seq"]
+        for k in KEYS:
+            np.testing.assert_array_equal(ar[k], tw[k], err_msg=k)
+        np.testing.assert_array_equal(ar["seg_ctop"], tw["ctop"])
+        # a side branch's source slot sits at its fork position in the producer sequence
+        for i in range(info["n_seq"]):
+            if ar["seq_src"][i] >= 0:
+                j = ar["seq_src"][i]
+                prod = ar["state_seq"][j]
+                assert ar["seq_anchor"][prod] + ar["state_pos"][j] == ar["seq_anchor"][i]
 
 
 @pytest.mark.parametrize("name", WORKLOAD_ORDER)
