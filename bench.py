@@ -38,6 +38,9 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--expanded", action="store_true",
                     help="also time the same kernels on the trajectory-expanded input")
+    ap.add_argument("--fidelity", action="store_true",
+                    help="also compare the forward outputs of the tree plans with the "
+                         "per-trajectory run, by handoff depth")
     ap.add_argument("--nodewise", action="store_true",
                     help="also time the same kernels on the node-wise plan of the forest")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -365,6 +368,9 @@ def run_ours(args):
     nodewise = None
     if args.nodewise:
         nodewise = run_nodewise(parent, seg_len, pl, x, wl, ms)
+    fidelity = None
+    if args.fidelity:
+        fidelity = run_fidelity(parent, seg_len, pl, x, wl)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -390,6 +396,8 @@ def run_ours(args):
             line["expanded"] = expanded
         if nodewise:
             line["nodewise"] = nodewise
+        if fidelity:
+            line["fidelity"] = fidelity
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -479,6 +487,93 @@ def run_nodewise(parent, seg_len, pl_tree, x, wl, tree_ms):
     return dict(calls=int(pl.info["n_rounds"]), sequences=int(pl.info["n_seq"]),
                 states=int(pl.info["n_states"]), chunks=int(pl.info["n_chunks"]),
                 ms_per_step=round(nms, 3), speedup_tree_vs_nodewise=round(nms / tree_ms, 3))
+
+
+def run_fidelity(parent, seg_len, pl_tree, x, wl):
+    """Forward outputs of the tree plans against the per-trajectory run of the same
+    kernels (every root-to-leaf trajectory its own sequence, chunk grid from its start):
+    the pages' replay-vs-no-replay fidelity comparison (section 5.3, Fig. 5), with the
+    per-trajectory run as the baseline.  Per handoff depth (sequence boundaries on the
+    path from the root to a row's segment, in each plan): rows, rel. L2 and max |diff|
+    of o, and the fraction of rows bit-identical to the baseline."""
+    import numpy as np
+    import torch
+    from prefix_shared_chunkwise_gb300.api import Plan, kda_fwd
+    from prefix_shared_chunkwise_gb300.synth import expand_rows
+    n = len(parent)
+    so_t = pl_tree.arrays()["seg_offset"]
+    rows, ptr, _ = expand_rows(parent, seg_len, so_t)
+    dev = x["q"].device
+    keys = ("q", "k", "v", "g", "beta")
+
+    def fwd(pl, xx):
+        o = torch.empty_like(xx["v"])
+        st = torch.empty((max(pl.info["n_states"], 1), wl.H, wl.dk, wl.dv), dtype=torch.float32, device=dev)
+        kda_fwd(pl, xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], o=o, states=st)
+        torch.cuda.synchronize()
+        return o
+
+    # baseline: one root sequence per trajectory
+    idx = torch.as_tensor(rows, device=dev)
+    n_traj = len(ptr) - 1
+    pl_e = Plan(-np.ones(n_traj, np.int32), np.diff(ptr).astype(np.int64), wl.chunk).upload()
+    o_base = fwd(pl_e, {k: x[k].index_select(0, idx) for k in keys})
+    # segment of every compact row of the tree layout
+    seg_of_row = np.empty(int(pl_tree.info["C"]), np.int64)
+    for v in range(n):
+        seg_of_row[so_t[v]:so_t[v] + seg_len[v]] = v
+    seg_of_exp = seg_of_row[rows]
+
+    def depth_of(pl):
+        ss = pl.arrays()["seg_seq"]
+        d = np.zeros(n, np.int64)
+        for v in range(n):
+            d[v] = 0 if parent[v] < 0 else d[parent[v]] + (ss[v] != ss[parent[v]])
+        return d
+
+    # the baseline's own spread: a shared row computed in several trajectories (with
+    # different chunk-mates where the trajectories fork) against its first occurrence
+    _, first = np.unique(rows, return_index=True)
+    first_of = np.empty(int(pl_tree.info["C"]), np.int64)
+    first_of[rows[first]] = first
+    o_first = o_base.index_select(0, torch.as_tensor(first_of[rows], device=dev))
+    out = {}
+    d_row = depth_of(pl_tree)[seg_of_exp]
+    spread = {}
+    for dd in range(int(d_row.max()) + 1):
+        sel = torch.as_tensor(np.nonzero(d_row == dd)[0], device=dev)
+        if sel.numel() == 0:
+            continue
+        a_, b_ = o_first.index_select(0, sel), o_base.index_select(0, sel)
+        spread[str(dd)] = dict(rel_l2=float((a_.float() - b_.float()).norm() / b_.float().norm()),
+                               bit_identical=round(float((a_ == b_).all(dim=2).all(dim=1).float().mean()), 6))
+    out["baseline_spread"] = dict(by_handoff_depth=spread)
+    for name, kw in (("harts", {}), ("noreplay", {"noreplay": True})):
+        pl = pl_tree if not kw else Plan(parent, seg_len, wl.chunk, **kw).upload()
+        so = pl.arrays()["seg_offset"]
+        t2p = np.empty(int(pl.info["C"]), np.int64)     # tree-layout row -> this plan's row
+        for v in range(n):
+            t2p[so_t[v]:so_t[v] + seg_len[v]] = so[v] + np.arange(seg_len[v])
+        p2t = np.empty_like(t2p)
+        p2t[t2p] = np.arange(len(t2p))
+        xp = {k: x[k].index_select(0, torch.as_tensor(p2t, device=dev)) for k in keys}
+        o_p = fwd(pl, xp).index_select(0, torch.as_tensor(t2p[rows], device=dev))
+        d_row = depth_of(pl)[seg_of_exp]
+        per = {}
+        for dd in range(int(d_row.max()) + 1):
+            sel = torch.as_tensor(np.nonzero(d_row == dd)[0], device=dev)
+            if sel.numel() == 0:
+                continue
+            op, ob = o_p.index_select(0, sel), o_base.index_select(0, sel)
+            df = op.float() - ob.float()
+            same = (op == ob).all(dim=2).all(dim=1)
+            ob = ob.float()
+            per[str(dd)] = dict(rows=int(sel.numel()),
+                                rel_l2=float(df.norm() / ob.norm()),
+                                max_abs=float(df.abs().max()),
+                                bit_identical=round(float(same.float().mean()), 6))
+        out[name] = dict(calls=int(pl.info["n_rounds"]), by_handoff_depth=per)
+    return out
 
 
 # ---- reference arm: the oracle on host cores ---------------------------------------------
