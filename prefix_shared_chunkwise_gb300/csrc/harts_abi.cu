@@ -115,7 +115,7 @@ int harts_plan_upload(harts_plan *P, void *dev_buf, size_t bytes, harts_stream_t
     v.chunk_seq = w + I.off_chunk_seq;
     v.n_rounds = P->info.n_rounds; v.n_seq = P->info.n_seq; v.n_states = P->info.n_states;
     v.n_roots = P->info.n_roots; v.n_fold = P->info.n_fold_rows; v.chunk = P->info.chunk;
-    v.R = P->info.R; v.n_chunks = P->info.n_chunks; v.C = P->info.C;
+    v.R = P->info.R; v.n_chunks = P->info.n_chunks; v.C = P->info.C; v.flags = P->info.flags;
     set_error("");
     return HARTS_OK;
 }

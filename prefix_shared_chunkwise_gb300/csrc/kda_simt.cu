@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(256) kda_fwd_simt(FwdParams p, PlanDev pd, int
         // rows, diag(e^{Gamma_{r-1}}) S + (K e^{Gamma_{r-1} - Gamma})_{<r}^T U_{<r}, as
         // e^{Gamma_{r-1} - Gamma_L} (diag(e^{Gamma_L}) S + e^{Gamma_L - m} Km_{<r}^T U_{<r}),
         // the first factor from the raw g rows r .. end of chunk
-        while (sp < sp_end && pd.state_lpos[sp] < min(c0 + BC, L)) {
+        while ((pd.flags & HARTS_PLAN_NOREPLAY) && sp < sp_end && pd.state_lpos[sp] < min(c0 + BC, L)) {
             __shared__ float s_gp[D];
             const int r = pd.state_lpos[sp] - c0;       // 1 <= r < rows of this chunk
             const int nv = min(BC, L - c0);

@@ -196,6 +196,9 @@ __device__ __forceinline__ void st_bf16x2(uint8_t *tile, int rows, int row, int 
     *reinterpret_cast<uint32_t *>(tile + tc::sw128_offset(rows, row, col)) = tc::pack_bf16(a, b);
 }
 
+// kInner: the plan may put slots inside a chunk (no-replay plans); the minimum-call and
+// node-wise plans never do, and their instance carries none of that code.
+template <bool kInner>
 __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int32_t round_base) {
     using namespace fwd_sm;
     extern __shared__ uint8_t smraw[];
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
         // (S^T diag(e^{Gamma_L}) + U_{<r}^T Kt_{<r}) diag(e^{Gamma_{r-1} - Gamma_L}), the last
         // factor from the raw g rows r .. nv-1 (read through the plan: the row table
         // already holds the next chunk).  Thread (dv = jv, 64 key channels per half).
-        while (sp < sp_end && pd.state_lpos[sp] < min(c0 + BC, L)) {
+        while (kInner && sp < sp_end && pd.state_lpos[sp] < min(c0 + BC, L)) {
             const int r = pd.state_lpos[sp] - c0;       // 1 <= r < nv
             if (tid < 128) {
                 float sum = 0.f;
@@ -1495,10 +1498,15 @@ bool tc_supported(bool, int dtype, int Dd, int BCc) {
 
 cudaError_t tc_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, int32_t n_items,
                          int32_t, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(kda_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool inner = (pd.flags & HARTS_PLAN_NOREPLAY) != 0;
+    cudaError_t e = cudaFuncSetAttribute(inner ? kda_fwd_tc<true> : kda_fwd_tc<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(fwd_sm::bytes));
     if (e != cudaSuccess) return e;
-    kda_fwd_tc<<<n_items, NT, fwd_sm::bytes, st>>>(p, pd, base);
+    if (inner)
+        kda_fwd_tc<true><<<n_items, NT, fwd_sm::bytes, st>>>(p, pd, base);
+    else
+        kda_fwd_tc<false><<<n_items, NT, fwd_sm::bytes, st>>>(p, pd, base);
     return cudaGetLastError();
 }
 

@@ -31,6 +31,7 @@ struct PlanDev {
     const int32_t *fold_occ;       // [R] replay occurrence ids grouped by row
     const int32_t *chunk_seq;      // [n_chunks] sequence of every chunk
     int32_t n_rounds, n_seq, n_states, n_roots, n_fold, chunk;
+    uint32_t flags;                // harts_plan_calls flags (HARTS_PLAN_NOREPLAY: slots inside chunks)
     int64_t R, n_chunks, C;
 };
 
