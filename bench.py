@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--fidelity", action="store_true",
                     help="also compare the forward outputs of the tree plans with the "
                          "per-trajectory run, by handoff depth")
+    ap.add_argument("--conv", action="store_true",
+                    help="also time the short convolution (fwd, bwd) on the forest's q")
     ap.add_argument("--nodewise", action="store_true",
                     help="also time the same kernels on the node-wise plan of the forest")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -368,6 +370,9 @@ def run_ours(args):
     nodewise = None
     if args.nodewise:
         nodewise = run_nodewise(parent, seg_len, pl, x, wl, ms)
+    conv = None
+    if args.conv:
+        conv = run_conv(pl, x, wl, hbm)
     fidelity = None
     if args.fidelity:
         fidelity = run_fidelity(parent, seg_len, pl, x, wl)
@@ -398,6 +403,8 @@ def run_ours(args):
             line["nodewise"] = nodewise
         if fidelity:
             line["fidelity"] = fidelity
+        if conv:
+            line["conv"] = conv
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -487,6 +494,47 @@ def run_nodewise(parent, seg_len, pl_tree, x, wl, tree_ms):
     return dict(calls=int(pl.info["n_rounds"]), sequences=int(pl.info["n_seq"]),
                 states=int(pl.info["n_states"]), chunks=int(pl.info["n_chunks"]),
                 ms_per_step=round(nms, 3), speedup_tree_vs_nodewise=round(nms / tree_ms, 3))
+
+
+def run_conv(pl, x, wl, hbm):
+    """Short convolution over the compact layout on the forest's q ([C, H*dk] bf16), width
+    4, SiLU, with bias: CUDA-event times of harts_conv_fwd and harts_conv_bwd, and their
+    algorithmic bytes (fwd: read x, write y; bwd: read x and dy, write dx; weights are
+    negligible) against the HBM peak.  Inputs are larger than L2."""
+    import torch
+    from prefix_shared_chunkwise_gb300.api import conv_bwd, conv_fwd
+    C = int(pl.info["C"])
+    xx = x["q"].reshape(C, -1)
+    ch = xx.shape[1]
+    g = torch.Generator(device=xx.device).manual_seed(11)
+    W = torch.randn((ch, 4), generator=g, device=xx.device) * 0.5
+    b = torch.randn(ch, generator=g, device=xx.device)
+    dy = x["v"].reshape(C, -1)
+    y = torch.empty_like(xx)
+    dx = torch.empty_like(xx)
+    dW = torch.empty_like(W)
+    db = torch.empty_like(b)
+
+    def timed(fn, reps=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    tf = timed(lambda: conv_fwd(pl, xx, W, b, activation="silu", y=y))
+    tb = timed(lambda: conv_bwd(pl, xx, W, b, dy, activation="silu", dx=dx, dweight=dW, dbias=db))
+    elem = C * ch * xx.element_size()
+    fb, bb = 2 * elem, 3 * elem
+    return dict(shape=[C, ch], width=4, activation="silu",
+                fwd=dict(ms=round(tf, 3), gb_s=round(fb / tf / 1e6, 1), frac=round(fb / tf / 1e6 / hbm, 3)),
+                bwd=dict(ms=round(tb, 3), gb_s=round(bb / tb / 1e6, 1), frac=round(bb / tb / 1e6 / hbm, 3)),
+                peak_gb_s=hbm)
 
 
 def run_fidelity(parent, seg_len, pl_tree, x, wl):

@@ -269,6 +269,57 @@ int harts_kda_bwd_static(const harts_plan *plan, const harts_kda_bwd_args *args,
 size_t harts_kda_bwd_static_max_bytes(void);
 
 /* Message for the last error on the calling thread ("" if none). */
+/* ------------------------------------------------------------------------------ */
+/* Causal short convolution over the compact layout.                              */
+/* ------------------------------------------------------------------------------ */
+
+/*
+ * The convolution that precedes KDA in the layer (page "HARTS ... 精读", section 4.3,
+ * KDA paragraph; summary page, section 4 "KDA execution"), run once per compact row:
+ * the window over the previous w - 1 tokens reads the row's real ancestors on its own
+ * trajectory (a temporary prefix of the parent's rows), never the neighbouring rows of
+ * another packed sequence, and is zero before the trajectory start.  Depthwise:
+ *   pre[r][c] = bias[c] + sum_{j<w} weight[c][w-1-j] * x[row j positions before r][c],
+ *   y = pre (activation 0) or pre * sigmoid(pre) (activation 1).
+ * The plan (uploaded) carries the ancestor context and the successor lists for any
+ * w <= 8; any of the three plan modes works.  Deterministic (no atomics).
+ */
+typedef struct {
+    int32_t channels;        /* ch: values per row (e.g. H * d), a multiple of 8 */
+    int32_t width;           /* w: 1..8 */
+    int32_t dtype;           /* harts_dtype of x, y, dy, dx */
+    int32_t activation;      /* 0 none, 1 SiLU */
+    const void *x;           /* device [C][ch], compact layout, 16-byte aligned */
+    const float *weight;     /* device [ch][w] fp32; weight[c][w-1] multiplies the current row */
+    const float *bias;       /* device [ch] fp32, or NULL */
+    void *y;                 /* device [C][ch] output (forward only), 16-byte aligned */
+} harts_conv_fwd_args;
+
+/* Forward.  Errors: HARTS_EINVAL (NULL / misaligned pointer, channels not a positive
+ * multiple of 8, activation), HARTS_EUNSUPPORTED (dtype, width outside 1..8),
+ * HARTS_ENOPLAN, HARTS_ECUDA. */
+int harts_conv_fwd(const harts_plan *plan, const harts_conv_fwd_args *args, harts_stream_t stream);
+
+typedef struct {
+    harts_conv_fwd_args fwd; /* y is not used */
+    const void *dy;          /* device [C][ch] dL/dy per compact row (already summed over the
+                                trajectories that share the row) */
+    void *dx;                /* device [C][ch] output */
+    float *dweight;          /* device [ch][w] output (overwritten) */
+    float *dbias;            /* device [ch] output (overwritten), or NULL */
+    void *workspace;         /* device, harts_conv_bwd_workspace_bytes, 16-byte aligned */
+    size_t workspace_bytes;
+} harts_conv_bwd_args;
+
+/* Workspace of harts_conv_bwd: the per-256-row partial sums of dweight / dbias, fp32
+ * [ceil(C/256)][ch][w+1].  0 for invalid arguments. */
+size_t harts_conv_bwd_workspace_bytes(const harts_plan *plan, int32_t channels, int32_t width);
+
+/* Backward: dx[r] sums weight * dL/dpre over the rows 0..w-1 positions after r on every
+ * branch below it (gathered in a fixed order); dweight and dbias are reduced over rows in
+ * a fixed order.  Errors as harts_conv_fwd, plus HARTS_ESMALLBUF (workspace). */
+int harts_conv_bwd(const harts_plan *plan, const harts_conv_bwd_args *args, harts_stream_t stream);
+
 const char *harts_last_error(void);
 
 #ifdef __cplusplus

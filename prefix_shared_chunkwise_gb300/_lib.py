@@ -24,7 +24,8 @@ EXPORTED = [
     "harts_plan_upload", "harts_plan_device_error", "harts_plan_free",
     "harts_kda_chunk_state_bytes", "harts_kda_fwd", "harts_kda_bwd_workspace_bytes",
     "harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad", "harts_kda_bwd_static",
-    "harts_kda_bwd_static_max_bytes", "harts_last_error",
+    "harts_kda_bwd_static_max_bytes", "harts_conv_fwd", "harts_conv_bwd_workspace_bytes",
+    "harts_conv_bwd", "harts_last_error",
 ]
 
 _i32, _i64, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
@@ -69,6 +70,16 @@ class BwdArgs(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t)]
 
 
+class ConvFwdArgs(ctypes.Structure):
+    _fields_ = [("channels", _i32), ("width", _i32), ("dtype", _i32), ("activation", _i32),
+                ("x", _vp), ("weight", _vp), ("bias", _vp), ("y", _vp)]
+
+
+class ConvBwdArgs(ctypes.Structure):
+    _fields_ = [("fwd", ConvFwdArgs), ("dy", _vp), ("dx", _vp), ("dweight", _vp), ("dbias", _vp),
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
+
+
 _lib = None
 
 
@@ -100,6 +111,12 @@ def lib():
         for fn in ("harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad", "harts_kda_bwd_static"):
             getattr(L, fn).argtypes = [_vp, ctypes.POINTER(BwdArgs), _vp]
             getattr(L, fn).restype = ctypes.c_int
+        L.harts_conv_fwd.argtypes = [_vp, ctypes.POINTER(ConvFwdArgs), _vp]
+        L.harts_conv_fwd.restype = ctypes.c_int
+        L.harts_conv_bwd.argtypes = [_vp, ctypes.POINTER(ConvBwdArgs), _vp]
+        L.harts_conv_bwd.restype = ctypes.c_int
+        L.harts_conv_bwd_workspace_bytes.argtypes = [_vp, _i32, _i32]
+        L.harts_conv_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.harts_last_error.argtypes = []
         L.harts_last_error.restype = ctypes.c_char_p
         for fn in ("harts_plan_calls", "harts_plan_get_info", "harts_plan_export",

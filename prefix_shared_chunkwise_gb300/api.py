@@ -9,7 +9,7 @@ import numpy as np
 
 from . import _lib as L
 
-__all__ = ["Plan", "kda_fwd", "kda_bwd", "dtype_code"]
+__all__ = ["Plan", "kda_fwd", "kda_bwd", "conv_fwd", "conv_bwd", "dtype_code"]
 
 
 def dtype_code(torch_dtype):
@@ -168,3 +168,49 @@ def kda_bwd(plan: Plan, q, k, v, g, beta, d_o, *, states, chunk_states, d_final=
     if dh0 is not None:
         grads["dh0"] = dh0
     return grads
+
+
+def _conv_args(x, weight, bias, y, activation):
+    C, ch = x.shape[0], int(x.numel() // x.shape[0])
+    a = L.ConvFwdArgs()
+    a.channels, a.width = ch, int(weight.shape[1])
+    a.dtype = dtype_code(x.dtype)
+    a.activation = {"none": 0, "silu": 1}[activation]
+    for n, t in dict(x=x, weight=weight, bias=bias, y=y).items():
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+        setattr(a, n, None if t is None else t.data_ptr())
+    return a
+
+
+def conv_fwd(plan: Plan, x, weight, bias=None, *, activation="none", y=None, stream=None):
+    """harts_conv_fwd.  x: [C, ...] compact rows (channels = the rest, flattened);
+    weight: [channels, w] fp32; bias: [channels] fp32 or None.  Returns y like x."""
+    import torch
+    if y is None:
+        y = torch.empty_like(x)
+    a = _conv_args(x, weight, bias, y, activation)
+    L.check(L.lib().harts_conv_fwd(plan.handle, ctypes.byref(a), _stream(stream)), "harts_conv_fwd")
+    return y
+
+
+def conv_bwd(plan: Plan, x, weight, bias, dy, *, activation="none", dx=None, dweight=None, dbias=None,
+             workspace=None, stream=None):
+    """harts_conv_bwd.  Returns (dx, dweight, dbias); dbias is None when bias is None."""
+    import torch
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dweight is None:
+        dweight = torch.empty_like(weight)
+    if dbias is None and bias is not None:
+        dbias = torch.empty_like(bias)
+    b = L.ConvBwdArgs()
+    b.fwd = _conv_args(x, weight, bias, None, activation)
+    nb = int(L.lib().harts_conv_bwd_workspace_bytes(plan.handle, b.fwd.channels, b.fwd.width))
+    if workspace is None:
+        workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=x.device)
+    b.dy, b.dx, b.dweight = dy.data_ptr(), dx.data_ptr(), dweight.data_ptr()
+    b.dbias = None if dbias is None else dbias.data_ptr()
+    b.workspace, b.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    L.check(L.lib().harts_conv_bwd(plan.handle, ctypes.byref(b), _stream(stream)), "harts_conv_bwd")
+    return dx, dweight, dbias

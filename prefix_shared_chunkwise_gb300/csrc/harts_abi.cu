@@ -113,6 +113,9 @@ int harts_plan_upload(harts_plan *P, void *dev_buf, size_t bytes, harts_stream_t
     v.replay_idx = w + I.off_replay_idx; v.fold_rows = w + I.off_fold_rows;
     v.fold_ptr = w + I.off_fold_ptr; v.fold_occ = w + I.off_fold_occ;
     v.chunk_seq = w + I.off_chunk_seq;
+    v.row_seg = w + I.off_row_seg; v.seg_row0 = w + I.off_seg_row0; v.seg_len = w + I.off_seg_len;
+    v.conv_ctx = w + I.off_conv_ctx; v.conv_sptr = w + I.off_conv_sptr; v.conv_succ = w + I.off_conv_succ;
+    v.n_seg = P->info.n_seg;
     v.n_rounds = P->info.n_rounds; v.n_seq = P->info.n_seq; v.n_states = P->info.n_states;
     v.n_roots = P->info.n_roots; v.n_fold = P->info.n_fold_rows; v.chunk = P->info.chunk;
     v.R = P->info.R; v.n_chunks = P->info.n_chunks; v.C = P->info.C; v.flags = P->info.flags;

@@ -261,6 +261,8 @@ int build(harts_plan &P, int32_t n, const int32_t *parent, const int64_t *len, i
     }
 
     P.seg_ctop = ctop; P.seg_tpre = tpre; P.seg_tin = tin;
+    P.parent.assign(parent, parent + n);
+    P.seg_len.assign(len, len + n);
     P.info.flags = flags;
     return HARTS_OK;
 }
@@ -328,6 +330,55 @@ void build_image(harts_plan &P) {
     for (int32_t i = 0; i < n_seq; ++i)
         for (int32_t c = 0; c < P.seq_nchunks[i]; ++c) cseq.push_back(i);
     put(I.off_chunk_seq, cseq.data(), cseq.size());
+
+    // ---- short-convolution context ----------------------------------------------------
+    // A compact row's window reaches back along its own trajectory, into its ancestors'
+    // last rows; a row feeds the next rows on every branch below it.
+    const int32_t n = P.info.n_seg;
+    constexpr int K = kConvMaxW - 1;
+    std::vector<int32_t> rseg(static_cast<size_t>(P.info.C)), srow0(n), slen(n);
+    for (int32_t v = 0; v < n; ++v) {
+        srow0[v] = static_cast<int32_t>(P.seg_offset[v]);
+        slen[v] = static_cast<int32_t>(P.seg_len[v]);
+        for (int64_t r = P.seg_offset[v]; r < P.seg_offset[v] + P.seg_len[v]; ++r) rseg[r] = v;
+    }
+    std::vector<int32_t> ctx(static_cast<size_t>(n) * K, -1);
+    for (int32_t v = 0; v < n; ++v) {
+        int k = 0;
+        for (int32_t u = P.parent[v]; u >= 0 && k < K; u = P.parent[u])
+            for (int64_t t = P.seg_len[u] - 1; t >= 0 && k < K; --t)
+                ctx[static_cast<size_t>(v) * K + k++] = static_cast<int32_t>(P.seg_offset[u] + t);
+    }
+    std::vector<int32_t> kptr(n + 1, 0), kids;
+    for (int32_t v = 0; v < n; ++v) if (P.parent[v] >= 0) kptr[P.parent[v] + 1]++;
+    for (int32_t v = 0; v < n; ++v) kptr[v + 1] += kptr[v];
+    kids.assign(kptr[n], 0);
+    {
+        std::vector<int32_t> fill(kptr.begin(), kptr.end() - 1);
+        for (int32_t v = 0; v < n; ++v) if (P.parent[v] >= 0) kids[fill[P.parent[v]]++] = v;
+    }
+    std::vector<int32_t> sptr(static_cast<size_t>(n) * K + 1, 0), succ;
+    // rows e positions into the subtrees below v's end (children in increasing id)
+    std::vector<std::pair<int32_t, int64_t>> stack;
+    for (int32_t v = 0; v < n; ++v)
+        for (int e = 0; e < K; ++e) {
+            sptr[static_cast<size_t>(v) * K + e] = static_cast<int32_t>(succ.size());
+            stack.clear();
+            for (int32_t j = kptr[v + 1] - 1; j >= kptr[v]; --j) stack.push_back({kids[j], e});
+            while (!stack.empty()) {
+                auto [c, off] = stack.back();
+                stack.pop_back();
+                if (off < P.seg_len[c]) { succ.push_back(static_cast<int32_t>(P.seg_offset[c] + off)); continue; }
+                for (int32_t j = kptr[c + 1] - 1; j >= kptr[c]; --j) stack.push_back({kids[j], off - P.seg_len[c]});
+            }
+        }
+    sptr[static_cast<size_t>(n) * K] = static_cast<int32_t>(succ.size());
+    put(I.off_row_seg, rseg.data(), rseg.size());
+    put(I.off_seg_row0, srow0.data(), n);
+    put(I.off_seg_len, slen.data(), n);
+    put(I.off_conv_ctx, ctx.data(), ctx.size());
+    put(I.off_conv_sptr, sptr.data(), sptr.size());
+    put(I.off_conv_succ, succ.data(), succ.size());
     while (w.size() % 64) w.push_back(0);
 }
 

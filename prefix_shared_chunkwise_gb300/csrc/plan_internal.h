@@ -9,6 +9,8 @@
 namespace harts {
 
 // Device view of an uploaded plan: pointers into one int32 image.
+constexpr int kConvMaxW = 8;       // widest short convolution the plan tables serve
+
 struct PlanDev {
     int32_t *err;                // [4] device error word: code, info, info, info
     const int32_t *round_seq_ptr;  // [n_rounds+1]
@@ -30,7 +32,14 @@ struct PlanDev {
     const int32_t *fold_ptr;       // [n_fold+1]
     const int32_t *fold_occ;       // [R] replay occurrence ids grouped by row
     const int32_t *chunk_seq;      // [n_chunks] sequence of every chunk
-    int32_t n_rounds, n_seq, n_states, n_roots, n_fold, chunk;
+    // short-convolution context (widths up to kConvMaxW)
+    const int32_t *row_seg;        // [C] segment of every compact row
+    const int32_t *seg_row0;       // [n_seg] first compact row of every segment
+    const int32_t *seg_len;        // [n_seg]
+    const int32_t *conv_ctx;       // [n_seg][kConvMaxW-1] rows 1..7 positions before the segment, -1 past the root
+    const int32_t *conv_sptr;      // [n_seg*(kConvMaxW-1)+1] successor lists of (segment end, lag e+1)
+    const int32_t *conv_succ;      // rows e+1 positions after the segment's end, on every branch
+    int32_t n_rounds, n_seq, n_states, n_roots, n_fold, chunk, n_seg;
     uint32_t flags;                // harts_plan_calls flags (HARTS_PLAN_NOREPLAY: slots inside chunks)
     int64_t R, n_chunks, C;
 };
@@ -41,7 +50,8 @@ struct PlanImage {
     int64_t off_err, off_round_seq_ptr, off_round_order, off_seq_row0, off_seq_nown,
         off_seq_rho, off_seq_rptr, off_seq_src, off_seq_sptr, off_state_lpos, off_seq_cbase,
         off_state_cptr, off_state_cons, off_root_cptr, off_root_cons, off_replay_idx,
-        off_fold_rows, off_fold_ptr, off_fold_occ, off_chunk_seq;
+        off_fold_rows, off_fold_ptr, off_fold_occ, off_chunk_seq, off_row_seg, off_seg_row0,
+        off_seg_len, off_conv_ctx, off_conv_sptr, off_conv_succ;
 };
 
 void set_error(const std::string &msg);
@@ -50,7 +60,8 @@ void set_error(const std::string &msg);
 
 struct harts_plan {
     harts_plan_info info{};
-    std::vector<int64_t> seg_offset, seg_pos;
+    std::vector<int32_t> parent;
+    std::vector<int64_t> seg_len, seg_offset, seg_pos;
     std::vector<int32_t> seg_seq, seg_ctop, seg_tpre, seg_tin;
     std::vector<int32_t> round_seq_ptr;
     std::vector<int64_t> cu_seqlens;
