@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--fidelity", action="store_true",
                     help="also compare the forward outputs of the tree plans with the "
                          "per-trajectory run, by handoff depth")
+    ap.add_argument("--logprob", action="store_true",
+                    help="also time the compact-to-semantic log-probabilities (64K-token forest, "
+                         "V = 157,184)")
     ap.add_argument("--conv", action="store_true",
                     help="also time the short convolution (fwd, bwd) on the forest's q")
     ap.add_argument("--nodewise", action="store_true",
@@ -373,6 +376,9 @@ def run_ours(args):
     conv = None
     if args.conv:
         conv = run_conv(pl, x, wl, hbm)
+    lp = None
+    if args.logprob:
+        lp = run_logprob(hbm)
     fidelity = None
     if args.fidelity:
         fidelity = run_fidelity(parent, seg_len, pl, x, wl)
@@ -405,6 +411,8 @@ def run_ours(args):
             line["fidelity"] = fidelity
         if conv:
             line["conv"] = conv
+        if lp:
+            line["logprob"] = lp
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -494,6 +502,53 @@ def run_nodewise(parent, seg_len, pl_tree, x, wl, tree_ms):
     return dict(calls=int(pl.info["n_rounds"]), sequences=int(pl.info["n_seq"]),
                 states=int(pl.info["n_states"]), chunks=int(pl.info["n_chunks"]),
                 ms_per_step=round(nms, 3), speedup_tree_vs_nodewise=round(nms / tree_ms, 3))
+
+
+def run_logprob(hbm):
+    """Compact-to-semantic log-probabilities on the 64K-token forest (fb64k_bf16) at the
+    pages' vocabulary (157,184), bf16 logits: CUDA-event times of harts_logprob_fwd and
+    _bwd, algorithmic bytes (fwd reads the C x V logits; bwd reads them and writes the
+    gradient) against the HBM peak, and S / C, the factor of vocabulary work that the
+    compact rows save over S x V expanded logits."""
+    import torch
+    from prefix_shared_chunkwise_gb300.api import Plan, logprob_bwd, logprob_fwd, semantic_map
+    from prefix_shared_chunkwise_gb300.synth import make_tree
+    parent, seg_len = make_tree("fb64k_bf16")
+    pl = Plan(parent, seg_len, 64)
+    sem_row, row_ptr, row_sem = semantic_map(pl)
+    C, S, V = int(pl.info["C"]), len(sem_row), 157_184
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(21)
+    z = (torch.randn((C, V), generator=g, device=dev) * 3).to(torch.bfloat16)
+    target = torch.randint(0, V, (S,), generator=g, device=dev, dtype=torch.int32)
+    dl = torch.randn(S, generator=g, device=dev)
+    rp, rs = torch.as_tensor(row_ptr, device=dev), torch.as_tensor(row_sem, device=dev)
+    logp = torch.empty(S, device=dev)
+    lse = torch.empty(C, device=dev)
+    dz = torch.empty_like(z)
+
+    def timed(fn, reps=5):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    tf = timed(lambda: logprob_fwd(z, rp, rs, target, lse=lse, logp=logp))
+    tb = timed(lambda: logprob_bwd(z, rp, rs, target, lse, dl, dlogits=dz))
+    fb, bb = C * V * 2, 2 * C * V * 2
+    out = dict(C=C, S=S, V=V, vocab_work_saved=round(S / C, 3),
+               fwd=dict(ms=round(tf, 3), gb_s=round(fb / tf / 1e6, 1), frac=round(fb / tf / 1e6 / hbm, 3)),
+               bwd=dict(ms=round(tb, 3), gb_s=round(bb / tb / 1e6, 1), frac=round(bb / tb / 1e6 / hbm, 3)),
+               peak_gb_s=hbm)
+    del z, dz
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_conv(pl, x, wl, hbm):

@@ -320,6 +320,52 @@ size_t harts_conv_bwd_workspace_bytes(const harts_plan *plan, int32_t channels, 
  * a fixed order.  Errors as harts_conv_fwd, plus HARTS_ESMALLBUF (workspace). */
 int harts_conv_bwd(const harts_plan *plan, const harts_conv_bwd_args *args, harts_stream_t stream);
 
+/* ------------------------------------------------------------------------------ */
+/* Compact-to-semantic log-probabilities.                                         */
+/* ------------------------------------------------------------------------------ */
+
+/*
+ * Page "HARTS ... 精读", section 4.4 ("紧凑到语义的 log 概率"); summary page "Semantic
+ * Preservation": a compact logit row is reduced over the vocabulary once (its
+ * log-sum-exp), and every semantic position s -- a token occurrence of an original
+ * trajectory -- reads its own target logit from the row its token maps to:
+ *   logp[s] = logits[c(s)][target[s]] - lse[c(s)].
+ * The backward (eq. 19) sums the independently formed gradients of a row's semantic
+ * positions onto it: dlogits[c] = sum_{s -> c} dlogp[s] (onehot(target[s]) - softmax(row c)).
+ * Work is O(C V) + O(S); no S x V array is formed.  Deterministic (no atomics).
+ *
+ * harts_plan_semantic_map fills, on the host: sem_row[S] (compact row of each semantic
+ * position; trajectories in increasing leaf id, each from its root to its leaf), and the
+ * positions grouped by row: row_ptr[C+1], row_sem[S] (ascending within a row).  Callers
+ * with another semantic order may build these arrays themselves.
+ */
+int harts_plan_semantic_map(const harts_plan *plan, int32_t *sem_row, int32_t *row_ptr, int32_t *row_sem);
+
+typedef struct {
+    int64_t C;               /* compact rows */
+    int32_t V;               /* vocabulary, a multiple of 8 */
+    int32_t dtype;           /* harts_dtype of logits / dlogits */
+    int64_t S;               /* semantic positions, < 2^31 */
+    const void *logits;      /* device [C][V], 16-byte aligned */
+    const int32_t *row_ptr;  /* device [C+1]: semantic positions of row c are row_sem[row_ptr[c] ..] */
+    const int32_t *row_sem;  /* device [S] */
+    const int32_t *target;   /* device [S] label of each semantic position, 0 <= target < V */
+    float *lse;              /* device [C]: written by the forward, read by the backward */
+    float *logp;             /* device [S]: written by the forward */
+} harts_logprob_fwd_args;
+
+/* Forward.  Errors: HARTS_EINVAL (NULL / misaligned pointers, V not a multiple of 8),
+ * HARTS_EUNSUPPORTED (dtype), HARTS_EOVERFLOW (S), HARTS_ECUDA. */
+int harts_logprob_fwd(const harts_logprob_fwd_args *args, harts_stream_t stream);
+
+typedef struct {
+    harts_logprob_fwd_args fwd;  /* lse as written by the forward; logp unused */
+    const float *dlogp;          /* device [S] dL/dlogp */
+    void *dlogits;               /* device [C][V] output (overwritten), 16-byte aligned */
+} harts_logprob_bwd_args;
+
+int harts_logprob_bwd(const harts_logprob_bwd_args *args, harts_stream_t stream);
+
 const char *harts_last_error(void);
 
 #ifdef __cplusplus

@@ -25,7 +25,8 @@ EXPORTED = [
     "harts_kda_chunk_state_bytes", "harts_kda_fwd", "harts_kda_bwd_workspace_bytes",
     "harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad", "harts_kda_bwd_static",
     "harts_kda_bwd_static_max_bytes", "harts_conv_fwd", "harts_conv_bwd_workspace_bytes",
-    "harts_conv_bwd", "harts_last_error",
+    "harts_conv_bwd", "harts_plan_semantic_map", "harts_logprob_fwd", "harts_logprob_bwd",
+    "harts_last_error",
 ]
 
 _i32, _i64, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
@@ -80,6 +81,15 @@ class ConvBwdArgs(ctypes.Structure):
                 ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
 
 
+class LogprobFwdArgs(ctypes.Structure):
+    _fields_ = [("C", _i64), ("V", _i32), ("dtype", _i32), ("S", _i64), ("logits", _vp),
+                ("row_ptr", _vp), ("row_sem", _vp), ("target", _vp), ("lse", _vp), ("logp", _vp)]
+
+
+class LogprobBwdArgs(ctypes.Structure):
+    _fields_ = [("fwd", LogprobFwdArgs), ("dlogp", _vp), ("dlogits", _vp)]
+
+
 _lib = None
 
 
@@ -117,6 +127,12 @@ def lib():
         L.harts_conv_bwd.restype = ctypes.c_int
         L.harts_conv_bwd_workspace_bytes.argtypes = [_vp, _i32, _i32]
         L.harts_conv_bwd_workspace_bytes.restype = ctypes.c_size_t
+        L.harts_plan_semantic_map.argtypes = [_vp, _pi32, _pi32, _pi32]
+        L.harts_plan_semantic_map.restype = ctypes.c_int
+        L.harts_logprob_fwd.argtypes = [ctypes.POINTER(LogprobFwdArgs), _vp]
+        L.harts_logprob_fwd.restype = ctypes.c_int
+        L.harts_logprob_bwd.argtypes = [ctypes.POINTER(LogprobBwdArgs), _vp]
+        L.harts_logprob_bwd.restype = ctypes.c_int
         L.harts_last_error.argtypes = []
         L.harts_last_error.restype = ctypes.c_char_p
         for fn in ("harts_plan_calls", "harts_plan_get_info", "harts_plan_export",

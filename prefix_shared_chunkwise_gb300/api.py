@@ -9,7 +9,8 @@ import numpy as np
 
 from . import _lib as L
 
-__all__ = ["Plan", "kda_fwd", "kda_bwd", "conv_fwd", "conv_bwd", "dtype_code"]
+__all__ = ["Plan", "kda_fwd", "kda_bwd", "conv_fwd", "conv_bwd", "semantic_map", "logprob_fwd",
+           "logprob_bwd", "dtype_code"]
 
 
 def dtype_code(torch_dtype):
@@ -214,3 +215,51 @@ def conv_bwd(plan: Plan, x, weight, bias, dy, *, activation="none", dx=None, dwe
     b.workspace, b.workspace_bytes = workspace.data_ptr(), workspace.numel()
     L.check(L.lib().harts_conv_bwd(plan.handle, ctypes.byref(b), _stream(stream)), "harts_conv_bwd")
     return dx, dweight, dbias
+
+
+def semantic_map(plan: Plan):
+    """harts_plan_semantic_map: numpy (sem_row [S], row_ptr [C+1], row_sem [S]) int32."""
+    C, S = plan.info["C"], plan.info["S"]
+    sem_row = np.zeros(max(S, 1), np.int32)
+    row_ptr = np.zeros(C + 1, np.int32)
+    row_sem = np.zeros(max(S, 1), np.int32)
+    L.check(L.lib().harts_plan_semantic_map(plan.handle, sem_row.ctypes.data_as(L._pi32),
+                                            row_ptr.ctypes.data_as(L._pi32), row_sem.ctypes.data_as(L._pi32)),
+            "harts_plan_semantic_map")
+    return sem_row[:S], row_ptr, row_sem[:S]
+
+
+def _lp_args(logits, row_ptr, row_sem, target, lse, logp):
+    a = L.LogprobFwdArgs()
+    a.C, a.V = logits.shape
+    a.dtype = dtype_code(logits.dtype)
+    a.S = target.numel()
+    for n, t in dict(logits=logits, row_ptr=row_ptr, row_sem=row_sem, target=target, lse=lse, logp=logp).items():
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+        setattr(a, n, None if t is None else t.data_ptr())
+    return a
+
+
+def logprob_fwd(logits, row_ptr, row_sem, target, *, lse=None, logp=None, stream=None):
+    """harts_logprob_fwd: returns (logp [S] fp32, lse [C] fp32)."""
+    import torch
+    if lse is None:
+        lse = torch.empty(logits.shape[0], dtype=torch.float32, device=logits.device)
+    if logp is None:
+        logp = torch.empty(target.numel(), dtype=torch.float32, device=logits.device)
+    a = _lp_args(logits, row_ptr, row_sem, target, lse, logp)
+    L.check(L.lib().harts_logprob_fwd(ctypes.byref(a), _stream(stream)), "harts_logprob_fwd")
+    return logp, lse
+
+
+def logprob_bwd(logits, row_ptr, row_sem, target, lse, dlogp, *, dlogits=None, stream=None):
+    """harts_logprob_bwd: returns dlogits like logits."""
+    import torch
+    if dlogits is None:
+        dlogits = torch.empty_like(logits)
+    b = L.LogprobBwdArgs()
+    b.fwd = _lp_args(logits, row_ptr, row_sem, target, lse, None)
+    b.dlogp, b.dlogits = dlogp.data_ptr(), dlogits.data_ptr()
+    L.check(L.lib().harts_logprob_bwd(ctypes.byref(b), _stream(stream)), "harts_logprob_bwd")
+    return dlogits
