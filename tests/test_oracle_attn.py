@@ -1,0 +1,47 @@
+"""Pins for the branch-attention oracle (oracle/attn.py): a plain chain equals torch's
+scaled_dot_product_attention (causal), shared rows agree across trajectories, and a
+hand case of the bottom-right alignment (a branch's first query sees the whole ancestor
+prefix and itself, not its sibling)."""
+import numpy as np
+import pytest
+
+from oracle import attn
+
+torch = pytest.importorskip("torch")
+
+
+def test_chain_equals_torch_sdpa():
+    rng = np.random.default_rng(1)
+    L, H, d = 37, 3, 16
+    q, k, v = (rng.standard_normal((L, H, d)) for _ in range(3))
+    r = attn.attn_forest(np.array([-1]), np.array([L]), np.array([0]), q, k, v, 0.25)
+    t = lambda a: torch.as_tensor(a.transpose(1, 0, 2)[None])      # [1, H, L, d]
+    ref = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), is_causal=True, scale=0.25)
+    np.testing.assert_allclose(r["o"], ref[0].numpy().transpose(1, 0, 2), atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_shared_rows_agree(seed):
+    rng = np.random.default_rng(10 + seed)
+    n = 9
+    parent = np.array([-1] + [int(rng.integers(0, i)) for i in range(1, n)])
+    seg_len = rng.integers(1, 6, size=n)
+    so = np.concatenate([[0], np.cumsum(seg_len)[:-1]])
+    C = int(seg_len.sum())
+    q, k, v = (rng.standard_normal((C, 2, 4)) for _ in range(3))
+    r = attn.attn_forest(parent, seg_len, so, q, k, v, 0.5)
+    assert r["occ_diff"] < 1e-12 and not np.isnan(r["o"]).any()
+
+
+def test_branch_sees_ancestors_not_sibling():
+    # root A (2 rows) -> B (1 row), C (1 row); rows: A0 A1 B0 C0
+    parent = np.array([-1, 0, 0])
+    seg_len = np.array([2, 1, 1])
+    so = np.array([0, 2, 3])
+    q = np.zeros((4, 1, 1))
+    k = np.zeros((4, 1, 1))
+    v = np.array([1.0, 2.0, 100.0, 5.0]).reshape(4, 1, 1)
+    o = attn.attn_forest(parent, seg_len, so, q, k, v, 1.0)["o"][:, 0, 0]
+    # zero scores: uniform over the visible rows
+    assert o[3] == pytest.approx((1 + 2 + 5) / 3)      # C0 sees A0, A1, C0 -- not B0
+    assert o[2] == pytest.approx((1 + 2 + 100) / 3)
