@@ -46,6 +46,8 @@ def parse():
                          "V = 157,184)")
     ap.add_argument("--conv", action="store_true",
                     help="also time the short convolution (fwd, bwd) on the forest's q")
+    ap.add_argument("--attn", action="store_true",
+                    help="also time the branch attention (forward) on the forest's q, k, v")
     ap.add_argument("--nodewise", action="store_true",
                     help="also time the same kernels on the node-wise plan of the forest")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -379,6 +381,9 @@ def run_ours(args):
     lp = None
     if args.logprob:
         lp = run_logprob(hbm)
+    attn = None
+    if args.attn:
+        attn = run_attn(parent, seg_len, pl, x, tf_burst)
     fidelity = None
     if args.fidelity:
         fidelity = run_fidelity(parent, seg_len, pl, x, wl)
@@ -413,6 +418,8 @@ def run_ours(args):
             line["conv"] = conv
         if lp:
             line["logprob"] = lp
+        if attn:
+            line["attn"] = attn
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -549,6 +556,61 @@ def run_logprob(hbm):
     del z, dz
     torch.cuda.empty_cache()
     return out
+
+
+def run_attn(parent, seg_len, pl, x, tf_peak):
+    """Branch attention (forward) over the compact layout on the forest's q, k, v ([C, H,
+    128] bf16): CUDA-event time of harts_attn_fwd, algorithmic FLOPs (4 d per head and
+    visible (query, key) pair: Q K^T and P V) against the bf16 tensor peak, the FLOPs of
+    the 128 x 128 tiles the kernel issues (masked entries included), and the pairs the
+    per-trajectory execution would compute instead (every trajectory causally over its
+    own tokens)."""
+    import numpy as np
+    import torch
+    from prefix_shared_chunkwise_gb300.api import attn_fwd
+    C, H, d = x["q"].shape
+    a = pl.arrays()
+    pos, ln = a["seg_pos"].astype(np.float64), np.asarray(seg_len, np.float64)
+    pairs = float((ln * pos + ln * (ln + 1) / 2).sum())
+    # the kernel's tiles: per sequence and 128-query tile, keys up to the tile's last query
+    cu, fs = a["cu_seqlens"], a["seq_first_seg"]
+    tiles = 0
+    for i in range(len(fs)):
+        own, h = int(cu[i + 1] - cu[i]), int(a["seg_pos"][fs[i]])
+        for t in range((own + 127) // 128):
+            tiles += (h + min(own, (t + 1) * 128) - 1) // 128 + 1
+    # per-trajectory pairs: sum over leaves of L (L + 1) / 2
+    parent = np.asarray(parent)
+    depth_len = np.zeros(len(parent))
+    for v in range(len(parent)):
+        depth_len[v] = ln[v] + (depth_len[parent[v]] if parent[v] >= 0 else 0)
+    leaf = np.ones(len(parent), bool)
+    leaf[parent[parent >= 0]] = False
+    traj_pairs = float((depth_len[leaf] * (depth_len[leaf] + 1) / 2).sum())
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((C, H), dtype=torch.float32, device=o.device)
+
+    def step():
+        attn_fwd(pl, x["q"], x["k"], x["v"], o=o, lse=lse)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+    reps = 10
+    e0.record()
+    for _ in range(reps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    flops = 4.0 * d * H * pairs
+    tile_flops = 4.0 * d * H * tiles * 128 * 128
+    return dict(shape=[C, H, d], ms=round(ms, 3), visible_pairs=int(pairs),
+                tflops=round(flops / ms / 1e9, 1), frac=round(flops / ms / 1e9 / tf_peak, 4),
+                tile_tflops=round(tile_flops / ms / 1e9, 1), tile_util=round(pairs * H / (tiles * 128 * 128 * H), 3),
+                per_trajectory_pairs=int(traj_pairs), work_saved=round(traj_pairs / pairs, 3),
+                peak_tflops=tf_peak, peak_source="bf16_tflops (burst, kernel timed alone)")
 
 
 def run_conv(pl, x, wl, hbm):

@@ -366,6 +366,39 @@ typedef struct {
 
 int harts_logprob_bwd(const harts_logprob_bwd_args *args, harts_stream_t stream);
 
+/* ------------------------------------------------------------------------------ */
+/* Branch attention over the compact layout (the softmax-attention layers).       */
+/* ------------------------------------------------------------------------------ */
+
+/*
+ * Page "HARTS ... 精读", section 4.3 (MLA paragraph); summary page, section 4 ("MLA
+ * execution"); figures page, Figure C.1(c).  Projections run once per compact row; each
+ * sequence of the plan is a branch whose queries (its own rows) attend to the keys and
+ * values of its ancestors and itself with bottom-right causal alignment: own query t sees
+ * view entries 0 .. h + t, where h is the number of trajectory positions before the
+ * sequence.  The view is gathered inside the kernel; outputs go to the unique compact
+ * rows.  Per head: o = softmax(scale q k^T) v, lse = log sum_j exp(scale q k_j).
+ * Equal to plain causal attention of every trajectory through a row.
+ *
+ * The plan's attention tables (each sequence's ancestor rows) are built when they add up
+ * to at most 2^27 rows; for deeper plans the call fails with HARTS_EOVERFLOW.
+ */
+typedef struct {
+    int32_t H;               /* heads */
+    int32_t d;               /* head dimension of q, k and v: 128 */
+    int32_t dtype;           /* harts_dtype of q, k, v, o: HARTS_BF16 */
+    float scale;             /* softmax scale (typically 1/sqrt(d)) */
+    const void *q, *k, *v;   /* device [C][H][d], compact layout, 16-byte aligned */
+    void *o;                 /* device [C][H][d] output, 16-byte aligned */
+    float *lse;              /* device [C][H] output (natural-log sum-exp of scaled scores), or NULL */
+} harts_attn_fwd_args;
+
+/* Forward.  Errors: HARTS_EINVAL (NULL / misaligned pointers, H < 1), HARTS_EUNSUPPORTED
+ * (dtype other than bf16, d other than 128), HARTS_ENOPLAN, HARTS_EOVERFLOW (no attention
+ * tables in the plan, too many blocks), HARTS_ECUDA.  A bounded wait that runs out records
+ * device code 3 (timeout) in the plan's device error word (harts_plan_device_error). */
+int harts_attn_fwd(const harts_plan *plan, const harts_attn_fwd_args *args, harts_stream_t stream);
+
 const char *harts_last_error(void);
 
 #ifdef __cplusplus

@@ -52,3 +52,37 @@ def attn_forest(parent, seg_len, seg_offset, q, k, v, scale):
             o[rows, h] = oo
             lse[rows, h] = ll
     return dict(o=o, lse=lse, occ_diff=occ)
+
+
+def trajectory_prefix(parent, seg_len, seg_offset, row):
+    """Compact rows of the trajectory positions 0 .. p(row): the ancestors' rows, root
+    first, then the row's own segment up to and including the row."""
+    parent = np.asarray(parent)
+    seg_offset = np.asarray(seg_offset)
+    ends = seg_offset + np.asarray(seg_len)
+    seg = int(np.nonzero((seg_offset <= row) & (row < ends))[0][0])
+    chain = []
+    v = int(parent[seg])
+    while v >= 0:
+        chain.append(v)
+        v = int(parent[v])
+    parts = [np.arange(seg_offset[u], seg_offset[u] + seg_len[u]) for u in reversed(chain)]
+    parts.append(np.arange(seg_offset[seg], row + 1))
+    return np.concatenate(parts).astype(np.int64)
+
+
+def attn_query(q_row, k_view, v_view, scale):
+    """One query over its whole view (every entry visible): q_row [H, dk], k_view
+    [n, H, dk], v_view [n, H, dv] -> (o [H, dv], lse [H])."""
+    q_row = np.asarray(q_row, np.float64)
+    k_view = np.asarray(k_view, np.float64)
+    v_view = np.asarray(v_view, np.float64)
+    o = np.empty((q_row.shape[0], v_view.shape[2]))
+    lse = np.empty(q_row.shape[0])
+    for h in range(q_row.shape[0]):
+        s = scale * k_view[:, h] @ q_row[h]
+        m = s.max()
+        p = np.exp(s - m)
+        o[h] = (p / p.sum()) @ v_view[:, h]
+        lse[h] = m + np.log(p.sum())
+    return o, lse

@@ -26,7 +26,7 @@ EXPORTED = [
     "harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad", "harts_kda_bwd_static",
     "harts_kda_bwd_static_max_bytes", "harts_conv_fwd", "harts_conv_bwd_workspace_bytes",
     "harts_conv_bwd", "harts_plan_semantic_map", "harts_logprob_fwd", "harts_logprob_bwd",
-    "harts_last_error",
+    "harts_attn_fwd", "harts_last_error",
 ]
 
 _i32, _i64, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
@@ -90,6 +90,11 @@ class LogprobBwdArgs(ctypes.Structure):
     _fields_ = [("fwd", LogprobFwdArgs), ("dlogp", _vp), ("dlogits", _vp)]
 
 
+class AttnFwdArgs(ctypes.Structure):
+    _fields_ = [("H", _i32), ("d", _i32), ("dtype", _i32), ("scale", ctypes.c_float),
+                ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp)]
+
+
 _lib = None
 
 
@@ -133,6 +138,8 @@ def lib():
         L.harts_logprob_fwd.restype = ctypes.c_int
         L.harts_logprob_bwd.argtypes = [ctypes.POINTER(LogprobBwdArgs), _vp]
         L.harts_logprob_bwd.restype = ctypes.c_int
+        L.harts_attn_fwd.argtypes = [_vp, ctypes.POINTER(AttnFwdArgs), _vp]
+        L.harts_attn_fwd.restype = ctypes.c_int
         L.harts_last_error.argtypes = []
         L.harts_last_error.restype = ctypes.c_char_p
         for fn in ("harts_plan_calls", "harts_plan_get_info", "harts_plan_export",

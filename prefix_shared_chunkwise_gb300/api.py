@@ -263,3 +263,23 @@ def logprob_bwd(logits, row_ptr, row_sem, target, lse, dlogp, *, dlogits=None, s
     b.dlogp, b.dlogits = dlogp.data_ptr(), dlogits.data_ptr()
     L.check(L.lib().harts_logprob_bwd(ctypes.byref(b), _stream(stream)), "harts_logprob_bwd")
     return dlogits
+
+
+def attn_fwd(plan: Plan, q, k, v, *, scale=None, o=None, lse=None, stream=None):
+    """harts_attn_fwd: branch attention over the compact layout.  q, k, v: [C, H, d]
+    bf16 (d = 128).  Returns (o [C, H, d] bf16, lse [C, H] fp32)."""
+    import torch
+    C, H, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((C, H), dtype=torch.float32, device=q.device)
+    for n, t in dict(q=q, k=k, v=v, o=o, lse=lse).items():
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    a = L.AttnFwdArgs()
+    a.H, a.d, a.dtype = H, d, dtype_code(q.dtype)
+    a.scale = float(d ** -0.5 if scale is None else scale)
+    a.q, a.k, a.v, a.o, a.lse = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr()
+    L.check(L.lib().harts_attn_fwd(plan.handle, ctypes.byref(a), _stream(stream)), "harts_attn_fwd")
+    return o, lse

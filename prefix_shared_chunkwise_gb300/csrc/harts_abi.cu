@@ -116,6 +116,8 @@ int harts_plan_upload(harts_plan *P, void *dev_buf, size_t bytes, harts_stream_t
     v.row_seg = w + I.off_row_seg; v.seg_row0 = w + I.off_seg_row0; v.seg_len = w + I.off_seg_len;
     v.conv_ctx = w + I.off_conv_ctx; v.conv_sptr = w + I.off_conv_sptr; v.conv_succ = w + I.off_conv_succ;
     v.n_seg = P->info.n_seg;
+    v.attn_hptr = w + I.off_attn_hptr; v.attn_hrows = w + I.off_attn_hrows; v.attn_qt = w + I.off_attn_qt;
+    v.n_qt = I.n_qt;
     v.n_rounds = P->info.n_rounds; v.n_seq = P->info.n_seq; v.n_states = P->info.n_states;
     v.n_roots = P->info.n_roots; v.n_fold = P->info.n_fold_rows; v.chunk = P->info.chunk;
     v.R = P->info.R; v.n_chunks = P->info.n_chunks; v.C = P->info.C; v.flags = P->info.flags;

@@ -379,6 +379,39 @@ void build_image(harts_plan &P) {
     put(I.off_conv_ctx, ctx.data(), ctx.size());
     put(I.off_conv_sptr, sptr.data(), sptr.size());
     put(I.off_conv_succ, succ.data(), succ.size());
+
+    // ---- branch attention -------------------------------------------------------------
+    // A sequence's view: the trajectory positions before its first own token (ancestor
+    // rows, root first), then its own rows.  Query tiles of kAttnTile own rows, ordered
+    // by decreasing work (view length up to the tile's end).
+    // The ancestor lists add up to sum_i (first position of sequence i), quadratic in the
+    // depth of chain-like trees: above kAttnMaxRows the plan carries no attention tables.
+    int64_t sum_h = 0;
+    for (int32_t i = 0; i < n_seq; ++i) sum_h += P.seg_pos[P.seq_first_seg[i]];
+    P.attn_ok = sum_h <= kAttnMaxRows;
+    std::vector<int32_t> hptr(n_seq + 1, 0), hrows;
+    std::vector<int32_t> chain;
+    for (int32_t i = 0; i < n_seq && P.attn_ok; ++i) {
+        hptr[i] = static_cast<int32_t>(hrows.size());
+        chain.clear();
+        for (int32_t u = P.parent[P.seq_first_seg[i]]; u >= 0; u = P.parent[u]) chain.push_back(u);
+        for (auto it = chain.rbegin(); it != chain.rend(); ++it)
+            for (int64_t t = 0; t < P.seg_len[*it]; ++t) hrows.push_back(static_cast<int32_t>(P.seg_offset[*it] + t));
+    }
+    hptr[n_seq] = static_cast<int32_t>(hrows.size());
+    std::vector<std::pair<int64_t, std::pair<int32_t, int32_t>>> qts;
+    for (int32_t i = 0; i < n_seq && P.attn_ok; ++i) {
+        const int64_t own = P.cu_seqlens[i + 1] - P.cu_seqlens[i], hh = hptr[i + 1] - hptr[i];
+        for (int64_t t = 0; t * kAttnTile < own; ++t)
+            qts.push_back({hh + std::min(own, (t + 1) * kAttnTile), {i, static_cast<int32_t>(t)}});
+    }
+    std::stable_sort(qts.begin(), qts.end(), [](const auto &a, const auto &b) { return a.first > b.first; });
+    std::vector<int32_t> qt(2 * qts.size());
+    for (size_t j = 0; j < qts.size(); ++j) { qt[2 * j] = qts[j].second.first; qt[2 * j + 1] = qts[j].second.second; }
+    I.n_qt = static_cast<int32_t>(qts.size());
+    put(I.off_attn_hptr, hptr.data(), hptr.size());
+    put(I.off_attn_hrows, hrows.data(), hrows.size());
+    put(I.off_attn_qt, qt.data(), qt.size());
     while (w.size() % 64) w.push_back(0);
 }
 

@@ -10,6 +10,8 @@ namespace harts {
 
 // Device view of an uploaded plan: pointers into one int32 image.
 constexpr int kConvMaxW = 8;       // widest short convolution the plan tables serve
+constexpr int kAttnTile = 128;     // query / key rows per branch-attention tile
+constexpr int64_t kAttnMaxRows = int64_t(1) << 27;   // largest ancestor-row table built
 
 struct PlanDev {
     int32_t *err;                // [4] device error word: code, info, info, info
@@ -39,6 +41,11 @@ struct PlanDev {
     const int32_t *conv_ctx;       // [n_seg][kConvMaxW-1] rows 1..7 positions before the segment, -1 past the root
     const int32_t *conv_sptr;      // [n_seg*(kConvMaxW-1)+1] successor lists of (segment end, lag e+1)
     const int32_t *conv_succ;      // rows e+1 positions after the segment's end, on every branch
+    // branch attention: each sequence's ancestor prefix, and the query tiles
+    const int32_t *attn_hptr;      // [n_seq+1] ancestor rows of sequence i: attn_hrows[attn_hptr[i] ..]
+    const int32_t *attn_hrows;     // compact rows of the trajectory positions before the sequence
+    const int32_t *attn_qt;        // [n_qt][2] (sequence, query tile), most work first
+    int32_t n_qt;
     int32_t n_rounds, n_seq, n_states, n_roots, n_fold, chunk, n_seg;
     uint32_t flags;                // harts_plan_calls flags (HARTS_PLAN_NOREPLAY: slots inside chunks)
     int64_t R, n_chunks, C;
@@ -51,7 +58,9 @@ struct PlanImage {
         off_seq_rho, off_seq_rptr, off_seq_src, off_seq_sptr, off_state_lpos, off_seq_cbase,
         off_state_cptr, off_state_cons, off_root_cptr, off_root_cons, off_replay_idx,
         off_fold_rows, off_fold_ptr, off_fold_occ, off_chunk_seq, off_row_seg, off_seg_row0,
-        off_seg_len, off_conv_ctx, off_conv_sptr, off_conv_succ;
+        off_seg_len, off_conv_ctx, off_conv_sptr, off_conv_succ, off_attn_hptr, off_attn_hrows,
+        off_attn_qt;
+    int32_t n_qt;
 };
 
 void set_error(const std::string &msg);
@@ -72,6 +81,7 @@ struct harts_plan {
     std::vector<int32_t> state_cons_ptr, state_cons, root_cons_ptr, root_cons;
     std::vector<int32_t> seq_nchunks;
     harts::PlanImage image;
+    bool attn_ok = false;          // the image holds the branch-attention tables
     void *dev = nullptr;           // uploaded image (caller-owned)
     harts::PlanDev view{};         // valid once uploaded
 };

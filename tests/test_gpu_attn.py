@@ -1,0 +1,111 @@
+"""GPU parity of the branch attention (harts_attn_fwd) against the fp64 oracle
+(oracle/attn.py) on the same bf16 inputs: o within 1e-2 relative L2 (bf16 output, P
+rounded to bf16 before P V), lse within 1e-5 (fp32).  Forests with ragged query tiles,
+ancestor prefixes longer than a tile and not a multiple of it, single-token segments,
+the node-wise plan (another sequence split of the same tree), and the full-size forest
+on sampled rows."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from oracle import attn as oat
+from prefix_shared_chunkwise_gb300.api import Plan, attn_fwd
+from prefix_shared_chunkwise_gb300.synth import make_tree
+from tests._parity import rel_l2
+
+pytestmark = pytest.mark.gpu
+
+O_TOL, LSE_TOL = 1e-2, 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from prefix_shared_chunkwise_gb300 import build
+    build.build()
+
+
+def _inputs(C, H, seed, qscale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn((C, H, 128), generator=g) * qscale).to(torch.bfloat16)
+    k = torch.randn((C, H, 128), generator=g).to(torch.bfloat16)
+    v = torch.randn((C, H, 128), generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+def _check(parent, seg_len, H, seed, nodewise=False, qscale=1.0):
+    pl = Plan(parent, seg_len, 64, nodewise=nodewise)
+    pl.upload()
+    C = pl.info["C"]
+    q, k, v = _inputs(C, H, seed, qscale)
+    o, lse = attn_fwd(pl, q.cuda(), k.cuda(), v.cuda())
+    assert pl.device_error() == 0
+    ref = oat.attn_forest(np.asarray(parent), np.asarray(seg_len), pl.arrays()["seg_offset"],
+                          q.double().numpy(), k.double().numpy(), v.double().numpy(), 128 ** -0.5)
+    eo = rel_l2(o.float().cpu().numpy(), ref["o"])
+    el = rel_l2(lse.cpu().numpy(), ref["lse"])
+    assert eo <= O_TOL and el <= LSE_TOL, (eo, el)
+
+
+def _random_forest(seed, n, len_hi):
+    rng = np.random.default_rng(seed)
+    parent = np.array([-1] + [int(rng.integers(-1, i)) if rng.random() < 0.1 else int(rng.integers(0, i))
+                              for i in range(1, n)], np.int32)
+    seg_len = rng.integers(1, len_hi, size=n).astype(np.int64)
+    return parent, seg_len
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_random_forest_ragged_tiles(seed):
+    parent, seg_len = _random_forest(seed, 14, 300)
+    _check(parent, seg_len, 2, seed)
+
+
+def test_deep_prefix_not_tile_multiple():
+    # chain 0 -> 1 -> 2 with side branches: prefixes of 333, 333 + 200 and 533 + 70 rows
+    parent = np.array([-1, 0, 1, 0, 1, 2, 2], np.int32)
+    seg_len = np.array([333, 200, 70, 129, 1, 257, 128], np.int64)
+    _check(parent, seg_len, 3, 11)
+
+
+def test_single_token_segments_and_nodewise():
+    parent, seg_len = _random_forest(7, 40, 3)           # many 1-2 token segments
+    _check(parent, seg_len, 1, 12)
+    parent, seg_len = _random_forest(8, 12, 200)
+    _check(parent, seg_len, 2, 13, nodewise=True)
+
+
+def test_sharp_scores():
+    """Scores spread over tens of units: the running max moves across key tiles."""
+    parent, seg_len = _random_forest(9, 6, 400)
+    _check(parent, seg_len, 2, 14, qscale=6.0)
+
+
+def test_fig1_tree():
+    parent, seg_len = make_tree("fig1_fp32")
+    _check(parent, seg_len, 2, 15)
+
+
+def test_full_size_sampled_rows():
+    """The 64K-token forest at H = 16: sampled rows (first, last, random) against the
+    oracle evaluated on each row's own trajectory prefix."""
+    parent, seg_len = make_tree("fb64k_bf16")
+    pl = Plan(parent, seg_len, 64)
+    pl.upload()
+    C, H = pl.info["C"], 16
+    g = torch.Generator(device="cuda").manual_seed(5)
+    q, k, v = (torch.randn((C, H, 128), generator=g, device="cuda").to(torch.bfloat16) for _ in range(3))
+    o, lse = attn_fwd(pl, q, k, v)
+    assert pl.device_error() == 0
+    so = pl.arrays()["seg_offset"]
+    rng = np.random.default_rng(6)
+    rows = np.unique(np.concatenate([[0, C - 1], rng.integers(0, C, size=12)]))
+    for r in rows:
+        view = oat.trajectory_prefix(parent, seg_len, so, int(r))
+        idx = torch.as_tensor(view, device="cuda")
+        ref_o, ref_l = oat.attn_query(q[int(r)].double().cpu().numpy(), k[idx].double().cpu().numpy(),
+                                      v[idx].double().cpu().numpy(), 128 ** -0.5)
+        assert rel_l2(o[int(r)].float().cpu().numpy(), ref_o) <= O_TOL
+        assert rel_l2(lse[int(r)].cpu().numpy(), ref_l) <= LSE_TOL

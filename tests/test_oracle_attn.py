@@ -45,3 +45,25 @@ def test_branch_sees_ancestors_not_sibling():
     # zero scores: uniform over the visible rows
     assert o[3] == pytest.approx((1 + 2 + 5) / 3)      # C0 sees A0, A1, C0 -- not B0
     assert o[2] == pytest.approx((1 + 2 + 100) / 3)
+
+
+def test_single_query_matches_forest():
+    """attn_query over trajectory_prefix (used for sampled rows of large forests) gives
+    the forest oracle's output for every row of a random forest, with the compact rows
+    laid out in a shuffled segment order."""
+    rng = np.random.default_rng(21)
+    n = 10
+    parent = np.array([-1] + [int(rng.integers(-1, i)) for i in range(1, n)])
+    seg_len = rng.integers(1, 7, size=n)
+    order = rng.permutation(n)
+    so = np.zeros(n, np.int64)
+    so[order] = np.concatenate([[0], np.cumsum(seg_len[order])[:-1]])
+    C = int(seg_len.sum())
+    q, k, v = (rng.standard_normal((C, 2, 5)) for _ in range(3))
+    full = attn.attn_forest(parent, seg_len, so, q, k, v, 0.3)
+    for r in range(C):
+        view = attn.trajectory_prefix(parent, seg_len, so, r)
+        assert view[-1] == r and len(np.unique(view)) == len(view)
+        o, lse = attn.attn_query(q[r], k[view], v[view], 0.3)
+        np.testing.assert_allclose(o, full["o"][r], atol=1e-12)
+        np.testing.assert_allclose(lse, full["lse"][r], atol=1e-12)

@@ -169,3 +169,34 @@ def test_planner_rejects_malformed_input(parent, seg_len, chunk):
     with pytest.raises(_lib.HartsError) as e:
         Plan(np.array(parent), np.array(seg_len), chunk)
     assert e.value.rc == -1
+
+
+def _attn_call(pl, H=2, d=128, dtype=_lib.HARTS_BF16, ptr=0x10000):
+    a = _lib.AttnFwdArgs()
+    a.H, a.d, a.dtype, a.scale = H, d, dtype, 0.1
+    a.q = a.k = a.v = a.o = ptr or None
+    return _lib.lib().harts_attn_fwd(pl.handle, ctypes.byref(a), None)
+
+
+def test_attention_argument_checks_on_the_host():
+    """harts_attn_fwd validates before it touches the device (no pointer is read):
+    dtype / head dimension, heads, NULL and misaligned pointers, then the upload."""
+    pl = Plan(np.array([-1, 0, 0], np.int32), np.array([5, 3, 4], np.int64), 64)
+    assert _attn_call(pl, dtype=_lib.HARTS_FP32) == -2
+    assert _attn_call(pl, d=64) == -2
+    assert _attn_call(pl, H=0) == -1
+    assert _attn_call(pl, ptr=0) == -1
+    assert _attn_call(pl, ptr=0x10008) == -1
+    assert _attn_call(pl) == -8                           # not uploaded
+
+
+def test_attention_tables_bounded_for_deep_combs():
+    """A comb (spine of 2000 segments, a one-token side branch at each) has ancestor
+    views adding up to about 2 * 10^8 rows: the plan is built without attention tables
+    and harts_attn_fwd reports HARTS_EOVERFLOW; a shallower comb keeps them."""
+    def comb(n, L):
+        parent = np.concatenate([[-1], np.arange(n - 1), np.arange(n)]).astype(np.int32)
+        seg_len = np.concatenate([np.full(n, L), np.ones(n)]).astype(np.int64)
+        return Plan(parent, seg_len, 64)
+    assert _attn_call(comb(2000, 100)) == -3
+    assert _attn_call(comb(200, 100)) == -8
