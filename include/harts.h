@@ -387,13 +387,13 @@ typedef struct {
     int32_t H;               /* heads */
     int32_t d;               /* head dimension of q, k and v: 128 */
     int32_t dtype;           /* harts_dtype of q, k, v, o: HARTS_BF16 */
-    float scale;             /* softmax scale (typically 1/sqrt(d)) */
+    float scale;             /* softmax scale, positive and finite (typically 1/sqrt(d)) */
     const void *q, *k, *v;   /* device [C][H][d], compact layout, 16-byte aligned */
     void *o;                 /* device [C][H][d] output, 16-byte aligned */
     float *lse;              /* device [C][H] output (natural-log sum-exp of scaled scores), or NULL */
 } harts_attn_fwd_args;
 
-/* Forward.  Errors: HARTS_EINVAL (NULL / misaligned pointers, H < 1), HARTS_EUNSUPPORTED
+/* Forward.  Errors: HARTS_EINVAL (NULL / misaligned pointers, H < 1, scale not positive), HARTS_EUNSUPPORTED
  * (dtype other than bf16, d other than 128), HARTS_ENOPLAN, HARTS_EOVERFLOW (no attention
  * tables in the plan, too many blocks), HARTS_ECUDA.  A bounded wait that runs out records
  * device code 3 (timeout) in the plan's device error word (harts_plan_device_error). */

@@ -382,8 +382,10 @@ void build_image(harts_plan &P) {
 
     // ---- branch attention -------------------------------------------------------------
     // A sequence's view: the trajectory positions before its first own token (ancestor
-    // rows, root first), then its own rows.  Query tiles of kAttnTile own rows, ordered
-    // by decreasing work (view length up to the tile's end).
+    // rows, root first), then its own rows.  Query tiles of kAttnTile own rows, grouped
+    // by tree (so the blocks that read a tree's keys and values run together and find
+    // them in L2), trees in decreasing order of their longest tile, and within a tree by
+    // decreasing work (view length up to the tile's end).
     // The ancestor lists add up to sum_i (first position of sequence i), quadratic in the
     // depth of chain-like trees: above kAttnMaxRows the plan carries no attention tables.
     int64_t sum_h = 0;
@@ -399,15 +401,29 @@ void build_image(harts_plan &P) {
             for (int64_t t = 0; t < P.seg_len[*it]; ++t) hrows.push_back(static_cast<int32_t>(P.seg_offset[*it] + t));
     }
     hptr[n_seq] = static_cast<int32_t>(hrows.size());
-    std::vector<std::pair<int64_t, std::pair<int32_t, int32_t>>> qts;
+    struct QTile { int64_t work; int32_t tree, seq, tile; };
+    std::vector<QTile> qts;
+    std::vector<int32_t> root(P.parent.size());
+    for (size_t v = 0; v < P.parent.size(); ++v) root[v] = P.parent[v] < 0 ? static_cast<int32_t>(v) : root[P.parent[v]];
+    std::vector<int64_t> tree_work(P.parent.size(), 0);
     for (int32_t i = 0; i < n_seq && P.attn_ok; ++i) {
         const int64_t own = P.cu_seqlens[i + 1] - P.cu_seqlens[i], hh = hptr[i + 1] - hptr[i];
-        for (int64_t t = 0; t * kAttnTile < own; ++t)
-            qts.push_back({hh + std::min(own, (t + 1) * kAttnTile), {i, static_cast<int32_t>(t)}});
+        const int32_t r = root[P.seq_first_seg[i]];
+        for (int64_t t = 0; t * kAttnTile < own; ++t) {
+            const int64_t w = hh + std::min(own, (t + 1) * kAttnTile);
+            qts.push_back({w, r, i, static_cast<int32_t>(t)});
+            tree_work[r] = std::max(tree_work[r], w);
+        }
     }
-    std::stable_sort(qts.begin(), qts.end(), [](const auto &a, const auto &b) { return a.first > b.first; });
+    std::stable_sort(qts.begin(), qts.end(), [&](const QTile &a, const QTile &b) {
+        if (a.tree != b.tree) {
+            if (tree_work[a.tree] != tree_work[b.tree]) return tree_work[a.tree] > tree_work[b.tree];
+            return a.tree < b.tree;
+        }
+        return a.work > b.work;
+    });
     std::vector<int32_t> qt(2 * qts.size());
-    for (size_t j = 0; j < qts.size(); ++j) { qt[2 * j] = qts[j].second.first; qt[2 * j + 1] = qts[j].second.second; }
+    for (size_t j = 0; j < qts.size(); ++j) { qt[2 * j] = qts[j].seq; qt[2 * j + 1] = qts[j].tile; }
     I.n_qt = static_cast<int32_t>(qts.size());
     put(I.off_attn_hptr, hptr.data(), hptr.size());
     put(I.off_attn_hrows, hrows.data(), hrows.size());
