@@ -28,13 +28,13 @@ Fig. 1(c) and Fig. 2 on page "thelatestinai ... 2608.28158"):
 
   The first case is a fork inside the chunk where v's own sequence starts: the
   side children can start in the same call from the same anchor state, replaying
-  [a(s_v), e_v) (Fig. 2(c): "replay-started v2" runs in round 1).
+  [a(s_v), e_v) (Fig. 2(c): v2, started by replay, runs in round 1).
 * Recovery is top-down and as-soon-as-possible.
 
 Conventions (several plans are optimal; these make the plan unique):
 * the continuation is the lowest-id child among those with maximal T_pre;
 * sequences are ordered by round, then by the id of their first segment
-  (Fig. 1(c): "Call 2 batches independent [C] and [E]");
+  (Fig. 1(c) lists the second call as [C], then [E]);
 * within a sequence, segments follow the continuation chain; compact rows follow
   that order (one compact physical layout, section 4.3);
 * one state slot per distinct (producer sequence, local position); slots are

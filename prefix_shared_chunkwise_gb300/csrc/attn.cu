@@ -13,9 +13,9 @@
 //   S_j = Q K_j^T           tcgen05, M = N = 128, K = d, fp32 in one of two TMEM buffers;
 //                           S_{j+1} is issued as soon as S_j is ready, so the tensor core
 //                           works while the warps run the softmax of tile j
-//   softmax                 eight warps, one query row and 64 columns each; scores in
-//                           base-2 units (scale * log2 e folded into one FMA); the row max
-//                           is shared between the column halves through shared memory; the
+//   softmax                 sixteen warps, one query row and 32 columns each; scores in
+//                           base-2 units (scale * log2 e folded into one FMA); the four
+//                           warps holding a row exchange its max through shared memory; the
 //                           running max moves (and O is rescaled in TMEM) only when a row's
 //                           max grows by more than 2^8 -- any common offset gives the same
 //                           softmax, the threshold only bounds P by 256
@@ -32,15 +32,15 @@
 namespace harts {
 namespace {
 
-constexpr int AD = 128, AT = kAttnTile, ANT = 256;
+constexpr int AD = 128, AT = kAttnTile, ANT = 512, NQ = ANT / AT;   // NQ column quarters
 constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;               // running max moves when a row max grows by more
 
 namespace at_sm {
 constexpr uint32_t Q = 0, K0 = 32768, K1 = 65536, V0 = 98304, V1 = 131072, P = 163840;
-constexpr uint32_t Max = 196608;                  // [2 tiles][2 halves][128] fp32 row maxima
-constexpr uint32_t Sum = Max + 2048;              // [2 halves][128] fp32 row sums
-constexpr uint32_t Tab = Sum + 1024;              // [4][128] int32 view rows of tiles j % 4
+constexpr uint32_t Max = 196608;                  // [2 tiles][4 quarters][128] fp32 row maxima
+constexpr uint32_t Sum = Max + 4096;              // [4 quarters][128] fp32 row sums
+constexpr uint32_t Tab = Sum + 2048;              // [4][128] int32 view rows of tiles j % 4
 constexpr uint32_t bytes = Tab + 2048 + 1024;     // + alignment slack
 }  // namespace at_sm
 
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(ANT, 1) attn_fwd_tc(AttnParams p, PlanDev pd) 
     __shared__ int s_fail;
     float *smax = reinterpret_cast<float *>(sm + Max), *ssum = reinterpret_cast<float *>(sm + Sum);
     int32_t *stab = reinterpret_cast<int32_t *>(sm + Tab);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, ch = warp >> 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, cq = warp >> 2;
     const int H = p.H;
     const int32_t h = blockIdx.x % H, qi = blockIdx.x / H;
     const int32_t sq = pd.attn_qt[2 * qi], qt = pd.attn_qt[2 * qi + 1];
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(ANT, 1) attn_fwd_tc(AttnParams p, PlanDev pd) 
         nc_s0 = 1;
     }
 
-    float m_run = -INFINITY, l_half = 0.f;
+    float m_run = -INFINITY, l_part = 0.f;
     for (int32_t kt = 0; kt < n_kt; ++kt) {
         const int b = kt & 1;
         // A: S_kt ready; K_{kt+1} in shared memory
@@ -185,28 +185,26 @@ __global__ void __launch_bounds__(ANT, 1) attn_fwd_tc(AttnParams p, PlanDev pd) 
         int32_t nxt = -1;
         if (tid < AT && (kt + 3) * AT + tid < n_kt * AT) nxt = view_row((kt + 3) * AT + tid);
         // D: scores, mask, row max of this half
-        float s[64];
-        {
-            float r[32];
-            tc::tmem_ld32(tm + b * 128 + lane_off + ch * 64, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[i] = r[i];
-            tc::tmem_ld32(tm + b * 128 + lane_off + ch * 64 + 32, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[32 + i] = r[i];
-        }
+        float s[32];
+        tc::tmem_ld32(tm + b * 128 + lane_off + cq * 32, s);
         if (kt >= first_masked) {
-            const int32_t lim = vis - (kt * AT + ch * 64);
+            const int32_t lim = vis - (kt * AT + cq * 32);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) s[i] = i <= lim ? s[i] : -INFINITY;
+            for (int i = 0; i < 32; ++i) s[i] = i <= lim ? s[i] : -INFINITY;
         }
-        float mx = s[0];
+        float mp[8];
 #pragma unroll
-        for (int i = 1; i < 64; ++i) mx = fmaxf(mx, s[i]);
-        smax[(b * 2 + ch) * AT + qrow] = mx;
-        __syncthreads();
-        // F: running max (moves only past the threshold), probabilities, row sum of this half
-        const float m_tile = c * fmaxf(smax[(b * 2) * AT + qrow], smax[(b * 2 + 1) * AT + qrow]);
+        for (int i = 0; i < 8; ++i) mp[i] = fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24]));
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) mp[i] = fmaxf(mp[i], mp[i + w]);
+        smax[(b * NQ + cq) * AT + qrow] = mp[0];
+        // the four warps holding these rows exchange their maxima (named barrier 1 + lg)
+        asm volatile("bar.sync %0, %1;" :: "r"(1 + lg), "n"(NQ * 32) : "memory");
+        // F: running max (moves only past the threshold), probabilities, row sum of this quarter
+        const float *mrow = smax + b * NQ * AT + qrow;
+        const float m_tile = c * fmaxf(fmaxf(mrow[0], mrow[AT]), fmaxf(mrow[2 * AT], mrow[3 * AT]));
         const bool move = __any_sync(0xffffffffu, m_tile > m_run + kRescaleLog2);
         float alpha = 1.f;
         if (move) {
@@ -214,27 +212,28 @@ __global__ void __launch_bounds__(ANT, 1) attn_fwd_tc(AttnParams p, PlanDev pd) 
             alpha = ex2(m_run - m_new);
             m_run = m_new;
         }
-        float sum = 0.f;
+        float sp[8];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
+        for (int i = 0; i < 32; ++i) {
             s[i] = ex2(fmaf(s[i], c, -m_run));
-            sum += s[i];
+            sp[i & 7] = (i < 8) ? s[i] : sp[i & 7] + s[i];
         }
-        l_half = l_half * alpha + sum;
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) sp[i] += sp[i + w];
+        l_part = l_part * alpha + sp[0];
         // G: O_{kt-1} done (P buffer and O free); P, rescale of O, V_{kt+1}
         if (kt > 0) wait_or_fail(&bars[2], (kt - 1) & 1, 2, &s_fail);
         tc::fence_after_sync();
 #pragma unroll
-        for (int i = 0; i < 64; i += 8) tc::st_sw128_8(sm + P, AT, qrow, ch * 64 + i, s + i);
+        for (int i = 0; i < 32; i += 8) tc::st_sw128_8(sm + P, AT, qrow, cq * 32 + i, s + i);
         if (move && kt > 0) {
+            float r[32];
+            tc::tmem_ld32(tO + lane_off + cq * 32, r);
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float r[32];
-                tc::tmem_ld32(tO + lane_off + ch * 64 + hf * 32, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] *= alpha;
-                tc::tmem_st32(tO + lane_off + ch * 64 + hf * 32, r);
-            }
+            for (int i = 0; i < 32; ++i) r[i] *= alpha;
+            tc::tmem_st32(tO + lane_off + cq * 32, r);
         }
         if (kt + 1 < n_kt) stage(p.v, kt + 1, sm + (b ? V0 : V1));
         tc::cp_async_commit();
@@ -251,30 +250,27 @@ __global__ void __launch_bounds__(ANT, 1) attn_fwd_tc(AttnParams p, PlanDev pd) 
     }
     wait_or_fail(&bars[2], (n_kt - 1) & 1, 2, &s_fail);
     tc::fence_after_sync();
-    ssum[ch * AT + qrow] = l_half;
+    ssum[cq * AT + qrow] = l_part;
     __syncthreads();
     // ---- outputs ------------------------------------------------------------------------
     if (!s_fail) {
-        const float l = ssum[qrow] + ssum[AT + qrow], inv = 1.f / l;
+        const float l = (ssum[qrow] + ssum[AT + qrow]) + (ssum[2 * AT + qrow] + ssum[3 * AT + qrow]), inv = 1.f / l;
         const int64_t row = static_cast<int64_t>(row0) + q0 + qrow;
+        float r[32];
+        tc::tmem_ld32(tO + lane_off + cq * 32, r);
+        if (qrow < nq) {
+            uint4 *dst = reinterpret_cast<uint4 *>(p.o + (row * H + h) * AD + cq * 32);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            float r[32];
-            tc::tmem_ld32(tO + lane_off + ch * 64 + hf * 32, r);
-            if (qrow < nq) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.o + (row * H + h) * AD + ch * 64 + hf * 32);
-#pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    uint4 w;
-                    w.x = tc::pack_bf16(r[i] * inv, r[i + 1] * inv);
-                    w.y = tc::pack_bf16(r[i + 2] * inv, r[i + 3] * inv);
-                    w.z = tc::pack_bf16(r[i + 4] * inv, r[i + 5] * inv);
-                    w.w = tc::pack_bf16(r[i + 6] * inv, r[i + 7] * inv);
-                    dst[i / 8] = w;
-                }
+            for (int i = 0; i < 32; i += 8) {
+                uint4 w;
+                w.x = tc::pack_bf16(r[i] * inv, r[i + 1] * inv);
+                w.y = tc::pack_bf16(r[i + 2] * inv, r[i + 3] * inv);
+                w.z = tc::pack_bf16(r[i + 4] * inv, r[i + 5] * inv);
+                w.w = tc::pack_bf16(r[i + 6] * inv, r[i + 7] * inv);
+                dst[i / 8] = w;
             }
         }
-        if (p.lse && ch == 0 && qrow < nq) p.lse[row * H + h] = m_run * kLn2 + logf(l);
+        if (p.lse && cq == 0 && qrow < nq) p.lse[row * H + h] = m_run * kLn2 + logf(l);
     }
     tc::cp_async_wait_all();
     if (s_fail && tid == 0) {                           // drain the products still in flight
