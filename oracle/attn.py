@@ -86,3 +86,29 @@ def attn_query(q_row, k_view, v_view, scale):
         o[h] = (p / p.sum()) @ v_view[:, h]
         lse[h] = m + np.log(p.sum())
     return o, lse
+
+
+def attn_forest_bwd(parent, seg_len, seg_offset, q, k, v, do, scale):
+    """Gradients of L = sum_r <do[r], o[r]> for the compact-row outputs of attn_forest:
+    each compact query row counts once, over its own trajectory prefix.  Returns dict(dq,
+    dk, dv), all [C, H, d]; keys and values collect the contributions of every query that
+    sees them, across branches."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.asarray(do, np.float64)
+    C, H, _ = q.shape
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for r in range(C):
+        view = trajectory_prefix(parent, seg_len, seg_offset, r)
+        for h in range(H):
+            kv, vv = k[view, h], v[view, h]
+            s = scale * kv @ q[r, h]
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            dv[view, h] += np.outer(p, do[r, h])
+            dp = vv @ do[r, h]
+            ds = p * (dp - p @ dp)
+            dq[r, h] = scale * ds @ kv
+            dk[view, h] += scale * np.outer(ds, q[r, h])
+    return dict(dq=dq, dk=dk, dv=dv)
