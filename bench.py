@@ -559,15 +559,16 @@ def run_logprob(hbm):
 
 
 def run_attn(parent, seg_len, pl, x, tf_peak):
-    """Branch attention (forward) over the compact layout on the forest's q, k, v ([C, H,
-    128] bf16): CUDA-event time of harts_attn_fwd, algorithmic FLOPs (4 d per head and
-    visible (query, key) pair: Q K^T and P V) against the bf16 tensor peak, the FLOPs of
+    """Branch attention over the compact layout on the forest's q, k, v ([C, H, 128] bf16):
+    CUDA-event times of harts_attn_fwd and harts_attn_bwd, algorithmic FLOPs (per head and
+    visible (query, key) pair: 4 d forward, Q K^T and P V; 10 d backward, S, dP, dV, dQ,
+    dK) against the bf16 tensor peak, the FLOPs of
     the 128 x 128 tiles the kernel issues (masked entries included), and the pairs the
     per-trajectory execution would compute instead (every trajectory causally over its
     own tokens)."""
     import numpy as np
     import torch
-    from prefix_shared_chunkwise_gb300.api import attn_fwd
+    from prefix_shared_chunkwise_gb300.api import attn_bwd, attn_fwd
     C, H, d = x["q"].shape
     a = pl.arrays()
     pos, ln = a["seg_pos"].astype(np.float64), np.asarray(seg_len, np.float64)
@@ -590,25 +591,40 @@ def run_attn(parent, seg_len, pl, x, tf_peak):
     o = torch.empty_like(x["q"])
     lse = torch.empty((C, H), dtype=torch.float32, device=o.device)
 
-    def step():
+    dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
+    do = x["v"]                                      # any [C, H, d] bf16 tensor serves as dL/do
+    from prefix_shared_chunkwise_gb300 import _lib
+    ws = torch.empty(max(int(_lib.lib().harts_attn_bwd_workspace_bytes(pl.handle, H)), 256), dtype=torch.uint8,
+                     device=o.device)
+
+    def fwd():
         attn_fwd(pl, x["q"], x["k"], x["v"], o=o, lse=lse)
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
-    reps = 10
-    e0.record()
-    for _ in range(reps):
-        step()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
+    def bwd():
+        attn_bwd(pl, x["q"], x["k"], x["v"], o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    def timed(fn, reps=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    ms = timed(fwd)
+    ms_b = timed(bwd)
     flops = 4.0 * d * H * pairs
+    flops_b = 10.0 * d * H * pairs                   # S, dP, dV, dQ, dK: 2 d each per pair
     tile_flops = 4.0 * d * H * tiles * 128 * 128
     return dict(shape=[C, H, d], ms=round(ms, 3), visible_pairs=int(pairs),
                 tflops=round(flops / ms / 1e9, 1), frac=round(flops / ms / 1e9 / tf_peak, 4),
                 tile_tflops=round(tile_flops / ms / 1e9, 1), tile_util=round(pairs * H / (tiles * 128 * 128 * H), 3),
+                bwd=dict(ms=round(ms_b, 3), tflops=round(flops_b / ms_b / 1e9, 1),
+                         frac=round(flops_b / ms_b / 1e9 / tf_peak, 4)),
                 per_trajectory_pairs=int(traj_pairs), work_saved=round(traj_pairs / pairs, 3),
                 peak_tflops=tf_peak, peak_source="bf16_tflops (burst, kernel timed alone)")
 

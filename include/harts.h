@@ -399,6 +399,30 @@ typedef struct {
  * device code 3 (timeout) in the plan's device error word (harts_plan_device_error). */
 int harts_attn_fwd(const harts_plan *plan, const harts_attn_fwd_args *args, harts_stream_t stream);
 
+/* Backward of harts_attn_fwd for L with dL/do = d_o: each compact query row counts once,
+ * over its own view; keys and values collect every query that sees them, across branches.
+ * With D = rowsum(d_o * o) and P recomputed from lse:
+ *   dv_j = sum_t P_tj d_o_t,  dS_tj = scale P_tj (d_o_t . v_j - D_t),
+ *   dq_t = sum_j dS_tj k_j,   dk_j = sum_t dS_tj q_t.
+ * Sums run in a fixed order (no atomics): per query tile over its view's key tiles, per
+ * key tile (128 own rows of a sequence) over the query tiles that see it, in ascending
+ * (sequence, tile) order. */
+typedef struct {
+    harts_attn_fwd_args fwd; /* q, k, v; o and lse as written by the forward (lse required) */
+    const void *d_o;         /* device [C][H][d] bf16 dL/do per compact row */
+    void *dq, *dk, *dv;      /* device [C][H][d] bf16 outputs (overwritten), 16-byte aligned */
+    void *workspace;         /* device, harts_attn_bwd_workspace_bytes, 16-byte aligned */
+    size_t workspace_bytes;
+} harts_attn_bwd_args;
+
+/* Workspace of harts_attn_bwd: D, fp32 [C][H] (rounded up to 256 bytes); 0 for invalid
+ * arguments. */
+size_t harts_attn_bwd_workspace_bytes(const harts_plan *plan, int32_t H);
+
+/* Errors as harts_attn_fwd, plus HARTS_EINVAL (NULL / misaligned lse, d_o, dq, dk, dv,
+ * workspace) and HARTS_ESMALLBUF (workspace). */
+int harts_attn_bwd(const harts_plan *plan, const harts_attn_bwd_args *args, harts_stream_t stream);
+
 const char *harts_last_error(void);
 
 #ifdef __cplusplus

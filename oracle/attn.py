@@ -88,6 +88,28 @@ def attn_query(q_row, k_view, v_view, scale):
     return o, lse
 
 
+def attn_query_bwd(q_row, k_view, v_view, do_row, scale):
+    """Backward of attn_query for dL/do = do_row: (dq_row [H, dk], dk_view [n, H, dk],
+    dv_view [n, H, dv])."""
+    q_row = np.asarray(q_row, np.float64)
+    k_view = np.asarray(k_view, np.float64)
+    v_view = np.asarray(v_view, np.float64)
+    do_row = np.asarray(do_row, np.float64)
+    dq = np.zeros_like(q_row)
+    dk, dv = np.zeros_like(k_view), np.zeros_like(v_view)
+    for h in range(q_row.shape[0]):
+        kv, vv = k_view[:, h], v_view[:, h]
+        s = scale * kv @ q_row[h]
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        dv[:, h] = np.outer(p, do_row[h])
+        dp = vv @ do_row[h]
+        ds = p * (dp - p @ dp)
+        dq[h] = scale * ds @ kv
+        dk[:, h] = scale * np.outer(ds, q_row[h])
+    return dq, dk, dv
+
+
 def attn_forest_bwd(parent, seg_len, seg_offset, q, k, v, do, scale):
     """Gradients of L = sum_r <do[r], o[r]> for the compact-row outputs of attn_forest:
     each compact query row counts once, over its own trajectory prefix.  Returns dict(dq,
@@ -97,18 +119,11 @@ def attn_forest_bwd(parent, seg_len, seg_offset, q, k, v, do, scale):
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
     do = np.asarray(do, np.float64)
-    C, H, _ = q.shape
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
-    for r in range(C):
+    for r in range(q.shape[0]):
         view = trajectory_prefix(parent, seg_len, seg_offset, r)
-        for h in range(H):
-            kv, vv = k[view, h], v[view, h]
-            s = scale * kv @ q[r, h]
-            p = np.exp(s - s.max())
-            p /= p.sum()
-            dv[view, h] += np.outer(p, do[r, h])
-            dp = vv @ do[r, h]
-            ds = p * (dp - p @ dp)
-            dq[r, h] = scale * ds @ kv
-            dk[view, h] += scale * np.outer(ds, q[r, h])
+        g_q, g_k, g_v = attn_query_bwd(q[r], k[view], v[view], do[r], scale)
+        dq[r] = g_q
+        np.add.at(dk, view, g_k)
+        np.add.at(dv, view, g_v)
     return dict(dq=dq, dk=dk, dv=dv)

@@ -26,7 +26,7 @@ EXPORTED = [
     "harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad", "harts_kda_bwd_static",
     "harts_kda_bwd_static_max_bytes", "harts_conv_fwd", "harts_conv_bwd_workspace_bytes",
     "harts_conv_bwd", "harts_plan_semantic_map", "harts_logprob_fwd", "harts_logprob_bwd",
-    "harts_attn_fwd", "harts_last_error",
+    "harts_attn_fwd", "harts_attn_bwd_workspace_bytes", "harts_attn_bwd", "harts_last_error",
 ]
 
 _i32, _i64, _vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
@@ -95,6 +95,11 @@ class AttnFwdArgs(ctypes.Structure):
                 ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("lse", _vp)]
 
 
+class AttnBwdArgs(ctypes.Structure):
+    _fields_ = [("fwd", AttnFwdArgs), ("d_o", _vp), ("dq", _vp), ("dk", _vp), ("dv", _vp),
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
+
+
 _lib = None
 
 
@@ -140,6 +145,10 @@ def lib():
         L.harts_logprob_bwd.restype = ctypes.c_int
         L.harts_attn_fwd.argtypes = [_vp, ctypes.POINTER(AttnFwdArgs), _vp]
         L.harts_attn_fwd.restype = ctypes.c_int
+        L.harts_attn_bwd_workspace_bytes.argtypes = [_vp, _i32]
+        L.harts_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        L.harts_attn_bwd.argtypes = [_vp, ctypes.POINTER(AttnBwdArgs), _vp]
+        L.harts_attn_bwd.restype = ctypes.c_int
         L.harts_last_error.argtypes = []
         L.harts_last_error.restype = ctypes.c_char_p
         for fn in ("harts_plan_calls", "harts_plan_get_info", "harts_plan_export",

@@ -277,9 +277,37 @@ def attn_fwd(plan: Plan, q, k, v, *, scale=None, o=None, lse=None, stream=None):
     for n, t in dict(q=q, k=k, v=v, o=o, lse=lse).items():
         if not t.is_contiguous():
             raise ValueError(f"{n} must be contiguous")
+    a = _attn_args(q, k, v, o, lse, scale)
+    L.check(L.lib().harts_attn_fwd(plan.handle, ctypes.byref(a), _stream(stream)), "harts_attn_fwd")
+    return o, lse
+
+
+def _attn_args(q, k, v, o, lse, scale):
+    C, H, d = q.shape
     a = L.AttnFwdArgs()
     a.H, a.d, a.dtype = H, d, dtype_code(q.dtype)
     a.scale = float(d ** -0.5 if scale is None else scale)
-    a.q, a.k, a.v, a.o, a.lse = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr()
-    L.check(L.lib().harts_attn_fwd(plan.handle, ctypes.byref(a), _stream(stream)), "harts_attn_fwd")
-    return o, lse
+    a.q, a.k, a.v, a.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
+    a.lse = None if lse is None else lse.data_ptr()
+    return a
+
+
+def attn_bwd(plan: Plan, q, k, v, o, lse, d_o, *, scale=None, dq=None, dk=None, dv=None, workspace=None,
+             stream=None):
+    """harts_attn_bwd: returns (dq, dk, dv) like q, from the forward's o and lse."""
+    import torch
+    for n, t in dict(q=q, k=k, v=v, o=o, lse=lse, d_o=d_o).items():
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    b = L.AttnBwdArgs()
+    b.fwd = _attn_args(q, k, v, o, lse, scale)
+    nb = int(L.lib().harts_attn_bwd_workspace_bytes(plan.handle, q.shape[1]))
+    if workspace is None:
+        workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
+    b.d_o, b.dq, b.dk, b.dv = d_o.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    b.workspace, b.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    L.check(L.lib().harts_attn_bwd(plan.handle, ctypes.byref(b), _stream(stream)), "harts_attn_bwd")
+    return dq, dk, dv

@@ -24,6 +24,7 @@
 // tiles and V one tile ahead.  Masking runs only on tiles that reach past the first
 // query's causal limit.  Every wait is bounded; a timeout records code 3 in the plan's
 // error word, stops issuing products and drains the ones in flight.
+#include <algorithm>
 #include <cstring>
 
 #include "kda_common.cuh"
@@ -286,14 +287,355 @@ __global__ void __launch_bounds__(ANT, 1) attn_fwd_tc(AttnParams p, PlanDev pd) 
     if (warp == 0) tc::tmem_dealloc(tm, 512);
 }
 
+
+// ======================================================================================
+// Backward.  With D_t = sum_d dO_t o_t (per query row and head), P = softmax(scale S):
+//   dV_j = sum_t P_tj dO_t,  dS_tj = scale P_tj (dP_tj - D_t) with dP = dO V^T,
+//   dQ_t = sum_j dS_tj K_j,  dK_j = sum_t dS_tj Q_t,
+// every query row once (its own compact row), over its view.  P is recomputed from the
+// forward's log-sum-exp.  dQ: one block per (query tile, head) over the view's key tiles,
+// as the forward.  dK, dV: one block per (key tile of a sequence's own rows, head) over
+// the query tiles that see it (planner lists: the sequence's own tiles, causal, and the
+// tiles of every sequence whose prefix runs through it, a prefix of the key tile
+// visible).  Fixed summation orders, no atomics.
+// ======================================================================================
+
+__global__ void attn_bwd_prep(const __nv_bfloat16 *o, const __nv_bfloat16 *dout, float *D, int64_t rows) {
+    // one warp per (row, head): 128 channels, 4 per lane
+    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int64_t r = w; r < rows; r += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(o + r * AD + lane * 4);
+        const uint2 g = *reinterpret_cast<const uint2 *>(dout + r * AD + lane * 4);
+        const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a);
+        const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g);
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float2 x = __bfloat1622float2(a2[i]), y = __bfloat1622float2(g2[i]);
+            acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+        if (lane == 0) D[r] = acc;
+    }
+}
+
+struct AttnBwdParams {
+    const __nv_bfloat16 *q, *k, *v, *dout;
+    const float *lse, *D;
+    __nv_bfloat16 *dq, *dk, *dv;
+    int32_t H;
+    float scale;
+};
+
+namespace bq_sm {
+constexpr uint32_t Q = 0, dO = 32768, K0 = 65536, K1 = 98304, V = 131072, dS = 163840;
+constexpr uint32_t Tab = 196608;                  // [4][128] int32 view rows of tiles j % 4
+constexpr uint32_t bytes = Tab + 2048 + 1024;
+}  // namespace bq_sm
+
+// Stage `rows` (row index per tile row, -1 = zero) of head h into a SW128 tile.
+__device__ __forceinline__ void stage_rows(const __nv_bfloat16 *src, const int32_t *tab, int H, int h, uint8_t *dst,
+                                           int tid) {
+#pragma unroll
+    for (int i = 0; i < AT * 16 / ANT; ++i) {
+        const int e = tid + i * ANT, r = e >> 4, pc = e & 15;
+        const int32_t row = tab[r];
+        const __nv_bfloat16 *g = src + (static_cast<int64_t>(row < 0 ? 0 : row) * H + h) * AD + pc * 8;
+        tc::cp_async16(dst + piece(r, pc), g, row >= 0 ? 16u : 0u);
+    }
+}
+
+// Stage rows first .. first + n - 1 (zeros for the rest of the tile).
+__device__ __forceinline__ void stage_run(const __nv_bfloat16 *src, int64_t first, int n, int H, int h, uint8_t *dst,
+                                          int tid) {
+#pragma unroll
+    for (int i = 0; i < AT * 16 / ANT; ++i) {
+        const int e = tid + i * ANT, r = e >> 4, pc = e & 15;
+        const bool ok = r < n;
+        const __nv_bfloat16 *g = src + ((first + (ok ? r : 0)) * H + h) * AD + pc * 8;
+        tc::cp_async16(dst + piece(r, pc), g, ok ? 16u : 0u);
+    }
+}
+
+__device__ __forceinline__ void store_tile_bf16(__nv_bfloat16 *dst_row, const float (&r)[32], float mul) {
+    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        uint4 w;
+        w.x = tc::pack_bf16(r[i] * mul, r[i + 1] * mul);
+        w.y = tc::pack_bf16(r[i + 2] * mul, r[i + 3] * mul);
+        w.z = tc::pack_bf16(r[i + 4] * mul, r[i + 5] * mul);
+        w.w = tc::pack_bf16(r[i + 6] * mul, r[i + 7] * mul);
+        dst[i / 8] = w;
+    }
+}
+
+__global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDev pd) {
+    using namespace bq_sm;
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
+    __shared__ uint64_t bars[2];                  // S and dP ready, dQ product done
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_fail;
+    int32_t *stab = reinterpret_cast<int32_t *>(sm + Tab);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, cq = warp >> 2;
+    const int H = p.H;
+    const int32_t h = blockIdx.x % H, qi = blockIdx.x / H;
+    const int32_t sq = pd.attn_qt[2 * qi], qt = pd.attn_qt[2 * qi + 1];
+    const int32_t hb = pd.attn_hptr[sq], hh = pd.attn_hptr[sq + 1] - hb;
+    const int32_t row0 = pd.seq_row0[sq], own = pd.seq_nown[sq], nview = hh + own;
+    const int32_t q0 = qt * AT, nq = min(AT, own - q0);
+    const int32_t n_kt = (hh + q0 + nq - 1) / AT + 1;
+    const int32_t first_masked = (hh + q0) / AT;
+    const float c = p.scale * kLog2e;
+    auto view_row = [&](int32_t j) -> int32_t {
+        return j < hh ? pd.attn_hrows[hb + j] : (j < nview ? row0 + (j - hh) : -1);
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) tc::mbar_init(&bars[i], 1);
+        tc::fence_mbar_init();
+        s_fail = 0;
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&s_tmem, 512);
+        tc::fence_before_sync();
+    }
+    if (tid < AT) stab[tid] = view_row(tid);
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = s_tmem, lane_off = static_cast<uint32_t>(lg * 32) << 16;
+    const uint32_t tS = tm, tP = tm + 128, tQ = tm + 256;
+    const int qrow = lg * 32 + lane;
+    const int32_t vis = hh + q0 + qrow;
+    const int64_t grow = static_cast<int64_t>(row0) + q0 + min(qrow, nq - 1);
+    const float lse2 = p.lse[grow * H + h] * kLog2e, Dq = p.D[grow * H + h];
+
+    stage_run(p.q, static_cast<int64_t>(row0) + q0, nq, H, h, sm + Q, tid);
+    stage_run(p.dout, static_cast<int64_t>(row0) + q0, nq, H, h, sm + dO, tid);
+    stage_rows(p.k, stab, H, h, sm + K0, tid);
+    stage_rows(p.v, stab, H, h, sm + V, tid);
+    tc::cp_async_commit();
+    uint32_t nc_s = 0, nc_q = 0;
+
+    for (int32_t kt = 0; kt < n_kt; ++kt) {
+        const int b = kt & 1;
+        tc::cp_async_wait_all();
+        sync_mma();
+        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s_fail)) {
+            tc::mma_op(tS, tc::Opnd{tc::smem_addr(sm + Q), 16384, false},
+                       tc::Opnd{tc::smem_addr(sm + (b ? K1 : K0)), 16384, false}, AT, AT, AD, false);
+            tc::mma_op(tP, tc::Opnd{tc::smem_addr(sm + dO), 16384, false},
+                       tc::Opnd{tc::smem_addr(sm + V), 16384, false}, AT, AT, AD, false);
+            tc::mma_commit(&bars[0]);
+            ++nc_s;
+        }
+        // the row table of the next tile (its slot was last read before the sync above)
+        if (tid < AT) stab[((kt + 1) & 1) * AT + tid] = (kt + 1 < n_kt) ? view_row((kt + 1) * AT + tid) : -1;
+        wait_or_fail(&bars[0], kt & 1, 0, &s_fail);
+        tc::fence_after_sync();
+        float sv[32], pv[32];
+        tc::tmem_ld32(tS + lane_off + cq * 32, sv);
+        tc::tmem_ld32(tP + lane_off + cq * 32, pv);
+        if (kt > 0) wait_or_fail(&bars[1], (kt - 1) & 1, 1, &s_fail);   // dQ_{kt-1}: dS and K free
+        tc::fence_after_sync();
+        __syncthreads();                                                  // next row table visible
+        if (kt + 1 < n_kt) {
+            stage_rows(p.v, stab + ((kt + 1) & 1) * AT, H, h, sm + V, tid);
+            stage_rows(p.k, stab + ((kt + 1) & 1) * AT, H, h, sm + (b ? K0 : K1), tid);
+        }
+        tc::cp_async_commit();
+        const int32_t lim = (kt >= first_masked) ? vis - (kt * AT + cq * 32) : 1 << 30;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float pr = i <= lim ? ex2(fmaf(sv[i], c, -lse2)) : 0.f;
+            sv[i] = p.scale * pr * (pv[i] - Dq);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) tc::st_sw128_8(sm + dS, AT, qrow, cq * 32 + i, sv + i);
+        sync_mma();
+        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s_fail)) {
+            tc::mma_op(tQ, tc::Opnd{tc::smem_addr(sm + dS), 16384, false},
+                       tc::Opnd{tc::smem_addr(sm + (b ? K1 : K0)), 16384, true}, AT, AD, AT, kt > 0);
+            tc::mma_commit(&bars[1]);
+            ++nc_q;
+        }
+    }
+    wait_or_fail(&bars[1], (n_kt - 1) & 1, 1, &s_fail);
+    tc::fence_after_sync();
+    __syncthreads();
+    if (!s_fail) {
+        float r[32];
+        tc::tmem_ld32(tQ + lane_off + cq * 32, r);
+        if (qrow < nq) store_tile_bf16(p.dq + ((static_cast<int64_t>(row0) + q0 + qrow) * H + h) * AD + cq * 32, r, 1.f);
+    }
+    tc::cp_async_wait_all();
+    if (s_fail && tid == 0) {
+        dev_error(pd, kDevErrTimeout, sq, h);
+        if (nc_s) tc::mbar_wait(&bars[0], (nc_s - 1) & 1, 1000000000LL);
+        if (nc_q) tc::mbar_wait(&bars[1], (nc_q - 1) & 1, 1000000000LL);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tm, 512);
+}
+
+namespace bk_sm {
+constexpr uint32_t K = 0, V = 32768, Q0 = 65536, Q1 = 98304, dO0 = 131072, dO1 = 163840, PT = 196608;
+constexpr uint32_t Vec = 229376;                  // [128] lse, [128] D of the current query tile
+constexpr uint32_t bytes = Vec + 1024 + 1024;     // 226 KB with the alignment slack
+}  // namespace bk_sm
+
+__global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, PlanDev pd) {
+    using namespace bk_sm;
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
+    __shared__ uint64_t bars[3];                  // S^T and dP^T ready, dV done, dK done
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_fail;
+    float *slse = reinterpret_cast<float *>(sm + Vec), *sD = slse + AT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, cq = warp >> 2;
+    const int H = p.H;
+    const int32_t h = blockIdx.x % H, ki = blockIdx.x / H;
+    const int32_t sk = pd.attn_kt[2 * ki], kti = pd.attn_kt[2 * ki + 1];
+    const int32_t e0 = pd.attn_kptr[ki], n_e = pd.attn_kptr[ki + 1] - e0;
+    const int32_t k0 = kti * AT, nk = min(AT, pd.seq_nown[sk] - k0);
+    const int64_t krow0 = static_cast<int64_t>(pd.seq_row0[sk]) + k0;
+    const float c = p.scale * kLog2e;
+    // query tile of entry e: rows, count, causal offset or visible-key limit
+    auto entry = [&](int32_t e, int64_t &qrow0, int &nq, int32_t &qoff, int32_t &f) {
+        const int32_t s_ = pd.attn_kq[3 * (e0 + e)], t_ = pd.attn_kq[3 * (e0 + e) + 1];
+        f = pd.attn_kq[3 * (e0 + e) + 2];
+        qrow0 = static_cast<int64_t>(pd.seq_row0[s_]) + t_ * AT;
+        nq = min(AT, pd.seq_nown[s_] - t_ * AT);
+        qoff = t_ * AT - k0;                          // query local position minus key tile start
+    };
+    auto stage_q = [&](int32_t e, int bb) {
+        int64_t qr; int nq; int32_t qoff, f;
+        entry(e, qr, nq, qoff, f);
+        stage_run(p.q, qr, nq, H, h, sm + (bb ? Q1 : Q0), tid);
+        stage_run(p.dout, qr, nq, H, h, sm + (bb ? dO1 : dO0), tid);
+    };
+    auto stage_vec = [&](int32_t e) {
+        int64_t qr; int nq; int32_t qoff, f;
+        entry(e, qr, nq, qoff, f);
+        if (tid < AT) {
+            const bool ok = tid < nq;
+            tc::cp_async4(slse + tid, p.lse + ((qr + (ok ? tid : 0)) * H + h), ok ? 4u : 0u);
+            tc::cp_async4(sD + tid, p.D + ((qr + (ok ? tid : 0)) * H + h), ok ? 4u : 0u);
+        }
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[i], 1);
+        tc::fence_mbar_init();
+        s_fail = 0;
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&s_tmem, 512);
+        tc::fence_before_sync();
+    }
+    stage_run(p.k, krow0, nk, H, h, sm + K, tid);
+    stage_run(p.v, krow0, nk, H, h, sm + V, tid);
+    stage_q(0, 0);
+    stage_vec(0);
+    tc::cp_async_commit();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = s_tmem, lane_off = static_cast<uint32_t>(lg * 32) << 16;
+    const uint32_t tS = tm, tP = tm + 128, tV = tm + 256, tK = tm + 384;
+    const int krow = lg * 32 + lane;                 // this thread's key row (TMEM lane)
+    uint32_t nc0 = 0, nc1 = 0, nc2 = 0;             // thread 0: commits per barrier
+
+    for (int32_t e = 0; e < n_e; ++e) {
+        const int b = e & 1;
+        tc::cp_async_wait_all();
+        sync_mma();
+        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s_fail)) {
+            tc::mma_op(tS, tc::Opnd{tc::smem_addr(sm + K), 16384, false},
+                       tc::Opnd{tc::smem_addr(sm + (b ? Q1 : Q0)), 16384, false}, AT, AT, AD, false);
+            tc::mma_op(tP, tc::Opnd{tc::smem_addr(sm + V), 16384, false},
+                       tc::Opnd{tc::smem_addr(sm + (b ? dO1 : dO0)), 16384, false}, AT, AT, AD, false);
+            tc::mma_commit(&bars[0]);
+            ++nc0;
+        }
+        int64_t qr; int nq; int32_t qoff, f;
+        entry(e, qr, nq, qoff, f);
+        wait_or_fail(&bars[0], e & 1, 0, &s_fail);
+        tc::fence_after_sync();
+        float sv[32], pv[32];
+        tc::tmem_ld32(tS + lane_off + cq * 32, sv);
+        tc::tmem_ld32(tP + lane_off + cq * 32, pv);
+        if (e > 0) wait_or_fail(&bars[2], (e - 1) & 1, 2, &s_fail);      // dK_{e-1}: PT, Q, dO free
+        tc::fence_after_sync();
+        if (e + 1 < n_e) stage_q(e + 1, b ^ 1);
+        tc::cp_async_commit();
+        // P^T and dS^T for this thread's key row and 32 query columns
+        const float *lq = slse + cq * 32, *dq_ = sD + cq * 32;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int qc = cq * 32 + i;
+            const bool vis = qc < nq && (f < 0 ? krow <= qoff + qc : k0 + krow < f);
+            const float pr = vis ? ex2(fmaf(sv[i], c, -lq[i] * kLog2e)) : 0.f;
+            sv[i] = pr;
+            pv[i] = p.scale * pr * (pv[i] - dq_[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) tc::st_sw128_8(sm + PT, AT, krow, cq * 32 + i, sv + i);
+        sync_mma();
+        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s_fail)) {
+            tc::mma_op(tV, tc::Opnd{tc::smem_addr(sm + PT), 16384, false},
+                       tc::Opnd{tc::smem_addr(sm + (b ? dO1 : dO0)), 16384, true}, AT, AD, AT, e > 0);
+            tc::mma_commit(&bars[1]);
+            ++nc1;
+        }
+        if (e + 1 < n_e) stage_vec(e + 1);              // every thread has read this tile's lse, D
+        tc::cp_async_commit();
+        wait_or_fail(&bars[1], e & 1, 1, &s_fail);
+        tc::fence_after_sync();
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) tc::st_sw128_8(sm + PT, AT, krow, cq * 32 + i, pv + i);
+        sync_mma();
+        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s_fail)) {
+            tc::mma_op(tK, tc::Opnd{tc::smem_addr(sm + PT), 16384, false},
+                       tc::Opnd{tc::smem_addr(sm + (b ? Q1 : Q0)), 16384, true}, AT, AD, AT, e > 0);
+            tc::mma_commit(&bars[2]);
+            ++nc2;
+        }
+    }
+    wait_or_fail(&bars[2], (n_e - 1) & 1, 2, &s_fail);
+    tc::fence_after_sync();
+    __syncthreads();
+    if (!s_fail) {                                    // warp-collective loads, guarded stores
+        float r[32];
+        tc::tmem_ld32(tV + lane_off + cq * 32, r);
+        if (krow < nk) store_tile_bf16(p.dv + ((krow0 + krow) * H + h) * AD + cq * 32, r, 1.f);
+        tc::tmem_ld32(tK + lane_off + cq * 32, r);
+        if (krow < nk) store_tile_bf16(p.dk + ((krow0 + krow) * H + h) * AD + cq * 32, r, 1.f);
+    }
+    tc::cp_async_wait_all();
+    if (s_fail && tid == 0) {
+        dev_error(pd, kDevErrTimeout, sk, h);
+        const uint32_t nc[3] = {nc0, nc1, nc2};
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            if (nc[i]) tc::mbar_wait(&bars[i], (nc[i] - 1) & 1, 1000000000LL);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tm, 512);
+}
+
 }  // namespace
 }  // namespace harts
 
 using namespace harts;
 
-extern "C" {
-
-int harts_attn_fwd(const harts_plan *P, const harts_attn_fwd_args *a, harts_stream_t stream) {
+static int check_attn(const harts_plan *P, const harts_attn_fwd_args *a) {
     if (!P || !a) { set_error("NULL plan or args"); return HARTS_EINVAL; }
     if (!P->attn_ok) { set_error("plan too deep for the branch-attention tables"); return HARTS_EOVERFLOW; }
     if (a->dtype != HARTS_BF16 || a->d != AD) { set_error("branch attention: bf16 and d = 128 only"); return HARTS_EUNSUPPORTED; }
@@ -305,8 +647,25 @@ int harts_attn_fwd(const harts_plan *P, const harts_attn_fwd_args *a, harts_stre
         set_error("q, k, v and o must be 16-byte aligned"); return HARTS_EINVAL;
     }
     if (!P->dev) { set_error("plan not uploaded (harts_plan_upload)"); return HARTS_ENOPLAN; }
+    if (int64_t(P->image.n_qt) * a->H > 0x7fffffff || int64_t(P->image.n_kt) * a->H > 0x7fffffff) {
+        set_error("too many (tile, head) blocks"); return HARTS_EOVERFLOW;
+    }
+    return HARTS_OK;
+}
+
+template <typename K, typename Prm>
+static cudaError_t launch_big(K kernel, unsigned blocks, uint32_t smem, cudaStream_t st, const Prm &p, const PlanDev &pd) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kernel<<<blocks, ANT, smem, st>>>(p, pd);
+    return cudaGetLastError();
+}
+
+extern "C" {
+
+int harts_attn_fwd(const harts_plan *P, const harts_attn_fwd_args *a, harts_stream_t stream) {
+    if (int rc = check_attn(P, a)) return rc;
     const int64_t blocks = int64_t(P->image.n_qt) * a->H;
-    if (blocks > 0x7fffffff) { set_error("too many (query tile, head) blocks"); return HARTS_EOVERFLOW; }
     if (blocks == 0) { set_error(""); return HARTS_OK; }
     AttnParams p;
     p.q = static_cast<const __nv_bfloat16 *>(a->q);
@@ -316,14 +675,54 @@ int harts_attn_fwd(const harts_plan *P, const harts_attn_fwd_args *a, harts_stre
     p.lse = a->lse;
     p.H = a->H;
     p.scale = a->scale;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(at_sm::bytes));
-    if (e == cudaSuccess) {
-        attn_fwd_tc<<<static_cast<unsigned>(blocks), ANT, at_sm::bytes, st>>>(p, P->view);
-        e = cudaGetLastError();
-    }
+    const cudaError_t e = launch_big(attn_fwd_tc, static_cast<unsigned>(blocks), at_sm::bytes,
+                                     reinterpret_cast<cudaStream_t>(stream), p, P->view);
     if (e != cudaSuccess) { set_error(std::string("attention launch: ") + cudaGetErrorString(e)); return HARTS_ECUDA; }
+    set_error("");
+    return HARTS_OK;
+}
+
+size_t harts_attn_bwd_workspace_bytes(const harts_plan *P, int32_t H) {
+    if (!P || H < 1) return 0;
+    return static_cast<size_t>((P->info.C * H * 4 + 255) / 256 * 256);
+}
+
+int harts_attn_bwd(const harts_plan *P, const harts_attn_bwd_args *a, harts_stream_t stream) {
+    if (!a) { set_error("NULL args"); return HARTS_EINVAL; }
+    if (int rc = check_attn(P, &a->fwd)) return rc;
+    if (!a->fwd.lse || !a->d_o || !a->dq || !a->dk || !a->dv) { set_error("NULL lse, d_o, dq, dk or dv"); return HARTS_EINVAL; }
+    if ((reinterpret_cast<uintptr_t>(a->d_o) | reinterpret_cast<uintptr_t>(a->dq) | reinterpret_cast<uintptr_t>(a->dk) |
+         reinterpret_cast<uintptr_t>(a->dv) | reinterpret_cast<uintptr_t>(a->fwd.lse) |
+         reinterpret_cast<uintptr_t>(a->workspace)) & 15) {
+        set_error("d_o, dq, dk, dv, lse and workspace must be 16-byte aligned"); return HARTS_EINVAL;
+    }
+    const size_t need = harts_attn_bwd_workspace_bytes(P, a->fwd.H);
+    if (!a->workspace || a->workspace_bytes < need) { set_error("workspace smaller than harts_attn_bwd_workspace_bytes"); return HARTS_ESMALLBUF; }
+    const int64_t rows = P->info.C * a->fwd.H;
+    if (rows == 0) { set_error(""); return HARTS_OK; }
+    AttnBwdParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(a->fwd.q);
+    p.k = static_cast<const __nv_bfloat16 *>(a->fwd.k);
+    p.v = static_cast<const __nv_bfloat16 *>(a->fwd.v);
+    p.dout = static_cast<const __nv_bfloat16 *>(a->d_o);
+    p.lse = a->fwd.lse;
+    float *D = static_cast<float *>(a->workspace);
+    p.D = D;
+    p.dq = static_cast<__nv_bfloat16 *>(a->dq);
+    p.dk = static_cast<__nv_bfloat16 *>(a->dk);
+    p.dv = static_cast<__nv_bfloat16 *>(a->dv);
+    p.H = a->fwd.H;
+    p.scale = a->fwd.scale;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t prep_blocks = std::min<int64_t>((rows * 32 + 255) / 256, 152 * 16);
+    attn_bwd_prep<<<static_cast<unsigned>(prep_blocks), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(a->fwd.o), p.dout, D, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = launch_big(attn_bwd_dq_tc, static_cast<unsigned>(int64_t(P->image.n_qt) * p.H), bq_sm::bytes, st, p, P->view);
+    if (e == cudaSuccess)
+        e = launch_big(attn_bwd_dkdv_tc, static_cast<unsigned>(int64_t(P->image.n_kt) * p.H), bk_sm::bytes, st, p, P->view);
+    if (e != cudaSuccess) { set_error(std::string("attention backward launch: ") + cudaGetErrorString(e)); return HARTS_ECUDA; }
     set_error("");
     return HARTS_OK;
 }

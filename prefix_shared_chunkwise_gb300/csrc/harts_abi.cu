@@ -117,7 +117,8 @@ int harts_plan_upload(harts_plan *P, void *dev_buf, size_t bytes, harts_stream_t
     v.conv_ctx = w + I.off_conv_ctx; v.conv_sptr = w + I.off_conv_sptr; v.conv_succ = w + I.off_conv_succ;
     v.n_seg = P->info.n_seg;
     v.attn_hptr = w + I.off_attn_hptr; v.attn_hrows = w + I.off_attn_hrows; v.attn_qt = w + I.off_attn_qt;
-    v.n_qt = I.n_qt;
+    v.attn_kt = w + I.off_attn_kt; v.attn_kptr = w + I.off_attn_kptr; v.attn_kq = w + I.off_attn_kq;
+    v.n_qt = I.n_qt; v.n_kt = I.n_kt;
     v.n_rounds = P->info.n_rounds; v.n_seq = P->info.n_seq; v.n_states = P->info.n_states;
     v.n_roots = P->info.n_roots; v.n_fold = P->info.n_fold_rows; v.chunk = P->info.chunk;
     v.R = P->info.R; v.n_chunks = P->info.n_chunks; v.C = P->info.C; v.flags = P->info.flags;

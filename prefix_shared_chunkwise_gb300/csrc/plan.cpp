@@ -14,6 +14,7 @@
 // bottom-up pass keeping the largest and second-largest child T_pre, one top-down
 // pass assigning rounds as early as possible.
 #include <algorithm>
+#include <array>
 #include <cstring>
 #include <new>
 
@@ -428,6 +429,75 @@ void build_image(harts_plan &P) {
     put(I.off_attn_hptr, hptr.data(), hptr.size());
     put(I.off_attn_hrows, hrows.data(), hrows.size());
     put(I.off_attn_qt, qt.data(), qt.size());
+
+    // Key tiles for the key / value gradients: kAttnTile own rows of a sequence.  The
+    // query tiles that see key tile (s, i): the sequence's own tiles from i on (causal),
+    // and every query tile of every sequence whose prefix runs through s, with the number
+    // f of s's own rows in that prefix (keys at local position < f visible, i < ceil(f/B)).
+    // Each key tile's list is in ascending (sequence, tile) order; key tiles are grouped
+    // by tree like the query tiles, then by decreasing work (query rows to visit).
+    std::vector<int32_t> kbase(n_seq + 1, 0);
+    for (int32_t i = 0; i < n_seq; ++i) {
+        const int64_t own = P.cu_seqlens[i + 1] - P.cu_seqlens[i];
+        kbase[i + 1] = kbase[i] + static_cast<int32_t>((own + kAttnTile - 1) / kAttnTile);
+    }
+    const int32_t n_ktile = P.attn_ok ? kbase[n_seq] : 0;
+    std::vector<std::vector<int32_t>> klist(n_ktile);   // (sequence, tile, f) triples
+    std::vector<int64_t> kwork(n_ktile, 0);
+    for (int32_t t = 0; t < n_seq && P.attn_ok; ++t) {
+        const int64_t own_t = P.cu_seqlens[t + 1] - P.cu_seqlens[t];
+        const int32_t nqt_t = static_cast<int32_t>((own_t + kAttnTile - 1) / kAttnTile);
+        auto add = [&](int32_t kt, int32_t tile, int32_t f) {
+            klist[kt].insert(klist[kt].end(), {t, tile, f});
+            kwork[kt] += std::min<int64_t>(kAttnTile, own_t - int64_t(tile) * kAttnTile);
+        };
+        for (int32_t u = P.parent[P.seq_first_seg[t]]; u >= 0;) {
+            const int32_t s_ = P.seg_seq[u];
+            const int64_t f = P.seg_pos[u] + P.seg_len[u] - P.seg_pos[P.seq_first_seg[s_]];
+            for (int32_t i = 0; int64_t(i) * kAttnTile < f; ++i)
+                for (int32_t qt2 = 0; qt2 < nqt_t; ++qt2) add(kbase[s_] + i, qt2, static_cast<int32_t>(f));
+            u = P.parent[P.seq_first_seg[s_]];
+        }
+        for (int32_t i = 0; i < nqt_t; ++i)
+            for (int32_t qt2 = i; qt2 < nqt_t; ++qt2) add(kbase[t] + i, qt2, -1);
+    }
+    // lists were appended by ascending query sequence t, ancestors before its own tiles;
+    // sort each into ascending (sequence, tile) so the order is a documented one
+    for (auto &l : klist) {
+        const size_t n = l.size() / 3;
+        std::vector<std::array<int32_t, 3>> e(n);
+        for (size_t j = 0; j < n; ++j) e[j] = {l[3 * j], l[3 * j + 1], l[3 * j + 2]};
+        std::sort(e.begin(), e.end());
+        for (size_t j = 0; j < n; ++j) { l[3 * j] = e[j][0]; l[3 * j + 1] = e[j][1]; l[3 * j + 2] = e[j][2]; }
+    }
+    struct KTile { int64_t work; int32_t tree, seq, tile; };
+    std::vector<KTile> kts;
+    std::vector<int64_t> ktree_work(P.parent.size(), 0);
+    for (int32_t i = 0; i < n_seq && P.attn_ok; ++i) {
+        const int32_t r = root[P.seq_first_seg[i]];
+        for (int32_t j = kbase[i]; j < kbase[i + 1]; ++j) {
+            kts.push_back({kwork[j], r, i, j - kbase[i]});
+            ktree_work[r] = std::max(ktree_work[r], kwork[j]);
+        }
+    }
+    std::stable_sort(kts.begin(), kts.end(), [&](const KTile &a, const KTile &b) {
+        if (a.tree != b.tree) {
+            if (ktree_work[a.tree] != ktree_work[b.tree]) return ktree_work[a.tree] > ktree_work[b.tree];
+            return a.tree < b.tree;
+        }
+        return a.work > b.work;
+    });
+    std::vector<int32_t> akt(2 * kts.size()), akptr(kts.size() + 1, 0), kq;
+    for (size_t j = 0; j < kts.size(); ++j) {
+        akt[2 * j] = kts[j].seq; akt[2 * j + 1] = kts[j].tile;
+        const auto &l = klist[kbase[kts[j].seq] + kts[j].tile];
+        kq.insert(kq.end(), l.begin(), l.end());
+        akptr[j + 1] = static_cast<int32_t>(kq.size() / 3);
+    }
+    I.n_kt = static_cast<int32_t>(kts.size());
+    put(I.off_attn_kt, akt.data(), akt.size());
+    put(I.off_attn_kptr, akptr.data(), akptr.size());
+    put(I.off_attn_kq, kq.data(), kq.size());
     while (w.size() % 64) w.push_back(0);
 }
 

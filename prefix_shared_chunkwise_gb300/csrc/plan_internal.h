@@ -44,8 +44,11 @@ struct PlanDev {
     // branch attention: each sequence's ancestor prefix, and the query tiles
     const int32_t *attn_hptr;      // [n_seq+1] ancestor rows of sequence i: attn_hrows[attn_hptr[i] ..]
     const int32_t *attn_hrows;     // compact rows of the trajectory positions before the sequence
-    const int32_t *attn_qt;        // [n_qt][2] (sequence, query tile), most work first
-    int32_t n_qt;
+    const int32_t *attn_qt;        // [n_qt][2] (sequence, query tile), tree by tree
+    const int32_t *attn_kt;        // [n_kt][2] (sequence, key tile of its own rows), tree by tree
+    const int32_t *attn_kptr;      // [n_kt+1] query tiles of key tile j: attn_kq[3 * kptr[j] ..]
+    const int32_t *attn_kq;        // (sequence, query tile, f): f own rows of the key's sequence visible, -1 causal
+    int32_t n_qt, n_kt;
     int32_t n_rounds, n_seq, n_states, n_roots, n_fold, chunk, n_seg;
     uint32_t flags;                // harts_plan_calls flags (HARTS_PLAN_NOREPLAY: slots inside chunks)
     int64_t R, n_chunks, C;
@@ -59,8 +62,8 @@ struct PlanImage {
         off_state_cptr, off_state_cons, off_root_cptr, off_root_cons, off_replay_idx,
         off_fold_rows, off_fold_ptr, off_fold_occ, off_chunk_seq, off_row_seg, off_seg_row0,
         off_seg_len, off_conv_ctx, off_conv_sptr, off_conv_succ, off_attn_hptr, off_attn_hrows,
-        off_attn_qt;
-    int32_t n_qt;
+        off_attn_qt, off_attn_kt, off_attn_kptr, off_attn_kq;
+    int32_t n_qt, n_kt;
 };
 
 void set_error(const std::string &msg);

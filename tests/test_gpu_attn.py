@@ -109,3 +109,75 @@ def test_full_size_sampled_rows():
                                       v[idx].double().cpu().numpy(), 128 ** -0.5)
         assert rel_l2(o[int(r)].float().cpu().numpy(), ref_o) <= O_TOL
         assert rel_l2(lse[int(r)].cpu().numpy(), ref_l) <= LSE_TOL
+
+
+# ---- backward -------------------------------------------------------------------------
+
+def _check_bwd(parent, seg_len, H, seed, nodewise=False, qscale=1.0):
+    from prefix_shared_chunkwise_gb300.api import attn_bwd
+    pl = Plan(parent, seg_len, 64, nodewise=nodewise)
+    pl.upload()
+    C = pl.info["C"]
+    q, k, v = _inputs(C, H, seed, qscale)
+    g = torch.Generator().manual_seed(seed + 100)
+    do = torch.randn((C, H, 128), generator=g).to(torch.bfloat16)
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = attn_fwd(pl, qc, kc, vc)
+    dq, dk, dv = attn_bwd(pl, qc, kc, vc, o, lse, doc)
+    assert pl.device_error() == 0
+    ref = oat.attn_forest_bwd(np.asarray(parent), np.asarray(seg_len), pl.arrays()["seg_offset"],
+                              q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                              do.double().numpy(), 128 ** -0.5)
+    errs = {n: rel_l2(t.float().cpu().numpy(), ref[n]) for n, t in (("dq", dq), ("dk", dk), ("dv", dv))}
+    assert max(errs.values()) <= O_TOL, errs
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_bwd_random_forest_ragged_tiles(seed):
+    parent, seg_len = _random_forest(seed, 14, 300)
+    _check_bwd(parent, seg_len, 2, seed)
+
+
+def test_bwd_deep_prefix_and_single_tokens():
+    parent = np.array([-1, 0, 1, 0, 1, 2, 2], np.int32)
+    seg_len = np.array([333, 200, 70, 129, 1, 257, 128], np.int64)
+    _check_bwd(parent, seg_len, 2, 21)
+    parent, seg_len = _random_forest(7, 40, 3)
+    _check_bwd(parent, seg_len, 1, 22)
+
+
+def test_bwd_nodewise_and_sharp_scores():
+    parent, seg_len = _random_forest(8, 12, 200)
+    _check_bwd(parent, seg_len, 2, 23, nodewise=True)
+    parent, seg_len = _random_forest(9, 6, 400)
+    _check_bwd(parent, seg_len, 2, 24, qscale=6.0)
+
+
+def test_bwd_full_size_sampled_rows_and_sum_rules():
+    """The 64K-token forest at H = 16: dq of sampled rows against the oracle on each row's
+    trajectory prefix; over all rows, sum dv = sum d_o (each query's probabilities sum to
+    one) and sum dk = 0 (each query's dS sums to zero), per head and channel."""
+    from prefix_shared_chunkwise_gb300.api import attn_bwd
+    parent, seg_len = make_tree("fb64k_bf16")
+    pl = Plan(parent, seg_len, 64)
+    pl.upload()
+    C, H = pl.info["C"], 16
+    g = torch.Generator(device="cuda").manual_seed(7)
+    q, k, v, do = (torch.randn((C, H, 128), generator=g, device="cuda").to(torch.bfloat16) for _ in range(4))
+    o, lse = attn_fwd(pl, q, k, v)
+    dq, dk, dv = attn_bwd(pl, q, k, v, o, lse, do)
+    assert pl.device_error() == 0
+    so = pl.arrays()["seg_offset"]
+    rng = np.random.default_rng(8)
+    for r in np.unique(np.concatenate([[0, C - 1], rng.integers(0, C, size=8)])):
+        view = oat.trajectory_prefix(parent, seg_len, so, int(r))
+        idx = torch.as_tensor(view, device="cuda")
+        ref_dq, _, _ = oat.attn_query_bwd(q[int(r)].double().cpu().numpy(), k[idx].double().cpu().numpy(),
+                                          v[idx].double().cpu().numpy(), do[int(r)].double().cpu().numpy(),
+                                          128 ** -0.5)
+        assert rel_l2(dq[int(r)].float().cpu().numpy(), ref_dq) <= O_TOL
+    sdv, sdo = dv.double().sum(0), do.double().sum(0)
+    e_dv = float((sdv - sdo).norm() / sdo.norm())
+    sdk, adk = dk.double().sum(0), dk.double().abs().sum(0)
+    e_dk = float(sdk.norm() / adk.norm())
+    assert e_dv <= 1e-2 and e_dk <= 1e-3, (e_dv, e_dk)

@@ -200,3 +200,15 @@ def test_attention_tables_bounded_for_deep_combs():
         return Plan(parent, seg_len, 64)
     assert _attn_call(comb(2000, 100)) == -3
     assert _attn_call(comb(200, 100)) == -8
+
+
+def test_attention_backward_workspace_and_checks():
+    pl = Plan(np.array([-1, 0, 0], np.int32), np.array([5, 3, 4], np.int64), 64)
+    assert _lib.lib().harts_attn_bwd_workspace_bytes(pl.handle, 3) == 256      # 12 rows x 3 heads x 4 B, rounded
+    assert _lib.lib().harts_attn_bwd_workspace_bytes(pl.handle, 0) == 0
+    b = _lib.AttnBwdArgs()
+    b.fwd.H, b.fwd.d, b.fwd.dtype, b.fwd.scale = 2, 128, _lib.HARTS_BF16, 0.1
+    b.fwd.q = b.fwd.k = b.fwd.v = b.fwd.o = 0x10000
+    assert _lib.lib().harts_attn_bwd(pl.handle, ctypes.byref(b), None) == -8   # not uploaded
+    b.fwd.d = 64
+    assert _lib.lib().harts_attn_bwd(pl.handle, ctypes.byref(b), None) == -2
