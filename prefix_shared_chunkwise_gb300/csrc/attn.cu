@@ -9,21 +9,22 @@
 //
 // One block per (sequence, 128-query tile, head); the planner orders the tiles tree by
 // tree (longest first within a tree) with the heads innermost, so the key / value rows a
-// tree's blocks share stay in L2.  Per key tile j of 128 view rows:
-//   S_j = Q K_j^T           tcgen05, M = N = 128, K = d, fp32 in one of two TMEM buffers;
-//                           S_{j+1} is issued as soon as S_j is ready, so the tensor core
-//                           works while the warps run the softmax of tile j
-//   softmax                 sixteen warps, one query row and 32 columns each; scores in
-//                           base-2 units (scale * log2 e folded into one FMA); the four
-//                           warps holding a row exchange its max through shared memory; the
-//                           running max moves (and O is rescaled in TMEM) only when a row's
-//                           max grows by more than 2^8 -- any common offset gives the same
-//                           softmax, the threshold only bounds P by 256
-//   O += P V_j              tcgen05, P bf16 in shared memory, V read MN-major
-// Keys and values are gathered by cp.async through a four-tile ring of row tables, K two
-// tiles and V one tile ahead.  Masking runs only on tiles that reach past the first
-// query's causal limit.  Every wait is bounded; a timeout records code 3 in the plan's
-// error word, stops issuing products and drains the ones in flight.
+// tree's blocks share stay in L2.  The block's warps have fixed roles and meet only at
+// mbarriers (every wait bounded):
+//   loaders (4 warps)   gather Q, then K_j and V_j of each 128-row key tile by cp.async
+//                       into two-slot K and V rings; a slot is refilled once the product
+//                       that reads it has completed (K after S_j, V after O_j)
+//   MMA (one thread)    S_j = Q K_j^T (tcgen05, fp32 in one of two TMEM buffers), issued a
+//                       tile ahead of O_{j-1} += P_{j-1} V_{j-1} (V read MN-major)
+//   softmax (8 warps)   one query row and 64 columns per thread; scores in base-2 units
+//                       (scale * log2 e folded into one FMA); the two warps holding a row
+//                       exchange its max through shared memory; the running max moves,
+//                       and O is rescaled in TMEM, only when a row max grows by more than
+//                       2^8 -- any common offset gives the same softmax, the threshold
+//                       only bounds P by 256; P goes to shared memory as bf16
+// Masking runs only on tiles that reach past the first query's causal limit.  A timeout
+// records code 3 in the plan's error word, stops issuing products and drains the ones
+// in flight.
 #include <algorithm>
 #include <cstring>
 
@@ -33,17 +34,21 @@
 namespace harts {
 namespace {
 
-constexpr int AD = 128, AT = kAttnTile, ANT = 512, NQ = ANT / AT;   // NQ column quarters
+constexpr int AD = 128, AT = kAttnTile, ANT = 512;   // ANT: threads of the backward kernels
 constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;               // running max moves when a row max grows by more
 
 namespace at_sm {
 constexpr uint32_t Q = 0, K0 = 32768, K1 = 65536, V0 = 98304, V1 = 131072, P = 163840;
-constexpr uint32_t Max = 196608;                  // [2 tiles][4 quarters][128] fp32 row maxima
-constexpr uint32_t Sum = Max + 4096;              // [4 quarters][128] fp32 row sums
-constexpr uint32_t Tab = Sum + 2048;              // [4][128] int32 view rows of tiles j % 4
-constexpr uint32_t bytes = Tab + 2048 + 1024;     // + alignment slack
+constexpr uint32_t Max = 196608;                  // [2 tiles][2 halves][128] fp32 row maxima
+constexpr uint32_t Sum = Max + 2048;              // [2 halves][128] fp32 row sums
+constexpr uint32_t bytes = Sum + 1024 + 1024;     // + alignment slack
 }  // namespace at_sm
+
+// Roles of the forward's 13 warps.
+constexpr int kFwdSoftmaxWarps = 8, kFwdMmaWarp = 8, kFwdLoadWarp0 = 9, kFwdLoadWarps = 4;
+constexpr int kFwdThreads = (kFwdLoadWarp0 + kFwdLoadWarps) * 32;
+constexpr int kLoadThreads = kFwdLoadWarps * 32, kSoftThreads = kFwdSoftmaxWarps * 32;
 
 struct AttnParams {
     const __nv_bfloat16 *q, *k, *v;
@@ -76,22 +81,29 @@ __device__ __forceinline__ void sync_mma() {
     tc::fence_after_sync();
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(tc::smem_addr(bar)) : "memory");
+}
+
 // Waits unless the block has already failed; a timeout records 1 + 2 * which + phase.
 __device__ __forceinline__ void wait_or_fail(uint64_t *bar, uint32_t phase, int which, int *s_fail) {
     if (*reinterpret_cast<volatile int *>(s_fail)) return;
     if (!tc::mbar_wait(bar, phase)) atomicCAS(s_fail, 0, 1 + 2 * which + static_cast<int>(phase));
 }
 
-__global__ void __launch_bounds__(ANT, 1) attn_fwd_tc(AttnParams p, PlanDev pd) {
+__device__ __forceinline__ bool failed(int *s_fail) { return *reinterpret_cast<volatile int *>(s_fail) != 0; }
+
+// Barriers of the forward (index into bars[]).
+enum FwdBar { bQ = 0, bKF = 1, bKE = 3, bVF = 5, bVE = 7, bSF = 9, bSE = 11, bPF = 13, bOD = 14, bN = 15 };
+
+__global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, PlanDev pd) {
     using namespace at_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    __shared__ uint64_t bars[3];                  // S buffer 0, S buffer 1, O
+    __shared__ uint64_t bars[bN];
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
-    float *smax = reinterpret_cast<float *>(sm + Max), *ssum = reinterpret_cast<float *>(sm + Sum);
-    int32_t *stab = reinterpret_cast<int32_t *>(sm + Tab);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, cq = warp >> 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
     const int32_t h = blockIdx.x % H, qi = blockIdx.x / H;
     const int32_t sq = pd.attn_qt[2 * qi], qt = pd.attn_qt[2 * qi + 1];
@@ -99,194 +111,229 @@ __global__ void __launch_bounds__(ANT, 1) attn_fwd_tc(AttnParams p, PlanDev pd) 
     const int32_t row0 = pd.seq_row0[sq], own = pd.seq_nown[sq], nview = hh + own;
     const int32_t q0 = qt * AT, nq = min(AT, own - q0);
     const int32_t n_kt = (hh + q0 + nq - 1) / AT + 1;   // key tiles covering every visible entry
-    const int32_t first_masked = (hh + q0) / AT;        // tiles from here reach past a causal limit
-    const float c = p.scale * kLog2e;
-
-    // compact row of view entry j (-1 past the view)
-    auto view_row = [&](int32_t j) -> int32_t {
-        return j < hh ? pd.attn_hrows[hb + j] : (j < nview ? row0 + (j - hh) : -1);
-    };
-    // 128 rows of K or V for tile `kt` from ring slot kt % 4 into `dst`
-    auto stage = [&](const __nv_bfloat16 *src, int32_t kt, uint8_t *dst) {
-        const int32_t *tab = stab + (kt & 3) * AT;
-#pragma unroll
-        for (int i = 0; i < AT * 16 / ANT; ++i) {
-            const int e = tid + i * ANT, r = e >> 4, pc = e & 15;
-            const int32_t row = tab[r];
-            const __nv_bfloat16 *g = src + (static_cast<int64_t>(row < 0 ? 0 : row) * H + h) * AD + pc * 8;
-            tc::cp_async16(dst + piece(r, pc), g, row >= 0 ? 16u : 0u);
-        }
-    };
 
     if (tid == 0) {
-        for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[i], 1);
+        tc::mbar_init(&bars[bQ], kLoadThreads);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&bars[bKF + i], kLoadThreads);
+            tc::mbar_init(&bars[bVF + i], kLoadThreads);
+            tc::mbar_init(&bars[bKE + i], 1);
+            tc::mbar_init(&bars[bVE + i], 1);
+            tc::mbar_init(&bars[bSF + i], 1);
+            tc::mbar_init(&bars[bSE + i], kSoftThreads);
+        }
+        tc::mbar_init(&bars[bPF], kSoftThreads);
+        tc::mbar_init(&bars[bOD], 1);
         tc::fence_mbar_init();
         s_fail = 0;
     }
-    if (warp == 0) {
+    if (warp == kFwdMmaWarp) {
         tc::tmem_alloc(&s_tmem, 512);
         tc::fence_before_sync();
     }
-    if (tid < AT) {
-#pragma unroll
-        for (int j = 0; j < 3; ++j) stab[j * AT + tid] = j * AT + tid < (n_kt * AT) ? view_row(j * AT + tid) : -1;
-    }
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tm = s_tmem, lane_off = static_cast<uint32_t>(lg * 32) << 16;
-    const uint32_t tO = tm + 256;
-    const int qrow = lg * 32 + lane;                    // this thread's query row (TMEM lane)
-    const int32_t vis = hh + q0 + qrow;                 // last view entry it sees
+    const uint32_t tm = s_tmem, tO = tm + 256;
 
-    // group 0: Q, K_0, V_0; group 1: K_1; group 2: empty (stands for "V_0" in the steady state)
-#pragma unroll
-    for (int i = 0; i < AT * 16 / ANT; ++i) {
-        const int e = tid + i * ANT, r = e >> 4, pc = e & 15;
-        const bool ok = r < nq;
-        const __nv_bfloat16 *g = p.q + ((static_cast<int64_t>(row0) + q0 + (ok ? r : 0)) * H + h) * AD + pc * 8;
-        tc::cp_async16(sm + Q + piece(r, pc), g, ok ? 16u : 0u);
-    }
-    stage(p.k, 0, sm + K0);
-    stage(p.v, 0, sm + V0);
-    tc::cp_async_commit();
-    if (n_kt > 1) stage(p.k, 1, sm + K1);
-    tc::cp_async_commit();
-    tc::cp_async_commit();
-    cp_wait_group<2>();
-    sync_mma();
-    uint32_t nc_s0 = 0, nc_s1 = 0, nc_o = 0;            // thread 0: commits per barrier
-    if (tid == 0) {
-        tc::mma_op(tm, tc::Opnd{tc::smem_addr(sm + Q), 16384, false}, tc::Opnd{tc::smem_addr(sm + K0), 16384, false},
-                   AT, AT, AD, false);
-        tc::mma_commit(&bars[0]);
-        nc_s0 = 1;
-    }
-
-    float m_run = -INFINITY, l_part = 0.f;
-    for (int32_t kt = 0; kt < n_kt; ++kt) {
-        const int b = kt & 1;
-        // A: S_kt ready; K_{kt+1} in shared memory
-        cp_wait_group<1>();
-        tc::fence_smem_to_async();
-        wait_or_fail(&bars[b], (kt >> 1) & 1, b, &s_fail);
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-        const bool failed = *reinterpret_cast<volatile int *>(&s_fail) != 0;
-        // B: S_{kt+1} into the other buffer
-        if (tid == 0 && kt + 1 < n_kt && !failed) {
-            tc::mma_op(tm + (b ^ 1) * 128, tc::Opnd{tc::smem_addr(sm + Q), 16384, false},
-                       tc::Opnd{tc::smem_addr(sm + (b ? K0 : K1)), 16384, false}, AT, AT, AD, false);
-            tc::mma_commit(&bars[b ^ 1]);
-            if (b) ++nc_s0; else ++nc_s1;
+    if (warp >= kFwdLoadWarp0) {
+        // ---- loaders: Q, then K_0, V_0, K_1, V_1, ...; a group's full barrier is
+        // arrived on once the next group is in flight (at most two groups per thread)
+        const int lt = tid - kFwdLoadWarp0 * 32, pc = lt & 15, r0 = lt >> 4;
+        uint64_t *pending = nullptr;
+        auto finish_prev = [&](uint64_t *next) {
+            cp_wait_group<1>();
+            tc::fence_smem_to_async();
+            if (pending) mbar_arrive(pending);
+            pending = next;
+        };
+        for (int i = 0; i < AT / 8; ++i) {
+            const int r = r0 + 8 * i;
+            const bool ok = r < nq;
+            const __nv_bfloat16 *g = p.q + ((static_cast<int64_t>(row0) + q0 + (ok ? r : 0)) * H + h) * AD + pc * 8;
+            tc::cp_async16(sm + Q + piece(r, pc), g, ok ? 16u : 0u);
         }
-        // C: K_{kt+2} into this tile's K buffer (S_kt has consumed it); row table of tile kt+3
-        if (kt + 2 < n_kt) stage(p.k, kt + 2, sm + (b ? K1 : K0));
         tc::cp_async_commit();
-        int32_t nxt = -1;
-        if (tid < AT && (kt + 3) * AT + tid < n_kt * AT) nxt = view_row((kt + 3) * AT + tid);
-        // D: scores, mask, row max of this half
-        float s[32];
-        tc::tmem_ld32(tm + b * 128 + lane_off + cq * 32, s);
-        if (kt >= first_masked) {
-            const int32_t lim = vis - (kt * AT + cq * 32);
+        finish_prev(&bars[bQ]);
+        for (int32_t kt = 0; kt < n_kt; ++kt) {
+            const int b = kt & 1;
+            int32_t rows[AT / 8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) s[i] = i <= lim ? s[i] : -INFINITY;
-        }
-        float mp[8];
+            for (int i = 0; i < AT / 8; ++i) {
+                const int32_t j = kt * AT + r0 + 8 * i;
+                rows[i] = j < hh ? pd.attn_hrows[hb + j] : (j < nview ? row0 + (j - hh) : -1);
+            }
+            for (int t = 0; t < 2; ++t) {                 // t = 0: K, 1: V
+                if (kt >= 2) wait_or_fail(&bars[(t ? bVE : bKE) + b], ((kt - 2) >> 1) & 1, 2, &s_fail);
+                uint8_t *dst = sm + (t ? (b ? V1 : V0) : (b ? K1 : K0));
+                const __nv_bfloat16 *src = t ? p.v : p.k;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mp[i] = fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24]));
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-            for (int i = 0; i < w; ++i) mp[i] = fmaxf(mp[i], mp[i + w]);
-        smax[(b * NQ + cq) * AT + qrow] = mp[0];
-        // the four warps holding these rows exchange their maxima (named barrier 1 + lg)
-        asm volatile("bar.sync %0, %1;" :: "r"(1 + lg), "n"(NQ * 32) : "memory");
-        // F: running max (moves only past the threshold), probabilities, row sum of this quarter
-        const float *mrow = smax + b * NQ * AT + qrow;
-        const float m_tile = c * fmaxf(fmaxf(mrow[0], mrow[AT]), fmaxf(mrow[2 * AT], mrow[3 * AT]));
-        const bool move = __any_sync(0xffffffffu, m_tile > m_run + kRescaleLog2);
-        float alpha = 1.f;
-        if (move) {
-            const float m_new = fmaxf(m_run, m_tile);
-            alpha = ex2(m_run - m_new);
-            m_run = m_new;
-        }
-        float sp[8];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            s[i] = ex2(fmaf(s[i], c, -m_run));
-            sp[i & 7] = (i < 8) ? s[i] : sp[i & 7] + s[i];
-        }
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-            for (int i = 0; i < w; ++i) sp[i] += sp[i + w];
-        l_part = l_part * alpha + sp[0];
-        // G: O_{kt-1} done (P buffer and O free); P, rescale of O, V_{kt+1}
-        if (kt > 0) wait_or_fail(&bars[2], (kt - 1) & 1, 2, &s_fail);
-        tc::fence_after_sync();
-#pragma unroll
-        for (int i = 0; i < 32; i += 8) tc::st_sw128_8(sm + P, AT, qrow, cq * 32 + i, s + i);
-        if (move && kt > 0) {
-            float r[32];
-            tc::tmem_ld32(tO + lane_off + cq * 32, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] *= alpha;
-            tc::tmem_st32(tO + lane_off + cq * 32, r);
-        }
-        if (kt + 1 < n_kt) stage(p.v, kt + 1, sm + (b ? V0 : V1));
-        tc::cp_async_commit();
-        cp_wait_group<2>();                             // V_kt has landed
-        if (tid < AT) stab[((kt + 3) & 3) * AT + tid] = nxt;
-        // H: O += P V_kt
-        sync_mma();
-        if (tid == 0 && *reinterpret_cast<volatile int *>(&s_fail) == 0) {
-            tc::mma_op(tO, tc::Opnd{tc::smem_addr(sm + P), 16384, false},
-                       tc::Opnd{tc::smem_addr(sm + (b ? V1 : V0)), 16384, true}, AT, AD, AT, kt > 0);
-            tc::mma_commit(&bars[2]);
-            ++nc_o;
-        }
-    }
-    wait_or_fail(&bars[2], (n_kt - 1) & 1, 2, &s_fail);
-    tc::fence_after_sync();
-    ssum[cq * AT + qrow] = l_part;
-    __syncthreads();
-    // ---- outputs ------------------------------------------------------------------------
-    if (!s_fail) {
-        const float l = (ssum[qrow] + ssum[AT + qrow]) + (ssum[2 * AT + qrow] + ssum[3 * AT + qrow]), inv = 1.f / l;
-        const int64_t row = static_cast<int64_t>(row0) + q0 + qrow;
-        float r[32];
-        tc::tmem_ld32(tO + lane_off + cq * 32, r);
-        if (qrow < nq) {
-            uint4 *dst = reinterpret_cast<uint4 *>(p.o + (row * H + h) * AD + cq * 32);
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-                uint4 w;
-                w.x = tc::pack_bf16(r[i] * inv, r[i + 1] * inv);
-                w.y = tc::pack_bf16(r[i + 2] * inv, r[i + 3] * inv);
-                w.z = tc::pack_bf16(r[i + 4] * inv, r[i + 5] * inv);
-                w.w = tc::pack_bf16(r[i + 6] * inv, r[i + 7] * inv);
-                dst[i / 8] = w;
+                for (int i = 0; i < AT / 8; ++i) {
+                    const int r = r0 + 8 * i;
+                    const __nv_bfloat16 *g = src + (static_cast<int64_t>(rows[i] < 0 ? 0 : rows[i]) * H + h) * AD + pc * 8;
+                    tc::cp_async16(dst + piece(r, pc), g, rows[i] >= 0 ? 16u : 0u);
+                }
+                tc::cp_async_commit();
+                finish_prev(&bars[(t ? bVF : bKF) + b]);
             }
         }
-        if (p.lse && cq == 0 && qrow < nq) p.lse[row * H + h] = m_run * kLn2 + logf(l);
-    }
-    tc::cp_async_wait_all();
-    if (s_fail && tid == 0) {                           // drain the products still in flight
-        dev_error(pd, kDevErrTimeout, sq, h);
-        const uint32_t nc[3] = {nc_s0, nc_s1, nc_o};
+        cp_wait_group<0>();
+        tc::fence_smem_to_async();
+        mbar_arrive(pending);
+    } else if (warp == kFwdMmaWarp) {
+        // ---- one thread issues every product: S_{j+1} ahead of O_j
+        if (lane == 0) {
+            const tc::Opnd aQ{tc::smem_addr(sm + Q), 16384, false};
+            uint32_t nc_s0 = 0, nc_s1 = 0, nc_o = 0;
+            wait_or_fail(&bars[bQ], 0, 0, &s_fail);
+            wait_or_fail(&bars[bKF], 0, 0, &s_fail);
+            tc::fence_after_sync();
+            if (!failed(&s_fail)) {
+                tc::mma_op(tm, aQ, tc::Opnd{tc::smem_addr(sm + K0), 16384, false}, AT, AT, AD, false);
+                tc::mma_commit(&bars[bSF]);
+                tc::mma_commit(&bars[bKE]);
+                nc_s0 = 1;
+            }
+            for (int32_t kt = 0; kt < n_kt && !failed(&s_fail); ++kt) {
+                const int b = kt & 1, nb = b ^ 1;
+                if (kt + 1 < n_kt) {
+                    wait_or_fail(&bars[bKF + nb], ((kt + 1) >> 1) & 1, 0, &s_fail);
+                    if (kt >= 1) wait_or_fail(&bars[bSE + nb], ((kt - 1) >> 1) & 1, 1, &s_fail);
+                    tc::fence_after_sync();
+                    if (failed(&s_fail)) break;
+                    tc::mma_op(tm + nb * 128, aQ, tc::Opnd{tc::smem_addr(sm + (nb ? K1 : K0)), 16384, false},
+                               AT, AT, AD, false);
+                    tc::mma_commit(&bars[bSF + nb]);
+                    tc::mma_commit(&bars[bKE + nb]);
+                    if (nb) ++nc_s1; else ++nc_s0;
+                }
+                wait_or_fail(&bars[bPF], kt & 1, 1, &s_fail);
+                wait_or_fail(&bars[bVF + b], (kt >> 1) & 1, 0, &s_fail);
+                tc::fence_after_sync();
+                if (failed(&s_fail)) break;
+                tc::mma_op(tO, tc::Opnd{tc::smem_addr(sm + P), 16384, false},
+                           tc::Opnd{tc::smem_addr(sm + (b ? V1 : V0)), 16384, true}, AT, AD, AT, kt > 0);
+                tc::mma_commit(&bars[bOD]);
+                tc::mma_commit(&bars[bVE + b]);
+                ++nc_o;
+            }
+            if (failed(&s_fail)) {                      // drain the products still in flight
+                dev_error(pd, kDevErrTimeout, sq, h);
+                if (nc_s0) tc::mbar_wait(&bars[bSF], (nc_s0 - 1) & 1, 1000000000LL);
+                if (nc_s1) tc::mbar_wait(&bars[bSF + 1], (nc_s1 - 1) & 1, 1000000000LL);
+                if (nc_o) tc::mbar_wait(&bars[bOD], (nc_o - 1) & 1, 1000000000LL);
+            }
+        }
+    } else {
+        // ---- softmax: one query row and 64 columns per thread
+        float *smax = reinterpret_cast<float *>(sm + Max), *ssum = reinterpret_cast<float *>(sm + Sum);
+        const int lg = warp & 3, half = warp >> 2;
+        const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+        const int qrow = lg * 32 + lane;
+        const int32_t vis = hh + q0 + qrow;
+        const int32_t first_masked = (hh + q0) / AT;
+        const float c = p.scale * kLog2e;
+        float m_run = -INFINITY, l_half = 0.f;
+        for (int32_t kt = 0; kt < n_kt; ++kt) {
+            const int b = kt & 1;
+            wait_or_fail(&bars[bSF + b], (kt >> 1) & 1, 1, &s_fail);
+            tc::fence_after_sync();
+            float s[64];
+            {
+                float r[32];
+                tc::tmem_ld32(tm + b * 128 + lane_off + half * 64, r);
 #pragma unroll
-        for (int i = 0; i < 3; ++i)
-            if (nc[i]) tc::mbar_wait(&bars[i], (nc[i] - 1) & 1, 1000000000LL);
+                for (int i = 0; i < 32; ++i) s[i] = r[i];
+                tc::tmem_ld32(tm + b * 128 + lane_off + half * 64 + 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[32 + i] = r[i];
+            }
+            tc::fence_before_sync();
+            mbar_arrive(&bars[bSE + b]);                 // S buffer may be overwritten
+            if (kt >= first_masked) {
+                const int32_t lim = vis - (kt * AT + half * 64);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) s[i] = i <= lim ? s[i] : -INFINITY;
+            }
+            float mp[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                mp[i] = fmaxf(fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24])),
+                              fmaxf(fmaxf(s[i + 32], s[i + 40]), fmaxf(s[i + 48], s[i + 56])));
+#pragma unroll
+            for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i) mp[i] = fmaxf(mp[i], mp[i + w]);
+            smax[(b * 2 + half) * AT + qrow] = mp[0];
+            asm volatile("bar.sync %0, 64;" :: "r"(1 + lg) : "memory");   // the row's two warps
+            const float m_tile = c * fmaxf(smax[(b * 2) * AT + qrow], smax[(b * 2 + 1) * AT + qrow]);
+            const bool move = __any_sync(0xffffffffu, m_tile > m_run + kRescaleLog2);
+            float alpha = 1.f;
+            if (move) {
+                const float m_new = fmaxf(m_run, m_tile);
+                alpha = ex2(m_run - m_new);
+                m_run = m_new;
+            }
+            float sp[8];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                s[i] = ex2(fmaf(s[i], c, -m_run));
+                sp[i & 7] = (i < 8) ? s[i] : sp[i & 7] + s[i];
+            }
+#pragma unroll
+            for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i) sp[i] += sp[i + w];
+            l_half = l_half * alpha + sp[0];
+            if (kt > 0) wait_or_fail(&bars[bOD], (kt - 1) & 1, 1, &s_fail);   // P free, O settled
+            tc::fence_after_sync();
+#pragma unroll
+            for (int i = 0; i < 64; i += 8) tc::st_sw128_8(sm + P, AT, qrow, half * 64 + i, s + i);
+            if (move && kt > 0) {
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    float r[32];
+                    tc::tmem_ld32(tO + lane_off + half * 64 + hf * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] *= alpha;
+                    tc::tmem_st32(tO + lane_off + half * 64 + hf * 32, r);
+                }
+            }
+            tc::fence_smem_to_async();
+            tc::fence_before_sync();
+            mbar_arrive(&bars[bPF]);
+        }
+        wait_or_fail(&bars[bOD], (n_kt - 1) & 1, 1, &s_fail);
+        tc::fence_after_sync();
+        ssum[half * AT + qrow] = l_half;
+        asm volatile("bar.sync %0, 64;" :: "r"(1 + lg) : "memory");
+        if (!failed(&s_fail)) {
+            const float l = ssum[qrow] + ssum[AT + qrow], inv = 1.f / l;
+            const int64_t row = static_cast<int64_t>(row0) + q0 + qrow;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float r[32];
+                tc::tmem_ld32(tO + lane_off + half * 64 + hf * 32, r);
+                if (qrow < nq) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + (row * H + h) * AD + half * 64 + hf * 32);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint4 w;
+                        w.x = tc::pack_bf16(r[i] * inv, r[i + 1] * inv);
+                        w.y = tc::pack_bf16(r[i + 2] * inv, r[i + 3] * inv);
+                        w.z = tc::pack_bf16(r[i + 4] * inv, r[i + 5] * inv);
+                        w.w = tc::pack_bf16(r[i + 6] * inv, r[i + 7] * inv);
+                        dst[i / 8] = w;
+                    }
+                }
+            }
+            if (p.lse && half == 0 && qrow < nq) p.lse[row * H + h] = m_run * kLn2 + logf(l);
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (warp == 0) tc::tmem_dealloc(tm, 512);
+    if (warp == kFwdMmaWarp) tc::tmem_dealloc(tm, 512);
 }
-
 
 // ======================================================================================
 // Backward.  With D_t = sum_d dO_t o_t (per query row and head), P = softmax(scale S):
@@ -654,10 +701,11 @@ static int check_attn(const harts_plan *P, const harts_attn_fwd_args *a) {
 }
 
 template <typename K, typename Prm>
-static cudaError_t launch_big(K kernel, unsigned blocks, uint32_t smem, cudaStream_t st, const Prm &p, const PlanDev &pd) {
+static cudaError_t launch_big(K kernel, unsigned blocks, int threads, uint32_t smem, cudaStream_t st, const Prm &p,
+                              const PlanDev &pd) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kernel<<<blocks, ANT, smem, st>>>(p, pd);
+    kernel<<<blocks, threads, smem, st>>>(p, pd);
     return cudaGetLastError();
 }
 
@@ -675,7 +723,7 @@ int harts_attn_fwd(const harts_plan *P, const harts_attn_fwd_args *a, harts_stre
     p.lse = a->lse;
     p.H = a->H;
     p.scale = a->scale;
-    const cudaError_t e = launch_big(attn_fwd_tc, static_cast<unsigned>(blocks), at_sm::bytes,
+    const cudaError_t e = launch_big(attn_fwd_tc, static_cast<unsigned>(blocks), kFwdThreads, at_sm::bytes,
                                      reinterpret_cast<cudaStream_t>(stream), p, P->view);
     if (e != cudaSuccess) { set_error(std::string("attention launch: ") + cudaGetErrorString(e)); return HARTS_ECUDA; }
     set_error("");
@@ -719,9 +767,11 @@ int harts_attn_bwd(const harts_plan *P, const harts_attn_bwd_args *a, harts_stre
         static_cast<const __nv_bfloat16 *>(a->fwd.o), p.dout, D, rows);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess)
-        e = launch_big(attn_bwd_dq_tc, static_cast<unsigned>(int64_t(P->image.n_qt) * p.H), bq_sm::bytes, st, p, P->view);
+        e = launch_big(attn_bwd_dq_tc, static_cast<unsigned>(int64_t(P->image.n_qt) * p.H), ANT, bq_sm::bytes, st, p,
+                       P->view);
     if (e == cudaSuccess)
-        e = launch_big(attn_bwd_dkdv_tc, static_cast<unsigned>(int64_t(P->image.n_kt) * p.H), bk_sm::bytes, st, p, P->view);
+        e = launch_big(attn_bwd_dkdv_tc, static_cast<unsigned>(int64_t(P->image.n_kt) * p.H), ANT, bk_sm::bytes, st, p,
+                       P->view);
     if (e != cudaSuccess) { set_error(std::string("attention backward launch: ") + cudaGetErrorString(e)); return HARTS_ECUDA; }
     set_error("");
     return HARTS_OK;
