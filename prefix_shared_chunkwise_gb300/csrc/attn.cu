@@ -11,9 +11,10 @@
 // tree (longest first within a tree) with the heads innermost, so the key / value rows a
 // tree's blocks share stay in L2.  The block's warps have fixed roles and meet only at
 // mbarriers (every wait bounded):
-//   loaders (4 warps)   gather Q, then K_j and V_j of each 128-row key tile by cp.async
-//                       into two-slot K and V rings; a slot is refilled once the product
-//                       that reads it has completed (K after S_j, V after O_j)
+//   loaders (2 + 2)     gather Q and the K_j, and (the other pair) the V_j of each 128-row
+//                       key tile by cp.async into two-slot K and V rings; a slot is
+//                       refilled once the product that reads it has completed (K after
+//                       S_j, V after O_j); the pairs run independent pipelines
 //   MMA (one thread)    S_j = Q K_j^T (tcgen05, fp32 in one of two TMEM buffers), issued a
 //                       tile ahead of O_{j-1} += P_{j-1} V_{j-1} (V read MN-major)
 //   softmax (8 warps)   one query row and 64 columns per thread; scores in base-2 units
@@ -30,6 +31,7 @@
 
 #include "kda_common.cuh"
 #include "tc_primitives.cuh"
+#include "tensor_map.h"
 
 namespace harts {
 namespace {
@@ -46,9 +48,9 @@ constexpr uint32_t bytes = Sum + 1024 + 1024;     // + alignment slack
 }  // namespace at_sm
 
 // Roles of the forward's 13 warps.
-constexpr int kFwdSoftmaxWarps = 8, kFwdMmaWarp = 8, kFwdLoadWarp0 = 9, kFwdLoadWarps = 4;
+constexpr int kFwdSoftmaxWarps = 8, kFwdMmaWarp = 8, kFwdLoadWarp0 = 9, kFwdLoadWarps = 2;
 constexpr int kFwdThreads = (kFwdLoadWarp0 + kFwdLoadWarps) * 32;
-constexpr int kLoadThreads = kFwdLoadWarps * 32, kSoftThreads = kFwdSoftmaxWarps * 32;
+constexpr int kSoftThreads = kFwdSoftmaxWarps * 32;
 
 struct AttnParams {
     const __nv_bfloat16 *q, *k, *v;
@@ -93,10 +95,68 @@ __device__ __forceinline__ void wait_or_fail(uint64_t *bar, uint32_t phase, int 
 
 __device__ __forceinline__ bool failed(int *s_fail) { return *reinterpret_cast<volatile int *>(s_fail) != 0; }
 
+// Tensor maps of [C][H][128] bf16 tensors: boxes of 64 channels x 128 rows (q, dO) and of
+// 64 channels x (8 << j) rows, j = 0..4 (k, v: any 8-aligned run of a view tile).
+struct AttnMaps {
+    CUtensorMap q, dout, k[5], v[5];
+};
+
+// Issue the TMA boxes of padded-view key tile `kt` of sequence `sq` into a [128][128] SW128
+// tile (two 64-channel halves 16 KB apart), 32 KB in all; `ri` walks the sequence's runs
+// across calls.  Runs start at multiples of 8 and pad up to one; positions past the view
+// read rows beyond the tensor (zeros).
+__device__ __forceinline__ void tma_view_tile(const CUtensorMap *maps, uint8_t *tile, const PlanDev &pd, int32_t sq,
+                                              int32_t kt, int h, int &ri, uint64_t *bar) {
+    const int32_t r_end = pd.attn_rptr[sq + 1];
+    int x = 0;
+    while (x < AT) {
+        const int32_t pos = kt * AT + x;
+        int32_t ps = 0, pend = 0, row = 0;
+        while (ri < r_end) {
+            ps = pd.attn_runs[3 * ri];
+            row = pd.attn_runs[3 * ri + 1];
+            pend = ps + ((pd.attn_runs[3 * ri + 2] + 7) & ~7);
+            if (pend > pos) break;
+            ++ri;
+        }
+        int n, src;
+        if (ri < r_end && ps <= pos) {
+            n = min(AT - x, pend - pos);
+            src = row + (pos - ps);
+        } else {
+            n = AT - x;
+            src = static_cast<int32_t>(pd.C);             // past the last row: zero fill
+        }
+        while (n > 0) {
+            const int j = n >= 128 ? 4 : n >= 64 ? 3 : n >= 32 ? 2 : n >= 16 ? 1 : 0;
+            const int R = 8 << j;
+            tc::tma_load_3d(tile + x * 128, &maps[j], 0, h, src, bar);
+            tc::tma_load_3d(tile + 16384 + x * 128, &maps[j], 64, h, src, bar);
+            x += R;
+            src += R;
+            n -= R;
+        }
+    }
+}
+
+// Validity of padded-view positions base .. base + 31 (base a multiple of 32): real
+// ancestor positions (planner bitmask) and own positions (hp .. hp + own - 1).
+__device__ __forceinline__ uint32_t view_bits(const PlanDev &pd, int32_t sq, int32_t hp, int32_t own, int32_t base) {
+    uint32_t m = 0;
+    if (base < hp) m = static_cast<uint32_t>(pd.attn_mask[pd.attn_mptr[sq] + base / 32]);
+    const int32_t lo = max(base, hp), hi = min(base + 32, hp + own);
+    if (lo < hi) {
+        const int a = lo - base, n = hi - lo;
+        m |= (n == 32 ? 0xffffffffu : ((1u << n) - 1u)) << a;
+    }
+    return m;
+}
+
 // Barriers of the forward (index into bars[]).
 enum FwdBar { bQ = 0, bKF = 1, bKE = 3, bVF = 5, bVE = 7, bSF = 9, bSE = 11, bPF = 13, bOD = 14, bN = 15 };
 
-__global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, PlanDev pd) {
+__global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, PlanDev pd,
+                                                                const __grid_constant__ AttnMaps maps) {
     using namespace at_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
@@ -107,16 +167,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
     const int H = p.H;
     const int32_t h = blockIdx.x % H, qi = blockIdx.x / H;
     const int32_t sq = pd.attn_qt[2 * qi], qt = pd.attn_qt[2 * qi + 1];
-    const int32_t hb = pd.attn_hptr[sq], hh = pd.attn_hptr[sq + 1] - hb;
-    const int32_t row0 = pd.seq_row0[sq], own = pd.seq_nown[sq], nview = hh + own;
+    const int32_t hh = pd.attn_hp[sq];                  // padded ancestor length
+    const int32_t row0 = pd.seq_row0[sq], own = pd.seq_nown[sq];
     const int32_t q0 = qt * AT, nq = min(AT, own - q0);
     const int32_t n_kt = (hh + q0 + nq - 1) / AT + 1;   // key tiles covering every visible entry
 
     if (tid == 0) {
-        tc::mbar_init(&bars[bQ], kLoadThreads);
+        tc::mbar_init(&bars[bQ], 1);
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&bars[bKF + i], kLoadThreads);
-            tc::mbar_init(&bars[bVF + i], kLoadThreads);
+            tc::mbar_init(&bars[bKF + i], 1);
+            tc::mbar_init(&bars[bVF + i], 1);
             tc::mbar_init(&bars[bKE + i], 1);
             tc::mbar_init(&bars[bVE + i], 1);
             tc::mbar_init(&bars[bSF + i], 1);
@@ -136,49 +196,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
     const uint32_t tm = s_tmem, tO = tm + 256;
 
     if (warp >= kFwdLoadWarp0) {
-        // ---- loaders: Q, then K_0, V_0, K_1, V_1, ...; a group's full barrier is
-        // arrived on once the next group is in flight (at most two groups per thread)
-        const int lt = tid - kFwdLoadWarp0 * 32, pc = lt & 15, r0 = lt >> 4;
-        uint64_t *pending = nullptr;
-        auto finish_prev = [&](uint64_t *next) {
-            cp_wait_group<1>();
-            tc::fence_smem_to_async();
-            if (pending) mbar_arrive(pending);
-            pending = next;
-        };
-        for (int i = 0; i < AT / 8; ++i) {
-            const int r = r0 + 8 * i;
-            const bool ok = r < nq;
-            const __nv_bfloat16 *g = p.q + ((static_cast<int64_t>(row0) + q0 + (ok ? r : 0)) * H + h) * AD + pc * 8;
-            tc::cp_async16(sm + Q + piece(r, pc), g, ok ? 16u : 0u);
-        }
-        tc::cp_async_commit();
-        finish_prev(&bars[bQ]);
-        for (int32_t kt = 0; kt < n_kt; ++kt) {
-            const int b = kt & 1;
-            int32_t rows[AT / 8];
-#pragma unroll
-            for (int i = 0; i < AT / 8; ++i) {
-                const int32_t j = kt * AT + r0 + 8 * i;
-                rows[i] = j < hh ? pd.attn_hrows[hb + j] : (j < nview ? row0 + (j - hh) : -1);
+        // ---- loaders: one thread for Q and the K ring, one for the V ring, tiled TMA
+        if (lane == 0) {
+            const int is_v = warp - kFwdLoadWarp0;
+            int ri = pd.attn_rptr[sq];
+            if (!is_v) {
+                tc::mbar_expect_tx(&bars[bQ], 32768);
+                tc::tma_load_3d(sm + Q, &maps.q, 0, h, row0 + q0, &bars[bQ]);
+                tc::tma_load_3d(sm + Q + 16384, &maps.q, 64, h, row0 + q0, &bars[bQ]);
             }
-            for (int t = 0; t < 2; ++t) {                 // t = 0: K, 1: V
-                if (kt >= 2) wait_or_fail(&bars[(t ? bVE : bKE) + b], ((kt - 2) >> 1) & 1, 2, &s_fail);
-                uint8_t *dst = sm + (t ? (b ? V1 : V0) : (b ? K1 : K0));
-                const __nv_bfloat16 *src = t ? p.v : p.k;
-#pragma unroll
-                for (int i = 0; i < AT / 8; ++i) {
-                    const int r = r0 + 8 * i;
-                    const __nv_bfloat16 *g = src + (static_cast<int64_t>(rows[i] < 0 ? 0 : rows[i]) * H + h) * AD + pc * 8;
-                    tc::cp_async16(dst + piece(r, pc), g, rows[i] >= 0 ? 16u : 0u);
-                }
-                tc::cp_async_commit();
-                finish_prev(&bars[(t ? bVF : bKF) + b]);
+            for (int32_t kt = 0; kt < n_kt; ++kt) {
+                const int b = kt & 1;
+                if (kt >= 2) wait_or_fail(&bars[(is_v ? bVE : bKE) + b], ((kt - 2) >> 1) & 1, 2, &s_fail);
+                uint64_t *full = &bars[(is_v ? bVF : bKF) + b];
+                tc::mbar_expect_tx(full, 32768);
+                tma_view_tile(is_v ? maps.v : maps.k, sm + (is_v ? (b ? V1 : V0) : (b ? K1 : K0)), pd, sq, kt, h, ri,
+                              full);
             }
         }
-        cp_wait_group<0>();
-        tc::fence_smem_to_async();
-        mbar_arrive(pending);
     } else if (warp == kFwdMmaWarp) {
         // ---- one thread issues every product: S_{j+1} ahead of O_j
         if (lane == 0) {
@@ -230,11 +265,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
         const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
         const int qrow = lg * 32 + lane;
         const int32_t vis = hh + q0 + qrow;
-        const int32_t first_masked = (hh + q0) / AT;
         const float c = p.scale * kLog2e;
         float m_run = -INFINITY, l_half = 0.f;
+        // validity of this thread's 64 columns, one tile ahead
+        uint32_t nb0 = view_bits(pd, sq, hh, own, half * 64), nb1 = view_bits(pd, sq, hh, own, half * 64 + 32);
         for (int32_t kt = 0; kt < n_kt; ++kt) {
             const int b = kt & 1;
+            const uint32_t vb0 = nb0, vb1 = nb1;
+            if (kt + 1 < n_kt) {
+                nb0 = view_bits(pd, sq, hh, own, (kt + 1) * AT + half * 64);
+                nb1 = view_bits(pd, sq, hh, own, (kt + 1) * AT + half * 64 + 32);
+            }
             wait_or_fail(&bars[bSF + b], (kt >> 1) & 1, 1, &s_fail);
             tc::fence_after_sync();
             float s[64];
@@ -249,10 +290,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
             }
             tc::fence_before_sync();
             mbar_arrive(&bars[bSE + b]);                 // S buffer may be overwritten
-            if (kt >= first_masked) {
-                const int32_t lim = vis - (kt * AT + half * 64);
+            const int32_t lim = vis - (kt * AT + half * 64);
+            if (__any_sync(0xffffffffu, (vb0 & vb1) != 0xffffffffu || lim < 63)) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) s[i] = i <= lim ? s[i] : -INFINITY;
+                for (int i = 0; i < 64; ++i) {
+                    const bool ok = ((i < 32 ? vb0 >> i : vb1 >> (i - 32)) & 1u) && i <= lim;
+                    s[i] = ok ? s[i] : -INFINITY;
+                }
             }
             float mp[8];
 #pragma unroll
@@ -378,21 +422,8 @@ struct AttnBwdParams {
 
 namespace bq_sm {
 constexpr uint32_t Q = 0, dO = 32768, K0 = 65536, K1 = 98304, V = 131072, dS = 163840;
-constexpr uint32_t Tab = 196608;                  // [4][128] int32 view rows of tiles j % 4
-constexpr uint32_t bytes = Tab + 2048 + 1024;
+constexpr uint32_t bytes = 196608 + 1024;
 }  // namespace bq_sm
-
-// Stage `rows` (row index per tile row, -1 = zero) of head h into a SW128 tile.
-__device__ __forceinline__ void stage_rows(const __nv_bfloat16 *src, const int32_t *tab, int H, int h, uint8_t *dst,
-                                           int tid) {
-#pragma unroll
-    for (int i = 0; i < AT * 16 / ANT; ++i) {
-        const int e = tid + i * ANT, r = e >> 4, pc = e & 15;
-        const int32_t row = tab[r];
-        const __nv_bfloat16 *g = src + (static_cast<int64_t>(row < 0 ? 0 : row) * H + h) * AD + pc * 8;
-        tc::cp_async16(dst + piece(r, pc), g, row >= 0 ? 16u : 0u);
-    }
-}
 
 // Stage rows first .. first + n - 1 (zeros for the rest of the tile).
 __device__ __forceinline__ void stage_run(const __nv_bfloat16 *src, int64_t first, int n, int H, int h, uint8_t *dst,
@@ -419,30 +450,27 @@ __device__ __forceinline__ void store_tile_bf16(__nv_bfloat16 *dst_row, const fl
     }
 }
 
-__global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDev pd) {
+__global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDev pd,
+                                                          const __grid_constant__ AttnMaps maps) {
     using namespace bq_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    __shared__ uint64_t bars[2];                  // S and dP ready, dQ product done
+    __shared__ uint64_t bars[5];                  // S and dP ready, dQ done, K slot 0 / 1 full, V full
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
-    int32_t *stab = reinterpret_cast<int32_t *>(sm + Tab);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, cq = warp >> 2;
     const int H = p.H;
     const int32_t h = blockIdx.x % H, qi = blockIdx.x / H;
     const int32_t sq = pd.attn_qt[2 * qi], qt = pd.attn_qt[2 * qi + 1];
-    const int32_t hb = pd.attn_hptr[sq], hh = pd.attn_hptr[sq + 1] - hb;
-    const int32_t row0 = pd.seq_row0[sq], own = pd.seq_nown[sq], nview = hh + own;
+    const int32_t hh = pd.attn_hp[sq];
+    const int32_t row0 = pd.seq_row0[sq], own = pd.seq_nown[sq];
     const int32_t q0 = qt * AT, nq = min(AT, own - q0);
     const int32_t n_kt = (hh + q0 + nq - 1) / AT + 1;
-    const int32_t first_masked = (hh + q0) / AT;
     const float c = p.scale * kLog2e;
-    auto view_row = [&](int32_t j) -> int32_t {
-        return j < hh ? pd.attn_hrows[hb + j] : (j < nview ? row0 + (j - hh) : -1);
-    };
+    uint64_t *bS = &bars[0], *bQd = &bars[1], *bK = &bars[2], *bV = &bars[4];
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) tc::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 5; ++i) tc::mbar_init(&bars[i], 1);
         tc::fence_mbar_init();
         s_fail = 0;
     }
@@ -450,7 +478,6 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDe
         tc::tmem_alloc(&s_tmem, 512);
         tc::fence_before_sync();
     }
-    if (tid < AT) stab[tid] = view_row(tid);
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = s_tmem, lane_off = static_cast<uint32_t>(lg * 32) << 16;
@@ -459,58 +486,68 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDe
     const int32_t vis = hh + q0 + qrow;
     const int64_t grow = static_cast<int64_t>(row0) + q0 + min(qrow, nq - 1);
     const float lse2 = p.lse[grow * H + h] * kLog2e, Dq = p.D[grow * H + h];
-
-    stage_run(p.q, static_cast<int64_t>(row0) + q0, nq, H, h, sm + Q, tid);
-    stage_run(p.dout, static_cast<int64_t>(row0) + q0, nq, H, h, sm + dO, tid);
-    stage_rows(p.k, stab, H, h, sm + K0, tid);
-    stage_rows(p.v, stab, H, h, sm + V, tid);
-    tc::cp_async_commit();
+    int ri_k = pd.attn_rptr[sq], ri_v = ri_k;            // thread 0: run cursors of the K and V tiles
+    if (tid == 0) {
+        // Q, dO and K_0 on K slot 0's barrier; V_0 on the V barrier
+        tc::mbar_expect_tx(&bK[0], 3 * 32768);
+        tc::tma_load_3d(sm + Q, &maps.q, 0, h, row0 + q0, &bK[0]);
+        tc::tma_load_3d(sm + Q + 16384, &maps.q, 64, h, row0 + q0, &bK[0]);
+        tc::tma_load_3d(sm + dO, &maps.dout, 0, h, row0 + q0, &bK[0]);
+        tc::tma_load_3d(sm + dO + 16384, &maps.dout, 64, h, row0 + q0, &bK[0]);
+        tma_view_tile(maps.k, sm + K0, pd, sq, 0, h, ri_k, &bK[0]);
+        tc::mbar_expect_tx(bV, 32768);
+        tma_view_tile(maps.v, sm + V, pd, sq, 0, h, ri_v, bV);
+    }
     uint32_t nc_s = 0, nc_q = 0;
+    uint32_t nb = view_bits(pd, sq, hh, own, cq * 32);
 
     for (int32_t kt = 0; kt < n_kt; ++kt) {
         const int b = kt & 1;
-        tc::cp_async_wait_all();
-        sync_mma();
-        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s_fail)) {
-            tc::mma_op(tS, tc::Opnd{tc::smem_addr(sm + Q), 16384, false},
-                       tc::Opnd{tc::smem_addr(sm + (b ? K1 : K0)), 16384, false}, AT, AT, AD, false);
-            tc::mma_op(tP, tc::Opnd{tc::smem_addr(sm + dO), 16384, false},
-                       tc::Opnd{tc::smem_addr(sm + V), 16384, false}, AT, AT, AD, false);
-            tc::mma_commit(&bars[0]);
-            ++nc_s;
+        const uint32_t vb = nb;
+        if (kt + 1 < n_kt) nb = view_bits(pd, sq, hh, own, (kt + 1) * AT + cq * 32);
+        if (tid == 0) {
+            wait_or_fail(&bK[b], (kt >> 1) & 1, 2, &s_fail);
+            wait_or_fail(bV, kt & 1, 2, &s_fail);
+            tc::fence_after_sync();
+            if (!failed(&s_fail)) {
+                tc::mma_op(tS, tc::Opnd{tc::smem_addr(sm + Q), 16384, false},
+                           tc::Opnd{tc::smem_addr(sm + (b ? K1 : K0)), 16384, false}, AT, AT, AD, false);
+                tc::mma_op(tP, tc::Opnd{tc::smem_addr(sm + dO), 16384, false},
+                           tc::Opnd{tc::smem_addr(sm + V), 16384, false}, AT, AT, AD, false);
+                tc::mma_commit(bS);
+                ++nc_s;
+            }
         }
-        // the row table of the next tile (its slot was last read before the sync above)
-        if (tid < AT) stab[((kt + 1) & 1) * AT + tid] = (kt + 1 < n_kt) ? view_row((kt + 1) * AT + tid) : -1;
-        wait_or_fail(&bars[0], kt & 1, 0, &s_fail);
+        wait_or_fail(bS, kt & 1, 0, &s_fail);
         tc::fence_after_sync();
         float sv[32], pv[32];
         tc::tmem_ld32(tS + lane_off + cq * 32, sv);
         tc::tmem_ld32(tP + lane_off + cq * 32, pv);
-        if (kt > 0) wait_or_fail(&bars[1], (kt - 1) & 1, 1, &s_fail);   // dQ_{kt-1}: dS and K free
+        if (kt > 0) wait_or_fail(bQd, (kt - 1) & 1, 1, &s_fail);      // dQ_{kt-1}: dS and K_{kt-1} free
         tc::fence_after_sync();
-        __syncthreads();                                                  // next row table visible
-        if (kt + 1 < n_kt) {
-            stage_rows(p.v, stab + ((kt + 1) & 1) * AT, H, h, sm + V, tid);
-            stage_rows(p.k, stab + ((kt + 1) & 1) * AT, H, h, sm + (b ? K0 : K1), tid);
+        if (tid == 0 && kt + 1 < n_kt) {               // V (read by dP_kt, done) and the other K slot
+            tc::mbar_expect_tx(bV, 32768);
+            tma_view_tile(maps.v, sm + V, pd, sq, kt + 1, h, ri_v, bV);
+            tc::mbar_expect_tx(&bK[b ^ 1], 32768);
+            tma_view_tile(maps.k, sm + (b ? K0 : K1), pd, sq, kt + 1, h, ri_k, &bK[b ^ 1]);
         }
-        tc::cp_async_commit();
-        const int32_t lim = (kt >= first_masked) ? vis - (kt * AT + cq * 32) : 1 << 30;
+        const int32_t lim = vis - (kt * AT + cq * 32);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const float pr = i <= lim ? ex2(fmaf(sv[i], c, -lse2)) : 0.f;
+            const float pr = (((vb >> i) & 1u) && i <= lim) ? ex2(fmaf(sv[i], c, -lse2)) : 0.f;
             sv[i] = p.scale * pr * (pv[i] - Dq);
         }
 #pragma unroll
         for (int i = 0; i < 32; i += 8) tc::st_sw128_8(sm + dS, AT, qrow, cq * 32 + i, sv + i);
         sync_mma();
-        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s_fail)) {
+        if (tid == 0 && !failed(&s_fail)) {
             tc::mma_op(tQ, tc::Opnd{tc::smem_addr(sm + dS), 16384, false},
                        tc::Opnd{tc::smem_addr(sm + (b ? K1 : K0)), 16384, true}, AT, AD, AT, kt > 0);
-            tc::mma_commit(&bars[1]);
+            tc::mma_commit(bQd);
             ++nc_q;
         }
     }
-    wait_or_fail(&bars[1], (n_kt - 1) & 1, 1, &s_fail);
+    wait_or_fail(bQd, (n_kt - 1) & 1, 1, &s_fail);
     tc::fence_after_sync();
     __syncthreads();
     if (!s_fail) {
@@ -518,11 +555,10 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDe
         tc::tmem_ld32(tQ + lane_off + cq * 32, r);
         if (qrow < nq) store_tile_bf16(p.dq + ((static_cast<int64_t>(row0) + q0 + qrow) * H + h) * AD + cq * 32, r, 1.f);
     }
-    tc::cp_async_wait_all();
-    if (s_fail && tid == 0) {
+    if (s_fail && tid == 0) {                          // drain products and copies in flight
         dev_error(pd, kDevErrTimeout, sq, h);
-        if (nc_s) tc::mbar_wait(&bars[0], (nc_s - 1) & 1, 1000000000LL);
-        if (nc_q) tc::mbar_wait(&bars[1], (nc_q - 1) & 1, 1000000000LL);
+        if (nc_s) tc::mbar_wait(bS, (nc_s - 1) & 1, 1000000000LL);
+        if (nc_q) tc::mbar_wait(bQd, (nc_q - 1) & 1, 1000000000LL);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -700,13 +736,30 @@ static int check_attn(const harts_plan *P, const harts_attn_fwd_args *a) {
     return HARTS_OK;
 }
 
-template <typename K, typename Prm>
-static cudaError_t launch_big(K kernel, unsigned blocks, int threads, uint32_t smem, cudaStream_t st, const Prm &p,
-                              const PlanDev &pd) {
+template <typename K, typename... Args>
+static cudaError_t launch_big(K kernel, unsigned blocks, int threads, uint32_t smem, cudaStream_t st,
+                              const Args &...args) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kernel<<<blocks, threads, smem, st>>>(p, pd);
+    kernel<<<blocks, threads, smem, st>>>(args...);
     return cudaGetLastError();
+}
+
+// [C][H][128] bf16 as a 3-D tensor {channels, heads, rows}; one box height.
+static bool rows_map(CUtensorMap *m, const void *base, int H, int64_t C, int box_rows) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(AD), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(C)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(AD) * 2, static_cast<cuuint64_t>(H) * AD * 2};
+    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+    return encode_bf16(m, base, 3, dims, strides, box);
+}
+
+static bool attn_maps(AttnMaps &m, const void *q, const void *dout, const void *k, const void *v, int H, int64_t C) {
+    if (!rows_map(&m.q, q, H, C, AT)) return false;
+    if (dout && !rows_map(&m.dout, dout, H, C, AT)) return false;
+    if (!dout) m.dout = m.q;
+    for (int j = 0; j < 5; ++j)
+        if (!rows_map(&m.k[j], k, H, C, 8 << j) || !rows_map(&m.v[j], v, H, C, 8 << j)) return false;
+    return true;
 }
 
 extern "C" {
@@ -723,8 +776,12 @@ int harts_attn_fwd(const harts_plan *P, const harts_attn_fwd_args *a, harts_stre
     p.lse = a->lse;
     p.H = a->H;
     p.scale = a->scale;
+    AttnMaps maps;
+    if (!attn_maps(maps, a->q, nullptr, a->k, a->v, a->H, P->info.C)) {
+        set_error("tensor map encoding failed"); return HARTS_ECUDA;
+    }
     const cudaError_t e = launch_big(attn_fwd_tc, static_cast<unsigned>(blocks), kFwdThreads, at_sm::bytes,
-                                     reinterpret_cast<cudaStream_t>(stream), p, P->view);
+                                     reinterpret_cast<cudaStream_t>(stream), p, P->view, maps);
     if (e != cudaSuccess) { set_error(std::string("attention launch: ") + cudaGetErrorString(e)); return HARTS_ECUDA; }
     set_error("");
     return HARTS_OK;
@@ -766,9 +823,13 @@ int harts_attn_bwd(const harts_plan *P, const harts_attn_bwd_args *a, harts_stre
     attn_bwd_prep<<<static_cast<unsigned>(prep_blocks), 256, 0, st>>>(
         static_cast<const __nv_bfloat16 *>(a->fwd.o), p.dout, D, rows);
     cudaError_t e = cudaGetLastError();
+    AttnMaps maps;
+    if (e == cudaSuccess && !attn_maps(maps, a->fwd.q, a->d_o, a->fwd.k, a->fwd.v, p.H, P->info.C)) {
+        set_error("tensor map encoding failed"); return HARTS_ECUDA;
+    }
     if (e == cudaSuccess)
         e = launch_big(attn_bwd_dq_tc, static_cast<unsigned>(int64_t(P->image.n_qt) * p.H), ANT, bq_sm::bytes, st, p,
-                       P->view);
+                       P->view, maps);
     if (e == cudaSuccess)
         e = launch_big(attn_bwd_dkdv_tc, static_cast<unsigned>(int64_t(P->image.n_kt) * p.H), ANT, bk_sm::bytes, st, p,
                        P->view);

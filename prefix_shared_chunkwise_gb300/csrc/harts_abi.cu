@@ -116,7 +116,8 @@ int harts_plan_upload(harts_plan *P, void *dev_buf, size_t bytes, harts_stream_t
     v.row_seg = w + I.off_row_seg; v.seg_row0 = w + I.off_seg_row0; v.seg_len = w + I.off_seg_len;
     v.conv_ctx = w + I.off_conv_ctx; v.conv_sptr = w + I.off_conv_sptr; v.conv_succ = w + I.off_conv_succ;
     v.n_seg = P->info.n_seg;
-    v.attn_hptr = w + I.off_attn_hptr; v.attn_hrows = w + I.off_attn_hrows; v.attn_qt = w + I.off_attn_qt;
+    v.attn_rptr = w + I.off_attn_rptr; v.attn_runs = w + I.off_attn_runs; v.attn_mptr = w + I.off_attn_mptr;
+    v.attn_mask = w + I.off_attn_mask; v.attn_hp = w + I.off_attn_hp; v.attn_qt = w + I.off_attn_qt;
     v.attn_kt = w + I.off_attn_kt; v.attn_kptr = w + I.off_attn_kptr; v.attn_kq = w + I.off_attn_kq;
     v.n_qt = I.n_qt; v.n_kt = I.n_kt;
     v.n_rounds = P->info.n_rounds; v.n_seq = P->info.n_seq; v.n_states = P->info.n_states;

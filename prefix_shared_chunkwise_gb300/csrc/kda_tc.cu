@@ -22,6 +22,7 @@
 
 #include "kda_common.cuh"
 #include "tc_primitives.cuh"
+#include "tensor_map.h"
 
 namespace harts {
 namespace {
@@ -1521,28 +1522,9 @@ cudaError_t tc_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t ba
 
 namespace {
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda).
-PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
 bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
             const cuuint32_t *box) {
-    auto fn = encode_tiled();
-    if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
-    const cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_bf16(m, base, rank, dims, strides, box);
 }
 
 // [C rows][H heads][D] bf16, boxes of (8 << j) rows of 64 channels, j = 0..3.

@@ -383,32 +383,55 @@ void build_image(harts_plan &P) {
 
     // ---- branch attention -------------------------------------------------------------
     // A sequence's view: the trajectory positions before its first own token (ancestor
-    // rows, root first), then its own rows.  Query tiles of kAttnTile own rows, grouped
-    // by tree (so the blocks that read a tree's keys and values run together and find
-    // them in L2), trees in decreasing order of their longest tile, and within a tree by
-    // decreasing work (view length up to the tile's end).
-    // The ancestor lists add up to sum_i (first position of sequence i), quadratic in the
-    // depth of chain-like trees: above kAttnMaxRows the plan carries no attention tables.
+    // segments, root first), then its own rows.  In the kernels' padded view every
+    // segment's run starts at a multiple of 8 positions (up to 7 pad positions after
+    // each ancestor run), so each 8-row group of a key tile is 8 consecutive compact rows
+    // and moves by one tiled TMA box; a bitmask marks the real positions of the ancestor
+    // part.  Runs: (padded start, first compact row, rows), the own run last at hp, the
+    // padded ancestor length.  Query tiles of kAttnTile own rows, grouped by tree (so
+    // the blocks that read a tree's keys and values run together and find them in L2),
+    // trees in decreasing order of their longest tile, within a tree by decreasing work
+    // (padded view length up to the tile's end).
+    // The key-tile lists below grow with sum_i (first position of sequence i), quadratic
+    // in the depth of chain-like trees: above kAttnMaxRows the plan carries no attention
+    // tables.
     int64_t sum_h = 0;
     for (int32_t i = 0; i < n_seq; ++i) sum_h += P.seg_pos[P.seq_first_seg[i]];
     P.attn_ok = sum_h <= kAttnMaxRows;
-    std::vector<int32_t> hptr(n_seq + 1, 0), hrows;
+    std::vector<int32_t> rptr(n_seq + 1, 0), runs, mptr(n_seq + 1, 0), vmask, hp(n_seq, 0);
     std::vector<int32_t> chain;
     for (int32_t i = 0; i < n_seq && P.attn_ok; ++i) {
-        hptr[i] = static_cast<int32_t>(hrows.size());
+        rptr[i] = static_cast<int32_t>(runs.size() / 3);
         chain.clear();
         for (int32_t u = P.parent[P.seq_first_seg[i]]; u >= 0; u = P.parent[u]) chain.push_back(u);
-        for (auto it = chain.rbegin(); it != chain.rend(); ++it)
-            for (int64_t t = 0; t < P.seg_len[*it]; ++t) hrows.push_back(static_cast<int32_t>(P.seg_offset[*it] + t));
+        int64_t ps = 0;
+        std::vector<std::pair<int64_t, int64_t>> real;    // (padded start, rows)
+        for (auto it = chain.rbegin(); it != chain.rend(); ++it) {
+            runs.insert(runs.end(), {static_cast<int32_t>(ps), static_cast<int32_t>(P.seg_offset[*it]),
+                                     static_cast<int32_t>(P.seg_len[*it])});
+            real.push_back({ps, P.seg_len[*it]});
+            ps += (P.seg_len[*it] + 7) / 8 * 8;
+        }
+        hp[i] = static_cast<int32_t>(ps);
+        const int64_t own = P.cu_seqlens[i + 1] - P.cu_seqlens[i];
+        runs.insert(runs.end(), {static_cast<int32_t>(ps), static_cast<int32_t>(P.seg_offset[P.seq_first_seg[i]]),
+                                 static_cast<int32_t>(own)});
+        mptr[i] = static_cast<int32_t>(vmask.size());
+        const size_t w0 = vmask.size();
+        vmask.resize(w0 + (ps + 31) / 32, 0);
+        for (const auto &r : real)
+            for (int64_t t = r.first; t < r.first + r.second; ++t)
+                vmask[w0 + t / 32] |= static_cast<int32_t>(1u << (t % 32));
     }
-    hptr[n_seq] = static_cast<int32_t>(hrows.size());
+    rptr[n_seq] = static_cast<int32_t>(runs.size() / 3);
+    mptr[n_seq] = static_cast<int32_t>(vmask.size());
     struct QTile { int64_t work; int32_t tree, seq, tile; };
     std::vector<QTile> qts;
     std::vector<int32_t> root(P.parent.size());
     for (size_t v = 0; v < P.parent.size(); ++v) root[v] = P.parent[v] < 0 ? static_cast<int32_t>(v) : root[P.parent[v]];
     std::vector<int64_t> tree_work(P.parent.size(), 0);
     for (int32_t i = 0; i < n_seq && P.attn_ok; ++i) {
-        const int64_t own = P.cu_seqlens[i + 1] - P.cu_seqlens[i], hh = hptr[i + 1] - hptr[i];
+        const int64_t own = P.cu_seqlens[i + 1] - P.cu_seqlens[i], hh = hp[i];
         const int32_t r = root[P.seq_first_seg[i]];
         for (int64_t t = 0; t * kAttnTile < own; ++t) {
             const int64_t w = hh + std::min(own, (t + 1) * kAttnTile);
@@ -426,8 +449,11 @@ void build_image(harts_plan &P) {
     std::vector<int32_t> qt(2 * qts.size());
     for (size_t j = 0; j < qts.size(); ++j) { qt[2 * j] = qts[j].seq; qt[2 * j + 1] = qts[j].tile; }
     I.n_qt = static_cast<int32_t>(qts.size());
-    put(I.off_attn_hptr, hptr.data(), hptr.size());
-    put(I.off_attn_hrows, hrows.data(), hrows.size());
+    put(I.off_attn_rptr, rptr.data(), rptr.size());
+    put(I.off_attn_runs, runs.data(), runs.size());
+    put(I.off_attn_mptr, mptr.data(), mptr.size());
+    put(I.off_attn_mask, vmask.data(), vmask.size());
+    put(I.off_attn_hp, hp.data(), hp.size());
     put(I.off_attn_qt, qt.data(), qt.size());
 
     // Key tiles for the key / value gradients: kAttnTile own rows of a sequence.  The

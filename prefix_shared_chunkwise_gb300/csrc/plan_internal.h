@@ -42,8 +42,11 @@ struct PlanDev {
     const int32_t *conv_sptr;      // [n_seg*(kConvMaxW-1)+1] successor lists of (segment end, lag e+1)
     const int32_t *conv_succ;      // rows e+1 positions after the segment's end, on every branch
     // branch attention: each sequence's ancestor prefix, and the query tiles
-    const int32_t *attn_hptr;      // [n_seq+1] ancestor rows of sequence i: attn_hrows[attn_hptr[i] ..]
-    const int32_t *attn_hrows;     // compact rows of the trajectory positions before the sequence
+    const int32_t *attn_rptr;      // [n_seq+1] runs of sequence i: attn_runs[3 * rptr[i] ..], own run last
+    const int32_t *attn_runs;      // (padded view start, first compact row, rows); starts are multiples of 8
+    const int32_t *attn_mptr;      // [n_seq+1] validity words of sequence i's padded ancestor part
+    const int32_t *attn_mask;      // bit t of word t / 32: padded position t holds a real row
+    const int32_t *attn_hp;        // [n_seq] padded ancestor length (start of the own run)
     const int32_t *attn_qt;        // [n_qt][2] (sequence, query tile), tree by tree
     const int32_t *attn_kt;        // [n_kt][2] (sequence, key tile of its own rows), tree by tree
     const int32_t *attn_kptr;      // [n_kt+1] query tiles of key tile j: attn_kq[3 * kptr[j] ..]
@@ -61,8 +64,8 @@ struct PlanImage {
         off_seq_rho, off_seq_rptr, off_seq_src, off_seq_sptr, off_state_lpos, off_seq_cbase,
         off_state_cptr, off_state_cons, off_root_cptr, off_root_cons, off_replay_idx,
         off_fold_rows, off_fold_ptr, off_fold_occ, off_chunk_seq, off_row_seg, off_seg_row0,
-        off_seg_len, off_conv_ctx, off_conv_sptr, off_conv_succ, off_attn_hptr, off_attn_hrows,
-        off_attn_qt, off_attn_kt, off_attn_kptr, off_attn_kq;
+        off_seg_len, off_conv_ctx, off_conv_sptr, off_conv_succ, off_attn_rptr, off_attn_runs,
+        off_attn_mptr, off_attn_mask, off_attn_hp, off_attn_qt, off_attn_kt, off_attn_kptr, off_attn_kq;
     int32_t n_qt, n_kt;
 };
 
