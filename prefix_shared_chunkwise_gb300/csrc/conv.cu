@@ -117,10 +117,21 @@ __device__ __forceinline__ float dsilu(float z) {
 }
 
 // Forward.  Item = (run of kRun consecutive rows, 8 channels); a thread keeps its channel
-// group (weights in registers) and walks its runs row by row; the predecessor rows it
-// reads are the rows it has just read (L1 hits), except the ancestor context of a
-// segment's first W-1 rows.
+// group (weights in registers) and walks its runs.  A run's segment is looked up once and
+// followed across segment boundaries; inside a segment, rows at least W-1 past its start
+// go in batches of 4, whose W+3 input rows are loaded together (the rows shared with the
+// previous batch are L1 hits); a segment's first W-1 rows take their context from the
+// ancestor table.
 constexpr int kRun = 32;
+
+template <typename T>
+__device__ __forceinline__ void act_store(const ConvParams &p, int64_t r, int c0, float (&v)[8]) {
+    if (p.act) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = silu(v[e]);
+    }
+    st8(static_cast<T *>(p.y) + r * p.ch + c0, v);
+}
 
 template <typename T, int W>
 __global__ void __launch_bounds__(256) conv_fwd_kernel(ConvParams p, PlanDev pd) {
@@ -130,21 +141,49 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(ConvParams p, PlanDev pd)
     int64_t it = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
     if (it >= n) return;
     const int c0 = static_cast<int>(it % G) * 8;
+    const T *x = static_cast<const T *>(p.x);
     Coef<W> k;
     load_coef<W>(p, c0, k);
     for (; it < n; it += stride) {
         const int64_t r0 = it / G * kRun, r1 = min(p.C, r0 + kRun);
-#pragma unroll 4
-        for (int64_t r = r0; r < r1; ++r) {
-            const int32_t seg = pd.row_seg[r];
-            const int32_t i = static_cast<int32_t>(r - pd.seg_row0[seg]);
-            float v[8];
-            conv_pre<T, W>(p, pd, k, r, seg, i, c0, v);
-            if (p.act) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = silu(v[e]);
+        int64_t r = r0;
+        int32_t seg = pd.row_seg[r];
+        int64_t srow0 = pd.seg_row0[seg], send = srow0 + pd.seg_len[seg];
+        while (r < r1) {
+            const int64_t rend = min(r1, send);
+            // a segment's first W-1 rows: context from the ancestor table
+            for (; r < rend && r - srow0 < W - 1; ++r) {
+                float v[8];
+                conv_pre<T, W>(p, pd, k, r, seg, static_cast<int32_t>(r - srow0), c0, v);
+                act_store<T>(p, r, c0, v);
             }
-            st8(static_cast<T *>(p.y) + r * p.ch + c0, v);
+            // the rest in batches of 4: inputs r-W+1 .. r+3, all in this segment
+            for (; r + 4 <= rend; r += 4) {
+                float xin[W + 3][8];
+#pragma unroll
+                for (int q = 0; q < W + 3; ++q) ld8(x + (r - (W - 1) + q) * p.ch + c0, xin[q]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = k.bias[e];
+#pragma unroll
+                    for (int j = 0; j < W; ++j)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] += k.wt[j][e] * xin[u + W - 1 - j][e];
+                    act_store<T>(p, r + u, c0, v);
+                }
+            }
+            for (; r < rend; ++r) {
+                float v[8];
+                conv_pre<T, W>(p, pd, k, r, seg, static_cast<int32_t>(r - srow0), c0, v);
+                act_store<T>(p, r, c0, v);
+            }
+            if (r < r1) {
+                seg = pd.row_seg[r];
+                srow0 = r;
+                send = srow0 + pd.seg_len[seg];
+            }
         }
     }
 }
