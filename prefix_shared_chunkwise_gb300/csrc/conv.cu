@@ -26,6 +26,7 @@ namespace {
 
 constexpr int K = kConvMaxW - 1;
 constexpr int kRowsPerPart = 256;       // rows per partial sum of dweight / dbias
+constexpr int kBwdN = 4;                // channels per backward thread (8-byte bf16 vectors)
 
 struct ConvParams {
     const void *x;
@@ -65,6 +66,35 @@ __device__ __forceinline__ void st8(__nv_bfloat16 *p, const float (&v)[8]) {
     *reinterpret_cast<uint4 *>(p) = u;
 }
 
+// N = 4 channels (8 or 16 bytes).
+__device__ __forceinline__ void ldn(const float *p, float (&v)[4]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+__device__ __forceinline__ void ldn(const __nv_bfloat16 *p, float (&v)[4]) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v[2 * i] = f.x; v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void ldn(const float *p, float (&v)[8]) { ld8(p, v); }
+__device__ __forceinline__ void ldn(const __nv_bfloat16 *p, float (&v)[8]) { ld8(p, v); }
+__device__ __forceinline__ void stn(float *p, const float (&v)[4]) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void stn(__nv_bfloat16 *p, const float (&v)[4]) {
+    uint2 u;
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+    h[0] = __floats2bfloat162_rn(v[0], v[1]);
+    h[1] = __floats2bfloat162_rn(v[2], v[3]);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+__device__ __forceinline__ void stn(float *p, const float (&v)[8]) { st8(p, v); }
+__device__ __forceinline__ void stn(__nv_bfloat16 *p, const float (&v)[8]) { st8(p, v); }
+
 // Row j positions before row r (r is row i of segment seg), or -1 before the trajectory.
 __device__ __forceinline__ int64_t pred_row(const PlanDev &pd, int64_t r, int32_t seg, int32_t i, int j) {
     return i >= j ? r - j : static_cast<int64_t>(pd.conv_ctx[seg * K + (j - i - 1)]);
@@ -76,37 +106,37 @@ __device__ __forceinline__ int64_t pred_row(const PlanDev &pd, int64_t r, int32_
 // in registers -- while it walks its rows (the rows it re-reads are ones it has just
 // read: L1 hits).
 
-template <int W>
+template <int W, int N = 8>
 struct Coef {
-    float wt[W][8];           // wt[j][e] = weight[c0+e][W-1-j]
-    float bias[8];
+    float wt[W][N];           // wt[j][e] = weight[c0+e][W-1-j]
+    float bias[N];
 };
 
-template <int W>
-__device__ __forceinline__ void load_coef(const ConvParams &p, int c0, Coef<W> &k) {
+template <int W, int N>
+__device__ __forceinline__ void load_coef(const ConvParams &p, int c0, Coef<W, N> &k) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) k.bias[e] = p.bias ? __ldg(p.bias + c0 + e) : 0.f;
+    for (int e = 0; e < N; ++e) k.bias[e] = p.bias ? __ldg(p.bias + c0 + e) : 0.f;
 #pragma unroll
     for (int j = 0; j < W; ++j)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) k.wt[j][e] = __ldg(p.weight + (c0 + e) * W + (W - 1 - j));
+        for (int e = 0; e < N; ++e) k.wt[j][e] = __ldg(p.weight + (c0 + e) * W + (W - 1 - j));
 }
 
-// pre = bias + sum_j weight[:, w-1-j] x[row j back], 8 channels from c0
-template <typename T, int W>
-__device__ __forceinline__ void conv_pre(const ConvParams &p, const PlanDev &pd, const Coef<W> &k, int64_t r,
-                                         int32_t seg, int32_t i, int c0, float (&pre)[8]) {
+// pre = bias + sum_j weight[:, w-1-j] x[row j back], N channels from c0
+template <typename T, int W, int N>
+__device__ __forceinline__ void conv_pre(const ConvParams &p, const PlanDev &pd, const Coef<W, N> &k, int64_t r,
+                                         int32_t seg, int32_t i, int c0, float (&pre)[N]) {
     const T *x = static_cast<const T *>(p.x);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) pre[e] = k.bias[e];
+    for (int e = 0; e < N; ++e) pre[e] = k.bias[e];
 #pragma unroll
     for (int j = 0; j < W; ++j) {
         const int64_t pr = pred_row(pd, r, seg, i, j);
         if (pr < 0) break;                       // so are all earlier positions
-        float xv[8];
-        ld8(x + pr * p.ch + c0, xv);
+        float xv[N];
+        ldn(x + pr * p.ch + c0, xv);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) pre[e] += k.wt[j][e] * xv[e];
+        for (int e = 0; e < N; ++e) pre[e] += k.wt[j][e] * xv[e];
     }
 }
 
@@ -143,7 +173,7 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(ConvParams p, PlanDev pd)
     const int c0 = static_cast<int>(it % G) * 8;
     const T *x = static_cast<const T *>(p.x);
     Coef<W> k;
-    load_coef<W>(p, c0, k);
+    load_coef<W, 8>(p, c0, k);
     for (; it < n; it += stride) {
         const int64_t r0 = it / G * kRun, r1 = min(p.C, r0 + kRun);
         int64_t r = r0;
@@ -154,7 +184,7 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(ConvParams p, PlanDev pd)
             // a segment's first W-1 rows: context from the ancestor table
             for (; r < rend && r - srow0 < W - 1; ++r) {
                 float v[8];
-                conv_pre<T, W>(p, pd, k, r, seg, static_cast<int32_t>(r - srow0), c0, v);
+                conv_pre<T, W, 8>(p, pd, k, r, seg, static_cast<int32_t>(r - srow0), c0, v);
                 act_store<T>(p, r, c0, v);
             }
             // the rest in batches of 4: inputs r-W+1 .. r+3, all in this segment
@@ -176,7 +206,7 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(ConvParams p, PlanDev pd)
             }
             for (; r < rend; ++r) {
                 float v[8];
-                conv_pre<T, W>(p, pd, k, r, seg, static_cast<int32_t>(r - srow0), c0, v);
+                conv_pre<T, W, 8>(p, pd, k, r, seg, static_cast<int32_t>(r - srow0), c0, v);
                 act_store<T>(p, r, c0, v);
             }
             if (r < r1) {
@@ -189,15 +219,15 @@ __global__ void __launch_bounds__(256) conv_fwd_kernel(ConvParams p, PlanDev pd)
 }
 
 // dL/dpre of row s (row i of segment seg): dy[s] * act'(pre[s]), pre recomputed.
-template <typename T, int W>
-__device__ __forceinline__ void dpre_of(const ConvParams &p, const PlanDev &pd, const Coef<W> &k, int64_t s,
-                                        int32_t seg, int32_t i, int c0, float (&g)[8]) {
-    ld8(static_cast<const T *>(p.dy) + s * p.ch + c0, g);
+template <typename T, int W, int N>
+__device__ __forceinline__ void dpre_of(const ConvParams &p, const PlanDev &pd, const Coef<W, N> &k, int64_t s,
+                                        int32_t seg, int32_t i, int c0, float (&g)[N]) {
+    ldn(static_cast<const T *>(p.dy) + s * p.ch + c0, g);
     if (p.act) {
-        float pre[8];
-        conv_pre<T, W>(p, pd, k, s, seg, i, c0, pre);
+        float pre[N];
+        conv_pre<T, W, N>(p, pd, k, s, seg, i, c0, pre);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) g[e] *= dsilu(pre[e]);
+        for (int e = 0; e < N; ++e) g[e] *= dsilu(pre[e]);
     }
 }
 
@@ -209,78 +239,88 @@ __device__ __forceinline__ void dpre_of(const ConvParams &p, const PlanDev &pd, 
 // written to the workspace.  Reads x and dy, writes dx: the op's own traffic.
 template <typename T, int W>
 __global__ void __launch_bounds__(256) conv_bwd_kernel(ConvParams p, PlanDev pd) {
-    const int G = p.ch / 8;
+    constexpr int N = kBwdN;
+    const int G = p.ch / N;
     const int64_t n_part = (p.C + kRowsPerPart - 1) / kRowsPerPart;
     const int64_t n = n_part * G;
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;   // a multiple of G
     const T *x = static_cast<const T *>(p.x);
     int64_t it = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
     if (it >= n) return;
-    const int c0 = static_cast<int>(it % G) * 8;
-    Coef<W> k;
-    load_coef<W>(p, c0, k);
+    const int c0 = static_cast<int>(it % G) * N;
+    Coef<W, N> k;
+    load_coef<W, N>(p, c0, k);
     for (; it < n; it += stride) {
         const int64_t pb = it / G;
-        float dw[W][8], db[8], dp[W][8];
+        float dw[W][N], db[N], dp[W][N];
 #pragma unroll
         for (int j = 0; j < W; ++j)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) { dw[j][e] = 0.f; dp[j][e] = 0.f; }
+            for (int e = 0; e < N; ++e) { dw[j][e] = 0.f; dp[j][e] = 0.f; }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) db[e] = 0.f;
+        for (int e = 0; e < N; ++e) db[e] = 0.f;
         const int64_t r0 = pb * kRowsPerPart, r1 = min(p.C, r0 + kRowsPerPart);
+        // the block's segment is looked up once and followed across boundaries
+        int32_t seg = pd.row_seg[r0];
+        int64_t row0 = pd.seg_row0[seg];
+        int32_t len = pd.seg_len[seg];
         for (int64_t r = r0; r < r1; ++r) {
-            const int32_t seg = pd.row_seg[r];
-            const int32_t row0 = pd.seg_row0[seg], len = pd.seg_len[seg];
+            if (r == row0 + len) {
+                seg = pd.row_seg[r];
+                row0 = r;
+                len = pd.seg_len[seg];
+            }
             const int32_t i = static_cast<int32_t>(r - row0);
             if (r == r0 || i == 0) {
                 // (re)fill dp[0 .. W-2] for this segment
 #pragma unroll
                 for (int d = 0; d + 1 < W; ++d)
-                    if (i + d < len) dpre_of<T, W>(p, pd, k, r + d, seg, i + d, c0, dp[d]);
+                    if (i + d < len) dpre_of<T, W, N>(p, pd, k, r + d, seg, i + d, c0, dp[d]);
             }
-            if (i + W - 1 < len) dpre_of<T, W>(p, pd, k, r + W - 1, seg, i + W - 1, c0, dp[W - 1]);
+            if (i + W - 1 < len) dpre_of<T, W, N>(p, pd, k, r + W - 1, seg, i + W - 1, c0, dp[W - 1]);
             // dx[r]
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float acc[N];
+#pragma unroll
+            for (int e = 0; e < N; ++e) acc[e] = 0.f;
 #pragma unroll
             for (int d = 0; d < W; ++d) {
                 if (i + d < len) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] += k.wt[d][e] * dp[d][e];
+                    for (int e = 0; e < N; ++e) acc[e] += k.wt[d][e] * dp[d][e];
                 } else {
                     const int ee = i + d - len;
                     const int32_t b = pd.conv_sptr[seg * K + ee], end = pd.conv_sptr[seg * K + ee + 1];
                     for (int32_t q = b; q < end; ++q) {
                         const int64_t sr = pd.conv_succ[q];
                         const int32_t ss = pd.row_seg[sr];
-                        float t[8];
-                        dpre_of<T, W>(p, pd, k, sr, ss, static_cast<int32_t>(sr - pd.seg_row0[ss]), c0, t);
+                        float t[N];
+                        dpre_of<T, W, N>(p, pd, k, sr, ss, static_cast<int32_t>(sr - pd.seg_row0[ss]), c0, t);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] += k.wt[d][e] * t[e];
+                        for (int e = 0; e < N; ++e) acc[e] += k.wt[d][e] * t[e];
                     }
                 }
             }
-            st8(static_cast<T *>(p.dx) + r * p.ch + c0, acc);
+            stn(static_cast<T *>(p.dx) + r * p.ch + c0, acc);
             // dweight / dbias partials with dL/dpre of row r
 #pragma unroll
-            for (int e = 0; e < 8; ++e) db[e] += dp[0][e];
+            for (int e = 0; e < N; ++e) db[e] += dp[0][e];
 #pragma unroll
             for (int j = 0; j < W; ++j) {
                 const int64_t pr = pred_row(pd, r, seg, i, j);
                 if (pr < 0) break;
-                float xv[8];
-                ld8(x + pr * p.ch + c0, xv);
+                float xv[N];
+                ldn(x + pr * p.ch + c0, xv);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) dw[j][e] += xv[e] * dp[0][e];
+                for (int e = 0; e < N; ++e) dw[j][e] += xv[e] * dp[0][e];
             }
 #pragma unroll
             for (int d = 0; d + 1 < W; ++d)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) dp[d][e] = dp[d + 1][e];
+                for (int e = 0; e < N; ++e) dp[d][e] = dp[d + 1][e];
         }
         float *out = p.part + (pb * p.ch + c0) * (W + 1);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < N; ++e) {
 #pragma unroll
             for (int j = 0; j < W; ++j) out[e * (W + 1) + (W - 1 - j)] = dw[j][e];
             out[e * (W + 1) + W] = db[e];
@@ -417,7 +457,7 @@ int harts_conv_bwd(const harts_plan *P, const harts_conv_bwd_args *a, harts_stre
     cudaError_t e = cudaSuccess;
     if (P->info.C > 0) {
         const int64_t n_part = (p.C + kRowsPerPart - 1) / kRowsPerPart;
-        const int g1 = grid_groups(n_part * (p.ch / 8), p.ch / 8);
+        const int g1 = grid_groups(n_part * (p.ch / kBwdN), p.ch / kBwdN);
         with_width(p.w, [&](auto wc) {
             constexpr int W = decltype(wc)::value;
             if (a->fwd.dtype == HARTS_BF16) conv_bwd_kernel<__nv_bfloat16, W><<<g1, 256, 0, st>>>(p, P->view);
