@@ -92,8 +92,6 @@ __device__ __forceinline__ void stn(__nv_bfloat16 *p, const float (&v)[4]) {
     h[1] = __floats2bfloat162_rn(v[2], v[3]);
     *reinterpret_cast<uint2 *>(p) = u;
 }
-__device__ __forceinline__ void stn(float *p, const float (&v)[8]) { st8(p, v); }
-__device__ __forceinline__ void stn(__nv_bfloat16 *p, const float (&v)[8]) { st8(p, v); }
 
 // Row j positions before row r (r is row i of segment seg), or -1 before the trajectory.
 __device__ __forceinline__ int64_t pred_row(const PlanDev &pd, int64_t r, int32_t seg, int32_t i, int j) {
