@@ -268,7 +268,70 @@ __global__ void __launch_bounds__(256) conv_bwd_kernel(ConvParams p, PlanDev pd)
                 row0 = r;
                 len = pd.seg_len[seg];
             }
-            const int32_t i = static_cast<int32_t>(r - row0);
+            int32_t i = static_cast<int32_t>(r - row0);
+            // interior rows (the window and the look-ahead inside the segment) run from
+            // registers: the x rows r-W+1 .. r+W-1 slide, and only x, dy of row r+W-1 are
+            // new, loaded one row ahead
+            if (r != r0 && i >= W - 1 && i + 2 * W - 2 < len) {
+                const int64_t fend = min(r1, row0 + len - (W - 1));
+                float xw[2 * W - 1][N];
+#pragma unroll
+                for (int q = 0; q < 2 * W - 2; ++q) ldn(x + (r - (W - 1) + q) * p.ch + c0, xw[q]);
+                float nx[N], nd[N];
+                ldn(x + (r + W - 1) * p.ch + c0, nx);
+                ldn(static_cast<const T *>(p.dy) + (r + W - 1) * p.ch + c0, nd);
+                for (; r < fend; ++r) {
+                    float cd[N];
+#pragma unroll
+                    for (int e = 0; e < N; ++e) { xw[2 * W - 2][e] = nx[e]; cd[e] = nd[e]; }
+                    if (r + 1 < fend) {
+                        ldn(x + (r + W) * p.ch + c0, nx);
+                        ldn(static_cast<const T *>(p.dy) + (r + W) * p.ch + c0, nd);
+                    }
+                    if (p.act) {
+                        float pre[N];
+#pragma unroll
+                        for (int e = 0; e < N; ++e) pre[e] = k.bias[e];
+#pragma unroll
+                        for (int j = 0; j < W; ++j)
+#pragma unroll
+                            for (int e = 0; e < N; ++e) pre[e] += k.wt[j][e] * xw[2 * W - 2 - j][e];
+#pragma unroll
+                        for (int e = 0; e < N; ++e) cd[e] *= dsilu(pre[e]);
+                    }
+#pragma unroll
+                    for (int e = 0; e < N; ++e) dp[W - 1][e] = cd[e];
+                    float acc[N];
+#pragma unroll
+                    for (int e = 0; e < N; ++e) acc[e] = 0.f;
+#pragma unroll
+                    for (int d = 0; d < W; ++d)
+#pragma unroll
+                        for (int e = 0; e < N; ++e) acc[e] += k.wt[d][e] * dp[d][e];
+                    stn(static_cast<T *>(p.dx) + r * p.ch + c0, acc);
+#pragma unroll
+                    for (int e = 0; e < N; ++e) db[e] += dp[0][e];
+#pragma unroll
+                    for (int j = 0; j < W; ++j)
+#pragma unroll
+                        for (int e = 0; e < N; ++e) dw[j][e] += xw[W - 1 - j][e] * dp[0][e];
+#pragma unroll
+                    for (int d = 0; d + 1 < W; ++d)
+#pragma unroll
+                        for (int e = 0; e < N; ++e) dp[d][e] = dp[d + 1][e];
+#pragma unroll
+                    for (int q = 0; q + 1 < 2 * W - 1; ++q)
+#pragma unroll
+                        for (int e = 0; e < N; ++e) xw[q][e] = xw[q + 1][e];
+                }
+                if (r >= r1) break;
+                if (r == row0 + len) {
+                    seg = pd.row_seg[r];
+                    row0 = r;
+                    len = pd.seg_len[seg];
+                }
+                i = static_cast<int32_t>(r - row0);
+            }
             if (r == r0 || i == 0) {
                 // (re)fill dp[0 .. W-2] for this segment
 #pragma unroll
