@@ -188,6 +188,34 @@ __device__ void prefetch_chunk(const FwdParams &p, const PlanDev &pd, int32_t se
     tc::cp_async_commit();
 }
 
+// q, k, v, g as {128 channels, H, C} with boxes of one head's 64 rows, unswizzled: a box
+// lands as the staging buffer's row-major [64][128] tile.
+struct FwdMaps {
+    CUtensorMap t[4];
+};
+
+// A chunk of own rows only, and full: staged by four TMA boxes instead of row gathers.
+__device__ __forceinline__ bool tma_chunk(int32_t rho, int32_t L, int32_t c0) { return c0 >= rho && c0 + BC <= L; }
+
+__device__ void prefetch_chunk_tma(const FwdParams &p, const FwdMaps &maps, int32_t h, int32_t row0, int32_t rho,
+                                   int32_t c0, uint8_t *sm, uint64_t *bar) {
+    using namespace fwd_sm;
+    const int H = p.H;
+    const int32_t r = row0 + (c0 - rho);
+    if (threadIdx.x == 0) {
+        tc::mbar_expect_tx(bar, 4 * 16384);
+#pragma unroll
+        for (int ten = 0; ten < 4; ++ten) tc::tma_load_3d(sm + Stage + ten * 16384, &maps.t[ten], 0, h, r, bar);
+    }
+    if (threadIdx.x < 64) {
+        const int64_t idx = (static_cast<int64_t>(r) + threadIdx.x) * H + h;
+        const uint8_t *src = static_cast<const uint8_t *>(p.beta) + (idx & ~int64_t(1)) * 2;
+        tc::cp_async4(sm + SBeta + threadIdx.x * 4, src, 4u);
+        reinterpret_cast<int *>(sm + SBpar)[threadIdx.x] = static_cast<int>(idx & 1);
+    }
+    tc::cp_async_commit();
+}
+
 __device__ __forceinline__ float2 stage2(const uint8_t *sm, uint32_t off, int t, int c) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm + off + t * 256 + c * 2));
 }
@@ -200,11 +228,12 @@ __device__ __forceinline__ void st_bf16x2(uint8_t *tile, int rows, int row, int 
 // kInner: the plan may put slots inside a chunk (no-replay plans); the minimum-call and
 // node-wise plans never do, and their instance carries none of that code.
 template <bool kInner>
-__global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int32_t round_base) {
+__global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int32_t round_base,
+                                                    const __grid_constant__ FwdMaps maps) {
     using namespace fwd_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    __shared__ uint64_t bars[4];
+    __shared__ uint64_t bars[5];                  // four MMA groups, staged chunk (TMA)
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
     __shared__ int s_rows[64];
@@ -225,11 +254,16 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
     uint8_t *cst = static_cast<uint8_t *>(p.chunk_states);
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) tc::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 5; ++i) tc::mbar_init(&bars[i], 1);
+        tc::fence_mbar_init();
         s_fail = 0;
     }
     if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
-    prefetch_chunk(p, pd, seq, h, rho, L, 0, sm, s_rows);
+    __syncthreads();
+    uint32_t n_tma = 0;                                  // chunks staged by TMA so far (uniform)
+    bool tma_pending = tma_chunk(rho, L, 0);
+    if (tma_pending) prefetch_chunk_tma(p, maps, h, row0, rho, 0, sm, &bars[4]);
+    else prefetch_chunk(p, pd, seq, h, rho, L, 0, sm, s_rows);
     tc::fence_after_sync();
     const uint32_t tm = s_tmem;
     const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
@@ -273,7 +307,13 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
         const int nv = min(BC, L - c0);
         const int mid = (nv - 1) / 2;
         tc::cp_async_wait_all();
+        if (tma_pending) {
+            if (!tc::mbar_wait(&bars[4], n_tma & 1)) atomicOr(&s_fail, 1);
+            ++n_tma;
+            tma_pending = false;
+        }
         __syncthreads();
+        if (s_fail) break;
         // ---- prep: cumulative decay, scaled operands (from the staged raw tiles) ----------
         // thread: key channels c2, c2 + 1; rows 16 qr .. 16 qr + 15
         {
@@ -353,7 +393,11 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
             tc::mma_commit(&bars[0]);
         }
         // the staging buffer is free: fetch the next chunk while this one computes
-        if (ci + 1 < nch) prefetch_chunk(p, pd, seq, h, rho, L, c0 + BC, sm, s_rows);
+        if (ci + 1 < nch) {
+            tma_pending = tma_chunk(rho, L, c0 + BC);
+            if (tma_pending) prefetch_chunk_tma(p, maps, h, row0, rho, c0 + BC, sm, &bars[4]);
+            else prefetch_chunk(p, pd, seq, h, rho, L, c0 + BC, sm, s_rows);
+        }
         // ---- scale the TMEM state by e^{Gamma_L} per key channel (used by MMA7) -----------
         for (int hf = 0; hf < 2; ++hf) {
             float r[32];
@@ -521,6 +565,7 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
         sync_for_mma();
     }
     tc::cp_async_wait_all();
+    if (tma_pending) tc::mbar_wait(&bars[4], n_tma & 1, 1000000000LL);   // a staged chunk still in flight
     if (s_fail) {
         dev_error(pd, kDevErrTimeout, seq, h);
         // let any MMA still in flight drain before the columns are released
@@ -1504,10 +1549,20 @@ cudaError_t tc_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, in
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(fwd_sm::bytes));
     if (e != cudaSuccess) return e;
+    FwdMaps maps;
+    {
+        const int H = p.H;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(pd.C)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+        const cuuint32_t box[3] = {D, 1, BC};
+        const void *src[4] = {p.q, p.k, p.v, p.g};
+        for (int i = 0; i < 4; ++i)
+            if (!encode_bf16(&maps.t[i], src[i], 3, dims, strides, box, false)) return cudaErrorInvalidValue;
+    }
     if (inner)
-        kda_fwd_tc<true><<<n_items, NT, fwd_sm::bytes, st>>>(p, pd, base);
+        kda_fwd_tc<true><<<n_items, NT, fwd_sm::bytes, st>>>(p, pd, base, maps);
     else
-        kda_fwd_tc<false><<<n_items, NT, fwd_sm::bytes, st>>>(p, pd, base);
+        kda_fwd_tc<false><<<n_items, NT, fwd_sm::bytes, st>>>(p, pd, base, maps);
     return cudaGetLastError();
 }
 
