@@ -694,11 +694,19 @@ constexpr uint32_t vBeta = Vec, vEl = vBeta + 256, vEkt = vEl + 512, vM = vEkt +
 constexpr uint32_t bytes = vEnd + 1024;
 }  // namespace bws_sm
 
-__global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev pd, int32_t round_base) {
+// q, k, g, dO as {128 channels, H, C} with boxes of 64 channels x 64 rows (128-byte
+// swizzle, the staging tiles' layout); the saved records as [rows][64] bf16 with 64 x 64
+// boxes (a chunk's T).
+struct StateMaps {
+    CUtensorMap q, k, g, dout, rec_t;
+};
+
+__global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev pd, int32_t round_base,
+                                                          const __grid_constant__ StateMaps maps) {
     using namespace bws_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    __shared__ uint64_t bars[4];
+    __shared__ uint64_t bars[5];                  // four MMA groups, staged chunk (TMA)
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
     __shared__ int s_rows[64];
@@ -718,7 +726,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
     uint8_t *dch = static_cast<uint8_t *>(p.dchunk);
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) tc::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 5; ++i) tc::mbar_init(&bars[i], 1);
+        tc::fence_mbar_init();
         s_fail = 0;
     }
     if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
@@ -745,8 +754,33 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
     const int32_t sp_begin = pd.seq_sptr[seq];
     int32_t sp = pd.seq_sptr[seq + 1] - 1;
     // Stage chunk cj's raw q, k, g, beta and (into buffer `b`) dO and the forward's T.
+    uint32_t n_tma = 0;                                  // chunks staged by TMA so far (uniform)
+    bool tma_pending = false;
     auto stage_chunk = [&](int32_t cj, int b) {
         const int32_t cc0 = cj * BC;
+        if (cc0 >= rho && cc0 + BC <= L) {
+            // own rows only, full: q, k, g, dO (two 64-channel halves each) and T by TMA
+            const int32_t r = pd.seq_row0[seq] + (cc0 - rho);
+            tma_pending = true;
+            if (tid == 0) {
+                uint64_t *bar = &bars[4];
+                tc::mbar_expect_tx(bar, 8 * 8192 + 8192);
+                const CUtensorMap *mp[4] = {&maps.q, &maps.k, &maps.g, &maps.dout};
+                uint8_t *dst[4] = {sm + RawQ, sm + RawK, sm + RawG, sm + (b ? dOm2 : dOm)};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    tc::tma_load_3d(dst[q], mp[q], 0, h, r, bar);
+                    tc::tma_load_3d(dst[q] + 8192, mp[q], 64, h, r, bar);
+                }
+                tc::tma_load_2d(sm + (b ? Tm2 : Tm), &maps.rec_t, 0,
+                                static_cast<int>((static_cast<int64_t>(cbase + cj) * H + h) * (kRecBytes / 128) + 2 * D),
+                                bar);
+            }
+            if (tid < 64) s_rows[tid] = r + tid;
+            stage_beta_tab(sm + SBeta, spar, f.beta, s_rows, h, H);   // each thread reads only its own entry
+            tc::cp_async_commit();
+            return;
+        }
         if (tid < 64) s_rows[tid] = static_cast<int>(local_row(pd, seq, rho, L, cc0 + tid));
         __syncthreads();
         stage_tab(sm + RawQ, f.q, s_rows, h, H, 0);
@@ -794,7 +828,13 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
             for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + dSTs, 128, jv, cb + j, r + j);
         }
         tc::cp_async_wait_all();
+        if (tma_pending) {
+            if (!tc::mbar_wait(&bars[4], n_tma & 1)) atomicOr(&s_fail, 1);
+            ++n_tma;
+            tma_pending = false;
+        }
         __syncthreads();
+        if (s_fail) break;
         {
             uint8_t *dst = dch + (static_cast<int64_t>(g) * H + h) * D * D * 2;
             for (int e = tid; e < 128 * 16; e += NT) {
@@ -907,6 +947,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
         if (!wait_all(&bars[3], ph, &s_fail)) break;
     }
     tc::cp_async_wait_all();
+    if (tma_pending) tc::mbar_wait(&bars[4], n_tma & 1, 1000000000LL);   // a staged chunk still in flight
     if (!s_fail && (src >= 0 || p.dh0)) {
         float *dst = p.ds_init + (static_cast<int64_t>(seq) * H + h) * D * D;
         for (int hf = 0; hf < 2; ++hf) {
@@ -1571,7 +1612,23 @@ cudaError_t tc_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t ba
     cudaError_t e = cudaFuncSetAttribute(kda_bwd_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(bws_sm::bytes));
     if (e != cudaSuccess) return e;
-    kda_bwd_state_tc<<<n_items, NT, bws_sm::bytes, st>>>(p, pd, base);
+    StateMaps maps;
+    {
+        const int H = p.f.H;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(pd.C)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+        const cuuint32_t box[3] = {64, 1, BC};
+        const void *src[4] = {p.f.q, p.f.k, p.f.g, p.d_o};
+        CUtensorMap *dst[4] = {&maps.q, &maps.k, &maps.g, &maps.dout};
+        for (int i = 0; i < 4; ++i)
+            if (!encode_bf16(dst[i], src[i], 3, dims, strides, box)) return cudaErrorInvalidValue;
+        const int64_t n_rec = pd.n_chunks * H;
+        const cuuint64_t rdims[2] = {64, static_cast<cuuint64_t>(n_rec * (kRecBytes / 128))};
+        const cuuint64_t rstrides[1] = {128};
+        const cuuint32_t rbox[2] = {64, 64};
+        if (!encode_bf16(&maps.rec_t, p.f.chunk_states, 2, rdims, rstrides, rbox)) return cudaErrorInvalidValue;
+    }
+    kda_bwd_state_tc<<<n_items, NT, bws_sm::bytes, st>>>(p, pd, base, maps);
     return cudaGetLastError();
 }
 
