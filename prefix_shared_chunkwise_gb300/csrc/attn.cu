@@ -60,11 +60,6 @@ struct AttnParams {
     float scale;
 };
 
-// 16-byte piece p of row r of a [128 rows][128 cols] SW128 tile.
-__device__ __forceinline__ uint32_t piece(int r, int p) {
-    return static_cast<uint32_t>((p >> 3) * 16384 + r * 128 + (((p & 7) ^ (r & 7)) << 4));
-}
-
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -425,18 +420,6 @@ constexpr uint32_t Q = 0, dO = 32768, K0 = 65536, K1 = 98304, V = 131072, dS = 1
 constexpr uint32_t bytes = 196608 + 1024;
 }  // namespace bq_sm
 
-// Stage rows first .. first + n - 1 (zeros for the rest of the tile).
-__device__ __forceinline__ void stage_run(const __nv_bfloat16 *src, int64_t first, int n, int H, int h, uint8_t *dst,
-                                          int tid) {
-#pragma unroll
-    for (int i = 0; i < AT * 16 / ANT; ++i) {
-        const int e = tid + i * ANT, r = e >> 4, pc = e & 15;
-        const bool ok = r < n;
-        const __nv_bfloat16 *g = src + ((first + (ok ? r : 0)) * H + h) * AD + pc * 8;
-        tc::cp_async16(dst + piece(r, pc), g, ok ? 16u : 0u);
-    }
-}
-
 __device__ __forceinline__ void store_tile_bf16(__nv_bfloat16 *dst_row, const float (&r)[32], float mul) {
     uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
 #pragma unroll
@@ -572,11 +555,12 @@ constexpr uint32_t Vec = 229376;                  // [128] lse, [128] D of the c
 constexpr uint32_t bytes = Vec + 1024 + 1024;     // 226 KB with the alignment slack
 }  // namespace bk_sm
 
-__global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, PlanDev pd) {
+__global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, PlanDev pd,
+                                                            const __grid_constant__ AttnMaps maps) {
     using namespace bk_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    __shared__ uint64_t bars[3];                  // S^T and dP^T ready, dV done, dK done
+    __shared__ uint64_t bars[6];                  // S^T and dP^T ready, dV done, dK done, K and V, Q and dO x 2
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
     float *slse = reinterpret_cast<float *>(sm + Vec), *sD = slse + AT;
@@ -596,11 +580,18 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
         nq = min(AT, pd.seq_nown[s_] - t_ * AT);
         qoff = t_ * AT - k0;                          // query local position minus key tile start
     };
+    // thread 0: Q and dO of entry e (128 rows from the tile's first; rows past the tile are
+    // masked, rows past the tensor read zeros) by tiled TMA into buffer bb
     auto stage_q = [&](int32_t e, int bb) {
         int64_t qr; int nq; int32_t qoff, f;
         entry(e, qr, nq, qoff, f);
-        stage_run(p.q, qr, nq, H, h, sm + (bb ? Q1 : Q0), tid);
-        stage_run(p.dout, qr, nq, H, h, sm + (bb ? dO1 : dO0), tid);
+        uint64_t *bar = &bars[4 + bb];
+        tc::mbar_expect_tx(bar, 65536);
+        uint8_t *dq_ = sm + (bb ? Q1 : Q0), *dd = sm + (bb ? dO1 : dO0);
+        tc::tma_load_3d(dq_, &maps.q, 0, h, static_cast<int>(qr), bar);
+        tc::tma_load_3d(dq_ + 16384, &maps.q, 64, h, static_cast<int>(qr), bar);
+        tc::tma_load_3d(dd, &maps.dout, 0, h, static_cast<int>(qr), bar);
+        tc::tma_load_3d(dd + 16384, &maps.dout, 64, h, static_cast<int>(qr), bar);
     };
     auto stage_vec = [&](int32_t e) {
         int64_t qr; int nq; int32_t qoff, f;
@@ -613,7 +604,7 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
     };
 
     if (tid == 0) {
-        for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 6; ++i) tc::mbar_init(&bars[i], 1);
         tc::fence_mbar_init();
         s_fail = 0;
     }
@@ -621,9 +612,14 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
         tc::tmem_alloc(&s_tmem, 512);
         tc::fence_before_sync();
     }
-    stage_run(p.k, krow0, nk, H, h, sm + K, tid);
-    stage_run(p.v, krow0, nk, H, h, sm + V, tid);
-    stage_q(0, 0);
+    if (tid == 0) {
+        tc::mbar_expect_tx(&bars[3], 65536);
+        tc::tma_load_3d(sm + K, &maps.k[4], 0, h, static_cast<int>(krow0), &bars[3]);
+        tc::tma_load_3d(sm + K + 16384, &maps.k[4], 64, h, static_cast<int>(krow0), &bars[3]);
+        tc::tma_load_3d(sm + V, &maps.v[4], 0, h, static_cast<int>(krow0), &bars[3]);
+        tc::tma_load_3d(sm + V + 16384, &maps.v[4], 64, h, static_cast<int>(krow0), &bars[3]);
+        stage_q(0, 0);
+    }
     stage_vec(0);
     tc::cp_async_commit();
     __syncthreads();
@@ -632,11 +628,19 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
     const uint32_t tS = tm, tP = tm + 128, tV = tm + 256, tK = tm + 384;
     const int krow = lg * 32 + lane;                 // this thread's key row (TMEM lane)
     uint32_t nc0 = 0, nc1 = 0, nc2 = 0;             // thread 0: commits per barrier
+    int32_t q_issued = 0, q_waited = -1;             // thread 0: last entry whose Q / dO were issued, awaited
+    bool kv_waited = false;
 
     for (int32_t e = 0; e < n_e; ++e) {
         const int b = e & 1;
         tc::cp_async_wait_all();
         sync_mma();
+        if (tid == 0) {
+            if (e == 0) { wait_or_fail(&bars[3], 0, 2, &s_fail); kv_waited = true; }
+            wait_or_fail(&bars[4 + b], (e >> 1) & 1, 2, &s_fail);
+            q_waited = e;
+            tc::fence_after_sync();
+        }
         if (tid == 0 && !*reinterpret_cast<volatile int *>(&s_fail)) {
             tc::mma_op(tS, tc::Opnd{tc::smem_addr(sm + K), 16384, false},
                        tc::Opnd{tc::smem_addr(sm + (b ? Q1 : Q0)), 16384, false}, AT, AT, AD, false);
@@ -654,8 +658,7 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
         tc::tmem_ld32(tP + lane_off + cq * 32, pv);
         if (e > 0) wait_or_fail(&bars[2], (e - 1) & 1, 2, &s_fail);      // dK_{e-1}: PT, Q, dO free
         tc::fence_after_sync();
-        if (e + 1 < n_e) stage_q(e + 1, b ^ 1);
-        tc::cp_async_commit();
+        if (tid == 0 && e + 1 < n_e) { stage_q(e + 1, b ^ 1); q_issued = e + 1; }
         // P^T and dS^T for this thread's key row and 32 query columns
         const float *lq = slse + cq * 32, *dq_ = sD + cq * 32;
 #pragma unroll
@@ -700,6 +703,10 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
         if (krow < nk) store_tile_bf16(p.dk + ((krow0 + krow) * H + h) * AD + cq * 32, r, 1.f);
     }
     tc::cp_async_wait_all();
+    if (tid == 0) {                                   // copies issued but never awaited (a timeout)
+        if (!kv_waited) tc::mbar_wait(&bars[3], 0, 1000000000LL);
+        if (q_issued > q_waited) tc::mbar_wait(&bars[4 + (q_issued & 1)], (q_issued >> 1) & 1, 1000000000LL);
+    }
     if (s_fail && tid == 0) {
         dev_error(pd, kDevErrTimeout, sk, h);
         const uint32_t nc[3] = {nc0, nc1, nc2};
@@ -832,7 +839,7 @@ int harts_attn_bwd(const harts_plan *P, const harts_attn_bwd_args *a, harts_stre
                        P->view, maps);
     if (e == cudaSuccess)
         e = launch_big(attn_bwd_dkdv_tc, static_cast<unsigned>(int64_t(P->image.n_kt) * p.H), ANT, bk_sm::bytes, st, p,
-                       P->view);
+                       P->view, maps);
     if (e != cudaSuccess) { set_error(std::string("attention backward launch: ") + cudaGetErrorString(e)); return HARTS_ECUDA; }
     set_error("");
     return HARTS_OK;
