@@ -156,6 +156,14 @@ int harts_plan_device_error(harts_plan *plan, harts_stream_t stream, int32_t *co
 
 void harts_plan_free(harts_plan *plan);
 
+/* Self-test of the device failure path (for tests of error reporting): one thread waits on
+ * a barrier that nothing completes, gives up after max_cycles SM cycles (1 .. 1e8) and
+ * records device code 3 (timeout) in the plan's error word, the way every kernel of the
+ * library reports a wait that ran out; harts_plan_device_error then returns HARTS_EDEVICE
+ * and the context stays usable.  Never traps.  Errors: HARTS_EINVAL, HARTS_ENOPLAN,
+ * HARTS_ECUDA. */
+int harts_selftest_timeout(harts_plan *plan, uint32_t max_cycles, harts_stream_t stream);
+
 /* ------------------------------------------------------------------------------ */
 /* Forward: one packed call per round (section 4.3, "KDA").                       */
 /* ------------------------------------------------------------------------------ */

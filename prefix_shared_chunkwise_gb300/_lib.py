@@ -21,7 +21,7 @@ ERRORS = {0: "HARTS_OK", -1: "HARTS_EINVAL", -2: "HARTS_EUNSUPPORTED", -3: "HART
 
 EXPORTED = [
     "harts_plan_calls", "harts_plan_get_info", "harts_plan_export", "harts_plan_device_bytes",
-    "harts_plan_upload", "harts_plan_device_error", "harts_plan_free",
+    "harts_plan_upload", "harts_plan_device_error", "harts_plan_free", "harts_selftest_timeout",
     "harts_kda_chunk_state_bytes", "harts_kda_fwd", "harts_kda_bwd_workspace_bytes",
     "harts_kda_bwd", "harts_kda_bwd_state", "harts_kda_bwd_grad", "harts_kda_bwd_static",
     "harts_kda_bwd_static_max_bytes", "harts_conv_fwd", "harts_conv_bwd_workspace_bytes",
@@ -121,6 +121,8 @@ def lib():
         L.harts_plan_device_error.argtypes = [_vp, _vp, _pi32]
         L.harts_plan_free.argtypes = [_vp]
         L.harts_plan_free.restype = None
+        L.harts_selftest_timeout.argtypes = [_vp, ctypes.c_uint32, _vp]
+        L.harts_selftest_timeout.restype = ctypes.c_int
         L.harts_kda_chunk_state_bytes.argtypes = [_vp, _i32, _i32, _i32, _i32]
         L.harts_kda_chunk_state_bytes.restype = ctypes.c_size_t
         L.harts_kda_fwd.argtypes = [_vp, ctypes.POINTER(FwdArgs), _vp]

@@ -3,6 +3,7 @@
 #include <mutex>
 
 #include "kda_common.cuh"
+#include "tc_primitives.cuh"
 
 namespace harts {
 
@@ -86,6 +87,24 @@ BwdWs bwd_ws(const harts_plan *P, int32_t H, int32_t D, bool tc) {
 
 using namespace harts;
 
+namespace harts {
+namespace {
+
+// The library's bounded-wait failure path, on its own: one thread waits on an mbarrier
+// that nothing completes, gives up after max_cycles and records device code 3 (timeout)
+// in the plan's error word, as every kernel of the library does when a wait runs out.
+__global__ void selftest_timeout_kernel(PlanDev pd, uint32_t max_cycles) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+        if (!tc::mbar_wait(&bar, 0, static_cast<long long>(max_cycles))) dev_error(pd, kDevErrTimeout, -1, -1);
+    }
+}
+
+}  // namespace
+}  // namespace harts
+
 extern "C" {
 
 int harts_plan_upload(harts_plan *P, void *dev_buf, size_t bytes, harts_stream_t stream) {
@@ -144,6 +163,17 @@ int harts_plan_device_error(harts_plan *P, harts_stream_t stream, int32_t *code)
                   ", pos " + std::to_string(host[2]) + ")");
         return HARTS_EDEVICE;
     }
+    return HARTS_OK;
+}
+
+int harts_selftest_timeout(harts_plan *P, uint32_t max_cycles, harts_stream_t stream) {
+    if (!P) { set_error("NULL plan"); return HARTS_EINVAL; }
+    if (!P->dev) { set_error("plan not uploaded"); return HARTS_ENOPLAN; }
+    if (max_cycles == 0 || max_cycles > 100000000u) { set_error("max_cycles must be in 1 .. 1e8"); return HARTS_EINVAL; }
+    selftest_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(P->view, max_cycles);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    set_error("");
     return HARTS_OK;
 }
 
