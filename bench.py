@@ -229,6 +229,15 @@ def oracle_sample(parent, seg_len, seg_offset, inputs, H_sample, B, target_S):
     return st["C"], H_sample, dt, min(threads, H_sample), st
 
 
+def oracle_rate(step, budget_s=4.0, max_units=10_000):
+    """Call `step()` (which runs the oracle on one sampled unit and returns the units it
+    processed) until `budget_s` seconds have passed; returns (units, seconds)."""
+    units, t0 = 0, time.time()
+    while time.time() - t0 < budget_s and units < max_units:
+        units += step()
+    return units, time.time() - t0
+
+
 # ---- our arm -----------------------------------------------------------------------------
 
 def run_ours(args):
@@ -588,7 +597,27 @@ def run_logprob(hbm):
     tf = timed(lambda: logprob_fwd(z, rp, rs, target, lse=lse, logp=logp))
     tb = timed(lambda: logprob_bwd(z, rp, rs, target, lse, dl, dlogits=dz))
     fb, bb = C * V * 2, 2 * C * V * 2
-    out = dict(C=C, S=S, V=V, vocab_work_saved=round(S / C, 3),
+    # the oracle beside it: forward + backward on sampled compact rows with their positions
+    import numpy as np
+    from oracle import logprob as olp
+    rng = np.random.default_rng(0)
+    tg, dlh = target.cpu().numpy(), dl.cpu().numpy()
+
+    def some_rows():
+        cs = rng.integers(0, C, size=8)
+        zc = z[torch.as_tensor(cs, device=dev)].double().cpu().numpy()
+        pos = [row_sem[row_ptr[c]:row_ptr[c + 1]] for c in cs]
+        sr = np.concatenate([np.full(len(pp), j) for j, pp in enumerate(pos)]).astype(np.int64)
+        pp = np.concatenate(pos).astype(np.int64)
+        olp.logprob_fwd(zc, sr, tg[pp])
+        olp.logprob_bwd(zc, sr, tg[pp], dlh[pp])
+        return len(cs)
+
+    n_o, t_o = oracle_rate(some_rows)
+    oracle_leg = dict(value=round(n_o / t_o, 2), unit="compact rows/s (fwd + bwd, V = 157,184)",
+                      gpu=round(C / ((tf + tb) / 1e3), 1), cores=len(os.sched_getaffinity(0)), kind="oracle",
+                      sample=f"{n_o} uniformly drawn rows with their semantic positions, {t_o:.1f} s")
+    out = dict(C=C, S=S, V=V, vocab_work_saved=round(S / C, 3), oracle=oracle_leg,
                fwd=dict(ms=round(tf, 3), gb_s=round(fb / tf / 1e6, 1), frac=round(fb / tf / 1e6 / hbm, 3)),
                bwd=dict(ms=round(tb, 3), gb_s=round(bb / tb / 1e6, 1), frac=round(bb / tb / 1e6 / hbm, 3)),
                peak_gb_s=hbm)
@@ -659,7 +688,27 @@ def run_attn(parent, seg_len, pl, x, tf_peak):
     flops = 4.0 * d * H * pairs
     flops_b = 10.0 * d * H * pairs                   # S, dP, dV, dQ, dK: 2 d each per pair
     tile_flops = 4.0 * d * H * tiles * 128 * 128
-    return dict(shape=[C, H, d], ms=round(ms, 3), visible_pairs=int(pairs),
+    # the oracle beside it: forward + backward of uniformly sampled compact rows over their
+    # trajectory prefixes (all heads), fp64 on the host
+    from oracle import attn as oattn
+    rng = np.random.default_rng(0)
+    so = a["seg_offset"]
+
+    def one_row():
+        r = int(rng.integers(0, C))
+        view = oattn.trajectory_prefix(parent, seg_len, so, r)
+        idx = torch.as_tensor(view, device=o.device)
+        qq = x["q"][r].double().cpu().numpy()
+        kk, vv = x["k"][idx].double().cpu().numpy(), x["v"][idx].double().cpu().numpy()
+        oattn.attn_query(qq, kk, vv, d ** -0.5)
+        oattn.attn_query_bwd(qq, kk, vv, do[r].double().cpu().numpy(), d ** -0.5)
+        return 1
+
+    n_o, t_o = oracle_rate(one_row)
+    oracle_leg = dict(value=round(n_o / t_o, 2), unit="compact query rows/s (fwd + bwd, all heads)",
+                      gpu=round(C / ((ms + ms_b) / 1e3), 1), cores=len(os.sched_getaffinity(0)), kind="oracle",
+                      sample=f"{n_o} uniformly drawn rows of the forest, {t_o:.1f} s")
+    return dict(shape=[C, H, d], ms=round(ms, 3), visible_pairs=int(pairs), oracle=oracle_leg,
                 tflops=round(flops / ms / 1e9, 1), frac=round(flops / ms / 1e9 / tf_peak, 4),
                 tile_tflops=round(tile_flops / ms / 1e9, 1), tile_util=round(pairs * H / (tiles * 128 * 128 * H), 3),
                 bwd=dict(ms=round(ms_b, 3), tflops=round(flops_b / ms_b / 1e9, 1),
@@ -703,7 +752,35 @@ def run_conv(pl, x, wl, hbm):
     tb = timed(lambda: conv_bwd(pl, xx, W, b, dy, activation="silu", dx=dx, dweight=dW, dbias=db))
     elem = C * ch * xx.element_size()
     fb, bb = 2 * elem, 3 * elem
-    return dict(shape=[C, ch], width=4, activation="silu",
+    # the oracle beside it: forward + backward over one tree of the forest, 256 channels at
+    # a time until the time budget is spent
+    import numpy as np
+    from oracle import conv as oconv
+    from prefix_shared_chunkwise_gb300.synth import make_tree
+    parent, seg_len = make_tree(wl.name)
+    ids, sub_parent, st = pick_sample_tree(parent, seg_len, 4000)
+    so = pl.arrays()["seg_offset"]
+    rows = np.concatenate([np.arange(so[v], so[v] + seg_len[v]) for v in ids])
+    sub_off = np.concatenate([[0], np.cumsum(seg_len[ids])[:-1]]).astype(np.int64)
+    idx = torch.as_tensor(rows, device=xx.device)
+    xs_all, dys_all = xx.index_select(0, idx), dy.index_select(0, idx)
+    blk = [0]
+
+    def one_block():
+        c0 = (blk[0] * 256) % ch
+        blk[0] += 1
+        xs = xs_all[:, c0:c0 + 256].double().cpu().numpy()
+        dys = dys_all[:, c0:c0 + 256].double().cpu().numpy()
+        Ws, bs = W[c0:c0 + 256].double().cpu().numpy(), b[c0:c0 + 256].double().cpu().numpy()
+        oconv.conv_forest(sub_parent, seg_len[ids], sub_off, xs, Ws, bs, act="silu")
+        oconv.conv_forest_bwd(sub_parent, seg_len[ids], sub_off, xs, Ws, bs, "silu", dys)
+        return len(rows) * 256
+
+    n_o, t_o = oracle_rate(one_block, budget_s=3.0, max_units=10 ** 12)
+    oracle_leg = dict(value=round(n_o / t_o, 1), unit="row-channels/s (fwd + bwd)",
+                      gpu=round(C * ch / ((tf + tb) / 1e3), 1), cores=1, kind="oracle",
+                      sample=f"one tree ({len(rows)} compact rows) x {n_o // len(rows)} channels, {t_o:.1f} s")
+    return dict(shape=[C, ch], width=4, activation="silu", oracle=oracle_leg,
                 fwd=dict(ms=round(tf, 3), gb_s=round(fb / tf / 1e6, 1), frac=round(fb / tf / 1e6 / hbm, 3)),
                 bwd=dict(ms=round(tb, 3), gb_s=round(bb / tb / 1e6, 1), frac=round(bb / tb / 1e6 / hbm, 3)),
                 peak_gb_s=hbm)
