@@ -16,6 +16,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import subprocess
 import sys
 import tempfile
@@ -260,7 +261,15 @@ def run_ours(args):
     wl = WORKLOADS[args.workload]
     H, D, B = wl.H, wl.dk, wl.chunk
     parent, seg_len, seed = forest_for_rank(args.workload, rank)
-    pl = Plan(parent, seg_len, B).upload()
+    # planning (host) and plan upload, reported apart from the kernels' time
+    t_pl = time.perf_counter()
+    pl = Plan(parent, seg_len, B)
+    plan_ms = (time.perf_counter() - t_pl) * 1e3
+    torch.cuda.synchronize()
+    t_up = time.perf_counter()
+    pl.upload()
+    torch.cuda.synchronize()
+    upload_ms = (time.perf_counter() - t_up) * 1e3
     info = pl.info
     C = info["C"]
     x = make_inputs(C, H, D, D, wl.dtype, seed=3 + rank, device="cuda")
@@ -440,7 +449,7 @@ def run_ours(args):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         c_s, h_s, dt, thr, st = oracle_sample(parent, seg_len, pl.arrays()["seg_offset"], x, H, B,
                                               target_S=12000)
-        cpu = dict(value=round(c_s / dt, 2), unit=UNIT, cores=thr, kind="oracle",
+        cpu = dict(value=round(c_s / dt, 2), unit=UNIT, cores=thr, kind="oracle", arch=platform.machine(),
                    sample=f"one tree of the forest ({c_s} compact / {st['S']} expanded tokens, "
                           f"all {h_s} heads), fp64 token recurrence fwd+bwd, {dt:.1f} s")
 
@@ -454,6 +463,7 @@ def run_ours(args):
                                 parallelism=f"dp{ws} (one forest per GPU)",
                                 l2=f"inputs larger than L2 (each input tensor {C * H * D * 2 / 1e9:.2f} GB)"),
                     phases_ms={k: round(v, 3) for k, v in phase_ms.items()},
+                    host_ms=dict(plan=round(plan_ms, 3), upload=round(upload_ms, 3)),
                     gpu_launches=K * (2 * info["n_rounds"] + 1 + (1 if info["n_fold_rows"] else 0)),
                     roofline=roofline, cpu_baseline=cpu, e2e=e2e, clocks=clk)
         if expanded:
