@@ -41,13 +41,15 @@ constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;               // running max moves when a row max grows by more
 
 namespace at_sm {
-constexpr uint32_t Q = 0, K0 = 32768, K1 = 65536, V0 = 98304, V1 = 131072, P = 163840;
+constexpr uint32_t Q = 0, K0 = 32768, V0 = 131072;    // K ring: 3 slots of 32 KB; V ring: 2 slots
 constexpr uint32_t Max = 196608;                  // [2 tiles][2 halves][128] fp32 row maxima
 constexpr uint32_t Sum = Max + 2048;              // [2 halves][128] fp32 row sums
 constexpr uint32_t bytes = Sum + 1024 + 1024;     // + alignment slack
 }  // namespace at_sm
 
-// Roles of the forward's 13 warps.
+constexpr int kKSlots = 3;
+
+// Roles of the forward's 11 warps.
 constexpr int kFwdSoftmaxWarps = 8, kFwdMmaWarp = 8, kFwdLoadWarp0 = 9, kFwdLoadWarps = 2;
 constexpr int kFwdThreads = (kFwdLoadWarp0 + kFwdLoadWarps) * 32;
 constexpr int kSoftThreads = kFwdSoftmaxWarps * 32;
@@ -148,7 +150,20 @@ __device__ __forceinline__ uint32_t view_bits(const PlanDev &pd, int32_t sq, int
 }
 
 // Barriers of the forward (index into bars[]).
-enum FwdBar { bQ = 0, bKF = 1, bKE = 3, bVF = 5, bVE = 7, bSF = 9, bSE = 11, bPF = 13, bOD = 14, bN = 15 };
+enum FwdBar { bQ = 0, bKF = 1, bKE = 4, bVF = 7, bVE = 9, bSF = 11, bPF = 13, bOD = 14, bN = 15 };
+
+// O (+)= P V with P (bf16, packed in pairs) read from TMEM: one row per lane, 8 columns per
+// 16 keys.
+__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_saddr, bool accumulate) {
+    const uint32_t id = tc::idesc_bf16(AT, AD, false, true);
+    for (int kk = 0; kk < AT / 16; ++kk) {
+        const uint64_t bd = tc::desc_sw128_mn(v_saddr + kk * 2048, 16384);
+        const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                     :: "r"(d_tmem), "r"(p_tmem + kk * 8), "l"(bd), "r"(id), "r"(acc) : "memory");
+    }
+}
 
 __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, PlanDev pd,
                                                                 const __grid_constant__ AttnMaps maps) {
@@ -169,13 +184,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
 
     if (tid == 0) {
         tc::mbar_init(&bars[bQ], 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kKSlots; ++i) {
             tc::mbar_init(&bars[bKF + i], 1);
-            tc::mbar_init(&bars[bVF + i], 1);
             tc::mbar_init(&bars[bKE + i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&bars[bVF + i], 1);
             tc::mbar_init(&bars[bVE + i], 1);
             tc::mbar_init(&bars[bSF + i], 1);
-            tc::mbar_init(&bars[bSE + i], kSoftThreads);
         }
         tc::mbar_init(&bars[bPF], kSoftThreads);
         tc::mbar_init(&bars[bOD], 1);
@@ -200,17 +216,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
                 tc::tma_load_3d(sm + Q, &maps.q, 0, h, row0 + q0, &bars[bQ]);
                 tc::tma_load_3d(sm + Q + 16384, &maps.q, 64, h, row0 + q0, &bars[bQ]);
             }
+            const int nslot = is_v ? 2 : kKSlots;
             for (int32_t kt = 0; kt < n_kt; ++kt) {
-                const int b = kt & 1;
-                if (kt >= 2) wait_or_fail(&bars[(is_v ? bVE : bKE) + b], ((kt - 2) >> 1) & 1, 2, &s_fail);
+                const int b = kt % nslot, use = kt / nslot;
+                if (use > 0) wait_or_fail(&bars[(is_v ? bVE : bKE) + b], (use - 1) & 1, 2, &s_fail);
                 uint64_t *full = &bars[(is_v ? bVF : bKF) + b];
                 tc::mbar_expect_tx(full, 32768);
-                tma_view_tile(is_v ? maps.v : maps.k, sm + (is_v ? (b ? V1 : V0) : (b ? K1 : K0)), pd, sq, kt, h, ri,
-                              full);
+                tma_view_tile(is_v ? maps.v : maps.k, sm + (is_v ? V0 : K0) + b * 32768, pd, sq, kt, h, ri, full);
             }
         }
     } else if (warp == kFwdMmaWarp) {
-        // ---- one thread issues every product: S_{j+1} ahead of O_j
+        // ---- one thread issues every product: S_{j+1} ahead of O_j; P_j is read from
+        // TMEM (it overwrote S_j there), so S_{j+2} waits for O_j to complete
         if (lane == 0) {
             const tc::Opnd aQ{tc::smem_addr(sm + Q), 16384, false};
             uint32_t nc_s0 = 0, nc_s1 = 0, nc_o = 0;
@@ -226,22 +243,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
             for (int32_t kt = 0; kt < n_kt && !failed(&s_fail); ++kt) {
                 const int b = kt & 1, nb = b ^ 1;
                 if (kt + 1 < n_kt) {
-                    wait_or_fail(&bars[bKF + nb], ((kt + 1) >> 1) & 1, 0, &s_fail);
-                    if (kt >= 1) wait_or_fail(&bars[bSE + nb], ((kt - 1) >> 1) & 1, 1, &s_fail);
+                    const int ks = (kt + 1) % kKSlots;
+                    wait_or_fail(&bars[bKF + ks], ((kt + 1) / kKSlots) & 1, 0, &s_fail);
+                    if (kt >= 1) wait_or_fail(&bars[bOD], (kt - 1) & 1, 1, &s_fail);   // O_{kt-1} read P there
                     tc::fence_after_sync();
                     if (failed(&s_fail)) break;
-                    tc::mma_op(tm + nb * 128, aQ, tc::Opnd{tc::smem_addr(sm + (nb ? K1 : K0)), 16384, false},
+                    tc::mma_op(tm + nb * 128, aQ, tc::Opnd{tc::smem_addr(sm + K0 + ks * 32768), 16384, false},
                                AT, AT, AD, false);
                     tc::mma_commit(&bars[bSF + nb]);
-                    tc::mma_commit(&bars[bKE + nb]);
+                    tc::mma_commit(&bars[bKE + ks]);
                     if (nb) ++nc_s1; else ++nc_s0;
                 }
                 wait_or_fail(&bars[bPF], kt & 1, 1, &s_fail);
                 wait_or_fail(&bars[bVF + b], (kt >> 1) & 1, 0, &s_fail);
                 tc::fence_after_sync();
                 if (failed(&s_fail)) break;
-                tc::mma_op(tO, tc::Opnd{tc::smem_addr(sm + P), 16384, false},
-                           tc::Opnd{tc::smem_addr(sm + (b ? V1 : V0)), 16384, true}, AT, AD, AT, kt > 0);
+                mma_pv(tO, tm + b * 128, tc::smem_addr(sm + V0 + b * 32768), kt > 0);
                 tc::mma_commit(&bars[bOD]);
                 tc::mma_commit(&bars[bVE + b]);
                 ++nc_o;
@@ -283,8 +300,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[32 + i] = r[i];
             }
-            tc::fence_before_sync();
-            mbar_arrive(&bars[bSE + b]);                 // S buffer may be overwritten
             const int32_t lim = vis - (kt * AT + half * 64);
             if (__any_sync(0xffffffffu, (vb0 & vb1) != 0xffffffffu || lim < 63)) {
 #pragma unroll
@@ -303,7 +318,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
 #pragma unroll
                 for (int i = 0; i < w; ++i) mp[i] = fmaxf(mp[i], mp[i + w]);
             smax[(b * 2 + half) * AT + qrow] = mp[0];
+            tc::fence_before_sync();                     // both halves' reads of S precede P's writes
             asm volatile("bar.sync %0, 64;" :: "r"(1 + lg) : "memory");   // the row's two warps
+            tc::fence_after_sync();
             const float m_tile = c * fmaxf(smax[(b * 2) * AT + qrow], smax[(b * 2 + 1) * AT + qrow]);
             const bool move = __any_sync(0xffffffffu, m_tile > m_run + kRescaleLog2);
             float alpha = 1.f;
@@ -323,11 +340,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
 #pragma unroll
                 for (int i = 0; i < w; ++i) sp[i] += sp[i + w];
             l_half = l_half * alpha + sp[0];
-            if (kt > 0) wait_or_fail(&bars[bOD], (kt - 1) & 1, 1, &s_fail);   // P free, O settled
-            tc::fence_after_sync();
+            {
+                // P_kt (bf16 pairs) over this half's 32 columns of S_kt's buffer; the row's
+                // other half finished reading S before the max exchange above
+                float w[32];
+                uint32_t *u = reinterpret_cast<uint32_t *>(w);
 #pragma unroll
-            for (int i = 0; i < 64; i += 8) tc::st_sw128_8(sm + P, AT, qrow, half * 64 + i, s + i);
+                for (int i = 0; i < 32; ++i) u[i] = tc::pack_bf16(s[2 * i], s[2 * i + 1]);
+                tc::tmem_st32(tm + b * 128 + lane_off + half * 32, w);
+            }
             if (move && kt > 0) {
+                wait_or_fail(&bars[bOD], (kt - 1) & 1, 1, &s_fail);    // O settled before its rescale
+                tc::fence_after_sync();
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     float r[32];
@@ -337,7 +361,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
                     tc::tmem_st32(tO + lane_off + half * 64 + hf * 32, r);
                 }
             }
-            tc::fence_smem_to_async();
             tc::fence_before_sync();
             mbar_arrive(&bars[bPF]);
         }
