@@ -154,6 +154,17 @@ enum FwdBar { bQ = 0, bKF = 1, bKE = 4, bVF = 7, bVE = 9, bSF = 11, bPF = 13, bO
 
 // O (+)= P V with P (bf16, packed in pairs) read from TMEM: one row per lane, 8 columns per
 // 16 keys.
+// 16 columns of one TMEM lane per thread (warp-collective), then wait for the stores.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&u)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        :: "r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]),
+           "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_saddr, bool accumulate) {
     const uint32_t id = tc::idesc_bf16(AT, AD, false, true);
     for (int kk = 0; kk < AT / 16; ++kk) {
@@ -573,9 +584,9 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDe
 }
 
 namespace bk_sm {
-constexpr uint32_t K = 0, V = 32768, Q0 = 65536, Q1 = 98304, dO0 = 131072, dO1 = 163840, PT = 196608;
-constexpr uint32_t Vec = 229376;                  // [128] lse, [128] D of the current query tile
-constexpr uint32_t bytes = Vec + 1024 + 1024;     // 226 KB with the alignment slack
+constexpr uint32_t K = 0, V = 32768, Q0 = 65536, Q1 = 98304, dO0 = 131072, dO1 = 163840;
+constexpr uint32_t Vec = 196608;                  // [128] lse, [128] D of the current query tile
+constexpr uint32_t bytes = Vec + 1024 + 1024;
 }  // namespace bk_sm
 
 __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, PlanDev pd,
@@ -583,7 +594,7 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
     using namespace bk_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    __shared__ uint64_t bars[6];                  // S^T and dP^T ready, dV done, dK done, K and V, Q and dO x 2
+    __shared__ uint64_t bars[6];                  // S^T and dP^T ready, (unused), dV and dK done, K and V, Q and dO x 2
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
     float *slse = reinterpret_cast<float *>(sm + Vec), *sD = slse + AT;
@@ -650,7 +661,7 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
     const uint32_t tm = s_tmem, lane_off = static_cast<uint32_t>(lg * 32) << 16;
     const uint32_t tS = tm, tP = tm + 128, tV = tm + 256, tK = tm + 384;
     const int krow = lg * 32 + lane;                 // this thread's key row (TMEM lane)
-    uint32_t nc0 = 0, nc1 = 0, nc2 = 0;             // thread 0: commits per barrier
+    uint32_t nc0 = 0, nc2 = 0;                      // thread 0: commits per barrier
     int32_t q_issued = 0, q_waited = -1;             // thread 0: last entry whose Q / dO were issued, awaited
     bool kv_waited = false;
 
@@ -662,15 +673,19 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
             if (e == 0) { wait_or_fail(&bars[3], 0, 2, &s_fail); kv_waited = true; }
             wait_or_fail(&bars[4 + b], (e >> 1) & 1, 2, &s_fail);
             q_waited = e;
+            // dV_{e-1} and dK_{e-1} read P^T and dS^T where S^T and dP^T go next, and Q, dO
+            // of the other buffer
+            if (e > 0) wait_or_fail(&bars[2], (e - 1) & 1, 2, &s_fail);
             tc::fence_after_sync();
-        }
-        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s_fail)) {
-            tc::mma_op(tS, tc::Opnd{tc::smem_addr(sm + K), 16384, false},
-                       tc::Opnd{tc::smem_addr(sm + (b ? Q1 : Q0)), 16384, false}, AT, AT, AD, false);
-            tc::mma_op(tP, tc::Opnd{tc::smem_addr(sm + V), 16384, false},
-                       tc::Opnd{tc::smem_addr(sm + (b ? dO1 : dO0)), 16384, false}, AT, AT, AD, false);
-            tc::mma_commit(&bars[0]);
-            ++nc0;
+            if (!failed(&s_fail)) {
+                tc::mma_op(tS, tc::Opnd{tc::smem_addr(sm + K), 16384, false},
+                           tc::Opnd{tc::smem_addr(sm + (b ? Q1 : Q0)), 16384, false}, AT, AT, AD, false);
+                tc::mma_op(tP, tc::Opnd{tc::smem_addr(sm + V), 16384, false},
+                           tc::Opnd{tc::smem_addr(sm + (b ? dO1 : dO0)), 16384, false}, AT, AT, AD, false);
+                tc::mma_commit(&bars[0]);
+                ++nc0;
+            }
+            if (e + 1 < n_e) { stage_q(e + 1, b ^ 1); q_issued = e + 1; }
         }
         int64_t qr; int nq; int32_t qoff, f;
         entry(e, qr, nq, qoff, f);
@@ -679,41 +694,48 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
         float sv[32], pv[32];
         tc::tmem_ld32(tS + lane_off + cq * 32, sv);
         tc::tmem_ld32(tP + lane_off + cq * 32, pv);
-        if (e > 0) wait_or_fail(&bars[2], (e - 1) & 1, 2, &s_fail);      // dK_{e-1}: PT, Q, dO free
-        tc::fence_after_sync();
-        if (tid == 0 && e + 1 < n_e) { stage_q(e + 1, b ^ 1); q_issued = e + 1; }
         // P^T and dS^T for this thread's key row and 32 query columns
         const float *lq = slse + cq * 32, *dq_ = sD + cq * 32;
+        uint32_t up[16], ud[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int qc = cq * 32 + i;
-            const bool vis = qc < nq && (f < 0 ? krow <= qoff + qc : k0 + krow < f);
-            const float pr = vis ? ex2(fmaf(sv[i], c, -lq[i] * kLog2e)) : 0.f;
-            sv[i] = pr;
-            pv[i] = p.scale * pr * (pv[i] - dq_[i]);
-        }
+        for (int i = 0; i < 32; i += 2) {
+            float pr[2], ds[2];
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) tc::st_sw128_8(sm + PT, AT, krow, cq * 32 + i, sv + i);
-        sync_mma();
-        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s_fail)) {
-            tc::mma_op(tV, tc::Opnd{tc::smem_addr(sm + PT), 16384, false},
-                       tc::Opnd{tc::smem_addr(sm + (b ? dO1 : dO0)), 16384, true}, AT, AD, AT, e > 0);
-            tc::mma_commit(&bars[1]);
-            ++nc1;
+            for (int u = 0; u < 2; ++u) {
+                const int qc = cq * 32 + i + u;
+                const bool vis = qc < nq && (f < 0 ? krow <= qoff + qc : k0 + krow < f);
+                pr[u] = vis ? ex2(fmaf(sv[i + u], c, -lq[i + u] * kLog2e)) : 0.f;
+                ds[u] = p.scale * pr[u] * (pv[i + u] - dq_[i + u]);
+            }
+            up[i / 2] = tc::pack_bf16(pr[0], pr[1]);
+            ud[i / 2] = tc::pack_bf16(ds[0], ds[1]);
         }
-        if (e + 1 < n_e) stage_vec(e + 1);              // every thread has read this tile's lse, D
-        tc::cp_async_commit();
-        wait_or_fail(&bars[1], e & 1, 1, &s_fail);
+        // the row's four warps have read S^T and dP^T before P^T and dS^T overwrite them
+        tc::fence_before_sync();
+        asm volatile("bar.sync %0, 128;" :: "r"(1 + lg) : "memory");
         tc::fence_after_sync();
-#pragma unroll
-        for (int i = 0; i < 32; i += 8) tc::st_sw128_8(sm + PT, AT, krow, cq * 32 + i, pv + i);
+        tmem_st16(tS + lane_off + cq * 16, up);
+        tmem_st16(tP + lane_off + cq * 16, ud);
         sync_mma();
-        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s_fail)) {
-            tc::mma_op(tK, tc::Opnd{tc::smem_addr(sm + PT), 16384, false},
-                       tc::Opnd{tc::smem_addr(sm + (b ? Q1 : Q0)), 16384, true}, AT, AD, AT, e > 0);
+        if (tid == 0 && !failed(&s_fail)) {
+            // dV += P^T dO, dK += dS^T Q, A from TMEM (bf16 pairs), B MN-major
+            const uint32_t id = tc::idesc_bf16(AT, AD, false, true);
+            for (int kk = 0; kk < AT / 16; ++kk) {
+                const uint32_t acc = (e > 0 || kk > 0) ? 1u : 0u;
+                const uint64_t bdo = tc::desc_sw128_mn(tc::smem_addr(sm + (b ? dO1 : dO0)) + kk * 2048, 16384);
+                const uint64_t bq = tc::desc_sw128_mn(tc::smem_addr(sm + (b ? Q1 : Q0)) + kk * 2048, 16384);
+                asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                             "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                             :: "r"(tV), "r"(tS + kk * 8), "l"(bdo), "r"(id), "r"(acc) : "memory");
+                asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                             "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                             :: "r"(tK), "r"(tP + kk * 8), "l"(bq), "r"(id), "r"(acc) : "memory");
+            }
             tc::mma_commit(&bars[2]);
             ++nc2;
         }
+        if (e + 1 < n_e) stage_vec(e + 1);              // every thread has read this tile's lse, D
+        tc::cp_async_commit();
     }
     wait_or_fail(&bars[2], (n_e - 1) & 1, 2, &s_fail);
     tc::fence_after_sync();
@@ -732,7 +754,7 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
     }
     if (s_fail && tid == 0) {
         dev_error(pd, kDevErrTimeout, sk, h);
-        const uint32_t nc[3] = {nc0, nc1, nc2};
+        const uint32_t nc[3] = {nc0, 0u, nc2};
 #pragma unroll
         for (int i = 0; i < 3; ++i)
             if (nc[i]) tc::mbar_wait(&bars[i], (nc[i] - 1) & 1, 1000000000LL);
