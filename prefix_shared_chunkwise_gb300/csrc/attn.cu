@@ -450,7 +450,7 @@ struct AttnBwdParams {
 };
 
 namespace bq_sm {
-constexpr uint32_t Q = 0, dO = 32768, K0 = 65536, K1 = 98304, V = 131072, dS = 163840;
+constexpr uint32_t Q = 0, dO = 32768, K0 = 65536, V0 = 131072;   // K and V: two slots of 32 KB each
 constexpr uint32_t bytes = 196608 + 1024;
 }  // namespace bq_sm
 
@@ -469,10 +469,12 @@ __device__ __forceinline__ void store_tile_bf16(__nv_bfloat16 *dst_row, const fl
 
 __global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDev pd,
                                                           const __grid_constant__ AttnMaps maps) {
+    // S_j goes to one of two TMEM buffers, dS_j (bf16 pairs) overwrites it there and dQ +=
+    // dS_j K_j reads it as the A operand; dQ_{j-1}, S_j and dP_j queue back to back.
     using namespace bq_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    __shared__ uint64_t bars[5];                  // S and dP ready, dQ done, K slot 0 / 1 full, V full
+    __shared__ uint64_t bars[6];                  // S and dP ready, dQ done, K slot 0 / 1, V slot 0 / 1
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, cq = warp >> 2;
@@ -487,7 +489,7 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDe
     uint64_t *bS = &bars[0], *bQd = &bars[1], *bK = &bars[2], *bV = &bars[4];
 
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) tc::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 6; ++i) tc::mbar_init(&bars[i], 1);
         tc::fence_mbar_init();
         s_fail = 0;
     }
@@ -498,68 +500,89 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDe
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = s_tmem, lane_off = static_cast<uint32_t>(lg * 32) << 16;
-    const uint32_t tS = tm, tP = tm + 128, tQ = tm + 256;
+    const uint32_t tP = tm + 256, tQ = tm + 384;        // S buffers at tm and tm + 128
     const int qrow = lg * 32 + lane;
     const int32_t vis = hh + q0 + qrow;
     const int64_t grow = static_cast<int64_t>(row0) + q0 + min(qrow, nq - 1);
     const float lse2 = p.lse[grow * H + h] * kLog2e, Dq = p.D[grow * H + h];
     int ri_k = pd.attn_rptr[sq], ri_v = ri_k;            // thread 0: run cursors of the K and V tiles
+    int32_t issued = 0, waited = -1;                     // thread 0: last tile issued / awaited
     if (tid == 0) {
-        // Q, dO and K_0 on K slot 0's barrier; V_0 on the V barrier
+        // Q, dO and K_0 on K slot 0's barrier; V_0 on V slot 0's
         tc::mbar_expect_tx(&bK[0], 3 * 32768);
         tc::tma_load_3d(sm + Q, &maps.q, 0, h, row0 + q0, &bK[0]);
         tc::tma_load_3d(sm + Q + 16384, &maps.q, 64, h, row0 + q0, &bK[0]);
         tc::tma_load_3d(sm + dO, &maps.dout, 0, h, row0 + q0, &bK[0]);
         tc::tma_load_3d(sm + dO + 16384, &maps.dout, 64, h, row0 + q0, &bK[0]);
         tma_view_tile(maps.k, sm + K0, pd, sq, 0, h, ri_k, &bK[0]);
-        tc::mbar_expect_tx(bV, 32768);
-        tma_view_tile(maps.v, sm + V, pd, sq, 0, h, ri_v, bV);
+        tc::mbar_expect_tx(&bV[0], 32768);
+        tma_view_tile(maps.v, sm + V0, pd, sq, 0, h, ri_v, &bV[0]);
     }
     uint32_t nc_s = 0, nc_q = 0;
     uint32_t nb = view_bits(pd, sq, hh, own, cq * 32);
 
     for (int32_t kt = 0; kt < n_kt; ++kt) {
         const int b = kt & 1;
+        const uint32_t tS = tm + b * 128;
         const uint32_t vb = nb;
         if (kt + 1 < n_kt) nb = view_bits(pd, sq, hh, own, (kt + 1) * AT + cq * 32);
         if (tid == 0) {
+            // S_kt's buffer was last read by dQ_{kt-2}, which completed before S_{kt-1};
+            // dP's was read by every thread before the last block barrier
             wait_or_fail(&bK[b], (kt >> 1) & 1, 2, &s_fail);
-            wait_or_fail(bV, kt & 1, 2, &s_fail);
+            wait_or_fail(&bV[b], (kt >> 1) & 1, 2, &s_fail);
+            waited = kt;
             tc::fence_after_sync();
             if (!failed(&s_fail)) {
                 tc::mma_op(tS, tc::Opnd{tc::smem_addr(sm + Q), 16384, false},
-                           tc::Opnd{tc::smem_addr(sm + (b ? K1 : K0)), 16384, false}, AT, AT, AD, false);
+                           tc::Opnd{tc::smem_addr(sm + K0 + b * 32768), 16384, false}, AT, AT, AD, false);
                 tc::mma_op(tP, tc::Opnd{tc::smem_addr(sm + dO), 16384, false},
-                           tc::Opnd{tc::smem_addr(sm + V), 16384, false}, AT, AT, AD, false);
+                           tc::Opnd{tc::smem_addr(sm + V0 + b * 32768), 16384, false}, AT, AT, AD, false);
                 tc::mma_commit(bS);
                 ++nc_s;
             }
         }
         wait_or_fail(bS, kt & 1, 0, &s_fail);
         tc::fence_after_sync();
+        if (tid == 0 && kt + 1 < n_kt) {
+            // S_kt and dP_kt are done, so is dQ_{kt-1}: the other K and V slots are free
+            tc::mbar_expect_tx(&bK[b ^ 1], 32768);
+            tma_view_tile(maps.k, sm + K0 + (b ^ 1) * 32768, pd, sq, kt + 1, h, ri_k, &bK[b ^ 1]);
+            tc::mbar_expect_tx(&bV[b ^ 1], 32768);
+            tma_view_tile(maps.v, sm + V0 + (b ^ 1) * 32768, pd, sq, kt + 1, h, ri_v, &bV[b ^ 1]);
+            issued = kt + 1;
+        }
         float sv[32], pv[32];
         tc::tmem_ld32(tS + lane_off + cq * 32, sv);
         tc::tmem_ld32(tP + lane_off + cq * 32, pv);
-        if (kt > 0) wait_or_fail(bQd, (kt - 1) & 1, 1, &s_fail);      // dQ_{kt-1}: dS and K_{kt-1} free
-        tc::fence_after_sync();
-        if (tid == 0 && kt + 1 < n_kt) {               // V (read by dP_kt, done) and the other K slot
-            tc::mbar_expect_tx(bV, 32768);
-            tma_view_tile(maps.v, sm + V, pd, sq, kt + 1, h, ri_v, bV);
-            tc::mbar_expect_tx(&bK[b ^ 1], 32768);
-            tma_view_tile(maps.k, sm + (b ? K0 : K1), pd, sq, kt + 1, h, ri_k, &bK[b ^ 1]);
-        }
         const int32_t lim = vis - (kt * AT + cq * 32);
+        uint32_t ud[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float pr = (((vb >> i) & 1u) && i <= lim) ? ex2(fmaf(sv[i], c, -lse2)) : 0.f;
-            sv[i] = p.scale * pr * (pv[i] - Dq);
+        for (int i = 0; i < 32; i += 2) {
+            float ds[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int ii = i + u;
+                const float pr = (((vb >> ii) & 1u) && ii <= lim) ? ex2(fmaf(sv[ii], c, -lse2)) : 0.f;
+                ds[u] = p.scale * pr * (pv[ii] - Dq);
+            }
+            ud[i / 2] = tc::pack_bf16(ds[0], ds[1]);
         }
-#pragma unroll
-        for (int i = 0; i < 32; i += 8) tc::st_sw128_8(sm + dS, AT, qrow, cq * 32 + i, sv + i);
+        // the row's four warps have read S before dS overwrites it
+        tc::fence_before_sync();
+        asm volatile("bar.sync %0, 128;" :: "r"(1 + lg) : "memory");
+        tc::fence_after_sync();
+        tmem_st16(tS + lane_off + cq * 16, ud);
         sync_mma();
         if (tid == 0 && !failed(&s_fail)) {
-            tc::mma_op(tQ, tc::Opnd{tc::smem_addr(sm + dS), 16384, false},
-                       tc::Opnd{tc::smem_addr(sm + (b ? K1 : K0)), 16384, true}, AT, AD, AT, kt > 0);
+            const uint32_t id = tc::idesc_bf16(AT, AD, false, true);
+            for (int kk = 0; kk < AT / 16; ++kk) {
+                const uint64_t bk = tc::desc_sw128_mn(tc::smem_addr(sm + K0 + b * 32768) + kk * 2048, 16384);
+                const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
+                asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                             "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                             :: "r"(tQ), "r"(tS + kk * 8), "l"(bk), "r"(id), "r"(acc) : "memory");
+            }
             tc::mma_commit(bQd);
             ++nc_q;
         }
@@ -572,7 +595,11 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDe
         tc::tmem_ld32(tQ + lane_off + cq * 32, r);
         if (qrow < nq) store_tile_bf16(p.dq + ((static_cast<int64_t>(row0) + q0 + qrow) * H + h) * AD + cq * 32, r, 1.f);
     }
-    if (s_fail && tid == 0) {                          // drain products and copies in flight
+    if (tid == 0 && issued > waited) {                // a tile issued but never awaited (a timeout)
+        tc::mbar_wait(&bK[issued & 1], (issued >> 1) & 1, 1000000000LL);
+        tc::mbar_wait(&bV[issued & 1], (issued >> 1) & 1, 1000000000LL);
+    }
+    if (s_fail && tid == 0) {                          // drain products in flight
         dev_error(pd, kDevErrTimeout, sq, h);
         if (nc_s) tc::mbar_wait(bS, (nc_s - 1) & 1, 1000000000LL);
         if (nc_q) tc::mbar_wait(bQd, (nc_q - 1) & 1, 1000000000LL);
