@@ -695,6 +695,8 @@ def run_attn(parent, seg_len, pl, x, tf_peak):
 
     ms = timed(fwd)
     ms_b = timed(bwd)
+    if pl.device_error() != 0:                       # a wait ran out: the times mean nothing
+        raise RuntimeError("branch attention reported a device error")
     flops = 4.0 * d * H * pairs
     flops_b = 10.0 * d * H * pairs                   # S, dP, dV, dQ, dK: 2 d each per pair
     tile_flops = 4.0 * d * H * tiles * 128 * 128

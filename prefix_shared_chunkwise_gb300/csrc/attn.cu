@@ -50,8 +50,8 @@ constexpr uint32_t bytes = Sum + 1024 + 1024;     // + alignment slack
 constexpr int kKSlots = 3;
 
 // Roles of the forward's 11 warps.
-constexpr int kFwdSoftmaxWarps = 8, kFwdMmaWarp = 8, kFwdLoadWarp0 = 9, kFwdLoadWarps = 2;
-constexpr int kFwdThreads = (kFwdLoadWarp0 + kFwdLoadWarps) * 32;
+constexpr int kFwdSoftmaxWarps = 8, kFwdMmaWarp = 8, kFwdPvWarp = 11, kFwdLoadWarp0 = 9, kFwdLoadWarps = 2;
+constexpr int kFwdThreads = 12 * 32;
 constexpr int kSoftThreads = kFwdSoftmaxWarps * 32;
 
 struct AttnParams {
@@ -150,7 +150,13 @@ __device__ __forceinline__ uint32_t view_bits(const PlanDev &pd, int32_t sq, int
 }
 
 // Barriers of the forward (index into bars[]).
-enum FwdBar { bQ = 0, bKF = 1, bKE = 4, bVF = 7, bVE = 9, bSF = 11, bPF = 13, bOD = 14, bN = 15 };
+// Per S buffer: S full, S released; per P buffer: P written, the O that read it done (which
+// also says every earlier O is done: one thread issues them all, in order).  Every barrier
+// that several warps arrive on, or that a wait may lag by one use, is per buffer: a warp can
+// then never arrive for use j + 2 of a barrier before use j completed, so arrivals of
+// different steps never mix in one phase and no parity check sees a barrier two phases
+// ahead.
+enum FwdBar { bQ = 0, bKF = 1, bKE = 4, bVF = 7, bVE = 9, bSF = 11, bSE = 13, bPF = 15, bPD = 17, bN = 19 };
 
 // O (+)= P V with P (bf16, packed in pairs) read from TMEM: one row per lane, 8 columns per
 // 16 keys.
@@ -203,9 +209,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
             tc::mbar_init(&bars[bVF + i], 1);
             tc::mbar_init(&bars[bVE + i], 1);
             tc::mbar_init(&bars[bSF + i], 1);
+            tc::mbar_init(&bars[bSE + i], kSoftThreads);
+            tc::mbar_init(&bars[bPD + i], 1);
         }
-        tc::mbar_init(&bars[bPF], kSoftThreads);
-        tc::mbar_init(&bars[bOD], 1);
+        for (int i = 0; i < 2; ++i) tc::mbar_init(&bars[bPF + i], kSoftThreads);
         tc::fence_mbar_init();
         s_fail = 0;
     }
@@ -215,9 +222,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
     }
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tm = s_tmem, tO = tm + 256;
+    const uint32_t tm = s_tmem, tO = tm + 256, tPb = tm + 384;
 
-    if (warp >= kFwdLoadWarp0) {
+    if (warp >= kFwdLoadWarp0 && warp < kFwdLoadWarp0 + kFwdLoadWarps) {
         // ---- loaders: one thread for Q and the K ring, one for the V ring, tiled TMA
         if (lane == 0) {
             const int is_v = warp - kFwdLoadWarp0;
@@ -237,48 +244,47 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
             }
         }
     } else if (warp == kFwdMmaWarp) {
-        // ---- one thread issues every product: S_{j+1} ahead of O_j; P_j is read from
-        // TMEM (it overwrote S_j there), so S_{j+2} waits for O_j to complete
+        // ---- S issuer: S_j = Q K_j^T into S buffer j % 2 once the softmax has read S_{j-2}
         if (lane == 0) {
             const tc::Opnd aQ{tc::smem_addr(sm + Q), 16384, false};
-            uint32_t nc_s0 = 0, nc_s1 = 0, nc_o = 0;
+            uint32_t nc_s0 = 0, nc_s1 = 0;
             wait_or_fail(&bars[bQ], 0, 0, &s_fail);
-            wait_or_fail(&bars[bKF], 0, 0, &s_fail);
-            tc::fence_after_sync();
-            if (!failed(&s_fail)) {
-                tc::mma_op(tm, aQ, tc::Opnd{tc::smem_addr(sm + K0), 16384, false}, AT, AT, AD, false);
-                tc::mma_commit(&bars[bSF]);
-                tc::mma_commit(&bars[bKE]);
-                nc_s0 = 1;
-            }
             for (int32_t kt = 0; kt < n_kt && !failed(&s_fail); ++kt) {
-                const int b = kt & 1, nb = b ^ 1;
-                if (kt + 1 < n_kt) {
-                    const int ks = (kt + 1) % kKSlots;
-                    wait_or_fail(&bars[bKF + ks], ((kt + 1) / kKSlots) & 1, 0, &s_fail);
-                    if (kt >= 1) wait_or_fail(&bars[bOD], (kt - 1) & 1, 1, &s_fail);   // O_{kt-1} read P there
-                    tc::fence_after_sync();
-                    if (failed(&s_fail)) break;
-                    tc::mma_op(tm + nb * 128, aQ, tc::Opnd{tc::smem_addr(sm + K0 + ks * 32768), 16384, false},
-                               AT, AT, AD, false);
-                    tc::mma_commit(&bars[bSF + nb]);
-                    tc::mma_commit(&bars[bKE + ks]);
-                    if (nb) ++nc_s1; else ++nc_s0;
-                }
-                wait_or_fail(&bars[bPF], kt & 1, 1, &s_fail);
-                wait_or_fail(&bars[bVF + b], (kt >> 1) & 1, 0, &s_fail);
+                const int b = kt & 1, ks = kt % kKSlots;
+                wait_or_fail(&bars[bKF + ks], (kt / kKSlots) & 1, 0, &s_fail);
+                if (kt >= 2) wait_or_fail(&bars[bSE + b], ((kt - 2) >> 1) & 1, 1, &s_fail);
                 tc::fence_after_sync();
                 if (failed(&s_fail)) break;
-                mma_pv(tO, tm + b * 128, tc::smem_addr(sm + V0 + b * 32768), kt > 0);
-                tc::mma_commit(&bars[bOD]);
-                tc::mma_commit(&bars[bVE + b]);
-                ++nc_o;
+                tc::mma_op(tm + b * 128, aQ, tc::Opnd{tc::smem_addr(sm + K0 + ks * 32768), 16384, false},
+                           AT, AT, AD, false);
+                tc::mma_commit(&bars[bSF + b]);
+                tc::mma_commit(&bars[bKE + ks]);
+                if (b) ++nc_s1; else ++nc_s0;
             }
             if (failed(&s_fail)) {                      // drain the products still in flight
                 dev_error(pd, kDevErrTimeout, sq, h);
                 if (nc_s0) tc::mbar_wait(&bars[bSF], (nc_s0 - 1) & 1, 1000000000LL);
                 if (nc_s1) tc::mbar_wait(&bars[bSF + 1], (nc_s1 - 1) & 1, 1000000000LL);
-                if (nc_o) tc::mbar_wait(&bars[bOD], (nc_o - 1) & 1, 1000000000LL);
+            }
+        }
+    } else if (warp == kFwdPvWarp) {
+        // ---- O issuer: O += P_j V_j once P_j is written (P from TMEM buffer j % 2)
+        if (lane == 0) {
+            uint32_t nc_o0 = 0, nc_o1 = 0;
+            for (int32_t kt = 0; kt < n_kt && !failed(&s_fail); ++kt) {
+                const int b = kt & 1;
+                wait_or_fail(&bars[bPF + b], (kt >> 1) & 1, 1, &s_fail);
+                wait_or_fail(&bars[bVF + b], (kt >> 1) & 1, 0, &s_fail);
+                tc::fence_after_sync();
+                if (failed(&s_fail)) break;
+                mma_pv(tO, tPb + b * 64, tc::smem_addr(sm + V0 + b * 32768), kt > 0);
+                tc::mma_commit(&bars[bPD + b]);
+                tc::mma_commit(&bars[bVE + b]);
+                if (b) ++nc_o1; else ++nc_o0;
+            }
+            if (failed(&s_fail)) {                      // drain the products still in flight
+                if (nc_o0) tc::mbar_wait(&bars[bPD], (nc_o0 - 1) & 1, 1000000000LL);
+                if (nc_o1) tc::mbar_wait(&bars[bPD + 1], (nc_o1 - 1) & 1, 1000000000LL);
             }
         }
     } else {
@@ -311,6 +317,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[32 + i] = r[i];
             }
+            tc::fence_before_sync();
+            mbar_arrive(&bars[bSE + b]);
             const int32_t lim = vis - (kt * AT + half * 64);
             if (__any_sync(0xffffffffu, (vb0 & vb1) != 0xffffffffu || lim < 63)) {
 #pragma unroll
@@ -351,17 +359,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
 #pragma unroll
                 for (int i = 0; i < w; ++i) sp[i] += sp[i + w];
             l_half = l_half * alpha + sp[0];
+            if (kt >= 2) wait_or_fail(&bars[bPD + b], ((kt - 2) >> 1) & 1, 1, &s_fail);
+            tc::fence_after_sync();
             {
-                // P_kt (bf16 pairs) over this half's 32 columns of S_kt's buffer; the row's
-                // other half finished reading S before the max exchange above
                 float w[32];
                 uint32_t *u = reinterpret_cast<uint32_t *>(w);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) u[i] = tc::pack_bf16(s[2 * i], s[2 * i + 1]);
-                tc::tmem_st32(tm + b * 128 + lane_off + half * 32, w);
+                tc::tmem_st32(tPb + b * 64 + lane_off + half * 32, w);
             }
             if (move && kt > 0) {
-                wait_or_fail(&bars[bOD], (kt - 1) & 1, 1, &s_fail);    // O settled before its rescale
+                wait_or_fail(&bars[bPD + ((kt - 1) & 1)], ((kt - 1) >> 1) & 1, 1, &s_fail);  // O_{kt-1} done
                 tc::fence_after_sync();
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
@@ -373,9 +381,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
                 }
             }
             tc::fence_before_sync();
-            mbar_arrive(&bars[bPF]);
+            mbar_arrive(&bars[bPF + b]);
         }
-        wait_or_fail(&bars[bOD], (n_kt - 1) & 1, 1, &s_fail);
+        wait_or_fail(&bars[bPD + ((n_kt - 1) & 1)], ((n_kt - 1) >> 1) & 1, 1, &s_fail);   // every O done
         tc::fence_after_sync();
         ssum[half * AT + qrow] = l_half;
         asm volatile("bar.sync %0, 64;" :: "r"(1 + lg) : "memory");
