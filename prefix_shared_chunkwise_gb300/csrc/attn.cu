@@ -1,4 +1,5 @@
-// Branch attention over the compact layout, forward, tensor cores (bf16, d = 128).
+// Branch attention over the compact layout, forward and backward, tensor cores (bf16,
+// d = 128).
 //
 // HARTS (page "HARTS ... 精读", section 4.3, MLA paragraph; summary page, section 4 "MLA
 // execution"; figures page, Figure C.1(c)): a branch's queries (its own l tokens) attend
@@ -7,22 +8,22 @@
 // gather inside the kernel; outputs go back to the unique compact rows.  The core is plain
 // softmax attention on projected inputs: o = softmax(scale q k^T) v per head.
 //
-// One block per (sequence, 128-query tile, head); the planner orders the tiles tree by
-// tree (longest first within a tree) with the heads innermost, so the key / value rows a
-// tree's blocks share stay in L2.  The block's warps have fixed roles and meet only at
-// mbarriers (every wait bounded):
-//   loaders (2 + 2)     gather Q and the K_j, and (the other pair) the V_j of each 128-row
-//                       key tile by cp.async into two-slot K and V rings; a slot is
-//                       refilled once the product that reads it has completed (K after
-//                       S_j, V after O_j); the pairs run independent pipelines
-//   MMA (one thread)    S_j = Q K_j^T (tcgen05, fp32 in one of two TMEM buffers), issued a
-//                       tile ahead of O_{j-1} += P_{j-1} V_{j-1} (V read MN-major)
+// Forward: one block per (sequence, 128-query tile, head); the planner orders the tiles
+// tree by tree (longest first within a tree) with the heads innermost, so the key / value
+// rows a tree's blocks share stay in L2.  The block's warps have fixed roles and meet only
+// at mbarriers (every wait bounded):
+//   loaders (2 threads) Q and the K_j of each 128-row key tile into a three-slot ring, and
+//                       the V_j into a two-slot ring, by tiled TMA over the padded view; a
+//                       slot is refilled once the product that reads it has completed
+//   S issuer (1 thread) S_j = Q K_j^T into TMEM buffer j mod 2 once the softmax has read
+//                       S_{j-2}
+//   O issuer (1 thread) O += P_j V_j (P from TMEM buffer j mod 2, V read MN-major)
 //   softmax (8 warps)   one query row and 64 columns per thread; scores in base-2 units
 //                       (scale * log2 e folded into one FMA); the two warps holding a row
 //                       exchange its max through shared memory; the running max moves,
 //                       and O is rescaled in TMEM, only when a row max grows by more than
 //                       2^8 -- any common offset gives the same softmax, the threshold
-//                       only bounds P by 256; P goes to shared memory as bf16
+//                       only bounds P by 256; P goes to TMEM as bf16 pairs
 // Masking runs only on tiles that reach past the first query's causal limit.  A timeout
 // records code 3 in the plan's error word, stops issuing products and drains the ones
 // in flight.
@@ -457,10 +458,24 @@ struct AttnBwdParams {
     float scale;
 };
 
+// dQ kernel roles: 16 warps form dS (lg = warp & 3: 32 query rows; cq = warp >> 2: 32 key
+// columns), one thread issues the products, one loads Q, dO and the K and V rings.
+constexpr int kDqWorkWarps = 16, kDqMmaWarp = 16, kDqLoadWarp = 17, kDqThreads = 18 * 32;
+constexpr int kDqWork = kDqWorkWarps * 32;
+constexpr int kDqKSlots = 3;
+
 namespace bq_sm {
-constexpr uint32_t Q = 0, dO = 32768, K0 = 65536, V0 = 131072;   // K and V: two slots of 32 KB each
-constexpr uint32_t bytes = 196608 + 1024;
+constexpr uint32_t Q = 0, dO = 32768, K0 = 65536;      // K ring: 3 slots of 32 KB (K_j is read by S_j and dQ_j)
+constexpr uint32_t V0 = K0 + kDqKSlots * 32768;         // V ring: 2 slots (V_j is read by dP_j only)
+constexpr uint32_t bytes = V0 + 2 * 32768 + 1024;       // + alignment slack
 }  // namespace bq_sm
+
+// Barriers of the dQ kernel (index into bars[]): Q and dO landed; K slot full / free; V slot
+// full / free; per S buffer: S_j and dP_j done; dP_j read by every dS thread; per S buffer:
+// dS_j written; per S buffer: dQ_j done (also every earlier product of the issuing thread).
+// As in the forward, a barrier that many threads arrive on is either per buffer or gates
+// the product that the next phase's arrivals depend on, so phases never mix.
+enum DqBar { qQ = 0, qKF = 1, qKE = 4, qVF = 7, qVE = 9, qSP = 11, qPE = 13, qDS = 14, qQD = 16, qN = 18 };
 
 __device__ __forceinline__ void store_tile_bf16(__nv_bfloat16 *dst_row, const float (&r)[32], float mul) {
     uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
@@ -475,17 +490,20 @@ __device__ __forceinline__ void store_tile_bf16(__nv_bfloat16 *dst_row, const fl
     }
 }
 
-__global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDev pd,
-                                                          const __grid_constant__ AttnMaps maps) {
-    // S_j goes to one of two TMEM buffers, dS_j (bf16 pairs) overwrites it there and dQ +=
-    // dS_j K_j reads it as the A operand; dQ_{j-1}, S_j and dP_j queue back to back.
+__global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDev pd,
+                                                                const __grid_constant__ AttnMaps maps) {
+    // S_j (one of two TMEM buffers) and dP_j (one buffer) feed the dS warps; dS_j (bf16
+    // pairs) overwrites S_j and dQ += dS_j K_j reads it there.  The issuing thread runs one
+    // tile ahead: S_{j+1} once dQ_{j-1} has released its buffer, dP_{j+1} once every dS
+    // thread has read dP_j, then dQ_j once dS_j is written, so the tensor pipe works through
+    // dQ_{j-1}, S_{j+1} and dP_{j+1} while the dS warps work on tile j.
     using namespace bq_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    __shared__ uint64_t bars[6];                  // S and dP ready, dQ done, K slot 0 / 1, V slot 0 / 1
+    __shared__ uint64_t bars[qN];
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, cq = warp >> 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, cq = (warp >> 2) & 3;
     const int H = p.H;
     const int32_t h = blockIdx.x % H, qi = blockIdx.x / H;
     const int32_t sq = pd.attn_qt[2 * qi], qt = pd.attn_qt[2 * qi + 1];
@@ -493,129 +511,182 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDe
     const int32_t row0 = pd.seq_row0[sq], own = pd.seq_nown[sq];
     const int32_t q0 = qt * AT, nq = min(AT, own - q0);
     const int32_t n_kt = (hh + q0 + nq - 1) / AT + 1;
-    const float c = p.scale * kLog2e;
-    uint64_t *bS = &bars[0], *bQd = &bars[1], *bK = &bars[2], *bV = &bars[4];
 
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) tc::mbar_init(&bars[i], 1);
+        tc::mbar_init(&bars[qQ], 1);
+        for (int i = 0; i < kDqKSlots; ++i) {
+            tc::mbar_init(&bars[qKF + i], 1);
+            tc::mbar_init(&bars[qKE + i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&bars[qVF + i], 1);
+            tc::mbar_init(&bars[qVE + i], 1);
+            tc::mbar_init(&bars[qSP + i], 1);
+            tc::mbar_init(&bars[qDS + i], kDqWork);
+            tc::mbar_init(&bars[qQD + i], 1);
+        }
+        tc::mbar_init(&bars[qPE], kDqWork);
         tc::fence_mbar_init();
         s_fail = 0;
     }
-    if (warp == 0) {
+    if (warp == kDqMmaWarp) {
         tc::tmem_alloc(&s_tmem, 512);
         tc::fence_before_sync();
     }
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tm = s_tmem, lane_off = static_cast<uint32_t>(lg * 32) << 16;
-    const uint32_t tP = tm + 256, tQ = tm + 384;        // S buffers at tm and tm + 128
-    const int qrow = lg * 32 + lane;
-    const int32_t vis = hh + q0 + qrow;
-    const int64_t grow = static_cast<int64_t>(row0) + q0 + min(qrow, nq - 1);
-    const float lse2 = p.lse[grow * H + h] * kLog2e, Dq = p.D[grow * H + h];
-    int ri_k = pd.attn_rptr[sq], ri_v = ri_k;            // thread 0: run cursors of the K and V tiles
-    int32_t issued = 0, waited = -1;                     // thread 0: last tile issued / awaited
-    if (tid == 0) {
-        // Q, dO and K_0 on K slot 0's barrier; V_0 on V slot 0's
-        tc::mbar_expect_tx(&bK[0], 3 * 32768);
-        tc::tma_load_3d(sm + Q, &maps.q, 0, h, row0 + q0, &bK[0]);
-        tc::tma_load_3d(sm + Q + 16384, &maps.q, 64, h, row0 + q0, &bK[0]);
-        tc::tma_load_3d(sm + dO, &maps.dout, 0, h, row0 + q0, &bK[0]);
-        tc::tma_load_3d(sm + dO + 16384, &maps.dout, 64, h, row0 + q0, &bK[0]);
-        tma_view_tile(maps.k, sm + K0, pd, sq, 0, h, ri_k, &bK[0]);
-        tc::mbar_expect_tx(&bV[0], 32768);
-        tma_view_tile(maps.v, sm + V0, pd, sq, 0, h, ri_v, &bV[0]);
-    }
-    uint32_t nc_s = 0, nc_q = 0;
-    uint32_t nb = view_bits(pd, sq, hh, own, cq * 32);
+    const uint32_t tm = s_tmem, tP = tm + 256, tQ = tm + 384;   // S buffers at tm and tm + 128
 
-    for (int32_t kt = 0; kt < n_kt; ++kt) {
-        const int b = kt & 1;
-        const uint32_t tS = tm + b * 128;
-        const uint32_t vb = nb;
-        if (kt + 1 < n_kt) nb = view_bits(pd, sq, hh, own, (kt + 1) * AT + cq * 32);
-        if (tid == 0) {
-            // S_kt's buffer was last read by dQ_{kt-2}, which completed before S_{kt-1};
-            // dP's was read by every thread before the last block barrier
-            wait_or_fail(&bK[b], (kt >> 1) & 1, 2, &s_fail);
-            wait_or_fail(&bV[b], (kt >> 1) & 1, 2, &s_fail);
-            waited = kt;
+    if (warp == kDqLoadWarp) {
+        // ---- loader: Q and dO once, then K_j and V_j in view order, tiled TMA
+        if (lane == 0) {
+            int ri_k = pd.attn_rptr[sq], ri_v = ri_k;
+            tc::mbar_expect_tx(&bars[qQ], 65536);
+            tc::tma_load_3d(sm + Q, &maps.q, 0, h, row0 + q0, &bars[qQ]);
+            tc::tma_load_3d(sm + Q + 16384, &maps.q, 64, h, row0 + q0, &bars[qQ]);
+            tc::tma_load_3d(sm + dO, &maps.dout, 0, h, row0 + q0, &bars[qQ]);
+            tc::tma_load_3d(sm + dO + 16384, &maps.dout, 64, h, row0 + q0, &bars[qQ]);
+            int32_t nk = 0, nv = 0;
+            for (int32_t j = 0; j < n_kt && !failed(&s_fail); ++j) {
+                const int ks = j % kDqKSlots, uk = j / kDqKSlots, vs = j & 1, uv = j >> 1;
+                if (uk > 0) wait_or_fail(&bars[qKE + ks], (uk - 1) & 1, 2, &s_fail);
+                if (failed(&s_fail)) break;
+                tc::mbar_expect_tx(&bars[qKF + ks], 32768);
+                tma_view_tile(maps.k, sm + K0 + ks * 32768, pd, sq, j, h, ri_k, &bars[qKF + ks]);
+                nk = j + 1;
+                if (uv > 0) wait_or_fail(&bars[qVE + vs], (uv - 1) & 1, 2, &s_fail);
+                if (failed(&s_fail)) break;
+                tc::mbar_expect_tx(&bars[qVF + vs], 32768);
+                tma_view_tile(maps.v, sm + V0 + vs * 32768, pd, sq, j, h, ri_v, &bars[qVF + vs]);
+                nv = j + 1;
+            }
+            // every copy lands before the block exits: only a slot's last load can be in flight
+            for (int i = 0; i < kDqKSlots; ++i) {
+                const int32_t uses = nk > i ? (nk - 1 - i) / kDqKSlots + 1 : 0;
+                if (uses) tc::mbar_wait(&bars[qKF + i], (uses - 1) & 1, 1000000000LL);
+            }
+            for (int i = 0; i < 2; ++i) {
+                const int32_t uses = nv > i ? (nv - 1 - i) / 2 + 1 : 0;
+                if (uses) tc::mbar_wait(&bars[qVF + i], (uses - 1) & 1, 1000000000LL);
+            }
+            tc::mbar_wait(&bars[qQ], 0, 1000000000LL);
+        }
+    } else if (warp == kDqMmaWarp) {
+        // ---- issuer: S_0, dP_0; then per tile j: S_{j+1}, dP_{j+1}, dQ_j
+        if (lane == 0) {
+            const tc::Opnd aQ{tc::smem_addr(sm + Q), 16384, false}, adO{tc::smem_addr(sm + dO), 16384, false};
+            const uint32_t id_dq = tc::idesc_bf16(AT, AD, false, true);
+            uint32_t nc_sp0 = 0, nc_sp1 = 0, nc_qd0 = 0, nc_qd1 = 0;
+            wait_or_fail(&bars[qQ], 0, 0, &s_fail);
+            wait_or_fail(&bars[qKF], 0, 0, &s_fail);
+            wait_or_fail(&bars[qVF], 0, 0, &s_fail);
             tc::fence_after_sync();
             if (!failed(&s_fail)) {
-                tc::mma_op(tS, tc::Opnd{tc::smem_addr(sm + Q), 16384, false},
-                           tc::Opnd{tc::smem_addr(sm + K0 + b * 32768), 16384, false}, AT, AT, AD, false);
-                tc::mma_op(tP, tc::Opnd{tc::smem_addr(sm + dO), 16384, false},
-                           tc::Opnd{tc::smem_addr(sm + V0 + b * 32768), 16384, false}, AT, AT, AD, false);
-                tc::mma_commit(bS);
-                ++nc_s;
+                tc::mma_op(tm, aQ, tc::Opnd{tc::smem_addr(sm + K0), 16384, false}, AT, AT, AD, false);
+                tc::mma_op(tP, adO, tc::Opnd{tc::smem_addr(sm + V0), 16384, false}, AT, AT, AD, false);
+                tc::mma_commit(&bars[qSP]);
+                tc::mma_commit(&bars[qVE]);
+                nc_sp0 = 1;
+            }
+            for (int32_t j = 0; j < n_kt && !failed(&s_fail); ++j) {
+                const int b = j & 1, nb = b ^ 1;
+                if (j + 1 < n_kt) {
+                    const int ks = (j + 1) % kDqKSlots;
+                    wait_or_fail(&bars[qKF + ks], ((j + 1) / kDqKSlots) & 1, 0, &s_fail);
+                    if (j >= 1) wait_or_fail(&bars[qQD + nb], ((j - 1) >> 1) & 1, 1, &s_fail);   // dQ_{j-1} read dS there
+                    tc::fence_after_sync();
+                    if (failed(&s_fail)) break;
+                    tc::mma_op(tm + nb * 128, aQ, tc::Opnd{tc::smem_addr(sm + K0 + ks * 32768), 16384, false},
+                               AT, AT, AD, false);
+                    wait_or_fail(&bars[qVF + nb], ((j + 1) >> 1) & 1, 0, &s_fail);
+                    wait_or_fail(&bars[qPE], j & 1, 1, &s_fail);                   // dP_j read by every dS thread
+                    tc::fence_after_sync();
+                    if (failed(&s_fail)) break;
+                    tc::mma_op(tP, adO, tc::Opnd{tc::smem_addr(sm + V0 + nb * 32768), 16384, false}, AT, AT, AD, false);
+                    tc::mma_commit(&bars[qSP + nb]);
+                    tc::mma_commit(&bars[qVE + nb]);
+                    if (nb) ++nc_sp1; else ++nc_sp0;
+                }
+                wait_or_fail(&bars[qDS + b], (j >> 1) & 1, 1, &s_fail);
+                tc::fence_after_sync();
+                if (failed(&s_fail)) break;
+                const uint32_t kaddr = tc::smem_addr(sm + K0 + (j % kDqKSlots) * 32768);
+                for (int kk = 0; kk < AT / 16; ++kk) {
+                    const uint64_t bk = tc::desc_sw128_mn(kaddr + kk * 2048, 16384);
+                    const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                                 :: "r"(tQ), "r"(tm + b * 128 + kk * 8), "l"(bk), "r"(id_dq), "r"(acc) : "memory");
+                }
+                tc::mma_commit(&bars[qQD + b]);
+                tc::mma_commit(&bars[qKE + j % kDqKSlots]);
+                if (b) ++nc_qd1; else ++nc_qd0;
+            }
+            if (failed(&s_fail)) {                      // drain the products still in flight
+                if (nc_sp0) tc::mbar_wait(&bars[qSP], (nc_sp0 - 1) & 1, 1000000000LL);
+                if (nc_sp1) tc::mbar_wait(&bars[qSP + 1], (nc_sp1 - 1) & 1, 1000000000LL);
+                if (nc_qd0) tc::mbar_wait(&bars[qQD], (nc_qd0 - 1) & 1, 1000000000LL);
+                if (nc_qd1) tc::mbar_wait(&bars[qQD + 1], (nc_qd1 - 1) & 1, 1000000000LL);
             }
         }
-        wait_or_fail(bS, kt & 1, 0, &s_fail);
-        tc::fence_after_sync();
-        if (tid == 0 && kt + 1 < n_kt) {
-            // S_kt and dP_kt are done, so is dQ_{kt-1}: the other K and V slots are free
-            tc::mbar_expect_tx(&bK[b ^ 1], 32768);
-            tma_view_tile(maps.k, sm + K0 + (b ^ 1) * 32768, pd, sq, kt + 1, h, ri_k, &bK[b ^ 1]);
-            tc::mbar_expect_tx(&bV[b ^ 1], 32768);
-            tma_view_tile(maps.v, sm + V0 + (b ^ 1) * 32768, pd, sq, kt + 1, h, ri_v, &bV[b ^ 1]);
-            issued = kt + 1;
-        }
-        float sv[32], pv[32];
-        tc::tmem_ld32(tS + lane_off + cq * 32, sv);
-        tc::tmem_ld32(tP + lane_off + cq * 32, pv);
-        const int32_t lim = vis - (kt * AT + cq * 32);
-        uint32_t ud[16];
+    } else {
+        // ---- dS warps: one query row and 32 key columns per thread
+        const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+        const int qrow = lg * 32 + lane;
+        const int32_t vis = hh + q0 + qrow;
+        const int64_t grow = static_cast<int64_t>(row0) + q0 + min(qrow, nq - 1);
+        const float c = p.scale * kLog2e;
+        const float lse2 = p.lse[grow * H + h] * kLog2e, Dq = p.D[grow * H + h];
+        uint32_t nbits = view_bits(pd, sq, hh, own, cq * 32);
+        for (int32_t j = 0; j < n_kt; ++j) {
+            const int b = j & 1;
+            const uint32_t tS = tm + b * 128;
+            const uint32_t vb = nbits;
+            if (j + 1 < n_kt) nbits = view_bits(pd, sq, hh, own, (j + 1) * AT + cq * 32);
+            wait_or_fail(&bars[qSP + b], (j >> 1) & 1, 0, &s_fail);
+            tc::fence_after_sync();
+            float sv[32], pv[32];
+            tc::tmem_ld32(tS + lane_off + cq * 32, sv);
+            tc::tmem_ld32(tP + lane_off + cq * 32, pv);
+            tc::fence_before_sync();
+            mbar_arrive(&bars[qPE]);
+            const int32_t lim = vis - (j * AT + cq * 32);
+            uint32_t ud[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            float ds[2];
+            for (int i = 0; i < 32; i += 2) {
+                float ds[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int ii = i + u;
-                const float pr = (((vb >> ii) & 1u) && ii <= lim) ? ex2(fmaf(sv[ii], c, -lse2)) : 0.f;
-                ds[u] = p.scale * pr * (pv[ii] - Dq);
+                for (int u = 0; u < 2; ++u) {
+                    const int ii = i + u;
+                    const float pr = (((vb >> ii) & 1u) && ii <= lim) ? ex2(fmaf(sv[ii], c, -lse2)) : 0.f;
+                    ds[u] = p.scale * pr * (pv[ii] - Dq);
+                }
+                ud[i / 2] = tc::pack_bf16(ds[0], ds[1]);
             }
-            ud[i / 2] = tc::pack_bf16(ds[0], ds[1]);
+            // the row's four warps have read S_j before dS_j overwrites it
+            tc::fence_before_sync();
+            asm volatile("bar.sync %0, 128;" :: "r"(1 + lg) : "memory");
+            tc::fence_after_sync();
+            tmem_st16(tS + lane_off + cq * 16, ud);
+            tc::fence_before_sync();
+            mbar_arrive(&bars[qDS + b]);
         }
-        // the row's four warps have read S before dS overwrites it
-        tc::fence_before_sync();
-        asm volatile("bar.sync %0, 128;" :: "r"(1 + lg) : "memory");
+        wait_or_fail(&bars[qQD + ((n_kt - 1) & 1)], ((n_kt - 1) >> 1) & 1, 1, &s_fail);   // every dQ product done
         tc::fence_after_sync();
-        tmem_st16(tS + lane_off + cq * 16, ud);
-        sync_mma();
-        if (tid == 0 && !failed(&s_fail)) {
-            const uint32_t id = tc::idesc_bf16(AT, AD, false, true);
-            for (int kk = 0; kk < AT / 16; ++kk) {
-                const uint64_t bk = tc::desc_sw128_mn(tc::smem_addr(sm + K0 + b * 32768) + kk * 2048, 16384);
-                const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
-                asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                             "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-                             :: "r"(tQ), "r"(tS + kk * 8), "l"(bk), "r"(id), "r"(acc) : "memory");
-            }
-            tc::mma_commit(bQd);
-            ++nc_q;
-        }
     }
-    wait_or_fail(bQd, (n_kt - 1) & 1, 1, &s_fail);
-    tc::fence_after_sync();
     __syncthreads();
-    if (!s_fail) {
+    if (tid == 0 && s_fail) dev_error(pd, kDevErrTimeout, sq, h);
+    if (warp < kDqWorkWarps && !s_fail) {
+        const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+        const int qrow = lg * 32 + lane;
         float r[32];
         tc::tmem_ld32(tQ + lane_off + cq * 32, r);
         if (qrow < nq) store_tile_bf16(p.dq + ((static_cast<int64_t>(row0) + q0 + qrow) * H + h) * AD + cq * 32, r, 1.f);
     }
-    if (tid == 0 && issued > waited) {                // a tile issued but never awaited (a timeout)
-        tc::mbar_wait(&bK[issued & 1], (issued >> 1) & 1, 1000000000LL);
-        tc::mbar_wait(&bV[issued & 1], (issued >> 1) & 1, 1000000000LL);
-    }
-    if (s_fail && tid == 0) {                          // drain products in flight
-        dev_error(pd, kDevErrTimeout, sq, h);
-        if (nc_s) tc::mbar_wait(bS, (nc_s - 1) & 1, 1000000000LL);
-        if (nc_q) tc::mbar_wait(bQd, (nc_q - 1) & 1, 1000000000LL);
-    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (warp == 0) tc::tmem_dealloc(tm, 512);
+    if (warp == kDqMmaWarp) tc::tmem_dealloc(tm, 512);
 }
 
 namespace bk_sm {
@@ -915,7 +986,7 @@ int harts_attn_bwd(const harts_plan *P, const harts_attn_bwd_args *a, harts_stre
         set_error("tensor map encoding failed"); return HARTS_ECUDA;
     }
     if (e == cudaSuccess)
-        e = launch_big(attn_bwd_dq_tc, static_cast<unsigned>(int64_t(P->image.n_qt) * p.H), ANT, bq_sm::bytes, st, p,
+        e = launch_big(attn_bwd_dq_tc, static_cast<unsigned>(int64_t(P->image.n_qt) * p.H), kDqThreads, bq_sm::bytes, st, p,
                        P->view, maps);
     if (e == cudaSuccess)
         e = launch_big(attn_bwd_dkdv_tc, static_cast<unsigned>(int64_t(P->image.n_kt) * p.H), ANT, bk_sm::bytes, st, p,
