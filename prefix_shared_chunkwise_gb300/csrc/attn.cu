@@ -37,7 +37,7 @@
 namespace harts {
 namespace {
 
-constexpr int AD = 128, AT = kAttnTile, ANT = 512;   // ANT: threads of the backward kernels
+constexpr int AD = 128, AT = kAttnTile;
 constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;               // running max moves when a row max grows by more
 
@@ -67,18 +67,6 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-template <int N>
-__device__ __forceinline__ void cp_wait_group() {
-    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
-}
-
-__device__ __forceinline__ void sync_mma() {
-    tc::fence_smem_to_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
@@ -689,29 +677,56 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p,
     if (warp == kDqMmaWarp) tc::tmem_dealloc(tm, 512);
 }
 
+// dK / dV kernel roles: 16 warps form P^T and dS^T (lg = warp & 3: 32 key rows; cq = warp >>
+// 2: 16 query columns of a 64-query half), one thread issues the products, one warp loads
+// K, V once and then Q, dO (tiled TMA) and lse, D (plain loads into shared memory) per
+// query tile.
+constexpr int kKvWorkWarps = 16, kKvMmaWarp = 16, kKvLoadWarp = 17, kKvThreads = 18 * 32;
+constexpr int kKvWork = kKvWorkWarps * 32;
+constexpr int kHalf = AT / 2;                     // queries per step
+
 namespace bk_sm {
 constexpr uint32_t K = 0, V = 32768, Q0 = 65536, Q1 = 98304, dO0 = 131072, dO1 = 163840;
-constexpr uint32_t Vec = 196608;                  // [128] lse, [128] D of the current query tile
-constexpr uint32_t bytes = Vec + 1024 + 1024;
+constexpr uint32_t Vec = 196608;                  // [2 slots][128] lse * log2 e, then [2 slots][128] D
+constexpr uint32_t bytes = Vec + 2048 + 1024;     // + alignment slack
 }  // namespace bk_sm
 
-__global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, PlanDev pd,
-                                                            const __grid_constant__ AttnMaps maps) {
+// Barriers of the dK / dV kernel: K and V landed; per Q slot: Q, dO, lse and D of a query
+// tile landed (32 loader lanes + the copy bytes), the slot free again; per step buffer:
+// S^T and dP^T done, P^T and dS^T written, dV and dK updated (also every earlier product).
+enum KvBar { vKV = 0, vQF = 1, vQE = 3, vSP = 5, vDS = 7, vDVK = 9, vN = 11 };
+
+// 8 columns of one TMEM lane per thread (warp-collective), then wait for the stores.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&u)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
+                    "r"(u[7]) : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams p, PlanDev pd,
+                                                                  const __grid_constant__ AttnMaps maps) {
+    // One block per (key tile of a sequence's own rows, head) over the query tiles that see
+    // it, each taken as one or two 64-query steps (a tile of at most 64 rows is one step).
+    // Step i: S^T = K Q_i^T and dP^T = V dO_i^T into TMEM buffer i mod 2 (64 columns each),
+    // P^T and dS^T (bf16 pairs) written over them, dV += P^T dO_i and dK += dS^T Q_i read
+    // them there.  The issuing thread runs a step ahead: S^T, dP^T of step i + 1 once dV, dK
+    // of step i - 1 have released that buffer, so the tensor pipe works through step i - 1's
+    // updates and step i + 1's products while the work warps form step i.
     using namespace bk_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    __shared__ uint64_t bars[6];                  // S^T and dP^T ready, (unused), dV and dK done, K and V, Q and dO x 2
+    __shared__ uint64_t bars[vN];
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
-    float *slse = reinterpret_cast<float *>(sm + Vec), *sD = slse + AT;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, cq = warp >> 2;
+    float *slse = reinterpret_cast<float *>(sm + Vec), *sD = slse + 2 * AT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, cq = (warp >> 2) & 3;
     const int H = p.H;
     const int32_t h = blockIdx.x % H, ki = blockIdx.x / H;
     const int32_t sk = pd.attn_kt[2 * ki], kti = pd.attn_kt[2 * ki + 1];
     const int32_t e0 = pd.attn_kptr[ki], n_e = pd.attn_kptr[ki + 1] - e0;
     const int32_t k0 = kti * AT, nk = min(AT, pd.seq_nown[sk] - k0);
     const int64_t krow0 = static_cast<int64_t>(pd.seq_row0[sk]) + k0;
-    const float c = p.scale * kLog2e;
     // query tile of entry e: rows, count, causal offset or visible-key limit
     auto entry = [&](int32_t e, int64_t &qrow0, int &nq, int32_t &qoff, int32_t &f) {
         const int32_t s_ = pd.attn_kq[3 * (e0 + e)], t_ = pd.attn_kq[3 * (e0 + e) + 1];
@@ -720,155 +735,212 @@ __global__ void __launch_bounds__(ANT, 1) attn_bwd_dkdv_tc(AttnBwdParams p, Plan
         nq = min(AT, pd.seq_nown[s_] - t_ * AT);
         qoff = t_ * AT - k0;                          // query local position minus key tile start
     };
-    // thread 0: Q and dO of entry e (128 rows from the tile's first; rows past the tile are
-    // masked, rows past the tensor read zeros) by tiled TMA into buffer bb
-    auto stage_q = [&](int32_t e, int bb) {
-        int64_t qr; int nq; int32_t qoff, f;
-        entry(e, qr, nq, qoff, f);
-        uint64_t *bar = &bars[4 + bb];
-        tc::mbar_expect_tx(bar, 65536);
-        uint8_t *dq_ = sm + (bb ? Q1 : Q0), *dd = sm + (bb ? dO1 : dO0);
-        tc::tma_load_3d(dq_, &maps.q, 0, h, static_cast<int>(qr), bar);
-        tc::tma_load_3d(dq_ + 16384, &maps.q, 64, h, static_cast<int>(qr), bar);
-        tc::tma_load_3d(dd, &maps.dout, 0, h, static_cast<int>(qr), bar);
-        tc::tma_load_3d(dd + 16384, &maps.dout, 64, h, static_cast<int>(qr), bar);
-    };
-    auto stage_vec = [&](int32_t e) {
-        int64_t qr; int nq; int32_t qoff, f;
-        entry(e, qr, nq, qoff, f);
-        if (tid < AT) {
-            const bool ok = tid < nq;
-            tc::cp_async4(slse + tid, p.lse + ((qr + (ok ? tid : 0)) * H + h), ok ? 4u : 0u);
-            tc::cp_async4(sD + tid, p.D + ((qr + (ok ? tid : 0)) * H + h), ok ? 4u : 0u);
-        }
-    };
+    auto n_steps = [&](int nq) { return nq > kHalf ? 2 : 1; };
 
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) tc::mbar_init(&bars[i], 1);
+        tc::mbar_init(&bars[vKV], 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&bars[vQF + i], 32);
+            tc::mbar_init(&bars[vQE + i], 1);
+            tc::mbar_init(&bars[vSP + i], 1);
+            tc::mbar_init(&bars[vDS + i], kKvWork);
+            tc::mbar_init(&bars[vDVK + i], 1);
+        }
         tc::fence_mbar_init();
         s_fail = 0;
     }
-    if (warp == 0) {
+    if (warp == kKvMmaWarp) {
         tc::tmem_alloc(&s_tmem, 512);
         tc::fence_before_sync();
     }
-    if (tid == 0) {
-        tc::mbar_expect_tx(&bars[3], 65536);
-        tc::tma_load_3d(sm + K, &maps.k[4], 0, h, static_cast<int>(krow0), &bars[3]);
-        tc::tma_load_3d(sm + K + 16384, &maps.k[4], 64, h, static_cast<int>(krow0), &bars[3]);
-        tc::tma_load_3d(sm + V, &maps.v[4], 0, h, static_cast<int>(krow0), &bars[3]);
-        tc::tma_load_3d(sm + V + 16384, &maps.v[4], 64, h, static_cast<int>(krow0), &bars[3]);
-        stage_q(0, 0);
-    }
-    stage_vec(0);
-    tc::cp_async_commit();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tm = s_tmem, lane_off = static_cast<uint32_t>(lg * 32) << 16;
-    const uint32_t tS = tm, tP = tm + 128, tV = tm + 256, tK = tm + 384;
-    const int krow = lg * 32 + lane;                 // this thread's key row (TMEM lane)
-    uint32_t nc0 = 0, nc2 = 0;                      // thread 0: commits per barrier
-    int32_t q_issued = 0, q_waited = -1;             // thread 0: last entry whose Q / dO were issued, awaited
-    bool kv_waited = false;
+    const uint32_t tm = s_tmem, tdP = tm + 128, tV = tm + 256, tK = tm + 384;   // S^T buffers at tm, tm + 64
 
-    for (int32_t e = 0; e < n_e; ++e) {
-        const int b = e & 1;
-        tc::cp_async_wait_all();
-        sync_mma();
-        if (tid == 0) {
-            if (e == 0) { wait_or_fail(&bars[3], 0, 2, &s_fail); kv_waited = true; }
-            wait_or_fail(&bars[4 + b], (e >> 1) & 1, 2, &s_fail);
-            q_waited = e;
-            // dV_{e-1} and dK_{e-1} read P^T and dS^T where S^T and dP^T go next, and Q, dO
-            // of the other buffer
-            if (e > 0) wait_or_fail(&bars[2], (e - 1) & 1, 2, &s_fail);
+    if (warp == kKvLoadWarp) {
+        // ---- loader warp: K and V once; per query tile Q and dO by tiled TMA (lane 0), lse
+        // and D by plain loads (4 rows per lane); all 32 lanes arrive on the slot's barrier
+        if (lane == 0) {
+            tc::mbar_expect_tx(&bars[vKV], 65536);
+            tc::tma_load_3d(sm + K, &maps.k[4], 0, h, static_cast<int>(krow0), &bars[vKV]);
+            tc::tma_load_3d(sm + K + 16384, &maps.k[4], 64, h, static_cast<int>(krow0), &bars[vKV]);
+            tc::tma_load_3d(sm + V, &maps.v[4], 0, h, static_cast<int>(krow0), &bars[vKV]);
+            tc::tma_load_3d(sm + V + 16384, &maps.v[4], 64, h, static_cast<int>(krow0), &bars[vKV]);
+        }
+        int32_t issued = 0;
+        for (int32_t e = 0; e < n_e; ++e) {
+            const int slot = e & 1, use = e >> 1;
+            if (use > 0) wait_or_fail(&bars[vQE + slot], (use - 1) & 1, 2, &s_fail);
+            if (failed(&s_fail)) break;
+            int64_t qr; int nq; int32_t qoff, f;
+            entry(e, qr, nq, qoff, f);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = lane + 32 * u;
+                const bool ok = r < nq;
+                slse[slot * AT + r] = ok ? p.lse[(qr + r) * H + h] * kLog2e : 0.f;
+                sD[slot * AT + r] = ok ? p.D[(qr + r) * H + h] : 0.f;
+            }
+            if (lane == 0) {
+                uint64_t *bar = &bars[vQF + slot];
+                tc::mbar_expect_tx(bar, 65536);
+                uint8_t *dq_ = sm + (slot ? Q1 : Q0), *dd = sm + (slot ? dO1 : dO0);
+                tc::tma_load_3d(dq_, &maps.q, 0, h, static_cast<int>(qr), bar);
+                tc::tma_load_3d(dq_ + 16384, &maps.q, 64, h, static_cast<int>(qr), bar);
+                tc::tma_load_3d(dd, &maps.dout, 0, h, static_cast<int>(qr), bar);
+                tc::tma_load_3d(dd + 16384, &maps.dout, 64, h, static_cast<int>(qr), bar);
+            } else {
+                mbar_arrive(&bars[vQF + slot]);
+            }
+            issued = e + 1;
+        }
+        if (lane == 0) {                                // every copy lands before the block exits
+            for (int i = 0; i < 2; ++i) {
+                const int32_t uses = issued > i ? (issued - 1 - i) / 2 + 1 : 0;
+                if (uses) tc::mbar_wait(&bars[vQF + i], (uses - 1) & 1, 1000000000LL);
+            }
+            tc::mbar_wait(&bars[vKV], 0, 1000000000LL);
+        }
+    } else if (warp == kKvMmaWarp) {
+        // ---- issuer
+        if (lane == 0 && n_e > 0) {
+            const tc::Opnd aK{tc::smem_addr(sm + K), 16384, false}, aV{tc::smem_addr(sm + V), 16384, false};
+            const uint32_t id_up = tc::idesc_bf16(AT, AD, false, true);
+            auto products = [&](int32_t e, int hf, int bb) {   // S^T and dP^T of (e, hf) into buffer bb
+                const uint32_t qa = tc::smem_addr(sm + ((e & 1) ? Q1 : Q0)) + hf * 8192;
+                const uint32_t da = tc::smem_addr(sm + ((e & 1) ? dO1 : dO0)) + hf * 8192;
+                tc::mma_op(tm + bb * 64, aK, tc::Opnd{qa, 16384, false}, AT, kHalf, AD, false);
+                tc::mma_op(tdP + bb * 64, aV, tc::Opnd{da, 16384, false}, AT, kHalf, AD, false);
+            };
+            uint32_t nc_sp0 = 0, nc_sp1 = 0, nc_u0 = 0, nc_u1 = 0;
+            wait_or_fail(&bars[vKV], 0, 0, &s_fail);
+            wait_or_fail(&bars[vQF], 0, 0, &s_fail);
             tc::fence_after_sync();
+            int32_t e = 0, hf = 0, i = 0;
+            int64_t qr; int nq; int32_t qoff, f;
+            entry(0, qr, nq, qoff, f);
+            int nh = n_steps(nq);
             if (!failed(&s_fail)) {
-                tc::mma_op(tS, tc::Opnd{tc::smem_addr(sm + K), 16384, false},
-                           tc::Opnd{tc::smem_addr(sm + (b ? Q1 : Q0)), 16384, false}, AT, AT, AD, false);
-                tc::mma_op(tP, tc::Opnd{tc::smem_addr(sm + V), 16384, false},
-                           tc::Opnd{tc::smem_addr(sm + (b ? dO1 : dO0)), 16384, false}, AT, AT, AD, false);
-                tc::mma_commit(&bars[0]);
-                ++nc0;
+                products(0, 0, 0);
+                tc::mma_commit(&bars[vSP]);
+                nc_sp0 = 1;
             }
-            if (e + 1 < n_e) { stage_q(e + 1, b ^ 1); q_issued = e + 1; }
+            while (!failed(&s_fail)) {
+                const int b = i & 1;
+                // the next step
+                int32_t ne = e, nhf = hf + 1;
+                int nnh = nh;
+                if (nhf == nh) {
+                    ne = e + 1; nhf = 0;
+                    if (ne < n_e) { entry(ne, qr, nq, qoff, f); nnh = n_steps(nq); }
+                }
+                if (ne < n_e) {
+                    if (nhf == 0) wait_or_fail(&bars[vQF + (ne & 1)], (ne >> 1) & 1, 0, &s_fail);
+                    if (i >= 1) wait_or_fail(&bars[vDVK + (b ^ 1)], ((i - 1) >> 1) & 1, 1, &s_fail);
+                    tc::fence_after_sync();
+                    if (failed(&s_fail)) break;
+                    products(ne, nhf, b ^ 1);
+                    tc::mma_commit(&bars[vSP + (b ^ 1)]);
+                    if (b) ++nc_sp0; else ++nc_sp1;
+                }
+                // dV += P^T dO_i, dK += dS^T Q_i
+                wait_or_fail(&bars[vDS + b], (i >> 1) & 1, 1, &s_fail);
+                tc::fence_after_sync();
+                if (failed(&s_fail)) break;
+                {
+                    const uint32_t qa = tc::smem_addr(sm + ((e & 1) ? Q1 : Q0)) + hf * 8192;
+                    const uint32_t da = tc::smem_addr(sm + ((e & 1) ? dO1 : dO0)) + hf * 8192;
+                    for (int kk = 0; kk < kHalf / 16; ++kk) {
+                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                        const uint64_t bdo = tc::desc_sw128_mn(da + kk * 2048, 16384);
+                        const uint64_t bq = tc::desc_sw128_mn(qa + kk * 2048, 16384);
+                        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                                     "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                                     :: "r"(tV), "r"(tm + b * 64 + kk * 8), "l"(bdo), "r"(id_up), "r"(acc) : "memory");
+                        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                                     "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                                     :: "r"(tK), "r"(tdP + b * 64 + kk * 8), "l"(bq), "r"(id_up), "r"(acc) : "memory");
+                    }
+                }
+                tc::mma_commit(&bars[vDVK + b]);
+                if (b) ++nc_u1; else ++nc_u0;
+                if (ne != e) tc::mma_commit(&bars[vQE + (e & 1)]);   // the query tile's last step
+                if (ne >= n_e) break;
+                e = ne; hf = nhf; nh = nnh; ++i;
+            }
+            if (failed(&s_fail)) {                      // drain the products still in flight
+                if (nc_sp0) tc::mbar_wait(&bars[vSP], (nc_sp0 - 1) & 1, 1000000000LL);
+                if (nc_sp1) tc::mbar_wait(&bars[vSP + 1], (nc_sp1 - 1) & 1, 1000000000LL);
+                if (nc_u0) tc::mbar_wait(&bars[vDVK], (nc_u0 - 1) & 1, 1000000000LL);
+                if (nc_u1) tc::mbar_wait(&bars[vDVK + 1], (nc_u1 - 1) & 1, 1000000000LL);
+            }
         }
-        int64_t qr; int nq; int32_t qoff, f;
-        entry(e, qr, nq, qoff, f);
-        wait_or_fail(&bars[0], e & 1, 0, &s_fail);
-        tc::fence_after_sync();
-        float sv[32], pv[32];
-        tc::tmem_ld32(tS + lane_off + cq * 32, sv);
-        tc::tmem_ld32(tP + lane_off + cq * 32, pv);
-        // P^T and dS^T for this thread's key row and 32 query columns
-        const float *lq = slse + cq * 32, *dq_ = sD + cq * 32;
-        uint32_t up[16], ud[16];
+    } else {
+        // ---- work warps: one key row and 16 query columns of a step per thread
+        const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+        const int krow = lg * 32 + lane;
+        const float c = p.scale * kLog2e;
+        int32_t i = 0;
+        for (int32_t e = 0; e < n_e; ++e) {
+            int64_t qr; int nq; int32_t qoff, f;
+            entry(e, qr, nq, qoff, f);
+            const int slot = e & 1;
+            wait_or_fail(&bars[vQF + slot], (e >> 1) & 1, 0, &s_fail);
+            const int nh = n_steps(nq);
+            for (int hf = 0; hf < nh; ++hf, ++i) {
+                const int b = i & 1;
+                wait_or_fail(&bars[vSP + b], (i >> 1) & 1, 0, &s_fail);
+                tc::fence_after_sync();
+                float sv[16], pv[16];
+                tc::tmem_ld16(tm + b * 64 + lane_off + cq * 16, sv);
+                tc::tmem_ld16(tdP + b * 64 + lane_off + cq * 16, pv);
+                const float *lq = slse + slot * AT + hf * kHalf + cq * 16;
+                const float *dq_ = sD + slot * AT + hf * kHalf + cq * 16;
+                uint32_t up[8], ud[8];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            float pr[2], ds[2];
+                for (int j = 0; j < 16; j += 2) {
+                    float pr[2], ds[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int qc = cq * 32 + i + u;
-                const bool vis = qc < nq && (f < 0 ? krow <= qoff + qc : k0 + krow < f);
-                pr[u] = vis ? ex2(fmaf(sv[i + u], c, -lq[i + u] * kLog2e)) : 0.f;
-                ds[u] = p.scale * pr[u] * (pv[i + u] - dq_[i + u]);
+                    for (int u = 0; u < 2; ++u) {
+                        const int qc = hf * kHalf + cq * 16 + j + u;
+                        const bool vis = qc < nq && (f < 0 ? krow <= qoff + qc : k0 + krow < f);
+                        pr[u] = vis ? ex2(fmaf(sv[j + u], c, -lq[j + u])) : 0.f;
+                        ds[u] = p.scale * pr[u] * (pv[j + u] - dq_[j + u]);
+                    }
+                    up[j / 2] = tc::pack_bf16(pr[0], pr[1]);
+                    ud[j / 2] = tc::pack_bf16(ds[0], ds[1]);
+                }
+                // the row's four warps have read S^T and dP^T before P^T and dS^T overwrite them
+                tc::fence_before_sync();
+                asm volatile("bar.sync %0, 128;" :: "r"(1 + lg) : "memory");
+                tc::fence_after_sync();
+                tmem_st8(tm + b * 64 + lane_off + cq * 8, up);
+                tmem_st8(tdP + b * 64 + lane_off + cq * 8, ud);
+                tc::fence_before_sync();
+                mbar_arrive(&bars[vDS + b]);
             }
-            up[i / 2] = tc::pack_bf16(pr[0], pr[1]);
-            ud[i / 2] = tc::pack_bf16(ds[0], ds[1]);
         }
-        // the row's four warps have read S^T and dP^T before P^T and dS^T overwrite them
-        tc::fence_before_sync();
-        asm volatile("bar.sync %0, 128;" :: "r"(1 + lg) : "memory");
+        if (i > 0) wait_or_fail(&bars[vDVK + ((i - 1) & 1)], ((i - 1) >> 1) & 1, 2, &s_fail);   // every update done
         tc::fence_after_sync();
-        tmem_st16(tS + lane_off + cq * 16, up);
-        tmem_st16(tP + lane_off + cq * 16, ud);
-        sync_mma();
-        if (tid == 0 && !failed(&s_fail)) {
-            // dV += P^T dO, dK += dS^T Q, A from TMEM (bf16 pairs), B MN-major
-            const uint32_t id = tc::idesc_bf16(AT, AD, false, true);
-            for (int kk = 0; kk < AT / 16; ++kk) {
-                const uint32_t acc = (e > 0 || kk > 0) ? 1u : 0u;
-                const uint64_t bdo = tc::desc_sw128_mn(tc::smem_addr(sm + (b ? dO1 : dO0)) + kk * 2048, 16384);
-                const uint64_t bq = tc::desc_sw128_mn(tc::smem_addr(sm + (b ? Q1 : Q0)) + kk * 2048, 16384);
-                asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                             "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-                             :: "r"(tV), "r"(tS + kk * 8), "l"(bdo), "r"(id), "r"(acc) : "memory");
-                asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                             "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-                             :: "r"(tK), "r"(tP + kk * 8), "l"(bq), "r"(id), "r"(acc) : "memory");
-            }
-            tc::mma_commit(&bars[2]);
-            ++nc2;
-        }
-        if (e + 1 < n_e) stage_vec(e + 1);              // every thread has read this tile's lse, D
-        tc::cp_async_commit();
     }
-    wait_or_fail(&bars[2], (n_e - 1) & 1, 2, &s_fail);
-    tc::fence_after_sync();
     __syncthreads();
-    if (!s_fail) {                                    // warp-collective loads, guarded stores
+    if (tid == 0 && s_fail) dev_error(pd, kDevErrTimeout, sk, h);
+    if (warp < kKvWorkWarps && !s_fail) {             // warp-collective loads, guarded stores
+        const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
+        const int krow = lg * 32 + lane;
+        const int cc = cq * 32;                         // 32 channels per thread
         float r[32];
-        tc::tmem_ld32(tV + lane_off + cq * 32, r);
-        if (krow < nk) store_tile_bf16(p.dv + ((krow0 + krow) * H + h) * AD + cq * 32, r, 1.f);
-        tc::tmem_ld32(tK + lane_off + cq * 32, r);
-        if (krow < nk) store_tile_bf16(p.dk + ((krow0 + krow) * H + h) * AD + cq * 32, r, 1.f);
-    }
-    tc::cp_async_wait_all();
-    if (tid == 0) {                                   // copies issued but never awaited (a timeout)
-        if (!kv_waited) tc::mbar_wait(&bars[3], 0, 1000000000LL);
-        if (q_issued > q_waited) tc::mbar_wait(&bars[4 + (q_issued & 1)], (q_issued >> 1) & 1, 1000000000LL);
-    }
-    if (s_fail && tid == 0) {
-        dev_error(pd, kDevErrTimeout, sk, h);
-        const uint32_t nc[3] = {nc0, 0u, nc2};
-#pragma unroll
-        for (int i = 0; i < 3; ++i)
-            if (nc[i]) tc::mbar_wait(&bars[i], (nc[i] - 1) & 1, 1000000000LL);
+        tc::tmem_ld32(tV + lane_off + cc, r);
+        if (n_e == 0) for (int j = 0; j < 32; ++j) r[j] = 0.f;
+        if (krow < nk) store_tile_bf16(p.dv + ((krow0 + krow) * H + h) * AD + cc, r, 1.f);
+        tc::tmem_ld32(tK + lane_off + cc, r);
+        if (n_e == 0) for (int j = 0; j < 32; ++j) r[j] = 0.f;
+        if (krow < nk) store_tile_bf16(p.dk + ((krow0 + krow) * H + h) * AD + cc, r, 1.f);
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (warp == 0) tc::tmem_dealloc(tm, 512);
+    if (warp == kKvMmaWarp) tc::tmem_dealloc(tm, 512);
 }
 
 }  // namespace
@@ -989,7 +1061,7 @@ int harts_attn_bwd(const harts_plan *P, const harts_attn_bwd_args *a, harts_stre
         e = launch_big(attn_bwd_dq_tc, static_cast<unsigned>(int64_t(P->image.n_qt) * p.H), kDqThreads, bq_sm::bytes, st, p,
                        P->view, maps);
     if (e == cudaSuccess)
-        e = launch_big(attn_bwd_dkdv_tc, static_cast<unsigned>(int64_t(P->image.n_kt) * p.H), ANT, bk_sm::bytes, st, p,
+        e = launch_big(attn_bwd_dkdv_tc, static_cast<unsigned>(int64_t(P->image.n_kt) * p.H), kKvThreads, bk_sm::bytes, st, p,
                        P->view, maps);
     if (e != cudaSuccess) { set_error(std::string("attention backward launch: ") + cudaGetErrorString(e)); return HARTS_ECUDA; }
     set_error("");
