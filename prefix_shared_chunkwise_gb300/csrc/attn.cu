@@ -688,7 +688,8 @@ constexpr int kHalf = AT / 2;                     // queries per step
 namespace bk_sm {
 constexpr uint32_t K = 0, V = 32768, Q0 = 65536, Q1 = 98304, dO0 = 131072, dO1 = 163840;
 constexpr uint32_t Vec = 196608;                  // [2 slots][128] lse * log2 e, then [2 slots][128] D
-constexpr uint32_t bytes = Vec + 2048 + 1024;     // + alignment slack
+constexpr uint32_t Ent = Vec + 2048;              // [2 slots] the query tile's nq, qoff, f
+constexpr uint32_t bytes = Ent + 32 + 1024;       // + alignment slack
 }  // namespace bk_sm
 
 // Barriers of the dK / dV kernel: K and V landed; per Q slot: Q, dO, lse and D of a query
@@ -720,6 +721,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
     float *slse = reinterpret_cast<float *>(sm + Vec), *sD = slse + 2 * AT;
+    int32_t *sent = reinterpret_cast<int32_t *>(sm + Ent);   // per slot: nq, qoff, f (decoded by the loader)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = warp & 3, cq = (warp >> 2) & 3;
     const int H = p.H;
     const int32_t h = blockIdx.x % H, ki = blockIdx.x / H;
@@ -759,7 +761,8 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
 
     if (warp == kKvLoadWarp) {
         // ---- loader warp: K and V once; per query tile Q and dO by tiled TMA (lane 0), lse
-        // and D by plain loads (4 rows per lane); all 32 lanes arrive on the slot's barrier
+        // and D by plain loads (4 rows per lane) and the tile's decoded entry; all 32 lanes
+        // arrive on the slot's barrier, so the consumers never wait on the plan tables
         if (lane == 0) {
             tc::mbar_expect_tx(&bars[vKV], 65536);
             tc::tma_load_3d(sm + K, &maps.k[4], 0, h, static_cast<int>(krow0), &bars[vKV]);
@@ -782,6 +785,9 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
                 sD[slot * AT + r] = ok ? p.D[(qr + r) * H + h] : 0.f;
             }
             if (lane == 0) {
+                sent[4 * slot] = nq;
+                sent[4 * slot + 1] = qoff;
+                sent[4 * slot + 2] = f;
                 uint64_t *bar = &bars[vQF + slot];
                 tc::mbar_expect_tx(bar, 65536);
                 uint8_t *dq_ = sm + (slot ? Q1 : Q0), *dd = sm + (slot ? dO1 : dO0);
@@ -817,9 +823,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
             wait_or_fail(&bars[vQF], 0, 0, &s_fail);
             tc::fence_after_sync();
             int32_t e = 0, hf = 0, i = 0;
-            int64_t qr; int nq; int32_t qoff, f;
-            entry(0, qr, nq, qoff, f);
-            int nh = n_steps(nq);
+            int nh = n_steps(sent[0]);
             if (!failed(&s_fail)) {
                 products(0, 0, 0);
                 tc::mma_commit(&bars[vSP]);
@@ -830,12 +834,12 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
                 // the next step
                 int32_t ne = e, nhf = hf + 1;
                 int nnh = nh;
-                if (nhf == nh) {
-                    ne = e + 1; nhf = 0;
-                    if (ne < n_e) { entry(ne, qr, nq, qoff, f); nnh = n_steps(nq); }
-                }
+                if (nhf == nh) { ne = e + 1; nhf = 0; }
                 if (ne < n_e) {
-                    if (nhf == 0) wait_or_fail(&bars[vQF + (ne & 1)], (ne >> 1) & 1, 0, &s_fail);
+                    if (nhf == 0) {                     // a new query tile: its slot has landed
+                        wait_or_fail(&bars[vQF + (ne & 1)], (ne >> 1) & 1, 0, &s_fail);
+                        nnh = n_steps(sent[4 * (ne & 1)]);
+                    }
                     if (i >= 1) wait_or_fail(&bars[vDVK + (b ^ 1)], ((i - 1) >> 1) & 1, 1, &s_fail);
                     tc::fence_after_sync();
                     if (failed(&s_fail)) break;
@@ -882,10 +886,9 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
         const float c = p.scale * kLog2e;
         int32_t i = 0;
         for (int32_t e = 0; e < n_e; ++e) {
-            int64_t qr; int nq; int32_t qoff, f;
-            entry(e, qr, nq, qoff, f);
             const int slot = e & 1;
             wait_or_fail(&bars[vQF + slot], (e >> 1) & 1, 0, &s_fail);
+            const int nq = sent[4 * slot], qoff = sent[4 * slot + 1], f = sent[4 * slot + 2];
             const int nh = n_steps(nq);
             for (int hf = 0; hf < nh; ++hf, ++i) {
                 const int b = i & 1;
