@@ -640,16 +640,27 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p,
             mbar_arrive(&bars[qPE]);
             const int32_t lim = vis - (j * AT + cq * 32);
             uint32_t ud[16];
+            if (__all_sync(0xffffffffu, vb == 0xffffffffu && lim >= 31)) {   // no masked column
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                float ds[2];
+                for (int i = 0; i < 32; i += 2) {
+                    float ds[2];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int ii = i + u;
-                    const float pr = (((vb >> ii) & 1u) && ii <= lim) ? ex2(fmaf(sv[ii], c, -lse2)) : 0.f;
-                    ds[u] = p.scale * pr * (pv[ii] - Dq);
+                    for (int u = 0; u < 2; ++u)
+                        ds[u] = p.scale * ex2(fmaf(sv[i + u], c, -lse2)) * (pv[i + u] - Dq);
+                    ud[i / 2] = tc::pack_bf16(ds[0], ds[1]);
                 }
-                ud[i / 2] = tc::pack_bf16(ds[0], ds[1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int ii = i + u;
+                        const float pr = (((vb >> ii) & 1u) && ii <= lim) ? ex2(fmaf(sv[ii], c, -lse2)) : 0.f;
+                        ds[u] = p.scale * pr * (pv[ii] - Dq);
+                    }
+                    ud[i / 2] = tc::pack_bf16(ds[0], ds[1]);
+                }
             }
             // the row's four warps have read S_j before dS_j overwrites it
             tc::fence_before_sync();
@@ -900,18 +911,36 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
                 const float *lq = slse + slot * AT + hf * kHalf + cq * 16;
                 const float *dq_ = sD + slot * AT + hf * kHalf + cq * 16;
                 uint32_t up[8], ud[8];
+                // every column of the warp visible (the visibility is monotone in the query
+                // column): no per-element mask
+                const int qc0 = hf * kHalf + cq * 16;
+                const bool all_vis = qc0 + 15 < nq && (f < 0 ? krow <= qoff + qc0 : k0 + krow < f);
+                if (__all_sync(0xffffffffu, all_vis)) {
 #pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    float pr[2], ds[2];
+                    for (int j = 0; j < 16; j += 2) {
+                        float pr[2], ds[2];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int qc = hf * kHalf + cq * 16 + j + u;
-                        const bool vis = qc < nq && (f < 0 ? krow <= qoff + qc : k0 + krow < f);
-                        pr[u] = vis ? ex2(fmaf(sv[j + u], c, -lq[j + u])) : 0.f;
-                        ds[u] = p.scale * pr[u] * (pv[j + u] - dq_[j + u]);
+                        for (int u = 0; u < 2; ++u) {
+                            pr[u] = ex2(fmaf(sv[j + u], c, -lq[j + u]));
+                            ds[u] = p.scale * pr[u] * (pv[j + u] - dq_[j + u]);
+                        }
+                        up[j / 2] = tc::pack_bf16(pr[0], pr[1]);
+                        ud[j / 2] = tc::pack_bf16(ds[0], ds[1]);
                     }
-                    up[j / 2] = tc::pack_bf16(pr[0], pr[1]);
-                    ud[j / 2] = tc::pack_bf16(ds[0], ds[1]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        float pr[2], ds[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int qc = qc0 + j + u;
+                            const bool vis = qc < nq && (f < 0 ? krow <= qoff + qc : k0 + krow < f);
+                            pr[u] = vis ? ex2(fmaf(sv[j + u], c, -lq[j + u])) : 0.f;
+                            ds[u] = p.scale * pr[u] * (pv[j + u] - dq_[j + u]);
+                        }
+                        up[j / 2] = tc::pack_bf16(pr[0], pr[1]);
+                        ud[j / 2] = tc::pack_bf16(ds[0], ds[1]);
+                    }
                 }
                 // the row's four warps have read S^T and dP^T before P^T and dS^T overwrite them
                 tc::fence_before_sync();
