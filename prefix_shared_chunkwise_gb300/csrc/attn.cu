@@ -410,7 +410,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
 //   dV_j = sum_t P_tj dO_t,  dS_tj = scale P_tj (dP_tj - D_t) with dP = dO V^T,
 //   dQ_t = sum_j dS_tj K_j,  dK_j = sum_t dS_tj Q_t,
 // every query row once (its own compact row), over its view.  P is recomputed from the
-// forward's log-sum-exp.  dQ: one block per (query tile, head) over the view's key tiles,
+// forward's log-sum-exp.  The kernels form dS / scale = P (dP - D) (bf16 into the products)
+// and apply the scale once, to dQ and dK as they are stored.
+// dQ: one block per (query tile, head) over the view's key tiles,
 // as the forward.  dK, dV: one block per (key tile of a sequence's own rows, head) over
 // the query tiles that see it (planner lists: the sequence's own tiles, causal, and the
 // tiles of every sequence whose prefix runs through it, a prefix of the key tile
@@ -646,7 +648,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p,
                     float ds[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u)
-                        ds[u] = p.scale * ex2(fmaf(sv[i + u], c, -lse2)) * (pv[i + u] - Dq);
+                        ds[u] = ex2(fmaf(sv[i + u], c, -lse2)) * (pv[i + u] - Dq);
                     ud[i / 2] = tc::pack_bf16(ds[0], ds[1]);
                 }
             } else {
@@ -657,7 +659,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p,
                     for (int u = 0; u < 2; ++u) {
                         const int ii = i + u;
                         const float pr = (((vb >> ii) & 1u) && ii <= lim) ? ex2(fmaf(sv[ii], c, -lse2)) : 0.f;
-                        ds[u] = p.scale * pr * (pv[ii] - Dq);
+                        ds[u] = pr * (pv[ii] - Dq);
                     }
                     ud[i / 2] = tc::pack_bf16(ds[0], ds[1]);
                 }
@@ -680,7 +682,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p,
         const int qrow = lg * 32 + lane;
         float r[32];
         tc::tmem_ld32(tQ + lane_off + cq * 32, r);
-        if (qrow < nq) store_tile_bf16(p.dq + ((static_cast<int64_t>(row0) + q0 + qrow) * H + h) * AD + cq * 32, r, 1.f);
+        if (qrow < nq) store_tile_bf16(p.dq + ((static_cast<int64_t>(row0) + q0 + qrow) * H + h) * AD + cq * 32, r, p.scale);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -922,7 +924,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
                             pr[u] = ex2(fmaf(sv[j + u], c, -lq[j + u]));
-                            ds[u] = p.scale * pr[u] * (pv[j + u] - dq_[j + u]);
+                            ds[u] = pr[u] * (pv[j + u] - dq_[j + u]);
                         }
                         up[j / 2] = tc::pack_bf16(pr[0], pr[1]);
                         ud[j / 2] = tc::pack_bf16(ds[0], ds[1]);
@@ -936,7 +938,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
                             const int qc = qc0 + j + u;
                             const bool vis = qc < nq && (f < 0 ? krow <= qoff + qc : k0 + krow < f);
                             pr[u] = vis ? ex2(fmaf(sv[j + u], c, -lq[j + u])) : 0.f;
-                            ds[u] = p.scale * pr[u] * (pv[j + u] - dq_[j + u]);
+                            ds[u] = pr[u] * (pv[j + u] - dq_[j + u]);
                         }
                         up[j / 2] = tc::pack_bf16(pr[0], pr[1]);
                         ud[j / 2] = tc::pack_bf16(ds[0], ds[1]);
@@ -967,7 +969,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
         if (krow < nk) store_tile_bf16(p.dv + ((krow0 + krow) * H + h) * AD + cc, r, 1.f);
         tc::tmem_ld32(tK + lane_off + cc, r);
         if (n_e == 0) for (int j = 0; j < 32; ++j) r[j] = 0.f;
-        if (krow < nk) store_tile_bf16(p.dk + ((krow0 + krow) * H + h) * AD + cc, r, 1.f);
+        if (krow < nk) store_tile_bf16(p.dk + ((krow0 + krow) * H + h) * AD + cc, r, p.scale);
     }
     tc::fence_before_sync();
     __syncthreads();
