@@ -149,6 +149,69 @@ enum FwdBar { bQ = 0, bKF = 1, bKE = 4, bVF = 7, bVE = 9, bSF = 11, bSE = 13, bP
 
 // O (+)= P V with P (bf16, packed in pairs) read from TMEM: one row per lane, 8 columns per
 // 16 keys.
+// Two TMEM loads of one warp, issued back to back and waited for once; the wait names the
+// destination registers so that no use of them can move above it.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&u)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld16x2(uint32_t (&a)[16], uint32_t (&b)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                   "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]),
+                   "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]),
+                   "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])
+                 :: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, float (&ra)[16], uint32_t tb, float (&rb)[16]) {
+    uint32_t(&ua)[16] = reinterpret_cast<uint32_t(&)[16]>(ra);
+    uint32_t(&ub)[16] = reinterpret_cast<uint32_t(&)[16]>(rb);
+    tmem_ld16_issue(ta, ua);
+    tmem_ld16_issue(tb, ub);
+    tmem_wait_ld16x2(ua, ub);
+}
+
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&u)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld32x2(uint32_t (&a)[32], uint32_t (&b)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]), "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]), "+r"(a[31]),
+                   "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]), "+r"(b[16]), "+r"(b[17]), "+r"(b[18]), "+r"(b[19]), "+r"(b[20]), "+r"(b[21]), "+r"(b[22]), "+r"(b[23]), "+r"(b[24]), "+r"(b[25]), "+r"(b[26]), "+r"(b[27]), "+r"(b[28]), "+r"(b[29]), "+r"(b[30]), "+r"(b[31])
+                 :: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, float (&ra)[32], uint32_t tb, float (&rb)[32]) {
+    uint32_t(&ua)[32] = reinterpret_cast<uint32_t(&)[32]>(ra);
+    uint32_t(&ub)[32] = reinterpret_cast<uint32_t(&)[32]>(rb);
+    tmem_ld32_issue(ta, ua);
+    tmem_ld32_issue(tb, ub);
+    tmem_wait_ld32x2(ua, ub);
+}
+
+// Two 8-column TMEM stores of one warp, then one wait.
+__device__ __forceinline__ void tmem_st8x2(uint32_t ta, const uint32_t (&a)[8], uint32_t tb, const uint32_t (&b)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "r"(ta), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
+                 : "memory");
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "r"(tb), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]), "r"(b[6]), "r"(b[7])
+                 : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // 16 columns of one TMEM lane per thread (warp-collective), then wait for the stores.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&u)[16]) {
     asm volatile(
@@ -297,15 +360,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
             wait_or_fail(&bars[bSF + b], (kt >> 1) & 1, 1, &s_fail);
             tc::fence_after_sync();
             float s[64];
-            {
-                float r[32];
-                tc::tmem_ld32(tm + b * 128 + lane_off + half * 64, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[i] = r[i];
-                tc::tmem_ld32(tm + b * 128 + lane_off + half * 64 + 32, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[32 + i] = r[i];
-            }
+            tmem_ld32x2(tm + b * 128 + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(s),
+                        tm + b * 128 + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(s + 32));
             tc::fence_before_sync();
             mbar_arrive(&bars[bSE + b]);
             const int32_t lim = vis - (kt * AT + half * 64);
@@ -636,8 +692,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p,
             wait_or_fail(&bars[qSP + b], (j >> 1) & 1, 0, &s_fail);
             tc::fence_after_sync();
             float sv[32], pv[32];
-            tc::tmem_ld32(tS + lane_off + cq * 32, sv);
-            tc::tmem_ld32(tP + lane_off + cq * 32, pv);
+            tmem_ld32x2(tS + lane_off + cq * 32, sv, tP + lane_off + cq * 32, pv);
             tc::fence_before_sync();
             mbar_arrive(&bars[qPE]);
             const int32_t lim = vis - (j * AT + cq * 32);
@@ -709,14 +764,6 @@ constexpr uint32_t bytes = Ent + 32 + 1024;       // + alignment slack
 // tile landed (32 loader lanes + the copy bytes), the slot free again; per step buffer:
 // S^T and dP^T done, P^T and dS^T written, dV and dK updated (also every earlier product).
 enum KvBar { vKV = 0, vQF = 1, vQE = 3, vSP = 5, vDS = 7, vDVK = 9, vN = 11 };
-
-// 8 columns of one TMEM lane per thread (warp-collective), then wait for the stores.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&u)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                 :: "r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
-                    "r"(u[7]) : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
 
 __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams p, PlanDev pd,
                                                                   const __grid_constant__ AttnMaps maps) {
@@ -908,8 +955,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
                 wait_or_fail(&bars[vSP + b], (i >> 1) & 1, 0, &s_fail);
                 tc::fence_after_sync();
                 float sv[16], pv[16];
-                tc::tmem_ld16(tm + b * 64 + lane_off + cq * 16, sv);
-                tc::tmem_ld16(tdP + b * 64 + lane_off + cq * 16, pv);
+                tmem_ld16x2(tm + b * 64 + lane_off + cq * 16, sv, tdP + b * 64 + lane_off + cq * 16, pv);
                 const float *lq = slse + slot * AT + hf * kHalf + cq * 16;
                 const float *dq_ = sD + slot * AT + hf * kHalf + cq * 16;
                 uint32_t up[8], ud[8];
@@ -948,8 +994,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
                 tc::fence_before_sync();
                 asm volatile("bar.sync %0, 128;" :: "r"(1 + lg) : "memory");
                 tc::fence_after_sync();
-                tmem_st8(tm + b * 64 + lane_off + cq * 8, up);
-                tmem_st8(tdP + b * 64 + lane_off + cq * 8, ud);
+                tmem_st8x2(tm + b * 64 + lane_off + cq * 8, up, tdP + b * 64 + lane_off + cq * 8, ud);
                 tc::fence_before_sync();
                 mbar_arrive(&bars[vDS + b]);
             }
