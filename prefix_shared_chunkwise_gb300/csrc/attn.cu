@@ -201,14 +201,20 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, float (&ra)[32], uint32
     tmem_wait_ld32x2(ua, ub);
 }
 
-// Two 8-column TMEM stores of one warp, then one wait.
-__device__ __forceinline__ void tmem_st8x2(uint32_t ta, const uint32_t (&a)[8], uint32_t tb, const uint32_t (&b)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                 :: "r"(ta), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
-                 : "memory");
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                 :: "r"(tb), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]), "r"(b[6]), "r"(b[7])
-                 : "memory");
+// Two 16-column TMEM stores of one warp, then one wait.
+__device__ __forceinline__ void tmem_st16x2(uint32_t ta, const uint32_t (&a)[16], uint32_t tb, const uint32_t (&b)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        :: "r"(ta), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
+           "r"(a[8]), "r"(a[9]), "r"(a[10]), "r"(a[11]), "r"(a[12]), "r"(a[13]), "r"(a[14]), "r"(a[15])
+        : "memory");
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        :: "r"(tb), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]), "r"(b[6]), "r"(b[7]),
+           "r"(b[8]), "r"(b[9]), "r"(b[10]), "r"(b[11]), "r"(b[12]), "r"(b[13]), "r"(b[14]), "r"(b[15])
+        : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
@@ -745,12 +751,13 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p,
     if (warp == kDqMmaWarp) tc::tmem_dealloc(tm, 512);
 }
 
-// dK / dV kernel roles: 16 warps form P^T and dS^T (lg = warp & 3: 32 key rows; cq = warp >>
-// 2: 16 query columns of a 64-query half), one thread issues the products, one warp loads
-// K, V once and then Q, dO (tiled TMA) and lse, D (plain loads into shared memory) per
-// query tile.
+// dK / dV kernel roles: two groups of 8 warps form P^T and dS^T, group g the g-th 64-query
+// half of every query tile (lg = warp & 3: 32 key rows; ch = (warp >> 2) & 1: 32 query
+// columns of the half), so that two consecutive steps are formed at once; one thread
+// issues the products; one warp loads K, V once and then Q, dO (tiled TMA) and lse, D
+// (plain loads into shared memory) per query tile.
 constexpr int kKvWorkWarps = 16, kKvMmaWarp = 16, kKvLoadWarp = 17, kKvThreads = 18 * 32;
-constexpr int kKvWork = kKvWorkWarps * 32;
+constexpr int kKvGroup = 8 * 32;                  // threads of one work group
 constexpr int kHalf = AT / 2;                     // queries per step
 
 namespace bk_sm {
@@ -761,19 +768,22 @@ constexpr uint32_t bytes = Ent + 32 + 1024;       // + alignment slack
 }  // namespace bk_sm
 
 // Barriers of the dK / dV kernel: K and V landed; per Q slot: Q, dO, lse and D of a query
-// tile landed (32 loader lanes + the copy bytes), the slot free again; per step buffer:
-// S^T and dP^T done, P^T and dS^T written, dV and dK updated (also every earlier product).
+// tile landed (lane 0's expect_tx, the 32 loader lanes' writes, the copy bytes), the slot
+// free again; per step buffer
+// (= per work group): S^T and dP^T done, P^T and dS^T written (the group's 256 threads),
+// dV and dK updated (also every earlier product).
 enum KvBar { vKV = 0, vQF = 1, vQE = 3, vSP = 5, vDS = 7, vDVK = 9, vN = 11 };
 
 __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams p, PlanDev pd,
                                                                   const __grid_constant__ AttnMaps maps) {
     // One block per (key tile of a sequence's own rows, head) over the query tiles that see
-    // it, each taken as one or two 64-query steps (a tile of at most 64 rows is one step).
-    // Step i: S^T = K Q_i^T and dP^T = V dO_i^T into TMEM buffer i mod 2 (64 columns each),
-    // P^T and dS^T (bf16 pairs) written over them, dV += P^T dO_i and dK += dS^T Q_i read
-    // them there.  The issuing thread runs a step ahead: S^T, dP^T of step i + 1 once dV, dK
-    // of step i - 1 have released that buffer, so the tensor pipe works through step i - 1's
-    // updates and step i + 1's products while the work warps form step i.
+    // it, each taken as two 64-query steps (the second is empty for a tile of at most 64
+    // rows: no products, the barriers still advance).  Step i = 2 e + g: S^T = K Q_i^T and
+    // dP^T = V dO_i^T into TMEM buffer g (64 columns each), P^T and dS^T (bf16 pairs)
+    // written over them by work group g, dV += P^T dO_i and dK += dS^T Q_i read them there.
+    // The issuing thread runs a step ahead: S^T, dP^T of step i + 1 once dV, dK of step
+    // i - 1 have released that buffer, so the tensor pipe works through step i - 1's
+    // updates and step i + 1's products while the groups form steps i and i + 1.
     using namespace bk_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
@@ -797,15 +807,14 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
         nq = min(AT, pd.seq_nown[s_] - t_ * AT);
         qoff = t_ * AT - k0;                          // query local position minus key tile start
     };
-    auto n_steps = [&](int nq) { return nq > kHalf ? 2 : 1; };
 
     if (tid == 0) {
         tc::mbar_init(&bars[vKV], 1);
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&bars[vQF + i], 32);
+            tc::mbar_init(&bars[vQF + i], 33);       // lane 0's expect_tx + 32 lanes' writes
             tc::mbar_init(&bars[vQE + i], 1);
             tc::mbar_init(&bars[vSP + i], 1);
-            tc::mbar_init(&bars[vDS + i], kKvWork);
+            tc::mbar_init(&bars[vDS + i], kKvGroup);
             tc::mbar_init(&bars[vDVK + i], 1);
         }
         tc::fence_mbar_init();
@@ -837,6 +846,18 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
             if (failed(&s_fail)) break;
             int64_t qr; int nq; int32_t qoff, f;
             entry(e, qr, nq, qoff, f);
+            if (lane == 0) {                            // the copies first: they take longest
+                uint64_t *bar = &bars[vQF + slot];
+                tc::mbar_expect_tx(bar, 65536);         // lane 0's first arrival
+                uint8_t *dq_ = sm + (slot ? Q1 : Q0), *dd = sm + (slot ? dO1 : dO0);
+                tc::tma_load_3d(dq_, &maps.q, 0, h, static_cast<int>(qr), bar);
+                tc::tma_load_3d(dq_ + 16384, &maps.q, 64, h, static_cast<int>(qr), bar);
+                tc::tma_load_3d(dd, &maps.dout, 0, h, static_cast<int>(qr), bar);
+                tc::tma_load_3d(dd + 16384, &maps.dout, 64, h, static_cast<int>(qr), bar);
+                sent[4 * slot] = nq;
+                sent[4 * slot + 1] = qoff;
+                sent[4 * slot + 2] = f;
+            }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int r = lane + 32 * u;
@@ -844,20 +865,7 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
                 slse[slot * AT + r] = ok ? p.lse[(qr + r) * H + h] * kLog2e : 0.f;
                 sD[slot * AT + r] = ok ? p.D[(qr + r) * H + h] : 0.f;
             }
-            if (lane == 0) {
-                sent[4 * slot] = nq;
-                sent[4 * slot + 1] = qoff;
-                sent[4 * slot + 2] = f;
-                uint64_t *bar = &bars[vQF + slot];
-                tc::mbar_expect_tx(bar, 65536);
-                uint8_t *dq_ = sm + (slot ? Q1 : Q0), *dd = sm + (slot ? dO1 : dO0);
-                tc::tma_load_3d(dq_, &maps.q, 0, h, static_cast<int>(qr), bar);
-                tc::tma_load_3d(dq_ + 16384, &maps.q, 64, h, static_cast<int>(qr), bar);
-                tc::tma_load_3d(dd, &maps.dout, 0, h, static_cast<int>(qr), bar);
-                tc::tma_load_3d(dd + 16384, &maps.dout, 64, h, static_cast<int>(qr), bar);
-            } else {
-                mbar_arrive(&bars[vQF + slot]);
-            }
+            mbar_arrive(&bars[vQF + slot]);             // every lane, after its writes
             issued = e + 1;
         }
         if (lane == 0) {                                // every copy lands before the block exits
@@ -882,38 +890,37 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
             wait_or_fail(&bars[vKV], 0, 0, &s_fail);
             wait_or_fail(&bars[vQF], 0, 0, &s_fail);
             tc::fence_after_sync();
-            int32_t e = 0, hf = 0, i = 0;
-            int nh = n_steps(sent[0]);
+            int nq_cur = sent[0], nq_nx = nq_cur;        // rows of the current / next step's tile
             if (!failed(&s_fail)) {
-                products(0, 0, 0);
+                products(0, 0, 0);                      // step 0 is never empty
                 tc::mma_commit(&bars[vSP]);
                 nc_sp0 = 1;
             }
-            while (!failed(&s_fail)) {
+            const int32_t n_st = 2 * n_e;
+            for (int32_t i = 0; i < n_st && !failed(&s_fail); ++i) {
                 const int b = i & 1;
-                // the next step
-                int32_t ne = e, nhf = hf + 1;
-                int nnh = nh;
-                if (nhf == nh) { ne = e + 1; nhf = 0; }
-                if (ne < n_e) {
-                    if (nhf == 0) {                     // a new query tile: its slot has landed
+                const int32_t e = i >> 1;
+                if (i + 1 < n_st) {                     // the next step's products
+                    const int32_t ne = (i + 1) >> 1;
+                    const int nb = b ^ 1;
+                    if (nb == 0) {                      // a new query tile: its slot has landed
                         wait_or_fail(&bars[vQF + (ne & 1)], (ne >> 1) & 1, 0, &s_fail);
-                        nnh = n_steps(sent[4 * (ne & 1)]);
+                        nq_nx = sent[4 * (ne & 1)];
                     }
-                    if (i >= 1) wait_or_fail(&bars[vDVK + (b ^ 1)], ((i - 1) >> 1) & 1, 1, &s_fail);
+                    if (i >= 1) wait_or_fail(&bars[vDVK + nb], ((i - 1) >> 1) & 1, 1, &s_fail);
                     tc::fence_after_sync();
                     if (failed(&s_fail)) break;
-                    products(ne, nhf, b ^ 1);
-                    tc::mma_commit(&bars[vSP + (b ^ 1)]);
-                    if (b) ++nc_sp0; else ++nc_sp1;
+                    if (nb == 0 || nq_nx > kHalf) products(ne, nb, nb);
+                    tc::mma_commit(&bars[vSP + nb]);
+                    if (nb) ++nc_sp1; else ++nc_sp0;
                 }
                 // dV += P^T dO_i, dK += dS^T Q_i
                 wait_or_fail(&bars[vDS + b], (i >> 1) & 1, 1, &s_fail);
                 tc::fence_after_sync();
                 if (failed(&s_fail)) break;
-                {
-                    const uint32_t qa = tc::smem_addr(sm + ((e & 1) ? Q1 : Q0)) + hf * 8192;
-                    const uint32_t da = tc::smem_addr(sm + ((e & 1) ? dO1 : dO0)) + hf * 8192;
+                if (b == 0 || nq_cur > kHalf) {
+                    const uint32_t qa = tc::smem_addr(sm + ((e & 1) ? Q1 : Q0)) + b * 8192;
+                    const uint32_t da = tc::smem_addr(sm + ((e & 1) ? dO1 : dO0)) + b * 8192;
                     for (int kk = 0; kk < kHalf / 16; ++kk) {
                         const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
                         const uint64_t bdo = tc::desc_sw128_mn(da + kk * 2048, 16384);
@@ -928,9 +935,10 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
                 }
                 tc::mma_commit(&bars[vDVK + b]);
                 if (b) ++nc_u1; else ++nc_u0;
-                if (ne != e) tc::mma_commit(&bars[vQE + (e & 1)]);   // the query tile's last step
-                if (ne >= n_e) break;
-                e = ne; hf = nhf; nh = nnh; ++i;
+                if (b == 1) {                           // the query tile's last step
+                    tc::mma_commit(&bars[vQE + (e & 1)]);
+                    nq_cur = nq_nx;
+                }
             }
             if (failed(&s_fail)) {                      // drain the products still in flight
                 if (nc_sp0) tc::mbar_wait(&bars[vSP], (nc_sp0 - 1) & 1, 1000000000LL);
@@ -940,28 +948,34 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
             }
         }
     } else {
-        // ---- work warps: one key row and 16 query columns of a step per thread
+        // ---- work group g = warp >> 3: one key row and 32 query columns of step 2 e + g per
+        // thread, in two passes of 16
+        const int g = warp >> 3, ch = (warp >> 2) & 1;
         const uint32_t lane_off = static_cast<uint32_t>(lg * 32) << 16;
         const int krow = lg * 32 + lane;
         const float c = p.scale * kLog2e;
-        int32_t i = 0;
+        const uint32_t tSb = tm + g * 64, tPb = tdP + g * 64;
         for (int32_t e = 0; e < n_e; ++e) {
             const int slot = e & 1;
             wait_or_fail(&bars[vQF + slot], (e >> 1) & 1, 0, &s_fail);
             const int nq = sent[4 * slot], qoff = sent[4 * slot + 1], f = sent[4 * slot + 2];
-            const int nh = n_steps(nq);
-            for (int hf = 0; hf < nh; ++hf, ++i) {
-                const int b = i & 1;
-                wait_or_fail(&bars[vSP + b], (i >> 1) & 1, 0, &s_fail);
-                tc::fence_after_sync();
+            wait_or_fail(&bars[vSP + g], e & 1, 0, &s_fail);
+            if (g == 1 && nq <= kHalf) {                // empty second half: nothing to form
+                mbar_arrive(&bars[vDS + g]);
+                continue;
+            }
+            tc::fence_after_sync();
+            uint32_t up[16], ud[16];
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                const int col = ch * 32 + part * 16;    // query column within the half
                 float sv[16], pv[16];
-                tmem_ld16x2(tm + b * 64 + lane_off + cq * 16, sv, tdP + b * 64 + lane_off + cq * 16, pv);
-                const float *lq = slse + slot * AT + hf * kHalf + cq * 16;
-                const float *dq_ = sD + slot * AT + hf * kHalf + cq * 16;
-                uint32_t up[8], ud[8];
+                tmem_ld16x2(tSb + lane_off + col, sv, tPb + lane_off + col, pv);
+                const float *lq = slse + slot * AT + g * kHalf + col;
+                const float *dq_ = sD + slot * AT + g * kHalf + col;
                 // every column of the warp visible (the visibility is monotone in the query
                 // column): no per-element mask
-                const int qc0 = hf * kHalf + cq * 16;
+                const int qc0 = g * kHalf + col;
                 const bool all_vis = qc0 + 15 < nq && (f < 0 ? krow <= qoff + qc0 : k0 + krow < f);
                 if (__all_sync(0xffffffffu, all_vis)) {
 #pragma unroll
@@ -972,8 +986,8 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
                             pr[u] = ex2(fmaf(sv[j + u], c, -lq[j + u]));
                             ds[u] = pr[u] * (pv[j + u] - dq_[j + u]);
                         }
-                        up[j / 2] = tc::pack_bf16(pr[0], pr[1]);
-                        ud[j / 2] = tc::pack_bf16(ds[0], ds[1]);
+                        up[part * 8 + j / 2] = tc::pack_bf16(pr[0], pr[1]);
+                        ud[part * 8 + j / 2] = tc::pack_bf16(ds[0], ds[1]);
                     }
                 } else {
 #pragma unroll
@@ -986,20 +1000,22 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
                             pr[u] = vis ? ex2(fmaf(sv[j + u], c, -lq[j + u])) : 0.f;
                             ds[u] = pr[u] * (pv[j + u] - dq_[j + u]);
                         }
-                        up[j / 2] = tc::pack_bf16(pr[0], pr[1]);
-                        ud[j / 2] = tc::pack_bf16(ds[0], ds[1]);
+                        up[part * 8 + j / 2] = tc::pack_bf16(pr[0], pr[1]);
+                        ud[part * 8 + j / 2] = tc::pack_bf16(ds[0], ds[1]);
                     }
                 }
-                // the row's four warps have read S^T and dP^T before P^T and dS^T overwrite them
-                tc::fence_before_sync();
-                asm volatile("bar.sync %0, 128;" :: "r"(1 + lg) : "memory");
-                tc::fence_after_sync();
-                tmem_st8x2(tm + b * 64 + lane_off + cq * 8, up, tdP + b * 64 + lane_off + cq * 8, ud);
-                tc::fence_before_sync();
-                mbar_arrive(&bars[vDS + b]);
             }
+            // the row's two warps of the group have read S^T and dP^T before P^T and dS^T
+            // overwrite them
+            tc::fence_before_sync();
+            asm volatile("bar.sync %0, 64;" :: "r"(1 + g * 4 + lg) : "memory");
+            tc::fence_after_sync();
+            tmem_st16x2(tSb + lane_off + ch * 16, up, tPb + lane_off + ch * 16, ud);
+            tc::fence_before_sync();
+            mbar_arrive(&bars[vDS + g]);
         }
-        if (i > 0) wait_or_fail(&bars[vDVK + ((i - 1) & 1)], ((i - 1) >> 1) & 1, 2, &s_fail);   // every update done
+        // the group of the last step waits for it: its update is the last product issued
+        if (n_e > 0 && g == 1) wait_or_fail(&bars[vDVK + 1], (n_e - 1) & 1, 2, &s_fail);
         tc::fence_after_sync();
     }
     __syncthreads();
