@@ -511,8 +511,9 @@ struct AttnBwdParams {
 };
 
 // dQ kernel roles: 16 warps form dS (lg = warp & 3: 32 query rows; cq = warp >> 2: 32 key
-// columns), one thread issues the products, one loads Q, dO and the K and V rings.
-constexpr int kDqWorkWarps = 16, kDqMmaWarp = 16, kDqLoadWarp = 17, kDqThreads = 18 * 32;
+// columns), one thread issues the products, one loads Q, dO and the K ring, one the V ring
+// (the two rings free their slots at different products, so neither waits for the other).
+constexpr int kDqWorkWarps = 16, kDqMmaWarp = 16, kDqLoadWarp = 17, kDqVLoadWarp = 18, kDqThreads = 19 * 32;
 constexpr int kDqWork = kDqWorkWarps * 32;
 constexpr int kDqKSlots = 3;
 
@@ -589,39 +590,37 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p,
     tc::fence_after_sync();
     const uint32_t tm = s_tmem, tP = tm + 256, tQ = tm + 384;   // S buffers at tm and tm + 128
 
-    if (warp == kDqLoadWarp) {
-        // ---- loader: Q and dO once, then K_j and V_j in view order, tiled TMA
+    if (warp == kDqLoadWarp || warp == kDqVLoadWarp) {
+        // ---- loaders: Q and dO once and the K_j (one thread), the V_j (another), in view
+        // order, tiled TMA
         if (lane == 0) {
-            int ri_k = pd.attn_rptr[sq], ri_v = ri_k;
-            tc::mbar_expect_tx(&bars[qQ], 65536);
-            tc::tma_load_3d(sm + Q, &maps.q, 0, h, row0 + q0, &bars[qQ]);
-            tc::tma_load_3d(sm + Q + 16384, &maps.q, 64, h, row0 + q0, &bars[qQ]);
-            tc::tma_load_3d(sm + dO, &maps.dout, 0, h, row0 + q0, &bars[qQ]);
-            tc::tma_load_3d(sm + dO + 16384, &maps.dout, 64, h, row0 + q0, &bars[qQ]);
-            int32_t nk = 0, nv = 0;
+            const bool is_v = warp == kDqVLoadWarp;
+            const int nslot = is_v ? 2 : kDqKSlots;
+            uint64_t *fullb = &bars[is_v ? qVF : qKF], *freeb = &bars[is_v ? qVE : qKE];
+            uint8_t *ring = sm + (is_v ? V0 : K0);
+            int ri = pd.attn_rptr[sq];
+            if (!is_v) {
+                tc::mbar_expect_tx(&bars[qQ], 65536);
+                tc::tma_load_3d(sm + Q, &maps.q, 0, h, row0 + q0, &bars[qQ]);
+                tc::tma_load_3d(sm + Q + 16384, &maps.q, 64, h, row0 + q0, &bars[qQ]);
+                tc::tma_load_3d(sm + dO, &maps.dout, 0, h, row0 + q0, &bars[qQ]);
+                tc::tma_load_3d(sm + dO + 16384, &maps.dout, 64, h, row0 + q0, &bars[qQ]);
+            }
+            int32_t n = 0;
             for (int32_t j = 0; j < n_kt && !failed(&s_fail); ++j) {
-                const int ks = j % kDqKSlots, uk = j / kDqKSlots, vs = j & 1, uv = j >> 1;
-                if (uk > 0) wait_or_fail(&bars[qKE + ks], (uk - 1) & 1, 2, &s_fail);
+                const int sl = j % nslot, use = j / nslot;
+                if (use > 0) wait_or_fail(freeb + sl, (use - 1) & 1, 2, &s_fail);
                 if (failed(&s_fail)) break;
-                tc::mbar_expect_tx(&bars[qKF + ks], 32768);
-                tma_view_tile(maps.k, sm + K0 + ks * 32768, pd, sq, j, h, ri_k, &bars[qKF + ks]);
-                nk = j + 1;
-                if (uv > 0) wait_or_fail(&bars[qVE + vs], (uv - 1) & 1, 2, &s_fail);
-                if (failed(&s_fail)) break;
-                tc::mbar_expect_tx(&bars[qVF + vs], 32768);
-                tma_view_tile(maps.v, sm + V0 + vs * 32768, pd, sq, j, h, ri_v, &bars[qVF + vs]);
-                nv = j + 1;
+                tc::mbar_expect_tx(fullb + sl, 32768);
+                tma_view_tile(is_v ? maps.v : maps.k, ring + sl * 32768, pd, sq, j, h, ri, fullb + sl);
+                n = j + 1;
             }
             // every copy lands before the block exits: only a slot's last load can be in flight
-            for (int i = 0; i < kDqKSlots; ++i) {
-                const int32_t uses = nk > i ? (nk - 1 - i) / kDqKSlots + 1 : 0;
-                if (uses) tc::mbar_wait(&bars[qKF + i], (uses - 1) & 1, 1000000000LL);
+            for (int i = 0; i < nslot; ++i) {
+                const int32_t uses = n > i ? (n - 1 - i) / nslot + 1 : 0;
+                if (uses) tc::mbar_wait(fullb + i, (uses - 1) & 1, 1000000000LL);
             }
-            for (int i = 0; i < 2; ++i) {
-                const int32_t uses = nv > i ? (nv - 1 - i) / 2 + 1 : 0;
-                if (uses) tc::mbar_wait(&bars[qVF + i], (uses - 1) & 1, 1000000000LL);
-            }
-            tc::mbar_wait(&bars[qQ], 0, 1000000000LL);
+            if (!is_v) tc::mbar_wait(&bars[qQ], 0, 1000000000LL);
         }
     } else if (warp == kDqMmaWarp) {
         // ---- issuer: S_0, dP_0; then per tile j: S_{j+1}, dP_{j+1}, dQ_j
