@@ -753,9 +753,11 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p,
 // dK / dV kernel roles: two groups of 8 warps form P^T and dS^T, group g the g-th 64-query
 // half of every query tile (lg = warp & 3: 32 key rows; ch = (warp >> 2) & 1: 32 query
 // columns of the half), so that two consecutive steps are formed at once; one thread
-// issues the products; one warp loads K, V once and then Q, dO (tiled TMA) and lse, D
-// (plain loads into shared memory) per query tile.
-constexpr int kKvWorkWarps = 16, kKvMmaWarp = 16, kKvLoadWarp = 17, kKvThreads = 18 * 32;
+// issues the products S^T and dP^T, another the updates of dV and dK (an issuing thread
+// blocks while the tensor pipe is full, so one thread for both left the pipe idle between
+// them); one warp loads K, V once and then Q, dO (tiled TMA) and lse, D (plain loads into
+// shared memory) per query tile.
+constexpr int kKvWorkWarps = 16, kKvMmaWarp = 16, kKvLoadWarp = 17, kKvUpdWarp = 18, kKvThreads = 19 * 32;
 constexpr int kKvGroup = 8 * 32;                  // threads of one work group
 constexpr int kHalf = AT / 2;                     // queries per step
 
@@ -875,49 +877,55 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
             tc::mbar_wait(&bars[vKV], 0, 1000000000LL);
         }
     } else if (warp == kKvMmaWarp) {
-        // ---- issuer
+        // ---- products issuer: S^T and dP^T of step i + 1 once dV, dK of step i - 1 have
+        // released that buffer
         if (lane == 0 && n_e > 0) {
             const tc::Opnd aK{tc::smem_addr(sm + K), 16384, false}, aV{tc::smem_addr(sm + V), 16384, false};
-            const uint32_t id_up = tc::idesc_bf16(AT, AD, false, true);
-            auto products = [&](int32_t e, int hf, int bb) {   // S^T and dP^T of (e, hf) into buffer bb
+            auto products = [&](int32_t e, int hf) {   // S^T and dP^T of (e, hf) into buffer hf
                 const uint32_t qa = tc::smem_addr(sm + ((e & 1) ? Q1 : Q0)) + hf * 8192;
                 const uint32_t da = tc::smem_addr(sm + ((e & 1) ? dO1 : dO0)) + hf * 8192;
-                tc::mma_op(tm + bb * 64, aK, tc::Opnd{qa, 16384, false}, AT, kHalf, AD, false);
-                tc::mma_op(tdP + bb * 64, aV, tc::Opnd{da, 16384, false}, AT, kHalf, AD, false);
+                tc::mma_op(tm + hf * 64, aK, tc::Opnd{qa, 16384, false}, AT, kHalf, AD, false);
+                tc::mma_op(tdP + hf * 64, aV, tc::Opnd{da, 16384, false}, AT, kHalf, AD, false);
             };
-            uint32_t nc_sp0 = 0, nc_sp1 = 0, nc_u0 = 0, nc_u1 = 0;
-            wait_or_fail(&bars[vKV], 0, 0, &s_fail);
-            wait_or_fail(&bars[vQF], 0, 0, &s_fail);
-            tc::fence_after_sync();
-            int nq_cur = sent[0], nq_nx = nq_cur;        // rows of the current / next step's tile
-            if (!failed(&s_fail)) {
-                products(0, 0, 0);                      // step 0 is never empty
-                tc::mma_commit(&bars[vSP]);
-                nc_sp0 = 1;
+            uint32_t nc_sp0 = 0, nc_sp1 = 0;
+            const int32_t n_st = 2 * n_e;
+            int nq_nx = 0;
+            for (int32_t i = 0; i < n_st && !failed(&s_fail); ++i) {
+                const int32_t e = i >> 1;
+                const int b = i & 1;
+                if (b == 0) {                           // a new query tile: its slot has landed
+                    if (i == 0) wait_or_fail(&bars[vKV], 0, 0, &s_fail);
+                    wait_or_fail(&bars[vQF + (e & 1)], (e >> 1) & 1, 0, &s_fail);
+                    nq_nx = sent[4 * (e & 1)];
+                }
+                if (i >= 2) wait_or_fail(&bars[vDVK + b], ((i - 2) >> 1) & 1, 1, &s_fail);
+                tc::fence_after_sync();
+                if (failed(&s_fail)) break;
+                if (b == 0 || nq_nx > kHalf) products(e, b);   // step 0 is never empty
+                tc::mma_commit(&bars[vSP + b]);
+                if (b) ++nc_sp1; else ++nc_sp0;
             }
+            if (failed(&s_fail)) {                      // drain the products still in flight
+                if (nc_sp0) tc::mbar_wait(&bars[vSP], (nc_sp0 - 1) & 1, 1000000000LL);
+                if (nc_sp1) tc::mbar_wait(&bars[vSP + 1], (nc_sp1 - 1) & 1, 1000000000LL);
+            }
+        }
+    } else if (warp == kKvUpdWarp) {
+        // ---- update issuer: dV += P^T dO_i, dK += dS^T Q_i once group i mod 2 has written
+        // P^T and dS^T; the query tile's slot is free after its second step's update (its
+        // products completed before that step's P^T and dS^T were formed)
+        if (lane == 0 && n_e > 0) {
+            const uint32_t id_up = tc::idesc_bf16(AT, AD, false, true);
+            uint32_t nc_u0 = 0, nc_u1 = 0;
             const int32_t n_st = 2 * n_e;
             for (int32_t i = 0; i < n_st && !failed(&s_fail); ++i) {
                 const int b = i & 1;
                 const int32_t e = i >> 1;
-                if (i + 1 < n_st) {                     // the next step's products
-                    const int32_t ne = (i + 1) >> 1;
-                    const int nb = b ^ 1;
-                    if (nb == 0) {                      // a new query tile: its slot has landed
-                        wait_or_fail(&bars[vQF + (ne & 1)], (ne >> 1) & 1, 0, &s_fail);
-                        nq_nx = sent[4 * (ne & 1)];
-                    }
-                    if (i >= 1) wait_or_fail(&bars[vDVK + nb], ((i - 1) >> 1) & 1, 1, &s_fail);
-                    tc::fence_after_sync();
-                    if (failed(&s_fail)) break;
-                    if (nb == 0 || nq_nx > kHalf) products(ne, nb, nb);
-                    tc::mma_commit(&bars[vSP + nb]);
-                    if (nb) ++nc_sp1; else ++nc_sp0;
-                }
-                // dV += P^T dO_i, dK += dS^T Q_i
                 wait_or_fail(&bars[vDS + b], (i >> 1) & 1, 1, &s_fail);
                 tc::fence_after_sync();
                 if (failed(&s_fail)) break;
-                if (b == 0 || nq_cur > kHalf) {
+                const int nq = sent[4 * (e & 1)];       // written before the slot's barrier, read after this step's
+                if (b == 0 || nq > kHalf) {
                     const uint32_t qa = tc::smem_addr(sm + ((e & 1) ? Q1 : Q0)) + b * 8192;
                     const uint32_t da = tc::smem_addr(sm + ((e & 1) ? dO1 : dO0)) + b * 8192;
                     for (int kk = 0; kk < kHalf / 16; ++kk) {
@@ -934,14 +942,9 @@ __global__ void __launch_bounds__(kKvThreads, 1) attn_bwd_dkdv_tc(AttnBwdParams 
                 }
                 tc::mma_commit(&bars[vDVK + b]);
                 if (b) ++nc_u1; else ++nc_u0;
-                if (b == 1) {                           // the query tile's last step
-                    tc::mma_commit(&bars[vQE + (e & 1)]);
-                    nq_cur = nq_nx;
-                }
+                if (b == 1) tc::mma_commit(&bars[vQE + (e & 1)]);   // the query tile's last step
             }
-            if (failed(&s_fail)) {                      // drain the products still in flight
-                if (nc_sp0) tc::mbar_wait(&bars[vSP], (nc_sp0 - 1) & 1, 1000000000LL);
-                if (nc_sp1) tc::mbar_wait(&bars[vSP + 1], (nc_sp1 - 1) & 1, 1000000000LL);
+            if (failed(&s_fail)) {                      // drain the updates still in flight
                 if (nc_u0) tc::mbar_wait(&bars[vDVK], (nc_u0 - 1) & 1, 1000000000LL);
                 if (nc_u1) tc::mbar_wait(&bars[vDVK + 1], (nc_u1 - 1) & 1, 1000000000LL);
             }
