@@ -511,9 +511,11 @@ struct AttnBwdParams {
 };
 
 // dQ kernel roles: 16 warps form dS (lg = warp & 3: 32 query rows; cq = warp >> 2: 32 key
-// columns), one thread issues the products, one loads Q, dO and the K ring, one the V ring
-// (the two rings free their slots at different products, so neither waits for the other).
-constexpr int kDqWorkWarps = 16, kDqMmaWarp = 16, kDqLoadWarp = 17, kDqVLoadWarp = 18, kDqThreads = 19 * 32;
+// columns), one thread issues S and dP, another dQ (an issuing thread blocks while the
+// tensor pipe is full), one loads Q, dO and the K ring, one the V ring (the two rings free
+// their slots at different products, so neither waits for the other).
+constexpr int kDqWorkWarps = 16, kDqMmaWarp = 16, kDqLoadWarp = 17, kDqVLoadWarp = 18, kDqQWarp = 19;
+constexpr int kDqThreads = 20 * 32;
 constexpr int kDqWork = kDqWorkWarps * 32;
 constexpr int kDqKSlots = 3;
 
@@ -525,7 +527,8 @@ constexpr uint32_t bytes = V0 + 2 * 32768 + 1024;       // + alignment slack
 
 // Barriers of the dQ kernel (index into bars[]): Q and dO landed; K slot full / free; V slot
 // full / free; per S buffer: S_j and dP_j done; dP_j read by every dS thread; per S buffer:
-// dS_j written; per S buffer: dQ_j done (also every earlier product of the issuing thread).
+// dS_j written; per S buffer: dQ_j done (also every earlier dQ product: one thread issues
+// them all).
 // As in the forward, a barrier that many threads arrive on is either per buffer or gates
 // the product that the next phase's arrivals depend on, so phases never mix.
 enum DqBar { qQ = 0, qKF = 1, qKE = 4, qVF = 7, qVE = 9, qSP = 11, qPE = 13, qDS = 14, qQD = 16, qN = 18 };
@@ -546,10 +549,10 @@ __device__ __forceinline__ void store_tile_bf16(__nv_bfloat16 *dst_row, const fl
 __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p, PlanDev pd,
                                                                 const __grid_constant__ AttnMaps maps) {
     // S_j (one of two TMEM buffers) and dP_j (one buffer) feed the dS warps; dS_j (bf16
-    // pairs) overwrites S_j and dQ += dS_j K_j reads it there.  The issuing thread runs one
-    // tile ahead: S_{j+1} once dQ_{j-1} has released its buffer, dP_{j+1} once every dS
-    // thread has read dP_j, then dQ_j once dS_j is written, so the tensor pipe works through
-    // dQ_{j-1}, S_{j+1} and dP_{j+1} while the dS warps work on tile j.
+    // pairs) overwrites S_j and dQ += dS_j K_j reads it there.  The products thread runs a
+    // tile ahead of the dQ thread: S_{j+1} once dQ_{j-1} has released its buffer, dP_{j+1}
+    // once every dS thread has read dP_j, so the tensor pipe works through dQ_{j-1}, S_{j+1}
+    // and dP_{j+1} while the dS warps work on tile j.
     using namespace bq_sm;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
@@ -623,41 +626,42 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p,
             if (!is_v) tc::mbar_wait(&bars[qQ], 0, 1000000000LL);
         }
     } else if (warp == kDqMmaWarp) {
-        // ---- issuer: S_0, dP_0; then per tile j: S_{j+1}, dP_{j+1}, dQ_j
+        // ---- products issuer: S_j once dQ_{j-2} has released its buffer, dP_j once every dS
+        // thread has read dP_{j-1}
         if (lane == 0) {
             const tc::Opnd aQ{tc::smem_addr(sm + Q), 16384, false}, adO{tc::smem_addr(sm + dO), 16384, false};
-            const uint32_t id_dq = tc::idesc_bf16(AT, AD, false, true);
-            uint32_t nc_sp0 = 0, nc_sp1 = 0, nc_qd0 = 0, nc_qd1 = 0;
+            uint32_t nc_sp0 = 0, nc_sp1 = 0;
             wait_or_fail(&bars[qQ], 0, 0, &s_fail);
-            wait_or_fail(&bars[qKF], 0, 0, &s_fail);
-            wait_or_fail(&bars[qVF], 0, 0, &s_fail);
-            tc::fence_after_sync();
-            if (!failed(&s_fail)) {
-                tc::mma_op(tm, aQ, tc::Opnd{tc::smem_addr(sm + K0), 16384, false}, AT, AT, AD, false);
-                tc::mma_op(tP, adO, tc::Opnd{tc::smem_addr(sm + V0), 16384, false}, AT, AT, AD, false);
-                tc::mma_commit(&bars[qSP]);
-                tc::mma_commit(&bars[qVE]);
-                nc_sp0 = 1;
-            }
             for (int32_t j = 0; j < n_kt && !failed(&s_fail); ++j) {
-                const int b = j & 1, nb = b ^ 1;
-                if (j + 1 < n_kt) {
-                    const int ks = (j + 1) % kDqKSlots;
-                    wait_or_fail(&bars[qKF + ks], ((j + 1) / kDqKSlots) & 1, 0, &s_fail);
-                    if (j >= 1) wait_or_fail(&bars[qQD + nb], ((j - 1) >> 1) & 1, 1, &s_fail);   // dQ_{j-1} read dS there
-                    tc::fence_after_sync();
-                    if (failed(&s_fail)) break;
-                    tc::mma_op(tm + nb * 128, aQ, tc::Opnd{tc::smem_addr(sm + K0 + ks * 32768), 16384, false},
-                               AT, AT, AD, false);
-                    wait_or_fail(&bars[qVF + nb], ((j + 1) >> 1) & 1, 0, &s_fail);
-                    wait_or_fail(&bars[qPE], j & 1, 1, &s_fail);                   // dP_j read by every dS thread
-                    tc::fence_after_sync();
-                    if (failed(&s_fail)) break;
-                    tc::mma_op(tP, adO, tc::Opnd{tc::smem_addr(sm + V0 + nb * 32768), 16384, false}, AT, AT, AD, false);
-                    tc::mma_commit(&bars[qSP + nb]);
-                    tc::mma_commit(&bars[qVE + nb]);
-                    if (nb) ++nc_sp1; else ++nc_sp0;
-                }
+                const int b = j & 1, ks = j % kDqKSlots;
+                wait_or_fail(&bars[qKF + ks], (j / kDqKSlots) & 1, 0, &s_fail);
+                if (j >= 2) wait_or_fail(&bars[qQD + b], ((j - 2) >> 1) & 1, 1, &s_fail);   // dQ_{j-2} read dS there
+                tc::fence_after_sync();
+                if (failed(&s_fail)) break;
+                tc::mma_op(tm + b * 128, aQ, tc::Opnd{tc::smem_addr(sm + K0 + ks * 32768), 16384, false},
+                           AT, AT, AD, false);
+                wait_or_fail(&bars[qVF + b], (j >> 1) & 1, 0, &s_fail);
+                if (j >= 1) wait_or_fail(&bars[qPE], (j - 1) & 1, 1, &s_fail);  // dP_{j-1} read by every dS thread
+                tc::fence_after_sync();
+                if (failed(&s_fail)) break;
+                tc::mma_op(tP, adO, tc::Opnd{tc::smem_addr(sm + V0 + b * 32768), 16384, false}, AT, AT, AD, false);
+                tc::mma_commit(&bars[qSP + b]);
+                tc::mma_commit(&bars[qVE + b]);
+                if (b) ++nc_sp1; else ++nc_sp0;
+            }
+            if (failed(&s_fail)) {                      // drain the products still in flight
+                if (nc_sp0) tc::mbar_wait(&bars[qSP], (nc_sp0 - 1) & 1, 1000000000LL);
+                if (nc_sp1) tc::mbar_wait(&bars[qSP + 1], (nc_sp1 - 1) & 1, 1000000000LL);
+            }
+        }
+    } else if (warp == kDqQWarp) {
+        // ---- dQ issuer: dQ += dS_j K_j once dS_j is written; K_j's slot is free after it (S_j
+        // completed before dS_j was formed)
+        if (lane == 0) {
+            const uint32_t id_dq = tc::idesc_bf16(AT, AD, false, true);
+            uint32_t nc_qd0 = 0, nc_qd1 = 0;
+            for (int32_t j = 0; j < n_kt && !failed(&s_fail); ++j) {
+                const int b = j & 1;
                 wait_or_fail(&bars[qDS + b], (j >> 1) & 1, 1, &s_fail);
                 tc::fence_after_sync();
                 if (failed(&s_fail)) break;
@@ -674,8 +678,6 @@ __global__ void __launch_bounds__(kDqThreads, 1) attn_bwd_dq_tc(AttnBwdParams p,
                 if (b) ++nc_qd1; else ++nc_qd0;
             }
             if (failed(&s_fail)) {                      // drain the products still in flight
-                if (nc_sp0) tc::mbar_wait(&bars[qSP], (nc_sp0 - 1) & 1, 1000000000LL);
-                if (nc_sp1) tc::mbar_wait(&bars[qSP + 1], (nc_sp1 - 1) & 1, 1000000000LL);
                 if (nc_qd0) tc::mbar_wait(&bars[qQD], (nc_qd0 - 1) & 1, 1000000000LL);
                 if (nc_qd1) tc::mbar_wait(&bars[qQD + 1], (nc_qd1 - 1) & 1, 1000000000LL);
             }
