@@ -472,13 +472,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) attn_fwd_tc(AttnParams p, Plan
 //   dV_j = sum_t P_tj dO_t,  dS_tj = scale P_tj (dP_tj - D_t) with dP = dO V^T,
 //   dQ_t = sum_j dS_tj K_j,  dK_j = sum_t dS_tj Q_t,
 // every query row once (its own compact row), over its view.  P is recomputed from the
-// forward's log-sum-exp.  The kernels form dS / scale = P (dP - D) (bf16 into the products)
-// and apply the scale once, to dQ and dK as they are stored.
-// dQ: one block per (query tile, head) over the view's key tiles,
-// as the forward.  dK, dV: one block per (key tile of a sequence's own rows, head) over
-// the query tiles that see it (planner lists: the sequence's own tiles, causal, and the
-// tiles of every sequence whose prefix runs through it, a prefix of the key tile
-// visible).  Fixed summation orders, no atomics.
+// forward's log-sum-exp.  The kernels form dS / scale = P (dP - D) (bf16 into the
+// products) and apply the scale once, to dQ and dK as they are stored.  dQ: one block per
+// (query tile, head) over the view's key tiles, as the forward.  dK, dV: one block per
+// (key tile of a sequence's own rows, head) over the query tiles that see it (planner
+// lists: the sequence's own tiles, causal, and the tiles of every sequence whose prefix
+// runs through it, a prefix of the key tile visible).  Fixed summation orders, no
+// atomics.
 // ======================================================================================
 
 __global__ void attn_bwd_prep(const __nv_bfloat16 *o, const __nv_bfloat16 *dout, float *D, int64_t rows) {
