@@ -399,13 +399,13 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
             else prefetch_chunk(p, pd, seq, h, rho, L, c0 + BC, sm, s_rows);
         }
         // ---- scale the TMEM state by e^{Gamma_L} per key channel (used by MMA7) -----------
-        for (int hf = 0; hf < 2; ++hf) {
-            float r[32];
-            const int cb = ch * 64 + hf * 32;
-            tc::tmem_ld32(tST + lane_off + cb, r);
+        {
+            float r0[32], r1[32];
+            const int cb = ch * 64;
+            tc::tmem_ld32x2(tST + lane_off + cb, r0, tST + lane_off + cb + 32, r1);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] *= vel[cb + j];
-            tc::tmem_st32(tST + lane_off + cb, r);
+            for (int j = 0; j < 32; ++j) { r0[j] *= vel[cb + j]; r1[j] *= vel[cb + 32 + j]; }
+            tc::tmem_st32x2(tST + lane_off + cb, r0, tST + lane_off + cb + 32, r1);
         }
         if (!wait_all(&bars[0], ph, &s_fail)) break;
         // ---- A -> Mf (scaled by beta, strict lower), P -> Pm (incl lower) -----------------
@@ -532,10 +532,12 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
         const int32_t pend = min(c0 + BC, L);     // a slot may sit at the sequence end
         const bool slot = sp < sp_end && pd.state_lpos[sp] == pend;
         const bool last = ci == nch - 1;
+        float rr2[2][32];
+        tc::tmem_ld32x2(tST + lane_off + ch * 64, rr2[0], tST + lane_off + ch * 64 + 32, rr2[1]);
+#pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-            float r[32];
+            float (&r)[32] = rr2[hf];
             const int cb = ch * 64 + hf * 32;
-            tc::tmem_ld32(tST + lane_off + cb, r);
             if (!last) {
 #pragma unroll
                 for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + STs, 128, jv, cb + j, r + j);
@@ -820,12 +822,15 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
             --sp;
         }
         // ---- save the carry dS' (bf16 dS^T) for the gradient kernel ----------------------
-        for (int hf = 0; hf < 2; ++hf) {
-            float r[32];
-            const int cb = ch * 64 + hf * 32;
-            tc::tmem_ld32(tST + lane_off + cb, r);
+        {
+            float r0[32], r1[32];
+            const int cb = ch * 64;
+            tc::tmem_ld32x2(tST + lane_off + cb, r0, tST + lane_off + cb + 32, r1);
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + dSTs, 128, jv, cb + j, r + j);
+            for (int j = 0; j < 32; j += 8) {
+                tc::st_sw128_8(sm + dSTs, 128, jv, cb + j, r0 + j);
+                tc::st_sw128_8(sm + dSTs, 128, jv, cb + 32 + j, r1 + j);
+            }
         }
         tc::cp_async_wait_all();
         if (tma_pending) {
@@ -882,16 +887,19 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
             tc::mma_commit(&bars[0]);
         }
         // carry: bf16 copy scaled by e^{Gamma_L - m} per key channel; TMEM scaled by e^{Gamma_L}
-        for (int hf = 0; hf < 2; ++hf) {
-            float r[32];
-            const int cb = ch * 64 + hf * 32;
-            tc::tmem_ld32(tST + lane_off + cb, r);
-            float w[32];
+        {
+            float r2[2][32];
+            tc::tmem_ld32x2(tST + lane_off + ch * 64, r2[0], tST + lane_off + ch * 64 + 32, r2[1]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) { w[j] = r[j] * vekt[cb + j]; r[j] *= vel[cb + j]; }
+            for (int hf = 0; hf < 2; ++hf) {
+                const int cb = ch * 64 + hf * 32;
+                float w[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + dSTs, 128, jv, cb + j, w + j);
-            tc::tmem_st32(tST + lane_off + cb, r);
+                for (int j = 0; j < 32; ++j) { w[j] = r2[hf][j] * vekt[cb + j]; r2[hf][j] *= vel[cb + j]; }
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + dSTs, 128, jv, cb + j, w + j);
+            }
+            tc::tmem_st32x2(tST + lane_off + ch * 64, r2[0], tST + lane_off + ch * 64 + 32, r2[1]);
         }
         if (!wait_all(&bars[0], ph, &s_fail)) break;
         // ---- P (M = 64 layout: warp lg holds rows 16 lg .. 16 lg + 15 in lanes 0-15) ------
