@@ -177,3 +177,26 @@ def test_bf16_d128_fwd_bwd_with_h0_tc():
     errs = _run(parent, seg_len, 64, 2, 128, "bf16", 22, backward=True, kernel=_lib.HARTS_KERNEL_TC,
                 h0=True, decay=0.05, scale=0.7)
     _assert(errs, TOL["bf16"])
+
+
+def test_tc_fwd_bwd_repeatable_on_64k_forest():
+    """Forward + backward twice on the same inputs over the 64K-token forest: every output
+    is identical bit for bit (fixed summation orders, no atomics: a race between the
+    staged copies, the products and the per-chunk phases would show as run-to-run
+    differences) and no device error is recorded."""
+    parent, seg_len = make_tree("fb64k_bf16")
+    pl = Plan(parent, seg_len, 64).upload()
+    C, H = pl.info["C"], 4
+    x = make_inputs(C, H, 128, 128, "bf16", 17, device="cuda")
+    cs = torch.empty(pl.chunk_state_bytes(H, 128, 128, 1) // 2, dtype=torch.bfloat16, device="cuda")
+    runs = []
+    for _ in range(2):
+        o, states, _, cs = kda_fwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], chunk_states=cs,
+                                   kernel=_lib.HARTS_KERNEL_TC)
+        gr = kda_bwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], x["W"], states=states,
+                     chunk_states=cs, kernel=_lib.HARTS_KERNEL_TC)
+        torch.cuda.synchronize()
+        assert pl.device_error() == 0
+        runs.append([o.clone()] + [gr[n].clone() for n in ("dq", "dk", "dv", "dg", "dbeta")])
+    for a, b in zip(*runs):
+        assert torch.equal(a, b)
