@@ -28,6 +28,8 @@ sys.path.insert(0, ROOT)
 WORKLOAD = "wide256k_bf16"
 METRIC = "packed-tree KDA fwd+bwd compact tokens/s"
 UNIT = "compact tokens/s"
+NOMINAL_HBM_GBS = 8000.0          # nominal HBM rate of one GB300 (8 TB/s)
+NOMINAL_BF16_TFLOPS = 2250.0      # nominal dense bf16 tensor peak of one GB300
 
 
 def parse():
@@ -37,8 +39,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--expanded", action="store_true",
-                    help="also time the same kernels on the trajectory-expanded input")
+    ap.add_argument("--no-expanded", action="store_true",
+                    help="skip the leg that times the same kernels on the trajectory-expanded input")
     ap.add_argument("--fidelity", action="store_true",
                     help="also compare the forward outputs of the tree plans with the "
                          "per-trajectory run, by handoff depth")
@@ -330,23 +332,31 @@ def run_ours(args):
 
     # ---- end to end through the public API with host buffers --------------------------
     # Every step copies its inputs (q, k, v, g, beta and the loss weight W) from pinned
-    # host memory and reads back its result, the loss L = sum W o (the gradients stay on
-    # the device for the optimizer).  Step i + 1's inputs are copied on a second stream
-    # into a second buffer set while step i computes.  `all_outputs` times the plain
-    # serial variant that also reads every output and gradient back.
+    # host memory, runs the forward and backward, and reads back the step's product: the
+    # gradients dq, dk, dv, dg, dbeta and the loss L = sum W o.  Copies overlap compute:
+    # step i + 1's inputs go up on one stream while step i computes, and step i's
+    # gradients come down on another while step i + 1 computes (inputs and gradients are
+    # double-buffered on the device).  `all_outputs` times the plain serial variant that
+    # also reads o back and overlaps nothing.
     e2e = None
     if not args.no_e2e:
         host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in x.items()}
         for k in host_in:
             host_in[k].copy_(x[k])
         bufs = [{k: torch.empty_like(v) for k, v in x.items()} for _ in range(2)]
+        gbufs = [grads] + [{k: torch.empty_like(v) for k, v in grads.items()}]
+        host_g = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in grads.items()}
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-        K2 = max(2, K)                                  # the first copy is the only one not overlapped
+        K2 = max(2, K)
         loss_dev = torch.empty((), dtype=o.dtype, device=dev)
         loss_host = torch.empty((K2 + 1,), dtype=o.dtype, pin_memory=True)
+        d2h = sum(t.numel() * t.element_size() for t in host_g.values()) + loss_dev.element_size()
         copy_s = torch.cuda.Stream(device=dev)
+        down_s = torch.cuda.Stream(device=dev)
         in_ready = [torch.cuda.Event() for _ in range(2)]
         buf_free = [torch.cuda.Event() for _ in range(2)]
+        g_ready = [torch.cuda.Event() for _ in range(2)]
+        g_free = [torch.cuda.Event() for _ in range(2)]
 
         def issue_copy(i):
             b_ = i & 1
@@ -360,10 +370,23 @@ def run_ours(args):
         def compute(i):
             b_ = i & 1
             stream.wait_event(in_ready[b_])
-            fwd(bufs[b_]); bwd(bufs[b_], "state"); bwd(bufs[b_], "grad")
-            torch.dot(bufs[b_]["W"].view(-1), o.view(-1), out=loss_dev)
+            if i >= 2:
+                stream.wait_event(g_free[b_])
+            inp = bufs[b_]
+            fwd(inp)
+            kda_bwd(pl, inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["W"], states=states,
+                    chunk_states=cs, grads=gbufs[b_], workspace=wsb, phase="state")
+            kda_bwd(pl, inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["W"], states=states,
+                    chunk_states=cs, grads=gbufs[b_], workspace=wsb, phase="grad")
+            torch.dot(inp["W"].view(-1), o.view(-1), out=loss_dev)
             buf_free[b_].record(stream)
             loss_host[i].copy_(loss_dev, non_blocking=True)
+            g_ready[b_].record(stream)
+            down_s.wait_event(g_ready[b_])
+            with torch.cuda.stream(down_s):
+                for k in host_g:
+                    host_g[k].copy_(gbufs[b_][k], non_blocking=True)
+            g_free[b_].record(down_s)
 
         issue_copy(0); compute(0)                       # warm the pipeline once
         torch.cuda.synchronize()
@@ -376,13 +399,15 @@ def run_ours(args):
             if i + 1 < K2:
                 issue_copy(i + 1)
             compute(i)
+        stream.wait_stream(down_s)
         a1.record(stream)
         torch.cuda.synchronize()
         _, ems = reduce_across_ranks(C, a0.elapsed_time(a1) / K2, dev)
         e2e = dict(value=round(C_all / (ems / 1e3), 1), unit=UNIT, h2d_bytes_per_step=int(h2d),
-                   d2h_bytes_per_step=int(loss_dev.numel() * loss_dev.element_size()), ms_per_step=round(ems, 3),
-                   loss=float(loss_host[K2 - 1]), overlap="inputs of step i+1 copied during step i")
-        # serial variant: copy in, compute, read every output and gradient back
+                   d2h_bytes_per_step=int(d2h), ms_per_step=round(ems, 3),
+                   loss=float(loss_host[K2 - 1]), returns="dq, dk, dv, dg, dbeta and the loss",
+                   overlap="step i+1's inputs copied up and step i's gradients copied down during compute")
+        # serial variant: copy in, compute, read the output and every gradient back
         outs = dict(o=o, **grads)
         host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
         d2h_all = sum(t.numel() * t.element_size() for t in host_out.values())
@@ -400,7 +425,8 @@ def run_ours(args):
         _, ams = reduce_across_ranks(C, b0.elapsed_time(b1) / 2, dev)
         e2e["all_outputs"] = dict(value=round(C_all / (ams / 1e3), 1), ms_per_step=round(ams, 3),
                                   h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h_all))
-        del host_in, host_out, bufs
+        del host_in, host_out, host_g, bufs, gbufs
+        torch.cuda.empty_cache()
 
     # ---- roofline ----------------------------------------------------------------------
     cm = cost_model(info, H, D, B)
@@ -419,15 +445,26 @@ def run_ours(args):
     traffic = traffic_from_profiles(kernel_name)
     step_bytes = cm["fwd_bytes"] + cm["bwd_bytes"]
     step_flops = cm["fwd_flops"] + cm["bwd_flops"]
-    t_star = max(step_bytes / (hbm * 1e9), step_flops / (tf_sus * 1e12))
-    roofline = dict(bound="hbm", kernel=kernel_name, achieved=round(achieved, 1), peak=hbm,
-                    unit="GB/s", frac=round(achieved / hbm, 4), traffic=traffic,
-                    peak_source=f"{src} hbm_gbs",
+    t_mem, t_math = step_bytes / (hbm * 1e9), step_flops / (tf_sus * 1e12)
+    t_star = max(t_mem, t_math)
+    # nominal roofline, beside the measured-peak one: the slower of 8 TB/s HBM and the
+    # nominal dense bf16 tensor peak (2.25 PFLOP/s) of one GB300
+    ns_mem, ns_math = step_bytes / (NOMINAL_HBM_GBS * 1e9), step_flops / (NOMINAL_BF16_TFLOPS * 1e12)
+    ns_t = max(ns_mem, ns_math)
+    roofline = dict(bound="hbm" if t_mem >= t_math else "tensor", kernel=kernel_name,
+                    achieved=round(achieved, 1), peak=hbm, unit="GB/s", frac=round(achieved / hbm, 4),
+                    traffic=traffic, peak_source=f"{src} hbm_gbs",
                     step=dict(algorithmic_bytes=int(step_bytes), algorithmic_flops=int(step_flops),
-                              t_star_ms=round(t_star * 1e3, 3), frac=round(t_star * 1e3 / ms, 4)))
+                              bound="hbm" if t_mem >= t_math else "tensor",
+                              t_star_ms=round(t_star * 1e3, 3), frac=round(t_star * 1e3 / ms, 4),
+                              frac_of="measured peaks (MEASURED_PEAKS.json: copy GB/s, sustained bf16)"),
+                    nominal=dict(hbm_gbs=NOMINAL_HBM_GBS, bf16_tflops=NOMINAL_BF16_TFLOPS,
+                                 bound="hbm" if ns_mem >= ns_math else "tensor",
+                                 t_star_ms=round(ns_t * 1e3, 3), frac=round(ns_t * 1e3 / ms, 4),
+                                 kernel_frac=round(achieved / NOMINAL_HBM_GBS, 4)))
 
     expanded = None
-    if args.expanded:
+    if not args.no_expanded:
         expanded = run_expanded(parent, seg_len, pl, x, wl, ms)
     nodewise = None
     if args.nodewise:

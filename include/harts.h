@@ -202,7 +202,8 @@ size_t harts_kda_chunk_state_bytes(const harts_plan *plan, int32_t H, int32_t dk
  * runs its replay rows and own rows chunk by chunk, writes o for its own rows only,
  * stores requested boundary states into their slots and its final state.
  * Errors: HARTS_EINVAL, HARTS_EUNSUPPORTED (dk, dv not in {32,64,128}, dk != dv,
- * B not in {16,32,64}), HARTS_ENOPLAN, HARTS_ECUDA.
+ * B not in {16,32,64}), HARTS_ENOPLAN, HARTS_EOVERFLOW (C * H above 2^31 - 1),
+ * HARTS_ECUDA.
  */
 int harts_kda_fwd(const harts_plan *plan, const harts_kda_fwd_args *args, harts_stream_t stream);
 
@@ -276,7 +277,6 @@ int harts_kda_bwd_grad(const harts_plan *plan, const harts_kda_bwd_args *args, h
 int harts_kda_bwd_static(const harts_plan *plan, const harts_kda_bwd_args *args, harts_stream_t stream);
 size_t harts_kda_bwd_static_max_bytes(void);
 
-/* Message for the last error on the calling thread ("" if none). */
 /* ------------------------------------------------------------------------------ */
 /* Causal short convolution over the compact layout.                              */
 /* ------------------------------------------------------------------------------ */
@@ -431,6 +431,7 @@ size_t harts_attn_bwd_workspace_bytes(const harts_plan *plan, int32_t H);
  * workspace) and HARTS_ESMALLBUF (workspace). */
 int harts_attn_bwd(const harts_plan *plan, const harts_attn_bwd_args *args, harts_stream_t stream);
 
+/* Message for the last error on the calling thread ("" if none). */
 const char *harts_last_error(void);
 
 #ifdef __cplusplus

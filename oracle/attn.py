@@ -11,7 +11,7 @@ values of its ancestors and itself (h + l), with bottom-right causal alignment, 
 i sees exactly the entries j <= h + i: the full ancestor prefix and the causal triangle
 of its own tokens.  Outputs go back to the unique compact rows.
 
-Reading taken where the pages are silent (listed in the design doc): the attention core is
+Reading taken where the pages are silent: the attention core is
 plain multi-head softmax attention, o = softmax(scale q k^T) v per head, on already
 projected (and position-rotated) q, k, v; head dimensions are the caller's.  Since a
 row's view is its own trajectory prefix, the output of a compact row is the causal

@@ -9,7 +9,7 @@ once per compact token; its window over the previous w - 1 tokens takes them fro
 token's real ancestors along its own trajectory (a temporary prefix of the parent's
 activations), and never from the neighbouring rows of another packed sequence.
 
-Readings taken where the pages are silent (listed in the design doc):
+Readings taken where the pages are silent:
 * depthwise (one filter per channel), width w, weight[c, w-1] on the current token and
   weight[c, w-1-j] on the token j positions earlier: pre[t] = bias +
   sum_j weight[:, w-1-j] * x[t-j], with zeros before the trajectory start;

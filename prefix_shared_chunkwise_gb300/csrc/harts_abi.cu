@@ -43,9 +43,11 @@ int check_fwd_args(const harts_plan *P, const harts_kda_fwd_args *a) {
     if (!a->q || !a->k || !a->v || !a->g || !a->beta) { set_error("NULL input"); return HARTS_EINVAL; }
     if (P->info.n_states > 0 && !a->states) { set_error("states required (n_states > 0)"); return HARTS_EINVAL; }
     if (a->kernel < HARTS_KERNEL_AUTO || a->kernel > HARTS_KERNEL_TC) { set_error("kernel"); return HARTS_EINVAL; }
-    const int64_t rows = P->info.C * a->H;
-    if (rows > (int64_t(1) << 31) / 1) {
-        // row * H * D products are formed in int64 inside the kernels; only C*H must fit int32
+    // row * H * D offsets are formed in int64 inside the kernels; (row, head) indices of
+    // beta and the launch grids are int32
+    if (P->info.C * int64_t(a->H) > int64_t(0x7fffffff)) {
+        set_error("C * H exceeds 2^31 - 1 (row, head) pairs");
+        return HARTS_EOVERFLOW;
     }
     return HARTS_OK;
 }

@@ -154,6 +154,14 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t phase, int *s_f
     return *s_fail == 0;
 }
 
+// Final bounded wait for a copy or product still in flight before the block releases
+// its shared memory and TMEM; a wait that runs out is recorded in the plan's error word
+// (the host then reports HARTS_EDEVICE), it is never silently dropped.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t phase, long long max_cycles,
+                                           const PlanDev &pd, int32_t a, int32_t b) {
+    if (!tc::mbar_wait(bar, phase, max_cycles)) dev_error(pd, kDevErrTimeout, a, b);
+}
+
 // Make shared-memory writes and TMEM reads of all threads ordered before the next MMA.
 __device__ __forceinline__ void sync_for_mma() {
     tc::fence_smem_to_async();
@@ -567,11 +575,11 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
         sync_for_mma();
     }
     tc::cp_async_wait_all();
-    if (tma_pending) tc::mbar_wait(&bars[4], n_tma & 1, 1000000000LL);   // a staged chunk still in flight
+    if (tma_pending) drain_wait(&bars[4], n_tma & 1, 1000000000LL, pd, seq, h);   // a staged chunk in flight
     if (s_fail) {
         dev_error(pd, kDevErrTimeout, seq, h);
         // let any MMA still in flight drain before the columns are released
-        for (int i = 0; i < 4; ++i) tc::mbar_wait(&bars[i], 0, 100000000LL);
+        for (int i = 0; i < 4; ++i) drain_wait(&bars[i], 0, 100000000LL, pd, seq, h);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -955,7 +963,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
         if (!wait_all(&bars[3], ph, &s_fail)) break;
     }
     tc::cp_async_wait_all();
-    if (tma_pending) tc::mbar_wait(&bars[4], n_tma & 1, 1000000000LL);   // a staged chunk still in flight
+    if (tma_pending) drain_wait(&bars[4], n_tma & 1, 1000000000LL, pd, seq, h);   // a staged chunk in flight
     if (!s_fail && (src >= 0 || p.dh0)) {
         float *dst = p.ds_init + (static_cast<int64_t>(seq) * H + h) * D * D;
         for (int hf = 0; hf < 2; ++hf) {
@@ -968,7 +976,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_state_tc(BwdParams p, PlanDev p
     }
     if (s_fail) {
         dev_error(pd, kDevErrTimeout, seq, h);
-        for (int i = 0; i < 4; ++i) tc::mbar_wait(&bars[i], 0, 100000000LL);
+        for (int i = 0; i < 4; ++i) drain_wait(&bars[i], 0, 100000000LL, pd, seq, h);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -1573,11 +1581,11 @@ done:
     tc::cp_async_wait_all();
     if (s_fail) {
         dev_error(pd, kDevErrTimeout, cur_seq, cur_h);
-        for (int i = 0; i < 6; ++i) tc::mbar_wait(&bars[i], ph, 100000000LL);
+        for (int i = 0; i < 6; ++i) drain_wait(&bars[i], ph, 100000000LL, pd, cur_seq, cur_h);
         // staging copies still in flight land before the block's shared memory is released
         if (tid == 0)
             for (int j = n_done; j < n_armed; ++j)
-                for (int k = 0; k < 3; ++k) tc::mbar_wait(&tbar[k], j & 1, 100000000LL);
+                for (int k = 0; k < 3; ++k) drain_wait(&tbar[k], j & 1, 100000000LL, pd, cur_seq, cur_h);
     }
     tc::fence_before_sync();
     __syncthreads();

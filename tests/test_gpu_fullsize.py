@@ -88,3 +88,88 @@ def test_full_size_workload_sampled_trajectories(name):
             off = torch.ones(C, dtype=torch.bool, device="cuda")
             off[idx] = False
             assert float(gr[n][off].abs().max()) == 0.0, (name, leaf, n, "off-path gradient")
+
+
+def _tree_properties(parent, seg_len, tw):
+    """Per tree (by root segment): the rounds its sequences run in, how many side branches
+    start by replay in their producer's round (delta = 0), how many boundary slots feed
+    two or more consumers, and its expanded size S."""
+    from prefix_shared_chunkwise_gb300.synth import tree_stats
+    n = len(parent)
+    root = np.zeros(n, np.int64)
+    for i in range(n):
+        root[i] = i if parent[i] < 0 else root[parent[i]]
+    seq_tree = root[tw["seq_first_seg"]]
+    ncons = np.diff(tw["state_cons_ptr"])
+    slot_tree = seq_tree[tw["state_seq"]]
+    out = []
+    for r in np.unique(root):
+        seqs = np.nonzero(seq_tree == r)[0]
+        d0 = 0
+        for s in seqs:
+            f = tw["seq_first_seg"][s]
+            if parent[f] >= 0 and tw["seq_round"][s] == tw["seq_round"][tw["seg_seq"][parent[f]]]:
+                d0 += 1
+        ids = np.nonzero(root == r)[0]
+        remap = {int(v): j for j, v in enumerate(ids)}
+        sub_parent = np.array([-1 if parent[v] < 0 else remap[int(parent[v])] for v in ids], np.int32)
+        out.append(dict(ids=ids, sub_parent=sub_parent, rounds=len(np.unique(tw["seq_round"][seqs])),
+                        d0=d0, multi=int((ncons[slot_tree == r] >= 2).sum()),
+                        S=tree_stats(sub_parent, seg_len[ids])["S"]))
+    return out
+
+
+@pytest.mark.parametrize("name,need", [
+    ("wide256k_bf16", dict(d0=1, multi=1, rounds=2)),     # 2-round forest: shared slots, delta = 0 starts
+    ("deep128k_bf16", dict(d0=0, multi=0, rounds=6)),     # 7-round forest: handoffs nested 6 deep
+])
+def test_full_size_backward_whole_tree(name, need):
+    """Backward at full size, in the bench's launch configuration, with the loss on every
+    row of one whole tree: dO = W on the tree's rows, zero elsewhere.  Every handoff of the
+    tree then carries gradient: consumers' initial-state gradients summed into shared slots,
+    same-round (delta = 0) starts, replay rows of many branches folded into one ancestor
+    row.  dq, dk, dv, dg, dbeta on all of the tree's rows are compared with the oracle run
+    on that tree (relative L2 over the tree and over each segment), and every row outside
+    the tree must get exactly zero gradient.  The tree is the smallest (in expanded
+    tokens) that has the listed features."""
+    wl = WORKLOADS[name]
+    H, D, B = wl.H, wl.dk, wl.chunk
+    parent, seg_len = make_tree(name)
+    tw = plan_twin.plan(parent, seg_len, B)
+    cands = [t for t in _tree_properties(parent, seg_len, tw)
+             if t["d0"] >= need["d0"] and t["multi"] >= need["multi"] and t["rounds"] >= need["rounds"]]
+    assert cands, name
+    tree = min(cands, key=lambda t: t["S"])
+    ids = tree["ids"]
+    so = tw["seg_offset"]
+    seg_rows = [np.arange(so[v], so[v] + seg_len[v]) for v in ids]
+    rows = np.concatenate(seg_rows)
+    sub_off = np.concatenate([[0], np.cumsum(seg_len[ids])[:-1]]).astype(np.int64)
+
+    pl = Plan(parent, seg_len, B).upload()
+    C = pl.info["C"]
+    x = make_inputs(C, H, D, D, wl.dtype, seed=11, device="cuda")
+    cs = torch.empty(pl.chunk_state_bytes(H, D, D, 1) // 2, dtype=torch.bfloat16, device="cuda")
+    o, states, _, cs = kda_fwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], chunk_states=cs)
+    idx = torch.as_tensor(rows, device="cuda")
+    dO = torch.zeros_like(x["W"])
+    dO[idx] = x["W"][idx]
+    gr = kda_bwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], dO, states=states, chunk_states=cs)
+    torch.cuda.synchronize()
+    assert pl.device_error() == 0
+
+    hs = [0, H - 1]
+    sub = {k: v.index_select(0, idx)[:, hs].float().cpu().double().numpy() for k, v in x.items()}
+    ref = oracle.kda_forest(tree["sub_parent"], seg_len[ids], sub_off, sub["q"], sub["k"], sub["v"],
+                            sub["g"], sub["beta"], chunk=B, W=sub["W"], n_threads=len(hs))
+    off = torch.ones(C, dtype=torch.bool, device="cuda")
+    off[idx] = False
+    bounds = np.concatenate([[0], np.cumsum(seg_len[ids])])
+    for n in ("dq", "dk", "dv", "dg", "dbeta"):
+        got = gr[n].index_select(0, idx)[:, hs].float().cpu().numpy()
+        assert rel_l2(got, ref[n]) <= TOL, (name, n, rel_l2(got, ref[n]))
+        for j in range(len(ids)):
+            a, b = bounds[j], bounds[j + 1]
+            e = rel_l2(got[a:b], ref[n][a:b])
+            assert e <= 2 * TOL, (name, n, "segment", int(ids[j]), e)
+        assert float(gr[n][off].abs().max()) == 0.0, (name, n, "gradient outside the tree")

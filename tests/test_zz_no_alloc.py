@@ -2,7 +2,11 @@
 device memory (a plugin inside a framework that owns the device pool, a step loop that
 must not allocate).  Its scratch is the library's own file-scope device array; the
 results must match harts_kda_bwd with a caller workspace, on two calls in a row (the
-array keeps the previous call's contents)."""
+array keeps the previous call's contents).
+
+So that a scratch entry read before it is written cannot go unnoticed, the array is
+first left holding another problem's values (a different forest and seed), and the
+reference run's caller workspace starts as all-ones bytes (NaN in every fp32 word)."""
 import numpy as np
 import pytest
 
@@ -34,25 +38,38 @@ def _case(parent, seg_len, B, H, D, dtype, seed):
     return pl, x, states, cs
 
 
-def _bwd(pl, x, states, cs, phase):
+def _bwd(pl, x, states, cs, phase, workspace=None):
     g = kda_bwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], x["W"], states=states,
-                chunk_states=cs, phase=phase)
+                chunk_states=cs, phase=phase, workspace=workspace)
     torch.cuda.synchronize()
     return {k: v.float().cpu().numpy() for k, v in g.items()}
 
 
+def _poisoned_workspace(pl, H, D):
+    return torch.full((max(pl.bwd_workspace_bytes(H, D, D), 256),), 0xFF, dtype=torch.uint8,
+                      device="cuda")
+
+
+_CASES = {
+    "fig1_fp32": lambda: (*fig1_tree(), (16, 1, 32, "fp32", 0), 1e-5),
+    "forest_bf16_d128": lambda: (np.array([-1, 0, 0, 1, 1, 2, -1, 6], np.int32),
+                                 np.random.Generator(np.random.PCG64(41)).integers(10, 180, size=8)
+                                 .astype(np.int64), (64, 2, 128, "bf16", 5), 1e-2),
+}
+
+
 @pytest.mark.parametrize("which", ["fig1_fp32", "forest_bf16_d128"])
 def test_static_scratch_backward_matches_workspace_backward(which):
-    if which == "fig1_fp32":
-        parent, seg_len = fig1_tree()
-        args, tol = (16, 1, 32, "fp32", 0), 1e-5
-    else:
-        rng = np.random.Generator(np.random.PCG64(41))
-        parent = np.array([-1, 0, 0, 1, 1, 2, -1, 6], np.int32)
-        seg_len = rng.integers(10, 180, size=len(parent)).astype(np.int64)
-        args, tol = (64, 2, 128, "bf16", 5), 1e-2
+    parent, seg_len, args, tol = _CASES[which]()
+    # leave the static array holding another problem's scratch: the other case, another seed
+    other = "forest_bf16_d128" if which == "fig1_fp32" else "fig1_fp32"
+    o_parent, o_len, o_args, _ = _CASES[other]()
+    o_args = o_args[:4] + (o_args[4] + 100,)
+    _bwd(*_case(o_parent, o_len, *o_args), "static")
     pl, x, states, cs = _case(parent, seg_len, *args)
-    ref = _bwd(pl, x, states, cs, "all")
+    ref = _bwd(pl, x, states, cs, "all", workspace=_poisoned_workspace(pl, args[1], args[2]))
+    for n in ref:
+        assert np.isfinite(ref[n]).all(), (which, n)
     for call in range(2):
         got = _bwd(pl, x, states, cs, "static")
         for n in ref:
