@@ -15,8 +15,11 @@ cudaError_t simt_bwd_round(int dtype, int BC, const BwdParams &p, const PlanDev 
 cudaError_t bwd_finish(int dtype, const BwdParams &p, const PlanDev &pd, cudaStream_t st);
 
 bool tc_supported(bool backward, int dtype, int D, int BC);
+cudaError_t tc2_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, int32_t n_items, cudaStream_t st);
 cudaError_t tc_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, int32_t n_items,
                          int32_t max_chunks, cudaStream_t st);
+cudaError_t tc2_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t base, int32_t n_items,
+                                cudaStream_t st);
 cudaError_t tc_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t base,
                                int32_t n_items, cudaStream_t st);
 cudaError_t tc_bwd_grad(const BwdParams &p, const PlanDev &pd, int32_t chunk_begin,
@@ -204,7 +207,10 @@ int harts_kda_fwd(const harts_plan *P, const harts_kda_fwd_args *a, harts_stream
         const int32_t base = P->round_seq_ptr[r];
         const int32_t n = (P->round_seq_ptr[r + 1] - base) * a->H;
         if (n == 0) continue;
-        cudaError_t e = fam == 1 ? tc_fwd_round(p, P->view, base, n, P->info.max_seq_chunks, st)
+        // plans with slots inside a chunk (no-replay) keep the kernel that emits them
+        const bool inner = (P->view.flags & HARTS_PLAN_NOREPLAY) != 0;
+        cudaError_t e = fam == 1 ? (inner ? tc_fwd_round(p, P->view, base, n, P->info.max_seq_chunks, st)
+                                          : tc2_fwd_round(p, P->view, base, n, st))
                                  : simt_fwd_round(a->dtype, BC, p, P->view, base, n, st);
         if (e != cudaSuccess) return cuda_fail(e, "forward launch");
     }
@@ -243,7 +249,7 @@ static int kda_bwd_phases(const harts_plan *P, const harts_kda_bwd_args *a, hart
             const int32_t base = P->round_seq_ptr[r];
             const int32_t n = (P->round_seq_ptr[r + 1] - base) * H;
             if (n == 0) continue;
-            cudaError_t e = fam == 1 ? tc_bwd_state_round(p, P->view, base, n, st)
+            cudaError_t e = fam == 1 ? tc2_bwd_state_round(p, P->view, base, n, st)
                                      : simt_bwd_round(a->fwd.dtype, BC, p, P->view, base, n, st);
             if (e != cudaSuccess) return cuda_fail(e, "backward launch");
         }
