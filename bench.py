@@ -440,7 +440,7 @@ def run_ours(args):
                        bwd_grad=cm["bwd_bytes"])
     phase_bytes["bwd_grad"] -= phase_bytes["bwd_state"]
     dom = max(phase_ms, key=phase_ms.get)
-    kernel_name = {"fwd": "kda_fwd_tc", "bwd_state": "kda_bwd_state_tc", "bwd_grad": "kda_bwd_grad_tc"}[dom]
+    kernel_name = {"fwd": "kda_fwd_tc2", "bwd_state": "kda_bwd_state_tc2", "bwd_grad": "kda_bwd_grad_tc2"}[dom]
     achieved = phase_bytes[dom] / (phase_ms[dom] / 1e3) / 1e9
     traffic = traffic_from_profiles(kernel_name)
     step_bytes = cm["fwd_bytes"] + cm["bwd_bytes"]

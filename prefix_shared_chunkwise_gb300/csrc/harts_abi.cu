@@ -22,6 +22,8 @@ cudaError_t tc2_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t b
                                 cudaStream_t st);
 cudaError_t tc_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t base,
                                int32_t n_items, cudaStream_t st);
+cudaError_t tc2_bwd_grad(const BwdParams &p, const PlanDev &pd, int32_t chunk_begin, int32_t n_items,
+                         cudaStream_t st);
 cudaError_t tc_bwd_grad(const BwdParams &p, const PlanDev &pd, int32_t chunk_begin,
                         int32_t n_items, cudaStream_t st);
 
@@ -259,7 +261,7 @@ static int kda_bwd_phases(const harts_plan *P, const harts_kda_bwd_args *a, hart
             // every chunk's gradients at once: they only depend on saved per-chunk states
             const int64_t items = P->info.n_chunks * H;
             if (items > 0x7fffffff) { set_error("too many (chunk, head) items"); return HARTS_EOVERFLOW; }
-            cudaError_t e = tc_bwd_grad(p, P->view, 0, static_cast<int32_t>(items), st);
+            cudaError_t e = tc2_bwd_grad(p, P->view, 0, static_cast<int32_t>(items), st);
             if (e != cudaSuccess) return cuda_fail(e, "backward gradient launch");
         }
         cudaError_t e = bwd_finish(a->fwd.dtype, p, P->view, st);

@@ -31,6 +31,7 @@
 #include "kda_common.cuh"
 #include "tc_primitives.cuh"
 #include "tensor_map.h"
+#include "kda_stage.cuh"
 
 namespace harts {
 namespace {
@@ -126,37 +127,8 @@ __device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_
 }
 
 struct Maps2 {
-    CUtensorMap q, k, v, g;   // {128 channels, H, C}, boxes of 64 channels x 64 rows, 128-byte swizzle
+    RowMaps q, k, v, g;
 };
-
-// Stage local rows [c0, c0 + 64) of one row tensor into two SW128 boxes (channels 0-63 at
-// dst0, 64-127 at dst1; rows 128 B apart from a 1024-aligned base), completing one phase
-// of `bar`.  Full chunks of own rows come by TMA; otherwise every thread gathers rows by
-// cp.async through the chunk's row table `tab` (-1: past the sequence end; rows below
-// `zero_below` also read as zero) and all of them must call this.
-__device__ __forceinline__ void stage_rows(bool tma, const void *src, const CUtensorMap *map, const int *tab,
-                                           int32_t h, int H, int32_t rho, int32_t row0, int32_t c0, uint8_t *dst0,
-                                           uint8_t *dst1, uint64_t *bar, int zero_below = 0) {
-    if (tma) {
-        if (threadIdx.x == 0) {
-            const int32_t r = row0 + (c0 - rho);
-            tc::mbar_expect_tx(bar, 16384);
-            tc::tma_load_3d(dst0, map, 0, h, r, bar);
-            tc::tma_load_3d(dst1, map, 64, h, r, bar);
-        }
-        return;
-    }
-    const uint8_t *s8 = static_cast<const uint8_t *>(src);
-    for (int e = threadIdx.x; e < 64 * 16; e += NT) {
-        const int t = e >> 4, pc = e & 15;
-        const int64_t row = t < zero_below ? -1 : tab[t];
-        uint8_t *dst = (pc < 8 ? dst0 : dst1) + t * 128 + (((pc & 7) ^ (t & 7)) << 4);
-        tc::cp_async16(dst, row >= 0 ? s8 + ((row * H + h) * D * 2 + pc * 16) : s8, row >= 0 ? 16u : 0u);
-    }
-    cp_async_arrive(bar);
-    __syncthreads();
-    if (threadIdx.x == 0) mbar_arrive1(bar);
-}
 
 // Pass A of a chunk whose raw g sits in the SW128 tile `g` ([64][128], atoms of 8 KB): sums
 // of g over 4-row groups, turned into exclusive prefixes (vqs, natural log units), the
@@ -420,7 +392,6 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
     const uint32_t tS = tm, tR = tm + 128, tW = tm + 192;
     const int jv = lq * 32 + lane;                   // this thread's TMEM lane
 
-    auto full = [&](int32_t c) { return c * BC >= rho && c * BC + BC <= L; };
     auto nv_of = [&](int32_t c) { return min(BC, L - c * BC); };
     // Row table of chunk c (threads 0-63; read by the gathers after a barrier) and this
     // thread's beta of row t = tid (raw bf16 bits, 0 past the end).
@@ -433,13 +404,14 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
     int armed[8] = {0, 0, 0, 0, 0, 0, 0, 0};     // phases armed per barrier (uniform over threads)
     auto stage = [&](int which, int32_t c) {
         ++armed[4 + which];
-        const bool tma = full(c);
         const int32_t c0 = c * BC;
+        const int t_own = max(0, rho - c0), t_end = nv_of(c);
+        const int32_t own0 = row0 + c0 - rho;
         switch (which) {
-        case 0: stage_rows(tma, p.g, &maps.g, s_rows, h, H, rho, row0, c0, sm + GP, sm + GP + 8192, &bars[4]); break;
-        case 1: stage_rows(tma, p.k, &maps.k, s_rows, h, H, rho, row0, c0, sm + KQ, sm + KQ + 16384, &bars[5]); break;
-        case 2: stage_rows(tma, p.q, &maps.q, s_rows, h, H, rho, row0, c0, sm + KQ + 8192, sm + KQ + 24576, &bars[6]); break;
-        default: stage_rows(tma, p.v, &maps.v, s_rows, h, H, rho, row0, c0, sm + VV, sm + VV + 8192, &bars[7]); break;
+        case 0: stage_chunk_rows<NT>(p.g, maps.g, s_rows, h, H, t_own, t_end, own0, 0, sm + GP, sm + GP + 8192, &bars[4]); break;
+        case 1: stage_chunk_rows<NT>(p.k, maps.k, s_rows, h, H, t_own, t_end, own0, 0, sm + KQ, sm + KQ + 16384, &bars[5]); break;
+        case 2: stage_chunk_rows<NT>(p.q, maps.q, s_rows, h, H, t_own, t_end, own0, 0, sm + KQ + 8192, sm + KQ + 24576, &bars[6]); break;
+        default: stage_chunk_rows<NT>(p.v, maps.v, s_rows, h, H, t_own, t_end, own0, 0, sm + VV, sm + VV + 8192, &bars[7]); break;
         }
     };
     auto pass_a = [&](int32_t c, uint16_t braw) {
@@ -792,7 +764,7 @@ constexpr uint32_t bytes = END + 1024;
 }  // namespace s2
 
 struct StateMaps2 {
-    CUtensorMap q, k, g, dout;   // {128, H, C}, boxes of 64 channels x 64 rows, 128-byte swizzle
+    RowMaps q, k, g, dout;
     CUtensorMap rec_t;           // chunk records as [rows of 128 B], boxes of 64 x 64 (a chunk's T)
 };
 
@@ -833,7 +805,6 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
     const int jv = lq * 32 + lane;
 
     int armed[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
-    auto full = [&](int32_t c) { return c * BC >= rho && c * BC + BC <= L; };
     auto nv_of = [&](int32_t c) { return min(BC, L - c * BC); };
     auto rows_of = [&](int32_t c) -> uint16_t {
         if (tid >= 64) return 0;
@@ -843,14 +814,15 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
     };
     auto stage = [&](int which, int32_t c) {
         ++armed[4 + which];
-        const bool tma = full(c);
         const int32_t c0 = c * BC;
+        const int t_own = max(0, rho - c0), t_end = nv_of(c);
+        const int32_t own0 = row0 + c0 - rho;
         switch (which) {
-        case 0: stage_rows(tma, f.g, &maps.g, s_rows, h, H, rho, row0, c0, sm + KM, sm + KM + 8192, &bars[4]); break;
-        case 1: stage_rows(tma, f.k, &maps.k, s_rows, h, H, rho, row0, c0, sm + KQ, sm + KQ + 16384, &bars[5]); break;
-        case 2: stage_rows(tma, f.q, &maps.q, s_rows, h, H, rho, row0, c0, sm + KQ + 8192, sm + KQ + 24576, &bars[6]); break;
-        case 3: stage_rows(tma, p.d_o, &maps.dout, s_rows, h, H, rho, row0, c0, sm + DO, sm + DO + 8192, &bars[7],
-                           max(0, rho - c0)); break;
+        case 0: stage_chunk_rows<NT>(f.g, maps.g, s_rows, h, H, t_own, t_end, own0, 0, sm + KM, sm + KM + 8192, &bars[4]); break;
+        case 1: stage_chunk_rows<NT>(f.k, maps.k, s_rows, h, H, t_own, t_end, own0, 0, sm + KQ, sm + KQ + 16384, &bars[5]); break;
+        case 2: stage_chunk_rows<NT>(f.q, maps.q, s_rows, h, H, t_own, t_end, own0, 0, sm + KQ + 8192, sm + KQ + 24576, &bars[6]); break;
+        case 3: stage_chunk_rows<NT>(p.d_o, maps.dout, s_rows, h, H, t_own, t_end, own0, t_own, sm + DO, sm + DO + 8192,
+                                     &bars[7]); break;
         default:
             if (tid == 0) {
                 tc::mbar_expect_tx(&bars[8], 8192);
@@ -1086,11 +1058,11 @@ cudaError_t tc2_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, i
         const int H = p.H;
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(pd.C)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
-        const cuuint32_t box[3] = {64, 1, BC};
+        (void)dims; (void)strides;
         const void *src[4] = {p.q, p.k, p.v, p.g};
-        CUtensorMap *dst[4] = {&maps.q, &maps.k, &maps.v, &maps.g};
+        RowMaps *dst[4] = {&maps.q, &maps.k, &maps.v, &maps.g};
         for (int i = 0; i < 4; ++i)
-            if (!encode_bf16(dst[i], src[i], 3, dims, strides, box)) return cudaErrorInvalidValue;
+            if (!encode_row_maps(dst[i], src[i], H, pd.C)) return cudaErrorInvalidValue;
     }
     kda_fwd_tc2<<<n_items, NT, f2::bytes, st>>>(p, pd, base, maps);
     return cudaGetLastError();
@@ -1109,11 +1081,11 @@ cudaError_t tc2_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t b
         const int H = p.f.H;
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(pd.C)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
-        const cuuint32_t box[3] = {64, 1, BC};
+        (void)dims; (void)strides;
         const void *src[4] = {p.f.q, p.f.k, p.f.g, p.d_o};
-        CUtensorMap *dst[4] = {&maps.q, &maps.k, &maps.g, &maps.dout};
+        RowMaps *dst[4] = {&maps.q, &maps.k, &maps.g, &maps.dout};
         for (int i = 0; i < 4; ++i)
-            if (!encode_bf16(dst[i], src[i], 3, dims, strides, box)) return cudaErrorInvalidValue;
+            if (!encode_row_maps(dst[i], src[i], H, pd.C)) return cudaErrorInvalidValue;
         const int64_t n_rec = pd.n_chunks * H;
         if (n_rec * (kRecBytes / 128) > INT32_MAX) return cudaErrorInvalidValue;   // TMA coordinates are int32
         const cuuint64_t rdims[2] = {64, static_cast<cuuint64_t>(n_rec * (kRecBytes / 128))};

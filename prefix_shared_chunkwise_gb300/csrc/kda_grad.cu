@@ -1,0 +1,767 @@
+// Gradient pass of bf16 packed-tree KDA on sm_103a (dk = dv = 128, chunk 64).
+//
+// Every (chunk, head) of every round is one independent item: with the chunk's start state
+// S (the forward's record), the state gradient dS' at its end (the state pass's record) and
+// T = (I + diag(beta) A)^-1 (the forward's record), all input gradients of the chunk follow
+// without any sequential dependence.  One CTA of 16 warps per SM walks the items in steps
+// of the grid size; every copy of the next item is issued before the current item's last
+// epilogue.  Notation (gamma the cumulative log-decay from the chunk start, m gamma at the
+// reference row, per key channel; t, s local rows):
+//   Kp = K e^{gamma-m}, Qp = scale Q e^{gamma-m}, Km = K e^{m-gamma}
+//   [A; P] = [Kp; Qp] Km^T, Tb = T diag(beta), R = S^T diag(e^m), Q' = dS'^T diag(e^{Gamma_L-m})
+//   Y^T = V^T - R Kp^T, U^T = Y^T Tb^T                              (the forward's U)
+//   dU^T = dO^T P + Q' Km^T,  dY^T = dU^T Tb,  dv = dY
+//   dP = lower(dO U^T),  dTb = dU Y^T,  dT = dTb diag(beta),  dM = -strict(T^T dT T^T)
+//   dA = diag(beta) dM,  dbeta = colsum(dTb .* T) + rowsum(dM .* A)
+//   dQp^T = R^T dO^T + Km^T dP^T,  dKp^T = -R^T dY^T + Km^T dA^T,
+//   dKm^T = Q'^T U^T + Kp^T dA + Qp^T dP
+//   dq = scale dQp e^{gamma-m},  dk = dKp e^{gamma-m} + dKm e^{m-gamma}
+//   dgamma = dKp Kp + dQp Qp - dKm Km (the rounded operands the products used),
+//   dGamma_L = colsum(Q' .* R) + colsum(Km .* (Q'^T U^T)^T), dg = suffix sums of dgamma + dGamma_L.
+// (Page "HARTS ... 精读", section 4.3, KDA paragraph: gradients of replayed rows add into the
+// ancestor rows they copy; they go to the replay-gradient buffer, folded later in a fixed
+// order.)
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kda_common.cuh"
+#include "tc_primitives.cuh"
+#include "tensor_map.h"
+#include "kda_stage.cuh"
+
+namespace harts {
+namespace {
+
+constexpr int D = 128, BC = 64, NT = 512;
+constexpr int64_t kRecBytes = (D * D + BC * BC) * 2;
+
+namespace g2 {
+constexpr uint32_t RR = 0;          // [128 dv][128 dk] S^T record -> R (atoms 16 KB)
+constexpr uint32_t QQ = 32768;      // [128 dv][128 dk] dS'^T record -> Q'
+constexpr uint32_t KQ = 65536;      // [128][128]: raw k -> Kp (rows 0-63), raw q -> Qp (64-127)
+constexpr uint32_t KM = 98304;      // [64][128] (atoms 8 KB): Km
+constexpr uint32_t VV = 114688;     // raw v [64][128] (atoms 8 KB) -> U^T [128][64]
+constexpr uint32_t DO = 131072;     // dO [64][128] (atoms 8 KB)
+constexpr uint32_t TT = 147456;     // T [64][64]
+constexpr uint32_t TB = 155648;     // Tb [64][64]    } TB..PT: raw g of the next item
+constexpr uint32_t PT = 163840;     // P -> dT [64][64] }
+constexpr uint32_t YT = 172032;     // Y^T [128][64] -> dv staging [64 t][128 dv] -> dq staging
+constexpr uint32_t DU = 188416;     // dU^T [128][64] -> -dY^T -> dk staging
+constexpr uint32_t DP = 204800;     // dP [64][64]   } DP..WA: dg staging
+constexpr uint32_t WA = 212992;     // W -> dA [64][64] }
+constexpr uint32_t VQS = 221184;    // fp32 [4][128] partial sums (several uses)
+constexpr uint32_t VMR = VQS + 2048;
+constexpr uint32_t VM2 = VMR + 512;       // m log2(e)
+constexpr uint32_t VEM = VM2 + 512;       // e^m
+constexpr uint32_t VEG = VEM + 512;       // e^{Gamma_L - m}
+constexpr uint32_t VBETA = VEG + 512;     // fp32 [64]
+constexpr uint32_t VDB = VBETA + 256;     // fp32 [4][64] dbeta partials
+constexpr uint32_t VDGL = VDB + 1024;     // fp32 [128] dGamma_L
+constexpr uint32_t END = VDGL + 512;
+constexpr uint32_t bytes = END + 1024;
+}  // namespace g2
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(tc::smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" :: "r"(tc::smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) { tc::tmem_ld16(taddr, r); }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&r)[16]) {
+    const uint32_t *u = reinterpret_cast<const uint32_t *>(r);
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 :: "r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
+                    "r"(u[7]), "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]),
+                    "r"(u[15]) : "memory");
+}
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&u)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
+                    "r"(u[7]) : "memory");
+}
+__device__ __forceinline__ void tmem_ld8u(uint32_t taddr, uint32_t (&u)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float bf(const uint8_t *p) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
+}
+__device__ __forceinline__ void unpack8(const uint4 &w, float (&f)[8]) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u[i]));
+        f[2 * i] = p.x;
+        f[2 * i + 1] = p.y;
+    }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    return make_uint4(tc::pack_bf16(f[0], f[1]), tc::pack_bf16(f[2], f[3]), tc::pack_bf16(f[4], f[5]),
+                      tc::pack_bf16(f[6], f[7]));
+}
+
+struct GradMaps2 {
+    RowMaps q, k, g, v, dout;
+    CUtensorMap rec_s;              // records as [rows of 256 B], boxes of 64 x 128 (a chunk's S^T)
+    CUtensorMap rec_t;              // records as [rows of 128 B], boxes of 64 x 64 (a chunk's T)
+    CUtensorMap dch;                // dS'^T records as [rows of 256 B], boxes of 64 x 128
+};
+
+struct Item {
+    int32_t h, g, seq, rho, L, c0, nv, row0, rptr;
+};
+
+__device__ __forceinline__ Item item_of(const PlanDev &pd, int32_t chunk_begin, int H, int32_t item) {
+    Item it;
+    it.h = item % H;
+    it.g = chunk_begin + item / H;
+    it.seq = pd.chunk_seq[it.g];
+    it.rho = pd.seq_rho[it.seq];
+    it.L = it.rho + pd.seq_nown[it.seq];
+    it.c0 = (it.g - pd.seq_cbase[it.seq]) * BC;
+    it.nv = min(BC, it.L - it.c0);
+    it.row0 = pd.seq_row0[it.seq];
+    it.rptr = pd.seq_rptr[it.seq];
+    return it;
+}
+
+__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t phase, int *s_fail) {
+    if (threadIdx.x == 0 && !tc::mbar_wait(bar, phase)) *s_fail = 1;
+    __syncthreads();
+    tc::fence_after_sync();
+    return *reinterpret_cast<volatile int *>(s_fail) == 0;
+}
+
+__device__ __forceinline__ void sync_mma() {
+    tc::fence_smem_to_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+}
+
+// Offset of element (row, col) in a [rows][64]-column SW128 atom (bf16).
+__device__ __forceinline__ uint32_t sw64(int row, int col) {
+    return static_cast<uint32_t>(row * 128 + ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1)));
+}
+
+__global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev pd, int32_t chunk_begin,
+                                                          int32_t n_items, const __grid_constant__ GradMaps2 maps) {
+    using namespace g2;
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
+    // mbarriers: 0-5 product batches; 6 q, 7 k, 8 g, 9 v, 10 dO, 11 T, 12 S^T, 13 dS'^T
+    __shared__ uint64_t bars[14];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_fail;
+    __shared__ int s_rows[64];
+    const FwdParams &f = p.f;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lq = warp & 3, cg = warp >> 2;
+    const int H = f.H;
+    const int W3 = 3 * D + 1;
+    const int jv = lq * 32 + lane;                  // TMEM lane of this thread
+    const uint32_t lane_off = static_cast<uint32_t>(lq * 32) << 16;
+    float *vqs = reinterpret_cast<float *>(sm + VQS), *vmr = reinterpret_cast<float *>(sm + VMR);
+    float *vm2 = reinterpret_cast<float *>(sm + VM2), *vem = reinterpret_cast<float *>(sm + VEM);
+    float *veg = reinterpret_cast<float *>(sm + VEG), *vbeta = reinterpret_cast<float *>(sm + VBETA);
+    float *vdb = reinterpret_cast<float *>(sm + VDB), *vdgl = reinterpret_cast<float *>(sm + VDGL);
+    const uint16_t *beta = static_cast<const uint16_t *>(f.beta);
+
+    if (tid == 0) {
+        for (int i = 0; i < 14; ++i) tc::mbar_init(&bars[i], 1);
+        tc::fence_mbar_init();
+        s_fail = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, 512);
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = s_tmem;
+    const uint32_t tAP = tm, tX = tm + 64, tDU = tm + 128, tDY = tm + 192, tDT = tm + 256, tKM = tm + 320,
+                   tGM = tm + 384, tPK = tm + 448;
+
+    int armed[14] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+    auto rows_of = [&](const Item &it) -> uint16_t {
+        if (tid >= 64) return 0;
+        const int64_t row = local_row(pd, it.seq, it.rho, it.L, it.c0 + tid);
+        s_rows[tid] = static_cast<int>(row);
+        return row >= 0 ? beta[row * H + it.h] : static_cast<uint16_t>(0);
+    };
+    // which: 0 q, 1 k, 2 g, 3 v, 4 dO, 5 T, 6 S^T record, 7 dS'^T record
+    auto stage = [&](int which, const Item &it, bool defer = false) {
+        ++armed[6 + which];
+        uint64_t *bar = &bars[6 + which];
+        const int t_own = max(0, it.rho - it.c0), t_end = it.nv;
+        const int32_t own0 = it.row0 + it.c0 - it.rho;
+        const int64_t rid = static_cast<int64_t>(it.g) * H + it.h;
+        switch (which) {
+        case 0: stage_chunk_rows<NT>(f.q, maps.q, s_rows, it.h, H, t_own, t_end, own0, 0, sm + KQ + 8192, sm + KQ + 24576, bar, defer); break;
+        case 1: stage_chunk_rows<NT>(f.k, maps.k, s_rows, it.h, H, t_own, t_end, own0, 0, sm + KQ, sm + KQ + 16384, bar, defer); break;
+        case 2: stage_chunk_rows<NT>(f.g, maps.g, s_rows, it.h, H, t_own, t_end, own0, 0, sm + TB, sm + TB + 8192, bar); break;
+        case 3: stage_chunk_rows<NT>(f.v, maps.v, s_rows, it.h, H, t_own, t_end, own0, 0, sm + VV, sm + VV + 8192, bar); break;
+        case 4: stage_chunk_rows<NT>(p.d_o, maps.dout, s_rows, it.h, H, t_own, t_end, own0, t_own, sm + DO, sm + DO + 8192,
+                                     bar, defer); break;
+        case 5:
+            if (tid == 0) {
+                tc::mbar_expect_tx(bar, 8192);
+                tc::tma_load_2d(sm + TT, &maps.rec_t, 0, static_cast<int>(rid * (kRecBytes / 128) + 2 * D), bar);
+            }
+            break;
+        case 6:
+            if (tid == 0) {
+                tc::mbar_expect_tx(bar, 32768);
+                tc::tma_load_2d(sm + RR, &maps.rec_s, 0, static_cast<int>(rid * (kRecBytes / 256)), bar);
+                tc::tma_load_2d(sm + RR + 16384, &maps.rec_s, 64, static_cast<int>(rid * (kRecBytes / 256)), bar);
+            }
+            break;
+        default:
+            if (tid == 0) {
+                tc::mbar_expect_tx(bar, 32768);
+                tc::tma_load_2d(sm + QQ, &maps.dch, 0, static_cast<int>(rid * D), bar);
+                tc::tma_load_2d(sm + QQ + 16384, &maps.dch, 64, static_cast<int>(rid * D), bar);
+            }
+            break;
+        }
+    };
+    auto wait_load = [&](int which, uint32_t ph) -> bool {
+        if (tid == 0 && !tc::mbar_wait(&bars[6 + which], ph)) s_fail = 1;
+        return true;
+    };
+
+    int32_t item = blockIdx.x;
+    Item cur{};
+    uint16_t braw = 0;
+    if (item < n_items) {
+        cur = item_of(pd, chunk_begin, H, item);
+        braw = rows_of(cur);
+        __syncthreads();
+        for (int w = 0; w < 8; ++w) stage(w, cur);
+    }
+    int32_t cur_seq = 0, cur_h = 0;
+    uint32_t n_done = 0;
+    for (; item < n_items; item += gridDim.x, ++n_done) {
+        const uint32_t ph = n_done & 1;
+        const Item I = cur;
+        cur_seq = I.seq; cur_h = I.h;
+        const int t_own = max(0, I.rho - I.c0), t_end = I.nv;
+        const int mid = (I.nv - 1) / 2;
+        const int32_t nxt = item + gridDim.x;
+        Item nx{};
+        if (nxt < n_items) nx = item_of(pd, chunk_begin, H, nxt);
+
+        // ---- pass A: sums of g over row quarters (g of this item sits in TB..PT) ---------------
+        wait_load(2, ph);
+        __syncthreads();
+        if (s_fail) break;
+        {
+            const int c = jv, q4 = cg;
+            float s_ = 0.f, mr = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int t = q4 * 16 + u;
+                s_ += bf(sm + TB + (c >> 6) * 8192 + sw64(t, c & 63));
+                if (t == mid) mr = s_;
+            }
+            vqs[q4 * 128 + c] = s_;
+            if (q4 == (mid >> 4)) vmr[c] = mr;
+            if (tid < 64) vbeta[tid] = __bfloat162float(__ushort_as_bfloat16(braw));
+        }
+        __syncthreads();
+        if (tid < 128) {
+            const int c = tid, qm = mid >> 4;
+            float m = vmr[c], gl = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float x = vqs[q * 128 + c];
+                gl += x;
+                if (q < qm) m += x;
+            }
+            if (-m > kMaxExpArg || m - gl > kMaxExpArg) dev_error(pd, kDevErrDecayRange, I.seq, I.c0);
+            vm2[c] = m * kLog2e;
+            vem[c] = ex2(m * kLog2e);
+            veg[c] = ex2((gl - m) * kLog2e);
+        }
+        wait_load(0, ph);
+        wait_load(1, ph);
+        __syncthreads();
+        if (s_fail) break;
+        // ---- pass B: Kp, Qp in place, Km; gamma and the bf16 Kp, Qp (pairs) into TMEM ----------
+        {
+            const int c = jv, q4 = cg;
+            float gam = 0.f;
+#pragma unroll
+            for (int q = 0; q < 3; ++q) gam += q < q4 ? vqs[q * 128 + c] : 0.f;
+            const float m2 = vm2[c], sc = f.scale;
+            float g2v[16];
+            uint32_t kpk[8], qpk[8];
+#pragma unroll
+            for (int u = 0; u < 16; u += 2) {
+                float kp2[2], qp2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = q4 * 16 + u + e;
+                    const uint32_t o = (c >> 6) * 16384 + sw64(t, c & 63), oq = (c >> 6) * 16384 + sw64(64 + t, c & 63);
+                    gam += bf(sm + TB + (c >> 6) * 8192 + sw64(t, c & 63));
+                    const float kk = bf(sm + KQ + o), qq = bf(sm + KQ + oq);
+                    const float x = fmaf(gam, kLog2e, -m2);
+                    const float e1 = ex2(x), e2 = ex2(-x);
+                    const __nv_bfloat16 kpb = __float2bfloat16_rn(kk * e1), qpb = __float2bfloat16_rn(sc * qq * e1);
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + KQ + o) = kpb;
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + KQ + oq) = qpb;
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + KM + (c >> 6) * 8192 + sw64(t, c & 63)) =
+                        __float2bfloat16_rn(kk * e2);
+                    g2v[u + e] = gam * kLog2e;
+                    kp2[e] = __bfloat162float(kpb);
+                    qp2[e] = __bfloat162float(qpb);
+                }
+                kpk[u / 2] = tc::pack_bf16(kp2[0], kp2[1]);
+                qpk[u / 2] = tc::pack_bf16(qp2[0], qp2[1]);
+            }
+            tmem_st16(tGM + lane_off + q4 * 16, g2v);
+            tmem_st8u(tPK + lane_off + q4 * 8, kpk);
+            tmem_st8u(tPK + lane_off + 32 + q4 * 8, qpk);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+        // ---- R = S^T diag(e^m), Q' = dS'^T diag(e^{Gamma_L - m}) in place; Tb = T diag(beta) --------
+        wait_load(5, ph);
+        wait_load(6, ph);
+        wait_load(7, ph);
+        __syncthreads();
+        if (s_fail) break;
+        {
+            // warp w: logical 8-column chunk w (atom w / 8) of every row; lane: rows lane + 32 i.
+            // Scales R and Q' in place and sums R .* Q' over the rows (dGamma_L's first term).
+            const int jl = warp & 7, atom = warp >> 3, col0 = atom * 64 + jl * 8;
+            const float4 ea = *reinterpret_cast<const float4 *>(vem + col0), eb = *reinterpret_cast<const float4 *>(vem + col0 + 4);
+            const float4 ga = *reinterpret_cast<const float4 *>(veg + col0), gb = *reinterpret_cast<const float4 *>(veg + col0 + 4);
+            const float es[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
+            const float gs[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+            float dot[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = lane + 32 * i;
+                const uint32_t off = atom * 16384 + r * 128 + ((jl ^ (r & 7)) << 4);
+                uint4 *pr = reinterpret_cast<uint4 *>(sm + RR + off), *pq = reinterpret_cast<uint4 *>(sm + QQ + off);
+                float vr[8], vq[8];
+                unpack8(*pr, vr);
+                unpack8(*pq, vq);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) { vr[k] *= es[k]; vq[k] *= gs[k]; }
+                const uint4 wr = pack8(vr), wq = pack8(vq);
+                *pr = wr;
+                *pq = wq;
+                unpack8(wr, vr);        // the rounded values the products will use
+                unpack8(wq, vq);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) dot[k] += vr[k] * vq[k];
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+#pragma unroll
+                for (int sh = 16; sh >= 1; sh >>= 1) dot[k] += __shfl_xor_sync(0xffffffffu, dot[k], sh);
+            }
+            if (lane == 0) {
+                *reinterpret_cast<float4 *>(vdgl + col0) = make_float4(dot[0], dot[1], dot[2], dot[3]);
+                *reinterpret_cast<float4 *>(vdgl + col0 + 4) = make_float4(dot[4], dot[5], dot[6], dot[7]);
+            }
+        }
+        {
+            const int t = tid >> 3, j = tid & 7;              // Tb: row t, 16-byte chunk j
+            const uint4 w = *reinterpret_cast<const uint4 *>(sm + TT + t * 128 + (j << 4));
+            const int col0 = (j ^ (t & 7)) << 3;
+            float v[8];
+            unpack8(w, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] *= vbeta[col0 + i];
+            *reinterpret_cast<uint4 *>(sm + TB + t * 128 + (j << 4)) = pack8(v);
+        }
+        sync_mma();
+        // ---- B1: [A; P] = [Kp; Qp] Km^T;  X = R Kp^T;  dU^T = Q' Km^T ---------------------------
+        if (tid == 0) {
+            const uint32_t id = tc::idesc_bf16(128, 64);
+            tc::mma_tile(tAP, tc::smem_addr(sm + KQ), 16384, tc::smem_addr(sm + KM), 8192, 128, id, false);
+            tc::mma_tile(tX, tc::smem_addr(sm + RR), 16384, tc::smem_addr(sm + KQ), 16384, 128, id, false);
+            tc::mma_tile(tDU, tc::smem_addr(sm + QQ), 16384, tc::smem_addr(sm + KM), 8192, 128, id, false);
+            tc::mma_commit(&bars[0]);
+        }
+        ++armed[0];
+        wait_load(3, ph);                                   // v, read below
+        if (!wait_mma(&bars[0], ph, &s_fail)) break;
+        // ---- E1: P -> PT (lower with the diagonal); Y^T = V^T - X -> YT ----------------------------
+        {
+            float r[16];
+            if (lq >= 2) {
+                tmem_ld16(tAP + lane_off + cg * 16, r);
+                const int t = jv - 64;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) r[j] = (cg * 16 + j <= t) ? r[j] : 0.f;
+                tc::st_sw128_8(sm + PT, 64, t, cg * 16, r);
+                tc::st_sw128_8(sm + PT, 64, t, cg * 16 + 8, r + 8);
+            }
+            tmem_ld16(tX + lane_off + cg * 16, r);
+            const int dv = jv;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = cg * 16 + j;
+                r[j] = bf(sm + VV + (dv >> 6) * 8192 + sw64(t, dv & 63)) - r[j];
+            }
+            tc::st_sw128_8(sm + YT, 128, dv, cg * 16, r);
+            tc::st_sw128_8(sm + YT, 128, dv, cg * 16 + 8, r + 8);
+        }
+        sync_mma();
+        // ---- B2: U^T = Y^T Tb^T;  dU^T += dO^T P -----------------------------------------------------
+        wait_load(4, ph);
+        __syncthreads();
+        if (s_fail) break;
+        if (tid == 0) {
+            tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + YT), 16384, false}, tc::Opnd{tc::smem_addr(sm + TB), 8192, false},
+                       128, 64, 64, false);
+            tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + DO), 8192, true}, tc::Opnd{tc::smem_addr(sm + PT), 8192, true},
+                       128, 64, 64, true);
+            tc::mma_commit(&bars[1]);
+        }
+        ++armed[1];
+        if (!wait_mma(&bars[1], ph, &s_fail)) break;
+        // ---- E2: U^T -> VV (raw v is consumed), dU^T -> DU -------------------------------------------
+        {
+            float r[16];
+            tmem_ld16(tX + lane_off + cg * 16, r);
+            tc::st_sw128_8(sm + VV, 128, jv, cg * 16, r);
+            tc::st_sw128_8(sm + VV, 128, jv, cg * 16 + 8, r + 8);
+            tmem_ld16(tDU + lane_off + cg * 16, r);
+            tc::st_sw128_8(sm + DU, 128, jv, cg * 16, r);
+            tc::st_sw128_8(sm + DU, 128, jv, cg * 16 + 8, r + 8);
+        }
+        sync_mma();
+        // ---- B3: dY^T = dU^T Tb;  dP = dO U^T (M = 64);  dTb = dU Y^T (M = 64);  Km' = Q'^T U^T -------
+        if (tid == 0) {
+            tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + DU), 16384, false}, tc::Opnd{tc::smem_addr(sm + TB), 8192, true},
+                       128, 64, 64, false);
+            tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + DO), 8192, false}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
+                       64, 64, 128, false);
+            tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + DU), 16384, true}, tc::Opnd{tc::smem_addr(sm + YT), 16384, true},
+                       64, 64, 128, false);
+            tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + QQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
+                       128, 64, 128, false);
+            tc::mma_commit(&bars[2]);
+        }
+        ++armed[2];
+        if (!wait_mma(&bars[2], ph, &s_fail)) break;
+        // Q' and V / U^T are consumed: the next item's dS'^T record and v.  Its row table (and
+        // beta) are formed first; the staging calls after the barrier read them.
+        if (nxt < n_items) braw = rows_of(nx);
+        __syncthreads();
+        if (nxt < n_items) {
+            stage(7, nx);
+            stage(3, nx);
+        }
+        // ---- E3a: dT -> PT and dbeta's Tb part (from dTb), then W = dT T^T is issued at once ------------
+        {
+            float bq[16], dbs[16];
+            tmem_ld16(tDT + lane_off + cg * 16, bq);       // M = 64: row 16 lq + lane in lanes 0-15
+            if (lane < 16) {
+                const int t = 16 * lq + lane;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int s = cg * 16 + j;
+                    dbs[j] = s <= t ? bq[j] * bf(sm + TT + sw64(t, s)) : 0.f;     // dTb .* T
+                    bq[j] = s < t ? bq[j] * vbeta[s] : 0.f;                       // dT
+                }
+                tc::st_sw128_8(sm + PT, 64, t, cg * 16, bq);
+                tc::st_sw128_8(sm + PT, 64, t, cg * 16 + 8, bq + 8);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) dbs[j] = 0.f;
+            }
+            // column sums of dTb .* T over this quarter's 16 rows (lanes 0-15)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float x = dbs[j];
+                x += __shfl_xor_sync(0xffffffffu, x, 8);
+                x += __shfl_xor_sync(0xffffffffu, x, 4);
+                x += __shfl_xor_sync(0xffffffffu, x, 2);
+                x += __shfl_xor_sync(0xffffffffu, x, 1);
+                if (lane == 0) vdb[lq * 64 + cg * 16 + j] = x;
+            }
+        }
+        sync_mma();
+        // ---- B4: W = dT T^T (M = 64) into the dTb columns -----------------------------------------------
+        if (tid == 0) {
+            tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + PT), 8192, false}, tc::Opnd{tc::smem_addr(sm + TT), 8192, false},
+                       64, 64, 64, false);
+            tc::mma_commit(&bars[3]);
+        }
+        ++armed[3];
+        // ---- E3b while W runs: dY -> dv (staged [t][dv] over Y^T) and -dY^T -> DU; dP -> DP;
+        //      sum_t Km Km' for dGamma_L; the dv rows out ----------------------------------------------------
+        {
+            float r[16];
+            tmem_ld16(tDY + lane_off + cg * 16, r);
+            const int dv = jv;
+            __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + YT);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = cg * 16 + j;
+                dvs[t * D + dv] = __float2bfloat16_rn(r[j]);
+                if (t < t_own && t < t_end)
+                    p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + D + dv] = r[j];
+                r[j] = -r[j];
+            }
+            tc::st_sw128_8(sm + DU, 128, dv, cg * 16, r);
+            tc::st_sw128_8(sm + DU, 128, dv, cg * 16 + 8, r + 8);
+            float a[16];
+            tmem_ld16(tDU + lane_off + cg * 16, a);        // dP, M = 64
+            if (lane < 16) {
+                const int t = 16 * lq + lane;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) a[j] = (cg * 16 + j <= t) ? a[j] : 0.f;
+                tc::st_sw128_8(sm + DP, 64, t, cg * 16, a);
+                tc::st_sw128_8(sm + DP, 64, t, cg * 16 + 8, a + 8);
+            }
+            // sum_t Km[t][c] Km'[c][t]
+            tmem_ld16(tKM + lane_off + cg * 16, a);
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc += a[j] * bf(sm + KM + (jv >> 6) * 8192 + sw64(cg * 16 + j, jv & 63));
+            vqs[cg * 128 + jv] = acc;
+        }
+        __syncthreads();
+        {
+            __nv_bfloat16 *dvo = static_cast<__nv_bfloat16 *>(p.dv);
+            for (int e = tid; e < 64 * 16; e += NT) {
+                const int t = e >> 4, pc = e & 15;
+                if (t < t_own || t >= t_end) continue;
+                const int64_t row = static_cast<int64_t>(I.row0) + (I.c0 + t - I.rho);
+                *reinterpret_cast<uint4 *>(dvo + (row * H + I.h) * D + pc * 8) =
+                    *reinterpret_cast<const uint4 *>(sm + YT + t * 256 + pc * 16);
+            }
+            if (tid < 128) vdgl[tid] += vqs[tid] + vqs[128 + tid] + vqs[256 + tid] + vqs[384 + tid];
+            if (tid < 64) vdb[tid] = vdb[tid] + vdb[64 + tid] + vdb[128 + tid] + vdb[192 + tid];
+        }
+        if (!wait_mma(&bars[3], ph, &s_fail)) break;
+        if (nxt < n_items) stage(2, nx);                   // Tb and dT are consumed: the next item's g
+        // ---- E4: W -> WA -------------------------------------------------------------------------------
+        {
+            float r[16];
+            tmem_ld16(tDT + lane_off + cg * 16, r);
+            if (lane < 16) {
+                const int t = 16 * lq + lane;
+                tc::st_sw128_8(sm + WA, 64, t, cg * 16, r);
+                tc::st_sw128_8(sm + WA, 64, t, cg * 16 + 8, r + 8);
+            }
+        }
+        sync_mma();
+        // ---- B5: T^T W (M = 128: rows 64-127 read Tb as padding, so row r lands in lane r) ------------
+        if (tid == 0) {
+            tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + TT), 8192, true}, tc::Opnd{tc::smem_addr(sm + WA), 8192, true},
+                       128, 64, 64, false);
+            tc::mma_commit(&bars[4]);
+        }
+        ++armed[4];
+        if (!wait_mma(&bars[4], ph, &s_fail)) break;
+        if (nxt < n_items) stage(5, nx);                   // T consumed: the next item's T
+        // ---- E5: dM = -strict(T^T W); dA = diag(beta) dM -> WA; dbeta += rowsum(dM .* A) ----------------
+        {
+            float r[16], a[16];
+            tmem_ld16(tDT + lane_off + cg * 16, r);
+            tmem_ld16(tAP + lane_off + cg * 16, a);
+            if (lq < 2) {
+                const int t = jv;
+                const float bt = vbeta[t];
+                float dba = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int s = cg * 16 + j;
+                    const float dm = s < t ? -r[j] : 0.f;
+                    dba += dm * a[j];
+                    r[j] = bt * dm;
+                }
+                vqs[cg * 64 + t] = dba;
+            }
+            __syncthreads();
+            if (lq < 2) {
+                const int t = jv;
+                tc::st_sw128_8(sm + WA, 64, t, cg * 16, r);
+                tc::st_sw128_8(sm + WA, 64, t, cg * 16 + 8, r + 8);
+            }
+            if (tid < 64) vdb[tid] += vqs[tid] + vqs[64 + tid] + vqs[128 + tid] + vqs[192 + tid];
+        }
+        sync_mma();
+        // ---- B6: dQp^T = R^T dO^T + Km^T dP^T;  dKp^T = -R^T dY^T + Km^T dA^T;  Km' += Kp^T dA + Qp^T dP --
+        if (tid == 0) {
+            tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DO), 8192, false},
+                       128, 64, 128, false);
+            tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + KM), 8192, true}, tc::Opnd{tc::smem_addr(sm + DP), 8192, false},
+                       128, 64, 64, true);
+            tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DU), 16384, true},
+                       128, 64, 128, false);
+            tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + KM), 8192, true}, tc::Opnd{tc::smem_addr(sm + WA), 8192, false},
+                       128, 64, 64, true);
+            tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + KQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + WA), 8192, true},
+                       128, 64, 64, true);
+            tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + KQ) + 8192, 16384, true},
+                       tc::Opnd{tc::smem_addr(sm + DP), 8192, true}, 128, 64, 64, true);
+            tc::mma_commit(&bars[5]);
+        }
+        ++armed[5];
+        if (!wait_mma(&bars[5], ph, &s_fail)) break;
+        // everything but Km (read below) is consumed: the next item's q, k, dO and S^T record
+        if (nxt < n_items) {
+            // q, k, dO of a gathered chunk share one barrier pass
+            const bool gq = chunk_gathers(max(0, nx.rho - nx.c0), nx.nv, 0);
+            const bool gd = chunk_gathers(max(0, nx.rho - nx.c0), nx.nv, max(0, nx.rho - nx.c0));
+            stage(0, nx, true);
+            stage(1, nx, true);
+            stage(4, nx, true);
+            stage(6, nx);
+            if (gq || gd) {
+                __syncthreads();
+                if (tid == 0) {
+                    if (gq) { mbar_arrive_one(&bars[6]); mbar_arrive_one(&bars[7]); }
+                    if (gd) mbar_arrive_one(&bars[10]);
+                }
+            }
+        }
+        // ---- E6: dq, dk, dgamma per (channel, row); dg = suffix sums + dGamma_L ---------------------------
+        {
+            const int c = jv;
+            float xq[16], xp[16], xm[16], g2v[16];
+            uint32_t kpk[8], qpk[8];
+            tmem_ld16(tX + lane_off + cg * 16, xq);
+            tmem_ld16(tDU + lane_off + cg * 16, xp);
+            tmem_ld16(tKM + lane_off + cg * 16, xm);
+            tmem_ld16(tGM + lane_off + cg * 16, g2v);
+            tmem_ld8u(tPK + lane_off + cg * 8, kpk);
+            tmem_ld8u(tPK + lane_off + 32 + cg * 8, qpk);
+            const float m2 = vm2[c], sc = f.scale;
+            __nv_bfloat16 *dqs = reinterpret_cast<__nv_bfloat16 *>(sm + YT);
+            __nv_bfloat16 *dks = reinterpret_cast<__nv_bfloat16 *>(sm + DU);
+            float dgm[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = cg * 16 + j;
+                const float2 kp2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kpk[j >> 1]));
+                const float2 qp2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qpk[j >> 1]));
+                const float kp = (j & 1) ? kp2.y : kp2.x, qp = (j & 1) ? qp2.y : qp2.x;
+                const float km = bf(sm + KM + (c >> 6) * 8192 + sw64(t, c & 63));
+                const float x = g2v[j] - m2;
+                const float e1 = ex2(x), e2 = ex2(-x);
+                const float dqv = sc * xq[j] * e1;
+                const float dkv = xp[j] * e1 + xm[j] * e2;
+                dgm[j] = xq[j] * qp + xp[j] * kp - xm[j] * km;
+                dqs[t * D + c] = __float2bfloat16_rn(dqv);
+                dks[t * D + c] = __float2bfloat16_rn(dkv);
+                if (t < t_own && t < t_end)
+                    p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + c] = dkv;
+            }
+            // suffix sums over t: within this thread's 16 rows, then the later quarters' totals
+            float run = 0.f;
+#pragma unroll
+            for (int j = 15; j >= 0; --j) { run += dgm[j]; dgm[j] = run; }
+            vqs[cg * 128 + c] = run;
+            __syncthreads();
+            float off = vdgl[c];
+#pragma unroll
+            for (int q = 1; q < 4; ++q) off += q > cg ? vqs[q * 128 + c] : 0.f;
+            __nv_bfloat16 *dgs = reinterpret_cast<__nv_bfloat16 *>(sm + DP);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = cg * 16 + j;
+                const float x = dgm[j] + off;
+                dgs[t * D + c] = __float2bfloat16_rn(x);
+                if (t < t_own && t < t_end)
+                    p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + 2 * D + c] = x;
+            }
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        for (int e = tid; e < 3 * 64 * 16; e += NT) {
+            const int which = e >> 10, t = (e >> 4) & 63, pc = e & 15;
+            if (t < t_own || t >= t_end) continue;
+            const int64_t row = static_cast<int64_t>(I.row0) + (I.c0 + t - I.rho);
+            void *dst = which == 0 ? p.dq : (which == 1 ? p.dk : p.dg);
+            const uint8_t *srcp = sm + (which == 0 ? YT : (which == 1 ? DU : DP));
+            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(dst) + (row * H + I.h) * D + pc * 8) =
+                *reinterpret_cast<const uint4 *>(srcp + t * 256 + pc * 16);
+        }
+        if (tid < 64) {
+            const int t = tid;
+            const float db = vdb[t];
+            if (t < t_end) {
+                if (t >= t_own)
+                    static_cast<__nv_bfloat16 *>(p.dbeta)[(static_cast<int64_t>(I.row0) + (I.c0 + t - I.rho)) * H + I.h] =
+                        __float2bfloat16_rn(db);
+                else
+                    p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + 3 * D] = db;
+            }
+        }
+        __syncthreads();
+        tc::fence_after_sync();
+        cur = nx;
+    }
+    // ---- drain --------------------------------------------------------------------------------------
+    tc::cp_async_wait_all();
+    __syncthreads();
+    if (s_fail) {
+        dev_error(pd, kDevErrTimeout, cur_seq, cur_h);
+        if (tid == 0)
+            for (int i = 0; i < 14; ++i)
+                if (armed[i] > 0 && !tc::mbar_wait(&bars[i], (armed[i] - 1) & 1, 200000000LL))
+                    dev_error(pd, kDevErrTimeout, cur_seq, cur_h);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tm, 512);
+}
+
+bool flat_map2(CUtensorMap *m, const void *base, int64_t n_rows, int cols, int box_rows) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(n_rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    return encode_bf16(m, base, 2, dims, strides, box);
+}
+
+}  // namespace
+
+cudaError_t tc2_bwd_grad(const BwdParams &p, const PlanDev &pd, int32_t chunk_begin, int32_t n_items,
+                         cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(kda_bwd_grad_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(g2::bytes));
+    if (e != cudaSuccess) return e;
+    if (n_items <= 0) return cudaSuccess;
+    const int H = p.f.H;
+    const int64_t n_rec = pd.n_chunks * H;
+    if (n_rec * (kRecBytes / 128) > INT32_MAX) return cudaErrorInvalidValue;   // TMA coordinates are int32
+    GradMaps2 maps;
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(pd.C)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+        (void)dims; (void)strides;
+        const void *src[5] = {p.f.q, p.f.k, p.f.g, p.f.v, p.d_o};
+        RowMaps *dst[5] = {&maps.q, &maps.k, &maps.g, &maps.v, &maps.dout};
+        for (int i = 0; i < 5; ++i)
+            if (!encode_row_maps(dst[i], src[i], H, pd.C)) return cudaErrorInvalidValue;
+        if (!flat_map2(&maps.rec_s, p.f.chunk_states, n_rec * (kRecBytes / 256), 128, 128) ||
+            !flat_map2(&maps.rec_t, p.f.chunk_states, n_rec * (kRecBytes / 128), 64, 64) ||
+            !flat_map2(&maps.dch, p.dchunk, n_rec * D, 128, 128))
+            return cudaErrorInvalidValue;
+    }
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    kda_bwd_grad_tc2<<<min(n_items, nsm), NT, g2::bytes, st>>>(p, pd, chunk_begin, n_items, maps);
+    return cudaGetLastError();
+}
+
+}  // namespace harts
