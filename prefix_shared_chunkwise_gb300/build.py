@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_harts.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["plan.cpp", "harts_abi.cu", "kda_simt.cu", "kda_tc.cu", "kda_fwd.cu", "kda_grad.cu", "conv.cu", "logprob.cu", "attn.cu"]
+SOURCES = ["plan.cpp", "harts_abi.cu", "kda_simt.cu", "kda_noreplay.cu", "kda_seq.cu", "kda_grad.cu", "conv.cu", "logprob.cu", "attn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

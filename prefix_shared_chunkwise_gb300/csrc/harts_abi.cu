@@ -20,12 +20,10 @@ cudaError_t tc_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, in
                          int32_t max_chunks, cudaStream_t st);
 cudaError_t tc2_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t base, int32_t n_items,
                                 cudaStream_t st);
-cudaError_t tc_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t base,
-                               int32_t n_items, cudaStream_t st);
+
 cudaError_t tc2_bwd_grad(const BwdParams &p, const PlanDev &pd, int32_t chunk_begin, int32_t n_items,
                          cudaStream_t st);
-cudaError_t tc_bwd_grad(const BwdParams &p, const PlanDev &pd, int32_t chunk_begin,
-                        int32_t n_items, cudaStream_t st);
+
 
 namespace {
 

@@ -95,6 +95,47 @@ __device__ __forceinline__ void tmem_ld8u(uint32_t taddr, uint32_t (&u)[8]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// TMEM loads issued back to back and waited for once.  The wait names the loaded registers
+// ("+r"), so no use of them can be scheduled above it.
+__device__ __forceinline__ void tld16(uint32_t taddr, float (&r)[16]) {
+    uint32_t *u = reinterpret_cast<uint32_t *>(r);
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+                   "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tld8(uint32_t taddr, uint32_t (&u)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
+                 : "r"(taddr));
+}
+#define HARTS_R16(a) "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), \
+    "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15])
+__device__ __forceinline__ void twait(float (&a)[16]) {
+    uint32_t *x = reinterpret_cast<uint32_t *>(a);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : HARTS_R16(x) :: "memory");
+}
+__device__ __forceinline__ void twait(float (&a)[16], float (&b)[16]) {
+    uint32_t *x = reinterpret_cast<uint32_t *>(a), *y = reinterpret_cast<uint32_t *>(b);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : HARTS_R16(x), HARTS_R16(y) :: "memory");
+}
+__device__ __forceinline__ void twait(float (&a)[16], float (&b)[16], float (&c)[16]) {
+    uint32_t *x = reinterpret_cast<uint32_t *>(a), *y = reinterpret_cast<uint32_t *>(b),
+             *z = reinterpret_cast<uint32_t *>(c);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : HARTS_R16(x), HARTS_R16(y), HARTS_R16(z) :: "memory");
+}
+__device__ __forceinline__ void twait(float (&a)[16], float (&b)[16], float (&c)[16], float (&d)[16]) {
+    uint32_t *x = reinterpret_cast<uint32_t *>(a), *y = reinterpret_cast<uint32_t *>(b),
+             *z = reinterpret_cast<uint32_t *>(c), *w = reinterpret_cast<uint32_t *>(d);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : HARTS_R16(x), HARTS_R16(y), HARTS_R16(z), HARTS_R16(w) :: "memory");
+}
+// Orders later uses of already-waited registers after the preceding wait.
+__device__ __forceinline__ void tkeep(uint32_t (&a)[8], uint32_t (&b)[8]) {
+    asm volatile("" : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                      "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]));
+}
+#undef HARTS_R16
+
 __device__ __forceinline__ float bf(const uint8_t *p) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
 }
@@ -399,16 +440,17 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
         if (!wait_mma(&bars[0], ph, &s_fail)) break;
         // ---- E1: P -> PT (lower with the diagonal); Y^T = V^T - X -> YT ----------------------------
         {
-            float r[16];
+            float r[16], pv[16];
+            tld16(tAP + lane_off + cg * 16, pv);
+            tld16(tX + lane_off + cg * 16, r);
+            twait(pv, r);
             if (lq >= 2) {
-                tmem_ld16(tAP + lane_off + cg * 16, r);
                 const int t = jv - 64;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) r[j] = (cg * 16 + j <= t) ? r[j] : 0.f;
-                tc::st_sw128_8(sm + PT, 64, t, cg * 16, r);
-                tc::st_sw128_8(sm + PT, 64, t, cg * 16 + 8, r + 8);
+                for (int j = 0; j < 16; ++j) pv[j] = (cg * 16 + j <= t) ? pv[j] : 0.f;
+                tc::st_sw128_8(sm + PT, 64, t, cg * 16, pv);
+                tc::st_sw128_8(sm + PT, 64, t, cg * 16 + 8, pv + 8);
             }
-            tmem_ld16(tX + lane_off + cg * 16, r);
             const int dv = jv;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -434,13 +476,14 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
         if (!wait_mma(&bars[1], ph, &s_fail)) break;
         // ---- E2: U^T -> VV (raw v is consumed), dU^T -> DU -------------------------------------------
         {
-            float r[16];
-            tmem_ld16(tX + lane_off + cg * 16, r);
+            float r[16], r2[16];
+            tld16(tX + lane_off + cg * 16, r);
+            tld16(tDU + lane_off + cg * 16, r2);
+            twait(r, r2);
             tc::st_sw128_8(sm + VV, 128, jv, cg * 16, r);
             tc::st_sw128_8(sm + VV, 128, jv, cg * 16 + 8, r + 8);
-            tmem_ld16(tDU + lane_off + cg * 16, r);
-            tc::st_sw128_8(sm + DU, 128, jv, cg * 16, r);
-            tc::st_sw128_8(sm + DU, 128, jv, cg * 16 + 8, r + 8);
+            tc::st_sw128_8(sm + DU, 128, jv, cg * 16, r2);
+            tc::st_sw128_8(sm + DU, 128, jv, cg * 16 + 8, r2 + 8);
         }
         sync_mma();
         // ---- B3: dY^T = dU^T Tb;  dP = dO U^T (M = 64);  dTb = dU Y^T (M = 64);  Km' = Q'^T U^T -------
@@ -505,8 +548,11 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
         // ---- E3b while W runs: dY -> dv (staged [t][dv] over Y^T) and -dY^T -> DU; dP -> DP;
         //      sum_t Km Km' for dGamma_L; the dv rows out ----------------------------------------------------
         {
-            float r[16];
-            tmem_ld16(tDY + lane_off + cg * 16, r);
+            float r[16], a[16], km2[16];
+            tld16(tDY + lane_off + cg * 16, r);
+            tld16(tDU + lane_off + cg * 16, a);            // dP, M = 64
+            tld16(tKM + lane_off + cg * 16, km2);
+            twait(r, a, km2);
             const int dv = jv;
             __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + YT);
 #pragma unroll
@@ -519,8 +565,6 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             }
             tc::st_sw128_8(sm + DU, 128, dv, cg * 16, r);
             tc::st_sw128_8(sm + DU, 128, dv, cg * 16 + 8, r + 8);
-            float a[16];
-            tmem_ld16(tDU + lane_off + cg * 16, a);        // dP, M = 64
             if (lane < 16) {
                 const int t = 16 * lq + lane;
 #pragma unroll
@@ -529,10 +573,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                 tc::st_sw128_8(sm + DP, 64, t, cg * 16 + 8, a + 8);
             }
             // sum_t Km[t][c] Km'[c][t]
-            tmem_ld16(tKM + lane_off + cg * 16, a);
             float acc = 0.f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc += a[j] * bf(sm + KM + (jv >> 6) * 8192 + sw64(cg * 16 + j, jv & 63));
+            for (int j = 0; j < 16; ++j) acc += km2[j] * bf(sm + KM + (jv >> 6) * 8192 + sw64(cg * 16 + j, jv & 63));
             vqs[cg * 128 + jv] = acc;
         }
         __syncthreads();
@@ -573,8 +616,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
         // ---- E5: dM = -strict(T^T W); dA = diag(beta) dM -> WA; dbeta += rowsum(dM .* A) ----------------
         {
             float r[16], a[16];
-            tmem_ld16(tDT + lane_off + cg * 16, r);
-            tmem_ld16(tAP + lane_off + cg * 16, a);
+            tld16(tDT + lane_off + cg * 16, r);
+            tld16(tAP + lane_off + cg * 16, a);
+            twait(r, a);
             if (lq < 2) {
                 const int t = jv;
                 const float bt = vbeta[t];
@@ -637,12 +681,14 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             const int c = jv;
             float xq[16], xp[16], xm[16], g2v[16];
             uint32_t kpk[8], qpk[8];
-            tmem_ld16(tX + lane_off + cg * 16, xq);
-            tmem_ld16(tDU + lane_off + cg * 16, xp);
-            tmem_ld16(tKM + lane_off + cg * 16, xm);
-            tmem_ld16(tGM + lane_off + cg * 16, g2v);
-            tmem_ld8u(tPK + lane_off + cg * 8, kpk);
-            tmem_ld8u(tPK + lane_off + 32 + cg * 8, qpk);
+            tld16(tX + lane_off + cg * 16, xq);
+            tld16(tDU + lane_off + cg * 16, xp);
+            tld16(tKM + lane_off + cg * 16, xm);
+            tld16(tGM + lane_off + cg * 16, g2v);
+            tld8(tPK + lane_off + cg * 8, kpk);
+            tld8(tPK + lane_off + 32 + cg * 8, qpk);
+            twait(xq, xp, xm, g2v);
+            tkeep(kpk, qpk);
             const float m2 = vm2[c], sc = f.scale;
             __nv_bfloat16 *dqs = reinterpret_cast<__nv_bfloat16 *>(sm + YT);
             __nv_bfloat16 *dks = reinterpret_cast<__nv_bfloat16 *>(sm + DU);

@@ -1,4 +1,5 @@
-// Forward of bf16 packed-tree KDA on sm_103a (dk = dv = 128, chunk 64): two CTAs per SM.
+// The two sequential passes of bf16 packed-tree KDA on sm_103a (dk = dv = 128, chunk 64),
+// forward and backward state pass, each with two CTAs per SM.
 //
 // One CTA (256 threads) per (sequence, head) of a round, chunks in order (page "HARTS ...
 // 精读", section 4.3, KDA paragraph: one packed call per round, each sequence resuming

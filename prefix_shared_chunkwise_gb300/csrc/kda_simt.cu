@@ -1,7 +1,7 @@
 // Exact fp32 CUDA-core kernels for packed-tree KDA (any of dk = dv in {32, 64, 128},
 // chunk B in {16, 32, 64}).  These are the precision path: every product is fp32
 // FMA, no tensor-core rounding, so fp32 workloads meet a 1e-5 relative error.  The
-// tensor-core kernels (kda_tc.cu) carry the bf16 throughput workloads.
+// tensor-core kernels (kda_seq.cu, kda_grad.cu) carry the bf16 throughput workloads.
 //
 // One CTA per (sequence, head) of a round.  The state S (D x D, fp32) lives in shared
 // memory for the whole sequence; chunks are processed in order.  Chunk math follows
