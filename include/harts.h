@@ -186,9 +186,15 @@ typedef struct {
                                 (NULL = zero state) */
     void *chunk_states;      /* device, nullable: per (chunk, head) a record of dk*dv + B*B
                                 elements in `dtype`: the state at the chunk start stored
-                                transposed (S^T, [dv][dk]) followed by the chunk's
+                                transposed ([dv][dk]) followed by the chunk's
                                 T = (I + diag(beta) A)^-1 ([B][B]); saved for the backward
-                                pass; records ordered [chunk][head], chunks by sequence */
+                                pass; records ordered [chunk][head], chunks by sequence.
+                                The tensor-core kernels store the state column-scaled as
+                                their products use it, S^T diag(e^m) with m the chunk's
+                                reference log-decay (the cumulative log-decay at row
+                                (n-1)/2 of the chunk's n rows); the exact-fp32 kernels
+                                store S^T.  A backward call must therefore select the same
+                                kernel family as the forward call that wrote the records. */
 } harts_kda_fwd_args;
 
 /* Bytes for chunk_states (n_chunks * H * (dk*dv + B*B) * sizeof(dtype)). */

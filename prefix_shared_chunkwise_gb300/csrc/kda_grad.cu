@@ -1,23 +1,27 @@
 // Gradient pass of bf16 packed-tree KDA on sm_103a (dk = dv = 128, chunk 64).
 //
-// Every (chunk, head) of every round is one independent item: with the chunk's start state
-// S (the forward's record), the state gradient dS' at its end (the state pass's record) and
-// T = (I + diag(beta) A)^-1 (the forward's record), all input gradients of the chunk follow
-// without any sequential dependence.  One CTA of 16 warps per SM walks the items in steps
-// of the grid size; every copy of the next item is issued before the current item's last
-// epilogue.  Notation (gamma the cumulative log-decay from the chunk start, m gamma at the
-// reference row, per key channel; t, s local rows):
+// Every (chunk, head) of every round is one independent item: with the chunk's R (the
+// forward's record), Q' (the state pass's record) and T = (I + diag(beta) A)^-1 (the
+// forward's record), all input gradients of the chunk follow without any sequential
+// dependence.  One CTA per SM walks the items in steps of the grid size: 16 compute warps
+// run the products and epilogues of one item while a 17th warp (the load warp) stages the
+// next item's tiles, each as soon as the product batch that last reads its buffer is done.
+// Notation (gamma the cumulative log-decay from the chunk start, m gamma at the reference
+// row, per key channel; t, s local rows):
 //   Kp = K e^{gamma-m}, Qp = scale Q e^{gamma-m}, Km = K e^{m-gamma}
 //   [A; P] = [Kp; Qp] Km^T, Tb = T diag(beta), R = S^T diag(e^m), Q' = dS'^T diag(e^{Gamma_L-m})
 //   Y^T = V^T - R Kp^T, U^T = Y^T Tb^T                              (the forward's U)
-//   dU^T = dO^T P + Q' Km^T,  dY^T = dU^T Tb,  dv = dY
-//   dP = lower(dO U^T),  dTb = dU Y^T,  dT = dTb diag(beta),  dM = -strict(T^T dT T^T)
-//   dA = diag(beta) dM,  dbeta = colsum(dTb .* T) + rowsum(dM .* A)
+//   dU^T = dO^T P + Q' Km^T,  Z = T^T dU,  dY = diag(beta) Z,  dv = dY
+//   dP = lower(dO U^T),  dM = -strict(Z U^T),  dA = diag(beta) dM
+//   dbeta = diag(Z Y^T) + rowsum(dM .* A)
 //   dQp^T = R^T dO^T + Km^T dP^T,  dKp^T = -R^T dY^T + Km^T dA^T,
 //   dKm^T = Q'^T U^T + Kp^T dA + Qp^T dP
 //   dq = scale dQp e^{gamma-m},  dk = dKp e^{gamma-m} + dKm e^{m-gamma}
 //   dgamma = dKp Kp + dQp Qp - dKm Km (the rounded operands the products used),
 //   dGamma_L = colsum(Q' .* R) + colsum(Km .* (Q'^T U^T)^T), dg = suffix sums of dgamma + dGamma_L.
+// Z collapses the inverse's gradient: with U = Tb Y, dT = dU Y^T diag(beta) and
+// T^T dT T^T = (T^T dU)(T diag(beta) Y)^T = Z U^T, so dM needs one product instead of two,
+// and colsum(dTb .* T) (dTb = dU Y^T) is the diagonal of Z Y^T.
 // (Page "HARTS ... 精读", section 4.3, KDA paragraph: gradients of replayed rows add into the
 // ancestor rows they copy; they go to the replay-gradient buffer, folded later in a fixed
 // order.)
@@ -32,31 +36,29 @@
 namespace harts {
 namespace {
 
-constexpr int D = 128, BC = 64, NT = 512;
+constexpr int D = 128, BC = 64, NC = 512, NT = NC + 128;    // 16 compute warps + 4 load warps
 constexpr int64_t kRecBytes = (D * D + BC * BC) * 2;
 
 namespace g2 {
-constexpr uint32_t RR = 0;          // [128 dv][128 dk] S^T record -> R (atoms 16 KB)
-constexpr uint32_t QQ = 32768;      // [128 dv][128 dk] dS'^T record -> Q'
+constexpr uint32_t RR = 0;          // [128 dv][128 dk] R record (atoms 16 KB)
+constexpr uint32_t QQ = 32768;      // [128 dv][128 dk] Q' record -> Z^T [128 dv][64 t] in its first atom
 constexpr uint32_t KQ = 65536;      // [128][128]: raw k -> Kp (rows 0-63), raw q -> Qp (64-127)
 constexpr uint32_t KM = 98304;      // [64][128] (atoms 8 KB): Km
 constexpr uint32_t VV = 114688;     // raw v [64][128] (atoms 8 KB) -> U^T [128][64]
 constexpr uint32_t DO = 131072;     // dO [64][128] (atoms 8 KB)
 constexpr uint32_t TT = 147456;     // T [64][64]
 constexpr uint32_t TB = 155648;     // Tb [64][64]    } TB..PT: raw g of the next item
-constexpr uint32_t PT = 163840;     // P -> dT [64][64] }
-constexpr uint32_t YT = 172032;     // Y^T [128][64] -> dv staging [64 t][128 dv] -> dq staging
+constexpr uint32_t PT = 163840;     // P [64][64]     }
+constexpr uint32_t YT = 172032;     // Y^T [128][64] -> dq staging [64 t][128]
 constexpr uint32_t DU = 188416;     // dU^T [128][64] -> -dY^T -> dk staging
 constexpr uint32_t DP = 204800;     // dP [64][64]   } DP..WA: dg staging
-constexpr uint32_t WA = 212992;     // W -> dA [64][64] }
+constexpr uint32_t WA = 212992;     // dA [64][64]   }
 constexpr uint32_t VQS = 221184;    // fp32 [4][128] partial sums (several uses)
 constexpr uint32_t VMR = VQS + 2048;
 constexpr uint32_t VM2 = VMR + 512;       // m log2(e)
-constexpr uint32_t VEM = VM2 + 512;       // e^m
-constexpr uint32_t VEG = VEM + 512;       // e^{Gamma_L - m}
-constexpr uint32_t VBETA = VEG + 512;     // fp32 [64]
-constexpr uint32_t VDB = VBETA + 256;     // fp32 [4][64] dbeta partials
-constexpr uint32_t VDGL = VDB + 1024;     // fp32 [128] dGamma_L
+constexpr uint32_t VBETA = VM2 + 512;     // fp32 [64]
+constexpr uint32_t VDB = VBETA + 256;     // fp32 [64] dbeta
+constexpr uint32_t VDGL = VDB + 256;      // fp32 [128] dGamma_L
 constexpr uint32_t END = VDGL + 512;
 constexpr uint32_t bytes = END + 1024;
 }  // namespace g2
@@ -67,33 +69,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 constexpr float kLog2e = 1.4426950408889634f;
-
-__device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(tc::smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" :: "r"(tc::smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) { tc::tmem_ld16(taddr, r); }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&r)[16]) {
-    const uint32_t *u = reinterpret_cast<const uint32_t *>(r);
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-                 :: "r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
-                    "r"(u[7]), "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]),
-                    "r"(u[15]) : "memory");
-}
-__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&u)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                 :: "r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
-                    "r"(u[7]) : "memory");
-}
-__device__ __forceinline__ void tmem_ld8u(uint32_t taddr, uint32_t (&u)[8]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
-                 : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 
 // TMEM loads issued back to back and waited for once.  The wait names the loaded registers
 // ("+r"), so no use of them can be scheduled above it.
@@ -111,10 +86,6 @@ __device__ __forceinline__ void tld8(uint32_t taddr, uint32_t (&u)[8]) {
 }
 #define HARTS_R16(a) "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), \
     "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15])
-__device__ __forceinline__ void twait(float (&a)[16]) {
-    uint32_t *x = reinterpret_cast<uint32_t *>(a);
-    asm volatile("tcgen05.wait::ld.sync.aligned;" : HARTS_R16(x) :: "memory");
-}
 __device__ __forceinline__ void twait(float (&a)[16], float (&b)[16]) {
     uint32_t *x = reinterpret_cast<uint32_t *>(a), *y = reinterpret_cast<uint32_t *>(b);
     asm volatile("tcgen05.wait::ld.sync.aligned;" : HARTS_R16(x), HARTS_R16(y) :: "memory");
@@ -124,16 +95,33 @@ __device__ __forceinline__ void twait(float (&a)[16], float (&b)[16], float (&c)
              *z = reinterpret_cast<uint32_t *>(c);
     asm volatile("tcgen05.wait::ld.sync.aligned;" : HARTS_R16(x), HARTS_R16(y), HARTS_R16(z) :: "memory");
 }
-__device__ __forceinline__ void twait(float (&a)[16], float (&b)[16], float (&c)[16], float (&d)[16]) {
+__device__ __forceinline__ void tmem_st8f(uint32_t taddr, const float (&r)[8]) {
+    const uint32_t *u = reinterpret_cast<const uint32_t *>(r);
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
+                    "r"(u[7]) : "memory");
+}
+__device__ __forceinline__ void tmem_st4u(uint32_t taddr, const uint32_t (&u)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
+                 :: "r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]) : "memory");
+}
+__device__ __forceinline__ void tld8f(uint32_t taddr, float (&r)[8]) { tld8(taddr, reinterpret_cast<uint32_t (&)[8]>(r)); }
+__device__ __forceinline__ void tld4(uint32_t taddr, uint32_t (&u)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]) : "r"(taddr));
+}
+#define HARTS_R8(a) "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7])
+#define HARTS_R4(a) "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3])
+// One wait for four 8-column and two 4-column loads (the wait names all their registers).
+__device__ __forceinline__ void twait8(float (&a)[8], float (&b)[8], float (&c)[8], float (&d)[8], uint32_t (&e)[4],
+                                       uint32_t (&g)[4]) {
     uint32_t *x = reinterpret_cast<uint32_t *>(a), *y = reinterpret_cast<uint32_t *>(b),
              *z = reinterpret_cast<uint32_t *>(c), *w = reinterpret_cast<uint32_t *>(d);
-    asm volatile("tcgen05.wait::ld.sync.aligned;" : HARTS_R16(x), HARTS_R16(y), HARTS_R16(z), HARTS_R16(w) :: "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : HARTS_R8(x), HARTS_R8(y), HARTS_R8(z), HARTS_R8(w), HARTS_R4(e), HARTS_R4(g)
+                 :: "memory");
 }
-// Orders later uses of already-waited registers after the preceding wait.
-__device__ __forceinline__ void tkeep(uint32_t (&a)[8], uint32_t (&b)[8]) {
-    asm volatile("" : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
-                      "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]));
-}
+#undef HARTS_R8
+#undef HARTS_R4
 #undef HARTS_R16
 
 __device__ __forceinline__ float bf(const uint8_t *p) {
@@ -155,9 +143,9 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 
 struct GradMaps2 {
     RowMaps q, k, g, v, dout;
-    CUtensorMap rec_s;              // records as [rows of 256 B], boxes of 64 x 128 (a chunk's S^T)
+    CUtensorMap rec_s;              // records as [rows of 256 B], boxes of 64 x 128 (a chunk's R)
     CUtensorMap rec_t;              // records as [rows of 128 B], boxes of 64 x 64 (a chunk's T)
-    CUtensorMap dch;                // dS'^T records as [rows of 256 B], boxes of 64 x 128
+    CUtensorMap dch;                // Q' records as [rows of 256 B], boxes of 64 x 128
 };
 
 struct Item {
@@ -178,18 +166,39 @@ __device__ __forceinline__ Item item_of(const PlanDev &pd, int32_t chunk_begin, 
     return it;
 }
 
-__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t phase, int *s_fail) {
-    if (threadIdx.x == 0 && !tc::mbar_wait(bar, phase)) *s_fail = 1;
-    __syncthreads();
-    tc::fence_after_sync();
-    return *reinterpret_cast<volatile int *>(s_fail) == 0;
+constexpr long long kWaitCycles = 4000000000LL;
+
+// The compute warps meet at named barrier 1 (the load warp never joins it).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" :: "n"(NC) : "memory"); }
+
+// The same meeting, returning the OR of `v` over the compute warps (a decision all of them take).
+__device__ __forceinline__ bool csync_or(bool v) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 1, %2, q;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r) : "r"(static_cast<uint32_t>(v)), "n"(NC) : "memory");
+    return r != 0;
 }
 
-__device__ __forceinline__ void sync_mma() {
+__device__ __forceinline__ void csync_mma() {
     tc::fence_smem_to_async();
     tc::fence_before_sync();
-    __syncthreads();
+    csync();
     tc::fence_after_sync();
+}
+
+// Bounded poll of one barrier phase; gives up (and records the failure) when it runs out or
+// when the other side has already failed.
+__device__ __forceinline__ bool poll_bar(uint64_t *bar, uint32_t phase, int *s_fail) {
+    if (tc::mbar_try(bar, phase)) return true;
+    const long long t0 = clock64();
+    while (!tc::mbar_try(bar, phase)) {
+        if (*reinterpret_cast<volatile int *>(s_fail) || clock64() - t0 > kWaitCycles) {
+            *reinterpret_cast<volatile int *>(s_fail) = 1;
+            return false;
+        }
+    }
+    return true;
 }
 
 // Offset of element (row, col) in a [rows][64]-column SW128 atom (bf16).
@@ -202,22 +211,24 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
     using namespace g2;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    // mbarriers: 0-5 product batches; 6 q, 7 k, 8 g, 9 v, 10 dO, 11 T, 12 S^T, 13 dS'^T
+    // mbarriers: 0-4 product batches B1, B2, B3, B4, B6; 6 q, 7 k, 8 g, 9 v, 10 dO, 11 T, 12 R, 13 Q'
     __shared__ uint64_t bars[14];
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
-    __shared__ int s_rows[64];
+    __shared__ int s_rows[4][64];                   // each load warp's row table
+    __shared__ uint16_t s_braw[2][64];              // raw beta of an item's rows, by item parity
+    // an item's indices, by item number mod 4: the load warp fills item n + 1's slot while the
+    // compute warps still read item n - 1's
+    __shared__ Item s_items[4];
     const FwdParams &f = p.f;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lq = warp & 3, cg = warp >> 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lq = warp & 3, cg = (warp >> 2) & 3;
     const int H = f.H;
     const int W3 = 3 * D + 1;
     const int jv = lq * 32 + lane;                  // TMEM lane of this thread
     const uint32_t lane_off = static_cast<uint32_t>(lq * 32) << 16;
     float *vqs = reinterpret_cast<float *>(sm + VQS), *vmr = reinterpret_cast<float *>(sm + VMR);
-    float *vm2 = reinterpret_cast<float *>(sm + VM2), *vem = reinterpret_cast<float *>(sm + VEM);
-    float *veg = reinterpret_cast<float *>(sm + VEG), *vbeta = reinterpret_cast<float *>(sm + VBETA);
+    float *vm2 = reinterpret_cast<float *>(sm + VM2), *vbeta = reinterpret_cast<float *>(sm + VBETA);
     float *vdb = reinterpret_cast<float *>(sm + VDB), *vdgl = reinterpret_cast<float *>(sm + VDGL);
-    const uint16_t *beta = static_cast<const uint16_t *>(f.beta);
 
     if (tid == 0) {
         for (int i = 0; i < 14; ++i) tc::mbar_init(&bars[i], 1);
@@ -230,541 +241,511 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
     const uint32_t tm = s_tmem;
     const uint32_t tAP = tm, tX = tm + 64, tDU = tm + 128, tDY = tm + 192, tDT = tm + 256, tKM = tm + 320,
                    tGM = tm + 384, tPK = tm + 448;
-
     int armed[14] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-    auto rows_of = [&](const Item &it) -> uint16_t {
-        if (tid >= 64) return 0;
-        const int64_t row = local_row(pd, it.seq, it.rho, it.L, it.c0 + tid);
-        s_rows[tid] = static_cast<int>(row);
-        return row >= 0 ? beta[row * H + it.h] : static_cast<uint16_t>(0);
-    };
-    // which: 0 q, 1 k, 2 g, 3 v, 4 dO, 5 T, 6 S^T record, 7 dS'^T record
-    auto stage = [&](int which, const Item &it, bool defer = false) {
-        ++armed[6 + which];
-        uint64_t *bar = &bars[6 + which];
-        const int t_own = max(0, it.rho - it.c0), t_end = it.nv;
-        const int32_t own0 = it.row0 + it.c0 - it.rho;
-        const int64_t rid = static_cast<int64_t>(it.g) * H + it.h;
-        switch (which) {
-        case 0: stage_chunk_rows<NT>(f.q, maps.q, s_rows, it.h, H, t_own, t_end, own0, 0, sm + KQ + 8192, sm + KQ + 24576, bar, defer); break;
-        case 1: stage_chunk_rows<NT>(f.k, maps.k, s_rows, it.h, H, t_own, t_end, own0, 0, sm + KQ, sm + KQ + 16384, bar, defer); break;
-        case 2: stage_chunk_rows<NT>(f.g, maps.g, s_rows, it.h, H, t_own, t_end, own0, 0, sm + TB, sm + TB + 8192, bar); break;
-        case 3: stage_chunk_rows<NT>(f.v, maps.v, s_rows, it.h, H, t_own, t_end, own0, 0, sm + VV, sm + VV + 8192, bar); break;
-        case 4: stage_chunk_rows<NT>(p.d_o, maps.dout, s_rows, it.h, H, t_own, t_end, own0, t_own, sm + DO, sm + DO + 8192,
-                                     bar, defer); break;
-        case 5:
-            if (tid == 0) {
-                tc::mbar_expect_tx(bar, 8192);
-                tc::tma_load_2d(sm + TT, &maps.rec_t, 0, static_cast<int>(rid * (kRecBytes / 128) + 2 * D), bar);
-            }
-            break;
-        case 6:
-            if (tid == 0) {
-                tc::mbar_expect_tx(bar, 32768);
-                tc::tma_load_2d(sm + RR, &maps.rec_s, 0, static_cast<int>(rid * (kRecBytes / 256)), bar);
-                tc::tma_load_2d(sm + RR + 16384, &maps.rec_s, 64, static_cast<int>(rid * (kRecBytes / 256)), bar);
-            }
-            break;
-        default:
-            if (tid == 0) {
-                tc::mbar_expect_tx(bar, 32768);
-                tc::tma_load_2d(sm + QQ, &maps.dch, 0, static_cast<int>(rid * D), bar);
-                tc::tma_load_2d(sm + QQ + 16384, &maps.dch, 64, static_cast<int>(rid * D), bar);
-            }
-            break;
-        }
-    };
-    auto wait_load = [&](int which, uint32_t ph) -> bool {
-        if (tid == 0 && !tc::mbar_wait(&bars[6 + which], ph)) s_fail = 1;
-        return true;
-    };
-
-    int32_t item = blockIdx.x;
-    Item cur{};
-    uint16_t braw = 0;
-    if (item < n_items) {
-        cur = item_of(pd, chunk_begin, H, item);
-        braw = rows_of(cur);
-        __syncthreads();
-        for (int w = 0; w < 8; ++w) stage(w, cur);
-    }
     int32_t cur_seq = 0, cur_h = 0;
-    uint32_t n_done = 0;
-    for (; item < n_items; item += gridDim.x, ++n_done) {
-        const uint32_t ph = n_done & 1;
-        const Item I = cur;
-        cur_seq = I.seq; cur_h = I.h;
-        const int t_own = max(0, I.rho - I.c0), t_end = I.nv;
-        const int mid = (I.nv - 1) / 2;
-        const int32_t nxt = item + gridDim.x;
-        Item nx{};
-        if (nxt < n_items) nx = item_of(pd, chunk_begin, H, nxt);
 
-        // ---- pass A: sums of g over row quarters (g of this item sits in TB..PT) ---------------
-        wait_load(2, ph);
-        __syncthreads();
-        if (s_fail) break;
-        {
-            const int c = jv, q4 = cg;
-            float s_ = 0.f, mr = 0.f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int t = q4 * 16 + u;
-                s_ += bf(sm + TB + (c >> 6) * 8192 + sw64(t, c & 63));
-                if (t == mid) mr = s_;
+    if (warp >= NC / 32) {
+        // ================= load warps: every copy of the next item, issued as its buffer frees ====
+        // Load warp 0: g, T and the two records (and the item's indices and beta for the compute
+        // warps); 1: dO and v; 2: q; 3: k.  Each walks the items on its own, so that one warp's
+        // row gathers (replay rows, a sequence's last partial chunk) never hold up another's copies.
+        const int lw = warp - NC / 32;
+        int *rows = s_rows[lw];
+        const uint16_t *beta = static_cast<const uint16_t *>(f.beta);
+        // row table of item number `n` (`it`); load warp 0 also publishes its indices and beta
+        auto rows_of = [&](const Item &it, uint32_t n) {
+            if (lw == 0 && lane == 0) s_items[n & 3] = it;
+            for (int t = lane; t < 64; t += 32) {
+                const int64_t row = local_row(pd, it.seq, it.rho, it.L, it.c0 + t);
+                rows[t] = static_cast<int>(row);
+                if (lw == 0) s_braw[n & 1][t] = row >= 0 ? beta[row * H + it.h] : static_cast<uint16_t>(0);
             }
-            vqs[q4 * 128 + c] = s_;
-            if (q4 == (mid >> 4)) vmr[c] = mr;
-            if (tid < 64) vbeta[tid] = __bfloat162float(__ushort_as_bfloat16(braw));
-        }
-        __syncthreads();
-        if (tid < 128) {
-            const int c = tid, qm = mid >> 4;
-            float m = vmr[c], gl = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float x = vqs[q * 128 + c];
-                gl += x;
-                if (q < qm) m += x;
-            }
-            if (-m > kMaxExpArg || m - gl > kMaxExpArg) dev_error(pd, kDevErrDecayRange, I.seq, I.c0);
-            vm2[c] = m * kLog2e;
-            vem[c] = ex2(m * kLog2e);
-            veg[c] = ex2((gl - m) * kLog2e);
-        }
-        wait_load(0, ph);
-        wait_load(1, ph);
-        __syncthreads();
-        if (s_fail) break;
-        // ---- pass B: Kp, Qp in place, Km; gamma and the bf16 Kp, Qp (pairs) into TMEM ----------
-        {
-            const int c = jv, q4 = cg;
-            float gam = 0.f;
-#pragma unroll
-            for (int q = 0; q < 3; ++q) gam += q < q4 ? vqs[q * 128 + c] : 0.f;
-            const float m2 = vm2[c], sc = f.scale;
-            float g2v[16];
-            uint32_t kpk[8], qpk[8];
-#pragma unroll
-            for (int u = 0; u < 16; u += 2) {
-                float kp2[2], qp2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = q4 * 16 + u + e;
-                    const uint32_t o = (c >> 6) * 16384 + sw64(t, c & 63), oq = (c >> 6) * 16384 + sw64(64 + t, c & 63);
-                    gam += bf(sm + TB + (c >> 6) * 8192 + sw64(t, c & 63));
-                    const float kk = bf(sm + KQ + o), qq = bf(sm + KQ + oq);
-                    const float x = fmaf(gam, kLog2e, -m2);
-                    const float e1 = ex2(x), e2 = ex2(-x);
-                    const __nv_bfloat16 kpb = __float2bfloat16_rn(kk * e1), qpb = __float2bfloat16_rn(sc * qq * e1);
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + KQ + o) = kpb;
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + KQ + oq) = qpb;
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + KM + (c >> 6) * 8192 + sw64(t, c & 63)) =
-                        __float2bfloat16_rn(kk * e2);
-                    g2v[u + e] = gam * kLog2e;
-                    kp2[e] = __bfloat162float(kpb);
-                    qp2[e] = __bfloat162float(qpb);
+            __syncwarp();
+        };
+        // which: 0 q, 1 k, 2 g, 3 v, 4 dO, 5 T, 6 R record, 7 Q' record
+        auto stage = [&](int which, const Item &it) {
+            ++armed[6 + which];
+            uint64_t *bar = &bars[6 + which];
+            const int t_own = max(0, it.rho - it.c0), t_end = it.nv;
+            const int32_t own0 = it.row0 + it.c0 - it.rho;
+            const int64_t rid = static_cast<int64_t>(it.g) * H + it.h;
+            switch (which) {
+            case 0: stage_chunk_rows_warp(f.q, maps.q, rows, it.h, H, t_own, t_end, own0, 0, sm + KQ + 8192, sm + KQ + 24576, bar); break;
+            case 1: stage_chunk_rows_warp(f.k, maps.k, rows, it.h, H, t_own, t_end, own0, 0, sm + KQ, sm + KQ + 16384, bar); break;
+            case 2: stage_chunk_rows_warp(f.g, maps.g, rows, it.h, H, t_own, t_end, own0, 0, sm + TB, sm + TB + 8192, bar); break;
+            case 3: stage_chunk_rows_warp(f.v, maps.v, rows, it.h, H, t_own, t_end, own0, 0, sm + VV, sm + VV + 8192, bar); break;
+            case 4: stage_chunk_rows_warp(p.d_o, maps.dout, rows, it.h, H, t_own, t_end, own0, t_own, sm + DO,
+                                          sm + DO + 8192, bar); break;
+            case 5:
+                if (lane == 0) {
+                    tc::mbar_expect_tx(bar, 8192);
+                    tc::tma_load_2d(sm + TT, &maps.rec_t, 0, static_cast<int>(rid * (kRecBytes / 128) + 2 * D), bar);
                 }
-                kpk[u / 2] = tc::pack_bf16(kp2[0], kp2[1]);
-                qpk[u / 2] = tc::pack_bf16(qp2[0], qp2[1]);
+                break;
+            case 6:
+                if (lane == 0) {
+                    tc::mbar_expect_tx(bar, 32768);
+                    tc::tma_load_2d(sm + RR, &maps.rec_s, 0, static_cast<int>(rid * (kRecBytes / 256)), bar);
+                    tc::tma_load_2d(sm + RR + 16384, &maps.rec_s, 64, static_cast<int>(rid * (kRecBytes / 256)), bar);
+                }
+                break;
+            default:
+                if (lane == 0) {
+                    tc::mbar_expect_tx(bar, 32768);
+                    tc::tma_load_2d(sm + QQ, &maps.dch, 0, static_cast<int>(rid * D), bar);
+                    tc::tma_load_2d(sm + QQ + 16384, &maps.dch, 64, static_cast<int>(rid * D), bar);
+                }
+                break;
             }
-            tmem_st16(tGM + lane_off + q4 * 16, g2v);
-            tmem_st8u(tPK + lane_off + q4 * 8, kpk);
-            tmem_st8u(tPK + lane_off + 32 + q4 * 8, qpk);
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        };
+        // lane 0 waits for a product batch of the compute warps (its operands are then free)
+        auto wait_free = [&](int b, uint32_t ph) -> bool {
+            int ok = 1;
+            if (lane == 0) ok = poll_bar(&bars[b], ph, &s_fail) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();
+            return ok != 0;
+        };
+        int32_t item = blockIdx.x;
+        if (item < n_items) {
+            const Item it = item_of(pd, chunk_begin, H, item);
+            rows_of(it, 0u);
+            if (lw == 0) { stage(2, it); stage(5, it); stage(6, it); stage(7, it); }
+            else if (lw == 1) { stage(4, it); stage(3, it); }
+            else stage(lw == 2 ? 0 : 1, it);
         }
-        // ---- R = S^T diag(e^m), Q' = dS'^T diag(e^{Gamma_L - m}) in place; Tb = T diag(beta) --------
-        wait_load(5, ph);
-        wait_load(6, ph);
-        wait_load(7, ph);
-        __syncthreads();
-        if (s_fail) break;
-        {
-            // warp w: logical 8-column chunk w (atom w / 8) of every row; lane: rows lane + 32 i.
-            // Scales R and Q' in place and sums R .* Q' over the rows (dGamma_L's first term).
-            const int jl = warp & 7, atom = warp >> 3, col0 = atom * 64 + jl * 8;
-            const float4 ea = *reinterpret_cast<const float4 *>(vem + col0), eb = *reinterpret_cast<const float4 *>(vem + col0 + 4);
-            const float4 ga = *reinterpret_cast<const float4 *>(veg + col0), gb = *reinterpret_cast<const float4 *>(veg + col0 + 4);
-            const float es[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
-            const float gs[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-            float dot[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = lane + 32 * i;
-                const uint32_t off = atom * 16384 + r * 128 + ((jl ^ (r & 7)) << 4);
-                uint4 *pr = reinterpret_cast<uint4 *>(sm + RR + off), *pq = reinterpret_cast<uint4 *>(sm + QQ + off);
-                float vr[8], vq[8];
-                unpack8(*pr, vr);
-                unpack8(*pq, vq);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) { vr[k] *= es[k]; vq[k] *= gs[k]; }
-                const uint4 wr = pack8(vr), wq = pack8(vq);
-                *pr = wr;
-                *pq = wq;
-                unpack8(wr, vr);        // the rounded values the products will use
-                unpack8(wq, vq);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) dot[k] += vr[k] * vq[k];
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-#pragma unroll
-                for (int sh = 16; sh >= 1; sh >>= 1) dot[k] += __shfl_xor_sync(0xffffffffu, dot[k], sh);
-            }
-            if (lane == 0) {
-                *reinterpret_cast<float4 *>(vdgl + col0) = make_float4(dot[0], dot[1], dot[2], dot[3]);
-                *reinterpret_cast<float4 *>(vdgl + col0 + 4) = make_float4(dot[4], dot[5], dot[6], dot[7]);
+        for (uint32_t n = 0; item < n_items; item += gridDim.x, ++n) {
+            const int32_t nxt = item + gridDim.x;
+            if (nxt >= n_items) break;
+            const uint32_t ph = n & 1;
+            const Item nx = item_of(pd, chunk_begin, H, nxt);
+            rows_of(nx, n + 1);
+            if (lw == 0) {
+                if (!wait_free(1, ph)) break;                // B2 done: Tb and P (TB..PT) are free
+                stage(2, nx);
+                if (!wait_free(2, ph)) break;                // B3 done: T is free
+                stage(5, nx);
+                if (!wait_free(3, ph)) break;                // B4 done: R and Q' (Z^T) are free
+                stage(6, nx);
+                stage(7, nx);
+            } else if (lw == 1) {
+                if (!wait_free(2, ph)) break;                // B3 done: dO is free
+                stage(4, nx);
+                if (!wait_free(3, ph)) break;                // B4 done: U^T (over v) is free
+                stage(3, nx);
+            } else {
+                if (!wait_free(4, ph)) break;                // B6 done: Kp, Qp are free
+                stage(lw == 2 ? 0 : 1, nx);
             }
         }
-        {
-            const int t = tid >> 3, j = tid & 7;              // Tb: row t, 16-byte chunk j
-            const uint4 w = *reinterpret_cast<const uint4 *>(sm + TT + t * 128 + (j << 4));
-            const int col0 = (j ^ (t & 7)) << 3;
-            float v[8];
-            unpack8(w, v);
+        // every copy issued lands before shared memory is released
+        tc::cp_async_wait_all();
+        __syncwarp();
+        if (lane == 0 && *reinterpret_cast<volatile int *>(&s_fail))
+            for (int i = 6; i < 14; ++i)
+                if (armed[i] > 0 && !tc::mbar_wait(&bars[i], (armed[i] - 1) & 1, 200000000LL))
+                    dev_error(pd, kDevErrTimeout, -1, i);
+    } else {
+        // ================= compute warps ===================================================
+        int32_t item = blockIdx.x;
+        uint32_t ph = 0;
+        bool tfail = false;                             // thread 0: a wait of its own ran out
+        auto poll = [&](int b) {
+            if (tid == 0 && !tfail) tfail = !poll_bar(&bars[b], ph, &s_fail);
+        };
+        // the compute warps meet; all of them stop when thread 0's waits failed or the load
+        // warp recorded a failure
+        auto meet = [&]() -> bool {
+            const bool stop = csync_or(tid == 0 && (tfail || *reinterpret_cast<volatile int *>(&s_fail) != 0));
+            tc::fence_after_sync();
+            if (stop && tid == 0) *reinterpret_cast<volatile int *>(&s_fail) = 1;
+            return !stop;
+        };
+        for (uint32_t n_done = 0; item < n_items; item += gridDim.x, ++n_done) {
+            ph = n_done & 1;
+            // ---- pass A: sums of g over row quarters (g of this item sits in TB..PT) -----------
+            poll(8);
+            if (!meet()) break;
+            const Item &I = s_items[n_done & 3];            // written by the load warp before g
+            cur_seq = I.seq; cur_h = I.h;
+            const int t_own = max(0, I.rho - I.c0), t_end = I.nv;
+            const int mid = (I.nv - 1) / 2;
+            {
+                const int c = jv, q4 = cg;
+                float s_ = 0.f, mr = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] *= vbeta[col0 + i];
-            *reinterpret_cast<uint4 *>(sm + TB + t * 128 + (j << 4)) = pack8(v);
-        }
-        sync_mma();
-        // ---- B1: [A; P] = [Kp; Qp] Km^T;  X = R Kp^T;  dU^T = Q' Km^T ---------------------------
-        if (tid == 0) {
-            const uint32_t id = tc::idesc_bf16(128, 64);
-            tc::mma_tile(tAP, tc::smem_addr(sm + KQ), 16384, tc::smem_addr(sm + KM), 8192, 128, id, false);
-            tc::mma_tile(tX, tc::smem_addr(sm + RR), 16384, tc::smem_addr(sm + KQ), 16384, 128, id, false);
-            tc::mma_tile(tDU, tc::smem_addr(sm + QQ), 16384, tc::smem_addr(sm + KM), 8192, 128, id, false);
-            tc::mma_commit(&bars[0]);
-        }
-        ++armed[0];
-        wait_load(3, ph);                                   // v, read below
-        if (!wait_mma(&bars[0], ph, &s_fail)) break;
-        // ---- E1: P -> PT (lower with the diagonal); Y^T = V^T - X -> YT ----------------------------
-        {
-            float r[16], pv[16];
-            tld16(tAP + lane_off + cg * 16, pv);
-            tld16(tX + lane_off + cg * 16, r);
-            twait(pv, r);
-            if (lq >= 2) {
-                const int t = jv - 64;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) pv[j] = (cg * 16 + j <= t) ? pv[j] : 0.f;
-                tc::st_sw128_8(sm + PT, 64, t, cg * 16, pv);
-                tc::st_sw128_8(sm + PT, 64, t, cg * 16 + 8, pv + 8);
+                for (int u = 0; u < 16; ++u) {
+                    const int t = q4 * 16 + u;
+                    s_ += bf(sm + TB + (c >> 6) * 8192 + sw64(t, c & 63));
+                    if (t == mid) mr = s_;
+                }
+                vqs[q4 * 128 + c] = s_;
+                if (q4 == (mid >> 4)) vmr[c] = mr;
+                if (tid < 64) vbeta[tid] = __bfloat162float(__ushort_as_bfloat16(s_braw[ph][tid]));
             }
-            const int dv = jv;
+            csync();
+            if (tid < 128) {
+                const int c = tid, qm = mid >> 4;
+                float m = vmr[c], gl = 0.f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = cg * 16 + j;
-                r[j] = bf(sm + VV + (dv >> 6) * 8192 + sw64(t, dv & 63)) - r[j];
+                for (int q = 0; q < 4; ++q) {
+                    const float x = vqs[q * 128 + c];
+                    gl += x;
+                    if (q < qm) m += x;
+                }
+                if (-m > kMaxExpArg || m - gl > kMaxExpArg) dev_error(pd, kDevErrDecayRange, I.seq, I.c0);
+                vm2[c] = m * kLog2e;
             }
-            tc::st_sw128_8(sm + YT, 128, dv, cg * 16, r);
-            tc::st_sw128_8(sm + YT, 128, dv, cg * 16 + 8, r + 8);
-        }
-        sync_mma();
-        // ---- B2: U^T = Y^T Tb^T;  dU^T += dO^T P -----------------------------------------------------
-        wait_load(4, ph);
-        __syncthreads();
-        if (s_fail) break;
-        if (tid == 0) {
-            tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + YT), 16384, false}, tc::Opnd{tc::smem_addr(sm + TB), 8192, false},
-                       128, 64, 64, false);
-            tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + DO), 8192, true}, tc::Opnd{tc::smem_addr(sm + PT), 8192, true},
-                       128, 64, 64, true);
-            tc::mma_commit(&bars[1]);
-        }
-        ++armed[1];
-        if (!wait_mma(&bars[1], ph, &s_fail)) break;
-        // ---- E2: U^T -> VV (raw v is consumed), dU^T -> DU -------------------------------------------
-        {
-            float r[16], r2[16];
-            tld16(tX + lane_off + cg * 16, r);
-            tld16(tDU + lane_off + cg * 16, r2);
-            twait(r, r2);
-            tc::st_sw128_8(sm + VV, 128, jv, cg * 16, r);
-            tc::st_sw128_8(sm + VV, 128, jv, cg * 16 + 8, r + 8);
-            tc::st_sw128_8(sm + DU, 128, jv, cg * 16, r2);
-            tc::st_sw128_8(sm + DU, 128, jv, cg * 16 + 8, r2 + 8);
-        }
-        sync_mma();
-        // ---- B3: dY^T = dU^T Tb;  dP = dO U^T (M = 64);  dTb = dU Y^T (M = 64);  Km' = Q'^T U^T -------
-        if (tid == 0) {
-            tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + DU), 16384, false}, tc::Opnd{tc::smem_addr(sm + TB), 8192, true},
-                       128, 64, 64, false);
-            tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + DO), 8192, false}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
-                       64, 64, 128, false);
-            tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + DU), 16384, true}, tc::Opnd{tc::smem_addr(sm + YT), 16384, true},
-                       64, 64, 128, false);
-            tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + QQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
-                       128, 64, 128, false);
-            tc::mma_commit(&bars[2]);
-        }
-        ++armed[2];
-        if (!wait_mma(&bars[2], ph, &s_fail)) break;
-        // Q' and V / U^T are consumed: the next item's dS'^T record and v.  Its row table (and
-        // beta) are formed first; the staging calls after the barrier read them.
-        if (nxt < n_items) braw = rows_of(nx);
-        __syncthreads();
-        if (nxt < n_items) {
-            stage(7, nx);
-            stage(3, nx);
-        }
-        // ---- E3a: dT -> PT and dbeta's Tb part (from dTb), then W = dT T^T is issued at once ------------
-        {
-            float bq[16], dbs[16];
-            tmem_ld16(tDT + lane_off + cg * 16, bq);       // M = 64: row 16 lq + lane in lanes 0-15
-            if (lane < 16) {
-                const int t = 16 * lq + lane;
+            poll(6);
+            poll(7);
+            if (!meet()) break;
+            // ---- pass B: Kp, Qp in place, Km; gamma and the bf16 Kp, Qp (pairs) into TMEM ------
+            {
+                const int c = jv, q4 = cg;
+                float gam = 0.f;
+#pragma unroll
+                for (int q = 0; q < 3; ++q) gam += q < q4 ? vqs[q * 128 + c] : 0.f;
+                const float m2 = vm2[c], sc = f.scale;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float g2v[8];
+                    uint32_t kpk[4], qpk[4];
+#pragma unroll
+                    for (int u = 0; u < 8; u += 2) {
+                        float kp2[2], qp2[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int t = q4 * 16 + hh * 8 + u + e;
+                            const uint32_t o = (c >> 6) * 16384 + sw64(t, c & 63), oq = (c >> 6) * 16384 + sw64(64 + t, c & 63);
+                            gam += bf(sm + TB + (c >> 6) * 8192 + sw64(t, c & 63));
+                            const float kk = bf(sm + KQ + o), qq = bf(sm + KQ + oq);
+                            const float x = fmaf(gam, kLog2e, -m2);
+                            const float e1 = ex2(x), e2 = ex2(-x);
+                            const __nv_bfloat16 kpb = __float2bfloat16_rn(kk * e1), qpb = __float2bfloat16_rn(sc * qq * e1);
+                            *reinterpret_cast<__nv_bfloat16 *>(sm + KQ + o) = kpb;
+                            *reinterpret_cast<__nv_bfloat16 *>(sm + KQ + oq) = qpb;
+                            *reinterpret_cast<__nv_bfloat16 *>(sm + KM + (c >> 6) * 8192 + sw64(t, c & 63)) =
+                                __float2bfloat16_rn(kk * e2);
+                            g2v[u + e] = gam * kLog2e;
+                            kp2[e] = __bfloat162float(kpb);
+                            qp2[e] = __bfloat162float(qpb);
+                        }
+                        kpk[u / 2] = tc::pack_bf16(kp2[0], kp2[1]);
+                        qpk[u / 2] = tc::pack_bf16(qp2[0], qp2[1]);
+                    }
+                    tmem_st8f(tGM + lane_off + q4 * 16 + hh * 8, g2v);
+                    tmem_st4u(tPK + lane_off + q4 * 8 + hh * 4, kpk);
+                    tmem_st4u(tPK + lane_off + 32 + q4 * 8 + hh * 4, qpk);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            // ---- colsum(Q' .* R) (dGamma_L's first term) from the records; Tb = T diag(beta) -----
+            poll(11);
+            poll(12);
+            poll(13);
+            if (!meet()) break;
+            {
+                // warp w: logical 8-column chunk w (atom w / 8) of every row; lane: rows lane + 32 i
+                const int jl = warp & 7, atom = warp >> 3, col0 = atom * 64 + jl * 8;
+                float dot[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = lane + 32 * i;
+                    const uint32_t off = atom * 16384 + r * 128 + ((jl ^ (r & 7)) << 4);
+                    float vr[8], vq[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(sm + RR + off), vr);
+                    unpack8(*reinterpret_cast<const uint4 *>(sm + QQ + off), vq);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) dot[k] += vr[k] * vq[k];
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+#pragma unroll
+                    for (int sh = 16; sh >= 1; sh >>= 1) dot[k] += __shfl_xor_sync(0xffffffffu, dot[k], sh);
+                }
+                if (lane == 0) {
+                    *reinterpret_cast<float4 *>(vdgl + col0) = make_float4(dot[0], dot[1], dot[2], dot[3]);
+                    *reinterpret_cast<float4 *>(vdgl + col0 + 4) = make_float4(dot[4], dot[5], dot[6], dot[7]);
+                }
+            }
+            {
+                const int t = tid >> 3, j = tid & 7;              // Tb: row t, 16-byte chunk j
+                const uint4 w = *reinterpret_cast<const uint4 *>(sm + TT + t * 128 + (j << 4));
+                const int col0 = (j ^ (t & 7)) << 3;
+                float v[8];
+                unpack8(w, v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] *= vbeta[col0 + i];
+                *reinterpret_cast<uint4 *>(sm + TB + t * 128 + (j << 4)) = pack8(v);
+            }
+            csync_mma();
+            // ---- B1: [A; P] = [Kp; Qp] Km^T;  X = R Kp^T;  dU^T = Q' Km^T -----------------------
+            if (tid == 0) {
+                const uint32_t id = tc::idesc_bf16(128, 64);
+                tc::mma_tile(tAP, tc::smem_addr(sm + KQ), 16384, tc::smem_addr(sm + KM), 8192, 128, id, false);
+                tc::mma_tile(tX, tc::smem_addr(sm + RR), 16384, tc::smem_addr(sm + KQ), 16384, 128, id, false);
+                tc::mma_tile(tDU, tc::smem_addr(sm + QQ), 16384, tc::smem_addr(sm + KM), 8192, 128, id, false);
+                tc::mma_commit(&bars[0]);
+            }
+            ++armed[0];
+            poll(9);                                            // v, read below
+            poll(0);
+            if (!meet()) break;
+            // ---- E1: P -> PT (lower with the diagonal); Y^T = V^T - X -> YT ------------------------
+            {
+                float r[16], pv[16];
+                tld16(tAP + lane_off + cg * 16, pv);
+                tld16(tX + lane_off + cg * 16, r);
+                twait(pv, r);
+                if (lq >= 2) {
+                    const int t = jv - 64;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) pv[j] = (cg * 16 + j <= t) ? pv[j] : 0.f;
+                    tc::st_sw128_8(sm + PT, 64, t, cg * 16, pv);
+                    tc::st_sw128_8(sm + PT, 64, t, cg * 16 + 8, pv + 8);
+                }
+                const int dv = jv;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int s = cg * 16 + j;
-                    dbs[j] = s <= t ? bq[j] * bf(sm + TT + sw64(t, s)) : 0.f;     // dTb .* T
-                    bq[j] = s < t ? bq[j] * vbeta[s] : 0.f;                       // dT
+                    const int t = cg * 16 + j;
+                    r[j] = bf(sm + VV + (dv >> 6) * 8192 + sw64(t, dv & 63)) - r[j];
                 }
-                tc::st_sw128_8(sm + PT, 64, t, cg * 16, bq);
-                tc::st_sw128_8(sm + PT, 64, t, cg * 16 + 8, bq + 8);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) dbs[j] = 0.f;
+                tc::st_sw128_8(sm + YT, 128, dv, cg * 16, r);
+                tc::st_sw128_8(sm + YT, 128, dv, cg * 16 + 8, r + 8);
             }
-            // column sums of dTb .* T over this quarter's 16 rows (lanes 0-15)
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float x = dbs[j];
-                x += __shfl_xor_sync(0xffffffffu, x, 8);
-                x += __shfl_xor_sync(0xffffffffu, x, 4);
-                x += __shfl_xor_sync(0xffffffffu, x, 2);
-                x += __shfl_xor_sync(0xffffffffu, x, 1);
-                if (lane == 0) vdb[lq * 64 + cg * 16 + j] = x;
+            poll(10);                                           // dO
+            tc::fence_smem_to_async();
+            tc::fence_before_sync();
+            if (!meet()) break;
+            // ---- B2: U^T = Y^T Tb^T;  dU^T += dO^T P -------------------------------------------------
+            if (tid == 0) {
+                tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + YT), 16384, false}, tc::Opnd{tc::smem_addr(sm + TB), 8192, false},
+                           128, 64, 64, false);
+                tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + DO), 8192, true}, tc::Opnd{tc::smem_addr(sm + PT), 8192, true},
+                           128, 64, 64, true);
+                tc::mma_commit(&bars[1]);
             }
-        }
-        sync_mma();
-        // ---- B4: W = dT T^T (M = 64) into the dTb columns -----------------------------------------------
-        if (tid == 0) {
-            tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + PT), 8192, false}, tc::Opnd{tc::smem_addr(sm + TT), 8192, false},
-                       64, 64, 64, false);
-            tc::mma_commit(&bars[3]);
-        }
-        ++armed[3];
-        // ---- E3b while W runs: dY -> dv (staged [t][dv] over Y^T) and -dY^T -> DU; dP -> DP;
-        //      sum_t Km Km' for dGamma_L; the dv rows out ----------------------------------------------------
-        {
-            float r[16], a[16], km2[16];
-            tld16(tDY + lane_off + cg * 16, r);
-            tld16(tDU + lane_off + cg * 16, a);            // dP, M = 64
-            tld16(tKM + lane_off + cg * 16, km2);
-            twait(r, a, km2);
-            const int dv = jv;
-            __nv_bfloat16 *dvs = reinterpret_cast<__nv_bfloat16 *>(sm + YT);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = cg * 16 + j;
-                dvs[t * D + dv] = __float2bfloat16_rn(r[j]);
-                if (t < t_own && t < t_end)
-                    p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + D + dv] = r[j];
-                r[j] = -r[j];
+            ++armed[1];
+            poll(1);
+            if (!meet()) break;
+            // ---- E2: U^T -> VV (raw v is consumed), dU^T -> DU -----------------------------------------
+            {
+                float r[16], r2[16];
+                tld16(tX + lane_off + cg * 16, r);
+                tld16(tDU + lane_off + cg * 16, r2);
+                twait(r, r2);
+                tc::st_sw128_8(sm + VV, 128, jv, cg * 16, r);
+                tc::st_sw128_8(sm + VV, 128, jv, cg * 16 + 8, r + 8);
+                tc::st_sw128_8(sm + DU, 128, jv, cg * 16, r2);
+                tc::st_sw128_8(sm + DU, 128, jv, cg * 16 + 8, r2 + 8);
             }
-            tc::st_sw128_8(sm + DU, 128, dv, cg * 16, r);
-            tc::st_sw128_8(sm + DU, 128, dv, cg * 16 + 8, r + 8);
-            if (lane < 16) {
-                const int t = 16 * lq + lane;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) a[j] = (cg * 16 + j <= t) ? a[j] : 0.f;
-                tc::st_sw128_8(sm + DP, 64, t, cg * 16, a);
-                tc::st_sw128_8(sm + DP, 64, t, cg * 16 + 8, a + 8);
+            csync_mma();
+            // ---- B3: Z^T = dU^T T;  dP = dO U^T (M = 64);  Km' = Q'^T U^T;  dQp^T = R^T dO^T ------------
+            if (tid == 0) {
+                tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + DU), 16384, false}, tc::Opnd{tc::smem_addr(sm + TT), 8192, true},
+                           128, 64, 64, false);
+                tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + DO), 8192, false}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
+                           64, 64, 128, false);
+                tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + QQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
+                           128, 64, 128, false);
+                tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DO), 8192, false},
+                           128, 64, 128, false);
+                tc::mma_commit(&bars[2]);
             }
-            // sum_t Km[t][c] Km'[c][t]
-            float acc = 0.f;
+            ++armed[2];
+            poll(2);
+            if (!meet()) break;
+            // ---- E3: Z^T -> ZT (over Q'); dY = diag(beta) Z -> dv rows, -dY^T -> DU; dP -> DP;
+            //      sum_t Km Km' for dGamma_L ---------------------------------------------------------------
+            {
+                float z[16], a[16], km2[16];
+                tld16(tDY + lane_off + cg * 16, z);
+                tld16(tDU + lane_off + cg * 16, a);             // dP, M = 64
+                tld16(tKM + lane_off + cg * 16, km2);
+                twait(z, a, km2);
+                const int dv = jv;
+                tc::st_sw128_8(sm + QQ, 128, dv, cg * 16, z);
+                tc::st_sw128_8(sm + QQ, 128, dv, cg * 16 + 8, z + 8);
+                __nv_bfloat16 *dvo = static_cast<__nv_bfloat16 *>(p.dv);
+                const int64_t orow = static_cast<int64_t>(I.row0) + I.c0 - I.rho;   // compact row of local row 0
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc += km2[j] * bf(sm + KM + (jv >> 6) * 8192 + sw64(cg * 16 + j, jv & 63));
-            vqs[cg * 128 + jv] = acc;
-        }
-        __syncthreads();
-        {
-            __nv_bfloat16 *dvo = static_cast<__nv_bfloat16 *>(p.dv);
-            for (int e = tid; e < 64 * 16; e += NT) {
-                const int t = e >> 4, pc = e & 15;
+                for (int j = 0; j < 16; ++j) {
+                    const int t = cg * 16 + j;
+                    const float y = z[j] * vbeta[t];
+                    if (t < t_end) {
+                        if (t >= t_own)
+                            dvo[((orow + t) * H + I.h) * D + dv] = __float2bfloat16_rn(y);
+                        else
+                            p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + D + dv] = y;
+                    }
+                    z[j] = -y;
+                }
+                tc::st_sw128_8(sm + DU, 128, dv, cg * 16, z);
+                tc::st_sw128_8(sm + DU, 128, dv, cg * 16 + 8, z + 8);
+                if (lane < 16) {
+                    const int t = 16 * lq + lane;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) a[j] = (cg * 16 + j <= t) ? a[j] : 0.f;
+                    tc::st_sw128_8(sm + DP, 64, t, cg * 16, a);
+                    tc::st_sw128_8(sm + DP, 64, t, cg * 16 + 8, a + 8);
+                }
+                // sum_t Km[t][c] Km'[c][t]
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc += km2[j] * bf(sm + KM + (jv >> 6) * 8192 + sw64(cg * 16 + j, jv & 63));
+                vqs[cg * 128 + jv] = acc;
+            }
+            csync_mma();
+            // ---- B4: W = Z U^T, D = Z Y^T (M = 128: rows 64-127 read the second Q' atom as padding, so
+            //      row t lands in lane t);  dKp^T = -R^T dY^T -------------------------------------------------
+            if (tid == 0) {
+                tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + QQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
+                           128, 64, 128, false);
+                tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + QQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + YT), 16384, true},
+                           128, 64, 128, false);
+                tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DU), 16384, true},
+                           128, 64, 128, false);
+                tc::mma_commit(&bars[3]);
+            }
+            ++armed[3];
+            if (tid < 128) vdgl[tid] += vqs[tid] + vqs[128 + tid] + vqs[256 + tid] + vqs[384 + tid];
+            poll(3);
+            if (!meet()) break;
+            // ---- E4: dM = -strict(W); dA = diag(beta) dM -> WA; dbeta = D[t][t] + rowsum(dM .* A) ----------
+            {
+                if (lq < 2) {
+                    float w[16], d2[16], a[16];
+                    tld16(tDU + lane_off + cg * 16, w);
+                    tld16(tX + lane_off + cg * 16, d2);
+                    tld16(tAP + lane_off + cg * 16, a);
+                    twait(w, d2, a);
+                    const int t = jv;
+                    const float bt = vbeta[t];
+                    float db = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int s = cg * 16 + j;
+                        const float dm = s < t ? -w[j] : 0.f;
+                        db += dm * a[j];
+                        if (s == t) db += d2[j];
+                        w[j] = bt * dm;
+                    }
+                    tc::st_sw128_8(sm + WA, 64, t, cg * 16, w);
+                    tc::st_sw128_8(sm + WA, 64, t, cg * 16 + 8, w + 8);
+                    vqs[cg * 64 + t] = db;
+                }
+                csync();
+                if (tid < 64) vdb[tid] = vqs[tid] + vqs[64 + tid] + vqs[128 + tid] + vqs[192 + tid];
+            }
+            csync_mma();
+            // ---- B6: dQp^T += Km^T dP^T;  dKp^T += Km^T dA^T;  Km' += Kp^T dA + Qp^T dP ------------------
+            if (tid == 0) {
+                tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + KM), 8192, true}, tc::Opnd{tc::smem_addr(sm + DP), 8192, false},
+                           128, 64, 64, true);
+                tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + KM), 8192, true}, tc::Opnd{tc::smem_addr(sm + WA), 8192, false},
+                           128, 64, 64, true);
+                tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + KQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + WA), 8192, true},
+                           128, 64, 64, true);
+                tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + KQ) + 8192, 16384, true},
+                           tc::Opnd{tc::smem_addr(sm + DP), 8192, true}, 128, 64, 64, true);
+                tc::mma_commit(&bars[4]);
+            }
+            ++armed[4];
+            poll(4);
+            if (!meet()) break;
+            // ---- E6: dq, dk, dgamma per (channel, row); dg = suffix sums + dGamma_L -----------------------
+            //      (two halves of 8 rows, the later half first, so the suffix sums run in one pass)
+            {
+                const int c = jv;
+                const float m2 = vm2[c], sc = f.scale;
+                __nv_bfloat16 *dqs = reinterpret_cast<__nv_bfloat16 *>(sm + YT);
+                __nv_bfloat16 *dks = reinterpret_cast<__nv_bfloat16 *>(sm + DU);
+                float dgm[16];
+                float run = 0.f;
+#pragma unroll
+                for (int hh = 1; hh >= 0; --hh) {
+                    const int cb = cg * 16 + hh * 8;
+                    float xq[8], xp[8], xm[8], g2v[8];
+                    uint32_t kpk[4], qpk[4];
+                    tld8f(tDT + lane_off + cb, xq);
+                    tld8f(tDY + lane_off + cb, xp);
+                    tld8f(tKM + lane_off + cb, xm);
+                    tld8f(tGM + lane_off + cb, g2v);
+                    tld4(tPK + lane_off + cg * 8 + hh * 4, kpk);
+                    tld4(tPK + lane_off + 32 + cg * 8 + hh * 4, qpk);
+                    twait8(xq, xp, xm, g2v, kpk, qpk);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int t = cb + j;
+                        const float2 kp2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kpk[j >> 1]));
+                        const float2 qp2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qpk[j >> 1]));
+                        const float kp = (j & 1) ? kp2.y : kp2.x, qp = (j & 1) ? qp2.y : qp2.x;
+                        const float km = bf(sm + KM + (c >> 6) * 8192 + sw64(t, c & 63));
+                        const float x = g2v[j] - m2;
+                        const float e1 = ex2(x), e2 = ex2(-x);
+                        const float dqv = sc * xq[j] * e1;
+                        const float dkv = xp[j] * e1 + xm[j] * e2;
+                        dgm[hh * 8 + j] = xq[j] * qp + xp[j] * kp - xm[j] * km;
+                        dqs[t * D + c] = __float2bfloat16_rn(dqv);
+                        dks[t * D + c] = __float2bfloat16_rn(dkv);
+                        if (t < t_own && t < t_end)
+                            p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + c] = dkv;
+                    }
+                    // suffix sums over t within this thread's rows, continuing the later half's
+#pragma unroll
+                    for (int j = 7; j >= 0; --j) { run += dgm[hh * 8 + j]; dgm[hh * 8 + j] = run; }
+                }
+                // then the later quarters' totals
+                vqs[cg * 128 + c] = run;
+                csync();
+                float off = vdgl[c];
+#pragma unroll
+                for (int q = 1; q < 4; ++q) off += q > cg ? vqs[q * 128 + c] : 0.f;
+                __nv_bfloat16 *dgs = reinterpret_cast<__nv_bfloat16 *>(sm + DP);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = cg * 16 + j;
+                    const float x = dgm[j] + off;
+                    dgs[t * D + c] = __float2bfloat16_rn(x);
+                    if (t < t_own && t < t_end)
+                        p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + 2 * D + c] = x;
+                }
+            }
+            tc::fence_before_sync();
+            csync();
+            for (int e = tid; e < 3 * 64 * 16; e += NC) {
+                const int which = e >> 10, t = (e >> 4) & 63, pc = e & 15;
                 if (t < t_own || t >= t_end) continue;
                 const int64_t row = static_cast<int64_t>(I.row0) + (I.c0 + t - I.rho);
-                *reinterpret_cast<uint4 *>(dvo + (row * H + I.h) * D + pc * 8) =
-                    *reinterpret_cast<const uint4 *>(sm + YT + t * 256 + pc * 16);
+                void *dst = which == 0 ? p.dq : (which == 1 ? p.dk : p.dg);
+                const uint8_t *srcp = sm + (which == 0 ? YT : (which == 1 ? DU : DP));
+                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(dst) + (row * H + I.h) * D + pc * 8) =
+                    *reinterpret_cast<const uint4 *>(srcp + t * 256 + pc * 16);
             }
-            if (tid < 128) vdgl[tid] += vqs[tid] + vqs[128 + tid] + vqs[256 + tid] + vqs[384 + tid];
-            if (tid < 64) vdb[tid] = vdb[tid] + vdb[64 + tid] + vdb[128 + tid] + vdb[192 + tid];
-        }
-        if (!wait_mma(&bars[3], ph, &s_fail)) break;
-        if (nxt < n_items) stage(2, nx);                   // Tb and dT are consumed: the next item's g
-        // ---- E4: W -> WA -------------------------------------------------------------------------------
-        {
-            float r[16];
-            tmem_ld16(tDT + lane_off + cg * 16, r);
-            if (lane < 16) {
-                const int t = 16 * lq + lane;
-                tc::st_sw128_8(sm + WA, 64, t, cg * 16, r);
-                tc::st_sw128_8(sm + WA, 64, t, cg * 16 + 8, r + 8);
-            }
-        }
-        sync_mma();
-        // ---- B5: T^T W (M = 128: rows 64-127 read Tb as padding, so row r lands in lane r) ------------
-        if (tid == 0) {
-            tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + TT), 8192, true}, tc::Opnd{tc::smem_addr(sm + WA), 8192, true},
-                       128, 64, 64, false);
-            tc::mma_commit(&bars[4]);
-        }
-        ++armed[4];
-        if (!wait_mma(&bars[4], ph, &s_fail)) break;
-        if (nxt < n_items) stage(5, nx);                   // T consumed: the next item's T
-        // ---- E5: dM = -strict(T^T W); dA = diag(beta) dM -> WA; dbeta += rowsum(dM .* A) ----------------
-        {
-            float r[16], a[16];
-            tld16(tDT + lane_off + cg * 16, r);
-            tld16(tAP + lane_off + cg * 16, a);
-            twait(r, a);
-            if (lq < 2) {
-                const int t = jv;
-                const float bt = vbeta[t];
-                float dba = 0.f;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int s = cg * 16 + j;
-                    const float dm = s < t ? -r[j] : 0.f;
-                    dba += dm * a[j];
-                    r[j] = bt * dm;
-                }
-                vqs[cg * 64 + t] = dba;
-            }
-            __syncthreads();
-            if (lq < 2) {
-                const int t = jv;
-                tc::st_sw128_8(sm + WA, 64, t, cg * 16, r);
-                tc::st_sw128_8(sm + WA, 64, t, cg * 16 + 8, r + 8);
-            }
-            if (tid < 64) vdb[tid] += vqs[tid] + vqs[64 + tid] + vqs[128 + tid] + vqs[192 + tid];
-        }
-        sync_mma();
-        // ---- B6: dQp^T = R^T dO^T + Km^T dP^T;  dKp^T = -R^T dY^T + Km^T dA^T;  Km' += Kp^T dA + Qp^T dP --
-        if (tid == 0) {
-            tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DO), 8192, false},
-                       128, 64, 128, false);
-            tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + KM), 8192, true}, tc::Opnd{tc::smem_addr(sm + DP), 8192, false},
-                       128, 64, 64, true);
-            tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DU), 16384, true},
-                       128, 64, 128, false);
-            tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + KM), 8192, true}, tc::Opnd{tc::smem_addr(sm + WA), 8192, false},
-                       128, 64, 64, true);
-            tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + KQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + WA), 8192, true},
-                       128, 64, 64, true);
-            tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + KQ) + 8192, 16384, true},
-                       tc::Opnd{tc::smem_addr(sm + DP), 8192, true}, 128, 64, 64, true);
-            tc::mma_commit(&bars[5]);
-        }
-        ++armed[5];
-        if (!wait_mma(&bars[5], ph, &s_fail)) break;
-        // everything but Km (read below) is consumed: the next item's q, k, dO and S^T record
-        if (nxt < n_items) {
-            // q, k, dO of a gathered chunk share one barrier pass
-            const bool gq = chunk_gathers(max(0, nx.rho - nx.c0), nx.nv, 0);
-            const bool gd = chunk_gathers(max(0, nx.rho - nx.c0), nx.nv, max(0, nx.rho - nx.c0));
-            stage(0, nx, true);
-            stage(1, nx, true);
-            stage(4, nx, true);
-            stage(6, nx);
-            if (gq || gd) {
-                __syncthreads();
-                if (tid == 0) {
-                    if (gq) { mbar_arrive_one(&bars[6]); mbar_arrive_one(&bars[7]); }
-                    if (gd) mbar_arrive_one(&bars[10]);
+            if (tid < 64) {
+                const int t = tid;
+                const float db = vdb[t];
+                if (t < t_end) {
+                    if (t >= t_own)
+                        static_cast<__nv_bfloat16 *>(p.dbeta)[(static_cast<int64_t>(I.row0) + (I.c0 + t - I.rho)) * H + I.h] =
+                            __float2bfloat16_rn(db);
+                    else
+                        p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + 3 * D] = db;
                 }
             }
+            csync();
+            tc::fence_after_sync();
         }
-        // ---- E6: dq, dk, dgamma per (channel, row); dg = suffix sums + dGamma_L ---------------------------
-        {
-            const int c = jv;
-            float xq[16], xp[16], xm[16], g2v[16];
-            uint32_t kpk[8], qpk[8];
-            tld16(tX + lane_off + cg * 16, xq);
-            tld16(tDU + lane_off + cg * 16, xp);
-            tld16(tKM + lane_off + cg * 16, xm);
-            tld16(tGM + lane_off + cg * 16, g2v);
-            tld8(tPK + lane_off + cg * 8, kpk);
-            tld8(tPK + lane_off + 32 + cg * 8, qpk);
-            twait(xq, xp, xm, g2v);
-            tkeep(kpk, qpk);
-            const float m2 = vm2[c], sc = f.scale;
-            __nv_bfloat16 *dqs = reinterpret_cast<__nv_bfloat16 *>(sm + YT);
-            __nv_bfloat16 *dks = reinterpret_cast<__nv_bfloat16 *>(sm + DU);
-            float dgm[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = cg * 16 + j;
-                const float2 kp2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kpk[j >> 1]));
-                const float2 qp2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qpk[j >> 1]));
-                const float kp = (j & 1) ? kp2.y : kp2.x, qp = (j & 1) ? qp2.y : qp2.x;
-                const float km = bf(sm + KM + (c >> 6) * 8192 + sw64(t, c & 63));
-                const float x = g2v[j] - m2;
-                const float e1 = ex2(x), e2 = ex2(-x);
-                const float dqv = sc * xq[j] * e1;
-                const float dkv = xp[j] * e1 + xm[j] * e2;
-                dgm[j] = xq[j] * qp + xp[j] * kp - xm[j] * km;
-                dqs[t * D + c] = __float2bfloat16_rn(dqv);
-                dks[t * D + c] = __float2bfloat16_rn(dkv);
-                if (t < t_own && t < t_end)
-                    p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + c] = dkv;
-            }
-            // suffix sums over t: within this thread's 16 rows, then the later quarters' totals
-            float run = 0.f;
-#pragma unroll
-            for (int j = 15; j >= 0; --j) { run += dgm[j]; dgm[j] = run; }
-            vqs[cg * 128 + c] = run;
-            __syncthreads();
-            float off = vdgl[c];
-#pragma unroll
-            for (int q = 1; q < 4; ++q) off += q > cg ? vqs[q * 128 + c] : 0.f;
-            __nv_bfloat16 *dgs = reinterpret_cast<__nv_bfloat16 *>(sm + DP);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = cg * 16 + j;
-                const float x = dgm[j] + off;
-                dgs[t * D + c] = __float2bfloat16_rn(x);
-                if (t < t_own && t < t_end)
-                    p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + 2 * D + c] = x;
-            }
-        }
-        tc::fence_before_sync();
-        __syncthreads();
-        for (int e = tid; e < 3 * 64 * 16; e += NT) {
-            const int which = e >> 10, t = (e >> 4) & 63, pc = e & 15;
-            if (t < t_own || t >= t_end) continue;
-            const int64_t row = static_cast<int64_t>(I.row0) + (I.c0 + t - I.rho);
-            void *dst = which == 0 ? p.dq : (which == 1 ? p.dk : p.dg);
-            const uint8_t *srcp = sm + (which == 0 ? YT : (which == 1 ? DU : DP));
-            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(dst) + (row * H + I.h) * D + pc * 8) =
-                *reinterpret_cast<const uint4 *>(srcp + t * 256 + pc * 16);
-        }
-        if (tid < 64) {
-            const int t = tid;
-            const float db = vdb[t];
-            if (t < t_end) {
-                if (t >= t_own)
-                    static_cast<__nv_bfloat16 *>(p.dbeta)[(static_cast<int64_t>(I.row0) + (I.c0 + t - I.rho)) * H + I.h] =
-                        __float2bfloat16_rn(db);
-                else
-                    p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + 3 * D] = db;
-            }
-        }
-        __syncthreads();
-        tc::fence_after_sync();
-        cur = nx;
-    }
-    // ---- drain --------------------------------------------------------------------------------------
-    tc::cp_async_wait_all();
-    __syncthreads();
-    if (s_fail) {
-        dev_error(pd, kDevErrTimeout, cur_seq, cur_h);
-        if (tid == 0)
-            for (int i = 0; i < 14; ++i)
+        // the last product batch armed on each barrier completes before TMEM and shared memory
+        // are released (batches complete in order)
+        if (tid == 0 && *reinterpret_cast<volatile int *>(&s_fail)) {
+            dev_error(pd, kDevErrTimeout, cur_seq, cur_h);
+            for (int i = 0; i < 5; ++i)
                 if (armed[i] > 0 && !tc::mbar_wait(&bars[i], (armed[i] - 1) & 1, 200000000LL))
                     dev_error(pd, kDevErrTimeout, cur_seq, cur_h);
+        }
     }
+    // ---- drain --------------------------------------------------------------------------------------
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();

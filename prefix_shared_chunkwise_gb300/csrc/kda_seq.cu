@@ -21,6 +21,9 @@
 // is never rescaled in place: the next chunk's R is S'^T diag(e^{m'}), formed once per chunk
 // as the fp32 state leaves TMEM and goes back in.
 //
+// Each chunk's record for the gradient pass holds the bf16 R the products used (not S^T)
+// and T, so the gradient pass needs neither m-scaling of the state nor an inversion.
+//
 // TMEM (256 columns): S = R in fp32 (128), R as bf16 pairs, the A operand of two products
 // (64), one work tile W (64) that holds in turn [A; P], Kp^T Tb^T, U^T and O^T.
 // Shared memory: KQ [Kp; Qp] (raw k and q land there), Km, V (then U^T, then the output
@@ -430,7 +433,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
     int32_t sp = pd.seq_sptr[seq];
     const int32_t sp_end = pd.seq_sptr[seq + 1];
     {
-        // S0^T (lane = value channel) into TMEM unscaled, and into the chunk-0 record
+        // S0^T (lane = value channel) into TMEM unscaled
         const float *S0 = src >= 0 ? p.states + (static_cast<int64_t>(src) * H + h) * D * D
                         : (p.h0 ? p.h0 + (static_cast<int64_t>(-1 - src) * H + h) * D * D : nullptr);
         float r0[32], r1[32];
@@ -440,24 +443,14 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
             r0[j] = S0 ? S0[(cb + j) * D + jv] : 0.f;
             r1[j] = S0 ? S0[(cb + 32 + j) * D + jv] : 0.f;
         }
-        if (rec) {
-            uint4 *dst = reinterpret_cast<uint4 *>(rec + (static_cast<int64_t>(cbase) * H + h) * kRecBytes + jv * 256 +
-                                                   cb * 2);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                dst[q] = make_uint4(tc::pack_bf16(r0[8 * q], r0[8 * q + 1]), tc::pack_bf16(r0[8 * q + 2], r0[8 * q + 3]),
-                                    tc::pack_bf16(r0[8 * q + 4], r0[8 * q + 5]), tc::pack_bf16(r0[8 * q + 6], r0[8 * q + 7]));
-                dst[q + 4] = make_uint4(tc::pack_bf16(r1[8 * q], r1[8 * q + 1]), tc::pack_bf16(r1[8 * q + 2], r1[8 * q + 3]),
-                                        tc::pack_bf16(r1[8 * q + 4], r1[8 * q + 5]), tc::pack_bf16(r1[8 * q + 6], r1[8 * q + 7]));
-            }
-        }
         tc::tmem_st32x2(tS + lane_off + cb, r0, tS + lane_off + cb + 32, r1);
     }
     bool ok = wait_data(&bars[4], 0, &s_fail);
     if (ok) {
         pass_a(0, braw);
         __syncthreads();
-        // R = S0^T diag(e^{m_0}): fp32 back into TMEM, bf16 pairs into the R columns
+        // R = S0^T diag(e^{m_0}): fp32 back into TMEM, bf16 pairs into the R columns and
+        // into the chunk-0 record
         const float *em = reinterpret_cast<const float *>(sm + VEM);
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
@@ -472,6 +465,12 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) pk[j] = tc::pack_bf16(r[2 * j], r[2 * j + 1]);
+            if (rec) {
+                uint4 *dst = reinterpret_cast<uint4 *>(rec + (static_cast<int64_t>(cbase) * H + h) * kRecBytes +
+                                                       jv * 256 + cb * 2);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
             tc::tmem_st32_issue(tS + lane_off + cb, r);
             asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
                          "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
@@ -662,16 +661,6 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
                     for (int j = 0; j < 32; ++j) fd[(cb + j) * D + jv] = r[j];
                 }
                 if (more) {
-                    if (rdst) {
-                        // staged [dv][64] per column half (SW128 rows), written out coalesced below
-                        uint8_t *stg = sm + (ch ? SC : KM) + jv * 128;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4 *>(stg + (((hf * 4 + q) ^ (jv & 7)) << 4)) =
-                                make_uint4(tc::pack_bf16(r[8 * q], r[8 * q + 1]), tc::pack_bf16(r[8 * q + 2], r[8 * q + 3]),
-                                           tc::pack_bf16(r[8 * q + 4], r[8 * q + 5]),
-                                           tc::pack_bf16(r[8 * q + 6], r[8 * q + 7]));
-                    }
                     uint32_t pk[16];
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {                         // next chunk's R
@@ -680,6 +669,15 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
                     }
 #pragma unroll
                     for (int j = 0; j < 16; ++j) pk[j] = tc::pack_bf16(r[2 * j], r[2 * j + 1]);
+                    if (rdst) {
+                        // the next chunk's record (its bf16 R), staged [dv][64] per column half
+                        // (SW128 rows), written out coalesced below
+                        uint8_t *stg = sm + (ch ? SC : KM) + jv * 128;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4 *>(stg + (((hf * 4 + q) ^ (jv & 7)) << 4)) =
+                                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    }
                     tc::tmem_st32_issue(tS + lane_off + cb, r);
                     asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
                                  "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
@@ -743,8 +741,8 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
 // initial-state gradients to the carry).  With dS' the gradient at the chunk end and
 // Q' = dS'^T diag(e^{Gamma_L - m}) (lane = value channel):
 //   dU^T = dO^T P + Q' Km^T,   dY^T = dU^T Tb,   dS^T = (Q' + dO^T Qp - dY^T Kp) diag(e^m)
-// where Tb = T diag(beta) with T from the forward's chunk record.  dS'^T is saved per chunk
-// (bf16) for the gradient pass.  TMEM: the carry C (fp32, 128 columns), Q' as bf16 pairs
+// where Tb = T diag(beta) with T from the forward's chunk record.  The bf16 Q' (the operand
+// the products use) is saved per chunk for the gradient pass.  TMEM: the carry C (fp32, 128 columns), Q' as bf16 pairs
 // (the A operand of Q' Km^T, 64), one work tile W (64) for P, dU^T and dY^T in turn.
 // ======================================================================================
 namespace s2 {
@@ -868,8 +866,8 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
         chunk_pass_a(sm, sm + KM, vqs, vmr, vbeta, sm + VM, sm + VEM, sm + VEG, nv, b, braw, pd, seq, c0);
         __syncthreads();
 
-        // ---- carry: dS' = C e^{m_next} (+ consumers' initial-state gradients at a slot),
-        //      saved for the gradient pass; then Q' = dS'^T diag(e^{Gamma_L - m}) ---------------
+        // ---- carry: dS' = C e^{m_next} (+ consumers' initial-state gradients at a slot);
+        //      Q' = dS'^T diag(e^{Gamma_L - m}), its bf16 copy saved for the gradient pass ------
         {
             const bool slot = sp >= sp_begin && pd.state_lpos[sp] == pend;
             const int32_t cb_ = slot ? pd.state_cptr[sp] : 0, ce_ = slot ? pd.state_cptr[sp + 1] : 0;
@@ -893,14 +891,6 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] += di[(cb + j) * D + jv];
                 }
-                // this half's 32 columns per row into DU ([dv][64]: columns ch * 32 .. + 31), then
-                // out to the record row by row, 64 contiguous bytes per row segment
-                uint8_t *stg = sm + DU + jv * 128;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4 *>(stg + (((ch * 4 + q) ^ (jv & 7)) << 4)) =
-                        make_uint4(tc::pack_bf16(r[8 * q], r[8 * q + 1]), tc::pack_bf16(r[8 * q + 2], r[8 * q + 3]),
-                                   tc::pack_bf16(r[8 * q + 4], r[8 * q + 5]), tc::pack_bf16(r[8 * q + 6], r[8 * q + 7]));
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
                     const float4 a = *reinterpret_cast<const float4 *>(eg + cb + j);
@@ -909,6 +899,14 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) pk[j] = tc::pack_bf16(r[2 * j], r[2 * j + 1]);
+                // the bf16 Q' of this half's 32 columns per row into DU ([dv][64]: columns
+                // ch * 32 .. + 31), then out to the record row by row, 64 contiguous bytes per
+                // row segment
+                uint8_t *stg = sm + DU + jv * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4 *>(stg + (((ch * 4 + q) ^ (jv & 7)) << 4)) =
+                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 tc::tmem_st32_issue(tC + lane_off + cb, r);
                 asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
                              "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"

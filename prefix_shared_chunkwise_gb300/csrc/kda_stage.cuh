@@ -56,6 +56,33 @@ __device__ __forceinline__ void stage_chunk_rows(const void *src, const RowMaps 
     if (tid == 0) mbar_arrive_one(bar);
 }
 
+// The same staging done by one warp alone (a load warp): a full own chunk as two 64-row TMA
+// boxes issued by lane 0, any other chunk gathered by the warp's 32 lanes.  All 32 lanes call
+// this; it completes one phase of `bar`.
+__device__ __forceinline__ void stage_chunk_rows_warp(const void *src, const RowMaps &maps, const int *tab,
+                                                      int32_t h, int H, int t_own, int t_end, int32_t own0,
+                                                      int zero_below, uint8_t *dst0, uint8_t *dst1, uint64_t *bar) {
+    const int lane = threadIdx.x & 31;
+    if (t_own == 0 && t_end == 64 && zero_below == 0) {
+        if (lane == 0) {
+            tc::mbar_expect_tx(bar, 16384);
+            tc::tma_load_3d(dst0, &maps.box64, 0, h, own0, bar);
+            tc::tma_load_3d(dst1, &maps.box64, 64, h, own0, bar);
+        }
+        return;
+    }
+    const uint8_t *s8 = static_cast<const uint8_t *>(src);
+    for (int e = lane; e < 64 * 16; e += 32) {
+        const int t = e >> 4, pc = e & 15;
+        const int64_t row = t < zero_below ? -1 : tab[t];
+        uint8_t *dst = (pc < 8 ? dst0 : dst1) + t * 128 + (((pc & 7) ^ (t & 7)) << 4);
+        tc::cp_async16(dst, row >= 0 ? s8 + ((row * H + h) * 256 + pc * 16) : s8, row >= 0 ? 16u : 0u);
+    }
+    cp_async_arrive_on(bar);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_one(bar);
+}
+
 // Whether stage_chunk_rows gathers (and, with defer, leaves the arrive to gather_done).
 __device__ __forceinline__ bool chunk_gathers(int t_own, int t_end, int zero_below) {
     return !(t_own == 0 && t_end == 64 && zero_below == 0);
