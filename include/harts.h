@@ -173,7 +173,8 @@ typedef struct {
     int32_t dtype;           /* harts_dtype of q, k, v, g, beta, o, chunk_states */
     int32_t kernel;          /* harts_kernel */
     float scale;             /* o = scale * S^T q */
-    const void *q;           /* device [C,H,dk] */
+    const void *q;           /* device [C,H,dk], 16-byte aligned (so are k, v, g, o,
+                                chunk_states and the backward's d_o, dq, dk, dv, dg) */
     const void *k;           /* device [C,H,dk] */
     const void *v;           /* device [C,H,dv] */
     const void *g;           /* device [C,H,dk] natural-log per-channel decay (<= 0) */
@@ -207,7 +208,7 @@ size_t harts_kda_chunk_state_bytes(const harts_plan *plan, int32_t H, int32_t dk
  * from the zero state (root; or h0), or from a slot written by an earlier round,
  * runs its replay rows and own rows chunk by chunk, writes o for its own rows only,
  * stores requested boundary states into their slots and its final state.
- * Errors: HARTS_EINVAL, HARTS_EUNSUPPORTED (dk, dv not in {32,64,128}, dk != dv,
+ * Errors: HARTS_EINVAL (NULL or misaligned pointers), HARTS_EUNSUPPORTED (dk, dv not in {32,64,128}, dk != dv,
  * B not in {16,32,64}), HARTS_ENOPLAN, HARTS_EOVERFLOW (C * H above 2^31 - 1),
  * HARTS_ECUDA.
  */

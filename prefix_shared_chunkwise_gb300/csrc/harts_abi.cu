@@ -37,6 +37,8 @@ int cuda_fail(cudaError_t e, const char *what) {
 
 size_t dtype_size(int32_t dt) { return dt == HARTS_FP32 ? 4 : 2; }
 
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }   // NULL passes
+
 int check_fwd_args(const harts_plan *P, const harts_kda_fwd_args *a) {
     if (!P || !a) { set_error("NULL plan or args"); return HARTS_EINVAL; }
     if (!P->dev) { set_error("plan not uploaded (harts_plan_upload)"); return HARTS_ENOPLAN; }
@@ -44,6 +46,12 @@ int check_fwd_args(const harts_plan *P, const harts_kda_fwd_args *a) {
     if (a->H < 1 || a->dk < 1 || a->dv < 1) { set_error("H, dk, dv must be >= 1"); return HARTS_EINVAL; }
     if (a->dk != a->dv) { set_error("dk != dv is not supported"); return HARTS_EUNSUPPORTED; }
     if (!a->q || !a->k || !a->v || !a->g || !a->beta) { set_error("NULL input"); return HARTS_EINVAL; }
+    // rows are moved 16 bytes at a time (tensor maps, vector loads and stores)
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->g) || !aligned16(a->o) ||
+        !aligned16(a->chunk_states)) {
+        set_error("q, k, v, g, o and chunk_states must be 16-byte aligned");
+        return HARTS_EINVAL;
+    }
     if (P->info.n_states > 0 && !a->states) { set_error("states required (n_states > 0)"); return HARTS_EINVAL; }
     if (a->kernel < HARTS_KERNEL_AUTO || a->kernel > HARTS_KERNEL_TC) { set_error("kernel"); return HARTS_EINVAL; }
     // row * H * D offsets are formed in int64 inside the kernels; (row, head) indices of
@@ -228,6 +236,10 @@ static int kda_bwd_phases(const harts_plan *P, const harts_kda_bwd_args *a, hart
         return HARTS_EUNSUPPORTED;
     }
     if (!a->d_o || !a->dq || !a->dk || !a->dv || !a->dg || !a->dbeta) { set_error("NULL gradient pointer"); return HARTS_EINVAL; }
+    if (!aligned16(a->d_o) || !aligned16(a->dq) || !aligned16(a->dk) || !aligned16(a->dv) || !aligned16(a->dg)) {
+        set_error("d_o, dq, dk, dv and dg must be 16-byte aligned");
+        return HARTS_EINVAL;
+    }
     if (!a->fwd.chunk_states) { set_error("chunk_states from the forward pass are required"); return HARTS_EINVAL; }
     const int D = a->fwd.dk, H = a->fwd.H, BC = P->info.chunk;
     const int fam = pick(&a->fwd, BC, true);

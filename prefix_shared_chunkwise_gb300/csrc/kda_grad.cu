@@ -45,13 +45,15 @@ constexpr uint32_t QQ = 32768;      // [128 dv][128 dk] Q' record -> Z^T [128 dv
 constexpr uint32_t KQ = 65536;      // [128][128]: raw k -> Kp (rows 0-63), raw q -> Qp (64-127)
 constexpr uint32_t KM = 98304;      // [64][128] (atoms 8 KB): Km
 constexpr uint32_t VV = 114688;     // raw v [64][128] (atoms 8 KB) -> U^T [128][64]
-constexpr uint32_t DO = 131072;     // dO [64][128] (atoms 8 KB)
-constexpr uint32_t TT = 147456;     // T [64][64]
-constexpr uint32_t TB = 155648;     // Tb [64][64]    } TB..PT: raw g of the next item
-constexpr uint32_t PT = 163840;     // P [64][64]     }
-constexpr uint32_t YT = 172032;     // Y^T [128][64] -> dq staging [64 t][128]
-constexpr uint32_t DU = 188416;     // dU^T [128][64] -> -dY^T -> dk staging
-constexpr uint32_t DP = 204800;     // dP [64][64]   } DP..WA: dg staging
+// DO: two atoms of [128 rows][64 columns] (16 KB apart): rows 0-63 hold dO [t][dv], rows 64-127
+// (DX) hold dU [t][dv] (the MN-major B operand of T^T dU), then -dY [t][dv].
+constexpr uint32_t DO = 131072;
+constexpr uint32_t DX = DO + 8192;  // the dU / -dY rows
+constexpr uint32_t TT = 163840;     // T [64][64]
+constexpr uint32_t TB = 172032;     // Tb [64][64]    } TB..PT: raw g of the next item
+constexpr uint32_t PT = 180224;     // P [64][64]     }
+constexpr uint32_t YT = 188416;     // Y^T [128][64]
+constexpr uint32_t DP = 204800;     // dP [64][64]   } one [128][64] operand [dP; dA]
 constexpr uint32_t WA = 212992;     // dA [64][64]   }
 constexpr uint32_t VQS = 221184;    // fp32 [4][128] partial sums (several uses)
 constexpr uint32_t VMR = VQS + 2048;
@@ -86,6 +88,10 @@ __device__ __forceinline__ void tld8(uint32_t taddr, uint32_t (&u)[8]) {
 }
 #define HARTS_R16(a) "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), \
     "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15])
+__device__ __forceinline__ void twait1(float (&a)[16]) {
+    uint32_t *x = reinterpret_cast<uint32_t *>(a);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : HARTS_R16(x) :: "memory");
+}
 __device__ __forceinline__ void twait(float (&a)[16], float (&b)[16]) {
     uint32_t *x = reinterpret_cast<uint32_t *>(a), *y = reinterpret_cast<uint32_t *>(b);
     asm volatile("tcgen05.wait::ld.sync.aligned;" : HARTS_R16(x), HARTS_R16(y) :: "memory");
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
     if (warp >= NC / 32) {
         // ================= load warps: every copy of the next item, issued as its buffer frees ====
         // Load warp 0: g, T and the two records (and the item's indices and beta for the compute
-        // warps); 1: dO and v; 2: q; 3: k.  Each walks the items on its own, so that one warp's
+        // warps); 1: dO; 2: q and v; 3: k.  Each walks the items on its own, so that one warp's
         // row gathers (replay rows, a sequence's last partial chunk) never hold up another's copies.
         const int lw = warp - NC / 32;
         int *rows = s_rows[lw];
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             case 2: stage_chunk_rows_warp(f.g, maps.g, rows, it.h, H, t_own, t_end, own0, 0, sm + TB, sm + TB + 8192, bar); break;
             case 3: stage_chunk_rows_warp(f.v, maps.v, rows, it.h, H, t_own, t_end, own0, 0, sm + VV, sm + VV + 8192, bar); break;
             case 4: stage_chunk_rows_warp(p.d_o, maps.dout, rows, it.h, H, t_own, t_end, own0, t_own, sm + DO,
-                                          sm + DO + 8192, bar); break;
+                                          sm + DO + 16384, bar); break;
             case 5:
                 if (lane == 0) {
                     tc::mbar_expect_tx(bar, 8192);
@@ -311,8 +317,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             const Item it = item_of(pd, chunk_begin, H, item);
             rows_of(it, 0u);
             if (lw == 0) { stage(2, it); stage(5, it); stage(6, it); stage(7, it); }
-            else if (lw == 1) { stage(4, it); stage(3, it); }
-            else stage(lw == 2 ? 0 : 1, it);
+            else if (lw == 1) stage(4, it);
+            else if (lw == 2) { stage(0, it); stage(3, it); }
+            else stage(1, it);
         }
         for (uint32_t n = 0; item < n_items; item += gridDim.x, ++n) {
             const int32_t nxt = item + gridDim.x;
@@ -329,13 +336,15 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                 stage(6, nx);
                 stage(7, nx);
             } else if (lw == 1) {
-                if (!wait_free(2, ph)) break;                // B3 done: dO is free
+                if (!wait_free(2, ph)) break;                // B3 done: the dO rows are free
                 stage(4, nx);
-                if (!wait_free(3, ph)) break;                // B4 done: U^T (over v) is free
-                stage(3, nx);
             } else {
-                if (!wait_free(4, ph)) break;                // B6 done: Kp, Qp are free
+                if (!wait_free(0, ph)) break;                // B1 done: the [Kp; Qp] tile is free
                 stage(lw == 2 ? 0 : 1, nx);
+                if (lw == 2) {
+                    if (!wait_free(3, ph)) break;            // B4 done: U^T (over v) is free
+                    stage(3, nx);
+                }
             }
         }
         // every copy issued lands before shared memory is released
@@ -439,11 +448,23 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
-            // ---- colsum(Q' .* R) (dGamma_L's first term) from the records; Tb = T diag(beta) -----
-            poll(11);
+            // ---- B1 once the records are in (pass B's tiles and TMEM copies are written) ------------
             poll(12);
             poll(13);
+            tc::fence_smem_to_async();
+            tc::fence_before_sync();
             if (!meet()) break;
+            // ---- B1: [A; P] = [Kp; Qp] Km^T;  X = R Kp^T;  dU = Km Q'^T (M = 64, rows t) ---------------
+            if (tid == 0) {
+                const uint32_t id = tc::idesc_bf16(128, 64);
+                tc::mma_tile(tAP, tc::smem_addr(sm + KQ), 16384, tc::smem_addr(sm + KM), 8192, 128, id, false);
+                tc::mma_tile(tX, tc::smem_addr(sm + RR), 16384, tc::smem_addr(sm + KQ), 16384, 128, id, false);
+                tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + KM), 8192, false}, tc::Opnd{tc::smem_addr(sm + QQ), 16384, false},
+                           64, 128, 128, false);
+                tc::mma_commit(&bars[0]);
+            }
+            ++armed[0];
+            // ---- while B1 runs: colsum(Q' .* R) (dGamma_L's first term); Tb = T diag(beta) -------
             {
                 // warp w: logical 8-column chunk w (atom w / 8) of every row; lane: rows lane + 32 i
                 const int jl = warp & 7, atom = warp >> 3, col0 = atom * 64 + jl * 8;
@@ -458,16 +479,36 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
 #pragma unroll
                     for (int k = 0; k < 8; ++k) dot[k] += vr[k] * vq[k];
                 }
+                // sum the 8 columns over the 32 lanes: three halving exchanges (each lane keeps the
+                // half of its columns selected by one lane bit), then two plain ones
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
+                for (int k = 0; k < 4; ++k) {
+                    const bool hi = lane & 16;
+                    const float send = hi ? dot[k] : dot[k + 4];
+                    const float keep = hi ? dot[k + 4] : dot[k];
+                    dot[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                }
 #pragma unroll
-                    for (int sh = 16; sh >= 1; sh >>= 1) dot[k] += __shfl_xor_sync(0xffffffffu, dot[k], sh);
+                for (int k = 0; k < 2; ++k) {
+                    const bool hi = lane & 8;
+                    const float send = hi ? dot[k] : dot[k + 2];
+                    const float keep = hi ? dot[k + 2] : dot[k];
+                    dot[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
                 }
-                if (lane == 0) {
-                    *reinterpret_cast<float4 *>(vdgl + col0) = make_float4(dot[0], dot[1], dot[2], dot[3]);
-                    *reinterpret_cast<float4 *>(vdgl + col0 + 4) = make_float4(dot[4], dot[5], dot[6], dot[7]);
+                {
+                    const bool hi = lane & 4;
+                    const float send = hi ? dot[0] : dot[1];
+                    const float keep = hi ? dot[1] : dot[0];
+                    dot[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
                 }
+                dot[0] += __shfl_xor_sync(0xffffffffu, dot[0], 2);
+                dot[0] += __shfl_xor_sync(0xffffffffu, dot[0], 1);
+                // lane bits 4, 3, 2 pick the column: 4 * b4 + 2 * b3 + b2
+                if ((lane & 3) == 0)
+                    vdgl[col0 + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1)] = dot[0];
             }
+            poll(11);
+            if (!meet()) break;
             {
                 const int t = tid >> 3, j = tid & 7;              // Tb: row t, 16-byte chunk j
                 const uint4 w = *reinterpret_cast<const uint4 *>(sm + TT + t * 128 + (j << 4));
@@ -478,16 +519,6 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                 for (int i = 0; i < 8; ++i) v[i] *= vbeta[col0 + i];
                 *reinterpret_cast<uint4 *>(sm + TB + t * 128 + (j << 4)) = pack8(v);
             }
-            csync_mma();
-            // ---- B1: [A; P] = [Kp; Qp] Km^T;  X = R Kp^T;  dU^T = Q' Km^T -----------------------
-            if (tid == 0) {
-                const uint32_t id = tc::idesc_bf16(128, 64);
-                tc::mma_tile(tAP, tc::smem_addr(sm + KQ), 16384, tc::smem_addr(sm + KM), 8192, 128, id, false);
-                tc::mma_tile(tX, tc::smem_addr(sm + RR), 16384, tc::smem_addr(sm + KQ), 16384, 128, id, false);
-                tc::mma_tile(tDU, tc::smem_addr(sm + QQ), 16384, tc::smem_addr(sm + KM), 8192, 128, id, false);
-                tc::mma_commit(&bars[0]);
-            }
-            ++armed[0];
             poll(9);                                            // v, read below
             poll(0);
             if (!meet()) break;
@@ -517,106 +548,132 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             tc::fence_smem_to_async();
             tc::fence_before_sync();
             if (!meet()) break;
-            // ---- B2: U^T = Y^T Tb^T;  dU^T += dO^T P -------------------------------------------------
+            // ---- B2: U^T = Y^T Tb^T;  dU += P^T dO (P and dO read MN-major) ----------------------------
             if (tid == 0) {
                 tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + YT), 16384, false}, tc::Opnd{tc::smem_addr(sm + TB), 8192, false},
                            128, 64, 64, false);
-                tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + DO), 8192, true}, tc::Opnd{tc::smem_addr(sm + PT), 8192, true},
-                           128, 64, 64, true);
+                tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + PT), 8192, true}, tc::Opnd{tc::smem_addr(sm + DO), 16384, true},
+                           64, 128, 64, true);
                 tc::mma_commit(&bars[1]);
             }
             ++armed[1];
             poll(1);
             if (!meet()) break;
-            // ---- E2: U^T -> VV (raw v is consumed), dU^T -> DU -----------------------------------------
+            // ---- E2: U^T -> VV (raw v is consumed), dU rows -> DX ----------------------------------------
             {
-                float r[16], r2[16];
+                float r[16], ua[16], ub[16];
                 tld16(tX + lane_off + cg * 16, r);
-                tld16(tDU + lane_off + cg * 16, r2);
-                twait(r, r2);
+                tld16(tDU + lane_off + cg * 32, ua);            // dU, M = 64: row 16 lq + lane in lanes 0-15
+                tld16(tDU + lane_off + cg * 32 + 16, ub);
+                twait(r, ua, ub);
                 tc::st_sw128_8(sm + VV, 128, jv, cg * 16, r);
                 tc::st_sw128_8(sm + VV, 128, jv, cg * 16 + 8, r + 8);
-                tc::st_sw128_8(sm + DU, 128, jv, cg * 16, r2);
-                tc::st_sw128_8(sm + DU, 128, jv, cg * 16 + 8, r2 + 8);
+                if (lane < 16) {
+                    const int t = 16 * lq + lane, dv0 = cg * 32;
+                    tc::st_sw128_8(sm + DX, 128, t, dv0, ua);
+                    tc::st_sw128_8(sm + DX, 128, t, dv0 + 8, ua + 8);
+                    tc::st_sw128_8(sm + DX, 128, t, dv0 + 16, ub);
+                    tc::st_sw128_8(sm + DX, 128, t, dv0 + 24, ub + 8);
+                }
             }
             csync_mma();
-            // ---- B3: Z^T = dU^T T;  dP = dO U^T (M = 64);  Km' = Q'^T U^T;  dQp^T = R^T dO^T ------------
+            // ---- B3: Z = T^T dU (M = 64, rows t; T and dU read MN-major; 128 columns from tX);
+            //      dP = dO U^T (M = 64);  Km' = Q'^T U^T;  dQp^T = R^T dO^T (dO is then free) ----------------
             if (tid == 0) {
-                tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + DU), 16384, false}, tc::Opnd{tc::smem_addr(sm + TT), 8192, true},
-                           128, 64, 64, false);
-                tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + DO), 8192, false}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
+                tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + TT), 8192, true}, tc::Opnd{tc::smem_addr(sm + DX), 16384, true},
+                           64, 128, 64, false);
+                tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + DO), 16384, false}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
                            64, 64, 128, false);
                 tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + QQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
                            128, 64, 128, false);
-                tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DO), 8192, false},
+                tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DO), 16384, false},
                            128, 64, 128, false);
                 tc::mma_commit(&bars[2]);
             }
             ++armed[2];
             poll(2);
             if (!meet()) break;
-            // ---- E3: Z^T -> ZT (over Q'); dY = diag(beta) Z -> dv rows, -dY^T -> DU; dP -> DP;
+            // ---- E3: Z rows -> QQ (over Q'); dY = diag(beta) Z: -dY rows -> DX; dP -> DP;
             //      sum_t Km Km' for dGamma_L ---------------------------------------------------------------
             {
-                float z[16], a[16], km2[16];
-                tld16(tDY + lane_off + cg * 16, z);
-                tld16(tDU + lane_off + cg * 16, a);             // dP, M = 64
-                tld16(tKM + lane_off + cg * 16, km2);
-                twait(z, a, km2);
-                const int dv = jv;
-                tc::st_sw128_8(sm + QQ, 128, dv, cg * 16, z);
-                tc::st_sw128_8(sm + QQ, 128, dv, cg * 16 + 8, z + 8);
-                __nv_bfloat16 *dvo = static_cast<__nv_bfloat16 *>(p.dv);
-                const int64_t orow = static_cast<int64_t>(I.row0) + I.c0 - I.rho;   // compact row of local row 0
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = cg * 16 + j;
-                    const float y = z[j] * vbeta[t];
-                    if (t < t_end) {
-                        if (t >= t_own)
-                            dvo[((orow + t) * H + I.h) * D + dv] = __float2bfloat16_rn(y);
-                        else
-                            p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + D + dv] = y;
-                    }
-                    z[j] = -y;
-                }
-                tc::st_sw128_8(sm + DU, 128, dv, cg * 16, z);
-                tc::st_sw128_8(sm + DU, 128, dv, cg * 16 + 8, z + 8);
+                float za[16], zb[16], a[16];
+                tld16(tX + lane_off + cg * 32, za);             // Z, M = 64: row 16 lq + lane in lanes 0-15
+                tld16(tX + lane_off + cg * 32 + 16, zb);
+                tld16(tDT + lane_off + cg * 16, a);             // dP, M = 64
+                twait(za, zb, a);
                 if (lane < 16) {
-                    const int t = 16 * lq + lane;
+                    const int t = 16 * lq + lane, dv0 = cg * 32;
+                    // Z rows: rows 0-63 of the K-major [128][64]-atom operand in QQ (rows 64-127: padding)
+                    tc::st_sw128_8(sm + QQ, 128, t, dv0, za);
+                    tc::st_sw128_8(sm + QQ, 128, t, dv0 + 8, za + 8);
+                    tc::st_sw128_8(sm + QQ, 128, t, dv0 + 16, zb);
+                    tc::st_sw128_8(sm + QQ, 128, t, dv0 + 24, zb + 8);
+                    const float bt = vbeta[t];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) { za[j] *= bt; zb[j] *= bt; }
+                    if (t < t_own && t < t_end) {
+                        // a replayed row's dv goes to the replay-gradient buffer in fp32 (rows of
+                        // 3 * 128 + 1 floats: no vector stores); own rows leave from DX below
+                        float *dst = p.rep_grad + (static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + D + dv0;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            dst[j] = za[j];
+                            dst[16 + j] = zb[j];
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) { za[j] = -za[j]; zb[j] = -zb[j]; }
+                    tc::st_sw128_8(sm + DX, 128, t, dv0, za);
+                    tc::st_sw128_8(sm + DX, 128, t, dv0 + 8, za + 8);
+                    tc::st_sw128_8(sm + DX, 128, t, dv0 + 16, zb);
+                    tc::st_sw128_8(sm + DX, 128, t, dv0 + 24, zb + 8);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) a[j] = (cg * 16 + j <= t) ? a[j] : 0.f;
                     tc::st_sw128_8(sm + DP, 64, t, cg * 16, a);
                     tc::st_sw128_8(sm + DP, 64, t, cg * 16 + 8, a + 8);
                 }
+            }
+            {
                 // sum_t Km[t][c] Km'[c][t]
+                float km2[16];
+                tld16(tKM + lane_off + cg * 16, km2);
+                twait1(km2);
                 float acc = 0.f;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) acc += km2[j] * bf(sm + KM + (jv >> 6) * 8192 + sw64(cg * 16 + j, jv & 63));
                 vqs[cg * 128 + jv] = acc;
             }
             csync_mma();
-            // ---- B4: W = Z U^T, D = Z Y^T (M = 128: rows 64-127 read the second Q' atom as padding, so
-            //      row t lands in lane t);  dKp^T = -R^T dY^T -------------------------------------------------
+            // ---- B4: [W D] = Z [U^T Y^T] (M = 128: rows 64-127 of the Z operand are padding, so row t
+            //      lands in lane t, next to A; N = 128: U^T and Y^T are the two 64-column blocks of one
+            //      MN-major operand);  dKp^T = -R^T dY^T ------------------------------------------------------
             if (tid == 0) {
-                tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + QQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
-                           128, 64, 128, false);
-                tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + QQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + YT), 16384, true},
-                           128, 64, 128, false);
-                tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DU), 16384, true},
+                tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + QQ), 16384, false}, tc::Opnd{tc::smem_addr(sm + VV), YT - VV, true},
+                           128, 128, 128, false);
+                tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DX), 16384, false},
                            128, 64, 128, false);
                 tc::mma_commit(&bars[3]);
             }
             ++armed[3];
             if (tid < 128) vdgl[tid] += vqs[tid] + vqs[128 + tid] + vqs[256 + tid] + vqs[384 + tid];
+            // the own rows' dv = -(the bf16 -dY rows in DX), 16 bytes per store, while B4 runs
+            for (int e = tid; e < 64 * 16; e += NC) {
+                const int t = e >> 4, pc = e & 15;
+                if (t < t_own || t >= t_end) continue;
+                const uint4 w = *reinterpret_cast<const uint4 *>(sm + DX + (pc >> 3) * 16384 + t * 128 +
+                                                                 (((pc & 7) ^ (t & 7)) << 4));
+                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dv) +
+                                           ((static_cast<int64_t>(I.row0) + I.c0 + t - I.rho) * H + I.h) * D + pc * 8) =
+                    make_uint4(w.x ^ 0x80008000u, w.y ^ 0x80008000u, w.z ^ 0x80008000u, w.w ^ 0x80008000u);
+            }
             poll(3);
             if (!meet()) break;
             // ---- E4: dM = -strict(W); dA = diag(beta) dM -> WA; dbeta = D[t][t] + rowsum(dM .* A) ----------
             {
                 if (lq < 2) {
                     float w[16], d2[16], a[16];
-                    tld16(tDU + lane_off + cg * 16, w);
-                    tld16(tX + lane_off + cg * 16, d2);
+                    tld16(tX + lane_off + cg * 16, w);
+                    tld16(tDU + lane_off + cg * 16, d2);
                     tld16(tAP + lane_off + cg * 16, a);
                     twait(w, d2, a);
                     const int t = jv;
@@ -638,28 +695,43 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                 if (tid < 64) vdb[tid] = vqs[tid] + vqs[64 + tid] + vqs[128 + tid] + vqs[192 + tid];
             }
             csync_mma();
-            // ---- B6: dQp^T += Km^T dP^T;  dKp^T += Km^T dA^T;  Km' += Kp^T dA + Qp^T dP ------------------
+            // ---- B6: [dQp^T dKp^T] += Km^T [dP; dA]^T (N = 128);  Km' += Kp^T dA + Qp^T dP ----------------
             if (tid == 0) {
-                tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + KM), 8192, true}, tc::Opnd{tc::smem_addr(sm + DP), 8192, false},
-                           128, 64, 64, true);
-                tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + KM), 8192, true}, tc::Opnd{tc::smem_addr(sm + WA), 8192, false},
-                           128, 64, 64, true);
-                tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + KQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + WA), 8192, true},
-                           128, 64, 64, true);
-                tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + KQ) + 8192, 16384, true},
-                           tc::Opnd{tc::smem_addr(sm + DP), 8192, true}, 128, 64, 64, true);
+                tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + KM), 8192, true}, tc::Opnd{tc::smem_addr(sm + DP), 16384, false},
+                           128, 128, 64, true);
+                // Kp^T and Qp^T from their bf16 copies in TMEM (lane = channel, column = row pair), so
+                // the [Kp; Qp] tile is free once B1 is done
+                const uint32_t id = tc::idesc_bf16(128, 64, false, true);
+                const tc::Opnd da{tc::smem_addr(sm + WA), 8192, true}, dp{tc::smem_addr(sm + DP), 8192, true};
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tKM, tPK + kk * 8, tc::opnd_desc(da, kk), id, 1u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tKM, tPK + 32 + kk * 8, tc::opnd_desc(dp, kk), id, 1u);
                 tc::mma_commit(&bars[4]);
             }
             ++armed[4];
             poll(4);
             if (!meet()) break;
             // ---- E6: dq, dk, dgamma per (channel, row); dg = suffix sums + dGamma_L -----------------------
-            //      (two halves of 8 rows, the later half first, so the suffix sums run in one pass)
+            //      (two halves of 8 rows, the later half first, so the suffix sums run in one pass).  The
+            //      rows go out through shared memory, 16 bytes per store: dq over Y^T, dk over [dP; dA],
+            //      then dg over Y^T.
             {
                 const int c = jv;
                 const float m2 = vm2[c], sc = f.scale;
+                const int64_t r0 = (static_cast<int64_t>(I.rptr + I.c0) * H + I.h) * W3 + c;   // replay rows
+                const int gs = H * W3;
                 __nv_bfloat16 *dqs = reinterpret_cast<__nv_bfloat16 *>(sm + YT);
-                __nv_bfloat16 *dks = reinterpret_cast<__nv_bfloat16 *>(sm + DU);
+                __nv_bfloat16 *dks = reinterpret_cast<__nv_bfloat16 *>(sm + DP);
+                auto rows_out = [&](uint32_t from, void *to) {
+                    for (int e = tid; e < 64 * 16; e += NC) {
+                        const int t = e >> 4, pc = e & 15;
+                        if (t < t_own || t >= t_end) continue;
+                        const int64_t row = static_cast<int64_t>(I.row0) + (I.c0 + t - I.rho);
+                        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(to) + (row * H + I.h) * D + pc * 8) =
+                            *reinterpret_cast<const uint4 *>(sm + from + t * 256 + pc * 16);
+                    }
+                };
                 float dgm[16];
                 float run = 0.f;
 #pragma unroll
@@ -667,8 +739,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                     const int cb = cg * 16 + hh * 8;
                     float xq[8], xp[8], xm[8], g2v[8];
                     uint32_t kpk[4], qpk[4];
-                    tld8f(tDT + lane_off + cb, xq);
-                    tld8f(tDY + lane_off + cb, xp);
+                    tld8f(tDY + lane_off + cb, xq);
+                    tld8f(tDT + lane_off + cb, xp);
                     tld8f(tKM + lane_off + cb, xm);
                     tld8f(tGM + lane_off + cb, g2v);
                     tld4(tPK + lane_off + cg * 8 + hh * 4, kpk);
@@ -688,8 +760,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                         dgm[hh * 8 + j] = xq[j] * qp + xp[j] * kp - xm[j] * km;
                         dqs[t * D + c] = __float2bfloat16_rn(dqv);
                         dks[t * D + c] = __float2bfloat16_rn(dkv);
-                        if (t < t_own && t < t_end)
-                            p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + c] = dkv;
+                        if (t < t_own && t < t_end) p.rep_grad[r0 + t * gs] = dkv;
                     }
                     // suffix sums over t within this thread's rows, continuing the later half's
 #pragma unroll
@@ -698,29 +769,21 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                 // then the later quarters' totals
                 vqs[cg * 128 + c] = run;
                 csync();
+                rows_out(YT, p.dq);
+                rows_out(DP, p.dk);
                 float off = vdgl[c];
 #pragma unroll
                 for (int q = 1; q < 4; ++q) off += q > cg ? vqs[q * 128 + c] : 0.f;
-                __nv_bfloat16 *dgs = reinterpret_cast<__nv_bfloat16 *>(sm + DP);
+                csync();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int t = cg * 16 + j;
                     const float x = dgm[j] + off;
-                    dgs[t * D + c] = __float2bfloat16_rn(x);
-                    if (t < t_own && t < t_end)
-                        p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + 2 * D + c] = x;
+                    dqs[t * D + c] = __float2bfloat16_rn(x);
+                    if (t < t_own && t < t_end) p.rep_grad[r0 + t * gs + 2 * D] = x;
                 }
-            }
-            tc::fence_before_sync();
-            csync();
-            for (int e = tid; e < 3 * 64 * 16; e += NC) {
-                const int which = e >> 10, t = (e >> 4) & 63, pc = e & 15;
-                if (t < t_own || t >= t_end) continue;
-                const int64_t row = static_cast<int64_t>(I.row0) + (I.c0 + t - I.rho);
-                void *dst = which == 0 ? p.dq : (which == 1 ? p.dk : p.dg);
-                const uint8_t *srcp = sm + (which == 0 ? YT : (which == 1 ? DU : DP));
-                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(dst) + (row * H + I.h) * D + pc * 8) =
-                    *reinterpret_cast<const uint4 *>(srcp + t * 256 + pc * 16);
+                csync();
+                rows_out(YT, p.dg);
             }
             if (tid < 64) {
                 const int t = tid;
@@ -733,6 +796,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                         p.rep_grad[(static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + 3 * D] = db;
                 }
             }
+            tc::fence_before_sync();
             csync();
             tc::fence_after_sync();
         }

@@ -122,13 +122,6 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" :: "r"(tc::smem_addr(bar)) : "memory");
 }
 
-// D (+)= A B with A (bf16 pairs, one row per lane, 8 columns per 16 K) in TMEM.
-__device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc) : "memory");
-}
 
 struct Maps2 {
     RowMaps q, k, v, g;
@@ -595,7 +588,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
             const uint32_t id = tc::idesc_bf16(128, 64, false, true);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_ta(tW, tR + kk * 8, tc::desc_sw128_mn(tc::smem_addr(sm + KQ) + (kk >> 2) * 16384 + (kk & 3) * 2048, 8192),
+                tc::mma_bf16_ta(tW, tR + kk * 8, tc::desc_sw128_mn(tc::smem_addr(sm + KQ) + (kk >> 2) * 16384 + (kk & 3) * 2048, 8192),
                        id, 1u);
             tc::mma_commit(&bars[2]);
         }
@@ -615,7 +608,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
             const uint32_t id = tc::idesc_bf16(128, 64, false, false);
             const tc::Opnd qp{tc::smem_addr(sm + KQ) + 8192, 16384, false};
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) mma_ta(tW, tR + kk * 8, tc::opnd_desc(qp, kk), id, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16_ta(tW, tR + kk * 8, tc::opnd_desc(qp, kk), id, kk > 0 ? 1u : 0u);
             tc::mma_op(tW, tc::Opnd{tc::smem_addr(sm + VV), 16384, false},
                        tc::Opnd{tc::smem_addr(sm + SC) + 8192, 8192, false}, 128, 64, 64, true);
             tc::mma_op(tS, tc::Opnd{tc::smem_addr(sm + VV), 16384, false}, tc::Opnd{tc::smem_addr(sm + KM), 8192, true},
@@ -971,7 +964,7 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
             const uint32_t id = tc::idesc_bf16(128, 64, false, false);
             const tc::Opnd kmo{tc::smem_addr(sm + KM), 8192, false};
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) mma_ta(tW, tQ + kk * 8, tc::opnd_desc(kmo, kk), id, 1u);
+            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16_ta(tW, tQ + kk * 8, tc::opnd_desc(kmo, kk), id, 1u);
             tc::mma_commit(&bars[1]);
         }
         ++armed[1];

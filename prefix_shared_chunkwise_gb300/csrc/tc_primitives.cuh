@@ -100,6 +100,15 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// D (+)= A B with A in TMEM (bf16 pairs: one row of A per lane, 8 columns per 16 K) and B
+// from shared memory.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // D[M x N] (+)= A[M x K] * B[N x K]^T with both operands K-major SW128 tiles; K is a
 // multiple of 16, atoms of 64 columns placed `a_atom_bytes` / `b_atom_bytes` apart.
 __device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_saddr, uint32_t a_atom_bytes,

@@ -103,3 +103,26 @@ def test_logprob_without_semantic_positions():
     assert logp.numel() == 0
     assert rel_l2(lse.cpu().numpy(), lse_ref) <= 1e-6
     assert float(dz.abs().max()) == 0.0                # no position: no gradient
+
+
+def test_kda_rejects_misaligned_tensors():
+    """Rows move 16 bytes at a time: a q (or dq) that does not start on a 16-byte boundary is
+    refused with HARTS_EINVAL before anything is launched."""
+    from prefix_shared_chunkwise_gb300.api import kda_fwd, kda_bwd
+    from prefix_shared_chunkwise_gb300.synth import make_inputs
+    pl = Plan(np.array([-1], np.int32), np.array([70], np.int64), 64)
+    pl.upload()
+    x = make_inputs(pl.info["C"], 2, 128, 128, "bf16", seed=5, device="cuda")
+    bad = torch.empty(x["q"].numel() + 8, dtype=x["q"].dtype, device="cuda")[1:1 + x["q"].numel()].view(x["q"].shape)
+    bad.copy_(x["q"])
+    with pytest.raises(_lib.HartsError) as e:
+        kda_fwd(pl, bad, x["k"], x["v"], x["g"], x["beta"])
+    assert e.value.rc == -1          # HARTS_EINVAL
+    cs = torch.empty(pl.chunk_state_bytes(2, 128, 128, 1) // 2, dtype=torch.bfloat16, device="cuda")
+    o, states, _, cs = kda_fwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], chunk_states=cs)
+    grads = {n: torch.empty_like(x["q"]) for n in ("dk", "dv", "dg")}
+    grads["dq"] = bad
+    grads["dbeta"] = torch.empty_like(x["beta"])
+    with pytest.raises(_lib.HartsError) as e:
+        kda_bwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], x["W"], states=states, chunk_states=cs, grads=grads)
+    assert e.value.rc == -1          # HARTS_EINVAL
