@@ -90,7 +90,7 @@ BwdWs bwd_ws(const harts_plan *P, int32_t H, int32_t D, bool tc) {
     BwdWs w{};
     w.ds_init = 0;
     w.rep_grad = align_up(sizeof(float) * size_t(P->info.n_seq) * H * D * D);
-    w.dchunk = w.rep_grad + align_up(sizeof(float) * size_t(P->info.R) * H * (3 * D + 1));
+    w.dchunk = w.rep_grad + align_up(sizeof(float) * size_t(P->info.R) * H * rep_width(D));
     w.total = w.dchunk + (tc ? align_up(size_t(2) * size_t(P->info.n_chunks) * H * D * D) : 0);
     return w;
 }

@@ -16,6 +16,10 @@ enum : int32_t {
     kDevErrTimeout = 3,      // a bounded wait ran out
 };
 
+// Floats per replay-gradient row: dk, dv, dg (D each) and dbeta, padded to 16 bytes so that
+// rows can be written with 16-byte stores.
+__host__ __device__ constexpr int rep_width(int D) { return 3 * D + 4; }
+
 // Largest |exponent| the reference-row factorisation may form (exp(85) < FLT_MAX).
 constexpr float kMaxExpArg = 85.f;
 
@@ -36,7 +40,7 @@ struct BwdParams {
     void *dq, *dk, *dv, *dg, *dbeta;
     float *dh0;
     float *ds_init;          // [n_seq, H, D, D] gradient w.r.t. each sequence's initial state
-    float *rep_grad;         // [R, H, 3*D+1]: dk, dv, dg, dbeta of every replay occurrence
+    float *rep_grad;         // [R, H, rep_width(D)]: dk, dv, dg, dbeta of every replay occurrence
     void *dchunk;            // [n_chunks, H, D, D] bf16: dL/dS^T at every chunk end (tensor-core path)
 };
 

@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
     const FwdParams &f = p.f;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lq = warp & 3, cg = (warp >> 2) & 3;
     const int H = f.H;
-    const int W3 = 3 * D + 1;
+    const int W3 = rep_width(D);
     const int jv = lq * 32 + lane;                  // TMEM lane of this thread
     const uint32_t lane_off = static_cast<uint32_t>(lq * 32) << 16;
     float *vqs = reinterpret_cast<float *>(sm + VQS), *vmr = reinterpret_cast<float *>(sm + VMR);
@@ -612,13 +612,14 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
 #pragma unroll
                     for (int j = 0; j < 16; ++j) { za[j] *= bt; zb[j] *= bt; }
                     if (t < t_own && t < t_end) {
-                        // a replayed row's dv goes to the replay-gradient buffer in fp32 (rows of
-                        // 3 * 128 + 1 floats: no vector stores); own rows leave from DX below
-                        float *dst = p.rep_grad + (static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + D + dv0;
+                        // a replayed row's dv goes to the replay-gradient buffer in fp32; own rows
+                        // leave from DX below
+                        float4 *dst = reinterpret_cast<float4 *>(
+                            p.rep_grad + (static_cast<int64_t>(I.rptr + I.c0 + t) * H + I.h) * W3 + D + dv0);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            dst[j] = za[j];
-                            dst[16 + j] = zb[j];
+                        for (int q = 0; q < 4; ++q) {
+                            dst[q] = make_float4(za[4 * q], za[4 * q + 1], za[4 * q + 2], za[4 * q + 3]);
+                            dst[4 + q] = make_float4(zb[4 * q], zb[4 * q + 1], zb[4 * q + 2], zb[4 * q + 3]);
                         }
                     }
 #pragma unroll

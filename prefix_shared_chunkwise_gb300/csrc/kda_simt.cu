@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(256) kda_bwd_simt(BwdParams p, PlanDev pd, int
                     const int64_t o = (row * H + h) * D + c;
                     st_out(dq, o, dqq); st_out(dk, o, dkk); st_out(dg, o, run);
                 } else {
-                    float *rg = p.rep_grad + (static_cast<int64_t>(pd.seq_rptr[seq] + r) * H + h) * (3 * D + 1);
+                    float *rg = p.rep_grad + (static_cast<int64_t>(pd.seq_rptr[seq] + r) * H + h) * rep_width(D);
                     rg[c] = dkk; rg[2 * D + c] = run;
                 }
             }
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(256) kda_bwd_simt(BwdParams p, PlanDev pd, int
                 const int64_t row = local_row(pd, seq, rho, L, r);
                 st_out(dv, (row * H + h) * D + j, x);
             } else {
-                p.rep_grad[(static_cast<int64_t>(pd.seq_rptr[seq] + r) * H + h) * (3 * D + 1) + D + j] = x;
+                p.rep_grad[(static_cast<int64_t>(pd.seq_rptr[seq] + r) * H + h) * rep_width(D) + D + j] = x;
             }
         }
         for (int t = tid; t < BC; t += nth) {
@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(256) kda_bwd_simt(BwdParams p, PlanDev pd, int
                 const int64_t row = local_row(pd, seq, rho, L, r);
                 st_out(db, row * H + h, dbet[t]);
             } else {
-                p.rep_grad[(static_cast<int64_t>(pd.seq_rptr[seq] + r) * H + h) * (3 * D + 1) + 3 * D] = dbet[t];
+                p.rep_grad[(static_cast<int64_t>(pd.seq_rptr[seq] + r) * H + h) * rep_width(D) + 3 * D] = dbet[t];
             }
         }
     }
@@ -499,7 +499,7 @@ template <typename T>
 __global__ void fold_replay_grads(BwdParams p, PlanDev pd, int D) {
     const int32_t f = blockIdx.x, h = blockIdx.y, H = p.f.H;
     const int32_t row = pd.fold_rows[f];
-    const int W = 3 * D + 1;
+    const int W = rep_width(D);
     T *dk = static_cast<T *>(p.dk), *dv = static_cast<T *>(p.dv), *dg = static_cast<T *>(p.dg),
       *db = static_cast<T *>(p.dbeta);
     for (int e = threadIdx.x; e < W; e += blockDim.x) {
