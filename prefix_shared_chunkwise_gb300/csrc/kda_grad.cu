@@ -217,8 +217,10 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
     using namespace g2;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    // mbarriers: 0-4 product batches B1, B2, B3, B4, B6; 6 q, 7 k, 8 g, 9 v, 10 dO, 11 T, 12 R, 13 Q'
-    __shared__ uint64_t bars[14];
+    // mbarriers: product batches 0 B1, 1 B2, 2 B3a, 5 B3b, 3 B4a, 14 B4b, 4 B6; copies 6 q, 7 k,
+    // 8 g, 9 v, 10 dO, 11 T, 12 R, 13 Q'; rdy: the compute warps' operands for B1, B2, B3, B4, B6
+    __shared__ uint64_t bars[15];
+    __shared__ uint64_t rdy[5];
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
     __shared__ int s_rows[4][64];                   // each load warp's row table
@@ -237,7 +239,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
     float *vdb = reinterpret_cast<float *>(sm + VDB), *vdgl = reinterpret_cast<float *>(sm + VDGL);
 
     if (tid == 0) {
-        for (int i = 0; i < 14; ++i) tc::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 15; ++i) tc::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 5; ++i) tc::mbar_init(&rdy[i], 1);
         tc::fence_mbar_init();
         s_fail = 0;
     }
@@ -247,14 +250,17 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
     const uint32_t tm = s_tmem;
     const uint32_t tAP = tm, tX = tm + 64, tDU = tm + 128, tDY = tm + 192, tDT = tm + 256, tKM = tm + 320,
                    tGM = tm + 384, tPK = tm + 448;
-    int armed[14] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+    int armed[15] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
     int32_t cur_seq = 0, cur_h = 0;
 
     if (warp >= NC / 32) {
         // ================= load warps: every copy of the next item, issued as its buffer frees ====
         // Load warp 0: g, T and the two records (and the item's indices and beta for the compute
-        // warps); 1: dO; 2: q and v; 3: k.  Each walks the items on its own, so that one warp's
+        // warps); 2: q and v; 3: k and dO.  Each walks the items on its own, so that one warp's
         // row gathers (replay rows, a sequence's last partial chunk) never hold up another's copies.
+        // Load warp 1 issues the product batches instead (lane 0), as the compute warps signal
+        // that their operands are written, so that no compute warp stalls while the tensor
+        // pipe's queue drains.
         const int lw = warp - NC / 32;
         int *rows = s_rows[lw];
         const uint16_t *beta = static_cast<const uint16_t *>(f.beta);
@@ -304,6 +310,71 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                 break;
             }
         };
+        // the product batches of every item, in order, each once the compute warps signal that
+        // its operands are in place (lane 0 of load warp 1)
+        auto issue_products = [&]() {
+            const uint32_t a = tc::smem_addr(sm);
+            for (uint32_t n = 0; static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x < n_items; ++n) {
+                const uint32_t ph = n & 1;
+                // B1: [A; P] = [Kp; Qp] Km^T;  X = R Kp^T;  dU = Km Q'^T (M = 64, rows t)
+                if (!poll_bar(&rdy[0], ph, &s_fail)) return;
+                tc::fence_after_sync();
+                {
+                    const uint32_t id = tc::idesc_bf16(128, 64);
+                    tc::mma_tile(tAP, a + KQ, 16384, a + KM, 8192, 128, id, false);
+                    tc::mma_tile(tX, a + RR, 16384, a + KQ, 16384, 128, id, false);
+                    tc::mma_op(tDU, tc::Opnd{a + KM, 8192, false}, tc::Opnd{a + QQ, 16384, false}, 64, 128, 128, false);
+                    tc::mma_commit(&bars[0]);
+                    ++armed[0];
+                }
+                // B2: U^T = Y^T Tb^T;  dU += P^T dO (P and dO read MN-major)
+                if (!poll_bar(&rdy[1], ph, &s_fail)) return;
+                tc::fence_after_sync();
+                tc::mma_op(tX, tc::Opnd{a + YT, 16384, false}, tc::Opnd{a + TB, 8192, false}, 128, 64, 64, false);
+                tc::mma_op(tDU, tc::Opnd{a + PT, 8192, true}, tc::Opnd{a + DO, 16384, true}, 64, 128, 64, true);
+                tc::mma_commit(&bars[1]);
+                ++armed[1];
+                // B3a: Z = T^T dU (M = 64; T and dU read MN-major; 128 columns from tX);  dP = dO U^T
+                // (M = 64);  B3b: Km' = Q'^T U^T;  dQp^T = R^T dO^T
+                if (!poll_bar(&rdy[2], ph, &s_fail)) return;
+                tc::fence_after_sync();
+                tc::mma_op(tX, tc::Opnd{a + TT, 8192, true}, tc::Opnd{a + DX, 16384, true}, 64, 128, 64, false);
+                tc::mma_op(tDT, tc::Opnd{a + DO, 16384, false}, tc::Opnd{a + VV, 16384, true}, 64, 64, 128, false);
+                tc::mma_commit(&bars[2]);
+                ++armed[2];
+                tc::mma_op(tKM, tc::Opnd{a + QQ, 16384, true}, tc::Opnd{a + VV, 16384, true}, 128, 64, 128, false);
+                tc::mma_op(tDY, tc::Opnd{a + RR, 16384, true}, tc::Opnd{a + DO, 16384, false}, 128, 64, 128, false);
+                tc::mma_commit(&bars[5]);
+                ++armed[5];
+                // B4a: [W D] = Z [U^T Y^T] (M = 128: rows 64-127 of the Z operand are padding, so row t
+                // lands in lane t, next to A; N = 128: U^T and Y^T are the two 64-column blocks of one
+                // MN-major operand);  B4b: dKp^T = -R^T dY^T
+                if (!poll_bar(&rdy[3], ph, &s_fail)) return;
+                tc::fence_after_sync();
+                tc::mma_op(tX, tc::Opnd{a + QQ, 16384, false}, tc::Opnd{a + VV, YT - VV, true}, 128, 128, 128, false);
+                tc::mma_commit(&bars[3]);
+                ++armed[3];
+                tc::mma_op(tDT, tc::Opnd{a + RR, 16384, true}, tc::Opnd{a + DX, 16384, false}, 128, 64, 128, false);
+                tc::mma_commit(&bars[14]);
+                ++armed[14];
+                // B6: [dQp^T dKp^T] += Km^T [dP; dA]^T (N = 128);  Km' += Kp^T dA + Qp^T dP with Kp^T
+                // and Qp^T from their bf16 copies in TMEM (lane = channel, column = row pair), so the
+                // [Kp; Qp] tile is free once B1 is done
+                if (!poll_bar(&rdy[4], ph, &s_fail)) return;
+                tc::fence_after_sync();
+                tc::mma_op(tDY, tc::Opnd{a + KM, 8192, true}, tc::Opnd{a + DP, 16384, false}, 128, 128, 64, true);
+                {
+                    const uint32_t id = tc::idesc_bf16(128, 64, false, true);
+                    const tc::Opnd da{a + WA, 8192, true}, dp{a + DP, 8192, true};
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tKM, tPK + kk * 8, tc::opnd_desc(da, kk), id, 1u);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tKM, tPK + 32 + kk * 8, tc::opnd_desc(dp, kk), id, 1u);
+                }
+                tc::mma_commit(&bars[4]);
+                ++armed[4];
+            }
+        };
         // lane 0 waits for a product batch of the compute warps (its operands are then free)
         auto wait_free = [&](int b, uint32_t ph) -> bool {
             int ok = 1;
@@ -317,41 +388,40 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             const Item it = item_of(pd, chunk_begin, H, item);
             rows_of(it, 0u);
             if (lw == 0) { stage(2, it); stage(5, it); stage(6, it); stage(7, it); }
-            else if (lw == 1) stage(4, it);
             else if (lw == 2) { stage(0, it); stage(3, it); }
-            else stage(1, it);
+            else if (lw == 3) { stage(1, it); stage(4, it); }
         }
-        for (uint32_t n = 0; item < n_items; item += gridDim.x, ++n) {
-            const int32_t nxt = item + gridDim.x;
-            if (nxt >= n_items) break;
-            const uint32_t ph = n & 1;
-            const Item nx = item_of(pd, chunk_begin, H, nxt);
-            rows_of(nx, n + 1);
-            if (lw == 0) {
-                if (!wait_free(1, ph)) break;                // B2 done: Tb and P (TB..PT) are free
-                stage(2, nx);
-                if (!wait_free(2, ph)) break;                // B3 done: T is free
-                stage(5, nx);
-                if (!wait_free(3, ph)) break;                // B4 done: R and Q' (Z^T) are free
-                stage(6, nx);
-                stage(7, nx);
-            } else if (lw == 1) {
-                if (!wait_free(2, ph)) break;                // B3 done: the dO rows are free
-                stage(4, nx);
-            } else {
-                if (!wait_free(0, ph)) break;                // B1 done: the [Kp; Qp] tile is free
-                stage(lw == 2 ? 0 : 1, nx);
-                if (lw == 2) {
-                    if (!wait_free(3, ph)) break;            // B4 done: U^T (over v) is free
-                    stage(3, nx);
+        if (lw == 1) {
+            if (lane == 0) issue_products();
+        } else {
+            for (uint32_t n = 0; item < n_items; item += gridDim.x, ++n) {
+                const int32_t nxt = item + gridDim.x;
+                if (nxt >= n_items) break;
+                const uint32_t ph = n & 1;
+                const Item nx = item_of(pd, chunk_begin, H, nxt);
+                rows_of(nx, n + 1);
+                if (lw == 0) {
+                    if (!wait_free(1, ph)) break;            // B2 done: Tb and P (TB..PT) are free
+                    stage(2, nx);
+                    if (!wait_free(2, ph)) break;            // B3a done: T is free
+                    stage(5, nx);
+                    if (!wait_free(14, ph)) break;           // B4b done: R and Q' (then Z) are free
+                    stage(6, nx);
+                    stage(7, nx);
+                } else {
+                    if (!wait_free(0, ph)) break;            // B1 done: the [Kp; Qp] tile is free
+                    stage(lw == 2 ? 0 : 1, nx);
+                    if (!wait_free(lw == 2 ? 3 : 5, ph)) break;   // B4a: U^T (over v) / B3b: dO rows
+                    stage(lw == 2 ? 3 : 4, nx);
                 }
             }
         }
         // every copy issued lands before shared memory is released
         tc::cp_async_wait_all();
         __syncwarp();
+        // (the issuer: every product batch it issued completes before TMEM is released)
         if (lane == 0 && *reinterpret_cast<volatile int *>(&s_fail))
-            for (int i = 6; i < 14; ++i)
+            for (int i = 0; i < 15; ++i)
                 if (armed[i] > 0 && !tc::mbar_wait(&bars[i], (armed[i] - 1) & 1, 200000000LL))
                     dev_error(pd, kDevErrTimeout, -1, i);
     } else {
@@ -455,15 +525,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             tc::fence_before_sync();
             if (!meet()) break;
             // ---- B1: [A; P] = [Kp; Qp] Km^T;  X = R Kp^T;  dU = Km Q'^T (M = 64, rows t) ---------------
-            if (tid == 0) {
-                const uint32_t id = tc::idesc_bf16(128, 64);
-                tc::mma_tile(tAP, tc::smem_addr(sm + KQ), 16384, tc::smem_addr(sm + KM), 8192, 128, id, false);
-                tc::mma_tile(tX, tc::smem_addr(sm + RR), 16384, tc::smem_addr(sm + KQ), 16384, 128, id, false);
-                tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + KM), 8192, false}, tc::Opnd{tc::smem_addr(sm + QQ), 16384, false},
-                           64, 128, 128, false);
-                tc::mma_commit(&bars[0]);
-            }
-            ++armed[0];
+            if (tid == 0) mbar_arrive_one(&rdy[0]);         // operands written: the issuer goes
             // ---- while B1 runs: colsum(Q' .* R) (dGamma_L's first term); Tb = T diag(beta) -------
             {
                 // warp w: logical 8-column chunk w (atom w / 8) of every row; lane: rows lane + 32 i
@@ -549,14 +611,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             tc::fence_before_sync();
             if (!meet()) break;
             // ---- B2: U^T = Y^T Tb^T;  dU += P^T dO (P and dO read MN-major) ----------------------------
-            if (tid == 0) {
-                tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + YT), 16384, false}, tc::Opnd{tc::smem_addr(sm + TB), 8192, false},
-                           128, 64, 64, false);
-                tc::mma_op(tDU, tc::Opnd{tc::smem_addr(sm + PT), 8192, true}, tc::Opnd{tc::smem_addr(sm + DO), 16384, true},
-                           64, 128, 64, true);
-                tc::mma_commit(&bars[1]);
-            }
-            ++armed[1];
+            if (tid == 0) mbar_arrive_one(&rdy[1]);         // operands written: the issuer goes
             poll(1);
             if (!meet()) break;
             // ---- E2: U^T -> VV (raw v is consumed), dU rows -> DX ----------------------------------------
@@ -579,18 +634,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             csync_mma();
             // ---- B3: Z = T^T dU (M = 64, rows t; T and dU read MN-major; 128 columns from tX);
             //      dP = dO U^T (M = 64);  Km' = Q'^T U^T;  dQp^T = R^T dO^T (dO is then free) ----------------
-            if (tid == 0) {
-                tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + TT), 8192, true}, tc::Opnd{tc::smem_addr(sm + DX), 16384, true},
-                           64, 128, 64, false);
-                tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + DO), 16384, false}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
-                           64, 64, 128, false);
-                tc::mma_op(tKM, tc::Opnd{tc::smem_addr(sm + QQ), 16384, true}, tc::Opnd{tc::smem_addr(sm + VV), 16384, true},
-                           128, 64, 128, false);
-                tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DO), 16384, false},
-                           128, 64, 128, false);
-                tc::mma_commit(&bars[2]);
-            }
-            ++armed[2];
+            if (tid == 0) mbar_arrive_one(&rdy[2]);         // operands written: the issuer goes
             poll(2);
             if (!meet()) break;
             // ---- E3: Z rows -> QQ (over Q'); dY = diag(beta) Z: -dY rows -> DX; dP -> DP;
@@ -634,6 +678,8 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                     tc::st_sw128_8(sm + DP, 64, t, cg * 16 + 8, a + 8);
                 }
             }
+            poll(5);                                            // B3b: Km'
+            if (!meet()) break;
             {
                 // sum_t Km[t][c] Km'[c][t]
                 float km2[16];
@@ -648,14 +694,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             // ---- B4: [W D] = Z [U^T Y^T] (M = 128: rows 64-127 of the Z operand are padding, so row t
             //      lands in lane t, next to A; N = 128: U^T and Y^T are the two 64-column blocks of one
             //      MN-major operand);  dKp^T = -R^T dY^T ------------------------------------------------------
-            if (tid == 0) {
-                tc::mma_op(tX, tc::Opnd{tc::smem_addr(sm + QQ), 16384, false}, tc::Opnd{tc::smem_addr(sm + VV), YT - VV, true},
-                           128, 128, 128, false);
-                tc::mma_op(tDT, tc::Opnd{tc::smem_addr(sm + RR), 16384, true}, tc::Opnd{tc::smem_addr(sm + DX), 16384, false},
-                           128, 64, 128, false);
-                tc::mma_commit(&bars[3]);
-            }
-            ++armed[3];
+            if (tid == 0) mbar_arrive_one(&rdy[3]);         // operands written: the issuer goes
             if (tid < 128) vdgl[tid] += vqs[tid] + vqs[128 + tid] + vqs[256 + tid] + vqs[384 + tid];
             // the own rows' dv = -(the bf16 -dY rows in DX), 16 bytes per store, while B4 runs
             for (int e = tid; e < 64 * 16; e += NC) {
@@ -697,20 +736,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             }
             csync_mma();
             // ---- B6: [dQp^T dKp^T] += Km^T [dP; dA]^T (N = 128);  Km' += Kp^T dA + Qp^T dP ----------------
-            if (tid == 0) {
-                tc::mma_op(tDY, tc::Opnd{tc::smem_addr(sm + KM), 8192, true}, tc::Opnd{tc::smem_addr(sm + DP), 16384, false},
-                           128, 128, 64, true);
-                // Kp^T and Qp^T from their bf16 copies in TMEM (lane = channel, column = row pair), so
-                // the [Kp; Qp] tile is free once B1 is done
-                const uint32_t id = tc::idesc_bf16(128, 64, false, true);
-                const tc::Opnd da{tc::smem_addr(sm + WA), 8192, true}, dp{tc::smem_addr(sm + DP), 8192, true};
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tKM, tPK + kk * 8, tc::opnd_desc(da, kk), id, 1u);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_ta(tKM, tPK + 32 + kk * 8, tc::opnd_desc(dp, kk), id, 1u);
-                tc::mma_commit(&bars[4]);
-            }
-            ++armed[4];
+            if (tid == 0) mbar_arrive_one(&rdy[4]);         // operands written: the issuer goes
             poll(4);
             if (!meet()) break;
             // ---- E6: dq, dk, dgamma per (channel, row); dg = suffix sums + dGamma_L -----------------------
@@ -801,14 +827,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             csync();
             tc::fence_after_sync();
         }
-        // the last product batch armed on each barrier completes before TMEM and shared memory
-        // are released (batches complete in order)
-        if (tid == 0 && *reinterpret_cast<volatile int *>(&s_fail)) {
-            dev_error(pd, kDevErrTimeout, cur_seq, cur_h);
-            for (int i = 0; i < 5; ++i)
-                if (armed[i] > 0 && !tc::mbar_wait(&bars[i], (armed[i] - 1) & 1, 200000000LL))
-                    dev_error(pd, kDevErrTimeout, cur_seq, cur_h);
-        }
+        if (tid == 0 && *reinterpret_cast<volatile int *>(&s_fail)) dev_error(pd, kDevErrTimeout, cur_seq, cur_h);
     }
     // ---- drain --------------------------------------------------------------------------------------
     tc::fence_before_sync();
