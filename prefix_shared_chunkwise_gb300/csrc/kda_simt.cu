@@ -497,20 +497,33 @@ __global__ void __launch_bounds__(256) kda_bwd_simt(BwdParams p, PlanDev pd, int
 // replayed row, occurrences are summed in ascending occurrence order, then added.
 template <typename T>
 __global__ void fold_replay_grads(BwdParams p, PlanDev pd, int D) {
-    const int32_t f = blockIdx.x, h = blockIdx.y, H = p.f.H;
+    // one block per ancestor row that replayed rows copy, all heads; each thread sums 4
+    // consecutive floats of a head's replay-gradient rows over the row's occurrences (in
+    // ascending occurrence order) and adds them to the row's dk, dv, dg, dbeta
+    const int32_t f = blockIdx.x, H = p.f.H;
     const int32_t row = pd.fold_rows[f];
-    const int W = rep_width(D);
+    const int W = rep_width(D), W4 = W / 4;
+    const int32_t j0 = pd.fold_ptr[f], j1 = pd.fold_ptr[f + 1];
     T *dk = static_cast<T *>(p.dk), *dv = static_cast<T *>(p.dv), *dg = static_cast<T *>(p.dg),
       *db = static_cast<T *>(p.dbeta);
-    for (int e = threadIdx.x; e < W; e += blockDim.x) {
-        float acc = 0.f;
-        for (int32_t j = pd.fold_ptr[f]; j < pd.fold_ptr[f + 1]; ++j)
-            acc += p.rep_grad[(static_cast<int64_t>(pd.fold_occ[j]) * H + h) * W + e];
+    for (int u = threadIdx.x; u < H * W4; u += blockDim.x) {
+        const int h = u / W4, e4 = u - h * W4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int32_t j = j0; j < j1; ++j) {
+            const float4 x = reinterpret_cast<const float4 *>(
+                p.rep_grad + (static_cast<int64_t>(pd.fold_occ[j]) * H + h) * W)[e4];
+            acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+        }
         const int64_t rh = static_cast<int64_t>(row) * H + h;
-        if (e < D) st_out(dk, rh * D + e, ld_in(dk, rh * D + e) + acc);
-        else if (e < 2 * D) st_out(dv, rh * D + e - D, ld_in(dv, rh * D + e - D) + acc);
-        else if (e < 3 * D) st_out(dg, rh * D + e - 2 * D, ld_in(dg, rh * D + e - 2 * D) + acc);
-        else st_out(db, rh, ld_in(db, rh) + acc);
+        const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = 4 * e4 + i;
+            if (e < D) st_out(dk, rh * D + e, ld_in(dk, rh * D + e) + a[i]);
+            else if (e < 2 * D) st_out(dv, rh * D + e - D, ld_in(dv, rh * D + e - D) + a[i]);
+            else if (e < 3 * D) st_out(dg, rh * D + e - 2 * D, ld_in(dg, rh * D + e - 2 * D) + a[i]);
+            else if (e == 3 * D) st_out(db, rh, ld_in(db, rh) + a[i]);
+        }
     }
 }
 
@@ -594,9 +607,8 @@ cudaError_t simt_bwd_round(int dtype, int BC, const BwdParams &p, const PlanDev 
 cudaError_t bwd_finish(int dtype, const BwdParams &p, const PlanDev &pd, cudaStream_t st) {
     const int D = p.f.D, H = p.f.H;
     if (pd.n_fold > 0) {
-        dim3 grid(pd.n_fold, H);
-        if (dtype == HARTS_FP32) fold_replay_grads<float><<<grid, 128, 0, st>>>(p, pd, D);
-        else fold_replay_grads<__nv_bfloat16><<<grid, 128, 0, st>>>(p, pd, D);
+        if (dtype == HARTS_FP32) fold_replay_grads<float><<<pd.n_fold, 256, 0, st>>>(p, pd, D);
+        else fold_replay_grads<__nv_bfloat16><<<pd.n_fold, 256, 0, st>>>(p, pd, D);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
