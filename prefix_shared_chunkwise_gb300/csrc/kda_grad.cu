@@ -217,7 +217,9 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
     using namespace g2;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
-    // mbarriers: product batches 0 B1, 1 B2, 2 B3a, 5 B3b, 3 B4a, 14 B4b, 4 B6; copies 6 q, 7 k,
+    // mbarriers: product batches 0 B1, 1 B2, 2 B3a, 5 B3b, 3 B4a, 14 B4b, 4 B6 (each of the
+    // compute warps' phases waits only for the batch whose results it reads, and writes no tile
+    // a batch still in flight reads); copies 6 q, 7 k,
     // 8 g, 9 v, 10 dO, 11 T, 12 R, 13 Q'; rdy: the compute warps' operands for B1, B2, B3, B4, B6
     __shared__ uint64_t bars[15];
     __shared__ uint64_t rdy[5];
@@ -335,14 +337,15 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                 tc::mma_commit(&bars[1]);
                 ++armed[1];
                 // B3a: Z = T^T dU (M = 64; T and dU read MN-major; 128 columns from tX);  dP = dO U^T
-                // (M = 64);  B3b: Km' = Q'^T U^T;  dQp^T = R^T dO^T
+                // (M = 64);  Km' = Q'^T U^T (the last read of Q': Z overwrites it once B3a is done);
+                // B3b: dQp^T = R^T dO^T
                 if (!poll_bar(&rdy[2], ph, &s_fail)) return;
                 tc::fence_after_sync();
                 tc::mma_op(tX, tc::Opnd{a + TT, 8192, true}, tc::Opnd{a + DX, 16384, true}, 64, 128, 64, false);
                 tc::mma_op(tDT, tc::Opnd{a + DO, 16384, false}, tc::Opnd{a + VV, 16384, true}, 64, 64, 128, false);
+                tc::mma_op(tKM, tc::Opnd{a + QQ, 16384, true}, tc::Opnd{a + VV, 16384, true}, 128, 64, 128, false);
                 tc::mma_commit(&bars[2]);
                 ++armed[2];
-                tc::mma_op(tKM, tc::Opnd{a + QQ, 16384, true}, tc::Opnd{a + VV, 16384, true}, 128, 64, 128, false);
                 tc::mma_op(tDY, tc::Opnd{a + RR, 16384, true}, tc::Opnd{a + DO, 16384, false}, 128, 64, 128, false);
                 tc::mma_commit(&bars[5]);
                 ++armed[5];
@@ -678,8 +681,6 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                     tc::st_sw128_8(sm + DP, 64, t, cg * 16 + 8, a + 8);
                 }
             }
-            poll(5);                                            // B3b: Km'
-            if (!meet()) break;
             {
                 // sum_t Km[t][c] Km'[c][t]
                 float km2[16];
