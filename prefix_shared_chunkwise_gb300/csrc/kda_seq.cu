@@ -107,21 +107,6 @@ __device__ __forceinline__ void mma16x8x8(float (&d)[4], const uint32_t (&a)[4],
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-__device__ __forceinline__ float2 ld_bf2(const uint8_t *p) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
-}
-__device__ __forceinline__ void st_bf2(uint8_t *p, float a, float b) {
-    *reinterpret_cast<uint32_t *>(p) = tc::pack_bf16(a, b);
-}
-
-__device__ __forceinline__ void mbar_arrive1(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(tc::smem_addr(bar)) : "memory");
-}
-// The barrier's current phase also waits for this thread's earlier cp.async copies.
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" :: "r"(tc::smem_addr(bar)) : "memory");
-}
-
 
 struct Maps2 {
     RowMaps q, k, v, g;
