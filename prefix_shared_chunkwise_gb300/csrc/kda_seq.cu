@@ -238,10 +238,8 @@ __device__ __forceinline__ void invert64(float *F) {
             for (int j = 0; j < i; ++j) a[j & 3] += F[fx(r, 16 * b + j)] * col[j];
             col[i] = i < s ? 0.f : (i == s ? 1.f : -((a[0] + a[1]) + (a[2] + a[3])));
         }
-    }
-    __syncthreads();
-    if (tid < 64) {
-        const int b = tid >> 4, s = tid & 15;
+        // a block's 16 columns are one half-warp's: the warp's reads finish before its writes
+        __syncwarp();
 #pragma unroll
         for (int i = 0; i < 16; ++i) F[fx(16 * b + i, 16 * b + s)] = col[i];
     }
