@@ -220,6 +220,20 @@ __device__ __forceinline__ void sync_mma() {
     tc::fence_after_sync();
 }
 
+// Thread 0 waits for a barrier phase (bounded) without a block barrier of its own; the next
+// sync_check / sync_mma_check publishes the outcome, so several waits share one barrier.
+__device__ __forceinline__ void poll0(uint64_t *bar, uint32_t phase, int *s_fail) {
+    if (threadIdx.x == 0 && *reinterpret_cast<volatile int *>(s_fail) == 0 && !tc::mbar_wait(bar, phase)) *s_fail = 1;
+}
+__device__ __forceinline__ bool sync_check(int *s_fail) {
+    __syncthreads();
+    return *reinterpret_cast<volatile int *>(s_fail) == 0;
+}
+__device__ __forceinline__ bool sync_mma_check(int *s_fail) {
+    sync_mma();
+    return *reinterpret_cast<volatile int *>(s_fail) == 0;
+}
+
 // In-place inversion of the unit lower-triangular I + M held (M strictly lower) in the fp32
 // scratch F.  The four diagonal 16 x 16 blocks by forward substitution (one column per
 // thread, fp32); then the blocks below them by T_ij = -T_ii (M_ij T_jj): first the 16-row
@@ -471,7 +485,9 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
         const int nv = nv_of(ci);
         const bool more = ci + 1 < nch, last = !more;
         // ---- pass B: scaled operands Kp, Qp (in place over raw k, q), Km ------------------
-        if (!wait_data(&bars[5], ph, &s_fail) || !wait_data(&bars[6], ph, &s_fail)) break;
+        poll0(&bars[5], ph, &s_fail);
+        poll0(&bars[6], ph, &s_fail);
+        if (!sync_check(&s_fail)) break;
         chunk_pass_b(sm + KQ, sm + GP, sm + KM, vqs, reinterpret_cast<const float *>(sm + VM) + b * 128, p.scale);
         if (more) braw = rows_of(ci + 1);
         sync_mma();
@@ -569,8 +585,8 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
                                tc::pack_bf16(-r[8 * q + 4], -r[8 * q + 5]), tc::pack_bf16(-r[8 * q + 6], -r[8 * q + 7]));
             }
         }
-        sync_mma();
-        if (!wait_data(&bars[7], ph, &s_fail)) break;     // this chunk's v
+        poll0(&bars[7], ph, &s_fail);                      // this chunk's v
+        if (!sync_mma_check(&s_fail)) break;
         if (tid == 0) {
             // U^T = V^T Tb^T - R (Kp^T Tb^T)
             tc::mma_op(tW, tc::Opnd{tc::smem_addr(sm + VV), 8192, true}, tc::Opnd{tc::smem_addr(sm + SC), 8192, false},
@@ -909,9 +925,10 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
             if (slot) --sp;
         }
         // ---- pass B: Kp, Qp in place, Km over g; Tb = T diag(beta) in place -------------------
-        if (!(ok = wait_data(&bars[5], ph, &s_fail))) break;
-        if (!(ok = wait_data(&bars[6], ph, &s_fail))) break;
-        if (!(ok = wait_data(&bars[8], ph, &s_fail))) break;
+        poll0(&bars[5], ph, &s_fail);
+        poll0(&bars[6], ph, &s_fail);
+        poll0(&bars[8], ph, &s_fail);
+        if (!(ok = sync_check(&s_fail))) break;
         chunk_pass_b(sm + KQ, sm + KM, sm + KM, vqs, reinterpret_cast<const float *>(sm + VM) + b * 128, f.scale);
         {
             const int t = tid >> 2, q = tid & 3;             // row t, 16-column quarter q of T
@@ -945,8 +962,8 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
 #pragma unroll
             for (int j = 0; j < 32; j += 8) tc::st_sw128_8(sm + PP, 64, tp, ch * 32 + j, pv + j);
         }
-        sync_mma();
-        if (!(ok = wait_data(&bars[7], ph, &s_fail))) break;     // dO
+        poll0(&bars[7], ph, &s_fail);                      // dO
+        if (!(ok = sync_mma_check(&s_fail))) break;
         if (tid == 0) {
             // dU^T = dO^T P + Q' Km^T
             tc::mma_op(tW, tc::Opnd{tc::smem_addr(sm + DO), 8192, true}, tc::Opnd{tc::smem_addr(sm + PP), 8192, true},
