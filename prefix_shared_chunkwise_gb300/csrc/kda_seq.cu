@@ -280,8 +280,10 @@ __device__ __forceinline__ void invert64(float *F) {
         F[fx(16 * bj + gid, cc + 1)] = d[1];
         F[fx(16 * bj + gid + 8, cc)] = d[2];
         F[fx(16 * bj + gid + 8, cc + 1)] = d[3];
-        // -T_ii X reads only the X columns this warp wrote
-        __syncwarp();
+        // -T_ii X reads only the X columns this warp wrote, but its result overwrites columns
+        // of M_ij that the pair's other warp reads above: the pair meets first
+        if (warp < 2) asm volatile("bar.sync 2, 64;" ::: "memory");
+        else asm volatile("bar.sync 3, 64;" ::: "memory");
     }
     if (warp < 4) {
         float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -325,13 +327,9 @@ __device__ __forceinline__ void invert64(float *F) {
         F[fx(16 * mt + gid + 8, cc)] = d[2];
         F[fx(16 * mt + gid + 8, cc + 1)] = d[3];
     }
-    // -T_II X reads the X columns of tile n8 from the two warps that wrote them
-    switch (n8) {                                         // literal ids: barriers 2-5
-    case 0: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
-    case 1: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
-    case 2: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
-    default: asm volatile("bar.sync 5, 64;" ::: "memory"); break;
-    }
+    // -T_II X reads X from the warps of both row tiles, and its result overwrites columns of
+    // M_IJ that the row tile's other warps read above: every warp meets
+    __syncthreads();
     {
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         const int r0 = 16 * mt + gid;                     // row of T_II (local)
