@@ -192,8 +192,8 @@ typedef struct {
                                 pass; records ordered [chunk][head], chunks by sequence.
                                 The tensor-core kernels store the state column-scaled as
                                 their products use it, S^T diag(e^m) with m the chunk's
-                                reference log-decay (the cumulative log-decay at row
-                                (n-1)/2 of the chunk's n rows); the exact-fp32 kernels
+                                reference log-decay (half the chunk's total per-channel
+                                log-decay, Gamma_L / 2); the exact-fp32 kernels
                                 store S^T.  A backward call must therefore select the same
                                 kernel family as the forward call that wrote the records. */
 } harts_kda_fwd_args;

@@ -11,7 +11,7 @@ namespace harts {
 // Device error codes written into PlanDev::err[0] (first error wins).
 enum : int32_t {
     kDevErrNone = 0,
-    kDevErrDecayRange = 1,   // per-chunk decay span too large for the reference-row scaling
+    kDevErrDecayRange = 1,   // a chunk's decay too large for the reference-scaled factorisation
     kDevErrBadIndex = 2,     // a plan index out of range
     kDevErrTimeout = 3,      // a bounded wait ran out
 };
@@ -20,7 +20,7 @@ enum : int32_t {
 // rows can be written with 16-byte stores.
 __host__ __device__ constexpr int rep_width(int D) { return 3 * D + 4; }
 
-// Largest |exponent| the reference-row factorisation may form (exp(85) < FLT_MAX).
+// Largest |exponent| the reference-scaled factorisation may form (exp(85) < FLT_MAX).
 constexpr float kMaxExpArg = 85.f;
 
 struct FwdParams {

@@ -56,8 +56,7 @@ constexpr uint32_t YT = 188416;     // Y^T [128][64]
 constexpr uint32_t DP = 204800;     // dP [64][64]   } one [128][64] operand [dP; dA]
 constexpr uint32_t WA = 212992;     // dA [64][64]   }
 constexpr uint32_t VQS = 221184;    // fp32 [4][128] partial sums (several uses)
-constexpr uint32_t VMR = VQS + 2048;
-constexpr uint32_t VM2 = VMR + 512;       // m log2(e)
+constexpr uint32_t VM2 = VQS + 2560;      // m log2(e)
 constexpr uint32_t VBETA = VM2 + 512;     // fp32 [64]
 constexpr uint32_t VDB = VBETA + 256;     // fp32 [64] dbeta
 constexpr uint32_t VDGL = VDB + 256;      // fp32 [128] dGamma_L
@@ -236,7 +235,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
     const int W3 = rep_width(D);
     const int jv = lq * 32 + lane;                  // TMEM lane of this thread
     const uint32_t lane_off = static_cast<uint32_t>(lq * 32) << 16;
-    float *vqs = reinterpret_cast<float *>(sm + VQS), *vmr = reinterpret_cast<float *>(sm + VMR);
+    float *vqs = reinterpret_cast<float *>(sm + VQS);
     float *vm2 = reinterpret_cast<float *>(sm + VM2), *vbeta = reinterpret_cast<float *>(sm + VBETA);
     float *vdb = reinterpret_cast<float *>(sm + VDB), *vdgl = reinterpret_cast<float *>(sm + VDGL);
 
@@ -451,31 +450,22 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
             const Item &I = s_items[n_done & 3];            // written by the load warp before g
             cur_seq = I.seq; cur_h = I.h;
             const int t_own = max(0, I.rho - I.c0), t_end = I.nv;
-            const int mid = (I.nv - 1) / 2;
             {
                 const int c = jv, q4 = cg;
-                float s_ = 0.f, mr = 0.f;
+                float s_ = 0.f;
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int t = q4 * 16 + u;
-                    s_ += bf(sm + TB + (c >> 6) * 8192 + sw64(t, c & 63));
-                    if (t == mid) mr = s_;
-                }
+                for (int u = 0; u < 16; ++u) s_ += bf(sm + TB + (c >> 6) * 8192 + sw64(q4 * 16 + u, c & 63));
                 vqs[q4 * 128 + c] = s_;
-                if (q4 == (mid >> 4)) vmr[c] = mr;
                 if (tid < 64) vbeta[tid] = __bfloat162float(__ushort_as_bfloat16(s_braw[ph][tid]));
             }
             csync();
             if (tid < 128) {
-                const int c = tid, qm = mid >> 4;
-                float m = vmr[c], gl = 0.f;
+                const int c = tid;
+                float gl = 0.f;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float x = vqs[q * 128 + c];
-                    gl += x;
-                    if (q < qm) m += x;
-                }
-                if (-m > kMaxExpArg || m - gl > kMaxExpArg) dev_error(pd, kDevErrDecayRange, I.seq, I.c0);
+                for (int q = 0; q < 4; ++q) gl += vqs[q * 128 + c];
+                const float m = 0.5f * gl;                  // the reference: Gamma_L / 2
+                if (-m > kMaxExpArg) dev_error(pd, kDevErrDecayRange, I.seq, I.c0);
                 vm2[c] = m * kLog2e;
             }
             poll(6);
@@ -724,7 +714,7 @@ __global__ void __launch_bounds__(NT, 1) kda_bwd_grad_tc2(BwdParams p, PlanDev p
                     for (int j = 0; j < 16; ++j) {
                         const int s = cg * 16 + j;
                         const float dm = s < t ? -w[j] : 0.f;
-                        db += dm * a[j];
+                        if (s < t) db += dm * a[j];         // A above the diagonal may be inf
                         if (s == t) db += d2[j];
                         w[j] = bt * dm;
                     }

@@ -14,8 +14,8 @@
 //   OT   = S^T Qd^T + U^T P^T       (= O^T)
 //   ST  <- ST diag(e^{Gamma_L}) + U^T Kt                                 (= S^T update)
 // with Kp = K e^{Gamma-m}, Km = K e^{m-Gamma}, Qp = Q e^{Gamma-m}, Kd = K e^{Gamma},
-// Qd = Q e^{Gamma}, Kt = K e^{Gamma_L-Gamma} (m: Gamma at a reference row, so no factor
-// exceeds exp(|Gamma_L|/2)), and T = (I + diag(beta) A)^-1 by blocked forward
+// Qd = Q e^{Gamma}, Kt = K e^{Gamma_L-Gamma} (m = Gamma_L / 2, half the chunk's total
+// log-decay, so no factor exceeds exp(|Gamma_L|/2)), and T = (I + diag(beta) A)^-1 by blocked forward
 // substitution in fp32 on the CUDA cores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
     __shared__ int s_fail;
     __shared__ int s_rows[64];
     float *vbeta = reinterpret_cast<float *>(sm + vBeta), *vel = reinterpret_cast<float *>(sm + vEl),
-          *vm = reinterpret_cast<float *>(sm + vM), *vpart = reinterpret_cast<float *>(sm + vPart),
+          *vpart = reinterpret_cast<float *>(sm + vPart),
           *vgp = reinterpret_cast<float *>(sm + vGp);
     float *Mfp = reinterpret_cast<float *>(sm + Mf), *Tfp = reinterpret_cast<float *>(sm + Tf);
 
@@ -315,7 +315,6 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
         const uint32_t ph = ci & 1;
         const int32_t c0 = ci * BC;
         const int nv = min(BC, L - c0);
-        const int mid = (nv - 1) / 2;
         tc::cp_async_wait_all();
         if (tma_pending) {
             if (!tc::mbar_wait(&bars[4], n_tma & 1)) atomicOr(&s_fail, 1);
@@ -327,17 +326,14 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
         // ---- prep: cumulative decay, scaled operands (from the staged raw tiles) ----------
         // thread: key channels c2, c2 + 1; rows 16 qr .. 16 qr + 15
         {
-            const int cp = tid & 63, qr = tid >> 6, c2 = 2 * cp, qmid = mid >> 4;
-            float s0 = 0.f, s1 = 0.f, ml0 = 0.f, ml1 = 0.f;
+            const int cp = tid & 63, qr = tid >> 6, c2 = 2 * cp;
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-                const int t = qr * 16 + u;
-                const float2 gg = stage2(sm, SG, t, c2);
+                const float2 gg = stage2(sm, SG, qr * 16 + u, c2);
                 s0 += gg.x; s1 += gg.y;
-                if (t == mid) { ml0 = s0; ml1 = s1; }
             }
             vpart[qr * 128 + c2] = s0; vpart[qr * 128 + c2 + 1] = s1;
-            if (qr == qmid) { vm[c2] = ml0; vm[c2 + 1] = ml1; }
             if (tid < 64) {
                 const uint32_t w = reinterpret_cast<const uint32_t *>(sm + SBeta)[tid];
                 const int par = reinterpret_cast<const int *>(sm + SBpar)[tid];
@@ -345,16 +341,15 @@ __global__ void __launch_bounds__(NT, 1) kda_fwd_tc(FwdParams p, PlanDev pd, int
                 vbeta[tid] = __bfloat162float(__ushort_as_bfloat16(hb));
             }
             __syncthreads();
-            float gam0 = 0.f, gam1 = 0.f, m0 = vm[c2], m1 = vm[c2 + 1], gl0 = 0.f, gl1 = 0.f;
+            float gam0 = 0.f, gam1 = 0.f, gl0 = 0.f, gl1 = 0.f;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float p0 = vpart[q * 128 + c2], p1 = vpart[q * 128 + c2 + 1];
                 if (q < qr) { gam0 += p0; gam1 += p1; }
-                if (q < qmid) { m0 += p0; m1 += p1; }
                 gl0 += p0; gl1 += p1;
             }
-            if (-m0 > kMaxExpArg || m0 - gl0 > kMaxExpArg || -m1 > kMaxExpArg || m1 - gl1 > kMaxExpArg)
-                dev_error(pd, kDevErrDecayRange, seq, c0);
+            const float m0 = 0.5f * gl0, m1 = 0.5f * gl1;        // the reference: Gamma_L / 2
+            if (-m0 > kMaxExpArg || -m1 > kMaxExpArg) dev_error(pd, kDevErrDecayRange, seq, c0);
             const float em0 = __expf(m0), ekt0 = __expf(gl0 - m0), em1 = __expf(m1), ekt1 = __expf(gl1 - m1);
             if (qr == 0) { vel[c2] = __expf(gl0); vel[c2 + 1] = __expf(gl1); }
             const bool lo = lane < 16;    // half-warps store even / odd rows of the transposed tiles

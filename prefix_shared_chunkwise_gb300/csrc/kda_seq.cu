@@ -8,8 +8,8 @@
 // holds about 104 KB of shared memory and 256 TMEM columns, so two CTAs share an SM and
 // one's elementwise phases run while the other waits on its products or loads.
 //
-// Chunk math (local rows t, s; gamma = cumulative log-decay from the chunk start, m = gamma
-// at the reference row, per key channel):
+// Chunk math (local rows t, s; gamma = cumulative log-decay from the chunk start, m = half
+// the chunk's total log-decay Gamma_L, per key channel):
 //   Kp = K e^{gamma-m}, Qp = scale Q e^{gamma-m}, Km = K e^{m-gamma}
 //   [A; P] = [Kp; Qp] Km^T          A strictly lower, P lower with the diagonal
 //   T = (I + diag(beta) A)^-1,  Tb = T diag(beta)
@@ -52,8 +52,7 @@ constexpr uint32_t VV = 49152;      // raw v [64][128] (atoms 8 KB) -> U^T [128]
 constexpr uint32_t SC = 65536;      // fp32 [64][64] diag(beta) A -> T; then Tb [64][64] bf16 and P at +8 KB
 constexpr uint32_t GP = 81920;      // next chunk's raw g [64][128], atoms of 8 KB
 constexpr uint32_t VQS = 98304;     // fp32 [16][128] sums of g over 4-row groups, then exclusive prefixes
-constexpr uint32_t VMR = VQS + 8192;      // fp32 [128] prefix of g at the reference row, inside its group
-constexpr uint32_t VM = VMR + 512;        // fp32 [2][128] m log2(e) (by chunk parity)
+constexpr uint32_t VM = VQS + 8704;         // fp32 [2][128] m log2(e) (by chunk parity)
 constexpr uint32_t VEM = VM + 1024;       // fp32 [2][128] e^m
 constexpr uint32_t VEG = VEM + 1024;      // fp32 [2][128] e^{Gamma_L - m}
 constexpr uint32_t VBETA = VEG + 1024;    // fp32 [64] beta of the current chunk
@@ -114,48 +113,41 @@ struct Maps2 {
 
 // Pass A of a chunk whose raw g sits in the SW128 tile `g` ([64][128], atoms of 8 KB): sums
 // of g over 4-row groups, turned into exclusive prefixes (vqs, natural log units), the
-// reference m = Gamma at the middle valid row, m log2(e), e^m, e^{Gamma_L - m} (into slot b
+// reference m = Gamma_L / 2 (half the chunk's total log-decay, so that every row's exponent
+// gamma - m lies within |Gamma_L| / 2 of zero), m log2(e), e^m, e^{Gamma_L - m} (into slot b
 // of vm / vem / veg), and beta (raw bf16 bits from this thread if tid < 64).  Records the
 // decay-range error when an exponent would leave the representable range.
 // Thread: 8 channels (group cg = tid % 16) x 4 rows (group rg = tid / 16).
-__device__ __forceinline__ void chunk_pass_a(uint8_t *sm, const uint8_t *g, float *vqs, float *vmr, float *vbeta,
-                                             uint8_t *vm, uint8_t *vem, uint8_t *veg, int nv, int b, uint16_t braw,
+__device__ __forceinline__ void chunk_pass_a(uint8_t *sm, const uint8_t *g, float *vqs, float *vbeta,
+                                             uint8_t *vm, uint8_t *vem, uint8_t *veg, int b, uint16_t braw,
                                              const PlanDev &pd, int32_t seq, int32_t c0) {
-    const int tid = threadIdx.x, mid = (nv - 1) / 2;
+    const int tid = threadIdx.x;
     const int cg = tid & 15, rg = tid >> 4;
-    float sacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, mr[8];
+    float sacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int t = 4 * rg + u;
         float gv[8];
         unpack8(*reinterpret_cast<const uint4 *>(g + (cg >> 3) * 8192 + chunk_off(t, cg & 7)), gv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            sacc[i] += gv[i];
-            if (t == mid) mr[i] = sacc[i];
-        }
+        for (int i = 0; i < 8; ++i) sacc[i] += gv[i];
     }
     float4 *q4 = reinterpret_cast<float4 *>(vqs + rg * 128 + 8 * cg);
     q4[0] = make_float4(sacc[0], sacc[1], sacc[2], sacc[3]);
     q4[1] = make_float4(sacc[4], sacc[5], sacc[6], sacc[7]);
-    if (rg == (mid >> 2)) {
-        float4 *m4 = reinterpret_cast<float4 *>(vmr + 8 * cg);
-        m4[0] = make_float4(mr[0], mr[1], mr[2], mr[3]);
-        m4[1] = make_float4(mr[4], mr[5], mr[6], mr[7]);
-    }
     if (tid < 64) vbeta[tid] = __bfloat162float(__ushort_as_bfloat16(braw));
     __syncthreads();
     if (tid < 128) {
-        const int gm = mid >> 2;
-        float run = 0.f, m = 0.f;
+        float run = 0.f;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             const float x = vqs[r * 128 + tid];
             vqs[r * 128 + tid] = run;
-            if (r == gm) m = run + vmr[tid];
             run += x;
         }
-        if (-m > kMaxExpArg || m - run > kMaxExpArg) dev_error(pd, kDevErrDecayRange, seq, c0);
+        // reference m = Gamma_L / 2: every row's exponent gamma - m stays within |Gamma_L| / 2
+        const float m = 0.5f * run;
+        if (-m > kMaxExpArg) dev_error(pd, kDevErrDecayRange, seq, c0);
         reinterpret_cast<float *>(vm)[b * 128 + tid] = m * kLog2e;
         reinterpret_cast<float *>(vem)[b * 128 + tid] = ex2(m * kLog2e);
         reinterpret_cast<float *>(veg)[b * 128 + tid] = ex2((run - m) * kLog2e);
@@ -363,7 +355,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
     __shared__ int s_rows[64];                      // compact rows of the chunk being staged (gathers)
-    float *vqs = reinterpret_cast<float *>(sm + VQS), *vmr = reinterpret_cast<float *>(sm + VMR);
+    float *vqs = reinterpret_cast<float *>(sm + VQS);
     float *vbeta = reinterpret_cast<float *>(sm + VBETA);
     float *F = reinterpret_cast<float *>(sm + SC);
 
@@ -414,7 +406,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
         }
     };
     auto pass_a = [&](int32_t c, uint16_t braw) {
-        chunk_pass_a(sm, sm + GP, vqs, vmr, vbeta, sm + VM, sm + VEM, sm + VEG, nv_of(c), c & 1, braw, pd, seq,
+        chunk_pass_a(sm, sm + GP, vqs, vbeta, sm + VM, sm + VEM, sm + VEG, c & 1, braw, pd, seq,
                      c * BC);
     };
 
@@ -750,8 +742,7 @@ constexpr uint32_t TB = 65536;      // [64][64]: T from the record -> Tb = T dia
 constexpr uint32_t PP = 73728;      // [64][64]: P (lower with the diagonal)
 constexpr uint32_t DU = 81920;      // [128][64]: dU^T, then -dY^T
 constexpr uint32_t VQS = 98304;     // fp32 [16][128]
-constexpr uint32_t VMR = VQS + 8192;
-constexpr uint32_t VM = VMR + 512;        // fp32 [2][128] m log2(e) (by processing parity)
+constexpr uint32_t VM = VQS + 8704;         // fp32 [2][128] m log2(e) (by processing parity)
 constexpr uint32_t VEM = VM + 1024;       // fp32 [2][128] e^m
 constexpr uint32_t VEG = VEM + 1024;      // fp32 [2][128] e^{Gamma_L - m}
 constexpr uint32_t VBETA = VEG + 1024;    // fp32 [64]
@@ -774,7 +765,7 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
     __shared__ int s_rows[64];
-    float *vqs = reinterpret_cast<float *>(sm + VQS), *vmr = reinterpret_cast<float *>(sm + VMR);
+    float *vqs = reinterpret_cast<float *>(sm + VQS);
     float *vbeta = reinterpret_cast<float *>(sm + VBETA);
     const FwdParams &f = p.f;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lq = warp & 3, ch = warp >> 2;
@@ -860,7 +851,7 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
         const bool more = ci > 0;
         // ---- pass A (needs g) ---------------------------------------------------------------
         if (!(ok = wait_data(&bars[4], ph, &s_fail))) break;
-        chunk_pass_a(sm, sm + KM, vqs, vmr, vbeta, sm + VM, sm + VEM, sm + VEG, nv, b, braw, pd, seq, c0);
+        chunk_pass_a(sm, sm + KM, vqs, vbeta, sm + VM, sm + VEM, sm + VEG, b, braw, pd, seq, c0);
         __syncthreads();
 
         // ---- carry: dS' = C e^{m_next} (+ consumers' initial-state gradients at a slot);

@@ -6,8 +6,7 @@
 // One CTA per (sequence, head) of a round.  The state S (D x D, fp32) lives in shared
 // memory for the whole sequence; chunks are processed in order.  Chunk math follows
 // the chunkwise form of the gated delta rule (local t = 1..L, Gamma = cumsum of g per
-// channel, m = Gamma at a reference row so that no exponential exceeds
-// exp(|Gamma_L|/2)):
+// channel, m = Gamma_L / 2 so that no exponential exceeds exp(|Gamma_L|/2)):
 //   Kp = K e^{Gamma-m}, Km = K e^{m-Gamma}, Qp = Q e^{Gamma-m}
 //   A  = strict_lower(Kp Km^T),  T = (I + diag(beta) A)^-1
 //   U  = T diag(beta) (V - Kd S),          Kd = Kp e^{m}
@@ -46,7 +45,7 @@ struct SimtBwdLayout {
 };
 
 // Load one chunk's tiles (rows past the sequence end read as zero) and form the
-// reference-row-scaled operands.  Gam receives the cumulative log decay.
+// reference-scaled operands.  Gam receives the cumulative log decay.
 template <int D, int BC, typename T>
 __device__ void load_and_prep(const FwdParams &p, const PlanDev &pd, int32_t seq, int32_t h,
                               int32_t rho, int32_t L, int32_t c0, float *Kp, float *Km,
@@ -74,13 +73,11 @@ __device__ void load_and_prep(const FwdParams &p, const PlanDev &pd, int32_t seq
         bet[t] = row >= 0 ? ld_in(beta, row * H + h) : 0.f;
     }
     __syncthreads();
-    const int nv = min(BC, L - c0);
-    const int mid = (nv - 1) / 2;
     for (int c = tid; c < D; c += nth) {
         float gam = 0.f;
         for (int t = 0; t < BC; ++t) { gam += Gam[t * D + c]; Gam[t * D + c] = gam; }
-        const float m = Gam[mid * D + c];
-        if (-m > kMaxExpArg || m - gam > kMaxExpArg) dev_error(pd, kDevErrDecayRange, seq, c0);
+        const float m = 0.5f * gam;        // rows past the end hold g = 0, so gam = Gamma_L
+        if (-m > kMaxExpArg) dev_error(pd, kDevErrDecayRange, seq, c0);
         for (int t = 0; t < BC; ++t) {
             const float gt = Gam[t * D + c], kk = Kp[t * D + c];
             Kp[t * D + c] = kk * expf(gt - m);
@@ -440,9 +437,8 @@ __global__ void __launch_bounds__(256) kda_bwd_simt(BwdParams p, PlanDev pd, int
         __syncthreads();
         // outputs
         for (int c = tid; c < D; c += nth) {
-            // recover m from the stored reference row through Gam (m = Gamma[mid])
-            const int nv = min(BC, L - c0);
-            const float mref = Gam[((nv - 1) / 2) * D + c];
+            // the reference m = Gamma_L / 2, recovered from the last row of Gam
+            const float mref = 0.5f * Gam[(BC - 1) * D + c];
             float run = dgl[c];
             for (int t = BC - 1; t >= 0; --t) {
                 const int i = t * D + c;

@@ -25,13 +25,15 @@ def built():
 
 
 def _run(parent, seg_len, B, H, D, dtype, seed, *, backward, kernel=_lib.HARTS_KERNEL_AUTO,
-         h0=False, d_final=False, decay=1.0, scale=1.0):
+         h0=False, d_final=False, decay=1.0, scale=1.0, g_rows=None):
     pl = Plan(parent, seg_len, B).upload()
     info = pl.info
     C = info["C"]
     x = make_inputs(C, H, D, D, dtype, seed, device="cpu")
     if decay != 1.0:
         x["g"] = (x["g"].float() * decay).to(x["g"].dtype)
+    if g_rows is not None:
+        x["g"] = g_rows(x["g"].float()).to(x["g"].dtype)
     dev = {k: v.cuda() for k, v in x.items()}
     td = dev["q"].dtype
     h0_t = None
@@ -180,24 +182,71 @@ def test_bf16_d128_fwd_bwd_with_h0_tc():
 
 
 def test_tc_fwd_bwd_repeatable_on_64k_forest():
-    """Forward + backward twice on the same inputs over the 64K-token forest: every output
-    is identical bit for bit (fixed summation orders, no atomics: a race between the
-    staged copies, the products and the per-chunk phases would show as run-to-run
-    differences) and no device error is recorded."""
+    """Forward + backward three times on the same inputs over the 64K-token forest: every
+    output, the chunk records (R and T), the state slots and the final states are identical
+    bit for bit (fixed summation orders, no atomics: a race between the staged copies, the
+    products and the per-chunk phases would show as run-to-run differences; the records'
+    tiny T entries show a race long before a bf16 output flips) and no device error is
+    recorded."""
     parent, seg_len = make_tree("fb64k_bf16")
     pl = Plan(parent, seg_len, 64).upload()
     C, H = pl.info["C"], 4
     x = make_inputs(C, H, 128, 128, "bf16", 17, device="cuda")
     cs = torch.empty(pl.chunk_state_bytes(H, 128, 128, 1) // 2, dtype=torch.bfloat16, device="cuda")
+    fin = torch.empty((pl.info["n_seq"], H, 128, 128), dtype=torch.float32, device="cuda")
+    names = ("o", "final", "records", "states", "dq", "dk", "dv", "dg", "dbeta")
     runs = []
-    for _ in range(2):
-        o, states, _, cs = kda_fwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], chunk_states=cs,
-                                   kernel=_lib.HARTS_KERNEL_TC)
+    for _ in range(3):
+        o, states, fin, cs = kda_fwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], final_state=fin,
+                                     chunk_states=cs, kernel=_lib.HARTS_KERNEL_TC)
+        torch.cuda.synchronize()
+        fwd = [o.clone(), fin.clone(), cs.clone(), states.clone()]
         gr = kda_bwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], x["W"], states=states,
                      chunk_states=cs, kernel=_lib.HARTS_KERNEL_TC)
         torch.cuda.synchronize()
         assert pl.device_error() == 0
-        runs.append([o.clone()] + [gr[n].clone() for n in ("dq", "dk", "dv", "dg", "dbeta")])
-    for name, a, b in zip(("o", "dq", "dk", "dv", "dg", "dbeta"), *runs):
-        diff = (a != b)
-        assert not bool(diff.any()), (name, int(diff.sum()), diff.nonzero()[:4].tolist())
+        runs.append(fwd + [gr[n].clone() for n in ("dq", "dk", "dv", "dg", "dbeta")])
+    for r in (1, 2):
+        for name, a, b in zip(names, runs[0], runs[r]):
+            diff = (a != b) & ~(a.isnan() & b.isnan())
+            assert not bool(diff.any()), (r, name, int(diff.sum()), diff.nonzero()[:4].tolist())
+
+
+def _row_depth(parent, seg_len):
+    """Trajectory position (depth in the tree) of every compact row, segments in id order."""
+    depth0 = np.zeros(len(parent), np.int64)
+    for i, p in enumerate(parent):
+        if p >= 0:
+            depth0[i] = depth0[p] + seg_len[p]
+    return np.concatenate([depth0[i] + np.arange(seg_len[i]) for i in range(len(parent))])
+
+
+def _late_decay(parent, seg_len, B, per_token):
+    """g that leaves the first half of every B-row chunk (by trajectory position) almost
+    undecayed and puts a strong decay of about `per_token` on each row of the second half,
+    so that a chunk's total log-decay is about B / 2 * per_token, all of it late."""
+    late = torch.from_numpy((_row_depth(parent, seg_len) % B) >= B // 2)
+
+    def f(g):
+        return torch.where(late[:, None, None], per_token + 0.1 * g, 0.01 * g)
+    return f
+
+
+def test_bf16_d128_fwd_bwd_late_decay_tc():
+    """A decay of about e^-112 per chunk, all of it in the chunk's second half: every exponent
+    of the half-total reference stays within e^+-56, so the tensor-core kernels compute the
+    chunk (a middle-row reference would need e^112 and refuse it)."""
+    parent = np.array([-1, 0, 0, 1, 1, -1], np.int32)
+    seg_len = np.array([100, 90, 70, 40, 75, 150], np.int64)
+    errs = _run(parent, seg_len, 64, 2, 128, "bf16", 23, backward=True, kernel=_lib.HARTS_KERNEL_TC,
+                d_final=True, g_rows=_late_decay(parent, seg_len, 64, -3.5))
+    _assert(errs, TOL["bf16"])
+
+
+def test_fp32_d64_fwd_bwd_late_decay_simt():
+    """The same e^-112 late decay per chunk on the exact fp32 CUDA-core kernels (B = 32)."""
+    parent = np.array([-1, 0, 0, 1, 1, -1], np.int32)
+    seg_len = np.array([100, 90, 70, 40, 75, 150], np.int64)
+    errs = _run(parent, seg_len, 32, 2, 64, "fp32", 24, backward=True, kernel=_lib.HARTS_KERNEL_SIMT,
+                d_final=True, g_rows=_late_decay(parent, seg_len, 32, -7.0))
+    _assert(errs, TOL["fp32"])
