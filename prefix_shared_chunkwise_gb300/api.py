@@ -104,9 +104,36 @@ class Plan:
         return int(L.lib().harts_kda_bwd_workspace_bytes(self._h, H, dk, dv))
 
 
+def _need(name, t, shape=None, dtype=None, nbytes=None, device=None):
+    """Size check of one buffer before its pointer crosses the C ABI (which cannot see sizes)."""
+    if t is None:
+        return
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if nbytes is not None and t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, needs {nbytes}")
+
+
 def _fwd_args(plan, q, k, v, g, beta, o, states, final_state, h0, chunk_states, scale, kernel):
+    import torch
     C, H, dk = q.shape
     dv = v.shape[2]
+    info, dev, f32 = plan.info, q.device, torch.float32
+    if C != info["C"]:
+        raise ValueError(f"q has {C} rows, the plan {info['C']}")
+    for n, t, sh in (("k", k, (C, H, dk)), ("v", v, (C, H, dv)), ("g", g, (C, H, dk)),
+                     ("beta", beta, (C, H)), ("o", o, (C, H, dv))):
+        _need(n, t, sh, q.dtype, device=dev)
+    per = H * dk * dv * 4                          # bytes of one fp32 state, all heads
+    _need("states", states, None, f32, info["n_states"] * per, dev)
+    _need("final_state", final_state, None, f32, info["n_seq"] * per, dev)
+    _need("h0", h0, None, f32, info["n_roots"] * per, dev)
+    _need("chunk_states", chunk_states, nbytes=plan.chunk_state_bytes(H, dk, dv, dtype_code(q.dtype)),
+          device=dev)
     a = L.FwdArgs()
     a.H, a.dk, a.dv = H, dk, dv
     a.dtype = dtype_code(q.dtype)
@@ -154,6 +181,15 @@ def kda_bwd(plan: Plan, q, k, v, g, beta, d_o, *, states, chunk_states, d_final=
     nb = plan.bwd_workspace_bytes(H, dk, dv)
     if workspace is None and phase != "static":
         workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+    info = plan.info
+    _need("d_o", d_o, (C, H, dv), q.dtype, device=dev)
+    per = H * dk * dv * 4
+    _need("d_final", d_final, None, torch.float32, info["n_seq"] * per, dev)
+    _need("dh0", dh0, None, torch.float32, info["n_roots"] * per, dev)
+    for n, ref in (("dq", q), ("dk", k), ("dv", v), ("dg", g), ("dbeta", beta)):
+        _need(n, grads[n], tuple(ref.shape), q.dtype, device=dev)
+    if phase != "static":
+        _need("workspace", workspace, nbytes=nb, device=dev)
     a = L.BwdArgs()
     a.fwd = _fwd_args(plan, q, k, v, g, beta, None, states, None, h0, chunk_states, scale, kernel)
     a.d_o = d_o.data_ptr()

@@ -212,3 +212,30 @@ def test_attention_backward_workspace_and_checks():
     assert _lib.lib().harts_attn_bwd(pl.handle, ctypes.byref(b), None) == -8   # not uploaded
     b.fwd.d = 64
     assert _lib.lib().harts_attn_bwd(pl.handle, ctypes.byref(b), None) == -2
+
+
+def test_binding_rejects_undersized_buffers_before_the_abi():
+    """The C ABI sees plain pointers, so the binding checks every buffer's shape or size
+    against the plan first: a short chunk_states, states or workspace, or a row tensor of
+    the wrong shape, raises ValueError and nothing is passed to the library."""
+    import torch
+    from prefix_shared_chunkwise_gb300.api import kda_bwd, kda_fwd
+    from prefix_shared_chunkwise_gb300.synth import make_inputs
+    pl = Plan(np.array([-1, 0, 0], np.int32), np.array([150, 90, 70], np.int64), 64)
+    H, D = 2, 128
+    assert pl.info["n_states"] >= 1
+    x = make_inputs(pl.info["C"], H, D, D, "bf16", 0)
+    need = pl.chunk_state_bytes(H, D, D, 1)
+    short = torch.empty(need // 2 - 1, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="chunk_states"):
+        kda_fwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], chunk_states=short)
+    with pytest.raises(ValueError, match="states"):
+        kda_fwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"],
+                states=torch.empty((max(pl.info["n_states"] - 1, 0), H, D, D)))
+    with pytest.raises(ValueError, match="shape"):
+        kda_fwd(pl, x["q"], x["k"][:-1], x["v"], x["g"], x["beta"])
+    cs = torch.empty(need // 2, dtype=torch.bfloat16)
+    st = torch.empty((pl.info["n_states"], H, D, D))
+    with pytest.raises(ValueError, match="workspace"):
+        kda_bwd(pl, x["q"], x["k"], x["v"], x["g"], x["beta"], x["W"], states=st, chunk_states=cs,
+                workspace=torch.empty(16, dtype=torch.uint8))
