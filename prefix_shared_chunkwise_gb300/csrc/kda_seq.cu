@@ -346,7 +346,7 @@ __device__ __forceinline__ void invert64(float *F) {
 }
 
 __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, int32_t round_base,
-                                                     const __grid_constant__ Maps2 maps) {
+                                                     int32_t hpb, const __grid_constant__ Maps2 maps) {
     using namespace f2;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
@@ -361,8 +361,13 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lq = warp & 3, ch = warp >> 2;
     const int H = p.H;
-    const int32_t h = blockIdx.x % H;
-    const int32_t seq = pd.round_order[round_base + blockIdx.x / H];
+    // one block: heads [hfirst, hfirst + hpb) of one sequence, one after the other; the next
+    // head's first chunk is staged, its reference formed and its initial state loaded while
+    // the current head's last chunk runs
+    const int32_t ngrp = H / hpb;
+    const int32_t seq = pd.round_order[round_base + blockIdx.x / ngrp];
+    const int32_t hfirst = (blockIdx.x % ngrp) * hpb, hlast = hfirst + hpb - 1;
+    int32_t h = hfirst;
     const int32_t rho = pd.seq_rho[seq], L = rho + pd.seq_nown[seq];
     const int32_t nch = (L + BC - 1) / BC;
     const int32_t src = pd.seq_src[seq];
@@ -386,43 +391,45 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
     auto nv_of = [&](int32_t c) { return min(BC, L - c * BC); };
     // Row table of chunk c (threads 0-63; read by the gathers after a barrier) and this
     // thread's beta of row t = tid (raw bf16 bits, 0 past the end).
-    auto rows_of = [&](int32_t c) -> uint16_t {
+    auto rows_of = [&](int32_t c, int32_t hh) -> uint16_t {
         if (tid >= 64) return 0;
         const int64_t row = local_row(pd, seq, rho, L, c * BC + tid);
         s_rows[tid] = static_cast<int>(row);
-        return row >= 0 ? beta[row * H + h] : static_cast<uint16_t>(0);
+        return row >= 0 ? beta[row * H + hh] : static_cast<uint16_t>(0);
     };
     int armed[8] = {0, 0, 0, 0, 0, 0, 0, 0};     // phases armed per barrier (uniform over threads)
-    auto stage = [&](int which, int32_t c) {
+    auto stage = [&](int which, int32_t c, int32_t hh) {
         ++armed[4 + which];
         const int32_t c0 = c * BC;
         const int t_own = max(0, rho - c0), t_end = nv_of(c);
         const int32_t own0 = row0 + c0 - rho;
         switch (which) {
-        case 0: stage_chunk_rows<NT>(p.g, maps.g, s_rows, h, H, t_own, t_end, own0, 0, sm + GP, sm + GP + 8192, &bars[4]); break;
-        case 1: stage_chunk_rows<NT>(p.k, maps.k, s_rows, h, H, t_own, t_end, own0, 0, sm + KQ, sm + KQ + 16384, &bars[5]); break;
-        case 2: stage_chunk_rows<NT>(p.q, maps.q, s_rows, h, H, t_own, t_end, own0, 0, sm + KQ + 8192, sm + KQ + 24576, &bars[6]); break;
-        default: stage_chunk_rows<NT>(p.v, maps.v, s_rows, h, H, t_own, t_end, own0, 0, sm + VV, sm + VV + 8192, &bars[7]); break;
+        case 0: stage_chunk_rows<NT>(p.g, maps.g, s_rows, hh, H, t_own, t_end, own0, 0, sm + GP, sm + GP + 8192, &bars[4]); break;
+        case 1: stage_chunk_rows<NT>(p.k, maps.k, s_rows, hh, H, t_own, t_end, own0, 0, sm + KQ, sm + KQ + 16384, &bars[5]); break;
+        case 2: stage_chunk_rows<NT>(p.q, maps.q, s_rows, hh, H, t_own, t_end, own0, 0, sm + KQ + 8192, sm + KQ + 24576, &bars[6]); break;
+        default: stage_chunk_rows<NT>(p.v, maps.v, s_rows, hh, H, t_own, t_end, own0, 0, sm + VV, sm + VV + 8192, &bars[7]); break;
         }
     };
-    auto pass_a = [&](int32_t c, uint16_t braw) {
-        chunk_pass_a(sm, sm + GP, vqs, vbeta, sm + VM, sm + VEM, sm + VEG, c & 1, braw, pd, seq,
-                     c * BC);
+    auto pass_a = [&](int32_t c, uint32_t slot, uint16_t braw) {
+        chunk_pass_a(sm, sm + GP, vqs, vbeta, sm + VM, sm + VEM, sm + VEG, slot, braw, pd, seq, c * BC);
+    };
+    // the initial state of head hh (null: zero)
+    auto state0 = [&](int32_t hh) -> const float * {
+        return src >= 0 ? p.states + (static_cast<int64_t>(src) * H + hh) * D * D
+                        : (p.h0 ? p.h0 + (static_cast<int64_t>(-1 - src) * H + hh) * D * D : nullptr);
     };
 
     // ---- sequence start: chunk 0's rows, the initial state (loaded while they arrive), pass A
-    uint16_t braw = rows_of(0);
+    uint16_t braw = rows_of(0, h);
     __syncthreads();
-    stage(0, 0);
-    stage(1, 0);
-    stage(2, 0);
-    stage(3, 0);
-    int32_t sp = pd.seq_sptr[seq];
+    stage(0, 0, h);
+    stage(1, 0, h);
+    stage(2, 0, h);
+    stage(3, 0, h);
     const int32_t sp_end = pd.seq_sptr[seq + 1];
     {
         // S0^T (lane = value channel) into TMEM unscaled
-        const float *S0 = src >= 0 ? p.states + (static_cast<int64_t>(src) * H + h) * D * D
-                        : (p.h0 ? p.h0 + (static_cast<int64_t>(-1 - src) * H + h) * D * D : nullptr);
+        const float *S0 = state0(h);
         float r0[32], r1[32];
         const int cb = ch * 64;
 #pragma unroll
@@ -434,7 +441,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
     }
     bool ok = wait_data(&bars[4], 0, &s_fail);
     if (ok) {
-        pass_a(0, braw);
+        pass_a(0, 0, braw);
         __syncthreads();
         // R = S0^T diag(e^{m_0}): fp32 back into TMEM, bf16 pairs into the R columns and
         // into the chunk-0 record
@@ -469,17 +476,22 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
         tc::fence_before_sync();
     }
 
-    for (int32_t ci = 0; ok && ci < nch; ++ci) {
-        const uint32_t ph = ci & 1, b = ci & 1;
+    uint32_t it = 0;                                  // chunks this block has processed
+    for (; ok; ++h) {
+    int32_t sp = pd.seq_sptr[seq];
+    for (int32_t ci = 0; ci < nch; ++ci, ++it) {
+        const uint32_t ph = it & 1, b = it & 1;       // barrier phases and vector slots
         const int32_t c0 = ci * BC;
         const int nv = nv_of(ci);
-        const bool more = ci + 1 < nch, last = !more;
+        // the next chunk: this head's, or the next head's first after this head's last
+        const bool last = ci + 1 == nch, hnext = last && h < hlast, more = !last || hnext;
+        const int32_t cn = last ? 0 : ci + 1, hn = last ? h + 1 : h;
         // ---- pass B: scaled operands Kp, Qp (in place over raw k, q), Km ------------------
         poll0(&bars[5], ph, &s_fail);
         poll0(&bars[6], ph, &s_fail);
         if (!sync_check(&s_fail)) break;
         chunk_pass_b(sm + KQ, sm + GP, sm + KM, vqs, reinterpret_cast<const float *>(sm + VM) + b * 128, p.scale);
-        if (more) braw = rows_of(ci + 1);
+        if (more) braw = rows_of(cn, hn);
         sync_mma();
         if (tid == 0) {
             tc::mma_tile(tW, tc::smem_addr(sm + KQ), 16384, tc::smem_addr(sm + KM), 8192, 128,
@@ -489,7 +501,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
         ++armed[0];
         // raw g is consumed, the V tile is free: fetch the next chunk's g and this chunk's v
         // ... v(ci) was requested at the previous chunk's end or the sequence start
-        if (more) stage(0, ci + 1);
+        if (more) stage(0, cn, hn);
         if (!wait_all2(&bars[0], ph, &s_fail)) break;
         // ---- [A; P] out of TMEM: diag(beta) A (strict lower, fp32) into the scratch ----------
         if (lq < 2) {
@@ -558,7 +570,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
         // ---- pass A of the next chunk while the product runs --------------------------------
         if (more) {
             if (!wait_data(&bars[4], ph ^ 1, &s_fail)) break;
-            pass_a(ci + 1, braw);
+            pass_a(cn, b ^ 1, braw);
         }
         if (!wait_all2(&bars[1], ph, &s_fail)) break;
         // ---- -(Kp^T Tb^T) as the MN-major B tile [dk][t] over the Kp half of KQ -----------------
@@ -590,7 +602,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
         }
         ++armed[2];
         if (!wait_all2(&bars[2], ph, &s_fail)) break;
-        if (more) stage(1, ci + 1);                         // the Kp half is free: next k
+        if (more) stage(1, cn, hn);                         // the Kp half is free: next k
         // ---- U^T -> bf16 tile [dv][t] (K-major A) over V --------------------------------------
         {
             float r[32];
@@ -613,7 +625,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
         }
         ++armed[3];
         if (!wait_all2(&bars[3], ph, &s_fail)) break;
-        if (more) stage(2, ci + 1);                         // the Qp half is free: next q
+        if (more) stage(2, cn, hn);                         // the Qp half is free: next q
         // ---- outputs: O rows (staged [t][dv] over U^T), the state leaves and re-enters TMEM ----
         {
             float r[32];
@@ -630,6 +642,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
             float *sdst = slot ? p.states + (static_cast<int64_t>(sp) * H + h) * D * D
                         : (last && p.final_state ? p.final_state + (static_cast<int64_t>(seq) * H + h) * D * D : nullptr);
             const bool rdst = more && rec;
+            const float *S0n = hnext ? state0(hn) : nullptr;
 #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
                 const int cb = ch * 64 + hf * 32;
@@ -651,6 +664,10 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
                 }
                 if (more) {
                     uint32_t pk[16];
+                    if (hnext) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = S0n ? S0n[(cb + j) * D + jv] : 0.f;
+                    }
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {                         // next chunk's R
                         const float4 a = *reinterpret_cast<const float4 *>(emn + cb + j);
@@ -691,7 +708,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
                     *reinterpret_cast<const uint4 *>(sm + VV + t * 256 + piece * 16);
             }
             if (more && rec) {
-                uint8_t *rd = rec + (static_cast<int64_t>(cbase + ci + 1) * H + h) * kRecBytes;
+                uint8_t *rd = rec + (static_cast<int64_t>(cbase + cn) * H + hn) * kRecBytes;
                 for (int e = tid; e < 128 * 16; e += NT) {
                     const int r = e >> 4, j = e & 15;
                     *reinterpret_cast<uint4 *>(rd + r * 256 + j * 16) = *reinterpret_cast<const uint4 *>(
@@ -701,7 +718,10 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
         }
         __syncthreads();
         tc::fence_after_sync();
-        if (more) stage(3, ci + 1);                         // the output staging is read: next v
+        if (more) stage(3, cn, hn);                         // the output staging is read: next v
+    }
+    // every stop inside the chunk loop follows a failed wait, which all threads see in s_fail
+    if (*reinterpret_cast<volatile int *>(&s_fail) != 0 || h == hlast) break;
     }
     // ---- drain: copies and products still in flight land before shared memory is released --
     tc::cp_async_wait_all();
@@ -1052,7 +1072,16 @@ cudaError_t tc2_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, i
         for (int i = 0; i < 4; ++i)
             if (!encode_row_maps(dst[i], src[i], H, pd.C)) return cudaErrorInvalidValue;
     }
-    kda_fwd_tc2<<<n_items, NT, f2::bytes, st>>>(p, pd, base, maps);
+    // heads per block: 4 or 2 when the round still gives every SM's two block slots eight
+    // blocks or more (a block then pays its start-up once for several heads and overlaps
+    // each next head's first loads with the current head's last chunk), else 1
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int hpb = 1;
+    for (int c : {4, 2})
+        if (p.H % c == 0 && n_items / c >= 16 * nsm) { hpb = c; break; }
+    kda_fwd_tc2<<<n_items / hpb, NT, f2::bytes, st>>>(p, pd, base, hpb, maps);
     return cudaGetLastError();
 }
 
