@@ -776,7 +776,7 @@ struct StateMaps2 {
 };
 
 __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev pd, int32_t round_base,
-                                                           const __grid_constant__ StateMaps2 maps) {
+                                                           int32_t hpb, const __grid_constant__ StateMaps2 maps) {
     using namespace s2;
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = smraw + ((1024 - (tc::smem_addr(smraw) & 1023)) & 1023);
@@ -790,8 +790,12 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
     const FwdParams &f = p.f;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lq = warp & 3, ch = warp >> 2;
     const int H = f.H;
-    const int32_t h = blockIdx.x % H;
-    const int32_t seq = pd.round_order[round_base + blockIdx.x / H];
+    // one block: heads [hfirst, hfirst + hpb) of one sequence in turn; the next head's last
+    // chunk is staged while the current head's first chunk runs
+    const int32_t ngrp = H / hpb;
+    const int32_t seq = pd.round_order[round_base + blockIdx.x / ngrp];
+    const int32_t hfirst = (blockIdx.x % ngrp) * hpb, hlast = hfirst + hpb - 1;
+    int32_t h = hfirst;
     const int32_t rho = pd.seq_rho[seq], L = rho + pd.seq_nown[seq];
     const int32_t nch = (L + BC - 1) / BC;
     const int32_t src = pd.seq_src[seq], cbase = pd.seq_cbase[seq], row0 = pd.seq_row0[seq];
@@ -813,37 +817,37 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
 
     int armed[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
     auto nv_of = [&](int32_t c) { return min(BC, L - c * BC); };
-    auto rows_of = [&](int32_t c) -> uint16_t {
+    auto rows_of = [&](int32_t c, int32_t hh) -> uint16_t {
         if (tid >= 64) return 0;
         const int64_t row = local_row(pd, seq, rho, L, c * BC + tid);
         s_rows[tid] = static_cast<int>(row);
-        return row >= 0 ? beta[row * H + h] : static_cast<uint16_t>(0);
+        return row >= 0 ? beta[row * H + hh] : static_cast<uint16_t>(0);
     };
-    auto stage = [&](int which, int32_t c) {
+    auto stage = [&](int which, int32_t c, int32_t hh) {
         ++armed[4 + which];
         const int32_t c0 = c * BC;
         const int t_own = max(0, rho - c0), t_end = nv_of(c);
         const int32_t own0 = row0 + c0 - rho;
         switch (which) {
-        case 0: stage_chunk_rows<NT>(f.g, maps.g, s_rows, h, H, t_own, t_end, own0, 0, sm + KM, sm + KM + 8192, &bars[4]); break;
-        case 1: stage_chunk_rows<NT>(f.k, maps.k, s_rows, h, H, t_own, t_end, own0, 0, sm + KQ, sm + KQ + 16384, &bars[5]); break;
-        case 2: stage_chunk_rows<NT>(f.q, maps.q, s_rows, h, H, t_own, t_end, own0, 0, sm + KQ + 8192, sm + KQ + 24576, &bars[6]); break;
-        case 3: stage_chunk_rows<NT>(p.d_o, maps.dout, s_rows, h, H, t_own, t_end, own0, t_own, sm + DO, sm + DO + 8192,
+        case 0: stage_chunk_rows<NT>(f.g, maps.g, s_rows, hh, H, t_own, t_end, own0, 0, sm + KM, sm + KM + 8192, &bars[4]); break;
+        case 1: stage_chunk_rows<NT>(f.k, maps.k, s_rows, hh, H, t_own, t_end, own0, 0, sm + KQ, sm + KQ + 16384, &bars[5]); break;
+        case 2: stage_chunk_rows<NT>(f.q, maps.q, s_rows, hh, H, t_own, t_end, own0, 0, sm + KQ + 8192, sm + KQ + 24576, &bars[6]); break;
+        case 3: stage_chunk_rows<NT>(p.d_o, maps.dout, s_rows, hh, H, t_own, t_end, own0, t_own, sm + DO, sm + DO + 8192,
                                      &bars[7]); break;
         default:
             if (tid == 0) {
                 tc::mbar_expect_tx(&bars[8], 8192);
                 tc::tma_load_2d(sm + TB, &maps.rec_t, 0,
-                                static_cast<int>((static_cast<int64_t>(cbase + c) * H + h) * (kRecBytes / 128) + 2 * D),
+                                static_cast<int>((static_cast<int64_t>(cbase + c) * H + hh) * (kRecBytes / 128) + 2 * D),
                                 &bars[8]);
             }
             break;
         }
     };
 
-    // carry <- d_final^T (the loop scales it by e^{m} of the chunk after; 1 for the last)
-    {
-        const float *df = p.d_final ? p.d_final + (static_cast<int64_t>(seq) * H + h) * D * D : nullptr;
+    // carry <- d_final^T of head hh (the loop scales it by e^{m} of the chunk after; 1 for the last)
+    auto carry_init = [&](int32_t hh) {
+        const float *df = p.d_final ? p.d_final + (static_cast<int64_t>(seq) * H + hh) * D * D : nullptr;
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
             const int cb = ch * 64 + hf * 32;
@@ -852,23 +856,28 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
             for (int j = 0; j < 32; ++j) r[j] = df ? df[(cb + j) * D + jv] : 0.f;
             tc::tmem_st32(tC + lane_off + cb, r);
         }
-    }
-    uint16_t braw = rows_of(nch - 1);
+    };
+    carry_init(h);
+    uint16_t braw = rows_of(nch - 1, h);
     __syncthreads();
-    for (int w = 0; w < 5; ++w) stage(w, nch - 1);
+    for (int w = 0; w < 5; ++w) stage(w, nch - 1, h);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
 
     const int32_t sp_begin = pd.seq_sptr[seq];
-    int32_t sp = pd.seq_sptr[seq + 1] - 1;
     bool ok = true;
-    for (int32_t ci = nch - 1; ci >= 0; --ci) {
-        const int32_t n = nch - 1 - ci;            // processing index
-        const uint32_t ph = n & 1, b = n & 1;
+    uint32_t it = 0;                               // chunks this block has processed
+    for (;; ++h) {
+    int32_t sp = pd.seq_sptr[seq + 1] - 1;
+    for (int32_t ci = nch - 1; ci >= 0; --ci, ++it) {
+        const int32_t n = nch - 1 - ci;            // processing index within the head
+        const uint32_t ph = it & 1, b = it & 1;    // barrier phases and vector slots
         const int32_t c0 = ci * BC, pend = min(c0 + BC, L);
         const int nv = nv_of(ci);
-        const bool more = ci > 0;
+        // the next chunk to process: this head's previous one, or the next head's last
+        const bool hnext = ci == 0 && h < hlast, more = ci > 0 || hnext;
+        const int32_t cn = ci > 0 ? ci - 1 : nch - 1, hn = ci > 0 ? h : h + 1;
         // ---- pass A (needs g) ---------------------------------------------------------------
         if (!(ok = wait_data(&bars[4], ph, &s_fail))) break;
         chunk_pass_a(sm, sm + KM, vqs, vbeta, sm + VM, sm + VEM, sm + VEG, b, braw, pd, seq, c0);
@@ -984,9 +993,9 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
             tc::mma_commit(&bars[1]);
         }
         ++armed[1];
-        if (more) braw = rows_of(ci - 1);                   // the previous chunk's rows, read after the wait
+        if (more) braw = rows_of(cn, hn);                   // the next chunk's rows, read after the wait
         if (!(ok = wait_all2(&bars[1], ph, &s_fail))) break;
-        if (more) stage(0, ci - 1);                          // Km is consumed: previous g
+        if (more) stage(0, cn, hn);                          // Km is consumed: next g
         {
             float r[32];
             tc::tmem_ld32(tW + lane_off + ch * 32, r);
@@ -1002,7 +1011,7 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
         }
         ++armed[2];
         if (!(ok = wait_all2(&bars[2], ph, &s_fail))) break;
-        if (more) stage(4, ci - 1);                          // T consumed: previous chunk's T
+        if (more) stage(4, cn, hn);                          // T consumed: next chunk's T
         {
             float r[32];
             tc::tmem_ld32(tW + lane_off + ch * 32, r);
@@ -1022,11 +1031,14 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
         }
         ++armed[3];
         if (!(ok = wait_all2(&bars[3], ph, &s_fail))) break;
-        if (more) { stage(1, ci - 1); stage(2, ci - 1); stage(3, ci - 1); }
+        if (more) { stage(1, cn, hn); stage(2, cn, hn); stage(3, cn, hn); }
     }
-    // ---- the sequence's initial-state gradient: dS_0 = C diag(e^{m_0}) ----------------------
-    if (ok && !s_fail && (src >= 0 || p.dh0)) {
-        const float *em = reinterpret_cast<const float *>(sm + VEM) + ((nch - 1) & 1) * 128;
+    // every stop inside the chunk loop follows a failed wait, which all threads see in s_fail
+    if (!ok || *reinterpret_cast<volatile int *>(&s_fail) != 0) break;
+    // ---- the head's initial-state gradient: dS_0 = C diag(e^{m_0}) (chunk 0 was the last
+    //      processed, slot (it - 1) & 1) ----------------------------------------------------------
+    if (src >= 0 || p.dh0) {
+        const float *em = reinterpret_cast<const float *>(sm + VEM) + ((it - 1) & 1) * 128;
         float *dst = p.ds_init + (static_cast<int64_t>(seq) * H + h) * D * D;
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
@@ -1036,6 +1048,13 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
 #pragma unroll
             for (int j = 0; j < 32; ++j) dst[(cb + j) * D + jv] = r[j] * em[cb + j];
         }
+    }
+    if (h == hlast) break;
+    // the next head's carry (each warp rewrites the TMEM lanes and columns it just read)
+    carry_init(h + 1);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
     }
     tc::cp_async_wait_all();
     __syncthreads();
@@ -1110,7 +1129,14 @@ cudaError_t tc2_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t b
         const cuuint32_t rbox[2] = {64, 64};
         if (!encode_bf16(&maps.rec_t, p.f.chunk_states, 2, rdims, rstrides, rbox)) return cudaErrorInvalidValue;
     }
-    kda_bwd_state_tc2<<<n_items, NT, s2::bytes, st>>>(p, pd, base, maps);
+    // heads per block: as the forward's
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int hpb = 1;
+    for (int c : {4, 2})
+        if (p.f.H % c == 0 && n_items / c >= 16 * nsm) { hpb = c; break; }
+    kda_bwd_state_tc2<<<n_items / hpb, NT, s2::bytes, st>>>(p, pd, base, hpb, maps);
     return cudaGetLastError();
 }
 
