@@ -109,6 +109,7 @@ __device__ __forceinline__ void mma16x8x8(float (&d)[4], const uint32_t (&a)[4],
 
 struct Maps2 {
     RowMaps q, k, v, g;
+    CUtensorMap rec_s;           // chunk records as [rows of 256 B], boxes of 64 columns x 128 rows
 };
 
 // Pass A of a chunk whose raw g sits in the SW128 tile `g` ([64][128], atoms of 8 KB): sums
@@ -487,6 +488,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
         const bool last = ci + 1 == nch, hnext = last && h < hlast, more = !last || hnext;
         const int32_t cn = last ? 0 : ci + 1, hn = last ? h + 1 : h;
         // ---- pass B: scaled operands Kp, Qp (in place over raw k, q), Km ------------------
+        if (tid == 0) tc::bulk_wait_read();             // the last record store has read KM and SC
         poll0(&bars[5], ph, &s_fail);
         poll0(&bars[6], ph, &s_fail);
         if (!sync_check(&s_fail)) break;
@@ -695,8 +697,16 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
             }
             if (slot) ++sp;
         }
+        tc::fence_smem_to_async();                       // the staged record, for its TMA store
         tc::fence_before_sync();
         __syncthreads();
+        if (tid == 0 && more && rec) {
+            // the next chunk's R record: columns 0-63 staged in KM, 64-127 in SC
+            const int y = static_cast<int>((static_cast<int64_t>(cbase + cn) * H + hn) * (kRecBytes / 256));
+            tc::tma_store_2d(&maps.rec_s, 0, y, sm + KM);
+            tc::tma_store_2d(&maps.rec_s, 64, y, sm + SC);
+            tc::bulk_commit();
+        }
         {
             __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
             const int t_lo = max(0, rho - c0);
@@ -707,14 +717,6 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
                 *reinterpret_cast<uint4 *>(o + (row * H + h) * D + piece * 8) =
                     *reinterpret_cast<const uint4 *>(sm + VV + t * 256 + piece * 16);
             }
-            if (more && rec) {
-                uint8_t *rd = rec + (static_cast<int64_t>(cbase + cn) * H + hn) * kRecBytes;
-                for (int e = tid; e < 128 * 16; e += NT) {
-                    const int r = e >> 4, j = e & 15;
-                    *reinterpret_cast<uint4 *>(rd + r * 256 + j * 16) = *reinterpret_cast<const uint4 *>(
-                        sm + (j < 8 ? KM : SC) + r * 128 + (((j & 7) ^ (r & 7)) << 4));
-                }
-            }
         }
         __syncthreads();
         tc::fence_after_sync();
@@ -723,6 +725,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
     // every stop inside the chunk loop follows a failed wait, which all threads see in s_fail
     if (*reinterpret_cast<volatile int *>(&s_fail) != 0 || h == hlast) break;
     }
+    if (tid == 0) tc::bulk_wait_all();               // the record stores have landed
     // ---- drain: copies and products still in flight land before shared memory is released --
     tc::cp_async_wait_all();
     __syncthreads();
@@ -773,6 +776,7 @@ constexpr uint32_t bytes = END + 1024;
 struct StateMaps2 {
     RowMaps q, k, g, dout;
     CUtensorMap rec_t;           // chunk records as [rows of 128 B], boxes of 64 x 64 (a chunk's T)
+    CUtensorMap dch;             // the saved Q' as [rows of 256 B], boxes of 64 columns x 128 rows
 };
 
 __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev pd, int32_t round_base,
@@ -799,7 +803,6 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
     const int32_t rho = pd.seq_rho[seq], L = rho + pd.seq_nown[seq];
     const int32_t nch = (L + BC - 1) / BC;
     const int32_t src = pd.seq_src[seq], cbase = pd.seq_cbase[seq], row0 = pd.seq_row0[seq];
-    uint8_t *dch = static_cast<uint8_t *>(p.dchunk);
     const uint16_t *beta = static_cast<const uint16_t *>(f.beta);
 
     if (tid == 0) {
@@ -890,10 +893,10 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
             const int32_t cb_ = slot ? pd.state_cptr[sp] : 0, ce_ = slot ? pd.state_cptr[sp + 1] : 0;
             const float *emn = reinterpret_cast<const float *>(sm + VEM) + (b ^ 1) * 128;
             const float *eg = reinterpret_cast<const float *>(sm + VEG) + b * 128;
-            uint8_t *rd = dch + (static_cast<int64_t>(cbase + ci) * H + h) * D * D * 2;
+            const int rec_row = static_cast<int>((static_cast<int64_t>(cbase + ci) * H + h) * D);
 #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
-                const int cb = ch * 64 + hf * 32;
+                const int cb = hf * 64 + ch * 32;           // columns [64 hf, 64 hf + 64): this warp's 32
                 float r[32];
                 tc::tmem_ld32(tC + lane_off + cb, r);
                 if (n > 0) {
@@ -916,9 +919,8 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) pk[j] = tc::pack_bf16(r[2 * j], r[2 * j + 1]);
-                // the bf16 Q' of this half's 32 columns per row into DU ([dv][64]: columns
-                // ch * 32 .. + 31), then out to the record row by row, 64 contiguous bytes per
-                // row segment
+                // the bf16 Q' of this half's 64 columns into DU as the record map's box ([dv][64],
+                // 128-byte swizzle), then out by one TMA store
                 uint8_t *stg = sm + DU + jv * 128;
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
@@ -931,14 +933,14 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
                                 "r"(pk[5]), "r"(pk[6]), "r"(pk[7]), "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]),
                                 "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15]) : "memory");
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc::fence_smem_to_async();
                 __syncthreads();
-                for (int e = tid; e < 128 * 8; e += NT) {
-                    const int r_ = e >> 3, j = e & 7;          // row, 16-byte chunk of the staged 64 columns
-                    const int col = (j >> 2) * 64 + hf * 32 + (j & 3) * 8;
-                    *reinterpret_cast<uint4 *>(rd + r_ * 256 + col * 2) =
-                        *reinterpret_cast<const uint4 *>(sm + DU + r_ * 128 + ((j ^ (r_ & 7)) << 4));
+                if (tid == 0) {
+                    tc::tma_store_2d(&maps.dch, hf * 64, rec_row, sm + DU);
+                    tc::bulk_commit();
+                    if (hf == 0) tc::bulk_wait_read();      // DU takes the second half next
                 }
-                __syncthreads();
+                if (hf == 0) __syncthreads();
             }
             if (slot) --sp;
         }
@@ -991,6 +993,7 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) tc::mma_bf16_ta(tW, tQ + kk * 8, tc::opnd_desc(kmo, kk), id, 1u);
             tc::mma_commit(&bars[1]);
+            tc::bulk_wait_read();                           // the Q' store has read DU (written below)
         }
         ++armed[1];
         if (more) braw = rows_of(cn, hn);                   // the next chunk's rows, read after the wait
@@ -1056,6 +1059,7 @@ __global__ void __launch_bounds__(NT, 2) kda_bwd_state_tc2(BwdParams p, PlanDev 
     __syncthreads();
     tc::fence_after_sync();
     }
+    if (tid == 0) tc::bulk_wait_all();               // the record stores have landed
     tc::cp_async_wait_all();
     __syncthreads();
     if (s_fail) {
@@ -1080,7 +1084,7 @@ cudaError_t tc2_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, i
     e = cudaFuncSetAttribute(kda_fwd_tc2, cudaFuncAttributePreferredSharedMemoryCarveout,
                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (e != cudaSuccess) return e;
-    Maps2 maps;
+    Maps2 maps{};
     {
         const int H = p.H;
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(pd.C)};
@@ -1090,6 +1094,14 @@ cudaError_t tc2_fwd_round(const FwdParams &p, const PlanDev &pd, int32_t base, i
         RowMaps *dst[4] = {&maps.q, &maps.k, &maps.v, &maps.g};
         for (int i = 0; i < 4; ++i)
             if (!encode_row_maps(dst[i], src[i], H, pd.C)) return cudaErrorInvalidValue;
+        if (p.chunk_states) {
+            const int64_t rows = pd.n_chunks * H * (kRecBytes / 256);
+            if (rows > INT32_MAX) return cudaErrorInvalidValue;      // TMA coordinates are int32
+            const cuuint64_t rdims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+            const cuuint64_t rstrides[1] = {static_cast<cuuint64_t>(D) * 2};
+            const cuuint32_t rbox[2] = {64, 128};
+            if (!encode_bf16(&maps.rec_s, p.chunk_states, 2, rdims, rstrides, rbox)) return cudaErrorInvalidValue;
+        }
     }
     // heads per block: 4 or 2 when the round still gives every SM's two block slots eight
     // blocks or more (a block then pays its start-up once for several heads and overlaps
@@ -1112,7 +1124,7 @@ cudaError_t tc2_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t b
     e = cudaFuncSetAttribute(kda_bwd_state_tc2, cudaFuncAttributePreferredSharedMemoryCarveout,
                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (e != cudaSuccess) return e;
-    StateMaps2 maps;
+    StateMaps2 maps{};
     {
         const int H = p.f.H;
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(pd.C)};
@@ -1128,6 +1140,10 @@ cudaError_t tc2_bwd_state_round(const BwdParams &p, const PlanDev &pd, int32_t b
         const cuuint64_t rstrides[1] = {128};
         const cuuint32_t rbox[2] = {64, 64};
         if (!encode_bf16(&maps.rec_t, p.f.chunk_states, 2, rdims, rstrides, rbox)) return cudaErrorInvalidValue;
+        const cuuint64_t qdims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(n_rec * D)};
+        const cuuint64_t qstrides[1] = {static_cast<cuuint64_t>(D) * 2};
+        const cuuint32_t qbox[2] = {64, 128};
+        if (!encode_bf16(&maps.dch, p.dchunk, 2, qdims, qstrides, qbox)) return cudaErrorInvalidValue;
     }
     // heads per block: as the forward's
     int dev = 0, nsm = 0;

@@ -206,6 +206,21 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x, i
         : "memory");
 }
 
+// ---- TMA tiled stores (completion tracked by bulk async-groups of the issuing thread) ----
+// The source tile is 1024-byte aligned and laid out as the map's box (128-byte swizzle);
+// the threads that wrote it fence it to the async proxy and meet before one thread issues
+// the store.  Every coordinate passed by this library lies inside the tensor.
+
+__device__ __forceinline__ void tma_store_2d(const void *map, int x, int y, const void *src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(src)) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of this thread's committed stores have been read (reusable)
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's committed stores have completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---- TMEM <-> registers (warp-collective; warp w may touch lanes 32*(w%4)..+31) ---------
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
