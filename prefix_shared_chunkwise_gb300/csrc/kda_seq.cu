@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(NT, 2) kda_fwd_tc2(FwdParams p, PlanDev pd, in
                     for (int j = 0; j < 16; ++j) pk[j] = tc::pack_bf16(r[2 * j], r[2 * j + 1]);
                     if (rdst) {
                         // the next chunk's record (its bf16 R), staged [dv][64] per column half
-                        // (SW128 rows), written out coalesced below
+                        // in the record map's box layout (128-byte swizzle) for its TMA stores
                         uint8_t *stg = sm + (ch ? SC : KM) + jv * 128;
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
