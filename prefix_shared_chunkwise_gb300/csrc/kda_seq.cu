@@ -1,12 +1,14 @@
 // The two sequential passes of bf16 packed-tree KDA on sm_103a (dk = dv = 128, chunk 64),
 // forward and backward state pass, each with two CTAs per SM.
 //
-// One CTA (256 threads) per (sequence, head) of a round, chunks in order (page "HARTS ...
-// 精读", section 4.3, KDA paragraph: one packed call per round, each sequence resuming
-// from its boundary state; section 4.2: a side branch first replays its ancestor rows
-// back to the chunk boundary, which update the state but write no output).  Each CTA
-// holds about 104 KB of shared memory and 256 TMEM columns, so two CTAs share an SM and
-// one's elementwise phases run while the other waits on its products or loads.
+// One CTA (256 threads) per sequence of a round and group of 1, 2 or 4 of its heads, the
+// heads in turn and each head's chunks in order (page "HARTS ... 精读", section 4.3, KDA
+// paragraph: one packed call per round, each sequence resuming from its boundary state;
+// section 4.2: a side branch first replays its ancestor rows back to the chunk boundary,
+// which update the state but write no output).  Each CTA holds about 104 KB of shared
+// memory and 256 TMEM columns, so two CTAs share an SM and one's elementwise phases run
+// while the other waits on its products or loads.  The next head's first chunk is fetched
+// while the current head's last runs, so a CTA sets up once for several short sequences.
 //
 // Chunk math (local rows t, s; gamma = cumulative log-decay from the chunk start, m = half
 // the chunk's total log-decay Gamma_L, per key channel):
@@ -22,7 +24,8 @@
 // as the fp32 state leaves TMEM and goes back in.
 //
 // Each chunk's record for the gradient pass holds the bf16 R the products used (not S^T)
-// and T, so the gradient pass needs neither m-scaling of the state nor an inversion.
+// and T, so the gradient pass needs neither m-scaling of the state nor an inversion; R
+// (forward) and Q' (state pass) leave shared memory by tiled TMA stores.
 //
 // TMEM (256 columns): S = R in fp32 (128), R as bf16 pairs, the A operand of two products
 // (64), one work tile W (64) that holds in turn [A; P], Kp^T Tb^T, U^T and O^T.
