@@ -4,10 +4,11 @@
 // forward's record), Q' (the state pass's record) and T = (I + diag(beta) A)^-1 (the
 // forward's record), all input gradients of the chunk follow without any sequential
 // dependence.  One CTA per SM walks the items in steps of the grid size: 16 compute warps
-// run the products and epilogues of one item while a 17th warp (the load warp) stages the
-// next item's tiles, each as soon as the product batch that last reads its buffer is done.
-// Notation (gamma the cumulative log-decay from the chunk start, m gamma at the reference
-// row, per key channel; t, s local rows):
+// run the products and epilogues of one item while four load warps stage the next item's
+// tiles, each as soon as the product batch that last reads its buffer is done (one lane of
+// load warp 1 issues the product batches).
+// Notation (gamma the cumulative log-decay from the chunk start, m = Gamma_L / 2 half the
+// chunk's total log-decay, per key channel; t, s local rows):
 //   Kp = K e^{gamma-m}, Qp = scale Q e^{gamma-m}, Km = K e^{m-gamma}
 //   [A; P] = [Kp; Qp] Km^T, Tb = T diag(beta), R = S^T diag(e^m), Q' = dS'^T diag(e^{Gamma_L-m})
 //   Y^T = V^T - R Kp^T, U^T = Y^T Tb^T                              (the forward's U)
@@ -173,7 +174,7 @@ __device__ __forceinline__ Item item_of(const PlanDev &pd, int32_t chunk_begin, 
 
 constexpr long long kWaitCycles = 4000000000LL;
 
-// The compute warps meet at named barrier 1 (the load warp never joins it).
+// The compute warps meet at named barrier 1 (the load warps never join it).
 __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" :: "n"(NC) : "memory"); }
 
 // The same meeting, returning the OR of `v` over the compute warps (a decision all of them take).
